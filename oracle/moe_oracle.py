@@ -1,0 +1,423 @@
+"""Plain CPU oracle of one Mixture-of-Experts layer, forward and backward.
+
+TEST INFRASTRUCTURE ONLY. Nothing in the library imports, links or runs this
+module; only the tests, ``__graft_entry__.smoke()`` and the CPU-baseline /
+reference legs of ``bench.py`` do. It shares no code with the CUDA path.
+
+What it computes follows "Scalable Training of Mixture-of-Experts Models with
+Megatron Core" (gist.science summaries, es: "Resumen técnico" §2.1, "Arquitectura
+de la Capa MoE"): the layer is four stages in sequence --
+
+  1. Route    -- a router assigns every token to its k best experts;
+  2. Dispatch -- tokens are moved to the experts they were assigned to (on one
+                 GPU this is a permutation into per-expert contiguous rows);
+  3. Compute  -- every expert runs its FFN on its tokens (grouped GEMM);
+  4. Combine  -- the inverse movement; results are summed with router weights.
+
+The router stays in fp32 (same page, §2.4: router kept in high precision).
+Everything the pages leave open is taken from the layer configuration and the
+readings listed below; every one of them is a reading, not a quote:
+
+  * logits l = x . W_r^T, accumulated in fp64, rounded once to fp32;
+  * softmax router: selection on the fp32 value l + b (b = optional logit bias),
+    ties to the lower expert index; weights = softmax over the k selected
+    (renormalised top-k probabilities);
+  * sigmoid router: s = sigmoid(l) in fp64, selection score s + b in fp64;
+    group-limited: groups of E/G contiguous experts scored by the sum of their
+    two best selection scores (or their maximum), the best topk_groups groups
+    kept (ties to the lower group), then top-k inside them; weights
+    route_scale * s_j / sum_sel s (bias only steers selection);
+  * capacity C = ceil(cf * T * k / E) rounded up to row_align; an expert keeps
+    its first C tokens in token order, dropped assignments contribute 0 and
+    the surviving weights are not renormalised;
+  * permutation: stable counting sort by (expert, token); each expert's segment
+    is padded to a multiple of row_align rows (padding rows are zero); shared
+    experts follow the routed segments, one row per token in token order;
+  * SwiGLU expert: W13[e] = [gate rows ; up rows] ([2F,H]), W2[e] is [H,F];
+    G,U = X W_gate^T, X W_up^T rounded to bf16, h = bf16(silu(G) * U),
+    y = bf16(h W2^T);
+  * combine: out[t] = bf16(sum_j w_tj y_tj + sum_s y_shared[s,t]);
+  * backward: the exact gradient of that function with the same bf16
+    materialisation points (dO, dGU, dX, dx, dW13, dW2 in bf16; dlogits, dW_r
+    in fp32); the router gradient flows into x and W_r.
+
+Rounding: ``round_bf16`` is round-to-nearest-even onto the bf16 grid, written
+from the format (8 exponent bits, 7 stored fraction bits). Pass
+``rounding=False`` to the layer functions for exact fp64 arithmetic (used by
+the finite-difference pins).
+"""
+from __future__ import annotations
+
+import math
+
+import numpy as np
+
+SOFTMAX = 0
+SIGMOID = 1
+GROUP_TOP2_SUM = 0
+GROUP_MAX = 1
+
+_BF16_MAX = (2.0 - 2.0 ** -7) * 2.0 ** 127
+_BF16_MIN_QUANTUM_EXP = -133          # 2^(-126 - 7): the subnormal spacing
+
+
+# --------------------------------------------------------------------------- #
+# number formats
+# --------------------------------------------------------------------------- #
+def round_bf16(a) -> np.ndarray:
+    """Round to the nearest bf16 value, ties to even; returns float64.
+
+    bf16 keeps 8 significant bits: for |a| in [2^e, 2^(e+1)) the spacing is
+    2^(e-7), never below the subnormal spacing 2^-133. Values whose rounded
+    magnitude exceeds the largest finite bf16 become +-inf.
+    """
+    a = np.asarray(a, dtype=np.float64)
+    out = np.array(a, copy=True)
+    fin = np.isfinite(a) & (a != 0)
+    if np.any(fin):
+        v = a[fin]
+        _, ex = np.frexp(v)                  # v = m * 2^ex, 0.5 <= |m| < 1
+        qexp = np.maximum(ex - 1 - 7, _BF16_MIN_QUANTUM_EXP)
+        r = np.ldexp(np.rint(np.ldexp(v, -qexp)), qexp)
+        r = np.where(np.abs(r) > _BF16_MAX, np.copysign(np.inf, v), r)
+        out[fin] = r
+    return out
+
+
+def round_f32(a) -> np.ndarray:
+    """Round to the nearest fp32 value (IEEE cast); returns float64."""
+    return np.asarray(a, dtype=np.float64).astype(np.float32).astype(np.float64)
+
+
+def _rb(a, rounding: bool):
+    return round_bf16(a) if rounding else np.asarray(a, dtype=np.float64)
+
+
+def _rf(a, rounding: bool):
+    return round_f32(a) if rounding else np.asarray(a, dtype=np.float64)
+
+
+def sigmoid(z):
+    return 1.0 / (1.0 + np.exp(-z))
+
+
+def silu(z):
+    return z / (1.0 + np.exp(-z))
+
+
+# --------------------------------------------------------------------------- #
+# stage 1: route
+# --------------------------------------------------------------------------- #
+def router_logits(x, W_r, rounding: bool = True) -> np.ndarray:
+    """l[t,e] = sum_h x[t,h] W_r[e,h], fp64 accumulation, one fp32 rounding."""
+    x = np.asarray(x, dtype=np.float64)
+    W_r = np.asarray(W_r, dtype=np.float64)
+    return _rf(x @ W_r.T, rounding)
+
+
+def _topk_rows(score, k, masked=None):
+    """Per row: the k columns with the largest score, ties to the lower column.
+
+    NaN scores rank below every number; masked columns rank below everything.
+    """
+    score = np.where(np.isnan(score), -np.inf, score)
+    n, m = score.shape
+    col = np.broadcast_to(np.arange(m), (n, m))
+    msk = np.zeros((n, m), dtype=np.int8) if masked is None else masked.astype(np.int8)
+    # lexsort: last key is primary -> (masked asc, -score asc, column asc)
+    order = np.lexsort((col, -score, msk), axis=-1)
+    return order[:, :k]
+
+
+def capacity(cfg) -> int:
+    """Rows each expert keeps in capacity mode; 0 means dropless."""
+    if cfg.capacity_factor <= 0:
+        return 0
+    cf = float(np.float32(cfg.capacity_factor))
+    c = math.ceil(cf * cfg.T * cfg.k / cfg.E)
+    a = cfg.row_align
+    return (c + a - 1) // a * a
+
+
+def route(logits, cfg, bias=None):
+    """Top-k selection and routing weights from fp32 logits.
+
+    Returns (idx [T,k] int64, w [T,k] float64). Follows the route stage of the
+    Megatron Core MoE layer (es summary, Resumen técnico §2.1, step 1: a router
+    assigns each token to its k best experts).
+    """
+    l = np.asarray(logits, dtype=np.float64)
+    T, E = l.shape
+    k = cfg.k
+    if cfg.score_fn == SOFTMAX:
+        # selection on the fp32 sum l + b (bit-reproducible), weights from
+        # the same sum in fp64 (identical whenever l is fp32-valued)
+        b64 = 0.0 if bias is None else np.asarray(bias, np.float32).astype(np.float64)[None, :]
+        l32 = l.astype(np.float32)
+        if bias is not None:
+            l32 = l32 + np.asarray(bias, dtype=np.float32)[None, :]
+        sc = l32.astype(np.float64)
+        masked = None
+        if cfg.n_groups > 1:
+            masked = _group_mask(sc, cfg)
+        idx = _topk_rows(sc, k, masked)
+        sel = np.take_along_axis(l + b64, idx, axis=1)
+        z = np.exp(sel - sel[:, :1])
+        w = z / z.sum(axis=1, keepdims=True)
+        return idx, w
+    if cfg.score_fn == SIGMOID:
+        s = sigmoid(l)
+        sc = s + (0.0 if bias is None else np.asarray(bias, dtype=np.float32).astype(np.float64)[None, :])
+        masked = _group_mask(sc, cfg) if cfg.n_groups > 1 else None
+        idx = _topk_rows(sc, k, masked)
+        ssel = np.take_along_axis(s, idx, axis=1)
+        w = cfg.route_scale * ssel / ssel.sum(axis=1, keepdims=True)
+        return idx, w
+    raise ValueError("score_fn")
+
+
+def _group_mask(sc, cfg):
+    """Mask (True = excluded) of experts outside the best topk_groups groups."""
+    T, E = sc.shape
+    G = cfg.n_groups
+    per = E // G
+    s = np.where(np.isnan(sc), -np.inf, sc).reshape(T, G, per)
+    srt = -np.sort(-s, axis=2)                     # descending within group
+    if cfg.group_score == GROUP_TOP2_SUM and per >= 2:
+        gs = srt[:, :, 0] + srt[:, :, 1]
+    else:
+        gs = srt[:, :, 0]
+    keep = _topk_rows(gs, cfg.topk_groups)         # [T, topk_groups]
+    gmask = np.ones((T, G), dtype=bool)
+    np.put_along_axis(gmask, keep, False, axis=1)
+    return np.repeat(gmask, per, axis=1)
+
+
+# --------------------------------------------------------------------------- #
+# stage 2: dispatch (permutation maps)
+# --------------------------------------------------------------------------- #
+def permutation_maps(idx, cfg) -> dict:
+    """Stable counting sort of the (token, slot) assignments by (expert, token).
+
+    counts[g]      rows kept by group g (routed experts, then shared experts)
+    offsets[g]     first row of group g's segment (segments padded to row_align,
+                   or C rows each in capacity mode); offsets[G] = rows used
+    row_of[t,j]    row of assignment (t,j), -1 if dropped by capacity
+    token_of[r]    token held by row r, -1 for padding rows
+    sel_offsets[e] / sel_tokens: for every routed expert, all tokens that
+                   selected it (dropped or not) in increasing token order
+    """
+    idx = np.asarray(idx)
+    T, k = idx.shape
+    E, S, a = cfg.E, cfg.n_shared, cfg.row_align
+    C = capacity(cfg)
+    total = np.zeros(E, dtype=np.int64)
+    rank = np.zeros((T, k), dtype=np.int64)
+    for t in range(T):                               # running counter per expert
+        for j in range(k):
+            e = int(idx[t, j])
+            rank[t, j] = total[e]
+            total[e] += 1
+    kept = np.minimum(total, C) if C > 0 else total.copy()
+    seglen = np.empty(E + S, dtype=np.int64)
+    for e in range(E):
+        seglen[e] = C if C > 0 else (kept[e] + a - 1) // a * a
+    for s in range(S):
+        seglen[E + s] = (T + a - 1) // a * a
+    offsets = np.zeros(E + S + 1, dtype=np.int64)
+    offsets[1:] = np.cumsum(seglen)
+    counts = np.concatenate([kept, np.full(S, T, dtype=np.int64)])
+    R = int(offsets[-1])
+    row_of = np.full((T, k), -1, dtype=np.int64)
+    token_of = np.full(R, -1, dtype=np.int64)
+    for t in range(T):
+        for j in range(k):
+            e = int(idx[t, j])
+            if C > 0 and rank[t, j] >= C:
+                continue
+            r = int(offsets[e] + rank[t, j])
+            row_of[t, j] = r
+            token_of[r] = t
+    for s in range(S):
+        token_of[offsets[E + s]: offsets[E + s] + T] = np.arange(T)
+    sel_offsets = np.zeros(E + 1, dtype=np.int64)
+    sel_offsets[1:] = np.cumsum(total)
+    sel_tokens = np.empty(T * k, dtype=np.int64)
+    for t in range(T):
+        for j in range(k):
+            e = int(idx[t, j])
+            sel_tokens[sel_offsets[e] + rank[t, j]] = t
+    return dict(counts=counts, offsets=offsets, row_of=row_of, token_of=token_of,
+                sel_offsets=sel_offsets, sel_tokens=sel_tokens, R=R, C=C)
+
+
+def permute(x, maps) -> np.ndarray:
+    """x_perm[r] = x[token_of[r]], zero rows for padding."""
+    x = np.asarray(x, dtype=np.float64)
+    tok = maps["token_of"]
+    out = np.zeros((tok.shape[0], x.shape[1]))
+    valid = tok >= 0
+    out[valid] = x[tok[valid]]
+    return out
+
+
+# --------------------------------------------------------------------------- #
+# stage 3: compute (one SwiGLU expert)
+# --------------------------------------------------------------------------- #
+def expert_fc1(X, W13_e, rounding: bool = True):
+    """GU = bf16(X W13_e^T) ([n,2F]: gate columns then up) and h = bf16(silu(G) U)."""
+    F = W13_e.shape[0] // 2
+    GU = _rb(np.asarray(X, np.float64) @ np.asarray(W13_e, np.float64).T, rounding)
+    h = _rb(silu(GU[:, :F]) * GU[:, F:], rounding)
+    return GU, h
+
+
+def expert_fc2(h, W2_e, rounding: bool = True):
+    """y = bf16(h W2_e^T)."""
+    return _rb(np.asarray(h, np.float64) @ np.asarray(W2_e, np.float64).T, rounding)
+
+
+def expert_fc2_dgrad_swiglu(dO, W2_e, GU, rounding: bool = True):
+    """dh = dO W2_e (kept in full precision), then the SwiGLU backward.
+
+    dG = dh * U * sig(G) * (1 + G (1 - sig(G))), dU = dh * silu(G); both bf16.
+    """
+    F = W2_e.shape[1]
+    dh = np.asarray(dO, np.float64) @ np.asarray(W2_e, np.float64)
+    G, U = GU[:, :F], GU[:, F:]
+    sg = sigmoid(G)
+    dG = dh * U * sg * (1.0 + G * (1.0 - sg))
+    dU = dh * silu(G)
+    return _rb(np.concatenate([dG, dU], axis=1), rounding)
+
+
+def expert_fc1_dgrad(dGU, W13_e, rounding: bool = True):
+    """dX = bf16(dGU W13_e)."""
+    return _rb(np.asarray(dGU, np.float64) @ np.asarray(W13_e, np.float64), rounding)
+
+
+def wgrad(A, B, rounding: bool = True):
+    """dW = bf16(A^T B): the weight gradient summed over an expert's rows."""
+    return _rb(np.asarray(A, np.float64).T @ np.asarray(B, np.float64), rounding)
+
+
+# --------------------------------------------------------------------------- #
+# the whole layer, token by token (the plain definition)
+# --------------------------------------------------------------------------- #
+def layer_forward(cfg, x, W_r, bias, W13, W2, logits=None, rounding: bool = True):
+    """One MoE layer forward; returns a dict of every intermediate.
+
+    out[t] = sum over kept slots j of w_tj * FFN_{e_tj}(x_t), plus every shared
+    expert's FFN(x_t) with weight 1. Per-assignment values are stored per
+    (t, j) so that they can be compared against any row layout.
+    """
+    x = np.asarray(x, np.float64)
+    T, H = x.shape
+    E, k, F, S = cfg.E, cfg.k, cfg.F, cfg.n_shared
+    if logits is None:
+        logits = router_logits(x, W_r, rounding)
+    logits = np.asarray(logits, np.float64)
+    idx, w = route(logits, cfg, bias)
+    maps = permutation_maps(idx, cfg)
+    kept = maps["row_of"] >= 0
+    GU = np.zeros((T, k, 2 * F))
+    h = np.zeros((T, k, F))
+    y = np.zeros((T, k, H))
+    for e in range(E):
+        tt, jj = np.nonzero((idx == e) & kept)
+        if tt.size == 0:
+            continue
+        g, hh = expert_fc1(x[tt], W13[e], rounding)
+        GU[tt, jj], h[tt, jj] = g, hh
+        y[tt, jj] = expert_fc2(hh, W2[e], rounding)
+    GU_s = np.zeros((S, T, 2 * F))
+    h_s = np.zeros((S, T, F))
+    y_s = np.zeros((S, T, H))
+    for s in range(S):
+        GU_s[s], h_s[s] = expert_fc1(x, W13[E + s], rounding)
+        y_s[s] = expert_fc2(h_s[s], W2[E + s], rounding)
+    acc = np.einsum("tj,tjh->th", np.where(kept, w, 0.0), y) + y_s.sum(axis=0)
+    out = _rb(acc, rounding)
+    return dict(logits=logits, idx=idx, w=w, maps=maps, GU=GU, h=h, y=y,
+                GU_s=GU_s, h_s=h_s, y_s=y_s, out=out)
+
+
+def router_dlogits(cfg, logits, idx, w, dw):
+    """Gradient of the routing weights w.r.t. the fp32 logits (dense [T,E]).
+
+    softmax renormalised top-k: dl_{e_j} = w_j (dw_j - sum_i w_i dw_i);
+    sigmoid normalised: ds_i = (r/S)(dw_i - sum_j (s_j/S) dw_j) on the selected
+    experts, dl_i = ds_i s_i (1 - s_i); every other entry is 0 (selection,
+    grouping and biases carry no gradient).
+    """
+    logits = np.asarray(logits, np.float64)
+    T, E = logits.shape
+    dl = np.zeros((T, E))
+    if cfg.score_fn == SOFTMAX:
+        inner = (w * dw).sum(axis=1, keepdims=True)
+        vals = w * (dw - inner)
+    else:
+        s = sigmoid(np.take_along_axis(logits, idx, axis=1))
+        Ssum = s.sum(axis=1, keepdims=True)
+        r = cfg.route_scale
+        ds = (r / Ssum) * (dw - ((s / Ssum) * dw).sum(axis=1, keepdims=True))
+        vals = ds * s * (1.0 - s)
+    np.put_along_axis(dl, idx, vals, axis=1)
+    return dl
+
+
+def layer_backward(cfg, x, W_r, W13, W2, fwd, dY, rounding: bool = True):
+    """Gradient of sum(out * dY) w.r.t. x, W_r, W13, W2, with the layer's
+    bf16 materialisation points. Returns a dict of every intermediate."""
+    x = np.asarray(x, np.float64)
+    dY = np.asarray(dY, np.float64)
+    T, H = x.shape
+    E, k, F, S = cfg.E, cfg.k, cfg.F, cfg.n_shared
+    idx, w, maps = fwd["idx"], fwd["w"], fwd["maps"]
+    kept = maps["row_of"] >= 0
+    # combine backward
+    dO = _rb(np.where(kept, w, 0.0)[:, :, None] * dY[:, None, :], rounding)
+    dw = np.where(kept, np.einsum("th,tjh->tj", dY, fwd["y"]), 0.0)
+    dGU = np.zeros((T, k, 2 * F))
+    dX = np.zeros((T, k, H))
+    dW13 = np.zeros((E + S, 2 * F, H))
+    dW2 = np.zeros((E + S, H, F))
+    for e in range(E):
+        tt, jj = np.nonzero((idx == e) & kept)
+        if tt.size == 0:
+            dW13[e] = 0.0
+            dW2[e] = 0.0
+            continue
+        d = expert_fc2_dgrad_swiglu(dO[tt, jj], W2[e], fwd["GU"][tt, jj], rounding)
+        dGU[tt, jj] = d
+        dX[tt, jj] = expert_fc1_dgrad(d, W13[e], rounding)
+        dW2[e] = wgrad(dO[tt, jj], fwd["h"][tt, jj], rounding)
+        dW13[e] = wgrad(d, x[tt], rounding)
+    dGU_s = np.zeros((S, T, 2 * F))
+    dX_s = np.zeros((S, T, H))
+    dYb = _rb(dY, rounding)
+    for s in range(S):
+        dGU_s[s] = expert_fc2_dgrad_swiglu(dYb, W2[E + s], fwd["GU_s"][s], rounding)
+        dX_s[s] = expert_fc1_dgrad(dGU_s[s], W13[E + s], rounding)
+        dW2[E + s] = wgrad(dYb, fwd["h_s"][s], rounding)
+        dW13[E + s] = wgrad(dGU_s[s], x, rounding)
+    dlogits = router_dlogits(cfg, fwd["logits"], idx, w, dw)
+    dx_router = dlogits @ np.asarray(W_r, np.float64)
+    dx = _rb(dX.sum(axis=1) + dX_s.sum(axis=0) + dx_router, rounding)
+    dW_r = _rf(dlogits.T @ x, rounding)
+    return dict(dO=dO, dw=dw, dGU=dGU, dX=dX, dGU_s=dGU_s, dX_s=dX_s,
+                dlogits=dlogits, dx=dx, dW_r=dW_r, dW13=dW13, dW2=dW2)
+
+
+def to_rows(per_slot, per_shared, maps, cfg, width):
+    """Place per-(t,j) and per-shared-expert values at their permuted rows."""
+    R = maps["R"]
+    out = np.zeros((R, width))
+    r = maps["row_of"]
+    ok = r >= 0
+    out[r[ok]] = per_slot[ok]
+    T = r.shape[0]
+    for s in range(cfg.n_shared):
+        o = maps["offsets"][cfg.E + s]
+        out[o:o + T] = per_shared[s]
+    return out

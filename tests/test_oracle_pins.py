@@ -1,0 +1,377 @@
+"""Pins of the CPU oracle against things other than itself (CPU only).
+
+Each test checks the oracle against a brute-force restatement in plain Python,
+an independent library routine (torch), a closed form, or an invariant of the
+MoE layer (per-expert counts sum to T*k; permute then unpermute with identity
+experts returns sum_k w_k x; top-k equals a full sort; the grouped FFN equals
+per-token dense products; gradients equal autograd and finite differences).
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import moe_oracle as O
+from workloads import GROUP_MAX, GROUP_TOP2_SUM, SIGMOID, SOFTMAX, TINY, MoEShape, make_inputs
+
+pytestmark = pytest.mark.filterwarnings("ignore::RuntimeWarning")
+
+
+def f64(t):
+    return t.detach().to(torch.float64).cpu().numpy()
+
+
+# --------------------------------------------------------------------------- #
+# bf16 rounding against torch's own conversion
+# --------------------------------------------------------------------------- #
+def test_round_bf16_matches_torch_on_fp32_inputs():
+    g = torch.Generator().manual_seed(1)
+    v = torch.cat([
+        torch.randn(200000, generator=g) * 10.0 ** torch.randint(-30, 30, (200000,), generator=g).float(),
+        torch.tensor([0.0, -0.0, 1.0, -1.0, 3.0e38, -3.0e38, 3.4e38, 1e-40, -1e-40, 1e-45,
+                      float("inf"), float("-inf")]),
+    ])
+    # exact halfway cases: 1 + 2^-8 (tie -> even 1), 1 + 3*2^-8 (tie -> up)
+    v = torch.cat([v, torch.tensor([1 + 2 ** -8, 1 + 3 * 2 ** -8, -(1 + 2 ** -8), 2 ** -130 * 1.5])])
+    ref = v.to(torch.bfloat16).to(torch.float64).numpy()
+    got = O.round_bf16(v.to(torch.float64).numpy())
+    np.testing.assert_array_equal(got, ref)
+
+
+def test_round_bf16_ties_and_overflow():
+    assert O.round_bf16(1 + 2 ** -8) == 1.0
+    assert O.round_bf16(1 + 3 * 2 ** -8) == 1 + 2 ** -6
+    assert O.round_bf16(np.float64(3.4e38)) == np.inf
+    assert np.isnan(O.round_bf16(np.nan))
+
+
+# --------------------------------------------------------------------------- #
+# stage 1: route
+# --------------------------------------------------------------------------- #
+def test_logits_brute_force():
+    inp = make_inputs(TINY.with_(T=5, H=16, E=4), seed=3, weights=False, grad=False)
+    x, W = f64(inp["x"]), f64(inp["W_r"])
+    got = O.router_logits(x, W)
+    for t in range(5):
+        for e in range(4):
+            s = 0.0
+            for h in range(16):
+                s += x[t, h] * W[e, h]
+            assert got[t, e] == float(np.float32(s))
+
+
+def _brute_topk(scores, k, allowed=None):
+    # sort by (-score, expert); NaN ranks below every number
+    cand = sorted(((-(s if not math.isnan(s) else -math.inf), e) for e, s in enumerate(scores)
+                   if allowed is None or e in allowed))
+    return [e for _, e in cand[:k]]
+
+
+def _brute_route(l, cfg, bias):
+    T, E = l.shape
+    idx = np.zeros((T, cfg.k), dtype=np.int64)
+    w = np.zeros((T, cfg.k))
+    for t in range(T):
+        if cfg.score_fn == SOFTMAX:
+            sc = [float(np.float32(l[t, e]) + (np.float32(0) if bias is None else np.float32(bias[e])))
+                  for e in range(E)]
+            z = [l[t, e] + (0.0 if bias is None else float(np.float32(bias[e]))) for e in range(E)]
+        else:
+            s = [1.0 / (1.0 + math.exp(-l[t, e])) for e in range(E)]
+            sc = [s[e] + (0.0 if bias is None else float(np.float32(bias[e]))) for e in range(E)]
+        sc = [-math.inf if math.isnan(v) else v for v in sc]     # NaN ranks last
+        allowed = None
+        if cfg.n_groups > 1:
+            per = E // cfg.n_groups
+            gsc = []
+            for gi in range(cfg.n_groups):
+                mem = sorted(sc[gi * per:(gi + 1) * per], reverse=True)
+                gsc.append(mem[0] + mem[1] if (cfg.group_score == GROUP_TOP2_SUM and per >= 2) else mem[0])
+            keep = _brute_topk(gsc, cfg.topk_groups)
+            allowed = {gi * per + i for gi in keep for i in range(per)}
+        sel = _brute_topk(sc, cfg.k, allowed)
+        idx[t] = sel
+        if cfg.score_fn == SOFTMAX:
+            m = z[sel[0]]
+            ex = [math.exp(z[e] - m) for e in sel]
+            w[t] = [v / sum(ex) for v in ex]
+        else:
+            ssum = sum(s[e] for e in sel)
+            w[t] = [cfg.route_scale * s[e] / ssum for e in sel]
+    return idx, w
+
+
+@pytest.mark.parametrize("score_fn,groups,topg,gmode,bias", [
+    (SOFTMAX, 1, 1, GROUP_TOP2_SUM, False),
+    (SOFTMAX, 1, 1, GROUP_TOP2_SUM, True),
+    (SIGMOID, 1, 1, GROUP_TOP2_SUM, True),
+    (SIGMOID, 4, 2, GROUP_TOP2_SUM, True),
+    (SIGMOID, 4, 2, GROUP_MAX, True),
+    (SIGMOID, 8, 3, GROUP_TOP2_SUM, False),
+])
+def test_route_matches_brute_force_with_ties(score_fn, groups, topg, gmode, bias):
+    E, k, T = 16, 3, 64
+    cfg = MoEShape("t", T=T, H=8, E=E, k=k, F=8, score_fn=score_fn, n_groups=groups,
+                   topk_groups=topg, group_score=gmode, route_scale=2.5 if score_fn == SIGMOID else 1.0)
+    rng = np.random.default_rng(5)
+    l = O.round_f32(rng.standard_normal((T, E)))
+    # inject exact ties: copy columns, repeat values, a NaN
+    l[:, 5] = l[:, 2]
+    l[::3, 9] = l[::3, 1]
+    l[7, :] = 0.25
+    l[11, 4] = np.nan
+    b = O.round_f32(rng.standard_normal(E) * 0.1) if bias else None
+    idx, w = O.route(l, cfg, b)
+    ridx, rw = _brute_route(l, cfg, b)
+    np.testing.assert_array_equal(idx, ridx)
+    ok = np.isfinite(rw).all(axis=1)
+    np.testing.assert_allclose(w[ok], rw[ok], rtol=1e-12, atol=0)
+
+
+def test_group_limited_with_one_group_is_plain_topk():
+    cfg = MoEShape("t", T=40, H=8, E=12, k=4, F=8, score_fn=SIGMOID)
+    rng = np.random.default_rng(0)
+    l = O.round_f32(rng.standard_normal((40, 12)))
+    a = O.route(l, cfg, None)
+    b = O.route(l, cfg.with_(n_groups=1, topk_groups=1), None)
+    np.testing.assert_array_equal(a[0], b[0])
+    # G = E groups of one expert, keep k groups: also plain top-k
+    c = O.route(l, cfg.with_(n_groups=12, topk_groups=4, group_score=GROUP_MAX), None)
+    np.testing.assert_array_equal(a[0], c[0])
+
+
+def test_softmax_weights_match_torch_softmax_and_sum_to_one():
+    cfg = MoEShape("t", T=50, H=8, E=10, k=3, F=8)
+    rng = np.random.default_rng(2)
+    l = O.round_f32(rng.standard_normal((50, 10)) * 3)
+    idx, w = O.route(l, cfg, None)
+    ref = torch.softmax(torch.gather(torch.tensor(l), 1, torch.tensor(idx)), dim=1).numpy()
+    np.testing.assert_allclose(w, ref, rtol=1e-13)
+    np.testing.assert_allclose(w.sum(1), 1.0, rtol=1e-14)
+    cfg2 = cfg.with_(score_fn=SIGMOID, route_scale=1.7)
+    _, w2 = O.route(l, cfg2, None)
+    np.testing.assert_allclose(w2.sum(1), 1.7, rtol=1e-14)
+
+
+# --------------------------------------------------------------------------- #
+# stage 2: dispatch maps
+# --------------------------------------------------------------------------- #
+def _brute_maps(idx, cfg):
+    T, k = idx.shape
+    C = O.capacity(cfg)
+    items = sorted((int(idx[t, j]), t, j) for t in range(T) for j in range(k))
+    row_of = -np.ones((T, k), dtype=np.int64)
+    off = 0
+    offsets = []
+    for e in range(cfg.E):
+        offsets.append(off)
+        mine = [(t, j) for (ee, t, j) in items if ee == e]
+        kept = mine[:C] if C else mine
+        for r, (t, j) in enumerate(kept):
+            row_of[t, j] = off + r
+        seg = C if C else int(math.ceil(len(kept) / cfg.row_align) * cfg.row_align)
+        off += seg
+    return row_of, offsets
+
+
+@pytest.mark.parametrize("E,k,align,cf,shared", [(8, 2, 1, 0.0, 0), (8, 2, 128, 0.0, 1),
+                                                  (16, 4, 8, 0.0, 0), (16, 4, 8, 1.0, 0),
+                                                  (5, 5, 4, 0.0, 2), (64, 1, 16, 1.25, 0)])
+def test_maps_invariants_and_brute_force(E, k, align, cf, shared):
+    T = 97
+    cfg = MoEShape("t", T=T, H=8, E=E, k=k, F=8, row_align=align, capacity_factor=cf, n_shared=shared)
+    rng = np.random.default_rng(E * 7 + k)
+    # skewed routing: distinct experts per token drawn with a hot head
+    p = np.arange(1, E + 1, dtype=np.float64) ** -1.2
+    p /= p.sum()
+    idx = np.stack([rng.choice(E, size=k, replace=False, p=p) for _ in range(T)])
+    m = O.permutation_maps(idx, cfg)
+    rrow, roff = _brute_maps(idx, cfg)
+    np.testing.assert_array_equal(m["row_of"], rrow)
+    np.testing.assert_array_equal(m["offsets"][:E], roff)
+    kept = m["row_of"] >= 0
+    # P1: kept counts sum to the kept assignments (= T*k when dropless)
+    assert m["counts"][:E].sum() == kept.sum()
+    if cf == 0:
+        assert kept.all() and m["counts"][:E].sum() == T * k
+    # every kept assignment has its own row, token_of inverts row_of
+    rows = m["row_of"][kept]
+    assert len(set(rows.tolist())) == rows.size
+    tt = np.nonzero(kept)[0]
+    np.testing.assert_array_equal(m["token_of"][rows], tt)
+    # segments aligned, rows increase with t inside an expert
+    assert (m["offsets"] % align == 0).all()
+    for e in range(E):
+        seg = m["token_of"][m["offsets"][e]:m["offsets"][e] + m["counts"][e]]
+        assert (np.diff(seg) > 0).all()
+        assert (m["token_of"][m["offsets"][e] + m["counts"][e]:m["offsets"][e + 1]] == -1).all()
+    for s in range(shared):
+        o = m["offsets"][E + s]
+        np.testing.assert_array_equal(m["token_of"][o:o + T], np.arange(T))
+    # selection lists hold every selecting token in token order
+    for e in range(E):
+        st = m["sel_tokens"][m["sel_offsets"][e]:m["sel_offsets"][e + 1]]
+        np.testing.assert_array_equal(st, np.nonzero((idx == e).any(1))[0])
+
+
+def test_capacity_value_and_keep_first_tokens():
+    cfg = MoEShape("t", T=16384, H=8, E=256, k=8, F=8, capacity_factor=1.25)
+    assert O.capacity(cfg) == 640
+    cfg = MoEShape("t", T=10, H=8, E=2, k=1, F=8, capacity_factor=0.5, row_align=1)
+    idx = np.zeros((10, 1), dtype=np.int64)
+    idx[7:] = 1
+    m = O.permutation_maps(idx, cfg)
+    assert O.capacity(cfg) == 3
+    np.testing.assert_array_equal(m["row_of"][:, 0], [0, 1, 2, -1, -1, -1, -1, 3, 4, 5])
+
+
+def test_identity_experts_round_trip():
+    """P3: permute, identity experts, unpermute: out = bf16(sum_j w_j x) = x."""
+    cfg = MoEShape("t", T=64, H=32, E=8, k=3, F=8)
+    inp = make_inputs(cfg, seed=4, weights=False, grad=False)
+    x = f64(inp["x"])
+    idx, w = O.route(O.router_logits(x, f64(inp["W_r"])), cfg, None)
+    m = O.permutation_maps(idx, cfg)
+    xp = O.permute(x, m)
+    out = np.zeros_like(x)
+    for t in range(64):
+        out[t] = sum(w[t, j] * xp[m["row_of"][t, j]] for j in range(3))
+    np.testing.assert_array_equal(O.round_bf16(out), x)
+    cfg2 = cfg.with_(score_fn=SIGMOID, route_scale=0.5)
+    idx2, w2 = O.route(O.router_logits(x, f64(inp["W_r"])), cfg2, None)
+    m2 = O.permutation_maps(idx2, cfg2)
+    xp2 = O.permute(x, m2)
+    out2 = np.stack([sum(w2[t, j] * xp2[m2["row_of"][t, j]] for j in range(3)) for t in range(64)])
+    np.testing.assert_allclose(out2, 0.5 * x, rtol=1e-14)
+
+
+# --------------------------------------------------------------------------- #
+# stage 3 / whole layer
+# --------------------------------------------------------------------------- #
+def _torch_bf16(a):
+    return a.to(torch.bfloat16).to(torch.float64)
+
+
+def test_single_expert_layer_is_dense_swiglu_mlp():
+    """P4: E=1, k=1 reduces the layer to one dense SwiGLU MLP (torch fp64)."""
+    cfg = MoEShape("t", T=48, H=64, E=1, k=1, F=96)
+    inp = make_inputs(cfg, seed=9)
+    fwd = O.layer_forward(cfg, f64(inp["x"]), f64(inp["W_r"]), None, f64(inp["W13"]), f64(inp["W2"]))
+    x = inp["x"].double()
+    W13, W2 = inp["W13"][0].double(), inp["W2"][0].double()
+    gu = _torch_bf16(x @ W13.T)
+    h = _torch_bf16(torch.nn.functional.silu(gu[:, :96]) * gu[:, 96:])
+    y = _torch_bf16(h @ W2.T)
+    np.testing.assert_allclose(fwd["out"], y.numpy(), rtol=2 ** -7, atol=1e-6)
+    assert np.mean(fwd["out"] == y.numpy()) > 0.99
+    np.testing.assert_allclose(fwd["w"], 1.0)
+
+
+def test_grouped_ffn_equals_per_token_products_and_is_equivariant():
+    """P5: batched expert FFN = one row at a time; permuting tokens permutes out."""
+    cfg = MoEShape("t", T=40, H=32, E=4, k=2, F=48)
+    inp = make_inputs(cfg, seed=11)
+    x, Wr, W13, W2 = (f64(inp[n]) for n in ("x", "W_r", "W13", "W2"))
+    fwd = O.layer_forward(cfg, x, Wr, None, W13, W2)
+    for t in range(0, 40, 7):
+        for j in range(2):
+            e = fwd["idx"][t, j]
+            g = np.array([sum(x[t, hh] * W13[e, n, hh] for hh in range(32)) for n in range(96)])
+            np.testing.assert_allclose(fwd["GU"][t, j], O.round_bf16(g), rtol=2 ** -7)
+    perm = np.random.default_rng(0).permutation(40)
+    fwd2 = O.layer_forward(cfg, x[perm], Wr, None, W13, W2)
+    np.testing.assert_allclose(fwd2["out"], fwd["out"][perm], rtol=2 ** -7, atol=1e-6)
+    np.testing.assert_array_equal(fwd2["idx"], fwd["idx"][perm])
+
+
+def test_capacity_to_infinity_is_dropless():
+    """P7: with an unreachable capacity nothing drops and values equal dropless."""
+    cfg = MoEShape("t", T=32, H=32, E=4, k=2, F=32)
+    inp = make_inputs(cfg, seed=12)
+    args = [f64(inp[n]) for n in ("x", "W_r")] + [None] + [f64(inp[n]) for n in ("W13", "W2")]
+    a = O.layer_forward(cfg, *args)
+    b = O.layer_forward(cfg.with_(capacity_factor=100.0), *args)
+    assert (b["maps"]["row_of"] >= 0).all()
+    np.testing.assert_array_equal(a["out"], b["out"])
+
+
+def _torch_layer(cfg, x, Wr, bias, W13, W2, idx, kept):
+    T, H = x.shape
+    l = x @ Wr.T
+    it = torch.tensor(idx)
+    if cfg.score_fn == SOFTMAX:
+        z = l + (0.0 if bias is None else torch.tensor(bias, dtype=torch.float64))
+        w = torch.softmax(torch.gather(z, 1, it), dim=1)
+    else:
+        s = torch.sigmoid(torch.gather(l, 1, it))
+        w = cfg.route_scale * s / s.sum(1, keepdim=True)
+    F = cfg.F
+    outs = []
+    for t in range(T):
+        acc = torch.zeros(H, dtype=torch.float64)
+        for j in range(cfg.k):
+            if not kept[t, j]:
+                continue
+            e = int(idx[t, j])
+            gu = W13[e] @ x[t]
+            hh = torch.nn.functional.silu(gu[:F]) * gu[F:]
+            acc = acc + w[t, j] * (W2[e] @ hh)
+        for s_ in range(cfg.n_shared):
+            gu = W13[cfg.E + s_] @ x[t]
+            hh = torch.nn.functional.silu(gu[:F]) * gu[F:]
+            acc = acc + W2[cfg.E + s_] @ hh
+        outs.append(acc)
+    return torch.stack(outs)
+
+
+@pytest.mark.parametrize("cfg", [
+    MoEShape("t", T=8, H=16, E=4, k=2, F=32, bias_kind="zipf"),
+    MoEShape("t", T=8, H=16, E=8, k=3, F=16, n_shared=1, score_fn=SIGMOID, n_groups=4,
+             topk_groups=2, bias_kind="normal", route_scale=1.5),
+    MoEShape("t", T=12, H=16, E=4, k=2, F=16, capacity_factor=0.5, row_align=1,
+             score_fn=SIGMOID, bias_kind="normal"),
+])
+def test_backward_equals_autograd_and_finite_differences(cfg):
+    """P6: the oracle's backward (no rounding) = torch autograd = central FD."""
+    inp = make_inputs(cfg, seed=21)
+    x, Wr, W13, W2, dY = (f64(inp[n]) for n in ("x", "W_r", "W13", "W2", "dY"))
+    W13 = W13 * 10.0          # make the FFN non-trivial at this size
+    W2 = W2 * 10.0
+    bias = None if inp["bias"] is None else f64(inp["bias"])
+    fwd = O.layer_forward(cfg, x, Wr, bias, W13, W2, rounding=False)
+    bwd = O.layer_backward(cfg, x, Wr, W13, W2, fwd, dY, rounding=False)
+    kept = fwd["maps"]["row_of"] >= 0
+    if cfg.capacity_factor > 0:
+        assert (~kept).any()
+    tx, tWr, tW13, tW2 = (torch.tensor(a, requires_grad=True) for a in (x, Wr, W13, W2))
+    out = _torch_layer(cfg, tx, tWr, bias, tW13, tW2, fwd["idx"], kept)
+    np.testing.assert_allclose(fwd["out"], out.detach().numpy(), rtol=1e-12, atol=1e-12)
+    (out * torch.tensor(dY)).sum().backward()
+    for name, t in (("dx", tx), ("dW_r", tWr), ("dW13", tW13), ("dW2", tW2)):
+        np.testing.assert_allclose(bwd[name], t.grad.numpy(), rtol=1e-9, atol=1e-10, err_msg=name)
+    # central finite differences on a few coordinates
+    def loss(xx, wr, w13, w2):
+        f = O.layer_forward(cfg, xx, wr, bias, w13, w2, rounding=False)
+        np.testing.assert_array_equal(f["idx"], fwd["idx"])
+        return float((f["out"] * dY).sum())
+    eps = 1e-6
+    for (arr_i, pos, gname) in ((0, (3, 5), "dx"), (1, (2, 7), "dW_r"), (2, (1, 3, 4), "dW13"),
+                                (3, (0, 2, 1), "dW2")):
+        args = [x.copy(), Wr.copy(), W13.copy(), W2.copy()]
+        args[arr_i][pos] += eps
+        lp = loss(*args)
+        args[arr_i][pos] -= 2 * eps
+        lm = loss(*args)
+        fd = (lp - lm) / (2 * eps)
+        assert abs(fd - bwd[gname][pos]) <= 1e-5 * (1 + abs(fd)), (gname, fd, bwd[gname][pos])
+
+
+def test_softmax_jacobian_rows_sum_to_zero():
+    cfg = MoEShape("t", T=30, H=8, E=6, k=3, F=8)
+    rng = np.random.default_rng(3)
+    l = rng.standard_normal((30, 6))
+    idx, w = O.route(l, cfg, None)
+    dl = O.router_dlogits(cfg, l, idx, w, rng.standard_normal((30, 3)))
+    np.testing.assert_allclose(dl.sum(1), 0.0, atol=1e-14)
+    assert (np.count_nonzero(dl, axis=1) <= 3).all()
