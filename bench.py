@@ -1,0 +1,349 @@
+"""Benchmark of one MoE layer step (forward + backward) on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload mixtral]
+                    [--impl ours|reference]
+
+A step is one pass of the whole layer over one batch of synthetic tokens:
+route, permute, grouped SwiGLU FFN, unpermute, and the backward of all of it
+(dx, dW_r, dW13, dW2). The default workload is the Mixtral-style layer
+(T=4096, H=4096, E=8, top-2 softmax, d_ff=14336, bf16). Prints one JSON line.
+
+  value      tokens/s of fwd+bwd with inputs resident in HBM (CUDA events)
+  e2e        the same through the public layer calls with host buffers: each
+             step copies x and dY from pinned host memory and reads out and dx
+             back inside the timed region
+  roofline   the grouped-GEMM kernel family (the dominant kernel) against the
+             measured dense bf16 tensor peak
+  cpu_baseline  the CPU oracle timed on a bounded sample of the same workload
+
+--impl reference times the CPU oracle instead (the reference arm of this
+build: there is no runnable upstream implementation).
+Multi-GPU: the layer is not sharded, so N GPUs run N independent replicas
+(weak scaling, no collective on the data path); value sums the replicas.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+import workloads as W  # noqa: E402
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default="mixtral", choices=sorted(W.SHAPES))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-sample-tokens", type=int, default=0)
+    return ap.parse_args()
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled during the timed region."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thr = threading.Thread(target=self._read, daemon=True)
+            self.thr.start()
+        except OSError:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            p = [x.strip() for x in line.split(",")]
+            if len(p) < 9:
+                continue
+            try:
+                sm.append(float(p[1]))
+                smax.append(float(p[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, p[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": float(np.median(sm)) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def gemm_flops(shape, counts) -> tuple:
+    """Algorithmic flops of the grouped GEMMs of one step (kept rows only)."""
+    rows = float(sum(counts))        # routed kept rows + shared rows (T each)
+    fwd = 2.0 * rows * shape.H * 2 * shape.F + 2.0 * rows * shape.F * shape.H
+    bwd = 2.0 * fwd
+    return fwd, bwd
+
+
+# ---------------------------------------------------------------------------- ours
+def run_ours(args, rank, world, local):
+    import routing_dispatch_expert_router_gb300.binding as B
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    shape = W.SHAPES[args.workload]
+    cfg = B.config(shape)
+    inp = W.make_inputs(shape, seed=args.seed + rank, device=str(dev))
+    bufs = B.alloc_buffers(cfg, dev)
+    T, H, E, F, S = shape.T, shape.H, shape.E, shape.F, shape.n_shared
+    G = E + S
+    out = torch.empty(T, H, dtype=torch.bfloat16, device=dev)
+    dx = torch.empty_like(out)
+    dW_r = torch.empty(E, H, dtype=torch.float32, device=dev)
+    dW13 = torch.empty(G, 2 * F, H, dtype=torch.bfloat16, device=dev)
+    dW2 = torch.empty(G, H, F, dtype=torch.bfloat16, device=dev)
+    P = B.params(inp["W_r"], inp["bias"], inp["W13"], inp["W2"])
+    f, b = bufs.fwd, bufs.bwd
+    x, dY = inp["x"], inp["dY"]
+    stream = torch.cuda.current_stream(dev)
+    sc = bufs.scratch
+
+    def step(ev=None):
+        # the layer step through the per-stage entry points (the same launches
+        # as moe_layer_fwd + moe_layer_bwd), with events around the GEMMs
+        B.moe_route(cfg, x, inp["W_r"], inp["bias"], f["logits"], f["idx"], f["w"], sc)
+        B.moe_permute(cfg, x, f["idx"], f["counts"], f["offsets"], f["row_of"], f["token_of"],
+                      f["sel_offsets"], f["sel_tokens"], f["x_perm"], sc)
+        if ev: ev[0].record(stream)
+        B.moe_grouped_ffn_fwd(cfg, f["x_perm"], f["counts"], f["offsets"], inp["W13"], inp["W2"],
+                              f["GU"], f["h"], f["y_perm"], sc)
+        if ev: ev[1].record(stream)
+        B.moe_unpermute(cfg, f["y_perm"], f["row_of"], f["w"], f["offsets"], out)
+        B.moe_unpermute_bwd(cfg, dY, f["y_perm"], f["row_of"], f["w"], f["counts"], f["offsets"],
+                            b["dO_perm"], b["dw"])
+        B.moe_route_bwd(cfg, f["logits"], f["idx"], f["w"], b["dw"], b["dlogits"])
+        if ev: ev[2].record(stream)
+        B.moe_grouped_ffn_bwd(cfg, b["dO_perm"], f["x_perm"], f["GU"], f["h"], f["counts"],
+                              f["offsets"], inp["W13"], inp["W2"], b["dGU"], b["dX_perm"], dW13,
+                              dW2, sc)
+        if ev: ev[3].record(stream)
+        B.moe_permute_bwd(cfg, b["dX_perm"], f["row_of"], f["offsets"], f["idx"], b["dlogits"],
+                          inp["W_r"], dx)
+        B.moe_router_wgrad(cfg, x, f["sel_offsets"], f["sel_tokens"], b["dlogits"], dW_r)
+
+    launches_per_step = 2 + 3 + 2 + 1 + 1 + 1 + 4 + 1 + 1
+    for _ in range(max(args.warmup, 3)):
+        step()
+    torch.cuda.synchronize(dev)
+    status = B.moe_last_device_status(sc)
+    if status != 0:
+        raise RuntimeError(f"device status {status} after warm-up")
+    counts = f["counts"].cpu().tolist()
+    fl_fwd, fl_bwd = gemm_flops(shape, counts)
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(local)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize(dev)
+    clocks.start()
+    t0.record(stream)
+    for i in range(args.steps):
+        step(evs[i])
+    t1.record(stream)
+    torch.cuda.synchronize(dev)
+    clk = clocks.stop()
+    ms = t0.elapsed_time(t1)
+    gemm_ms = sum(e[0].elapsed_time(e[1]) + e[2].elapsed_time(e[3]) for e in evs) / args.steps
+    fwd_gemm_ms = sum(e[0].elapsed_time(e[1]) for e in evs) / args.steps
+    bwd_gemm_ms = sum(e[2].elapsed_time(e[3]) for e in evs) / args.steps
+
+    # end to end through the public layer calls, host buffers
+    xh = x.cpu().pin_memory()
+    dYh = dY.cpu().pin_memory()
+    outh = torch.empty_like(xh).pin_memory()
+    dxh = torch.empty_like(xh).pin_memory()
+    xd = torch.empty_like(x)
+    dYd = torch.empty_like(dY)
+
+    def e2e_step():
+        xd.copy_(xh, non_blocking=True)
+        dYd.copy_(dYh, non_blocking=True)
+        B.moe_layer_fwd(cfg, P, xd, out, bufs.fwd_struct, sc)
+        B.moe_layer_bwd(cfg, P, xd, dYd, bufs.fwd_struct, bufs.bwd_struct, dx, dW_r, dW13, dW2, sc)
+        outh.copy_(out, non_blocking=True)
+        dxh.copy_(dx, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = e0.elapsed_time(e1)
+    status = B.moe_last_device_status(sc)
+    if status != 0:
+        raise RuntimeError(f"device status {status} after timed steps")
+
+    times = torch.tensor([ms, e2e_ms], dtype=torch.float64, device=dev)
+    if world > 1:
+        torch.distributed.all_reduce(times, op=torch.distributed.ReduceOp.MAX)
+    ms, e2e_ms = times.tolist()
+    pk, src = peaks()
+    peak = pk.get("bf16_tflops_sustained", pk["bf16_tflops"])
+    achieved = (fl_fwd + fl_bwd) / (gemm_ms * 1e-3) / 1e12
+    tokens = T * args.steps * world
+    res = {
+        "metric": "MoE-layer tokens/s fwd+bwd on 1 GB300",
+        "value": tokens / (ms * 1e-3),
+        "unit": "tokens/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": ms / args.steps,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) tokens, N(0,0.02^2) weights; no dataset)",
+        "config": {"workload": f"{shape.name}: T={T} H={H} E={E}(+{S} shared) top-{shape.k} "
+                               f"F={F} fwd+bwd", "l2": "inputs larger than L2 (weights "
+                               f"{2 * G * 3 * H * F / 1e9:.2f} GB streamed per step)",
+                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "e2e": {"value": tokens / (e2e_ms * 1e-3), "unit": "tokens/s",
+                "h2d_bytes_per_step": 2 * T * H * 2, "d2h_bytes_per_step": 2 * T * H * 2},
+        "gpu_launches": launches_per_step * args.steps,
+        "roofline": {"kernel": "grouped_gemm_kernel (tcgen05; FC1+SwiGLU, FC2, 2 dgrad, 2 wgrad)",
+                     "bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                     "frac": achieved / peak, "peak_source": f"{src} bf16_tflops_sustained",
+                     "traffic": None, "gemm_ms_per_step": gemm_ms,
+                     "fwd_gemm_ms": fwd_gemm_ms, "bwd_gemm_ms": bwd_gemm_ms,
+                     "gemm_tflop_per_step": (fl_fwd + fl_bwd) / 1e12},
+        "clocks": clk,
+    }
+    return res, shape
+
+
+# ---------------------------------------------------------------------- the oracle
+def oracle_sample(shape, n_tok: int, seed: int):
+    """The CPU oracle's fwd+bwd on the first n_tok tokens of the workload."""
+    from oracle import moe_oracle as O
+    sub = shape.with_(T=n_tok)
+    inp = W.make_inputs(shape, seed=seed, device="cpu")
+    x = inp["x"][:n_tok].double().numpy()
+    dY = inp["dY"][:n_tok].double().numpy()
+    Wr = inp["W_r"].double().numpy()
+    bias = None if inp["bias"] is None else inp["bias"].double().numpy()
+    W13 = inp["W13"].double().numpy()
+    W2 = inp["W2"].double().numpy()
+    t0 = time.perf_counter()
+    fwd = O.layer_forward(sub, x, Wr, bias, W13, W2)
+    O.layer_backward(sub, x, Wr, W13, W2, fwd, dY)
+    return time.perf_counter() - t0
+
+
+def cpu_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def run_reference(args):
+    shape = W.SHAPES[args.workload]
+    n_tok = args.cpu_sample_tokens or (64 if shape.name != "tiny" else shape.T)
+    for _ in range(max(args.warmup, 0) and 1):
+        oracle_sample(shape, min(n_tok, 8), args.seed)
+    secs = [oracle_sample(shape, n_tok, args.seed) for _ in range(args.steps)]
+    tot = sum(secs)
+    val = n_tok * args.steps / tot
+    cb = {"value": val, "unit": "tokens/s", "cores": cpu_cores(), "kind": "oracle",
+          "sample": f"first {n_tok} tokens of {shape.name} per step (routing, experts, combine, "
+                    "full backward incl. weight gradients of those tokens), fp64 numpy"}
+    return {"impl": "reference", "metric": "MoE-layer tokens/s fwd+bwd on 1 GB300", "value": val,
+            "unit": "tokens/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1e3 * tot / args.steps, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": shape.name}, "cpu_baseline": cb,
+            "e2e": {"value": val, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+
+
+def main():
+    args = parse()
+    rank, world, local = dist_env()
+    if world > 1:
+        torch.distributed.init_process_group("nccl" if args.impl == "ours" else "gloo")
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args)), flush=True)
+        if world > 1:
+            torch.distributed.destroy_process_group()
+        return
+    res, shape = run_ours(args, rank, world, local)
+    if rank == 0:
+        if not args.no_cpu_baseline:
+            n_tok = args.cpu_sample_tokens or 64
+            secs = oracle_sample(shape, n_tok, args.seed)
+            res["cpu_baseline"] = {
+                "value": n_tok / secs, "unit": "tokens/s", "cores": cpu_cores(), "kind": "oracle",
+                "sample": f"first {n_tok} tokens of {shape.name}: oracle fwd+bwd incl. weight "
+                          "gradients of those tokens, fp64 numpy, one pass"}
+        print(json.dumps(res), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,233 @@
+/*
+ * moe_abi.h -- C-ABI of a single-GPU Mixture-of-Experts layer for GB300 (sm_103a).
+ *
+ * The layer is the four-stage MoE layer of "Scalable Training of
+ * Mixture-of-Experts Models with Megatron Core" (gist.science summaries; es:
+ * "Resumen técnico" §2.1 "Arquitectura de la Capa MoE"):
+ *   route    -- a router picks the k best experts of every token,
+ *   dispatch -- tokens are moved to their experts (here: a permutation into
+ *               per-expert contiguous rows of one buffer, since all experts
+ *               live on this GPU),
+ *   compute  -- every expert's SwiGLU FFN runs as one grouped GEMM,
+ *   combine  -- the results return to their tokens, weighted by the router,
+ * plus the backward of all four.
+ *
+ * Conventions shared by every call:
+ *  - Pointers named x, W_*, out, ... are DEVICE pointers unless stated.
+ *    cfg / params / state structs themselves live in HOST memory.
+ *  - The caller owns every buffer; the library never allocates or frees
+ *    device memory. Buffers are sized for the worst case with
+ *    moe_query_sizes() (the Hybrid-EP article's "worst-case pre-reservation",
+ *    hyper.ai, on dynamic token counts).
+ *  - All calls are asynchronous on `stream` (a cudaStream_t, NULL = legacy
+ *    default stream) and never synchronise the host or read device memory
+ *    from the host, except moe_last_device_status(). Token counts stay on the
+ *    device: kernels read them there (the sync-free, device-initiated
+ *    execution of the same page, §2.3.C).
+ *  - Layouts are row-major. bf16 tensors are passed as `void*` holding IEEE
+ *    bfloat16. Index tensors are int32.
+ *  - Argument errors are returned synchronously (MOE_ERR_INVALID_ARG /
+ *    MOE_ERR_UNSUPPORTED) before anything is launched. Problems detected by a
+ *    kernel (an index out of range, a bounded wait that ran out) are recorded
+ *    in a status word at the start of `scratch`; kernels never trap.
+ *
+ * Shapes: T tokens, H hidden, E routed experts, k experts per token, F FFN
+ * width of one expert, S = n_shared shared experts, G = E + S groups,
+ * R = rows_max (moe_query_sizes) rows in every permuted buffer.
+ */
+#ifndef MOE_ABI_H
+#define MOE_ABI_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define MOE_API __attribute__((visibility("default")))
+#else
+#define MOE_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum moe_status {
+    MOE_OK = 0,
+    MOE_ERR_INVALID_ARG = 1,   /* bad pointer, shape or alignment            */
+    MOE_ERR_UNSUPPORTED = 2,   /* a valid configuration this build lacks      */
+    MOE_ERR_WORKSPACE = 3,     /* scratch too small                           */
+    MOE_ERR_CUDA = 4,          /* a CUDA runtime call failed                  */
+    MOE_ERR_TIMEOUT = 5,       /* a device-side bounded wait ran out          */
+    MOE_ERR_DEVICE_CHECK = 6   /* a kernel found an out-of-range index        */
+} moe_status;
+
+enum { MOE_SCORE_SOFTMAX = 0, MOE_SCORE_SIGMOID = 1 };
+enum { MOE_GROUP_TOP2_SUM = 0, MOE_GROUP_MAX = 1 };
+enum { MOE_DTYPE_BF16 = 0 };
+
+/* One layer configuration. */
+typedef struct moe_config {
+    int32_t T, H, E, k, F;
+    int32_t n_shared;        /* shared experts (weight 1, every token), 0..4    */
+    int32_t score_fn;        /* MOE_SCORE_SOFTMAX | MOE_SCORE_SIGMOID           */
+    int32_t n_groups;        /* expert groups for group-limited top-k (1 = off) */
+    int32_t topk_groups;     /* groups kept per token                           */
+    int32_t group_score;     /* MOE_GROUP_TOP2_SUM | MOE_GROUP_MAX              */
+    float route_scale;       /* sigmoid weights: route_scale * s_j / sum s      */
+    int32_t dtype;           /* MOE_DTYPE_BF16                                  */
+    float capacity_factor;   /* 0 = dropless; else C = ceil(cf*T*k/E) rows      */
+    int32_t row_align;       /* every expert segment is a multiple of this (128)*/
+} moe_config;
+
+/* Worst-case sizes of the caller-owned buffers for one configuration. */
+typedef struct moe_sizes {
+    int64_t rows_max;        /* R: rows of x_perm, GU, h, y_perm, dO, dGU, dX   */
+    int64_t groups;          /* G = E + n_shared                                */
+    int64_t capacity;        /* C rows per expert (0 = dropless)                */
+    int64_t scratch_bytes;   /* bytes of `scratch` (zero-fill it once)          */
+} moe_sizes;
+
+/* Layer parameters (device pointers).
+ * W_r [E,H] fp32 router weight; bias [E] fp32 or NULL (softmax: added to the
+ * logits; sigmoid: added to the scores for selection only);
+ * W13 [G,2F,H] bf16 (rows 0..F-1 gate, F..2F-1 up); W2 [G,H,F] bf16. Shared
+ * experts are the last S groups. */
+typedef struct moe_params {
+    const float* W_r;
+    const float* bias;
+    const void* W13;
+    const void* W2;
+} moe_params;
+
+/* Forward state, kept for the backward (device pointers, caller-owned). */
+typedef struct moe_fwd_state {
+    float* logits;           /* [T,E]   fp32 router logits (before bias)        */
+    int32_t* idx;            /* [T,k]   selected experts, best first            */
+    float* w;                /* [T,k]   routing weights                         */
+    int32_t* counts;         /* [G]     rows kept per group                     */
+    int32_t* offsets;        /* [G+1]   first row of every group segment        */
+    int32_t* row_of;         /* [T,k]   row of assignment (t,j); -1 = dropped   */
+    int32_t* token_of;       /* [R]     token of row r; -1 = padding            */
+    int32_t* sel_offsets;    /* [E+1]   per expert: start in sel_tokens         */
+    int32_t* sel_tokens;     /* [T*k]   per expert, every selecting token, in t */
+    void* x_perm;            /* [R,H]   bf16 dispatched tokens (padding = 0)    */
+    void* GU;                /* [R,2F]  bf16 gate|up pre-activations            */
+    void* h;                 /* [R,F]   bf16 SwiGLU output                      */
+    void* y_perm;            /* [R,H]   bf16 expert outputs                     */
+} moe_fwd_state;
+
+/* Backward temporaries (device pointers, caller-owned). */
+typedef struct moe_bwd_state {
+    void* dO_perm;           /* [R,H]   bf16 gradient at the expert outputs     */
+    float* dw;               /* [T,k]   gradient of the routing weights         */
+    float* dlogits;          /* [T,E]   gradient of the logits                  */
+    void* dGU;               /* [R,2F]  bf16 gradient of gate|up                */
+    void* dX_perm;           /* [R,H]   bf16 gradient of the dispatched tokens  */
+} moe_bwd_state;
+
+/* Worst-case buffer sizes. Returns MOE_ERR_INVALID_ARG / MOE_ERR_UNSUPPORTED
+ * for configurations the library rejects: H and F must be multiples of 128,
+ * 1 <= k <= E <= 256, E % n_groups == 0, topk_groups*(E/n_groups) >= k,
+ * row_align a multiple of 128. Host only. */
+MOE_API moe_status moe_query_sizes(const moe_config* cfg, moe_sizes* out);
+
+/* Stage 1, route (es summary §2.1 step 1; router in fp32, §2.4).
+ * logits = x W_r^T (fp32 accumulation); selection of the k best experts with
+ * ties to the lower index -- softmax: on the fp32 value logits + bias;
+ * sigmoid: on sigmoid(logits) + bias evaluated in fp64, optionally limited to
+ * the topk_groups best groups (group score: sum of the two best, or the best,
+ * selection scores of the group). Weights: softmax over the k selected
+ * (renormalised), or route_scale * s_j / sum_sel s.
+ * x [T,H] bf16, W_r [E,H] f32, bias [E] f32 or NULL -> logits [T,E] f32,
+ * idx [T,k] i32, w [T,k] f32. */
+MOE_API moe_status moe_route(const moe_config* cfg, const void* x, const float* W_r, const float* bias,
+                     float* logits, int32_t* idx, float* w, void* scratch, void* stream);
+
+/* Stage 2, dispatch (es summary §2.1 step 2, done locally). A stable counting
+ * sort of the (token, slot) assignments by (expert, token): expert e's kept
+ * tokens occupy rows offsets[e] .. offsets[e]+counts[e]-1 in increasing token
+ * order; segments are padded to row_align rows (or are C rows in capacity
+ * mode, where the first C tokens of an expert are kept); shared experts
+ * follow, one row per token. Writes the maps and x_perm (padding rows zero).
+ * scratch: moe_sizes.scratch_bytes bytes. */
+MOE_API moe_status moe_permute(const moe_config* cfg, const void* x, const int32_t* idx,
+                       int32_t* counts, int32_t* offsets, int32_t* row_of, int32_t* token_of,
+                       int32_t* sel_offsets, int32_t* sel_tokens, void* x_perm,
+                       void* scratch, void* stream);
+
+/* Stage 3, compute (es summary §2.1 step 3; grouped GEMM, §2.3.C): for every
+ * group g, on its rows X: [G|U] = X W13[g]^T (GU, bf16), h = bf16(silu(G) U),
+ * y_perm = bf16(h W2[g]^T). tcgen05 grouped GEMMs that read counts/offsets on
+ * the device. */
+MOE_API moe_status moe_grouped_ffn_fwd(const moe_config* cfg, const void* x_perm, const int32_t* counts,
+                               const int32_t* offsets, const void* W13, const void* W2,
+                               void* GU, void* h, void* y_perm, void* scratch, void* stream);
+
+/* Stage 4, combine (es summary §2.1 step 4, done locally):
+ * out[t] = bf16( sum_j w[t,j] y_perm[row_of[t,j]] + sum_s y_perm[offsets[E+s]+t] ),
+ * fp32 accumulation; dropped assignments contribute 0. */
+MOE_API moe_status moe_unpermute(const moe_config* cfg, const void* y_perm, const int32_t* row_of,
+                         const float* w, const int32_t* offsets, void* out, void* stream);
+
+/* Backward of stage 4: dO_perm[row_of[t,j]] = bf16(w[t,j] dY[t]),
+ * dw[t,j] = <dY[t], y_perm[row_of[t,j]]> (0 if dropped); shared rows get dY;
+ * padding rows of dO_perm are zeroed. */
+MOE_API moe_status moe_unpermute_bwd(const moe_config* cfg, const void* dY, const void* y_perm,
+                             const int32_t* row_of, const float* w, const int32_t* counts,
+                             const int32_t* offsets, void* dO_perm, float* dw, void* stream);
+
+/* Backward of stage 3 (the W/D split of es summary §2.3.B: separate data- and
+ * weight-gradient GEMMs): dh = dO W2[g] (fp32, not stored); SwiGLU backward
+ * with the stored GU -> dGU (bf16); dW2[g] = dO^T h; dX_perm = dGU W13[g];
+ * dW13[g] = dGU^T x_perm (weight gradients in bf16, zero for empty groups). */
+MOE_API moe_status moe_grouped_ffn_bwd(const moe_config* cfg, const void* dO_perm, const void* x_perm,
+                               const void* GU, const void* h, const int32_t* counts,
+                               const int32_t* offsets, const void* W13, const void* W2,
+                               void* dGU, void* dX_perm, void* dW13, void* dW2,
+                               void* scratch, void* stream);
+
+/* Backward of the routing weights to the logits (dense [T,E], zero outside the
+ * selected experts). softmax: dl_j = w_j (dw_j - sum_i w_i dw_i); sigmoid:
+ * ds_j = (r/S)(dw_j - sum_i (s_i/S) dw_i), dl_j = ds_j s_j (1 - s_j). */
+MOE_API moe_status moe_route_bwd(const moe_config* cfg, const float* logits, const int32_t* idx,
+                         const float* w, const float* dw, float* dlogits, void* stream);
+
+/* Backward of stage 2 plus the router's input gradient:
+ * dx[t] = bf16( sum_j dX_perm[row_of[t,j]] + sum_s dX_perm[offsets[E+s]+t]
+ *               + sum_j dlogits[t, idx[t,j]] W_r[idx[t,j]] ). */
+MOE_API moe_status moe_permute_bwd(const moe_config* cfg, const void* dX_perm, const int32_t* row_of,
+                           const int32_t* offsets, const int32_t* idx, const float* dlogits,
+                           const float* W_r, void* dx, void* stream);
+
+/* Router weight gradient: dW_r[e] = sum over tokens t that selected e of
+ * dlogits[t,e] x[t] (fp32, fixed summation order). */
+MOE_API moe_status moe_router_wgrad(const moe_config* cfg, const void* x, const int32_t* sel_offsets,
+                            const int32_t* sel_tokens, const float* dlogits, float* dW_r,
+                            void* stream);
+
+/* The whole layer forward: route, permute, grouped FFN, unpermute. */
+MOE_API moe_status moe_layer_fwd(const moe_config* cfg, const moe_params* params, const void* x,
+                         void* out, const moe_fwd_state* st, void* scratch, void* stream);
+
+/* The whole layer backward from the forward state: dx (bf16), dW_r (fp32),
+ * dW13, dW2 (bf16). */
+MOE_API moe_status moe_layer_bwd(const moe_config* cfg, const moe_params* params, const void* x,
+                         const void* dY, const moe_fwd_state* st, const moe_bwd_state* bs,
+                         void* dx, float* dW_r, void* dW13, void* dW2, void* scratch,
+                         void* stream);
+
+/* Synchronises `stream`, then copies the device status word from scratch to
+ * *code (0 = no problem recorded). */
+MOE_API moe_status moe_last_device_status(const void* scratch, int32_t* code, void* stream);
+
+/* Resets the device status word (async on stream). */
+MOE_API moe_status moe_clear_device_status(void* scratch, void* stream);
+
+/* Static text for a status code. */
+MOE_API const char* moe_status_string(moe_status s);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_ABI_H */

@@ -1,0 +1,363 @@
+// Stage 4 of the MoE layer (combine, done locally), its backward, the backward
+// of stage 2 (dispatch) and of the router.
+//
+// Follows the combine stage of "Scalable Training of Mixture-of-Experts Models
+// with Megatron Core" (es summary, Resumen técnico §2.1 step 4: results return
+// to their tokens and are weighted by the router). Every kernel here is
+// bandwidth-bound: one warp per token, 16-byte vector accesses, fp32
+// accumulation in a fixed order.
+#include "common.cuh"
+#include "internal.h"
+
+namespace moe {
+
+// Loads the k rows/weights of token t into lane-indexed registers and appends
+// the shared experts' rows (weight 1).
+__device__ __forceinline__ void token_rows(const int32_t* row_of, const float* w,
+                                           const int32_t* offsets, int t, int k, int E, int S,
+                                           int lane, int& row, float& wt) {
+  row = -1;
+  wt = 0.f;
+  if (lane < k) {
+    row = row_of[(size_t)t * k + lane];
+    wt = w ? w[(size_t)t * k + lane] : 1.f;
+  } else if (lane < k + S) {
+    row = offsets[E + lane - k] + t;
+    wt = 1.f;
+  }
+}
+
+// out[t] = bf16( sum_j w_tj y[row_tj] + sum_s y[shared row] )
+__global__ void __launch_bounds__(256)
+unpermute_kernel(const __nv_bfloat16* __restrict__ y, const int32_t* __restrict__ row_of,
+                 const float* __restrict__ w, const int32_t* __restrict__ offsets,
+                 __nv_bfloat16* __restrict__ out, int T, int H, int k, int E, int S) {
+  const int lane = threadIdx.x & 31;
+  const int nvec = H >> 3, nr = k + S;
+  const int warps = gridDim.x * (blockDim.x >> 5);
+  for (int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); t < T; t += warps) {
+    int myrow;
+    float mywt;
+    token_rows(row_of, w, offsets, t, k, E, S, lane, myrow, mywt);
+    int rows[kMaxK + 4];
+    float wts[kMaxK + 4];
+#pragma unroll
+    for (int j = 0; j < kMaxK + 4; ++j) {
+      rows[j] = __shfl_sync(0xffffffffu, myrow, j);
+      wts[j] = __shfl_sync(0xffffffffu, mywt, j);
+    }
+    for (int c = lane; c < nvec; c += 32) {
+      float acc[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) acc[i] = 0.f;
+#pragma unroll
+      for (int j = 0; j < kMaxK + 4; ++j) {
+        if (j >= nr || rows[j] < 0) continue;
+        float f[8];
+        unpack8(ldg_nc_v4(y + (size_t)rows[j] * H + (size_t)c * 8), f);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) acc[i] = fmaf(wts[j], f[i], acc[i]);
+      }
+      stg_v4(out + (size_t)t * H + (size_t)c * 8, pack8(acc));
+    }
+  }
+}
+
+__device__ __forceinline__ int find_pad_group(const int* prefix, int G, int p) {
+  int lo = 0, hi = G - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (prefix[mid] <= p) lo = mid;
+    else hi = mid - 1;
+  }
+  return lo;
+}
+
+// dO[row_tj] = bf16(w_tj dY[t]); dw_tj = <dY[t], y[row_tj]>; shared rows get dY;
+// virtual rows past T zero the padding rows of dO.
+__global__ void __launch_bounds__(256)
+unpermute_bwd_kernel(const __nv_bfloat16* __restrict__ dY, const __nv_bfloat16* __restrict__ y,
+                     const int32_t* __restrict__ row_of, const float* __restrict__ w,
+                     const int32_t* __restrict__ counts, const int32_t* __restrict__ offsets,
+                     __nv_bfloat16* __restrict__ dO, float* __restrict__ dw, int T, int H, int k,
+                     int E, int S) {
+  __shared__ int s_pp[kMaxGroups + 1];
+  __shared__ int s_off[kMaxGroups + 1];
+  __shared__ int s_cnt[kMaxGroups];
+  __shared__ int s_tmp[33];
+  const int G = E + S;
+  for (int g = threadIdx.x; g <= G; g += blockDim.x) s_off[g] = offsets[g];
+  for (int g = threadIdx.x; g < G; g += blockDim.x) s_cnt[g] = counts[g];
+  __syncthreads();
+  for (int g = threadIdx.x; g < G; g += blockDim.x) s_pp[g] = s_off[g + 1] - s_off[g] - s_cnt[g];
+  __syncthreads();
+  const int P = block_exclusive_scan(s_pp, G, s_tmp);
+  if (threadIdx.x == 0) s_pp[G] = P;
+  __syncthreads();
+  const int lane = threadIdx.x & 31;
+  const int nvec = H >> 3, nr = k + S;
+  const int warps = gridDim.x * (blockDim.x >> 5);
+  for (int v = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); v < T + P; v += warps) {
+    if (v >= T) {
+      const int p = v - T;
+      const int g = find_pad_group(s_pp, G, p);
+      const int r = s_off[g] + s_cnt[g] + (p - s_pp[g]);
+      const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+      for (int c = lane; c < nvec; c += 32) stg_v4(dO + (size_t)r * H + (size_t)c * 8, z);
+      continue;
+    }
+    const int t = v;
+    int myrow;
+    float mywt;
+    token_rows(row_of, w, offsets, t, k, E, S, lane, myrow, mywt);
+    int rows[kMaxK + 4];
+    float wts[kMaxK + 4];
+#pragma unroll
+    for (int j = 0; j < kMaxK + 4; ++j) {
+      rows[j] = __shfl_sync(0xffffffffu, myrow, j);
+      wts[j] = __shfl_sync(0xffffffffu, mywt, j);
+    }
+    float dot[kMaxK];
+#pragma unroll
+    for (int j = 0; j < kMaxK; ++j) dot[j] = 0.f;
+    for (int c = lane; c < nvec; c += 32) {
+      const uint4 gq = ldg_nc_v4(dY + (size_t)t * H + (size_t)c * 8);
+      float g[8];
+      unpack8(gq, g);
+#pragma unroll
+      for (int j = 0; j < kMaxK; ++j) {
+        if (j >= k || rows[j] < 0) continue;
+        float f[8], o[8];
+        unpack8(ldg_nc_v4(y + (size_t)rows[j] * H + (size_t)c * 8), f);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          dot[j] = fmaf(g[i], f[i], dot[j]);
+          o[i] = wts[j] * g[i];
+        }
+        stg_v4(dO + (size_t)rows[j] * H + (size_t)c * 8, pack8(o));
+      }
+#pragma unroll
+      for (int j = 0; j < kMaxK + 4; ++j) {
+        if (j < k || j >= nr) continue;
+        stg_v4(dO + (size_t)rows[j] * H + (size_t)c * 8, gq);
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < kMaxK; ++j) {
+      const float s = warp_sum(dot[j]);
+      if (lane == 0 && j < k) dw[(size_t)t * k + j] = (rows[j] >= 0) ? s : 0.f;
+    }
+  }
+}
+
+// dlogits[t,:] = 0 except the selected experts:
+//   softmax: dl_j = w_j (dw_j - sum_i w_i dw_i)
+//   sigmoid: ds_j = (r/S)(dw_j - sum_i (s_i/S) dw_i), dl_j = ds_j s_j (1 - s_j)
+__global__ void __launch_bounds__(256)
+route_bwd_kernel(const float* __restrict__ logits, const int32_t* __restrict__ idx,
+                 const float* __restrict__ w, const float* __restrict__ dw,
+                 float* __restrict__ dlogits, int T, int E, int k, int score_fn,
+                 float route_scale) {
+  const int lane = threadIdx.x & 31;
+  const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (t >= T) return;
+  float* row = dlogits + (size_t)t * E;
+  for (int e = lane; e < E; e += 32) row[e] = 0.f;
+  __syncwarp();
+  int e = 0;
+  double wj = 0.0, dwj = 0.0, sj = 0.0;
+  if (lane < k) {
+    e = idx[(size_t)t * k + lane];
+    wj = w[(size_t)t * k + lane];
+    dwj = dw[(size_t)t * k + lane];
+    if ((unsigned)e < (unsigned)E) sj = 1.0 / (1.0 + exp(-(double)logits[(size_t)t * E + e]));
+  }
+  double v;
+  if (score_fn == MOE_SCORE_SOFTMAX) {
+    double inner = wj * dwj;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) inner += __shfl_xor_sync(0xffffffffu, inner, o);
+    v = wj * (dwj - inner);
+  } else {
+    double ssum = sj, sdw = sj * dwj;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      ssum += __shfl_xor_sync(0xffffffffu, ssum, o);
+      sdw += __shfl_xor_sync(0xffffffffu, sdw, o);
+    }
+    const double ds = ((double)route_scale / ssum) * (dwj - sdw / ssum);
+    v = ds * sj * (1.0 - sj);
+  }
+  if (lane < k && (unsigned)e < (unsigned)E) row[e] = (float)v;
+}
+
+// dx[t] = bf16( sum_j dX[row_tj] + sum_s dX[shared row] + sum_j dl_tj W_r[e_tj] )
+__global__ void __launch_bounds__(256)
+permute_bwd_kernel(const __nv_bfloat16* __restrict__ dX, const int32_t* __restrict__ row_of,
+                   const int32_t* __restrict__ offsets, const int32_t* __restrict__ idx,
+                   const float* __restrict__ dlogits, const float* __restrict__ W_r,
+                   __nv_bfloat16* __restrict__ dx, int T, int H, int k, int E, int S) {
+  const int lane = threadIdx.x & 31;
+  const int nvec = H >> 3, nr = k + S;
+  const int warps = gridDim.x * (blockDim.x >> 5);
+  for (int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); t < T; t += warps) {
+    int myrow;
+    float unused;
+    token_rows(row_of, nullptr, offsets, t, k, E, S, lane, myrow, unused);
+    int mye = 0;
+    float mydl = 0.f;
+    if (lane < k) {
+      mye = idx[(size_t)t * k + lane];
+      mydl = ((unsigned)mye < (unsigned)E) ? dlogits[(size_t)t * E + mye] : 0.f;
+      if ((unsigned)mye >= (unsigned)E) mye = 0;
+    }
+    int rows[kMaxK + 4], es[kMaxK];
+    float dls[kMaxK];
+#pragma unroll
+    for (int j = 0; j < kMaxK + 4; ++j) rows[j] = __shfl_sync(0xffffffffu, myrow, j);
+#pragma unroll
+    for (int j = 0; j < kMaxK; ++j) {
+      es[j] = __shfl_sync(0xffffffffu, mye, j);
+      dls[j] = __shfl_sync(0xffffffffu, mydl, j);
+    }
+    for (int c = lane; c < nvec; c += 32) {
+      float acc[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) acc[i] = 0.f;
+#pragma unroll
+      for (int j = 0; j < kMaxK + 4; ++j) {
+        if (j >= nr || rows[j] < 0) continue;
+        float f[8];
+        unpack8(ldg_nc_v4(dX + (size_t)rows[j] * H + (size_t)c * 8), f);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) acc[i] += f[i];
+      }
+#pragma unroll
+      for (int j = 0; j < kMaxK; ++j) {
+        if (j >= k) continue;
+        const float d = dls[j];
+        const float4* wr = reinterpret_cast<const float4*>(W_r + (size_t)es[j] * H + (size_t)c * 8);
+        const float4 a = wr[0], b = wr[1];
+        acc[0] = fmaf(d, a.x, acc[0]);
+        acc[1] = fmaf(d, a.y, acc[1]);
+        acc[2] = fmaf(d, a.z, acc[2]);
+        acc[3] = fmaf(d, a.w, acc[3]);
+        acc[4] = fmaf(d, b.x, acc[4]);
+        acc[5] = fmaf(d, b.y, acc[5]);
+        acc[6] = fmaf(d, b.z, acc[6]);
+        acc[7] = fmaf(d, b.w, acc[7]);
+      }
+      stg_v4(dx + (size_t)t * H + (size_t)c * 8, pack8(acc));
+    }
+  }
+}
+
+// dW_r[e, cols] = sum over the tokens that selected e (in token order, split
+// across the block's 8 warps in a fixed interleave) of dlogits[t,e] x[t, cols].
+// Block (e, 256-column slab); lane owns 8 columns; warps combined in order.
+__global__ void __launch_bounds__(256)
+router_wgrad_kernel(const __nv_bfloat16* __restrict__ x, const int32_t* __restrict__ sel_offsets,
+                    const int32_t* __restrict__ sel_tokens, const float* __restrict__ dlogits,
+                    float* __restrict__ dW_r, int H, int E) {
+  __shared__ float part[8][256];
+  const int e = blockIdx.x;
+  const int col0 = blockIdx.y * 256;
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  const int c = col0 + lane * 8;
+  const bool on = c < H;
+  const int beg = sel_offsets[e], end = sel_offsets[e + 1];
+  float acc[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) acc[i] = 0.f;
+  int i = beg + wid;
+  for (; i + 24 < end; i += 32) {
+    int tt[4];
+    float d[4];
+    uint4 q[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) tt[u] = sel_tokens[i + 8 * u];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      d[u] = dlogits[(size_t)tt[u] * E + e];
+      if (on) q[u] = ldg_nc_v4(x + (size_t)tt[u] * H + c);
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      if (!on) continue;
+      float f[8];
+      unpack8(q[u], f);
+#pragma unroll
+      for (int m = 0; m < 8; ++m) acc[m] = fmaf(d[u], f[m], acc[m]);
+    }
+  }
+  for (; i < end; i += 8) {
+    const int t = sel_tokens[i];
+    const float d = dlogits[(size_t)t * E + e];
+    if (!on) continue;
+    float f[8];
+    unpack8(ldg_nc_v4(x + (size_t)t * H + c), f);
+#pragma unroll
+    for (int m = 0; m < 8; ++m) acc[m] = fmaf(d, f[m], acc[m]);
+  }
+#pragma unroll
+  for (int m = 0; m < 8; ++m) part[wid][lane * 8 + m] = acc[m];
+  __syncthreads();
+  const int col = col0 + threadIdx.x;
+  if (col < H) {
+    float s = 0.f;
+#pragma unroll
+    for (int q2 = 0; q2 < 8; ++q2) s += part[q2][threadIdx.x];
+    dW_r[(size_t)e * H + col] = s;
+  }
+}
+
+static int grid_for_warps(int n_items) {
+  const int blocks = (n_items + 7) / 8;
+  const int cap = num_sms() * 16;
+  return blocks < cap ? (blocks > 0 ? blocks : 1) : cap;
+}
+
+cudaError_t launch_unpermute(const moe_config& c, const void* y_perm, const int32_t* row_of,
+                             const float* w, const int32_t* offsets, void* out, cudaStream_t s) {
+  unpermute_kernel<<<grid_for_warps(c.T), 256, 0, s>>>(
+      static_cast<const __nv_bfloat16*>(y_perm), row_of, w, offsets,
+      static_cast<__nv_bfloat16*>(out), c.T, c.H, c.k, c.E, c.n_shared);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_unpermute_bwd(const moe_config& c, const void* dY, const void* y_perm,
+                                 const int32_t* row_of, const float* w, const int32_t* counts,
+                                 const int32_t* offsets, void* dO_perm, float* dw,
+                                 cudaStream_t s) {
+  unpermute_bwd_kernel<<<num_sms() * 8, 256, 0, s>>>(
+      static_cast<const __nv_bfloat16*>(dY), static_cast<const __nv_bfloat16*>(y_perm), row_of, w,
+      counts, offsets, static_cast<__nv_bfloat16*>(dO_perm), dw, c.T, c.H, c.k, c.E, c.n_shared);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_route_bwd(const moe_config& c, const float* logits, const int32_t* idx,
+                             const float* w, const float* dw, float* dlogits, cudaStream_t s) {
+  route_bwd_kernel<<<(c.T + 7) / 8, 256, 0, s>>>(logits, idx, w, dw, dlogits, c.T, c.E, c.k,
+                                                 c.score_fn, c.route_scale);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_permute_bwd(const moe_config& c, const void* dX_perm, const int32_t* row_of,
+                               const int32_t* offsets, const int32_t* idx, const float* dlogits,
+                               const float* W_r, void* dx, cudaStream_t s) {
+  permute_bwd_kernel<<<grid_for_warps(c.T), 256, 0, s>>>(
+      static_cast<const __nv_bfloat16*>(dX_perm), row_of, offsets, idx, dlogits, W_r,
+      static_cast<__nv_bfloat16*>(dx), c.T, c.H, c.k, c.E, c.n_shared);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_router_wgrad(const moe_config& c, const void* x, const int32_t* sel_offsets,
+                                const int32_t* sel_tokens, const float* dlogits, float* dW_r,
+                                cudaStream_t s) {
+  dim3 grid(c.E, (c.H + 255) / 256);
+  router_wgrad_kernel<<<grid, 256, 0, s>>>(static_cast<const __nv_bfloat16*>(x), sel_offsets,
+                                          sel_tokens, dlogits, dW_r, c.H, c.E);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -1,0 +1,583 @@
+// Stage 3 of the MoE layer, compute: the experts' SwiGLU FFNs as grouped GEMMs
+// on the fifth-generation tensor cores (tcgen05, accumulators in tensor
+// memory), operands staged by TMA, with the group shapes read on the device.
+//
+// Follows the compute stage of "Scalable Training of Mixture-of-Experts Models
+// with Megatron Core" (es summary, Resumen técnico §2.1 step 3 and §2.3.C:
+// many small expert GEMMs grouped into one kernel so the tensor cores stay
+// busy; kernels read token counts from GPU memory, no host synchronisation).
+// The backward keeps the page's W/D split (§2.3.B): data-gradient and
+// weight-gradient GEMMs are separate launches.
+//
+// One persistent kernel family, one CTA per SM, 192 threads:
+//   warp 0     TMA producer (one lane): A and B tiles into a STAGES-deep ring;
+//   warp 1     MMA issuer (one lane) and tensor-memory owner;
+//   warps 2-5  epilogue: tcgen05.ld of the 128 x BN fp32 accumulator, the
+//              fused element-wise work, bf16 stores.
+// Two accumulators live in tensor memory so the epilogue of one tile overlaps
+// the main loop of the next.
+//
+// Two problem shapes:
+//   row-grouped (forward and data gradients): group g owns rows
+//     offsets[g] .. offsets[g]+counts[g]-1 of A and of the output, B is the
+//     group's weight; tiles are 128 rows x BN columns inside the group;
+//   K-grouped (weight gradients): the group's rows are the reduction
+//     dimension; the output is the group's own [Mw x N] matrix.
+// Every group segment is a multiple of 128 rows whose padding rows are zero,
+// so no tile crosses into another group and no masking is needed.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include "common.cuh"
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace moe {
+namespace gg {
+
+constexpr int BM = 128;
+constexpr int BK = 64;                       // 64 bf16 = one 128-byte swizzle row
+constexpr int kThreads = 192;
+constexpr int kCtrlBytes = 5120;
+constexpr long long kWaitBudget = 4000000000LL;   // clock64 cycles (~2 s)
+
+enum Epi : int { kEpiSwigluFwd = 0, kEpiStore = 1, kEpiSwigluBwd = 2, kEpiWgrad = 3 };
+
+struct Params {
+  int kgrouped;               // 0: row-grouped, 1: K-grouped
+  int G;
+  int N;                      // output columns per group (unused by SwiGLU-fwd)
+  int K;                      // reduction length (row-grouped)
+  int Mw;                     // output rows per group (K-grouped)
+  int F;                      // SwiGLU width
+  int b_rows;                 // rows of one group in B's 2D view (row-grouped)
+  const int32_t* counts;
+  const int32_t* offsets;
+  __nv_bfloat16* out;
+  long long ldo;
+  long long out_gstride;      // K-grouped: elements between groups' outputs
+  __nv_bfloat16* out2;        // SwiGLU-fwd: h
+  long long ldo2;
+  const __nv_bfloat16* aux;   // SwiGLU-bwd: GU
+  long long ldaux;
+  int32_t* status;
+};
+
+template <int BN, int STAGES>
+struct Layout {
+  static constexpr int A_BYTES = BM * BK * 2;
+  static constexpr int B_BYTES = BN * BK * 2;
+  static constexpr int STAGE = A_BYTES + B_BYTES;
+  static constexpr int TILES = STAGES * STAGE;
+  static constexpr int SMEM = TILES + kCtrlBytes + 1024;
+  static constexpr int TMEM_COLS = 2 * BN;
+};
+
+struct Tile {
+  int g, mt, nt, nk;
+};
+
+__device__ __forceinline__ int find_group(const int* prefix, int G, int tile) {
+  int lo = 0, hi = G - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (prefix[mid] <= tile) lo = mid;
+    else hi = mid - 1;
+  }
+  return lo;
+}
+
+__device__ __forceinline__ Tile decode(int tile, const int* prefix, const int* mtiles,
+                                       const int* cnt, int G, int kgrouped, int K) {
+  Tile t;
+  t.g = find_group(prefix, G, tile);
+  const int local = tile - prefix[t.g];
+  const int mt = mtiles[t.g];
+  t.mt = local % mt;
+  t.nt = local / mt;
+  t.nk = kgrouped ? (cnt[t.g] + BK - 1) / BK : K / BK;
+  return t;
+}
+
+__device__ __forceinline__ float silu_f(float z) { return z / (1.f + expf(-z)); }
+
+template <int EPI, int BN, int A_MN, int B_MN, int STAGES>
+__global__ void __launch_bounds__(kThreads, 1)
+grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                    const Params p) {
+  using L = Layout<BN, STAGES>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = ptx::smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* ctrl = smem_raw + (base - raw) + L::TILES;
+  const uint32_t ctrl_u = base + L::TILES;
+  // control block: barriers, tensor-memory address, abort flag, tile tables
+  const uint32_t bar_full = ctrl_u;                       // [STAGES]
+  const uint32_t bar_empty = ctrl_u + 8 * STAGES;         // [STAGES]
+  const uint32_t bar_tfull = ctrl_u + 16 * STAGES;        // [2]
+  const uint32_t bar_tempty = ctrl_u + 16 * STAGES + 16;  // [2]
+  const uint32_t bar_drain = ctrl_u + 16 * STAGES + 32;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(ctrl + 192);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(ctrl + 196);
+  int* prefix = reinterpret_cast<int*>(ctrl + 256);       // [kMaxGroups+1]
+  int* mtiles = reinterpret_cast<int*>(ctrl + 1344);      // [kMaxGroups]
+  int* s_off = reinterpret_cast<int*>(ctrl + 2432);       // [kMaxGroups+1]
+  int* s_cnt = reinterpret_cast<int*>(ctrl + 3520);       // [kMaxGroups]
+  int* tmp = reinterpret_cast<int*>(ctrl + 4608);         // [33] scan scratch
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int G = p.G;
+  const int NT = (EPI == kEpiSwigluFwd) ? p.F / (BN / 2) : p.N / BN;
+  for (int g = tid; g < G; g += kThreads) {
+    const int c = p.counts[g];
+    s_cnt[g] = c;
+    s_off[g] = p.offsets[g];
+    const int mt = p.kgrouped ? p.Mw / BM : (c + BM - 1) / BM;
+    mtiles[g] = mt;
+    prefix[g] = mt * NT;
+  }
+  if (tid == 0) *abort_flag = 0;
+  __syncthreads();
+  const int total = block_exclusive_scan(prefix, G, tmp);
+  if (tid == 0) prefix[G] = total;
+  __syncthreads();
+  if ((int)blockIdx.x >= total) return;
+
+  if (tid == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      ptx::mbar_init(bar_full + 8 * s, 1);
+      ptx::mbar_init(bar_empty + 8 * s, 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      ptx::mbar_init(bar_tfull + 8 * a, 1);
+      ptx::mbar_init(bar_tempty + 8 * a, 128);
+    }
+    ptx::mbar_init(bar_drain, 1);
+    ptx::fence_mbar_init();
+  }
+  if (warp == 1) {
+    ptx::tmem_alloc(ptx::smem_u32(tmem_slot), L::TMEM_COLS);
+    ptx::tmem_relinquish();
+  }
+  if (tid == 32 * 0) {
+    ptx::tma_prefetch_desc(&tmA);
+    ptx::tma_prefetch_desc(&tmB);
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      uint32_t stage = 0, phase = 0;
+      uint32_t issued_mask = 0, issued_phase = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+        const Tile t = decode(tile, prefix, mtiles, s_cnt, G, p.kgrouped, p.K);
+        for (int kb = 0; kb < t.nk; ++kb) {
+          if (!ptx::mbar_wait(bar_empty + 8 * stage, phase ^ 1u, kWaitBudget, abort_flag)) {
+            ok = false;
+            break;
+          }
+          const uint32_t fb = bar_full + 8 * stage;
+          ptx::mbar_arrive_expect_tx(fb, L::STAGE);
+          const uint32_t sA = base + stage * L::STAGE;
+          const uint32_t sB = sA + L::A_BYTES;
+          const int k0 = kb * BK;
+          if (A_MN == 0) {
+            ptx::tma_load_2d(sA, &tmA, fb, k0, s_off[t.g] + t.mt * BM);
+          } else {
+            const int kr = s_off[t.g] + k0;
+            ptx::tma_load_2d(sA, &tmA, fb, t.mt * BM, kr);
+            ptx::tma_load_2d(sA + 8192, &tmA, fb, t.mt * BM + 64, kr);
+          }
+          if (EPI == kEpiSwigluFwd) {
+            const int f0 = t.nt * (BN / 2);
+            ptx::tma_load_2d(sB, &tmB, fb, k0, t.g * p.b_rows + f0);
+            ptx::tma_load_2d(sB + (BN / 2) * 128, &tmB, fb, k0, t.g * p.b_rows + p.F + f0);
+          } else if (B_MN == 0) {
+            ptx::tma_load_2d(sB, &tmB, fb, k0, t.g * p.b_rows + t.nt * BN);
+          } else {
+            const int kr = p.kgrouped ? s_off[t.g] + k0 : t.g * p.b_rows + k0;
+#pragma unroll
+            for (int j = 0; j < BN / 64; ++j)
+              ptx::tma_load_2d(sB + j * 8192, &tmB, fb, t.nt * BN + 64 * j, kr);
+          }
+          issued_mask |= 1u << stage;
+          issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      if (!ok) {
+        record_status(p.status, MOE_ERR_TIMEOUT);
+        *abort_flag = 1;
+      }
+      // every load issued must land before the CTA may exit
+      for (int s = 0; s < STAGES; ++s)
+        if (issued_mask & (1u << s))
+          ptx::mbar_wait(bar_full + 8 * s, (issued_phase >> s) & 1u, kWaitBudget, nullptr);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t IDESC = ptx::idesc_bf16(BM, BN, A_MN, B_MN);
+      uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
+      bool ok = true, issued = false;
+      for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+        const Tile t = decode(tile, prefix, mtiles, s_cnt, G, p.kgrouped, p.K);
+        if (!ptx::mbar_wait(bar_tempty + 8 * acc, acc_phase ^ 1u, kWaitBudget, abort_flag)) {
+          ok = false;
+          break;
+        }
+        ptx::tc_fence_after();
+        const uint32_t d = tmem_base + acc * BN;
+        for (int kb = 0; kb < t.nk; ++kb) {
+          if (!ptx::mbar_wait(bar_full + 8 * stage, phase, kWaitBudget, abort_flag)) {
+            ok = false;
+            break;
+          }
+          ptx::tc_fence_after();
+          const uint32_t sA = base + stage * L::STAGE;
+          const uint32_t sB = sA + L::A_BYTES;
+#pragma unroll
+          for (int kk = 0; kk < BK / 16; ++kk) {
+            const uint64_t ad = A_MN ? ptx::smem_desc_sw128(sA + kk * 2048, 8192, 1024)
+                                     : ptx::smem_desc_sw128(sA + kk * 32, 16, 1024);
+            const uint64_t bd = B_MN ? ptx::smem_desc_sw128(sB + kk * 2048, 8192, 1024)
+                                     : ptx::smem_desc_sw128(sB + kk * 32, 16, 1024);
+            ptx::mma_bf16(d, ad, bd, IDESC, (kb | kk) ? 1u : 0u);
+          }
+          issued = true;
+          ptx::mma_commit(bar_empty + 8 * stage);
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        if (t.nk > 0) ptx::mma_commit(bar_tfull + 8 * acc);
+        else ptx::mbar_arrive(bar_tfull + 8 * acc);   // empty group: nothing to wait for
+        if (++acc == 2) {
+          acc = 0;
+          acc_phase ^= 1u;
+        }
+      }
+      if (!ok) {
+        record_status(p.status, MOE_ERR_TIMEOUT);
+        *abort_flag = 1;
+      }
+      // wait for every MMA issued by this thread before tensor memory is freed
+      if (issued) {
+        ptx::mma_commit(bar_drain);
+        ptx::mbar_wait(bar_drain, 0, kWaitBudget, nullptr);
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int q = warp & 3;                        // tensor-memory lane quarter
+    const int rloc = q * 32 + lane;                // accumulator row of this thread
+    uint32_t acc = 0, acc_phase = 0;
+    for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
+      const Tile t = decode(tile, prefix, mtiles, s_cnt, G, p.kgrouped, p.K);
+      bool ok = ptx::mbar_wait(bar_tfull + 8 * acc, acc_phase, kWaitBudget, abort_flag);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) {
+        if (lane == 0) {
+          record_status(p.status, MOE_ERR_TIMEOUT);
+          *abort_flag = 1;
+        }
+        break;
+      }
+      ptx::tc_fence_after();
+      const uint32_t tbase = tmem_base + acc * BN + ((uint32_t)(q * 32) << 16);
+      if (EPI == kEpiSwigluFwd) {
+        const long long row = s_off[t.g] + t.mt * BM + rloc;
+        const int f0 = t.nt * (BN / 2);
+        __nv_bfloat16* gu = p.out + row * p.ldo;
+        __nv_bfloat16* hr = p.out2 + row * p.ldo2;
+#pragma unroll 1
+        for (int c = 0; c < BN / 2; c += 32) {
+          uint32_t rg[32], ru[32];
+          ptx::tmem_ld32(tbase + c, rg);
+          ptx::tmem_ld32(tbase + BN / 2 + c, ru);
+          ptx::tmem_ld_wait();
+#pragma unroll
+          for (int v = 0; v < 4; ++v) {
+            float gf[8], uf[8], hf[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              gf[i] = __uint_as_float(rg[v * 8 + i]);
+              uf[i] = __uint_as_float(ru[v * 8 + i]);
+            }
+            const uint4 gb = pack8(gf), ub = pack8(uf);
+            float gr[8], ur[8];
+            unpack8(gb, gr);
+            unpack8(ub, ur);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) hf[i] = silu_f(gr[i]) * ur[i];
+            stg_v4(gu + f0 + c + v * 8, gb);
+            stg_v4(gu + p.F + f0 + c + v * 8, ub);
+            stg_v4(hr + f0 + c + v * 8, pack8(hf));
+          }
+        }
+      } else if (EPI == kEpiStore) {
+        const long long row = s_off[t.g] + t.mt * BM + rloc;
+        __nv_bfloat16* o = p.out + row * p.ldo + t.nt * BN;
+#pragma unroll 1
+        for (int c = 0; c < BN; c += 32) {
+          uint32_t r[32];
+          ptx::tmem_ld32(tbase + c, r);
+          ptx::tmem_ld_wait();
+#pragma unroll
+          for (int v = 0; v < 4; ++v) {
+            float f[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) f[i] = __uint_as_float(r[v * 8 + i]);
+            stg_v4(o + c + v * 8, pack8(f));
+          }
+        }
+      } else if (EPI == kEpiSwigluBwd) {
+        const long long row = s_off[t.g] + t.mt * BM + rloc;
+        const int f0 = t.nt * BN;
+        const __nv_bfloat16* gu = p.aux + row * p.ldaux;
+        __nv_bfloat16* o = p.out + row * p.ldo;
+#pragma unroll 1
+        for (int c = 0; c < BN; c += 32) {
+          uint32_t r[32];
+          ptx::tmem_ld32(tbase + c, r);
+          ptx::tmem_ld_wait();
+#pragma unroll
+          for (int v = 0; v < 4; ++v) {
+            float gf[8], uf[8], dg[8], du[8];
+            unpack8(ldg_v4(gu + f0 + c + v * 8), gf);
+            unpack8(ldg_v4(gu + p.F + f0 + c + v * 8), uf);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              const float dh = __uint_as_float(r[v * 8 + i]);
+              const float sg = 1.f / (1.f + expf(-gf[i]));
+              dg[i] = dh * uf[i] * sg * (1.f + gf[i] * (1.f - sg));
+              du[i] = dh * gf[i] * sg;
+            }
+            stg_v4(o + f0 + c + v * 8, pack8(dg));
+            stg_v4(o + p.F + f0 + c + v * 8, pack8(du));
+          }
+        }
+      } else {  // kEpiWgrad
+        __nv_bfloat16* o = p.out + (long long)t.g * p.out_gstride +
+                           (long long)(t.mt * BM + rloc) * p.ldo + t.nt * BN;
+#pragma unroll 1
+        for (int c = 0; c < BN; c += 32) {
+          uint32_t r[32];
+          if (t.nk > 0) {
+            ptx::tmem_ld32(tbase + c, r);
+            ptx::tmem_ld_wait();
+          } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) r[i] = 0u;
+          }
+#pragma unroll
+          for (int v = 0; v < 4; ++v) {
+            float f[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) f[i] = __uint_as_float(r[v * 8 + i]);
+            stg_v4(o + c + v * 8, pack8(f));
+          }
+        }
+      }
+      ptx::tc_fence_before();
+      ptx::mbar_arrive(bar_tempty + 8 * acc);
+      if (++acc == 2) {
+        acc = 0;
+        acc_phase ^= 1u;
+      }
+    }
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem_base, L::TMEM_COLS);
+  }
+}
+
+// ----------------------------------------------------------------- host side
+static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  }
+  return fn;
+}
+
+// 2D bf16 view [outer rows, inner columns] with a {64, box_outer} box and
+// 128-byte swizzle; elements outside the view read as zero.
+static bool make_map(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t outer,
+                     uint32_t box_outer) {
+  PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {inner * 2};
+  cuuint32_t box[2] = {64, box_outer};
+  cuuint32_t es[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box,
+            es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int EPI, int BN, int A_MN, int B_MN, int STAGES>
+static cudaError_t run(const CUtensorMap& a, const CUtensorMap& b, const Params& p,
+                       cudaStream_t s) {
+  using L = Layout<BN, STAGES>;
+  auto kern = grouped_gemm_kernel<EPI, BN, A_MN, B_MN, STAGES>;
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::SMEM);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  kern<<<num_sms(), kThreads, L::SMEM, s>>>(a, b, p);
+  return cudaGetLastError();
+}
+
+static Params base_params(const moe_config& c, const int32_t* counts, const int32_t* offsets,
+                          int32_t* status) {
+  Params p{};
+  p.G = c.E + c.n_shared;
+  p.F = c.F;
+  p.counts = counts;
+  p.offsets = offsets;
+  p.status = status;
+  return p;
+}
+
+}  // namespace gg
+
+using namespace gg;
+
+cudaError_t launch_ffn_fc1(const moe_config& c, const void* x_perm, const int32_t* counts,
+                           const int32_t* offsets, const void* W13, void* GU, void* h,
+                           int32_t* status, cudaStream_t s) {
+  const int64_t R = rows_max(c);
+  const int G = c.E + c.n_shared;
+  CUtensorMap a, b;
+  if (!make_map(&a, x_perm, c.H, R, 128) || !make_map(&b, W13, c.H, (uint64_t)G * 2 * c.F, 128))
+    return cudaErrorInvalidValue;
+  Params p = base_params(c, counts, offsets, status);
+  p.K = c.H;
+  p.b_rows = 2 * c.F;
+  p.out = static_cast<__nv_bfloat16*>(GU);
+  p.ldo = 2LL * c.F;
+  p.out2 = static_cast<__nv_bfloat16*>(h);
+  p.ldo2 = c.F;
+  return run<kEpiSwigluFwd, 256, 0, 0, 4>(a, b, p, s);
+}
+
+cudaError_t launch_ffn_fc2(const moe_config& c, const void* h, const int32_t* counts,
+                           const int32_t* offsets, const void* W2, void* y_perm,
+                           int32_t* status, cudaStream_t s) {
+  const int64_t R = rows_max(c);
+  const int G = c.E + c.n_shared;
+  const int bn = (c.H % 256 == 0) ? 256 : 128;
+  CUtensorMap a, b;
+  if (!make_map(&a, h, c.F, R, 128) || !make_map(&b, W2, c.F, (uint64_t)G * c.H, bn))
+    return cudaErrorInvalidValue;
+  Params p = base_params(c, counts, offsets, status);
+  p.N = c.H;
+  p.K = c.F;
+  p.b_rows = c.H;
+  p.out = static_cast<__nv_bfloat16*>(y_perm);
+  p.ldo = c.H;
+  return bn == 256 ? run<kEpiStore, 256, 0, 0, 4>(a, b, p, s)
+                   : run<kEpiStore, 128, 0, 0, 6>(a, b, p, s);
+}
+
+cudaError_t launch_ffn_fc2_dgrad(const moe_config& c, const void* dO_perm, const int32_t* counts,
+                                 const int32_t* offsets, const void* W2, const void* GU,
+                                 void* dGU, int32_t* status, cudaStream_t s) {
+  const int64_t R = rows_max(c);
+  const int G = c.E + c.n_shared;
+  const int bn = (c.F % 256 == 0) ? 256 : 128;
+  CUtensorMap a, b;
+  if (!make_map(&a, dO_perm, c.H, R, 128) || !make_map(&b, W2, c.F, (uint64_t)G * c.H, 64))
+    return cudaErrorInvalidValue;
+  Params p = base_params(c, counts, offsets, status);
+  p.N = c.F;
+  p.K = c.H;
+  p.b_rows = c.H;
+  p.out = static_cast<__nv_bfloat16*>(dGU);
+  p.ldo = 2LL * c.F;
+  p.aux = static_cast<const __nv_bfloat16*>(GU);
+  p.ldaux = 2LL * c.F;
+  return bn == 256 ? run<kEpiSwigluBwd, 256, 0, 1, 4>(a, b, p, s)
+                   : run<kEpiSwigluBwd, 128, 0, 1, 6>(a, b, p, s);
+}
+
+cudaError_t launch_ffn_fc1_dgrad(const moe_config& c, const void* dGU, const int32_t* counts,
+                                 const int32_t* offsets, const void* W13, void* dX_perm,
+                                 int32_t* status, cudaStream_t s) {
+  const int64_t R = rows_max(c);
+  const int G = c.E + c.n_shared;
+  const int bn = (c.H % 256 == 0) ? 256 : 128;
+  CUtensorMap a, b;
+  if (!make_map(&a, dGU, 2ULL * c.F, R, 128) ||
+      !make_map(&b, W13, c.H, (uint64_t)G * 2 * c.F, 64))
+    return cudaErrorInvalidValue;
+  Params p = base_params(c, counts, offsets, status);
+  p.N = c.H;
+  p.K = 2 * c.F;
+  p.b_rows = 2 * c.F;
+  p.out = static_cast<__nv_bfloat16*>(dX_perm);
+  p.ldo = c.H;
+  return bn == 256 ? run<kEpiStore, 256, 0, 1, 4>(a, b, p, s)
+                   : run<kEpiStore, 128, 0, 1, 6>(a, b, p, s);
+}
+
+cudaError_t launch_ffn_wgrad_fc2(const moe_config& c, const void* dO_perm, const void* h,
+                                 const int32_t* counts, const int32_t* offsets, void* dW2,
+                                 int32_t* status, cudaStream_t s) {
+  const int64_t R = rows_max(c);
+  const int bn = (c.F % 256 == 0) ? 256 : 128;
+  CUtensorMap a, b;
+  if (!make_map(&a, dO_perm, c.H, R, 64) || !make_map(&b, h, c.F, R, 64))
+    return cudaErrorInvalidValue;
+  Params p = base_params(c, counts, offsets, status);
+  p.kgrouped = 1;
+  p.Mw = c.H;
+  p.N = c.F;
+  p.out = static_cast<__nv_bfloat16*>(dW2);
+  p.ldo = c.F;
+  p.out_gstride = (long long)c.H * c.F;
+  return bn == 256 ? run<kEpiWgrad, 256, 1, 1, 4>(a, b, p, s)
+                   : run<kEpiWgrad, 128, 1, 1, 6>(a, b, p, s);
+}
+
+cudaError_t launch_ffn_wgrad_fc1(const moe_config& c, const void* dGU, const void* x_perm,
+                                 const int32_t* counts, const int32_t* offsets, void* dW13,
+                                 int32_t* status, cudaStream_t s) {
+  const int64_t R = rows_max(c);
+  const int bn = (c.H % 256 == 0) ? 256 : 128;
+  CUtensorMap a, b;
+  if (!make_map(&a, dGU, 2ULL * c.F, R, 64) || !make_map(&b, x_perm, c.H, R, 64))
+    return cudaErrorInvalidValue;
+  Params p = base_params(c, counts, offsets, status);
+  p.kgrouped = 1;
+  p.Mw = 2 * c.F;
+  p.N = c.H;
+  p.out = static_cast<__nv_bfloat16*>(dW13);
+  p.ldo = c.H;
+  p.out_gstride = 2LL * c.F * c.H;
+  return bn == 256 ? run<kEpiWgrad, 256, 1, 1, 4>(a, b, p, s)
+                   : run<kEpiWgrad, 128, 1, 1, 6>(a, b, p, s);
+}
+
+}  // namespace moe

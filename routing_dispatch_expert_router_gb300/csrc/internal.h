@@ -1,0 +1,63 @@
+// Host-side launchers shared between the translation units of the library.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/moe_abi.h"
+
+namespace moe {
+
+int64_t capacity_rows(const moe_config& c);
+int64_t rows_max(const moe_config& c);
+int n_chunks(const moe_config& c);
+int num_sms();
+
+cudaError_t launch_route(const moe_config& c, const void* x, const float* W_r, const float* bias,
+                         float* logits, int32_t* idx, float* w, cudaStream_t s);
+
+cudaError_t launch_permute(const moe_config& c, const void* x, const int32_t* idx,
+                           int32_t* counts, int32_t* offsets, int32_t* row_of, int32_t* token_of,
+                           int32_t* sel_offsets, int32_t* sel_tokens, void* x_perm,
+                           uint8_t* scratch, cudaStream_t s);
+
+cudaError_t launch_unpermute(const moe_config& c, const void* y_perm, const int32_t* row_of,
+                             const float* w, const int32_t* offsets, void* out, cudaStream_t s);
+
+cudaError_t launch_unpermute_bwd(const moe_config& c, const void* dY, const void* y_perm,
+                                 const int32_t* row_of, const float* w, const int32_t* counts,
+                                 const int32_t* offsets, void* dO_perm, float* dw, cudaStream_t s);
+
+cudaError_t launch_route_bwd(const moe_config& c, const float* logits, const int32_t* idx,
+                             const float* w, const float* dw, float* dlogits, cudaStream_t s);
+
+cudaError_t launch_permute_bwd(const moe_config& c, const void* dX_perm, const int32_t* row_of,
+                               const int32_t* offsets, const int32_t* idx, const float* dlogits,
+                               const float* W_r, void* dx, cudaStream_t s);
+
+cudaError_t launch_router_wgrad(const moe_config& c, const void* x, const int32_t* sel_offsets,
+                                const int32_t* sel_tokens, const float* dlogits, float* dW_r,
+                                cudaStream_t s);
+
+// Grouped GEMMs (tcgen05). Return cudaErrorInvalidValue when a tensor map
+// cannot be encoded for the given pointers.
+cudaError_t launch_ffn_fc1(const moe_config& c, const void* x_perm, const int32_t* counts,
+                           const int32_t* offsets, const void* W13, void* GU, void* h,
+                           int32_t* status, cudaStream_t s);
+cudaError_t launch_ffn_fc2(const moe_config& c, const void* h, const int32_t* counts,
+                           const int32_t* offsets, const void* W2, void* y_perm,
+                           int32_t* status, cudaStream_t s);
+cudaError_t launch_ffn_fc2_dgrad(const moe_config& c, const void* dO_perm, const int32_t* counts,
+                                 const int32_t* offsets, const void* W2, const void* GU,
+                                 void* dGU, int32_t* status, cudaStream_t s);
+cudaError_t launch_ffn_fc1_dgrad(const moe_config& c, const void* dGU, const int32_t* counts,
+                                 const int32_t* offsets, const void* W13, void* dX_perm,
+                                 int32_t* status, cudaStream_t s);
+cudaError_t launch_ffn_wgrad_fc2(const moe_config& c, const void* dO_perm, const void* h,
+                                 const int32_t* counts, const int32_t* offsets, void* dW2,
+                                 int32_t* status, cudaStream_t s);
+cudaError_t launch_ffn_wgrad_fc1(const moe_config& c, const void* dGU, const void* x_perm,
+                                 const int32_t* counts, const int32_t* offsets, void* dW13,
+                                 int32_t* status, cudaStream_t s);
+
+}  // namespace moe

@@ -1,0 +1,280 @@
+// The library's C entry points: argument checks, buffer sizes, and the layer
+// composition. Every compute step runs in this library's own kernels; nothing
+// here falls back to another implementation.
+#include <math.h>
+#include <stdio.h>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace moe {
+
+int64_t capacity_rows(const moe_config& c) {
+  if (!(c.capacity_factor > 0.f)) return 0;
+  const double cf = (double)c.capacity_factor;
+  const int64_t cap = (int64_t)ceil(cf * (double)c.T * (double)c.k / (double)c.E);
+  return (cap + c.row_align - 1) / c.row_align * c.row_align;
+}
+
+int64_t rows_max(const moe_config& c) {
+  const int64_t a = c.row_align;
+  const int64_t shared = (int64_t)c.n_shared * (((int64_t)c.T + a - 1) / a * a);
+  const int64_t C = capacity_rows(c);
+  if (C > 0) return (int64_t)c.E * C + shared;
+  return (int64_t)c.T * c.k + (int64_t)c.E * (a - 1) + shared;
+}
+
+int n_chunks(const moe_config& c) { return (c.T + kChunkTokens - 1) / kChunkTokens; }
+
+int num_sms() {
+  static int cache[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+  if (cache[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+      n = 148;
+    cache[dev] = n;
+  }
+  return cache[dev];
+}
+
+static int64_t scratch_bytes(const moe_config& c) {
+  return (int64_t)kScratchHist + (int64_t)n_chunks(c) * c.E * 4 + 256;
+}
+
+static moe_status check_config(const moe_config* c) {
+  if (!c) return MOE_ERR_INVALID_ARG;
+  if (c->T < 0 || c->H < 128 || c->F < 128 || c->E < 1 || c->k < 1) return MOE_ERR_INVALID_ARG;
+  if (c->H % 128 || c->F % 128) return MOE_ERR_INVALID_ARG;
+  if (c->E > kMaxExperts || c->k > kMaxK || c->k > c->E) return MOE_ERR_INVALID_ARG;
+  if (c->n_shared < 0 || c->n_shared > 4) return MOE_ERR_INVALID_ARG;
+  if (c->score_fn != MOE_SCORE_SOFTMAX && c->score_fn != MOE_SCORE_SIGMOID)
+    return MOE_ERR_INVALID_ARG;
+  if (c->n_groups < 1 || c->n_groups > 32 || c->E % c->n_groups) return MOE_ERR_INVALID_ARG;
+  if (c->topk_groups < 1 || c->topk_groups > c->n_groups) return MOE_ERR_INVALID_ARG;
+  if (c->n_groups > 1 && c->topk_groups * (c->E / c->n_groups) < c->k) return MOE_ERR_INVALID_ARG;
+  if (c->group_score != MOE_GROUP_TOP2_SUM && c->group_score != MOE_GROUP_MAX)
+    return MOE_ERR_INVALID_ARG;
+  if (!(c->capacity_factor >= 0.f) || !isfinite(c->capacity_factor)) return MOE_ERR_INVALID_ARG;
+  if (!isfinite(c->route_scale)) return MOE_ERR_INVALID_ARG;
+  if (c->row_align < 128 || c->row_align % 128) return MOE_ERR_INVALID_ARG;
+  if (c->dtype != MOE_DTYPE_BF16) return MOE_ERR_UNSUPPORTED;
+  if ((int64_t)c->T * c->k >= (1LL << 31) || rows_max(*c) >= (1LL << 31))
+    return MOE_ERR_INVALID_ARG;
+  if ((int64_t)c->E * 2 * c->F >= (1LL << 31) || (int64_t)(c->E + c->n_shared) * c->H >= (1LL << 31))
+    return MOE_ERR_INVALID_ARG;
+  return MOE_OK;
+}
+
+static bool al16(const void* p) { return p && ((uintptr_t)p & 15u) == 0; }
+static bool al4(const void* p) { return p && ((uintptr_t)p & 3u) == 0; }
+
+static moe_status cuda_status(cudaError_t e) {
+  if (e == cudaSuccess) return MOE_OK;
+  if (e == cudaErrorInvalidValue) return MOE_ERR_INVALID_ARG;
+  return MOE_ERR_CUDA;
+}
+
+static int32_t* status_word(void* scratch) {
+  return reinterpret_cast<int32_t*>(static_cast<uint8_t*>(scratch) + kScratchStatus);
+}
+
+}  // namespace moe
+
+using namespace moe;
+
+#define MOE_TRY(expr)                    \
+  do {                                   \
+    moe_status _s = (expr);              \
+    if (_s != MOE_OK) return _s;         \
+  } while (0)
+
+#define MOE_CUDA(expr)                   \
+  do {                                   \
+    cudaError_t _e = (expr);             \
+    if (_e != cudaSuccess) return cuda_status(_e); \
+  } while (0)
+
+#define MOE_REQUIRE(cond)                \
+  do {                                   \
+    if (!(cond)) return MOE_ERR_INVALID_ARG; \
+  } while (0)
+
+extern "C" {
+
+moe_status moe_query_sizes(const moe_config* cfg, moe_sizes* out) {
+  MOE_TRY(check_config(cfg));
+  MOE_REQUIRE(out);
+  out->rows_max = rows_max(*cfg);
+  out->groups = cfg->E + cfg->n_shared;
+  out->capacity = capacity_rows(*cfg);
+  out->scratch_bytes = scratch_bytes(*cfg);
+  return MOE_OK;
+}
+
+moe_status moe_route(const moe_config* cfg, const void* x, const float* W_r, const float* bias,
+                     float* logits, int32_t* idx, float* w, void* scratch, void* stream) {
+  MOE_TRY(check_config(cfg));
+  MOE_REQUIRE(al16(x) && al16(W_r) && al4(logits) && al4(idx) && al4(w));
+  MOE_REQUIRE(bias == nullptr || al4(bias));
+  (void)scratch;
+  if (cfg->T == 0) return MOE_OK;
+  MOE_CUDA(launch_route(*cfg, x, W_r, bias, logits, idx, w, (cudaStream_t)stream));
+  return MOE_OK;
+}
+
+moe_status moe_permute(const moe_config* cfg, const void* x, const int32_t* idx, int32_t* counts,
+                       int32_t* offsets, int32_t* row_of, int32_t* token_of, int32_t* sel_offsets,
+                       int32_t* sel_tokens, void* x_perm, void* scratch, void* stream) {
+  MOE_TRY(check_config(cfg));
+  MOE_REQUIRE(al16(x) && al4(idx) && al4(counts) && al4(offsets) && al4(row_of));
+  MOE_REQUIRE(al4(token_of) && al4(sel_offsets) && al4(sel_tokens) && al16(x_perm));
+  MOE_REQUIRE(al16(scratch));
+  MOE_CUDA(launch_permute(*cfg, x, idx, counts, offsets, row_of, token_of, sel_offsets,
+                          sel_tokens, x_perm, static_cast<uint8_t*>(scratch),
+                          (cudaStream_t)stream));
+  return MOE_OK;
+}
+
+moe_status moe_grouped_ffn_fwd(const moe_config* cfg, const void* x_perm, const int32_t* counts,
+                               const int32_t* offsets, const void* W13, const void* W2, void* GU,
+                               void* h, void* y_perm, void* scratch, void* stream) {
+  MOE_TRY(check_config(cfg));
+  MOE_REQUIRE(al16(x_perm) && al4(counts) && al4(offsets) && al16(W13) && al16(W2));
+  MOE_REQUIRE(al16(GU) && al16(h) && al16(y_perm) && al16(scratch));
+  cudaStream_t s = (cudaStream_t)stream;
+  int32_t* st = status_word(scratch);
+  MOE_CUDA(launch_ffn_fc1(*cfg, x_perm, counts, offsets, W13, GU, h, st, s));
+  MOE_CUDA(launch_ffn_fc2(*cfg, h, counts, offsets, W2, y_perm, st, s));
+  return MOE_OK;
+}
+
+moe_status moe_unpermute(const moe_config* cfg, const void* y_perm, const int32_t* row_of,
+                         const float* w, const int32_t* offsets, void* out, void* stream) {
+  MOE_TRY(check_config(cfg));
+  MOE_REQUIRE(al16(y_perm) && al4(row_of) && al4(w) && al4(offsets) && al16(out));
+  MOE_CUDA(launch_unpermute(*cfg, y_perm, row_of, w, offsets, out, (cudaStream_t)stream));
+  return MOE_OK;
+}
+
+moe_status moe_unpermute_bwd(const moe_config* cfg, const void* dY, const void* y_perm,
+                             const int32_t* row_of, const float* w, const int32_t* counts,
+                             const int32_t* offsets, void* dO_perm, float* dw, void* stream) {
+  MOE_TRY(check_config(cfg));
+  MOE_REQUIRE(al16(dY) && al16(y_perm) && al4(row_of) && al4(w) && al4(counts));
+  MOE_REQUIRE(al4(offsets) && al16(dO_perm) && al4(dw));
+  MOE_CUDA(launch_unpermute_bwd(*cfg, dY, y_perm, row_of, w, counts, offsets, dO_perm, dw,
+                                (cudaStream_t)stream));
+  return MOE_OK;
+}
+
+moe_status moe_grouped_ffn_bwd(const moe_config* cfg, const void* dO_perm, const void* x_perm,
+                               const void* GU, const void* h, const int32_t* counts,
+                               const int32_t* offsets, const void* W13, const void* W2,
+                               void* dGU, void* dX_perm, void* dW13, void* dW2, void* scratch,
+                               void* stream) {
+  MOE_TRY(check_config(cfg));
+  MOE_REQUIRE(al16(dO_perm) && al16(x_perm) && al16(GU) && al16(h) && al4(counts));
+  MOE_REQUIRE(al4(offsets) && al16(W13) && al16(W2) && al16(dGU) && al16(dX_perm));
+  MOE_REQUIRE(al16(dW13) && al16(dW2) && al16(scratch));
+  cudaStream_t s = (cudaStream_t)stream;
+  int32_t* st = status_word(scratch);
+  MOE_CUDA(launch_ffn_fc2_dgrad(*cfg, dO_perm, counts, offsets, W2, GU, dGU, st, s));
+  MOE_CUDA(launch_ffn_wgrad_fc2(*cfg, dO_perm, h, counts, offsets, dW2, st, s));
+  MOE_CUDA(launch_ffn_fc1_dgrad(*cfg, dGU, counts, offsets, W13, dX_perm, st, s));
+  MOE_CUDA(launch_ffn_wgrad_fc1(*cfg, dGU, x_perm, counts, offsets, dW13, st, s));
+  return MOE_OK;
+}
+
+moe_status moe_route_bwd(const moe_config* cfg, const float* logits, const int32_t* idx,
+                         const float* w, const float* dw, float* dlogits, void* stream) {
+  MOE_TRY(check_config(cfg));
+  MOE_REQUIRE(al4(logits) && al4(idx) && al4(w) && al4(dw) && al4(dlogits));
+  if (cfg->T == 0) return MOE_OK;
+  MOE_CUDA(launch_route_bwd(*cfg, logits, idx, w, dw, dlogits, (cudaStream_t)stream));
+  return MOE_OK;
+}
+
+moe_status moe_permute_bwd(const moe_config* cfg, const void* dX_perm, const int32_t* row_of,
+                           const int32_t* offsets, const int32_t* idx, const float* dlogits,
+                           const float* W_r, void* dx, void* stream) {
+  MOE_TRY(check_config(cfg));
+  MOE_REQUIRE(al16(dX_perm) && al4(row_of) && al4(offsets) && al4(idx) && al4(dlogits));
+  MOE_REQUIRE(al16(W_r) && al16(dx));
+  MOE_CUDA(launch_permute_bwd(*cfg, dX_perm, row_of, offsets, idx, dlogits, W_r, dx,
+                              (cudaStream_t)stream));
+  return MOE_OK;
+}
+
+moe_status moe_router_wgrad(const moe_config* cfg, const void* x, const int32_t* sel_offsets,
+                            const int32_t* sel_tokens, const float* dlogits, float* dW_r,
+                            void* stream) {
+  MOE_TRY(check_config(cfg));
+  MOE_REQUIRE(al16(x) && al4(sel_offsets) && al4(sel_tokens) && al4(dlogits) && al4(dW_r));
+  MOE_CUDA(launch_router_wgrad(*cfg, x, sel_offsets, sel_tokens, dlogits, dW_r,
+                               (cudaStream_t)stream));
+  return MOE_OK;
+}
+
+moe_status moe_layer_fwd(const moe_config* cfg, const moe_params* P, const void* x, void* out,
+                         const moe_fwd_state* st, void* scratch, void* stream) {
+  MOE_TRY(check_config(cfg));
+  MOE_REQUIRE(P && st);
+  MOE_TRY(moe_route(cfg, x, P->W_r, P->bias, st->logits, st->idx, st->w, scratch, stream));
+  MOE_TRY(moe_permute(cfg, x, st->idx, st->counts, st->offsets, st->row_of, st->token_of,
+                      st->sel_offsets, st->sel_tokens, st->x_perm, scratch, stream));
+  MOE_TRY(moe_grouped_ffn_fwd(cfg, st->x_perm, st->counts, st->offsets, P->W13, P->W2, st->GU,
+                              st->h, st->y_perm, scratch, stream));
+  MOE_TRY(moe_unpermute(cfg, st->y_perm, st->row_of, st->w, st->offsets, out, stream));
+  return MOE_OK;
+}
+
+moe_status moe_layer_bwd(const moe_config* cfg, const moe_params* P, const void* x,
+                         const void* dY, const moe_fwd_state* st, const moe_bwd_state* bs,
+                         void* dx, float* dW_r, void* dW13, void* dW2, void* scratch,
+                         void* stream) {
+  MOE_TRY(check_config(cfg));
+  MOE_REQUIRE(P && st && bs);
+  MOE_TRY(moe_unpermute_bwd(cfg, dY, st->y_perm, st->row_of, st->w, st->counts, st->offsets,
+                            bs->dO_perm, bs->dw, stream));
+  MOE_TRY(moe_route_bwd(cfg, st->logits, st->idx, st->w, bs->dw, bs->dlogits, stream));
+  MOE_TRY(moe_grouped_ffn_bwd(cfg, bs->dO_perm, st->x_perm, st->GU, st->h, st->counts,
+                              st->offsets, P->W13, P->W2, bs->dGU, bs->dX_perm, dW13, dW2,
+                              scratch, stream));
+  MOE_TRY(moe_permute_bwd(cfg, bs->dX_perm, st->row_of, st->offsets, st->idx, bs->dlogits,
+                          P->W_r, dx, stream));
+  MOE_TRY(moe_router_wgrad(cfg, x, st->sel_offsets, st->sel_tokens, bs->dlogits, dW_r, stream));
+  return MOE_OK;
+}
+
+moe_status moe_last_device_status(const void* scratch, int32_t* code, void* stream) {
+  MOE_REQUIRE(al16(scratch) && code);
+  cudaStream_t s = (cudaStream_t)stream;
+  MOE_CUDA(cudaStreamSynchronize(s));
+  MOE_CUDA(cudaMemcpy(code, static_cast<const uint8_t*>(scratch) + kScratchStatus,
+                      sizeof(int32_t), cudaMemcpyDeviceToHost));
+  return MOE_OK;
+}
+
+moe_status moe_clear_device_status(void* scratch, void* stream) {
+  MOE_REQUIRE(al16(scratch));
+  MOE_CUDA(cudaMemsetAsync(static_cast<uint8_t*>(scratch) + kScratchStatus, 0, sizeof(int32_t),
+                           (cudaStream_t)stream));
+  return MOE_OK;
+}
+
+const char* moe_status_string(moe_status s) {
+  switch (s) {
+    case MOE_OK: return "ok";
+    case MOE_ERR_INVALID_ARG: return "invalid argument (pointer, shape or alignment)";
+    case MOE_ERR_UNSUPPORTED: return "configuration not supported by this build";
+    case MOE_ERR_WORKSPACE: return "scratch buffer too small";
+    case MOE_ERR_CUDA: return "a CUDA runtime call failed";
+    case MOE_ERR_TIMEOUT: return "a device-side bounded wait ran out";
+    case MOE_ERR_DEVICE_CHECK: return "a kernel found an out-of-range index";
+  }
+  return "unknown status";
+}
+
+}  // extern "C"

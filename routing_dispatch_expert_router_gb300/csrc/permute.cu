@@ -1,0 +1,225 @@
+// Stage 2 of the MoE layer, dispatch, done locally: a stable counting sort of
+// the (token, slot) assignments by (expert, token), then a copy of every token
+// row into its experts' contiguous segments.
+//
+// Follows the dispatch stage of "Scalable Training of Mixture-of-Experts
+// Models with Megatron Core" (es summary, Resumen técnico §2.1 step 2); with
+// every expert on one GPU the all-to-all becomes this permutation. The maps
+// are computed without atomics whose order matters, so they are
+// deterministic and bit-identical from run to run.
+//
+// Three launches:
+//   hist    one block per chunk of 256 tokens: per-expert counts of the chunk;
+//   rank    one block per chunk: global counts, segment offsets, and the rank
+//           of every assignment = (assignments of its expert in earlier
+//           chunks) + (earlier tokens of this chunk that chose the same
+//           expert, read from a per-expert bitmap of the chunk's tokens);
+//   scatter one warp per token: reads the row once, writes it to each of its
+//           rows with 16-byte stores; padding rows are zero-filled.
+#include "common.cuh"
+#include "internal.h"
+
+namespace moe {
+
+__global__ void __launch_bounds__(256)
+permute_hist_kernel(const int32_t* __restrict__ idx, int32_t* __restrict__ hist, int T, int k,
+                    int E, int32_t* status) {
+  __shared__ int cnt[kMaxExperts];
+  for (int e = threadIdx.x; e < E; e += blockDim.x) cnt[e] = 0;
+  __syncthreads();
+  const int c = blockIdx.x;
+  const int t0 = c * kChunkTokens, t1 = min(T, t0 + kChunkTokens);
+  for (int i = t0 * k + threadIdx.x; i < t1 * k; i += blockDim.x) {
+    const int e = idx[i];
+    if ((unsigned)e < (unsigned)E) atomicAdd(&cnt[e], 1);
+    else record_status(status, MOE_ERR_DEVICE_CHECK);
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += blockDim.x) hist[(size_t)c * E + e] = cnt[e];
+}
+
+__global__ void __launch_bounds__(256)
+permute_rank_kernel(const int32_t* __restrict__ idx, const int32_t* __restrict__ hist,
+                    int n_chunk, int T, int k, int E, int S, int align, int C,
+                    int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
+                    int32_t* __restrict__ row_of, int32_t* __restrict__ token_of,
+                    int32_t* __restrict__ sel_offsets, int32_t* __restrict__ sel_tokens,
+                    int32_t* __restrict__ pad_prefix) {
+  __shared__ int tot[kMaxExperts];
+  __shared__ int before[kMaxExperts];
+  __shared__ int seg[kMaxGroups + 1];
+  __shared__ int kept[kMaxGroups];
+  __shared__ int pad[kMaxGroups + 1];
+  __shared__ int soff[kMaxExperts + 1];
+  __shared__ uint32_t bm[kMaxExperts][kChunkTokens / 32];
+  __shared__ int tmp[33];
+  const int c = blockIdx.x, G = E + S, tid = threadIdx.x, nt = blockDim.x;
+
+  for (int e = tid; e < E; e += nt) {
+    int a = 0, b = 0;
+    for (int cc = 0; cc < n_chunk; ++cc) {
+      const int h = hist[(size_t)cc * E + e];
+      a += h;
+      if (cc < c) b += h;
+    }
+    tot[e] = a;
+    before[e] = b;
+    soff[e] = a;
+  }
+  for (int i = tid; i < E * (kChunkTokens / 32); i += nt) (&bm[0][0])[i] = 0u;
+  __syncthreads();
+  for (int g = tid; g < G; g += nt) {
+    int kp, sl;
+    if (g < E) {
+      kp = C > 0 ? min(tot[g], C) : tot[g];
+      sl = C > 0 ? C : (kp + align - 1) / align * align;
+    } else {
+      kp = T;
+      sl = (T + align - 1) / align * align;
+    }
+    kept[g] = kp;
+    seg[g] = sl;
+    pad[g] = sl - kp;
+  }
+  __syncthreads();
+  const int R = block_exclusive_scan(seg, G, tmp);
+  const int P = block_exclusive_scan(pad, G, tmp);
+  const int A = block_exclusive_scan(soff, E, tmp);
+  if (tid == 0) {
+    seg[G] = R;
+    pad[G] = P;
+    soff[E] = A;
+  }
+  __syncthreads();
+  if (c == 0) {
+    for (int g = tid; g < G; g += nt) counts[g] = kept[g];
+    for (int g = tid; g <= G; g += nt) {
+      offsets[g] = seg[g];
+      pad_prefix[g] = pad[g];
+    }
+    for (int e = tid; e <= E; e += nt) sel_offsets[e] = soff[e];
+  }
+  const int t0 = c * kChunkTokens, t1 = min(T, t0 + kChunkTokens);
+  for (int i = t0 * k + tid; i < t1 * k; i += nt) {
+    const int e = idx[i];
+    if ((unsigned)e >= (unsigned)E) continue;
+    const int tl = i / k - t0;
+    atomicOr(&bm[e][tl >> 5], 1u << (tl & 31));
+  }
+  __syncthreads();
+  for (int i = t0 * k + tid; i < t1 * k; i += nt) {
+    const int e = idx[i];
+    if ((unsigned)e >= (unsigned)E) {
+      row_of[i] = -1;
+      continue;
+    }
+    const int t = i / k, tl = t - t0, wd = tl >> 5;
+    int local = __popc(bm[e][wd] & ((1u << (tl & 31)) - 1u));
+    for (int q = 0; q < wd; ++q) local += __popc(bm[e][q]);
+    const int rank = before[e] + local;
+    sel_tokens[soff[e] + rank] = t;
+    int row = -1;
+    if (C == 0 || rank < C) {
+      row = seg[e] + rank;
+      token_of[row] = t;
+    }
+    row_of[i] = row;
+  }
+  for (int s = 0; s < S; ++s)
+    for (int t = t0 + tid; t < t1; t += nt) token_of[seg[E + s] + t] = t;
+  for (int g = c; g < G; g += n_chunk)
+    for (int r = seg[g] + kept[g] + tid; r < seg[g + 1]; r += nt) token_of[r] = -1;
+}
+
+// Finds the group whose padding range holds padding row number p.
+__device__ __forceinline__ int find_group(const int* prefix, int G, int p) {
+  int lo = 0, hi = G - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (prefix[mid] <= p) lo = mid;
+    else hi = mid - 1;
+  }
+  return lo;
+}
+
+// Virtual rows v < T copy token v to its rows; v >= T zero one padding row.
+__global__ void __launch_bounds__(256)
+permute_scatter_kernel(const __nv_bfloat16* __restrict__ x, const int32_t* __restrict__ row_of,
+                       const int32_t* __restrict__ counts, const int32_t* __restrict__ offsets,
+                       const int32_t* __restrict__ pad_prefix, __nv_bfloat16* __restrict__ x_perm,
+                       int T, int H, int k, int E, int S) {
+  __shared__ int s_pp[kMaxGroups + 1];
+  __shared__ int s_off[kMaxGroups + 1];
+  __shared__ int s_cnt[kMaxGroups];
+  const int G = E + S;
+  for (int g = threadIdx.x; g <= G; g += blockDim.x) {
+    s_pp[g] = pad_prefix[g];
+    s_off[g] = offsets[g];
+    if (g < G) s_cnt[g] = counts[g];
+  }
+  __syncthreads();
+  const int P = s_pp[G];
+  const int lane = threadIdx.x & 31;
+  const int nvec = H >> 3;
+  const int warps = gridDim.x * (blockDim.x >> 5);
+  for (int v = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); v < T + P; v += warps) {
+    if (v < T) {
+      const int t = v;
+      int myrow = (lane < k) ? row_of[(size_t)t * k + lane] : -1;
+      if (lane >= k && lane < k + S) myrow = s_off[E + lane - k] + t;
+      const int nr = k + S;
+      int rows[kMaxK + 4];
+#pragma unroll
+      for (int j = 0; j < kMaxK + 4; ++j) rows[j] = __shfl_sync(0xffffffffu, myrow, j);
+      const __nv_bfloat16* src = x + (size_t)t * H;
+      for (int c0 = lane; c0 < nvec; c0 += 32 * 4) {
+        uint4 q[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+          if (c0 + 32 * u < nvec) q[u] = ldg_nc_v4(src + (size_t)(c0 + 32 * u) * 8);
+#pragma unroll
+        for (int j = 0; j < kMaxK + 4; ++j) {
+          if (j >= nr || rows[j] < 0) continue;
+          __nv_bfloat16* dst = x_perm + (size_t)rows[j] * H;
+#pragma unroll
+          for (int u = 0; u < 4; ++u)
+            if (c0 + 32 * u < nvec) stg_v4(dst + (size_t)(c0 + 32 * u) * 8, q[u]);
+        }
+      }
+    } else {
+      const int p = v - T;
+      const int g = find_group(s_pp, G, p);
+      const int r = s_off[g] + s_cnt[g] + (p - s_pp[g]);
+      __nv_bfloat16* dst = x_perm + (size_t)r * H;
+      const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+      for (int c0 = lane; c0 < nvec; c0 += 32) stg_v4(dst + (size_t)c0 * 8, z);
+    }
+  }
+}
+
+cudaError_t launch_permute(const moe_config& c, const void* x, const int32_t* idx,
+                           int32_t* counts, int32_t* offsets, int32_t* row_of, int32_t* token_of,
+                           int32_t* sel_offsets, int32_t* sel_tokens, void* x_perm,
+                           uint8_t* scratch, cudaStream_t s) {
+  int32_t* status = reinterpret_cast<int32_t*>(scratch + kScratchStatus);
+  int32_t* pad_prefix = reinterpret_cast<int32_t*>(scratch + kScratchPadPrefix);
+  int32_t* hist = reinterpret_cast<int32_t*>(scratch + kScratchHist);
+  const int nc = n_chunks(c);
+  cudaError_t err;
+  if (nc > 0) {
+    permute_hist_kernel<<<nc, 256, 0, s>>>(idx, hist, c.T, c.k, c.E, status);
+    err = cudaGetLastError();
+    if (err != cudaSuccess) return err;
+  }
+  permute_rank_kernel<<<nc > 0 ? nc : 1, 256, 0, s>>>(idx, hist, nc, c.T, c.k, c.E, c.n_shared, c.row_align,
+                                         (int)capacity_rows(c), counts, offsets, row_of,
+                                         token_of, sel_offsets, sel_tokens, pad_prefix);
+  err = cudaGetLastError();
+  if (err != cudaSuccess) return err;
+  permute_scatter_kernel<<<num_sms() * 8, 256, 0, s>>>(
+      static_cast<const __nv_bfloat16*>(x), row_of, counts, offsets, pad_prefix,
+      static_cast<__nv_bfloat16*>(x_perm), c.T, c.H, c.k, c.E, c.n_shared);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -1,0 +1,257 @@
+// Stage 1 of the MoE layer, route: fp32 router logits and top-k selection.
+//
+// Follows the route stage of "Scalable Training of Mixture-of-Experts Models
+// with Megatron Core" (es summary, Resumen técnico §2.1 step 1: a router sends
+// every token to its k best experts), with the router kept in fp32 (§2.4).
+#include "common.cuh"
+#include "internal.h"
+
+namespace moe {
+
+// logits[t,e] = sum_h x[t,h] W_r[e,h] in fp32, one thread owning a 4x4 block of
+// (token, expert) outputs; x and W_r staged through shared memory in 32-wide
+// slices of H. The summation order over h is fixed (sequential FMA).
+template <int BT, int BE>
+__global__ void __launch_bounds__(256)
+route_logits_kernel(const __nv_bfloat16* __restrict__ x, const float* __restrict__ W,
+                    float* __restrict__ logits, int T, int H, int E) {
+  constexpr int HC = 32;
+  constexpr int TX = BE / 4;
+  constexpr int TY = BT / 4;
+  static_assert(TX * TY == 256, "256 threads");
+  __shared__ __align__(16) float xs[HC][BT + 4];
+  __shared__ __align__(16) float ws[HC][BE + 4];
+  const int t0 = blockIdx.x * BT, e0 = blockIdx.y * BE;
+  const int tx = threadIdx.x % TX, ty = threadIdx.x / TX;
+  float acc[4][4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+#pragma unroll
+    for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
+
+  for (int h0 = 0; h0 < H; h0 += HC) {
+    for (int v = threadIdx.x; v < BT * 4; v += 256) {
+      const int tt = v >> 2, hq = (v & 3) * 8, t = t0 + tt;
+      float f[8];
+      if (t < T) {
+        unpack8(ldg_nc_v4(x + (size_t)t * H + h0 + hq), f);
+      } else {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) f[i] = 0.f;
+      }
+#pragma unroll
+      for (int i = 0; i < 8; ++i) xs[hq + i][tt] = f[i];
+    }
+    for (int v = threadIdx.x; v < BE * 8; v += 256) {
+      const int ee = v >> 3, hq = (v & 7) * 4, e = e0 + ee;
+      float4 q = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (e < E) q = *reinterpret_cast<const float4*>(W + (size_t)e * H + h0 + hq);
+      ws[hq][ee] = q.x;
+      ws[hq + 1][ee] = q.y;
+      ws[hq + 2][ee] = q.z;
+      ws[hq + 3][ee] = q.w;
+    }
+    __syncthreads();
+#pragma unroll 8
+    for (int h = 0; h < HC; ++h) {
+      const float4 a = *reinterpret_cast<const float4*>(&xs[h][ty * 4]);
+      const float4 b = *reinterpret_cast<const float4*>(&ws[h][tx * 4]);
+      const float av[4] = {a.x, a.y, a.z, a.w};
+      const float bv[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(av[i], bv[j], acc[i][j]);
+    }
+    __syncthreads();
+  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int t = t0 + ty * 4 + i;
+    if (t >= T) continue;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int e = e0 + tx * 4 + j;
+      if (e < E) logits[(size_t)t * E + e] = acc[i][j];
+    }
+  }
+}
+
+struct Cand {
+  double key;
+  int e;  // -1 = no candidate
+};
+
+__device__ __forceinline__ bool better(const Cand& a, const Cand& b) {
+  if (a.e < 0) return false;
+  if (b.e < 0) return true;
+  if (a.key > b.key) return true;
+  if (a.key < b.key) return false;
+  return a.e < b.e;
+}
+
+__device__ __forceinline__ Cand warp_best(Cand c) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    Cand d;
+    d.key = __shfl_xor_sync(0xffffffffu, c.key, o);
+    d.e = __shfl_xor_sync(0xffffffffu, c.e, o);
+    if (better(d, c)) c = d;
+  }
+  return c;
+}
+
+// The two largest values held by the warp (duplicates count twice).
+__device__ __forceinline__ void warp_top2(double& a1, double& a2) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const double b1 = __shfl_xor_sync(0xffffffffu, a1, o);
+    const double b2 = __shfl_xor_sync(0xffffffffu, a2, o);
+    const double hi = fmax(a1, b1);
+    const double lo = fmax(fmin(a1, b1), fmax(a2, b2));
+    a1 = hi;
+    a2 = lo;
+  }
+}
+
+// One warp per token: selection keys, optional group limit, top-k, weights.
+// Lane l owns experts l, l+32, l+64, ... (at most 8).
+__global__ void __launch_bounds__(256)
+route_select_kernel(const float* __restrict__ logits, const float* __restrict__ bias,
+                    int32_t* __restrict__ idx, float* __restrict__ wout, int T, int E, int k,
+                    int score_fn, int n_groups, int topk_groups, int group_score,
+                    float route_scale) {
+  const int lane = threadIdx.x & 31;
+  const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (t >= T) return;
+  const float* lrow = logits + (size_t)t * E;
+  constexpr int NPL = kMaxExperts / 32;
+  double key[NPL];
+  bool avail[NPL];
+#pragma unroll
+  for (int i = 0; i < NPL; ++i) {
+    const int e = lane + 32 * i;
+    avail[i] = e < E;
+    key[i] = -INFINITY;
+    if (e < E) {
+      const float l = lrow[e];
+      const float b = bias ? bias[e] : 0.f;
+      double v;
+      if (score_fn == MOE_SCORE_SOFTMAX) {
+        v = (double)__fadd_rn(l, b);
+      } else {
+        const double s = 1.0 / (1.0 + exp(-(double)l));
+        v = s + (double)b;
+      }
+      key[i] = isnan(v) ? -INFINITY : v;
+    }
+  }
+  if (n_groups > 1) {
+    const int per = E / n_groups;
+    double gs_mine = -INFINITY;   // lane g keeps group g's score
+    for (int g = 0; g < n_groups; ++g) {
+      double a1 = -INFINITY, a2 = -INFINITY;
+#pragma unroll
+      for (int i = 0; i < NPL; ++i) {
+        const int e = lane + 32 * i;
+        if (e < E && e / per == g) {
+          const double v = key[i];
+          if (v > a1) { a2 = a1; a1 = v; }
+          else if (v > a2) { a2 = v; }
+        }
+      }
+      warp_top2(a1, a2);
+      const double gsc = (group_score == MOE_GROUP_TOP2_SUM && per >= 2) ? a1 + a2 : a1;
+      if (lane == g) gs_mine = gsc;
+    }
+    // keep the topk_groups best groups (ties -> lower group)
+    uint32_t kept = 0;
+    for (int r = 0; r < topk_groups; ++r) {
+      Cand c;
+      c.key = gs_mine;
+      c.e = (lane < n_groups && !((kept >> lane) & 1u)) ? lane : -1;
+      c = warp_best(c);
+      if (c.e >= 0) kept |= 1u << c.e;
+    }
+#pragma unroll
+    for (int i = 0; i < NPL; ++i) {
+      const int e = lane + 32 * i;
+      if (e < E && !((kept >> (e / per)) & 1u)) avail[i] = false;
+    }
+  }
+  int sel_e[kMaxK];
+  for (int j = 0; j < k; ++j) {
+    Cand c;
+    c.key = -INFINITY;
+    c.e = -1;
+#pragma unroll
+    for (int i = 0; i < NPL; ++i) {
+      Cand d;
+      d.key = key[i];
+      d.e = avail[i] ? lane + 32 * i : -1;
+      if (better(d, c)) c = d;
+    }
+    c = warp_best(c);
+    sel_e[j] = c.e;
+#pragma unroll
+    for (int i = 0; i < NPL; ++i)
+      if (lane + 32 * i == c.e) avail[i] = false;
+  }
+  // weights: every lane computes them; lane j writes slot j
+  if (score_fn == MOE_SCORE_SOFTMAX) {
+    float z[kMaxK];
+    float zs = 0.f;
+    for (int j = 0; j < k; ++j) {
+      const int e = sel_e[j];
+      z[j] = __fadd_rn(lrow[e], bias ? bias[e] : 0.f);
+    }
+    const float z0 = z[0];
+    for (int j = 0; j < k; ++j) {
+      z[j] = expf(z[j] - z0);
+      zs += z[j];
+    }
+    if (lane < k) {
+      float v = 0.f;
+      int ee = 0;
+      for (int j = 0; j < k; ++j)
+        if (j == lane) { v = z[j]; ee = sel_e[j]; }
+      idx[(size_t)t * k + lane] = ee;
+      wout[(size_t)t * k + lane] = v / zs;
+    }
+  } else {
+    double s[kMaxK];
+    double ss = 0.0;
+    for (int j = 0; j < k; ++j) {
+      s[j] = 1.0 / (1.0 + exp(-(double)lrow[sel_e[j]]));
+      ss += s[j];
+    }
+    if (lane < k) {
+      double v = 0.0;
+      int ee = 0;
+      for (int j = 0; j < k; ++j)
+        if (j == lane) { v = s[j]; ee = sel_e[j]; }
+      idx[(size_t)t * k + lane] = ee;
+      wout[(size_t)t * k + lane] = (float)((double)route_scale * v / ss);
+    }
+  }
+}
+
+cudaError_t launch_route(const moe_config& c, const void* x, const float* W_r, const float* bias,
+                         float* logits, int32_t* idx, float* w, cudaStream_t s) {
+  const __nv_bfloat16* xb = static_cast<const __nv_bfloat16*>(x);
+  if (c.E <= 16) {
+    dim3 grid((c.T + 255) / 256, 1);
+    route_logits_kernel<256, 16><<<grid, 256, 0, s>>>(xb, W_r, logits, c.T, c.H, c.E);
+  } else {
+    dim3 grid((c.T + 63) / 64, (c.E + 63) / 64);
+    route_logits_kernel<64, 64><<<grid, 256, 0, s>>>(xb, W_r, logits, c.T, c.H, c.E);
+  }
+  cudaError_t err = cudaGetLastError();
+  if (err != cudaSuccess) return err;
+  route_select_kernel<<<(c.T + 7) / 8, 256, 0, s>>>(logits, bias, idx, w, c.T, c.E, c.k,
+                                                    c.score_fn, c.n_groups, c.topk_groups,
+                                                    c.group_score, c.route_scale);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

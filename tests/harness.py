@@ -1,0 +1,210 @@
+"""GPU-vs-oracle parity harness shared by the GPU tests.
+
+Runs one layer step through the C-ABI (forward and backward), returns every
+output and intermediate as host arrays, and checks each step against the CPU
+oracle applied to the GPU's own inputs of that step (so a mismatch points at
+one kernel), plus the whole layer against the oracle from the raw inputs.
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import routing_dispatch_expert_router_gb300.binding as B
+from oracle import moe_oracle as O
+
+BF16_ATOL = 1e-2
+BF16_RTOL = 1e-2
+
+
+def f64(t) -> np.ndarray:
+    return t.detach().to(torch.float64).cpu().numpy()
+
+
+def i64(t) -> np.ndarray:
+    return t.detach().cpu().numpy().astype(np.int64)
+
+
+def assert_close(name, got, ref, atol=BF16_ATOL, rtol=BF16_RTOL):
+    got = np.asarray(got, np.float64)
+    ref = np.asarray(ref, np.float64)
+    assert got.shape == ref.shape, (name, got.shape, ref.shape)
+    err = np.abs(got - ref)
+    bad = ~(err <= atol + rtol * np.abs(ref))
+    if bad.any():
+        i = np.unravel_index(np.argmax(np.where(bad, err, -1)), bad.shape)
+        raise AssertionError(f"{name}: {int(bad.sum())}/{bad.size} elements out of tolerance; "
+                             f"worst at {i}: gpu={got[i]!r} ref={ref[i]!r}")
+
+
+def assert_equal(name, got, ref):
+    got = np.asarray(got)
+    ref = np.asarray(ref)
+    assert got.shape == ref.shape, (name, got.shape, ref.shape)
+    bad = got != ref
+    if bad.any():
+        i = np.argwhere(bad)[0]
+        raise AssertionError(f"{name}: {int(bad.sum())}/{bad.size} differ; first at {tuple(i)}: "
+                             f"gpu={got[tuple(i)]} ref={ref[tuple(i)]}")
+
+
+def _poison(t: torch.Tensor):
+    """Fill with 0xFF bytes (NaN for floats, -1 for int32): unwritten output shows."""
+    t.view(torch.uint8).fill_(0xFF)
+
+
+def run_layer(shape, inp: dict, backward: bool = True, device: str = "cuda") -> dict:
+    """One forward (+backward) through moe_layer_fwd / moe_layer_bwd."""
+    cfg = B.config(shape)
+    bufs = B.alloc_buffers(cfg, device, backward=backward)
+    for t in list(bufs.fwd.values()) + list(bufs.bwd.values()):
+        _poison(t)
+    d = {k: (v.to(device) if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
+    T, H, E, F = shape.T, shape.H, shape.E, shape.F
+    G = E + shape.n_shared
+    P = B.params(d["W_r"], d["bias"], d["W13"], d["W2"])
+    out = torch.empty(T, H, dtype=torch.bfloat16, device=device)
+    _poison(out)
+    B.moe_layer_fwd(cfg, P, d["x"], out, bufs.fwd_struct, bufs.scratch)
+    res = {"out": out}
+    if backward:
+        dx = torch.empty(T, H, dtype=torch.bfloat16, device=device)
+        dW_r = torch.empty(E, H, dtype=torch.float32, device=device)
+        dW13 = torch.empty(G, 2 * F, H, dtype=torch.bfloat16, device=device)
+        dW2 = torch.empty(G, H, F, dtype=torch.bfloat16, device=device)
+        for t in (dx, dW_r, dW13, dW2):
+            _poison(t)
+        B.moe_layer_bwd(cfg, P, d["x"], d["dY"], bufs.fwd_struct, bufs.bwd_struct, dx, dW_r,
+                        dW13, dW2, bufs.scratch)
+        res.update(dx=dx, dW_r=dW_r, dW13=dW13, dW2=dW2)
+    torch.cuda.synchronize()
+    status = B.moe_last_device_status(bufs.scratch)
+    assert status == 0, f"device status {status}"
+    res.update(bufs.fwd)
+    res.update(bufs.bwd)
+    res["rows_max"] = int(bufs.sizes.rows_max)
+    return res
+
+
+def check_steps(shape, inp: dict, g: dict, backward: bool = True):
+    """Every step of the GPU path against the oracle fed the GPU's step inputs."""
+    T, H, E, k, F, S = shape.T, shape.H, shape.E, shape.k, shape.F, shape.n_shared
+    G = E + S
+    x = f64(inp["x"])
+    Wr = f64(inp["W_r"])
+    bias = None if inp["bias"] is None else f64(inp["bias"])
+    W13 = inp["W13"]
+    W2 = inp["W2"]
+    # a1: logits within the fp32 accumulation bound
+    lg = f64(g["logits"])
+    ref_l = O.router_logits(x, Wr)
+    scale = np.abs(x) @ np.abs(Wr).T
+    bad = np.abs(lg - ref_l) > 1e-5 * scale + 1e-30
+    assert not bad.any(), f"logits: {int(bad.sum())} beyond 1e-5*sum|x w|"
+    # a2: selection bit-exact on the GPU's logits, weights close
+    idx_ref, w_ref = O.route(lg, shape, bias)
+    assert_equal("idx", i64(g["idx"]), idx_ref)
+    assert_close("w", f64(g["w"]), w_ref, atol=1e-6, rtol=1e-5)
+    # a3/a4: maps bit-exact, x_perm exact
+    m = O.permutation_maps(i64(g["idx"]), shape)
+    R = m["R"]
+    assert_equal("counts", i64(g["counts"]), m["counts"])
+    assert_equal("offsets", i64(g["offsets"]), m["offsets"])
+    assert_equal("row_of", i64(g["row_of"]), m["row_of"])
+    assert_equal("token_of", i64(g["token_of"])[:R], m["token_of"])
+    assert_equal("sel_offsets", i64(g["sel_offsets"]), m["sel_offsets"])
+    assert_equal("sel_tokens", i64(g["sel_tokens"])[:T * k], m["sel_tokens"])
+    xp = f64(g["x_perm"])[:R]
+    assert_equal("x_perm", xp, O.permute(x, m))
+    # a5/a6 per group on the GPU's rows
+    off, cnt = m["offsets"], m["counts"]
+    GU = f64(g["GU"])
+    hh = f64(g["h"])
+    yp = f64(g["y_perm"])
+    for gi in range(G):
+        if cnt[gi] == 0:
+            continue
+        rows = slice(off[gi], off[gi] + cnt[gi])
+        w13 = f64(W13[gi])
+        w2 = f64(W2[gi])
+        gu_ref, h_ref = O.expert_fc1(xp[rows], w13)
+        assert_close(f"GU[g={gi}]", GU[rows], gu_ref)
+        assert_close(f"h[g={gi}]", hh[rows], O.round_bf16(O.silu(GU[rows, :F]) * GU[rows, F:]))
+        assert_close(f"y[g={gi}]", yp[rows], O.expert_fc2(hh[rows], w2))
+    # a7 combine on the GPU's y and weights
+    wg = f64(g["w"])
+    rof = m["row_of"]
+    acc = np.zeros((T, H))
+    for j in range(k):
+        ok = rof[:, j] >= 0
+        acc[ok] += wg[ok, j:j + 1] * yp[rof[ok, j]]
+    for s in range(S):
+        acc += yp[off[E + s]: off[E + s] + T]
+    assert_close("out", f64(g["out"]), O.round_bf16(acc))
+    if not backward:
+        return
+    dY = f64(inp["dY"])
+    # a8 combine backward
+    dO = f64(g["dO_perm"])
+    dw = f64(g["dw"])
+    for j in range(k):
+        ok = rof[:, j] >= 0
+        assert_close(f"dO[slot {j}]", dO[rof[ok, j]], O.round_bf16(wg[ok, j:j + 1] * dY[ok]))
+        ref_dw = np.where(ok, np.einsum("th,th->t", dY, yp[np.maximum(rof[:, j], 0)]), 0.0)
+        assert_close(f"dw[slot {j}]", dw[:, j], ref_dw, atol=1e-3, rtol=1e-3)
+    for s in range(S):
+        assert_equal("dO[shared]", dO[off[E + s]: off[E + s] + T], dY)
+    pad = m["token_of"] < 0
+    assert_equal("dO padding", dO[:R][pad], np.zeros((int(pad.sum()), H)))
+    assert_equal("x_perm padding", xp[pad], np.zeros((int(pad.sum()), H)))
+    # a14a: dlogits on the GPU's dw
+    dl = f64(g["dlogits"])
+    dl_ref = O.router_dlogits(shape, lg, i64(g["idx"]), wg, dw)
+    assert_close("dlogits", dl, dl_ref, atol=1e-4, rtol=1e-4)
+    # a9..a12 per group
+    dGU = f64(g["dGU"])
+    dX = f64(g["dX_perm"])
+    dW13 = g["dW13"]
+    dW2 = g["dW2"]
+    for gi in range(G):
+        w13 = f64(W13[gi])
+        w2 = f64(W2[gi])
+        if cnt[gi] == 0:
+            assert_equal(f"dW2[g={gi}] empty", f64(dW2[gi]), np.zeros((H, F)))
+            assert_equal(f"dW13[g={gi}] empty", f64(dW13[gi]), np.zeros((2 * F, H)))
+            continue
+        rows = slice(off[gi], off[gi] + cnt[gi])
+        assert_close(f"dGU[g={gi}]", dGU[rows], O.expert_fc2_dgrad_swiglu(dO[rows], w2, GU[rows]))
+        assert_close(f"dX[g={gi}]", dX[rows], O.expert_fc1_dgrad(dGU[rows], w13))
+        assert_close(f"dW2[g={gi}]", f64(dW2[gi]), O.wgrad(dO[rows], hh[rows]))
+        assert_close(f"dW13[g={gi}]", f64(dW13[gi]), O.wgrad(dGU[rows], xp[rows]))
+    # a13 + router dx
+    acc = np.zeros((T, H))
+    for j in range(k):
+        ok = rof[:, j] >= 0
+        acc[ok] += dX[rof[ok, j]]
+    for s in range(S):
+        acc += dX[off[E + s]: off[E + s] + T]
+    acc += dl @ Wr
+    assert_close("dx", f64(g["dx"]), O.round_bf16(acc))
+    # a14b
+    assert_close("dW_r", f64(g["dW_r"]), dl.T @ x, atol=1e-3, rtol=1e-4)
+
+
+def check_end_to_end(shape, inp: dict, g: dict, backward: bool = True):
+    """The whole layer against the oracle run from the raw inputs."""
+    x = f64(inp["x"])
+    Wr = f64(inp["W_r"])
+    bias = None if inp["bias"] is None else f64(inp["bias"])
+    W13 = f64(inp["W13"])
+    W2 = f64(inp["W2"])
+    fwd = O.layer_forward(shape, x, Wr, bias, W13, W2, logits=f64(g["logits"]))
+    assert_equal("idx (e2e)", i64(g["idx"]), fwd["idx"])
+    assert_close("out (e2e)", f64(g["out"]), fwd["out"])
+    if not backward:
+        return
+    bwd = O.layer_backward(shape, x, Wr, W13, W2, fwd, f64(inp["dY"]))
+    assert_close("dx (e2e)", f64(g["dx"]), bwd["dx"])
+    assert_close("dW13 (e2e)", f64(g["dW13"]), bwd["dW13"])
+    assert_close("dW2 (e2e)", f64(g["dW2"]), bwd["dW2"])
+    assert_close("dW_r (e2e)", f64(g["dW_r"]), bwd["dW_r"], atol=1e-2, rtol=1e-2)

@@ -1,0 +1,86 @@
+"""The C-ABI library on the CPU: it builds, loads, exports every entry point
+declared in include/moe_abi.h, and validates arguments on the host (no kernel
+is launched by these tests)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import routing_dispatch_expert_router_gb300.binding as B
+from routing_dispatch_expert_router_gb300.build import build
+from workloads import DSV3, DSV3_FP8, MIXTRAL, QWEN3, TINY, MoEShape
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    build()
+
+
+def declared_symbols():
+    text = open(os.path.join(ROOT, "include", "moe_abi.h")).read()
+    return sorted(set(re.findall(r"MOE_API\s+[\w\s\*]+?\b(moe_\w+)\s*\(", text)))
+
+
+def test_library_exports_every_declared_symbol():
+    names = declared_symbols()
+    assert len(names) >= 15
+    lib = ctypes.CDLL(B.LIB_PATH)
+    for n in names:
+        assert hasattr(lib, n), n
+    assert sorted(B.ENTRY_POINTS) == names
+
+
+def test_query_sizes_worst_case_rows():
+    s = B.moe_query_sizes(MIXTRAL)
+    assert s.rows_max == 4096 * 2 + 8 * 127 and s.groups == 8 and s.capacity == 0
+    s = B.moe_query_sizes(DSV3)
+    assert s.rows_max == 8192 * 8 + 256 * 127 + 8192 and s.groups == 257
+    s = B.moe_query_sizes(QWEN3)
+    assert s.rows_max == 16384 * 8 + 128 * 127
+    s = B.moe_query_sizes(TINY)
+    assert s.rows_max == 512 + 8 * 127
+    s = B.moe_query_sizes(MoEShape("c", T=16384, H=128, E=256, k=8, F=128, capacity_factor=1.25))
+    assert s.capacity == 640 and s.rows_max == 256 * 640
+    assert s.scratch_bytes >= 4096 + 64 * 256 * 4
+
+
+@pytest.mark.parametrize("bad", [
+    dict(H=100), dict(F=200), dict(k=0), dict(k=9), dict(E=300), dict(k=5, E=4),
+    dict(n_groups=3), dict(n_groups=8, topk_groups=0), dict(n_groups=4, topk_groups=1, k=3, E=8),
+    dict(row_align=64), dict(capacity_factor=-1.0), dict(score_fn=7), dict(T=-1),
+    dict(n_shared=5),
+])
+def test_invalid_configs_rejected(bad):
+    with pytest.raises(B.MoEError) as e:
+        B.moe_query_sizes(TINY.with_(**bad))
+    assert e.value.code == 1
+
+
+def test_fp8_dtype_reported_unsupported():
+    with pytest.raises(B.MoEError) as e:
+        B.moe_query_sizes(DSV3_FP8)
+    assert e.value.code == 2
+
+
+def test_null_and_misaligned_pointers_rejected_before_launch():
+    cfg = B.config(TINY)
+    lib = B.lib()
+    vp = ctypes.c_void_p
+    rc = lib.moe_route(ctypes.byref(cfg), vp(None), vp(4096), vp(None), vp(4096), vp(4096),
+                       vp(4096), vp(4096), vp(None))
+    assert rc == 1
+    rc = lib.moe_unpermute(ctypes.byref(cfg), vp(4096 + 8), vp(4096), vp(4096), vp(4096),
+                           vp(4096), vp(None))
+    assert rc == 1
+    rc = lib.moe_layer_fwd(ctypes.byref(cfg), vp(None), vp(4096), vp(4096), vp(None), vp(4096),
+                           vp(None))
+    assert rc == 1
+
+
+def test_status_strings():
+    for code in range(7):
+        assert B.status_string(code)
+    assert "unknown" in B.status_string(99)
