@@ -25,7 +25,9 @@
  *    device: kernels read them there (the sync-free, device-initiated
  *    execution of the same page, §2.3.C).
  *  - Layouts are row-major. bf16 tensors are passed as `void*` holding IEEE
- *    bfloat16. Index tensors are int32.
+ *    bfloat16. Index tensors are int32. Device buffers must be 16-byte aligned
+ *    (4-byte for int32/fp32 vectors); buffers indexed by token may be NULL
+ *    when T == 0.
  *  - Argument errors are returned synchronously (MOE_ERR_INVALID_ARG /
  *    MOE_ERR_UNSUPPORTED) before anything is launched. Problems detected by a
  *    kernel (an index out of range, a bounded wait that ran out) are recorded

@@ -69,6 +69,9 @@ static moe_status check_config(const moe_config* c) {
 
 static bool al16(const void* p) { return p && ((uintptr_t)p & 15u) == 0; }
 static bool al4(const void* p) { return p && ((uintptr_t)p & 3u) == 0; }
+// Token-indexed buffers may be NULL when the batch is empty (T == 0).
+static bool tok16(const moe_config* c, const void* p) { return (c->T == 0 && !p) || al16(p); }
+static bool tok4(const moe_config* c, const void* p) { return (c->T == 0 && !p) || al4(p); }
 
 static moe_status cuda_status(cudaError_t e) {
   if (e == cudaSuccess) return MOE_OK;
@@ -116,7 +119,7 @@ moe_status moe_query_sizes(const moe_config* cfg, moe_sizes* out) {
 moe_status moe_route(const moe_config* cfg, const void* x, const float* W_r, const float* bias,
                      float* logits, int32_t* idx, float* w, void* scratch, void* stream) {
   MOE_TRY(check_config(cfg));
-  MOE_REQUIRE(al16(x) && al16(W_r) && al4(logits) && al4(idx) && al4(w));
+  MOE_REQUIRE(tok16(cfg, x) && al16(W_r) && tok4(cfg, logits) && tok4(cfg, idx) && tok4(cfg, w));
   MOE_REQUIRE(bias == nullptr || al4(bias));
   (void)scratch;
   if (cfg->T == 0) return MOE_OK;
@@ -128,8 +131,8 @@ moe_status moe_permute(const moe_config* cfg, const void* x, const int32_t* idx,
                        int32_t* offsets, int32_t* row_of, int32_t* token_of, int32_t* sel_offsets,
                        int32_t* sel_tokens, void* x_perm, void* scratch, void* stream) {
   MOE_TRY(check_config(cfg));
-  MOE_REQUIRE(al16(x) && al4(idx) && al4(counts) && al4(offsets) && al4(row_of));
-  MOE_REQUIRE(al4(token_of) && al4(sel_offsets) && al4(sel_tokens) && al16(x_perm));
+  MOE_REQUIRE(tok16(cfg, x) && tok4(cfg, idx) && al4(counts) && al4(offsets) && tok4(cfg, row_of));
+  MOE_REQUIRE(al4(token_of) && al4(sel_offsets) && tok4(cfg, sel_tokens) && al16(x_perm));
   MOE_REQUIRE(al16(scratch));
   MOE_CUDA(launch_permute(*cfg, x, idx, counts, offsets, row_of, token_of, sel_offsets,
                           sel_tokens, x_perm, static_cast<uint8_t*>(scratch),
@@ -153,7 +156,7 @@ moe_status moe_grouped_ffn_fwd(const moe_config* cfg, const void* x_perm, const 
 moe_status moe_unpermute(const moe_config* cfg, const void* y_perm, const int32_t* row_of,
                          const float* w, const int32_t* offsets, void* out, void* stream) {
   MOE_TRY(check_config(cfg));
-  MOE_REQUIRE(al16(y_perm) && al4(row_of) && al4(w) && al4(offsets) && al16(out));
+  MOE_REQUIRE(al16(y_perm) && tok4(cfg, row_of) && tok4(cfg, w) && al4(offsets) && tok16(cfg, out));
   MOE_CUDA(launch_unpermute(*cfg, y_perm, row_of, w, offsets, out, (cudaStream_t)stream));
   return MOE_OK;
 }
@@ -162,8 +165,8 @@ moe_status moe_unpermute_bwd(const moe_config* cfg, const void* dY, const void* 
                              const int32_t* row_of, const float* w, const int32_t* counts,
                              const int32_t* offsets, void* dO_perm, float* dw, void* stream) {
   MOE_TRY(check_config(cfg));
-  MOE_REQUIRE(al16(dY) && al16(y_perm) && al4(row_of) && al4(w) && al4(counts));
-  MOE_REQUIRE(al4(offsets) && al16(dO_perm) && al4(dw));
+  MOE_REQUIRE(tok16(cfg, dY) && al16(y_perm) && tok4(cfg, row_of) && tok4(cfg, w) && al4(counts));
+  MOE_REQUIRE(al4(offsets) && al16(dO_perm) && tok4(cfg, dw));
   MOE_CUDA(launch_unpermute_bwd(*cfg, dY, y_perm, row_of, w, counts, offsets, dO_perm, dw,
                                 (cudaStream_t)stream));
   return MOE_OK;
@@ -190,7 +193,7 @@ moe_status moe_grouped_ffn_bwd(const moe_config* cfg, const void* dO_perm, const
 moe_status moe_route_bwd(const moe_config* cfg, const float* logits, const int32_t* idx,
                          const float* w, const float* dw, float* dlogits, void* stream) {
   MOE_TRY(check_config(cfg));
-  MOE_REQUIRE(al4(logits) && al4(idx) && al4(w) && al4(dw) && al4(dlogits));
+  MOE_REQUIRE(tok4(cfg, logits) && tok4(cfg, idx) && tok4(cfg, w) && tok4(cfg, dw) && tok4(cfg, dlogits));
   if (cfg->T == 0) return MOE_OK;
   MOE_CUDA(launch_route_bwd(*cfg, logits, idx, w, dw, dlogits, (cudaStream_t)stream));
   return MOE_OK;
@@ -200,8 +203,8 @@ moe_status moe_permute_bwd(const moe_config* cfg, const void* dX_perm, const int
                            const int32_t* offsets, const int32_t* idx, const float* dlogits,
                            const float* W_r, void* dx, void* stream) {
   MOE_TRY(check_config(cfg));
-  MOE_REQUIRE(al16(dX_perm) && al4(row_of) && al4(offsets) && al4(idx) && al4(dlogits));
-  MOE_REQUIRE(al16(W_r) && al16(dx));
+  MOE_REQUIRE(al16(dX_perm) && tok4(cfg, row_of) && al4(offsets) && tok4(cfg, idx) && tok4(cfg, dlogits));
+  MOE_REQUIRE(al16(W_r) && tok16(cfg, dx));
   MOE_CUDA(launch_permute_bwd(*cfg, dX_perm, row_of, offsets, idx, dlogits, W_r, dx,
                               (cudaStream_t)stream));
   return MOE_OK;
@@ -211,7 +214,7 @@ moe_status moe_router_wgrad(const moe_config* cfg, const void* x, const int32_t*
                             const int32_t* sel_tokens, const float* dlogits, float* dW_r,
                             void* stream) {
   MOE_TRY(check_config(cfg));
-  MOE_REQUIRE(al16(x) && al4(sel_offsets) && al4(sel_tokens) && al4(dlogits) && al4(dW_r));
+  MOE_REQUIRE(tok16(cfg, x) && al4(sel_offsets) && tok4(cfg, sel_tokens) && tok4(cfg, dlogits) && al4(dW_r));
   MOE_CUDA(launch_router_wgrad(*cfg, x, sel_offsets, sel_tokens, dlogits, dW_r,
                                (cudaStream_t)stream));
   return MOE_OK;
