@@ -272,24 +272,24 @@ def run_ours(args, rank, world, local):
                      "gemm_tflop_per_step": (fl_fwd + fl_bwd) / 1e12},
         "clocks": clk,
     }
-    return res, shape
+    return res, shape, inp
 
 
 # ---------------------------------------------------------------------- the oracle
-def oracle_sample(shape, n_tok: int, seed: int):
-    """The CPU oracle's fwd+bwd on the first n_tok tokens of the workload."""
+def oracle_inputs(inp: dict, n_tok: int) -> dict:
+    """Host fp64 copies of the first n_tok tokens and all weights (not timed)."""
+    h = lambda t: None if t is None else t.detach().to("cpu").double().numpy()  # noqa: E731
+    return {"x": h(inp["x"][:n_tok]), "dY": h(inp["dY"][:n_tok]), "W_r": h(inp["W_r"]),
+            "bias": h(inp["bias"]), "W13": h(inp["W13"]), "W2": h(inp["W2"])}
+
+
+def oracle_sample(shape, o: dict) -> float:
+    """Seconds the CPU oracle takes for fwd+bwd of the sampled tokens."""
     from oracle import moe_oracle as O
-    sub = shape.with_(T=n_tok)
-    inp = W.make_inputs(shape, seed=seed, device="cpu")
-    x = inp["x"][:n_tok].double().numpy()
-    dY = inp["dY"][:n_tok].double().numpy()
-    Wr = inp["W_r"].double().numpy()
-    bias = None if inp["bias"] is None else inp["bias"].double().numpy()
-    W13 = inp["W13"].double().numpy()
-    W2 = inp["W2"].double().numpy()
+    sub = shape.with_(T=o["x"].shape[0])
     t0 = time.perf_counter()
-    fwd = O.layer_forward(sub, x, Wr, bias, W13, W2)
-    O.layer_backward(sub, x, Wr, W13, W2, fwd, dY)
+    fwd = O.layer_forward(sub, o["x"], o["W_r"], o["bias"], o["W13"], o["W2"])
+    O.layer_backward(sub, o["x"], o["W_r"], o["W13"], o["W2"], fwd, o["dY"])
     return time.perf_counter() - t0
 
 
@@ -302,10 +302,11 @@ def cpu_cores() -> int:
 
 def run_reference(args):
     shape = W.SHAPES[args.workload]
-    n_tok = args.cpu_sample_tokens or (64 if shape.name != "tiny" else shape.T)
-    for _ in range(max(args.warmup, 0) and 1):
-        oracle_sample(shape, min(n_tok, 8), args.seed)
-    secs = [oracle_sample(shape, n_tok, args.seed) for _ in range(args.steps)]
+    n_tok = args.cpu_sample_tokens or (shape.T if shape.name == "tiny" else 64)
+    o = oracle_inputs(W.make_inputs(shape, seed=args.seed, device="cpu"), n_tok)
+    if args.warmup > 0:
+        oracle_sample(shape, oracle_inputs_slice(o, min(n_tok, 4)))
+    secs = [oracle_sample(shape, o) for _ in range(args.steps)]
     tot = sum(secs)
     val = n_tok * args.steps / tot
     cb = {"value": val, "unit": "tokens/s", "cores": cpu_cores(), "kind": "oracle",
@@ -320,6 +321,13 @@ def run_reference(args):
                     "d2h_bytes_per_step": 0}}
 
 
+def oracle_inputs_slice(o: dict, n: int) -> dict:
+    d = dict(o)
+    d["x"] = o["x"][:n]
+    d["dY"] = o["dY"][:n]
+    return d
+
+
 def main():
     args = parse()
     rank, world, local = dist_env()
@@ -331,11 +339,13 @@ def main():
         if world > 1:
             torch.distributed.destroy_process_group()
         return
-    res, shape = run_ours(args, rank, world, local)
+    res, shape, inp = run_ours(args, rank, world, local)
     if rank == 0:
         if not args.no_cpu_baseline:
-            n_tok = args.cpu_sample_tokens or 64
-            secs = oracle_sample(shape, n_tok, args.seed)
+            n_tok = args.cpu_sample_tokens or (shape.T if shape.name == "tiny" else 64)
+            o = oracle_inputs(inp, n_tok)
+            del inp
+            secs = oracle_sample(shape, o)
             res["cpu_baseline"] = {
                 "value": n_tok / secs, "unit": "tokens/s", "cores": cpu_cores(), "kind": "oracle",
                 "sample": f"first {n_tok} tokens of {shape.name}: oracle fwd+bwd incl. weight "

@@ -28,38 +28,50 @@ __device__ __forceinline__ void token_rows(const int32_t* row_of, const float* w
 }
 
 // out[t] = bf16( sum_j w_tj y[row_tj] + sum_s y[shared row] )
+// One thread per 16-byte slice of an output row: it issues the k (+S) row
+// loads of its slice back to back, then sums them in slot order.
 __global__ void __launch_bounds__(256)
 unpermute_kernel(const __nv_bfloat16* __restrict__ y, const int32_t* __restrict__ row_of,
                  const float* __restrict__ w, const int32_t* __restrict__ offsets,
                  __nv_bfloat16* __restrict__ out, int T, int H, int k, int E, int S) {
-  const int lane = threadIdx.x & 31;
   const int nvec = H >> 3, nr = k + S;
-  const int warps = gridDim.x * (blockDim.x >> 5);
-  for (int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); t < T; t += warps) {
-    int myrow;
-    float mywt;
-    token_rows(row_of, w, offsets, t, k, E, S, lane, myrow, mywt);
-    int rows[kMaxK + 4];
-    float wts[kMaxK + 4];
+  const long long n = (long long)T * nvec;
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n;
+       i += (long long)gridDim.x * blockDim.x) {
+    const int t = (int)(i / nvec), c = (int)(i % nvec);
+    uint4 q[kMaxK + 4];
+    float wt[kMaxK + 4];
+    bool on[kMaxK + 4];
 #pragma unroll
     for (int j = 0; j < kMaxK + 4; ++j) {
-      rows[j] = __shfl_sync(0xffffffffu, myrow, j);
-      wts[j] = __shfl_sync(0xffffffffu, mywt, j);
-    }
-    for (int c = lane; c < nvec; c += 32) {
-      float acc[8];
-#pragma unroll
-      for (int i = 0; i < 8; ++i) acc[i] = 0.f;
-#pragma unroll
-      for (int j = 0; j < kMaxK + 4; ++j) {
-        if (j >= nr || rows[j] < 0) continue;
-        float f[8];
-        unpack8(ldg_nc_v4(y + (size_t)rows[j] * H + (size_t)c * 8), f);
-#pragma unroll
-        for (int i = 0; i < 8; ++i) acc[i] = fmaf(wts[j], f[i], acc[i]);
+      on[j] = false;
+      wt[j] = 0.f;
+      if (j >= nr) continue;
+      int r;
+      if (j < k) {
+        r = row_of[(size_t)t * k + j];
+        wt[j] = w[(size_t)t * k + j];
+      } else {
+        r = offsets[E + j - k] + t;
+        wt[j] = 1.f;
       }
-      stg_v4(out + (size_t)t * H + (size_t)c * 8, pack8(acc));
+      if (r >= 0) {
+        on[j] = true;
+        q[j] = ldg_nc_v4(y + (size_t)r * H + (size_t)c * 8);
+      }
     }
+    float acc[8];
+#pragma unroll
+    for (int m = 0; m < 8; ++m) acc[m] = 0.f;
+#pragma unroll
+    for (int j = 0; j < kMaxK + 4; ++j) {
+      if (!on[j]) continue;
+      float f[8];
+      unpack8(q[j], f);
+#pragma unroll
+      for (int m = 0; m < 8; ++m) acc[m] = fmaf(wt[j], f[m], acc[m]);
+    }
+    stg_v4(out + (size_t)t * H + (size_t)c * 8, pack8(acc));
   }
 }
 
@@ -73,8 +85,10 @@ __device__ __forceinline__ int find_pad_group(const int* prefix, int G, int p) {
   return lo;
 }
 
-// dO[row_tj] = bf16(w_tj dY[t]); dw_tj = <dY[t], y[row_tj]>; shared rows get dY;
-// virtual rows past T zero the padding rows of dO.
+// dO[row_tj] = bf16(w_tj dY[t]); dw_tj = <dY[t], y[row_tj]>; shared rows get dY.
+// One block per token (grid-stride over tokens, then over the padding rows of
+// dO, which are zeroed). Threads own 16-byte slices; the dot products are
+// reduced warp by warp and then across warps in a fixed order.
 __global__ void __launch_bounds__(256)
 unpermute_bwd_kernel(const __nv_bfloat16* __restrict__ dY, const __nv_bfloat16* __restrict__ y,
                      const int32_t* __restrict__ row_of, const float* __restrict__ w,
@@ -85,6 +99,7 @@ unpermute_bwd_kernel(const __nv_bfloat16* __restrict__ dY, const __nv_bfloat16* 
   __shared__ int s_off[kMaxGroups + 1];
   __shared__ int s_cnt[kMaxGroups];
   __shared__ int s_tmp[33];
+  __shared__ float s_dot[8][kMaxK];
   const int G = E + S;
   for (int g = threadIdx.x; g <= G; g += blockDim.x) s_off[g] = offsets[g];
   for (int g = threadIdx.x; g < G; g += blockDim.x) s_cnt[g] = counts[g];
@@ -94,41 +109,49 @@ unpermute_bwd_kernel(const __nv_bfloat16* __restrict__ dY, const __nv_bfloat16* 
   const int P = block_exclusive_scan(s_pp, G, s_tmp);
   if (threadIdx.x == 0) s_pp[G] = P;
   __syncthreads();
-  const int lane = threadIdx.x & 31;
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, nwarp = blockDim.x >> 5;
   const int nvec = H >> 3, nr = k + S;
-  const int warps = gridDim.x * (blockDim.x >> 5);
-  for (int v = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); v < T + P; v += warps) {
+  for (int v = blockIdx.x; v < T + P; v += gridDim.x) {
     if (v >= T) {
       const int p = v - T;
       const int g = find_pad_group(s_pp, G, p);
       const int r = s_off[g] + s_cnt[g] + (p - s_pp[g]);
       const uint4 z = make_uint4(0u, 0u, 0u, 0u);
-      for (int c = lane; c < nvec; c += 32) stg_v4(dO + (size_t)r * H + (size_t)c * 8, z);
+      for (int c = threadIdx.x; c < nvec; c += blockDim.x)
+        stg_v4(dO + (size_t)r * H + (size_t)c * 8, z);
       continue;
     }
     const int t = v;
-    int myrow;
-    float mywt;
-    token_rows(row_of, w, offsets, t, k, E, S, lane, myrow, mywt);
     int rows[kMaxK + 4];
     float wts[kMaxK + 4];
 #pragma unroll
     for (int j = 0; j < kMaxK + 4; ++j) {
-      rows[j] = __shfl_sync(0xffffffffu, myrow, j);
-      wts[j] = __shfl_sync(0xffffffffu, mywt, j);
+      rows[j] = -1;
+      wts[j] = 0.f;
+      if (j >= nr) continue;
+      if (j < k) {
+        rows[j] = row_of[(size_t)t * k + j];
+        wts[j] = w[(size_t)t * k + j];
+      } else {
+        rows[j] = s_off[E + j - k] + t;
+      }
     }
     float dot[kMaxK];
 #pragma unroll
     for (int j = 0; j < kMaxK; ++j) dot[j] = 0.f;
-    for (int c = lane; c < nvec; c += 32) {
+    for (int c = threadIdx.x; c < nvec; c += blockDim.x) {
       const uint4 gq = ldg_nc_v4(dY + (size_t)t * H + (size_t)c * 8);
+      uint4 yq[kMaxK];
+#pragma unroll
+      for (int j = 0; j < kMaxK; ++j)
+        if (j < k && rows[j] >= 0) yq[j] = ldg_nc_v4(y + (size_t)rows[j] * H + (size_t)c * 8);
       float g[8];
       unpack8(gq, g);
 #pragma unroll
       for (int j = 0; j < kMaxK; ++j) {
         if (j >= k || rows[j] < 0) continue;
         float f[8], o[8];
-        unpack8(ldg_nc_v4(y + (size_t)rows[j] * H + (size_t)c * 8), f);
+        unpack8(yq[j], f);
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
           dot[j] = fmaf(g[i], f[i], dot[j]);
@@ -144,9 +167,16 @@ unpermute_bwd_kernel(const __nv_bfloat16* __restrict__ dY, const __nv_bfloat16* 
     }
 #pragma unroll
     for (int j = 0; j < kMaxK; ++j) {
-      const float s = warp_sum(dot[j]);
-      if (lane == 0 && j < k) dw[(size_t)t * k + j] = (rows[j] >= 0) ? s : 0.f;
+      const float sj = warp_sum(dot[j]);
+      if (lane == 0) s_dot[wid][j] = sj;
     }
+    __syncthreads();
+    if (threadIdx.x < k) {
+      float sj = 0.f;
+      for (int q = 0; q < nwarp; ++q) sj += s_dot[q][threadIdx.x];
+      dw[(size_t)t * k + threadIdx.x] = (rows[threadIdx.x] >= 0) ? sj : 0.f;
+    }
+    __syncthreads();
   }
 }
 
@@ -192,63 +222,58 @@ route_bwd_kernel(const float* __restrict__ logits, const int32_t* __restrict__ i
 }
 
 // dx[t] = bf16( sum_j dX[row_tj] + sum_s dX[shared row] + sum_j dl_tj W_r[e_tj] )
+// One thread per 16-byte slice of a dx row, all row loads issued together.
 __global__ void __launch_bounds__(256)
 permute_bwd_kernel(const __nv_bfloat16* __restrict__ dX, const int32_t* __restrict__ row_of,
                    const int32_t* __restrict__ offsets, const int32_t* __restrict__ idx,
                    const float* __restrict__ dlogits, const float* __restrict__ W_r,
                    __nv_bfloat16* __restrict__ dx, int T, int H, int k, int E, int S) {
-  const int lane = threadIdx.x & 31;
   const int nvec = H >> 3, nr = k + S;
-  const int warps = gridDim.x * (blockDim.x >> 5);
-  for (int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); t < T; t += warps) {
-    int myrow;
-    float unused;
-    token_rows(row_of, nullptr, offsets, t, k, E, S, lane, myrow, unused);
-    int mye = 0;
-    float mydl = 0.f;
-    if (lane < k) {
-      mye = idx[(size_t)t * k + lane];
-      mydl = ((unsigned)mye < (unsigned)E) ? dlogits[(size_t)t * E + mye] : 0.f;
-      if ((unsigned)mye >= (unsigned)E) mye = 0;
-    }
-    int rows[kMaxK + 4], es[kMaxK];
-    float dls[kMaxK];
+  const long long n = (long long)T * nvec;
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n;
+       i += (long long)gridDim.x * blockDim.x) {
+    const int t = (int)(i / nvec), c = (int)(i % nvec);
+    uint4 q[kMaxK + 4];
+    bool on[kMaxK + 4];
 #pragma unroll
-    for (int j = 0; j < kMaxK + 4; ++j) rows[j] = __shfl_sync(0xffffffffu, myrow, j);
+    for (int j = 0; j < kMaxK + 4; ++j) {
+      on[j] = false;
+      if (j >= nr) continue;
+      const int r = (j < k) ? row_of[(size_t)t * k + j] : offsets[E + j - k] + t;
+      if (r >= 0) {
+        on[j] = true;
+        q[j] = ldg_nc_v4(dX + (size_t)r * H + (size_t)c * 8);
+      }
+    }
+    float acc[8];
+#pragma unroll
+    for (int m = 0; m < 8; ++m) acc[m] = 0.f;
+#pragma unroll
+    for (int j = 0; j < kMaxK + 4; ++j) {
+      if (!on[j]) continue;
+      float f[8];
+      unpack8(q[j], f);
+#pragma unroll
+      for (int m = 0; m < 8; ++m) acc[m] += f[m];
+    }
 #pragma unroll
     for (int j = 0; j < kMaxK; ++j) {
-      es[j] = __shfl_sync(0xffffffffu, mye, j);
-      dls[j] = __shfl_sync(0xffffffffu, mydl, j);
+      if (j >= k) continue;
+      int e = idx[(size_t)t * k + j];
+      if ((unsigned)e >= (unsigned)E) continue;
+      const float d = dlogits[(size_t)t * E + e];
+      const float4* wr = reinterpret_cast<const float4*>(W_r + (size_t)e * H + (size_t)c * 8);
+      const float4 a = __ldg(wr), b = __ldg(wr + 1);
+      acc[0] = fmaf(d, a.x, acc[0]);
+      acc[1] = fmaf(d, a.y, acc[1]);
+      acc[2] = fmaf(d, a.z, acc[2]);
+      acc[3] = fmaf(d, a.w, acc[3]);
+      acc[4] = fmaf(d, b.x, acc[4]);
+      acc[5] = fmaf(d, b.y, acc[5]);
+      acc[6] = fmaf(d, b.z, acc[6]);
+      acc[7] = fmaf(d, b.w, acc[7]);
     }
-    for (int c = lane; c < nvec; c += 32) {
-      float acc[8];
-#pragma unroll
-      for (int i = 0; i < 8; ++i) acc[i] = 0.f;
-#pragma unroll
-      for (int j = 0; j < kMaxK + 4; ++j) {
-        if (j >= nr || rows[j] < 0) continue;
-        float f[8];
-        unpack8(ldg_nc_v4(dX + (size_t)rows[j] * H + (size_t)c * 8), f);
-#pragma unroll
-        for (int i = 0; i < 8; ++i) acc[i] += f[i];
-      }
-#pragma unroll
-      for (int j = 0; j < kMaxK; ++j) {
-        if (j >= k) continue;
-        const float d = dls[j];
-        const float4* wr = reinterpret_cast<const float4*>(W_r + (size_t)es[j] * H + (size_t)c * 8);
-        const float4 a = wr[0], b = wr[1];
-        acc[0] = fmaf(d, a.x, acc[0]);
-        acc[1] = fmaf(d, a.y, acc[1]);
-        acc[2] = fmaf(d, a.z, acc[2]);
-        acc[3] = fmaf(d, a.w, acc[3]);
-        acc[4] = fmaf(d, b.x, acc[4]);
-        acc[5] = fmaf(d, b.y, acc[5]);
-        acc[6] = fmaf(d, b.z, acc[6]);
-        acc[7] = fmaf(d, b.w, acc[7]);
-      }
-      stg_v4(dx + (size_t)t * H + (size_t)c * 8, pack8(acc));
-    }
+    stg_v4(dx + (size_t)t * H + (size_t)c * 8, pack8(acc));
   }
 }
 
@@ -311,6 +336,15 @@ router_wgrad_kernel(const __nv_bfloat16* __restrict__ x, const int32_t* __restri
   }
 }
 
+// Blocks of 256 threads for one thread per 16-byte slice of every token row.
+static int grid_for_vectors(const moe_config& c) {
+  const long long n = (long long)c.T * (c.H / 8);
+  long long blocks = (n + 255) / 256;
+  const long long cap = (long long)num_sms() * 32;
+  if (blocks > cap) blocks = cap;
+  return blocks > 0 ? (int)blocks : 1;
+}
+
 static int grid_for_warps(int n_items) {
   const int blocks = (n_items + 7) / 8;
   const int cap = num_sms() * 16;
@@ -319,7 +353,7 @@ static int grid_for_warps(int n_items) {
 
 cudaError_t launch_unpermute(const moe_config& c, const void* y_perm, const int32_t* row_of,
                              const float* w, const int32_t* offsets, void* out, cudaStream_t s) {
-  unpermute_kernel<<<grid_for_warps(c.T), 256, 0, s>>>(
+  unpermute_kernel<<<grid_for_vectors(c), 256, 0, s>>>(
       static_cast<const __nv_bfloat16*>(y_perm), row_of, w, offsets,
       static_cast<__nv_bfloat16*>(out), c.T, c.H, c.k, c.E, c.n_shared);
   return cudaGetLastError();
@@ -329,7 +363,7 @@ cudaError_t launch_unpermute_bwd(const moe_config& c, const void* dY, const void
                                  const int32_t* row_of, const float* w, const int32_t* counts,
                                  const int32_t* offsets, void* dO_perm, float* dw,
                                  cudaStream_t s) {
-  unpermute_bwd_kernel<<<num_sms() * 8, 256, 0, s>>>(
+  unpermute_bwd_kernel<<<num_sms() * 16, 256, 0, s>>>(
       static_cast<const __nv_bfloat16*>(dY), static_cast<const __nv_bfloat16*>(y_perm), row_of, w,
       counts, offsets, static_cast<__nv_bfloat16*>(dO_perm), dw, c.T, c.H, c.k, c.E, c.n_shared);
   return cudaGetLastError();
@@ -345,7 +379,7 @@ cudaError_t launch_route_bwd(const moe_config& c, const float* logits, const int
 cudaError_t launch_permute_bwd(const moe_config& c, const void* dX_perm, const int32_t* row_of,
                                const int32_t* offsets, const int32_t* idx, const float* dlogits,
                                const float* W_r, void* dx, cudaStream_t s) {
-  permute_bwd_kernel<<<grid_for_warps(c.T), 256, 0, s>>>(
+  permute_bwd_kernel<<<grid_for_vectors(c), 256, 0, s>>>(
       static_cast<const __nv_bfloat16*>(dX_perm), row_of, offsets, idx, dlogits, W_r,
       static_cast<__nv_bfloat16*>(dx), c.T, c.H, c.k, c.E, c.n_shared);
   return cudaGetLastError();

@@ -127,7 +127,8 @@ permute_rank_kernel(const int32_t* __restrict__ idx, const int32_t* __restrict__
   }
   for (int s = 0; s < S; ++s)
     for (int t = t0 + tid; t < t1; t += nt) token_of[seg[E + s] + t] = t;
-  for (int g = c; g < G; g += n_chunk)
+  // padding rows of groups g = c, c + gridDim.x, ... (gridDim.x >= 1 even when T == 0)
+  for (int g = c; g < G; g += gridDim.x)
     for (int r = seg[g] + kept[g] + tid; r < seg[g + 1]; r += nt) token_of[r] = -1;
 }
 

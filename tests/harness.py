@@ -25,12 +25,14 @@ def i64(t) -> np.ndarray:
     return t.detach().cpu().numpy().astype(np.int64)
 
 
-def assert_close(name, got, ref, atol=BF16_ATOL, rtol=BF16_RTOL):
+def assert_close(name, got, ref, atol=BF16_ATOL, rtol=BF16_RTOL, scale=None):
+    """|got - ref| <= atol + rtol * scale, scale = |ref| unless given (NaN fails)."""
     got = np.asarray(got, np.float64)
     ref = np.asarray(ref, np.float64)
     assert got.shape == ref.shape, (name, got.shape, ref.shape)
     err = np.abs(got - ref)
-    bad = ~(err <= atol + rtol * np.abs(ref))
+    scale = np.abs(ref) if scale is None else np.asarray(scale, np.float64)
+    bad = ~(err <= atol + rtol * scale)
     if bad.any():
         i = np.unravel_index(np.argmax(np.where(bad, err, -1)), bad.shape)
         raise AssertionError(f"{name}: {int(bad.sum())}/{bad.size} elements out of tolerance; "
