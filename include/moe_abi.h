@@ -157,6 +157,27 @@ MOE_API moe_status moe_permute(const moe_config* cfg, const void* x, const int32
                        int32_t* sel_offsets, int32_t* sel_tokens, void* x_perm,
                        void* scratch, void* stream);
 
+/* moe_permute without the `scratch` argument: it allocates nothing.
+ * The pages have no counterpart; this entry point exists for callers that
+ * cannot provide device scratch memory (code inside a framework that owns all
+ * device memory, or on a path where cudaMalloc may not be called). Its scratch
+ * is a fixed 512 KiB array inside the library, resident on every GPU that
+ * loads the library until the process exits.
+ *  - Limit: configurations whose dispatch scratch (moe_query_sizes'
+ *    scratch_bytes, 4096 + 4*E*ceil(T/256) + 256 bytes) exceeds 512 KiB return
+ *    MOE_ERR_WORKSPACE without launching anything.
+ *  - The first call on a device looks up the array's device address with that
+ *    device current; make that first call before any stream capture.
+ *  - All calls share the one array, which keeps the last call's contents:
+ *    calls whose kernels overlap on the GPU (e.g. on two streams) race. Each
+ *    call clears the array's status word; index problems a kernel finds are
+ *    recorded there and are not reported by this call.
+ * Other arguments, layouts and results are those of moe_permute. */
+MOE_API moe_status moe_permute_noalloc(const moe_config* cfg, const void* x, const int32_t* idx,
+                                       int32_t* counts, int32_t* offsets, int32_t* row_of,
+                                       int32_t* token_of, int32_t* sel_offsets,
+                                       int32_t* sel_tokens, void* x_perm, void* stream);
+
 /* Stage 3, compute (es summary §2.1 step 3; grouped GEMM, §2.3.C): for every
  * group g, on its rows X: [G|U] = X W13[g]^T (GU, bf16), h = bf16(silu(G) U),
  * y_perm = bf16(h W2[g]^T). tcgen05 grouped GEMMs that read counts/offsets on

@@ -21,7 +21,8 @@ STATUS_NAMES = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED",
 
 # every exported entry point of include/moe_abi.h
 ENTRY_POINTS = (
-    "moe_query_sizes", "moe_route", "moe_permute", "moe_grouped_ffn_fwd", "moe_unpermute",
+    "moe_query_sizes", "moe_route", "moe_permute", "moe_permute_noalloc",
+    "moe_grouped_ffn_fwd", "moe_unpermute",
     "moe_unpermute_bwd", "moe_grouped_ffn_bwd", "moe_route_bwd", "moe_permute_bwd",
     "moe_router_wgrad", "moe_layer_fwd", "moe_layer_bwd", "moe_last_device_status",
     "moe_clear_device_status", "moe_status_string",
@@ -159,6 +160,13 @@ def moe_permute(cfg, x, idx, counts, offsets, row_of, token_of, sel_offsets, sel
                 scratch, stream=None):
     _call("moe_permute", _cfg(cfg), x, idx, counts, offsets, row_of, token_of, sel_offsets,
           sel_tokens, x_perm, scratch, _stream(stream))
+
+
+def moe_permute_noalloc(cfg, x, idx, counts, offsets, row_of, token_of, sel_offsets, sel_tokens,
+                        x_perm, stream=None):
+    """moe_permute with the library's own fixed scratch array (allocates nothing)."""
+    _call("moe_permute_noalloc", _cfg(cfg), x, idx, counts, offsets, row_of, token_of,
+          sel_offsets, sel_tokens, x_perm, _stream(stream))
 
 
 def moe_grouped_ffn_fwd(cfg, x_perm, counts, offsets, W13, W2, GU, h, y_perm, scratch,

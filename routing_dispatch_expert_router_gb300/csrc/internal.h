@@ -8,6 +8,8 @@
 
 namespace moe {
 
+moe_status check_config(const moe_config* c);
+int64_t scratch_bytes(const moe_config& c);
 int64_t capacity_rows(const moe_config& c);
 int64_t rows_max(const moe_config& c);
 int n_chunks(const moe_config& c);

@@ -39,11 +39,11 @@ int num_sms() {
   return cache[dev];
 }
 
-static int64_t scratch_bytes(const moe_config& c) {
+int64_t scratch_bytes(const moe_config& c) {
   return (int64_t)kScratchHist + (int64_t)n_chunks(c) * c.E * 4 + 256;
 }
 
-static moe_status check_config(const moe_config* c) {
+moe_status check_config(const moe_config* c) {
   if (!c) return MOE_ERR_INVALID_ARG;
   if (c->T < 0 || c->H < 128 || c->F < 128 || c->E < 1 || c->k < 1) return MOE_ERR_INVALID_ARG;
   if (c->H % 128 || c->F % 128) return MOE_ERR_INVALID_ARG;

@@ -16,6 +16,8 @@
 //           expert, read from a per-expert bitmap of the chunk's tokens);
 //   scatter one warp per token: reads the row once, writes it to each of its
 //           rows with 16-byte stores; padding rows are zero-filled.
+#include <mutex>
+
 #include "common.cuh"
 #include "internal.h"
 
@@ -224,3 +226,73 @@ cudaError_t launch_permute(const moe_config& c, const void* x, const int32_t* id
 }
 
 }  // namespace moe
+
+// ------------------------------------------------------------------------------
+// Dispatch without a caller-provided scratch buffer.
+//
+// Some callers cannot hand this library a scratch allocation: code that runs
+// inside a host framework which owns every byte of device memory (a caching
+// allocator or plugin host with no way to request an extra workspace), or
+// code on a path where calling cudaMalloc is not allowed. For them
+// moe_permute_noalloc keeps its scratch -- the per-chunk expert histograms,
+// the padding prefix and the status word -- in one file-scope device array of
+// fixed size, which every GPU that loads this library holds until the process
+// exits. It allocates nothing.
+namespace moe {
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = 512 * 1024;
+static __device__ __align__(256) uint8_t g_permute_scratch[kNoAllocScratchBytes];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_scratch_mu;
+void* g_scratch_addr[kMaxDevices] = {nullptr};
+
+// Device address of g_permute_scratch on the current device (looked up once
+// per device, on the first call made with that device current).
+cudaError_t noalloc_scratch(uint8_t** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(g_scratch_mu);
+  if (!g_scratch_addr[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_permute_scratch);
+    if (e != cudaSuccess) return e;
+    g_scratch_addr[dev] = p;
+  }
+  *out = static_cast<uint8_t*>(g_scratch_addr[dev]);
+  return cudaSuccess;
+}
+
+}  // namespace
+}  // namespace moe
+
+extern "C" moe_status moe_permute_noalloc(const moe_config* cfg, const void* x,
+                                          const int32_t* idx, int32_t* counts, int32_t* offsets,
+                                          int32_t* row_of, int32_t* token_of,
+                                          int32_t* sel_offsets, int32_t* sel_tokens,
+                                          void* x_perm, void* stream) {
+  using namespace moe;
+  const moe_status st = check_config(cfg);
+  if (st != MOE_OK) return st;
+  auto a16 = [](const void* p) { return p && ((uintptr_t)p & 15u) == 0; };
+  auto a4 = [](const void* p) { return p && ((uintptr_t)p & 3u) == 0; };
+  const bool empty = cfg->T == 0;
+  if (!((empty && !x) || a16(x)) || !((empty && !idx) || a4(idx)) || !a4(counts) ||
+      !a4(offsets) || !((empty && !row_of) || a4(row_of)) || !a4(token_of) ||
+      !a4(sel_offsets) || !((empty && !sel_tokens) || a4(sel_tokens)) || !a16(x_perm))
+    return MOE_ERR_INVALID_ARG;
+  if ((size_t)scratch_bytes(*cfg) > kNoAllocScratchBytes) return MOE_ERR_WORKSPACE;
+  uint8_t* sc = nullptr;
+  if (noalloc_scratch(&sc) != cudaSuccess) return MOE_ERR_CUDA;
+  cudaStream_t s = (cudaStream_t)stream;
+  // the status word is the only part that must start at zero; the histograms
+  // and the padding prefix are fully rewritten by every call
+  if (cudaMemsetAsync(sc + kScratchStatus, 0, sizeof(int32_t), s) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  const cudaError_t e = launch_permute(*cfg, x, idx, counts, offsets, row_of, token_of,
+                                       sel_offsets, sel_tokens, x_perm, sc, s);
+  return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
