@@ -101,6 +101,110 @@ __device__ __forceinline__ Tile decode(int tile, const int* prefix, const int* m
 
 __device__ __forceinline__ float silu_f(float z) { return z / (1.f + expf(-z)); }
 
+// Drains one 128 x BN fp32 accumulator (this thread: row `rloc`, from tensor
+// memory at `tbase`) through the fused epilogue and stores bf16 results.
+//   mt: m-tile of the group (rows offsets[g] + 128*mt, or output rows 128*mt
+//       for weight gradients); nt: n-tile; nk: k-blocks accumulated (0 = the
+//       accumulator was never written: weight gradients of empty groups).
+template <int EPI, int BN>
+__device__ __forceinline__ void epilogue_tile(const Params& p, uint32_t tbase, int g, int mt,
+                                              int nt, int nk, int rloc, const int* s_off) {
+  if (EPI == kEpiSwigluFwd) {
+    const long long row = s_off[g] + mt * BM + rloc;
+    const int f0 = nt * (BN / 2);
+    __nv_bfloat16* gu = p.out + row * p.ldo;
+    __nv_bfloat16* hr = p.out2 + row * p.ldo2;
+#pragma unroll 1
+    for (int c = 0; c < BN / 2; c += 32) {
+      uint32_t rg[32], ru[32];
+      ptx::tmem_ld32(tbase + c, rg);
+      ptx::tmem_ld32(tbase + BN / 2 + c, ru);
+      ptx::tmem_ld_wait();
+#pragma unroll
+      for (int v = 0; v < 4; ++v) {
+        float gf[8], uf[8], hf[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          gf[i] = __uint_as_float(rg[v * 8 + i]);
+          uf[i] = __uint_as_float(ru[v * 8 + i]);
+        }
+        const uint4 gb = pack8(gf), ub = pack8(uf);
+        float gr[8], ur[8];
+        unpack8(gb, gr);
+        unpack8(ub, ur);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) hf[i] = silu_f(gr[i]) * ur[i];
+        stg_v4(gu + f0 + c + v * 8, gb);
+        stg_v4(gu + p.F + f0 + c + v * 8, ub);
+        stg_v4(hr + f0 + c + v * 8, pack8(hf));
+      }
+    }
+  } else if (EPI == kEpiStore) {
+    const long long row = s_off[g] + mt * BM + rloc;
+    __nv_bfloat16* o = p.out + row * p.ldo + nt * BN;
+#pragma unroll 1
+    for (int c = 0; c < BN; c += 32) {
+      uint32_t r[32];
+      ptx::tmem_ld32(tbase + c, r);
+      ptx::tmem_ld_wait();
+#pragma unroll
+      for (int v = 0; v < 4; ++v) {
+        float f[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) f[i] = __uint_as_float(r[v * 8 + i]);
+        stg_v4(o + c + v * 8, pack8(f));
+      }
+    }
+  } else if (EPI == kEpiSwigluBwd) {
+    const long long row = s_off[g] + mt * BM + rloc;
+    const int f0 = nt * BN;
+    const __nv_bfloat16* gu = p.aux + row * p.ldaux;
+    __nv_bfloat16* o = p.out + row * p.ldo;
+#pragma unroll 1
+    for (int c = 0; c < BN; c += 32) {
+      uint32_t r[32];
+      ptx::tmem_ld32(tbase + c, r);
+      ptx::tmem_ld_wait();
+#pragma unroll
+      for (int v = 0; v < 4; ++v) {
+        float gf[8], uf[8], dg[8], du[8];
+        unpack8(ldg_v4(gu + f0 + c + v * 8), gf);
+        unpack8(ldg_v4(gu + p.F + f0 + c + v * 8), uf);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const float dh = __uint_as_float(r[v * 8 + i]);
+          const float sg = 1.f / (1.f + expf(-gf[i]));
+          dg[i] = dh * uf[i] * sg * (1.f + gf[i] * (1.f - sg));
+          du[i] = dh * gf[i] * sg;
+        }
+        stg_v4(o + f0 + c + v * 8, pack8(dg));
+        stg_v4(o + p.F + f0 + c + v * 8, pack8(du));
+      }
+    }
+  } else {  // kEpiWgrad
+    __nv_bfloat16* o = p.out + (long long)g * p.out_gstride +
+                       (long long)(mt * BM + rloc) * p.ldo + nt * BN;
+#pragma unroll 1
+    for (int c = 0; c < BN; c += 32) {
+      uint32_t r[32];
+      if (nk > 0) {
+        ptx::tmem_ld32(tbase + c, r);
+        ptx::tmem_ld_wait();
+      } else {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) r[i] = 0u;
+      }
+#pragma unroll
+      for (int v = 0; v < 4; ++v) {
+        float f[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) f[i] = __uint_as_float(r[v * 8 + i]);
+        stg_v4(o + c + v * 8, pack8(f));
+      }
+    }
+  }
+}
+
 template <int EPI, int BN, int A_MN, int B_MN, int STAGES>
 __global__ void __launch_bounds__(kThreads, 1)
 grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
@@ -295,100 +399,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
       }
       ptx::tc_fence_after();
       const uint32_t tbase = tmem_base + acc * BN + ((uint32_t)(q * 32) << 16);
-      if (EPI == kEpiSwigluFwd) {
-        const long long row = s_off[t.g] + t.mt * BM + rloc;
-        const int f0 = t.nt * (BN / 2);
-        __nv_bfloat16* gu = p.out + row * p.ldo;
-        __nv_bfloat16* hr = p.out2 + row * p.ldo2;
-#pragma unroll 1
-        for (int c = 0; c < BN / 2; c += 32) {
-          uint32_t rg[32], ru[32];
-          ptx::tmem_ld32(tbase + c, rg);
-          ptx::tmem_ld32(tbase + BN / 2 + c, ru);
-          ptx::tmem_ld_wait();
-#pragma unroll
-          for (int v = 0; v < 4; ++v) {
-            float gf[8], uf[8], hf[8];
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-              gf[i] = __uint_as_float(rg[v * 8 + i]);
-              uf[i] = __uint_as_float(ru[v * 8 + i]);
-            }
-            const uint4 gb = pack8(gf), ub = pack8(uf);
-            float gr[8], ur[8];
-            unpack8(gb, gr);
-            unpack8(ub, ur);
-#pragma unroll
-            for (int i = 0; i < 8; ++i) hf[i] = silu_f(gr[i]) * ur[i];
-            stg_v4(gu + f0 + c + v * 8, gb);
-            stg_v4(gu + p.F + f0 + c + v * 8, ub);
-            stg_v4(hr + f0 + c + v * 8, pack8(hf));
-          }
-        }
-      } else if (EPI == kEpiStore) {
-        const long long row = s_off[t.g] + t.mt * BM + rloc;
-        __nv_bfloat16* o = p.out + row * p.ldo + t.nt * BN;
-#pragma unroll 1
-        for (int c = 0; c < BN; c += 32) {
-          uint32_t r[32];
-          ptx::tmem_ld32(tbase + c, r);
-          ptx::tmem_ld_wait();
-#pragma unroll
-          for (int v = 0; v < 4; ++v) {
-            float f[8];
-#pragma unroll
-            for (int i = 0; i < 8; ++i) f[i] = __uint_as_float(r[v * 8 + i]);
-            stg_v4(o + c + v * 8, pack8(f));
-          }
-        }
-      } else if (EPI == kEpiSwigluBwd) {
-        const long long row = s_off[t.g] + t.mt * BM + rloc;
-        const int f0 = t.nt * BN;
-        const __nv_bfloat16* gu = p.aux + row * p.ldaux;
-        __nv_bfloat16* o = p.out + row * p.ldo;
-#pragma unroll 1
-        for (int c = 0; c < BN; c += 32) {
-          uint32_t r[32];
-          ptx::tmem_ld32(tbase + c, r);
-          ptx::tmem_ld_wait();
-#pragma unroll
-          for (int v = 0; v < 4; ++v) {
-            float gf[8], uf[8], dg[8], du[8];
-            unpack8(ldg_v4(gu + f0 + c + v * 8), gf);
-            unpack8(ldg_v4(gu + p.F + f0 + c + v * 8), uf);
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-              const float dh = __uint_as_float(r[v * 8 + i]);
-              const float sg = 1.f / (1.f + expf(-gf[i]));
-              dg[i] = dh * uf[i] * sg * (1.f + gf[i] * (1.f - sg));
-              du[i] = dh * gf[i] * sg;
-            }
-            stg_v4(o + f0 + c + v * 8, pack8(dg));
-            stg_v4(o + p.F + f0 + c + v * 8, pack8(du));
-          }
-        }
-      } else {  // kEpiWgrad
-        __nv_bfloat16* o = p.out + (long long)t.g * p.out_gstride +
-                           (long long)(t.mt * BM + rloc) * p.ldo + t.nt * BN;
-#pragma unroll 1
-        for (int c = 0; c < BN; c += 32) {
-          uint32_t r[32];
-          if (t.nk > 0) {
-            ptx::tmem_ld32(tbase + c, r);
-            ptx::tmem_ld_wait();
-          } else {
-#pragma unroll
-            for (int i = 0; i < 32; ++i) r[i] = 0u;
-          }
-#pragma unroll
-          for (int v = 0; v < 4; ++v) {
-            float f[8];
-#pragma unroll
-            for (int i = 0; i < 8; ++i) f[i] = __uint_as_float(r[v * 8 + i]);
-            stg_v4(o + c + v * 8, pack8(f));
-          }
-        }
-      }
+      epilogue_tile<EPI, BN>(p, tbase, t.g, t.mt, t.nt, t.nk, rloc, s_off);
       ptx::tc_fence_before();
       ptx::mbar_arrive(bar_tempty + 8 * acc);
       if (++acc == 2) {
@@ -402,6 +413,254 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
   if (warp == 1) {
     ptx::tc_fence_after();
     ptx::tmem_dealloc(tmem_base, L::TMEM_COLS);
+  }
+}
+
+// ------------------------------------------------------------ CTA-pair variant
+// The same grouped GEMM with 256 x 256 tiles computed by a pair of CTAs on two
+// SMs (a cluster of 2) with tcgen05.mma.cta_group::2: each CTA holds 128 rows
+// of the A tile and 128 of the 256 B columns, so every SM streams 32 KB per
+// 64-deep k-block instead of 48 KB for the same tensor work, and six stages
+// fit in shared memory. Only the even CTA issues MMAs; both CTAs' TMA loads
+// count on the even CTA's "full" barrier, the MMA completion is multicast to
+// both CTAs, and both epilogues report back to the even CTA.
+constexpr int kPairStages = 6;
+constexpr int kPairStage = 32768;                 // 16 KB of A + 16 KB of B per CTA
+constexpr int kPairSmem = kPairStages * kPairStage + kCtrlBytes + 1024;
+
+template <int EPI, int A_MN, int B_MN>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA,
+                         const __grid_constant__ CUtensorMap tmB, const Params p) {
+  constexpr int BN = 256, STAGES = kPairStages;
+  constexpr int A_BYTES = 16384;
+  constexpr uint32_t TMEM_COLS = 2 * BN;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = ptx::smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* ctrl = smem_raw + (base - raw) + STAGES * kPairStage;
+  const uint32_t ctrl_u = base + STAGES * kPairStage;
+  const uint32_t bar_full = ctrl_u;
+  const uint32_t bar_empty = ctrl_u + 8 * STAGES;
+  const uint32_t bar_tfull = ctrl_u + 16 * STAGES;
+  const uint32_t bar_tempty = ctrl_u + 16 * STAGES + 16;
+  const uint32_t bar_drain = ctrl_u + 16 * STAGES + 32;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(ctrl + 192);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(ctrl + 196);
+  int* prefix = reinterpret_cast<int*>(ctrl + 256);
+  int* mtiles = reinterpret_cast<int*>(ctrl + 1344);
+  int* s_off = reinterpret_cast<int*>(ctrl + 2432);
+  int* s_cnt = reinterpret_cast<int*>(ctrl + 3520);
+  int* tmp = reinterpret_cast<int*>(ctrl + 4608);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const uint32_t rank = ptx::cluster_ctarank();
+  const int cluster = blockIdx.x >> 1, nclusters = gridDim.x >> 1;
+  const int G = p.G;
+  const int NT = (EPI == kEpiSwigluFwd) ? p.F / (BN / 2) : p.N / BN;
+  for (int g = tid; g < G; g += kThreads) {
+    const int c = p.counts[g];
+    s_cnt[g] = c;
+    s_off[g] = p.offsets[g];
+    const int mt = p.kgrouped ? p.Mw / BM : (c + BM - 1) / BM;
+    mtiles[g] = mt;
+    prefix[g] = ((mt + 1) >> 1) * NT;              // pair tiles of the group
+  }
+  if (tid == 0) *abort_flag = 0;
+  __syncthreads();
+  const int total = block_exclusive_scan(prefix, G, tmp);
+  if (tid == 0) prefix[G] = total;
+  __syncthreads();
+  if (cluster >= total) return;                    // both CTAs of the pair leave together
+
+  if (tid == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      ptx::mbar_init(bar_full + 8 * s, 1);
+      ptx::mbar_init(bar_empty + 8 * s, 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      ptx::mbar_init(bar_tfull + 8 * a, 1);
+      ptx::mbar_init(bar_tempty + 8 * a, 8);       // 4 epilogue warps x 2 CTAs
+    }
+    ptx::mbar_init(bar_drain, 1);
+    ptx::fence_mbar_init();
+  }
+  if (warp == 1) {
+    ptx::tmem_alloc_pair(ptx::smem_u32(tmem_slot), TMEM_COLS);
+    ptx::tmem_relinquish_pair();
+  }
+  if (tid == 0) {
+    ptx::tma_prefetch_desc(&tmA);
+    ptx::tma_prefetch_desc(&tmB);
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::cluster_sync();
+  ptx::tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  // pair tile -> (group, m-pair, n-tile); m-pairs fastest
+  auto decode_pair = [&](int pt, int& g, int& mp, int& nt, int& nk) {
+    g = find_group(prefix, G, pt);
+    const int local = pt - prefix[g];
+    const int npairs = (mtiles[g] + 1) >> 1;
+    mp = local % npairs;
+    nt = local / npairs;
+    nk = p.kgrouped ? (s_cnt[g] + BK - 1) / BK : p.K / BK;
+  };
+
+  if (warp == 0) {
+    if (lane == 0) {
+      uint32_t stage = 0, phase = 0;
+      bool ok = true;
+      uint32_t leader_full[STAGES];
+#pragma unroll
+      for (int s = 0; s < STAGES; ++s) leader_full[s] = ptx::mapa_shared(bar_full + 8 * s, 0);
+      for (int pt = cluster; pt < total && ok; pt += nclusters) {
+        int g, mp, nt, nk;
+        decode_pair(pt, g, mp, nt, nk);
+        const int mt = 2 * mp + (int)rank;
+        for (int kb = 0; kb < nk; ++kb) {
+          if (!ptx::mbar_wait(bar_empty + 8 * stage, phase ^ 1u, kWaitBudget, abort_flag)) {
+            ok = false;
+            break;
+          }
+          if (rank == 0) ptx::mbar_arrive_expect_tx(bar_full + 8 * stage, 2 * kPairStage);
+          const uint32_t fb = leader_full[stage];
+          const uint32_t sA = base + stage * kPairStage;
+          const uint32_t sB = sA + A_BYTES;
+          const int k0 = kb * BK;
+          if (A_MN == 0) {
+            ptx::tma_load_2d_pair(sA, &tmA, fb, k0, s_off[g] + mt * BM);
+          } else {
+            const int kr = s_off[g] + k0;
+            ptx::tma_load_2d_pair(sA, &tmA, fb, mt * BM, kr);
+            ptx::tma_load_2d_pair(sA + 8192, &tmA, fb, mt * BM + 64, kr);
+          }
+          if (EPI == kEpiSwigluFwd) {
+            // CTA 0 brings the 128 gate rows, CTA 1 the matching 128 up rows
+            ptx::tma_load_2d_pair(sB, &tmB, fb, k0,
+                                  g * p.b_rows + (rank ? p.F : 0) + nt * (BN / 2));
+          } else if (B_MN == 0) {
+            ptx::tma_load_2d_pair(sB, &tmB, fb, k0, g * p.b_rows + nt * BN + (int)rank * 128);
+          } else {
+            const int kr = p.kgrouped ? s_off[g] + k0 : g * p.b_rows + k0;
+            ptx::tma_load_2d_pair(sB, &tmB, fb, nt * BN + (int)rank * 128, kr);
+            ptx::tma_load_2d_pair(sB + 8192, &tmB, fb, nt * BN + (int)rank * 128 + 64, kr);
+          }
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      if (!ok) {
+        record_status(p.status, MOE_ERR_TIMEOUT);
+        *abort_flag = 1;
+        // loads already issued land within microseconds; give them time
+        const long long t0 = clock64();
+        while (clock64() - t0 < 200000) {
+        }
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0 && rank == 0) {
+      constexpr uint32_t IDESC = ptx::idesc_bf16(2 * BM, BN, A_MN, B_MN);
+      uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
+      bool ok = true, issued = false;
+      const uint32_t peer_tfull[2] = {ptx::mapa_shared(bar_tfull, 1),
+                                      ptx::mapa_shared(bar_tfull + 8, 1)};
+      for (int pt = cluster; pt < total && ok; pt += nclusters) {
+        int g, mp, nt, nk;
+        decode_pair(pt, g, mp, nt, nk);
+        if (!ptx::mbar_wait(bar_tempty + 8 * acc, acc_phase ^ 1u, kWaitBudget, abort_flag)) {
+          ok = false;
+          break;
+        }
+        ptx::tc_fence_after();
+        const uint32_t d = tmem_base + acc * BN;
+        for (int kb = 0; kb < nk; ++kb) {
+          if (!ptx::mbar_wait(bar_full + 8 * stage, phase, kWaitBudget, abort_flag)) {
+            ok = false;
+            break;
+          }
+          ptx::tc_fence_after();
+          const uint32_t sA = base + stage * kPairStage;
+          const uint32_t sB = sA + A_BYTES;
+#pragma unroll
+          for (int kk = 0; kk < BK / 16; ++kk) {
+            const uint64_t ad = A_MN ? ptx::smem_desc_sw128(sA + kk * 2048, 8192, 1024)
+                                     : ptx::smem_desc_sw128(sA + kk * 32, 16, 1024);
+            const uint64_t bd = B_MN ? ptx::smem_desc_sw128(sB + kk * 2048, 8192, 1024)
+                                     : ptx::smem_desc_sw128(sB + kk * 32, 16, 1024);
+            ptx::mma_bf16_pair(d, ad, bd, IDESC, (kb | kk) ? 1u : 0u);
+          }
+          issued = true;
+          ptx::mma_commit_pair(bar_empty + 8 * stage, 3);
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        if (nk > 0) {
+          ptx::mma_commit_pair(bar_tfull + 8 * acc, 3);
+        } else {                                   // empty group: nothing to wait for
+          ptx::mbar_arrive(bar_tfull + 8 * acc);
+          ptx::mbar_arrive_cluster(peer_tfull[acc]);
+        }
+        if (++acc == 2) {
+          acc = 0;
+          acc_phase ^= 1u;
+        }
+      }
+      if (!ok) {
+        record_status(p.status, MOE_ERR_TIMEOUT);
+        *abort_flag = 1;
+      }
+      if (issued) {
+        ptx::mma_commit_pair(bar_drain, 1);
+        ptx::mbar_wait(bar_drain, 0, kWaitBudget, nullptr);
+      }
+    }
+  } else {
+    const int q = warp & 3;
+    const int rloc = q * 32 + lane;
+    const uint32_t leader_tempty[2] = {ptx::mapa_shared(bar_tempty, 0),
+                                       ptx::mapa_shared(bar_tempty + 8, 0)};
+    uint32_t acc = 0, acc_phase = 0;
+    for (int pt = cluster; pt < total; pt += nclusters) {
+      int g, mp, nt, nk;
+      decode_pair(pt, g, mp, nt, nk);
+      bool ok = ptx::mbar_wait(bar_tfull + 8 * acc, acc_phase, kWaitBudget, abort_flag);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) {
+        if (lane == 0) {
+          record_status(p.status, MOE_ERR_TIMEOUT);
+          *abort_flag = 1;
+        }
+        break;
+      }
+      ptx::tc_fence_after();
+      const int mt = 2 * mp + (int)rank;
+      if (mt < mtiles[g]) {                        // the odd tile of a group has no partner rows
+        const uint32_t tbase = tmem_base + acc * BN + ((uint32_t)(q * 32) << 16);
+        epilogue_tile<EPI, BN>(p, tbase, g, mt, nt, nk, rloc, s_off);
+      }
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive_cluster(leader_tempty[acc]);
+      if (++acc == 2) {
+        acc = 0;
+        acc_phase ^= 1u;
+      }
+    }
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::cluster_sync();
+  if (warp == 1) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc_pair(tmem_base, TMEM_COLS);
   }
 }
 
@@ -449,6 +708,37 @@ static cudaError_t run(const CUtensorMap& a, const CUtensorMap& b, const Params&
   return cudaGetLastError();
 }
 
+// CTA-pair launch: as many clusters as can be resident at once (the tile loop
+// strides statically over clusters, so every launched cluster must run).
+template <int EPI, int A_MN, int B_MN>
+static cudaError_t run_pair(const CUtensorMap& a, const CUtensorMap& b, const Params& p,
+                            cudaStream_t s) {
+  auto kern = grouped_gemm_pair_kernel<EPI, A_MN, B_MN>;
+  static int grid = 0;
+  if (grid == 0) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         kPairSmem);
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t lc = {};
+    lc.gridDim = dim3(2 * (num_sms() / 2), 1, 1);
+    lc.blockDim = dim3(kThreads, 1, 1);
+    lc.dynamicSmemBytes = kPairSmem;
+    int clusters = 0;
+    e = cudaOccupancyMaxActiveClusters(&clusters, kern, &lc);
+    if (e != cudaSuccess || clusters <= 0) {
+      (void)cudaGetLastError();
+      clusters = num_sms() / 2;
+    }
+    grid = 2 * clusters;
+  }
+  kern<<<grid, kThreads, kPairSmem, s>>>(a, b, p);
+  return cudaGetLastError();
+}
+
+// CTA pairs for every GEMM whose output width is a multiple of 256; the
+// single-CTA kernel covers the rest (128-wide tiles).
+static bool use_pairs(int n) { return n % 256 == 0; }
+
 static Params base_params(const moe_config& c, const int32_t* counts, const int32_t* offsets,
                           int32_t* status) {
   Params p{};
@@ -479,6 +769,7 @@ cudaError_t launch_ffn_fc1(const moe_config& c, const void* x_perm, const int32_
   p.ldo = 2LL * c.F;
   p.out2 = static_cast<__nv_bfloat16*>(h);
   p.ldo2 = c.F;
+  if (use_pairs(256)) return run_pair<kEpiSwigluFwd, 0, 0>(a, b, p, s);
   return run<kEpiSwigluFwd, 256, 0, 0, 4>(a, b, p, s);
 }
 
@@ -488,8 +779,10 @@ cudaError_t launch_ffn_fc2(const moe_config& c, const void* h, const int32_t* co
   const int64_t R = rows_max(c);
   const int G = c.E + c.n_shared;
   const int bn = (c.H % 256 == 0) ? 256 : 128;
+  const bool pair = use_pairs(c.H);
   CUtensorMap a, b;
-  if (!make_map(&a, h, c.F, R, 128) || !make_map(&b, W2, c.F, (uint64_t)G * c.H, bn))
+  if (!make_map(&a, h, c.F, R, 128) ||
+      !make_map(&b, W2, c.F, (uint64_t)G * c.H, pair ? 128 : bn))
     return cudaErrorInvalidValue;
   Params p = base_params(c, counts, offsets, status);
   p.N = c.H;
@@ -497,6 +790,7 @@ cudaError_t launch_ffn_fc2(const moe_config& c, const void* h, const int32_t* co
   p.b_rows = c.H;
   p.out = static_cast<__nv_bfloat16*>(y_perm);
   p.ldo = c.H;
+  if (pair) return run_pair<kEpiStore, 0, 0>(a, b, p, s);
   return bn == 256 ? run<kEpiStore, 256, 0, 0, 4>(a, b, p, s)
                    : run<kEpiStore, 128, 0, 0, 6>(a, b, p, s);
 }
@@ -518,6 +812,7 @@ cudaError_t launch_ffn_fc2_dgrad(const moe_config& c, const void* dO_perm, const
   p.ldo = 2LL * c.F;
   p.aux = static_cast<const __nv_bfloat16*>(GU);
   p.ldaux = 2LL * c.F;
+  if (use_pairs(c.F)) return run_pair<kEpiSwigluBwd, 0, 1>(a, b, p, s);
   return bn == 256 ? run<kEpiSwigluBwd, 256, 0, 1, 4>(a, b, p, s)
                    : run<kEpiSwigluBwd, 128, 0, 1, 6>(a, b, p, s);
 }
@@ -538,6 +833,7 @@ cudaError_t launch_ffn_fc1_dgrad(const moe_config& c, const void* dGU, const int
   p.b_rows = 2 * c.F;
   p.out = static_cast<__nv_bfloat16*>(dX_perm);
   p.ldo = c.H;
+  if (use_pairs(c.H)) return run_pair<kEpiStore, 0, 1>(a, b, p, s);
   return bn == 256 ? run<kEpiStore, 256, 0, 1, 4>(a, b, p, s)
                    : run<kEpiStore, 128, 0, 1, 6>(a, b, p, s);
 }
@@ -557,6 +853,7 @@ cudaError_t launch_ffn_wgrad_fc2(const moe_config& c, const void* dO_perm, const
   p.out = static_cast<__nv_bfloat16*>(dW2);
   p.ldo = c.F;
   p.out_gstride = (long long)c.H * c.F;
+  if (use_pairs(c.F)) return run_pair<kEpiWgrad, 1, 1>(a, b, p, s);
   return bn == 256 ? run<kEpiWgrad, 256, 1, 1, 4>(a, b, p, s)
                    : run<kEpiWgrad, 128, 1, 1, 6>(a, b, p, s);
 }
@@ -576,6 +873,7 @@ cudaError_t launch_ffn_wgrad_fc1(const moe_config& c, const void* dGU, const voi
   p.out = static_cast<__nv_bfloat16*>(dW13);
   p.ldo = c.H;
   p.out_gstride = 2LL * c.F * c.H;
+  if (use_pairs(c.H)) return run_pair<kEpiWgrad, 1, 1>(a, b, p, s);
   return bn == 256 ? run<kEpiWgrad, 256, 1, 1, 4>(a, b, p, s)
                    : run<kEpiWgrad, 128, 1, 1, 6>(a, b, p, s);
 }
