@@ -41,6 +41,14 @@ readings listed below; every one of them is a reading, not a quote:
     materialisation points (dO, dGU, dX, dx, dW13, dW2 in bf16; dlogits, dW_r
     in fp32); the router gradient flows into x and W_r.
 
+FP8 (the FP8 configuration): E4M3 values with power-of-two block scales
+(reading of the pages' MXFP8 recipe for Blackwell, es summary §2.4:
+scale = 2^ceil(log2(amax/448)), 1 for an all-zero block); activations take
+1x128 blocks along the reduction dimension of the GEMM that consumes them,
+expert weights 128x128 blocks, weight-gradient operands 128x1 blocks along
+the tokens of each expert (quantised from the bf16 tensors). Quantised values
+are exact in bf16 and in fp64, so the GEMMs below multiply them exactly.
+
 Rounding: ``round_bf16`` is round-to-nearest-even onto the bf16 grid, written
 from the format (8 exponent bits, 7 stored fraction bits). Pass
 ``rounding=False`` to the layer functions for exact fp64 arithmetic (used by
@@ -82,6 +90,67 @@ def round_bf16(a) -> np.ndarray:
         r = np.where(np.abs(r) > _BF16_MAX, np.copysign(np.inf, v), r)
         out[fin] = r
     return out
+
+
+E4M3_MAX = 448.0
+_E4M3_MIN_QUANTUM_EXP = -9            # 2^(-6 - 3): the subnormal spacing
+
+
+def round_e4m3(a) -> np.ndarray:
+    """Round to the nearest E4M3 value, ties to even, saturating at +-448.
+
+    E4M3 keeps 4 significant bits: for |a| in [2^e, 2^(e+1)) the spacing is
+    2^(e-3), never below the subnormal spacing 2^-9; the largest finite value
+    is 1.75 * 2^8 = 448 (the format has no infinities).
+    """
+    a = np.asarray(a, dtype=np.float64)
+    out = np.array(a, copy=True)
+    fin = np.isfinite(a) & (a != 0)
+    if np.any(fin):
+        v = a[fin]
+        _, ex = np.frexp(v)
+        qexp = np.maximum(ex - 1 - 3, _E4M3_MIN_QUANTUM_EXP)
+        r = np.ldexp(np.rint(np.ldexp(v, -qexp)), qexp)
+        out[fin] = np.clip(r, -E4M3_MAX, E4M3_MAX)
+    return out
+
+
+def e4m3_scale(amax) -> np.ndarray:
+    """Power-of-two block scale 2^ceil(log2(amax/448)); 1 where amax == 0."""
+    amax = np.asarray(amax, dtype=np.float64)
+    m, ex = np.frexp(amax / E4M3_MAX)             # amax/448 = m * 2^ex, 0.5 <= m < 1
+    k = np.where(m == 0.5, ex - 1, ex)            # ceil(log2(.))
+    return np.where(amax > 0, np.ldexp(1.0, k), 1.0)
+
+
+def quant_rows(X, block: int = 128) -> np.ndarray:
+    """Dequantised E4M3 values of X with one scale per 1 x `block` slice of a row."""
+    X = np.asarray(X, np.float64)
+    n, c = X.shape
+    Xb = X.reshape(n, c // block, block)
+    s = e4m3_scale(np.abs(Xb).max(axis=2, keepdims=True))
+    return (round_e4m3(Xb / s) * s).reshape(n, c)
+
+
+def quant_cols(X, block: int = 128) -> np.ndarray:
+    """One scale per `block` x 1 slice of a column (consecutive rows; a short
+    last block is scaled by its own rows)."""
+    X = np.asarray(X, np.float64)
+    out = np.empty_like(X)
+    for r0 in range(0, X.shape[0], block):
+        B = X[r0:r0 + block]
+        s = e4m3_scale(np.abs(B).max(axis=0, keepdims=True))
+        out[r0:r0 + block] = round_e4m3(B / s) * s
+    return out
+
+
+def quant_tiles(W, block: int = 128) -> np.ndarray:
+    """One scale per `block` x `block` tile of a matrix."""
+    W = np.asarray(W, np.float64)
+    r, c = W.shape
+    Wb = W.reshape(r // block, block, c // block, block)
+    s = e4m3_scale(np.abs(Wb).max(axis=(1, 3), keepdims=True))
+    return (round_e4m3(Wb / s) * s).reshape(r, c)
 
 
 def round_f32(a) -> np.ndarray:
@@ -421,3 +490,80 @@ def to_rows(per_slot, per_shared, maps, cfg, width):
         o = maps["offsets"][cfg.E + s]
         out[o:o + T] = per_shared[s]
     return out
+
+
+# --------------------------------------------------------------------------- #
+# the FP8 layer (E4M3 with power-of-two block scales)
+# --------------------------------------------------------------------------- #
+def layer_forward_fp8(cfg, x, W_r, bias, W13, W2, logits=None):
+    """The layer with its expert GEMMs on E4M3-quantised operands.
+
+    Routing stays in fp32 (es summary §2.4: the router keeps high precision).
+    Per expert: X_q = quant_rows(X) (1x128 along H), W13_q/W2_q = quant_tiles
+    (128x128), GU = bf16(X_q W13_q^T), h = bf16(silu(G) U),
+    y = bf16(quant_rows(h) W2_q^T) (1x128 along F); combine as in bf16.
+    """
+    x = np.asarray(x, np.float64)
+    T, H = x.shape
+    E, k, F = cfg.E, cfg.k, cfg.F
+    if logits is None:
+        logits = router_logits(x, W_r)
+    logits = np.asarray(logits, np.float64)
+    idx, w = route(logits, cfg, bias)
+    maps = permutation_maps(idx, cfg)
+    kept = maps["row_of"] >= 0
+    GU = np.zeros((T, k, 2 * F))
+    h = np.zeros((T, k, F))
+    y = np.zeros((T, k, H))
+    Wq13, Wq2 = {}, {}
+    for e in range(E):
+        tt, jj = np.nonzero((idx == e) & kept)
+        if tt.size == 0:
+            continue
+        order = np.argsort(tt, kind="stable")            # rows in token order
+        tt, jj = tt[order], jj[order]
+        Wq13[e] = quant_tiles(W13[e])
+        Wq2[e] = quant_tiles(W2[e])
+        g, hh = expert_fc1(quant_rows(x[tt]), Wq13[e])
+        GU[tt, jj], h[tt, jj] = g, hh
+        y[tt, jj] = expert_fc2(quant_rows(hh), Wq2[e])
+    acc = np.einsum("tj,tjh->th", np.where(kept, w, 0.0), y)
+    return dict(logits=logits, idx=idx, w=w, maps=maps, GU=GU, h=h, y=y, out=round_bf16(acc),
+                Wq13=Wq13, Wq2=Wq2)
+
+
+def layer_backward_fp8(cfg, x, W_r, W13, W2, fwd, dY):
+    """Backward of layer_forward_fp8. Data gradients: dO and dGU quantised in
+    1x128 slices along the dimension their GEMM reduces (H, 2F), weights as in
+    the forward; weight gradients: both operands quantised in 128x1 slices
+    along the expert's tokens (in token order)."""
+    x = np.asarray(x, np.float64)
+    dY = np.asarray(dY, np.float64)
+    T, H = x.shape
+    E, k, F = cfg.E, cfg.k, cfg.F
+    idx, w, maps = fwd["idx"], fwd["w"], fwd["maps"]
+    kept = maps["row_of"] >= 0
+    dO = round_bf16(np.where(kept, w, 0.0)[:, :, None] * dY[:, None, :])
+    dw = np.where(kept, np.einsum("th,tjh->tj", dY, fwd["y"]), 0.0)
+    dGU = np.zeros((T, k, 2 * F))
+    dX = np.zeros((T, k, H))
+    dW13 = np.zeros((E, 2 * F, H))
+    dW2 = np.zeros((E, H, F))
+    for e in range(E):
+        tt, jj = np.nonzero((idx == e) & kept)
+        if tt.size == 0:
+            continue
+        order = np.argsort(tt, kind="stable")
+        tt, jj = tt[order], jj[order]
+        Wq13, Wq2 = fwd["Wq13"][e], fwd["Wq2"][e]
+        dOe = dO[tt, jj]
+        d = expert_fc2_dgrad_swiglu(quant_rows(dOe), Wq2, fwd["GU"][tt, jj])
+        dGU[tt, jj] = d
+        dX[tt, jj] = expert_fc1_dgrad(quant_rows(d), Wq13)
+        dW2[e] = wgrad(quant_cols(dOe), quant_cols(fwd["h"][tt, jj]))
+        dW13[e] = wgrad(quant_cols(d), quant_cols(x[tt]))
+    dlogits = router_dlogits(cfg, fwd["logits"], idx, w, dw)
+    dx = round_bf16(dX.sum(axis=1) + dlogits @ np.asarray(W_r, np.float64))
+    dW_r = round_f32(dlogits.T @ x)
+    return dict(dO=dO, dw=dw, dGU=dGU, dX=dX, dlogits=dlogits, dx=dx, dW_r=dW_r, dW13=dW13,
+                dW2=dW2)

@@ -375,3 +375,104 @@ def test_softmax_jacobian_rows_sum_to_zero():
     dl = O.router_dlogits(cfg, l, idx, w, rng.standard_normal((30, 3)))
     np.testing.assert_allclose(dl.sum(1), 0.0, atol=1e-14)
     assert (np.count_nonzero(dl, axis=1) <= 3).all()
+
+
+# --------------------------------------------------------------------------- #
+# FP8 (E4M3, power-of-two block scales)
+# --------------------------------------------------------------------------- #
+def test_round_e4m3_matches_torch_float8_in_range():
+    g = torch.Generator().manual_seed(7)
+    v = torch.randn(200000, generator=g) * 2.0 ** torch.randint(-12, 9, (200000,), generator=g).float()
+    grid = torch.arange(0, 256, dtype=torch.uint8).view(torch.float8_e4m3fn).float()
+    grid = grid[torch.isfinite(grid)]
+    v = torch.cat([v, grid, -grid, torch.tensor([1 + 1 / 16, 1 + 3 / 16, 2.0 ** -10, 3 * 2.0 ** -10])])
+    v = v[v.abs() <= 448]
+    ref = v.to(torch.float8_e4m3fn).float().double().numpy()
+    got = O.round_e4m3(v.double().numpy())
+    np.testing.assert_array_equal(got, ref)
+
+
+def test_round_e4m3_saturates_and_scale_closed_form():
+    np.testing.assert_array_equal(O.round_e4m3([1000.0, -1e6, 448.0, 460.0]), [448, -448, 448, 448])
+    amax = np.abs(np.random.default_rng(1).standard_normal(5000)) * 10.0 ** np.random.default_rng(2).integers(-8, 8, 5000)
+    s = O.e4m3_scale(amax)
+    k = np.log2(s)
+    np.testing.assert_array_equal(k, np.round(k))              # powers of two
+    r = amax / s
+    assert (r > 224).all() and (r <= 448).all()                 # smallest power >= amax/448
+    assert O.e4m3_scale(0.0) == 1.0
+    assert O.e4m3_scale(448.0 * 2 ** -5) == 2 ** -5
+
+
+def test_block_quantisers_structure():
+    rng = np.random.default_rng(3)
+    X = rng.standard_normal((256, 384)) * np.repeat(10.0 ** rng.integers(-3, 3, (256, 3)), 128, axis=1)
+    Q = O.quant_rows(X)
+    np.testing.assert_array_equal(O.quant_rows(Q), Q)           # idempotent
+    for blk in range(3):                                        # each block scaled on its own
+        Bq, B = Q[:, blk * 128:(blk + 1) * 128], X[:, blk * 128:(blk + 1) * 128]
+        s = O.e4m3_scale(np.abs(B).max(axis=1, keepdims=True))
+        np.testing.assert_array_equal(Bq, O.round_e4m3(B / s) * s)
+    np.testing.assert_array_equal(O.quant_cols(X.T).T, O.quant_rows(X))  # columns = rows of X^T
+    # values already on the grid with block max 448*2^k are left unchanged
+    G = O.round_e4m3(rng.uniform(-448, 448, (4, 128)))
+    G[:, 0] = 448.0
+    np.testing.assert_array_equal(O.quant_rows(G * 2.0 ** 5), G * 2.0 ** 5)
+    # short last block of quant_cols uses its own rows
+    C = rng.standard_normal((200, 8))
+    C[150:] *= 1000
+    Qc = O.quant_cols(C)
+    s = O.e4m3_scale(np.abs(C[128:]).max(axis=0, keepdims=True))
+    np.testing.assert_array_equal(Qc[128:], O.round_e4m3(C[128:] / s) * s)
+
+
+def test_quant_tiles_brute_force():
+    rng = np.random.default_rng(4)
+    W = rng.standard_normal((256, 384)) * 0.02
+    W[:128, 128:256] *= 50
+    got = O.quant_tiles(W)
+    for i in range(2):
+        for j in range(3):
+            B = W[i * 128:(i + 1) * 128, j * 128:(j + 1) * 128]
+            amax = max(abs(float(v)) for v in B.ravel())
+            k = math.ceil(math.log2(amax / 448.0))
+            s = 2.0 ** k
+            np.testing.assert_array_equal(got[i * 128:(i + 1) * 128, j * 128:(j + 1) * 128],
+                                          O.round_e4m3(B / s) * s)
+
+
+def _torch_fq(t, dims):
+    """Fake-quantise with torch's own float8 conversion; `dims` = block reduce dims."""
+    amax = t.abs().amax(dim=dims, keepdim=True)
+    k = torch.ceil(torch.log2(amax / 448.0))
+    s = torch.where(amax > 0, torch.exp2(k), torch.ones_like(amax))
+    return (t / s).to(torch.float8_e4m3fn).double() * s
+
+
+def test_fp8_single_expert_layer_is_dense_fp8_mlp():
+    cfg = MoEShape("t", T=256, H=256, E=1, k=1, F=256, dtype=1)
+    inp = make_inputs(cfg, seed=13)
+    x, Wr, W13, W2, dY = (f64(inp[n]) for n in ("x", "W_r", "W13", "W2", "dY"))
+    fwd = O.layer_forward_fp8(cfg, x, Wr, None, W13, W2)
+    bwd = O.layer_backward_fp8(cfg, x, Wr, W13, W2, fwd, dY)
+    tx, t13, t2, tdY = (torch.tensor(a) for a in (x, W13[0], W2[0], dY))
+    rows = lambda t: _torch_fq(t.view(t.shape[0], -1, 128), (2,)).view(t.shape)  # noqa: E731
+    tiles = lambda t: _torch_fq(t.view(t.shape[0] // 128, 128, t.shape[1] // 128, 128), (1, 3)).reshape(t.shape)  # noqa: E731
+    cols = lambda t: rows(t.T.contiguous()).T  # noqa: E731
+    q13, q2 = tiles(t13), tiles(t2)
+    gu = _torch_bf16(rows(tx) @ q13.T)
+    h = _torch_bf16(torch.nn.functional.silu(gu[:, :256]) * gu[:, 256:])
+    y = _torch_bf16(rows(h) @ q2.T)
+    np.testing.assert_allclose(fwd["out"], y.numpy(), rtol=2 ** -7, atol=1e-6)
+    dO = tdY                                             # weight 1
+    dh = rows(dO) @ q2
+    G, U = gu[:, :256], gu[:, 256:]
+    sg = torch.sigmoid(G)
+    dGU = _torch_bf16(torch.cat([dh * U * sg * (1 + G * (1 - sg)), dh * G * sg], dim=1))
+    dX = _torch_bf16(rows(dGU) @ q13)
+    np.testing.assert_allclose(bwd["dGU"][:, 0], dGU.numpy(), rtol=2 ** -6, atol=1e-5)
+    np.testing.assert_allclose(bwd["dX"][:, 0], dX.numpy(), rtol=2 ** -6, atol=1e-4)
+    dW2 = _torch_bf16(cols(dO).T @ cols(h))
+    dW13 = _torch_bf16(cols(dGU).T @ cols(tx))
+    np.testing.assert_allclose(bwd["dW2"][0], dW2.numpy(), rtol=2 ** -6, atol=1e-4)
+    np.testing.assert_allclose(bwd["dW13"][0], dW13.numpy(), rtol=2 ** -6, atol=1e-4)
