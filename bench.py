@@ -43,7 +43,7 @@ import workloads as W  # noqa: E402
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default="mixtral", choices=sorted(W.SHAPES))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
@@ -121,6 +121,23 @@ class ClockSampler:
         return {"sm_mhz": float(np.median(sm)) if sm else None,
                 "sm_max_mhz": max(smax) if smax else None,
                 "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def gemm_traffic(workload: str):
+    """DRAM bytes per step of the grouped-GEMM launches from a committed ncu
+    capture, or None when the GEMM source changed since it was taken."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", "gemm_traffic.json")
+    src = os.path.join(ROOT, "routing_dispatch_expert_router_gb300", "csrc", "grouped_gemm.cu")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        d = json.load(f)
+    with open(src, "rb") as f:
+        h = hashlib.sha256(f.read()).hexdigest()
+    if d.get("grouped_gemm_cu_sha256") != h or d.get("workload") != workload:
+        return None
+    return d.get("dram_bytes_per_step")
 
 
 def gemm_flops(shape, counts) -> tuple:
@@ -267,7 +284,10 @@ def run_ours(args, rank, world, local):
         "roofline": {"kernel": "grouped_gemm_kernel (tcgen05; FC1+SwiGLU, FC2, 2 dgrad, 2 wgrad)",
                      "bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                      "frac": achieved / peak, "peak_source": f"{src} bf16_tflops_sustained",
-                     "traffic": None, "gemm_ms_per_step": gemm_ms,
+                     "traffic": gemm_traffic(shape.name),
+                     "traffic_note": "DRAM bytes of the six grouped-GEMM launches of one step "
+                                     "(ncu dram__bytes_read+write); achieved is per step too",
+                     "gemm_ms_per_step": gemm_ms,
                      "fwd_gemm_ms": fwd_gemm_ms, "bwd_gemm_ms": bwd_gemm_ms,
                      "gemm_tflop_per_step": (fl_fwd + fl_bwd) / 1e12},
         "clocks": clk,

@@ -65,7 +65,16 @@ typedef enum moe_status {
 
 enum { MOE_SCORE_SOFTMAX = 0, MOE_SCORE_SIGMOID = 1 };
 enum { MOE_GROUP_TOP2_SUM = 0, MOE_GROUP_MAX = 1 };
-enum { MOE_DTYPE_BF16 = 0 };
+/* MOE_DTYPE_FP8_E4M3_BLOCK: every expert-GEMM operand is quantised to E4M3
+ * with power-of-two block scales (2^ceil(log2(amax/448))): expert weights in
+ * 128x128 tiles, activations in 1x128 slices along the dimension their GEMM
+ * reduces, weight-gradient operands in 128x1 slices along each expert's
+ * tokens. Router, routing weights and all outputs stay as in bf16 mode. In
+ * this mode `scratch` also holds the quantised weights and activations
+ * (moe_query_sizes counts them), and the scratch used by a forward must be
+ * passed unchanged to its backward. Shared experts are not supported in this
+ * mode (n_shared must be 0). */
+enum { MOE_DTYPE_BF16 = 0, MOE_DTYPE_FP8_E4M3_BLOCK = 1 };
 
 /* One layer configuration. */
 typedef struct moe_config {
@@ -76,7 +85,7 @@ typedef struct moe_config {
     int32_t topk_groups;     /* groups kept per token                           */
     int32_t group_score;     /* MOE_GROUP_TOP2_SUM | MOE_GROUP_MAX              */
     float route_scale;       /* sigmoid weights: route_scale * s_j / sum s      */
-    int32_t dtype;           /* MOE_DTYPE_BF16                                  */
+    int32_t dtype;           /* MOE_DTYPE_BF16 | MOE_DTYPE_FP8_E4M3_BLOCK        */
     float capacity_factor;   /* 0 = dropless; else C = ceil(cf*T*k/E) rows      */
     int32_t row_align;       /* every expert segment is a multiple of this (128)*/
 } moe_config;

@@ -27,51 +27,73 @@ __device__ __forceinline__ void token_rows(const int32_t* row_of, const float* w
   }
 }
 
+// Row indices and weights of token t, slot j (j >= k: shared experts, weight 1).
+__device__ __forceinline__ void slot_row(const int32_t* row_of, const float* w,
+                                         const int32_t* offsets, int t, int j, int k, int E,
+                                         int& r, float& wt) {
+  if (j < k) {
+    r = row_of[(size_t)t * k + j];
+    wt = w ? w[(size_t)t * k + j] : 1.f;
+  } else {
+    r = offsets[E + j - k] + t;
+    wt = 1.f;
+  }
+}
+
 // out[t] = bf16( sum_j w_tj y[row_tj] + sum_s y[shared row] )
-// One thread per 16-byte slice of an output row: it issues the k (+S) row
-// loads of its slice back to back, then sums them in slot order.
+// One warp per (token, 64-slice segment of the row): lanes j < k+S fetch the
+// token's rows once, then every lane keeps the k+S loads of its two 16-byte
+// slices in flight together and sums them in slot order.
+template <int MAXR>
 __global__ void __launch_bounds__(256)
 unpermute_kernel(const __nv_bfloat16* __restrict__ y, const int32_t* __restrict__ row_of,
                  const float* __restrict__ w, const int32_t* __restrict__ offsets,
                  __nv_bfloat16* __restrict__ out, int T, int H, int k, int E, int S) {
+  const int lane = threadIdx.x & 31;
   const int nvec = H >> 3, nr = k + S;
-  const long long n = (long long)T * nvec;
-  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n;
-       i += (long long)gridDim.x * blockDim.x) {
-    const int t = (int)(i / nvec), c = (int)(i % nvec);
-    uint4 q[kMaxK + 4];
-    float wt[kMaxK + 4];
-    bool on[kMaxK + 4];
+  constexpr int VPL = (MAXR <= 4) ? 2 : 1;   // 16-byte slices per lane
+  const int segs = (nvec + 32 * VPL - 1) / (32 * VPL);
+  const long long items = (long long)T * segs;
+  const long long warps = (long long)gridDim.x * (blockDim.x >> 5);
+  for (long long it = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); it < items;
+       it += warps) {
+    const int t = (int)(it / segs), c0 = (int)(it % segs) * (32 * VPL) + lane;
+    int myrow = -1;
+    float mywt = 0.f;
+    if (lane < nr) slot_row(row_of, w, offsets, t, lane, k, E, myrow, mywt);
+    int rows[MAXR];
+    float wts[MAXR];
 #pragma unroll
-    for (int j = 0; j < kMaxK + 4; ++j) {
-      on[j] = false;
-      wt[j] = 0.f;
-      if (j >= nr) continue;
-      int r;
-      if (j < k) {
-        r = row_of[(size_t)t * k + j];
-        wt[j] = w[(size_t)t * k + j];
-      } else {
-        r = offsets[E + j - k] + t;
-        wt[j] = 1.f;
-      }
-      if (r >= 0) {
-        on[j] = true;
-        q[j] = ldg_nc_v4(y + (size_t)r * H + (size_t)c * 8);
-      }
+    for (int j = 0; j < MAXR; ++j) {
+      rows[j] = __shfl_sync(0xffffffffu, myrow, j);
+      wts[j] = __shfl_sync(0xffffffffu, mywt, j);
     }
-    float acc[8];
+    uint4 q[VPL][MAXR];
 #pragma unroll
-    for (int m = 0; m < 8; ++m) acc[m] = 0.f;
+    for (int u = 0; u < VPL; ++u) {
+      const int c = c0 + 32 * u;
 #pragma unroll
-    for (int j = 0; j < kMaxK + 4; ++j) {
-      if (!on[j]) continue;
-      float f[8];
-      unpack8(q[j], f);
-#pragma unroll
-      for (int m = 0; m < 8; ++m) acc[m] = fmaf(wt[j], f[m], acc[m]);
+      for (int j = 0; j < MAXR; ++j)
+        if (j < nr && rows[j] >= 0 && c < nvec)
+          q[u][j] = ldg_nc_v4(y + (size_t)rows[j] * H + (size_t)c * 8);
     }
-    stg_v4(out + (size_t)t * H + (size_t)c * 8, pack8(acc));
+#pragma unroll
+    for (int u = 0; u < VPL; ++u) {
+      const int c = c0 + 32 * u;
+      if (c >= nvec) continue;
+      float acc[8];
+#pragma unroll
+      for (int m = 0; m < 8; ++m) acc[m] = 0.f;
+#pragma unroll
+      for (int j = 0; j < MAXR; ++j) {
+        if (j >= nr || rows[j] < 0) continue;
+        float f[8];
+        unpack8(q[u][j], f);
+#pragma unroll
+        for (int m = 0; m < 8; ++m) acc[m] = fmaf(wts[j], f[m], acc[m]);
+      }
+      stg_v4(out + (size_t)t * H + (size_t)c * 8, pack8(acc));
+    }
   }
 }
 
@@ -222,58 +244,83 @@ route_bwd_kernel(const float* __restrict__ logits, const int32_t* __restrict__ i
 }
 
 // dx[t] = bf16( sum_j dX[row_tj] + sum_s dX[shared row] + sum_j dl_tj W_r[e_tj] )
-// One thread per 16-byte slice of a dx row, all row loads issued together.
+// Same warp-per-segment scheme as unpermute; the router term adds k fp32 rows
+// of W_r scaled by the token's dlogits.
+template <int MAXR>
 __global__ void __launch_bounds__(256)
 permute_bwd_kernel(const __nv_bfloat16* __restrict__ dX, const int32_t* __restrict__ row_of,
                    const int32_t* __restrict__ offsets, const int32_t* __restrict__ idx,
                    const float* __restrict__ dlogits, const float* __restrict__ W_r,
                    __nv_bfloat16* __restrict__ dx, int T, int H, int k, int E, int S) {
+  const int lane = threadIdx.x & 31;
   const int nvec = H >> 3, nr = k + S;
-  const long long n = (long long)T * nvec;
-  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n;
-       i += (long long)gridDim.x * blockDim.x) {
-    const int t = (int)(i / nvec), c = (int)(i % nvec);
-    uint4 q[kMaxK + 4];
-    bool on[kMaxK + 4];
-#pragma unroll
-    for (int j = 0; j < kMaxK + 4; ++j) {
-      on[j] = false;
-      if (j >= nr) continue;
-      const int r = (j < k) ? row_of[(size_t)t * k + j] : offsets[E + j - k] + t;
-      if (r >= 0) {
-        on[j] = true;
-        q[j] = ldg_nc_v4(dX + (size_t)r * H + (size_t)c * 8);
-      }
+  constexpr int VPL = (MAXR <= 4) ? 2 : 1;   // 16-byte slices per lane
+  const int segs = (nvec + 32 * VPL - 1) / (32 * VPL);
+  const long long items = (long long)T * segs;
+  const long long warps = (long long)gridDim.x * (blockDim.x >> 5);
+  for (long long it = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); it < items;
+       it += warps) {
+    const int t = (int)(it / segs), c0 = (int)(it % segs) * (32 * VPL) + lane;
+    int myrow = -1;
+    float unused = 0.f;
+    if (lane < nr) slot_row(row_of, nullptr, offsets, t, lane, k, E, myrow, unused);
+    int mye = -1;
+    float mydl = 0.f;
+    if (lane < k) {
+      mye = idx[(size_t)t * k + lane];
+      if ((unsigned)mye < (unsigned)E) mydl = dlogits[(size_t)t * E + mye];
+      else mye = -1;
     }
-    float acc[8];
+    int rows[MAXR], es[kMaxK];
+    float dls[kMaxK];
 #pragma unroll
-    for (int m = 0; m < 8; ++m) acc[m] = 0.f;
-#pragma unroll
-    for (int j = 0; j < kMaxK + 4; ++j) {
-      if (!on[j]) continue;
-      float f[8];
-      unpack8(q[j], f);
-#pragma unroll
-      for (int m = 0; m < 8; ++m) acc[m] += f[m];
-    }
+    for (int j = 0; j < MAXR; ++j) rows[j] = __shfl_sync(0xffffffffu, myrow, j);
 #pragma unroll
     for (int j = 0; j < kMaxK; ++j) {
-      if (j >= k) continue;
-      int e = idx[(size_t)t * k + j];
-      if ((unsigned)e >= (unsigned)E) continue;
-      const float d = dlogits[(size_t)t * E + e];
-      const float4* wr = reinterpret_cast<const float4*>(W_r + (size_t)e * H + (size_t)c * 8);
-      const float4 a = __ldg(wr), b = __ldg(wr + 1);
-      acc[0] = fmaf(d, a.x, acc[0]);
-      acc[1] = fmaf(d, a.y, acc[1]);
-      acc[2] = fmaf(d, a.z, acc[2]);
-      acc[3] = fmaf(d, a.w, acc[3]);
-      acc[4] = fmaf(d, b.x, acc[4]);
-      acc[5] = fmaf(d, b.y, acc[5]);
-      acc[6] = fmaf(d, b.z, acc[6]);
-      acc[7] = fmaf(d, b.w, acc[7]);
+      es[j] = __shfl_sync(0xffffffffu, mye, j);
+      dls[j] = __shfl_sync(0xffffffffu, mydl, j);
     }
-    stg_v4(dx + (size_t)t * H + (size_t)c * 8, pack8(acc));
+    uint4 q[VPL][MAXR];
+#pragma unroll
+    for (int u = 0; u < VPL; ++u) {
+      const int c = c0 + 32 * u;
+#pragma unroll
+      for (int j = 0; j < MAXR; ++j)
+        if (j < nr && rows[j] >= 0 && c < nvec)
+          q[u][j] = ldg_nc_v4(dX + (size_t)rows[j] * H + (size_t)c * 8);
+    }
+#pragma unroll
+    for (int u = 0; u < VPL; ++u) {
+      const int c = c0 + 32 * u;
+      if (c >= nvec) continue;
+      float acc[8];
+#pragma unroll
+      for (int m = 0; m < 8; ++m) acc[m] = 0.f;
+#pragma unroll
+      for (int j = 0; j < MAXR; ++j) {
+        if (j >= nr || rows[j] < 0) continue;
+        float f[8];
+        unpack8(q[u][j], f);
+#pragma unroll
+        for (int m = 0; m < 8; ++m) acc[m] += f[m];
+      }
+#pragma unroll
+      for (int j = 0; j < kMaxK; ++j) {
+        if (j >= k || es[j] < 0) continue;
+        const float d = dls[j];
+        const float4* wr = reinterpret_cast<const float4*>(W_r + (size_t)es[j] * H + (size_t)c * 8);
+        const float4 a = __ldg(wr), b = __ldg(wr + 1);
+        acc[0] = fmaf(d, a.x, acc[0]);
+        acc[1] = fmaf(d, a.y, acc[1]);
+        acc[2] = fmaf(d, a.z, acc[2]);
+        acc[3] = fmaf(d, a.w, acc[3]);
+        acc[4] = fmaf(d, b.x, acc[4]);
+        acc[5] = fmaf(d, b.y, acc[5]);
+        acc[6] = fmaf(d, b.z, acc[6]);
+        acc[7] = fmaf(d, b.w, acc[7]);
+      }
+      stg_v4(dx + (size_t)t * H + (size_t)c * 8, pack8(acc));
+    }
   }
 }
 
@@ -338,7 +385,7 @@ router_wgrad_kernel(const __nv_bfloat16* __restrict__ x, const int32_t* __restri
 
 // Blocks of 256 threads for one thread per 16-byte slice of every token row.
 static int grid_for_vectors(const moe_config& c) {
-  const long long n = (long long)c.T * (c.H / 8);
+  const long long n = (long long)c.T * ((c.H / 8 + 31) / 32) * 32;   // up to one warp per segment
   long long blocks = (n + 255) / 256;
   const long long cap = (long long)num_sms() * 32;
   if (blocks > cap) blocks = cap;
@@ -353,9 +400,15 @@ static int grid_for_warps(int n_items) {
 
 cudaError_t launch_unpermute(const moe_config& c, const void* y_perm, const int32_t* row_of,
                              const float* w, const int32_t* offsets, void* out, cudaStream_t s) {
-  unpermute_kernel<<<grid_for_vectors(c), 256, 0, s>>>(
-      static_cast<const __nv_bfloat16*>(y_perm), row_of, w, offsets,
-      static_cast<__nv_bfloat16*>(out), c.T, c.H, c.k, c.E, c.n_shared);
+  auto yp = static_cast<const __nv_bfloat16*>(y_perm);
+  auto o = static_cast<__nv_bfloat16*>(out);
+  if (c.k + c.n_shared <= 4)
+    unpermute_kernel<4><<<grid_for_vectors(c), 256, 0, s>>>(yp, row_of, w, offsets, o, c.T, c.H,
+                                                           c.k, c.E, c.n_shared);
+  else
+    unpermute_kernel<kMaxK + 4><<<grid_for_vectors(c), 256, 0, s>>>(yp, row_of, w, offsets, o,
+                                                                   c.T, c.H, c.k, c.E,
+                                                                   c.n_shared);
   return cudaGetLastError();
 }
 
@@ -379,9 +432,15 @@ cudaError_t launch_route_bwd(const moe_config& c, const float* logits, const int
 cudaError_t launch_permute_bwd(const moe_config& c, const void* dX_perm, const int32_t* row_of,
                                const int32_t* offsets, const int32_t* idx, const float* dlogits,
                                const float* W_r, void* dx, cudaStream_t s) {
-  permute_bwd_kernel<<<grid_for_vectors(c), 256, 0, s>>>(
-      static_cast<const __nv_bfloat16*>(dX_perm), row_of, offsets, idx, dlogits, W_r,
-      static_cast<__nv_bfloat16*>(dx), c.T, c.H, c.k, c.E, c.n_shared);
+  auto dXp = static_cast<const __nv_bfloat16*>(dX_perm);
+  auto o = static_cast<__nv_bfloat16*>(dx);
+  if (c.k + c.n_shared <= 4)
+    permute_bwd_kernel<4><<<grid_for_vectors(c), 256, 0, s>>>(dXp, row_of, offsets, idx, dlogits,
+                                                             W_r, o, c.T, c.H, c.k, c.E,
+                                                             c.n_shared);
+  else
+    permute_bwd_kernel<kMaxK + 4><<<grid_for_vectors(c), 256, 0, s>>>(
+        dXp, row_of, offsets, idx, dlogits, W_r, o, c.T, c.H, c.k, c.E, c.n_shared);
   return cudaGetLastError();
 }
 

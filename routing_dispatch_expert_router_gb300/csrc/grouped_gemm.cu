@@ -160,16 +160,31 @@ __device__ __forceinline__ void epilogue_tile(const Params& p, uint32_t tbase, i
     const int f0 = nt * BN;
     const __nv_bfloat16* gu = p.aux + row * p.ldaux;
     __nv_bfloat16* o = p.out + row * p.ldo;
+    // G and U of the next 32 columns are loaded one slice ahead, before this
+    // slice's stores, so the loads overlap the math and the stores
+    uint4 gq[4], uq[4];
+#pragma unroll
+    for (int v = 0; v < 4; ++v) {
+      gq[v] = ldg_nc_v4(gu + f0 + v * 8);
+      uq[v] = ldg_nc_v4(gu + p.F + f0 + v * 8);
+    }
 #pragma unroll 1
     for (int c = 0; c < BN; c += 32) {
       uint32_t r[32];
       ptx::tmem_ld32(tbase + c, r);
+      uint4 gn[4], un[4];
+      const int cn = (c + 32 < BN) ? c + 32 : c;
+#pragma unroll
+      for (int v = 0; v < 4; ++v) {
+        gn[v] = ldg_nc_v4(gu + f0 + cn + v * 8);
+        un[v] = ldg_nc_v4(gu + p.F + f0 + cn + v * 8);
+      }
       ptx::tmem_ld_wait();
 #pragma unroll
       for (int v = 0; v < 4; ++v) {
         float gf[8], uf[8], dg[8], du[8];
-        unpack8(ldg_v4(gu + f0 + c + v * 8), gf);
-        unpack8(ldg_v4(gu + p.F + f0 + c + v * 8), uf);
+        unpack8(gq[v], gf);
+        unpack8(uq[v], uf);
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
           const float dh = __uint_as_float(r[v * 8 + i]);
@@ -179,6 +194,11 @@ __device__ __forceinline__ void epilogue_tile(const Params& p, uint32_t tbase, i
         }
         stg_v4(o + f0 + c + v * 8, pack8(dg));
         stg_v4(o + p.F + f0 + c + v * 8, pack8(du));
+      }
+#pragma unroll
+      for (int v = 0; v < 4; ++v) {
+        gq[v] = gn[v];
+        uq[v] = un[v];
       }
     }
   } else {  // kEpiWgrad

@@ -41,6 +41,24 @@ cudaError_t launch_router_wgrad(const moe_config& c, const void* x, const int32_
                                 const int32_t* sel_tokens, const float* dlogits, float* dW_r,
                                 cudaStream_t s);
 
+// FP8 block quantisation (E4M3 values with power-of-two scales, stored as bf16).
+cudaError_t launch_quant_tiles(const void* W, void* Wq, int G, int rows, int cols, cudaStream_t s);
+cudaError_t launch_quant_rows(const void* X, void* Xq, const int32_t* offsets, int G,
+                              int64_t rows_max, int cols, cudaStream_t s);
+cudaError_t launch_quant_cols(const void* X, void* Xq, const int32_t* offsets, int G,
+                              int64_t rows_max, int cols, cudaStream_t s);
+
+// Where the FP8 mode keeps its quantised tensors inside `scratch`.
+struct Fp8Scratch {
+  void* W13q;   // [G,2F,H]
+  void* W2q;    // [G,H,F]
+  void* aH;     // [R,H]  x_perm rows, then x_perm columns
+  void* bF;     // [R,F]  h rows, then h columns
+  void* cH;     // [R,H]  dO rows, then dO columns
+  void* d2F;    // [R,2F] dGU rows, then dGU columns
+};
+Fp8Scratch fp8_scratch(const moe_config& c, void* scratch);
+
 // Grouped GEMMs (tcgen05). Return cudaErrorInvalidValue when a tensor map
 // cannot be encoded for the given pointers.
 cudaError_t launch_ffn_fc1(const moe_config& c, const void* x_perm, const int32_t* counts,

@@ -39,8 +39,38 @@ int num_sms() {
   return cache[dev];
 }
 
+static int64_t align256(int64_t v) { return (v + 255) / 256 * 256; }
+
+static int64_t base_scratch_bytes(const moe_config& c) {
+  return align256((int64_t)kScratchHist + (int64_t)n_chunks(c) * c.E * 4 + 256);
+}
+
 int64_t scratch_bytes(const moe_config& c) {
-  return (int64_t)kScratchHist + (int64_t)n_chunks(c) * c.E * 4 + 256;
+  int64_t b = base_scratch_bytes(c);
+  if (c.dtype == MOE_DTYPE_FP8_E4M3_BLOCK) {
+    const int64_t G = c.E + c.n_shared, R = rows_max(c), H = c.H, F = c.F;
+    b += align256(G * 2 * F * H * 2) + align256(G * H * F * 2);
+    b += 2 * align256(R * H * 2) + align256(R * F * 2) + align256(R * 2 * F * 2);
+  }
+  return b;
+}
+
+Fp8Scratch fp8_scratch(const moe_config& c, void* scratch) {
+  const int64_t G = c.E + c.n_shared, R = rows_max(c), H = c.H, F = c.F;
+  uint8_t* p = static_cast<uint8_t*>(scratch) + base_scratch_bytes(c);
+  Fp8Scratch f;
+  f.W13q = p;
+  p += align256(G * 2 * F * H * 2);
+  f.W2q = p;
+  p += align256(G * H * F * 2);
+  f.aH = p;
+  p += align256(R * H * 2);
+  f.bF = p;
+  p += align256(R * F * 2);
+  f.cH = p;
+  p += align256(R * H * 2);
+  f.d2F = p;
+  return f;
 }
 
 moe_status check_config(const moe_config* c) {
@@ -59,7 +89,9 @@ moe_status check_config(const moe_config* c) {
   if (!(c->capacity_factor >= 0.f) || !isfinite(c->capacity_factor)) return MOE_ERR_INVALID_ARG;
   if (!isfinite(c->route_scale)) return MOE_ERR_INVALID_ARG;
   if (c->row_align < 128 || c->row_align % 128) return MOE_ERR_INVALID_ARG;
-  if (c->dtype != MOE_DTYPE_BF16) return MOE_ERR_UNSUPPORTED;
+  if (c->dtype != MOE_DTYPE_BF16 && c->dtype != MOE_DTYPE_FP8_E4M3_BLOCK)
+    return MOE_ERR_INVALID_ARG;
+  if (c->dtype == MOE_DTYPE_FP8_E4M3_BLOCK && c->n_shared != 0) return MOE_ERR_UNSUPPORTED;
   if ((int64_t)c->T * c->k >= (1LL << 31) || rows_max(*c) >= (1LL << 31))
     return MOE_ERR_INVALID_ARG;
   if ((int64_t)c->E * 2 * c->F >= (1LL << 31) || (int64_t)(c->E + c->n_shared) * c->H >= (1LL << 31))
@@ -148,6 +180,18 @@ moe_status moe_grouped_ffn_fwd(const moe_config* cfg, const void* x_perm, const 
   MOE_REQUIRE(al16(GU) && al16(h) && al16(y_perm) && al16(scratch));
   cudaStream_t s = (cudaStream_t)stream;
   int32_t* st = status_word(scratch);
+  if (cfg->dtype == MOE_DTYPE_FP8_E4M3_BLOCK) {
+    const Fp8Scratch q = fp8_scratch(*cfg, scratch);
+    const int G = cfg->E + cfg->n_shared;
+    const int64_t R = rows_max(*cfg);
+    MOE_CUDA(launch_quant_tiles(W13, q.W13q, G, 2 * cfg->F, cfg->H, s));
+    MOE_CUDA(launch_quant_tiles(W2, q.W2q, G, cfg->H, cfg->F, s));
+    MOE_CUDA(launch_quant_rows(x_perm, q.aH, offsets, G, R, cfg->H, s));
+    MOE_CUDA(launch_ffn_fc1(*cfg, q.aH, counts, offsets, q.W13q, GU, h, st, s));
+    MOE_CUDA(launch_quant_rows(h, q.bF, offsets, G, R, cfg->F, s));
+    MOE_CUDA(launch_ffn_fc2(*cfg, q.bF, counts, offsets, q.W2q, y_perm, st, s));
+    return MOE_OK;
+  }
   MOE_CUDA(launch_ffn_fc1(*cfg, x_perm, counts, offsets, W13, GU, h, st, s));
   MOE_CUDA(launch_ffn_fc2(*cfg, h, counts, offsets, W2, y_perm, st, s));
   return MOE_OK;
@@ -183,6 +227,24 @@ moe_status moe_grouped_ffn_bwd(const moe_config* cfg, const void* dO_perm, const
   MOE_REQUIRE(al16(dW13) && al16(dW2) && al16(scratch));
   cudaStream_t s = (cudaStream_t)stream;
   int32_t* st = status_word(scratch);
+  if (cfg->dtype == MOE_DTYPE_FP8_E4M3_BLOCK) {
+    // the quantised weights are the ones the forward left in scratch
+    const Fp8Scratch q = fp8_scratch(*cfg, scratch);
+    const int G = cfg->E + cfg->n_shared;
+    const int64_t R = rows_max(*cfg);
+    const int H = cfg->H, F = cfg->F;
+    MOE_CUDA(launch_quant_rows(dO_perm, q.cH, offsets, G, R, H, s));
+    MOE_CUDA(launch_ffn_fc2_dgrad(*cfg, q.cH, counts, offsets, q.W2q, GU, dGU, st, s));
+    MOE_CUDA(launch_quant_cols(dO_perm, q.cH, offsets, G, R, H, s));
+    MOE_CUDA(launch_quant_cols(h, q.bF, offsets, G, R, F, s));
+    MOE_CUDA(launch_ffn_wgrad_fc2(*cfg, q.cH, q.bF, counts, offsets, dW2, st, s));
+    MOE_CUDA(launch_quant_rows(dGU, q.d2F, offsets, G, R, 2 * F, s));
+    MOE_CUDA(launch_ffn_fc1_dgrad(*cfg, q.d2F, counts, offsets, q.W13q, dX_perm, st, s));
+    MOE_CUDA(launch_quant_cols(dGU, q.d2F, offsets, G, R, 2 * F, s));
+    MOE_CUDA(launch_quant_cols(x_perm, q.aH, offsets, G, R, H, s));
+    MOE_CUDA(launch_ffn_wgrad_fc1(*cfg, q.d2F, q.aH, counts, offsets, dW13, st, s));
+    return MOE_OK;
+  }
   MOE_CUDA(launch_ffn_fc2_dgrad(*cfg, dO_perm, counts, offsets, W2, GU, dGU, st, s));
   MOE_CUDA(launch_ffn_wgrad_fc2(*cfg, dO_perm, h, counts, offsets, dW2, st, s));
   MOE_CUDA(launch_ffn_fc1_dgrad(*cfg, dGU, counts, offsets, W13, dX_perm, st, s));

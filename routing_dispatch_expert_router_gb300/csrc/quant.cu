@@ -1,0 +1,185 @@
+// FP8 E4M3 block quantisation for the FP8 layer configuration.
+//
+// "Scalable Training of Mixture-of-Experts Models with Megatron Core" (es
+// summary, Resumen técnico §2.4) quantises the expert GEMMs and their
+// activations to FP8 (MXFP8 on Blackwell) while the router stays in high
+// precision. Here every GEMM operand is replaced by its E4M3 value times a
+// power-of-two block scale, scale = 2^ceil(log2(amax/448)) (1 for an all-zero
+// block):
+//   tiles  128 x 128 blocks of the expert weights,
+//   rows   1 x 128 slices along a row (activations entering a GEMM that
+//          reduces along that row),
+//   cols   128 x 1 slices along the tokens of each 128-row block of the
+//          permuted buffer (weight-gradient operands).
+// The quantised values are written back as bf16, which holds every E4M3 value
+// times a power of two exactly, so the tcgen05 bf16 GEMMs that consume them
+// form exactly the products an FP8 block-scaled MMA would (fp32 accumulation).
+// E4M3 rounding (to nearest even, saturating) uses the hardware conversion.
+#include <cuda_fp16.h>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace moe {
+
+__device__ __forceinline__ float e4m3_scale(float amax) {
+  if (!(amax > 0.f)) return 1.f;
+  int e;
+  const float m = frexpf(__fdiv_rn(amax, 448.f), &e);   // amax/448 = m * 2^e
+  return ldexpf(1.f, m == 0.5f ? e - 1 : e);
+}
+
+// E4M3(a / s) * s for two values (s a power of two, so a / s and the product
+// are exact).
+__device__ __forceinline__ void q2(float a, float b, float inv_s, float s, float& qa, float& qb) {
+  uint16_t packed;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(packed) : "f"(b * inv_s), "f"(a * inv_s));
+  uint32_t h2;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(packed));
+  const __half2 hv = *reinterpret_cast<const __half2*>(&h2);
+  qa = __low2float(hv) * s;
+  qb = __high2float(hv) * s;
+}
+
+__device__ __forceinline__ float q1(float a, float inv_s, float s) {
+  float qa, unused;
+  q2(a, 0.f, inv_s, s, qa, unused);
+  return qa;
+}
+
+__device__ __forceinline__ uint4 quant8(const float (&f)[8], float s) {
+  const float inv = 1.f / s;                              // exact: s is a power of two
+  float o[8];
+#pragma unroll
+  for (int i = 0; i < 8; i += 2) q2(f[i], f[i + 1], inv, s, o[i], o[i + 1]);
+  return pack8(o);
+}
+
+__device__ __forceinline__ float amax8(const float (&f)[8]) {
+  float m = 0.f;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) m = fmaxf(m, fabsf(f[i]));
+  return m;
+}
+
+// 128 x 128 tiles: one block per tile, thread owns 8 vectors of 8 elements.
+__global__ void __launch_bounds__(256)
+quant_tiles_kernel(const __nv_bfloat16* __restrict__ W, __nv_bfloat16* __restrict__ Wq,
+                   long long n_tiles, int rows, int cols) {
+  __shared__ float red[8];
+  const int tc = cols / 128, tr = rows / 128;
+  for (long long tile = blockIdx.x; tile < n_tiles; tile += gridDim.x) {
+    const long long g = tile / ((long long)tr * tc);
+    const int rem = (int)(tile % ((long long)tr * tc));
+    const int r0 = (rem / tc) * 128, c0 = (rem % tc) * 128;
+    const size_t base = (size_t)g * rows * cols;
+    float f[8][8];
+    float m = 0.f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int v = threadIdx.x + 256 * i;                // 2048 vectors per tile
+      const int r = v >> 4, c = (v & 15) * 8;
+      unpack8(ldg_nc_v4(W + base + (size_t)(r0 + r) * cols + c0 + c), f[i]);
+      m = fmaxf(m, amax8(f[i]));
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = m;
+    __syncthreads();
+    float amax = red[0];
+#pragma unroll
+    for (int i = 1; i < 8; ++i) amax = fmaxf(amax, red[i]);
+    const float s = e4m3_scale(amax);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int v = threadIdx.x + 256 * i;
+      const int r = v >> 4, c = (v & 15) * 8;
+      stg_v4(Wq + base + (size_t)(r0 + r) * cols + c0 + c, quant8(f[i], s));
+    }
+    __syncthreads();
+  }
+}
+
+// 1 x 128 slices of rows [0, offsets[G]): 16 lanes per slice.
+__global__ void __launch_bounds__(256)
+quant_rows_kernel(const __nv_bfloat16* __restrict__ X, __nv_bfloat16* __restrict__ Xq,
+                  const int32_t* __restrict__ offsets, int G, int cols) {
+  const long long rows = offsets[G];
+  const int nvec = cols >> 3;
+  const long long n = rows * nvec;                        // nvec is a multiple of 16
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n;
+       i += (long long)gridDim.x * blockDim.x) {
+    float f[8];
+    unpack8(ldg_nc_v4(X + i * 8), f);
+    float m = amax8(f);
+    // the 16 lanes of this half-warp hold one 128-element slice; n is a
+    // multiple of 16, so a half-warp is either wholly in range or wholly out
+    const unsigned half = (threadIdx.x & 16) ? 0xffff0000u : 0x0000ffffu;
+#pragma unroll
+    for (int o = 8; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(half, m, o));
+    stg_v4(Xq + i * 8, quant8(f, e4m3_scale(m)));
+  }
+}
+
+// 128 x 1 slices: every 128-row block of [0, offsets[G]) (group segments are
+// multiples of 128 rows, so blocks never straddle two experts), thread owns
+// two adjacent columns of one block.
+__global__ void __launch_bounds__(256)
+quant_cols_kernel(const __nv_bfloat16* __restrict__ X, __nv_bfloat16* __restrict__ Xq,
+                  const int32_t* __restrict__ offsets, int G, int cols) {
+  const long long rblocks = offsets[G] / 128;
+  const int cpairs = cols >> 1;
+  const long long n = rblocks * cpairs;
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n;
+       i += (long long)gridDim.x * blockDim.x) {
+    const long long rb = i / cpairs;
+    const int c = (int)(i % cpairs) * 2;
+    const __nv_bfloat16* src = X + (size_t)rb * 128 * cols + c;
+    float m0 = 0.f, m1 = 0.f;
+#pragma unroll 8
+    for (int r = 0; r < 128; ++r) {
+      const uint32_t v = *reinterpret_cast<const uint32_t*>(src + (size_t)r * cols);
+      m0 = fmaxf(m0, fabsf(bf16_lo(v)));
+      m1 = fmaxf(m1, fabsf(bf16_hi(v)));
+    }
+    const float s0 = e4m3_scale(m0), s1 = e4m3_scale(m1);
+    const float i0 = 1.f / s0, i1 = 1.f / s1;
+    __nv_bfloat16* dst = Xq + (size_t)rb * 128 * cols + c;
+#pragma unroll 8
+    for (int r = 0; r < 128; ++r) {
+      const uint32_t v = *reinterpret_cast<const uint32_t*>(src + (size_t)r * cols);
+      *reinterpret_cast<uint32_t*>(dst + (size_t)r * cols) =
+          pack_bf16x2(q1(bf16_lo(v), i0, s0), q1(bf16_hi(v), i1, s1));
+    }
+  }
+}
+
+static int grid_cap(long long work_items, int per_block) {
+  long long b = (work_items + per_block - 1) / per_block;
+  const long long cap = (long long)num_sms() * 16;
+  if (b > cap) b = cap;
+  return b > 0 ? (int)b : 1;
+}
+
+cudaError_t launch_quant_tiles(const void* W, void* Wq, int G, int rows, int cols, cudaStream_t s) {
+  const long long n = (long long)G * (rows / 128) * (cols / 128);
+  quant_tiles_kernel<<<grid_cap(n, 1), 256, 0, s>>>(static_cast<const __nv_bfloat16*>(W),
+                                                    static_cast<__nv_bfloat16*>(Wq), n, rows, cols);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_quant_rows(const void* X, void* Xq, const int32_t* offsets, int G,
+                              int64_t rows_max, int cols, cudaStream_t s) {
+  quant_rows_kernel<<<grid_cap(rows_max * (cols / 8), 256), 256, 0, s>>>(
+      static_cast<const __nv_bfloat16*>(X), static_cast<__nv_bfloat16*>(Xq), offsets, G, cols);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_quant_cols(const void* X, void* Xq, const int32_t* offsets, int G,
+                              int64_t rows_max, int cols, cudaStream_t s) {
+  quant_cols_kernel<<<grid_cap(rows_max / 128 * (cols / 2), 256), 256, 0, s>>>(
+      static_cast<const __nv_bfloat16*>(X), static_cast<__nv_bfloat16*>(Xq), offsets, G, cols);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

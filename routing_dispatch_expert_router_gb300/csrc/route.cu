@@ -77,58 +77,72 @@ route_logits_kernel(const __nv_bfloat16* __restrict__ x, const float* __restrict
   }
 }
 
-// Few experts (E <= 16): the logits are a pure stream over x. One warp owns 4
-// consecutive tokens; each lane walks its 16-byte slices of the 4 rows (4
-// loads in flight per step, two steps unrolled) and multiplies them with the
-// matching W_r slices, which are shared by the 4 tokens. Per-lane partial sums
-// are combined by a fixed butterfly, so the summation order is deterministic.
+// Few experts (E <= 16): the logits are a pure stream over x. A block of 4
+// warps owns 4 consecutive tokens; warp w walks the w-th quarter of H, each
+// lane loading 16-byte slices of the 4 rows (two slices in flight per row)
+// and the matching W_r slices, which the 4 tokens share. Lane partial sums are
+// combined by a fixed butterfly, then the 4 warps' sums in warp order, so the
+// summation order is deterministic.
 template <int EP>
-__global__ void __launch_bounds__(256)
+__global__ void __launch_bounds__(128)
 route_logits_few_kernel(const __nv_bfloat16* __restrict__ x, const float* __restrict__ W,
                         float* __restrict__ logits, int T, int H, int E) {
-  constexpr int TPW = 4;
-  const int lane = threadIdx.x & 31;
-  const int t0 = (blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5)) * TPW;
-  if (t0 >= T) return;
-  float acc[TPW][EP];
+  constexpr int TPB = 4;
+  __shared__ float part[4][TPB][EP];
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  const int t0 = blockIdx.x * TPB;
+  float acc[TPB][EP];
 #pragma unroll
-  for (int i = 0; i < TPW; ++i)
+  for (int i = 0; i < TPB; ++i)
 #pragma unroll
     for (int e = 0; e < EP; ++e) acc[i][e] = 0.f;
-  const int nvec = H >> 3;
-  for (int c = lane; c < nvec; c += 32) {
-    float xf[TPW][8];
+  const int nvec = H >> 3, per = nvec >> 2;
+  const int cbeg = wid * per, cend = cbeg + per;
+  for (int c0 = cbeg + lane; c0 < cend; c0 += 64) {
+    float xf[2][TPB][8];
 #pragma unroll
-    for (int i = 0; i < TPW; ++i) {
-      if (t0 + i < T) unpack8(ldg_nc_v4(x + (size_t)(t0 + i) * H + (size_t)c * 8), xf[i]);
-      else {
+    for (int u = 0; u < 2; ++u) {
+      const int c = c0 + 32 * u;
 #pragma unroll
-        for (int q = 0; q < 8; ++q) xf[i][q] = 0.f;
+      for (int i = 0; i < TPB; ++i) {
+        if (c < cend && t0 + i < T) {
+          unpack8(ldg_nc_v4(x + (size_t)(t0 + i) * H + (size_t)c * 8), xf[u][i]);
+        } else {
+#pragma unroll
+          for (int q = 0; q < 8; ++q) xf[u][i][q] = 0.f;
+        }
       }
     }
 #pragma unroll
-    for (int e = 0; e < EP; ++e) {
-      if (e >= E) break;
-      const float4* wp = reinterpret_cast<const float4*>(W + (size_t)e * H + (size_t)c * 8);
-      const float4 a = __ldg(wp), b = __ldg(wp + 1);
-      const float wv[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+    for (int u = 0; u < 2; ++u) {
+      const int c = c0 + 32 * u;
+      if (c >= cend) break;
 #pragma unroll
-      for (int i = 0; i < TPW; ++i)
+      for (int e = 0; e < EP; ++e) {
+        if (e >= E) break;
+        const float4* wp = reinterpret_cast<const float4*>(W + (size_t)e * H + (size_t)c * 8);
+        const float4 a = __ldg(wp), b = __ldg(wp + 1);
+        const float wv[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
 #pragma unroll
-        for (int q = 0; q < 8; ++q) acc[i][e] = fmaf(xf[i][q], wv[q], acc[i][e]);
+        for (int i = 0; i < TPB; ++i)
+#pragma unroll
+          for (int q = 0; q < 8; ++q) acc[i][e] = fmaf(xf[u][i][q], wv[q], acc[i][e]);
+      }
     }
   }
 #pragma unroll
-  for (int i = 0; i < TPW; ++i)
+  for (int i = 0; i < TPB; ++i)
 #pragma unroll
-    for (int e = 0; e < EP; ++e) acc[i][e] = warp_sum(acc[i][e]);
-  if (lane == 0) {
-#pragma unroll
-    for (int i = 0; i < TPW; ++i) {
-      if (t0 + i >= T) break;
-#pragma unroll
-      for (int e = 0; e < EP; ++e)
-        if (e < E) logits[(size_t)(t0 + i) * E + e] = acc[i][e];
+    for (int e = 0; e < EP; ++e) {
+      const float v = warp_sum(acc[i][e]);
+      if (lane == 0) part[wid][i][e] = v;
+    }
+  __syncthreads();
+  if (threadIdx.x < TPB * EP) {
+    const int i = threadIdx.x / EP, e = threadIdx.x % EP;
+    if (e < E && t0 + i < T) {
+      const float v = ((part[0][i][e] + part[1][i][e]) + part[2][i][e]) + part[3][i][e];
+      logits[(size_t)(t0 + i) * E + e] = v;
     }
   }
 }
@@ -296,11 +310,11 @@ cudaError_t launch_route(const moe_config& c, const void* x, const float* W_r, c
                          float* logits, int32_t* idx, float* w, cudaStream_t s) {
   const __nv_bfloat16* xb = static_cast<const __nv_bfloat16*>(x);
   if (c.E <= 16) {
-    const int blocks = (c.T + 31) / 32;      // 8 warps x 4 tokens
+    const int blocks = (c.T + 3) / 4;        // 4 tokens per block of 4 warps
     if (c.E <= 8)
-      route_logits_few_kernel<8><<<blocks, 256, 0, s>>>(xb, W_r, logits, c.T, c.H, c.E);
+      route_logits_few_kernel<8><<<blocks, 128, 0, s>>>(xb, W_r, logits, c.T, c.H, c.E);
     else
-      route_logits_few_kernel<16><<<blocks, 256, 0, s>>>(xb, W_r, logits, c.T, c.H, c.E);
+      route_logits_few_kernel<16><<<blocks, 128, 0, s>>>(xb, W_r, logits, c.T, c.H, c.E);
   } else {
     dim3 grid((c.T + 63) / 64, (c.E + 63) / 64);
     route_logits_kernel<64, 64><<<grid, 256, 0, s>>>(xb, W_r, logits, c.T, c.H, c.E);

@@ -88,8 +88,22 @@ def run_layer(shape, inp: dict, backward: bool = True, device: str = "cuda") -> 
     return res
 
 
+def _ident(a):
+    return a
+
+
 def check_steps(shape, inp: dict, g: dict, backward: bool = True):
-    """Every step of the GPU path against the oracle fed the GPU's step inputs."""
+    """Every step of the GPU path against the oracle fed the GPU's step inputs.
+
+    In the FP8 configuration the oracle quantises those inputs the way the
+    layer does (weights in 128x128 tiles, activations in 1x128 slices along
+    the reduction, weight-gradient operands in 128x1 slices along tokens);
+    quantising identical inputs is exact on both sides, so the same per-element
+    tolerance applies."""
+    fp8 = getattr(shape, "dtype", 0) == 1
+    qr = O.quant_rows if fp8 else _ident
+    qc = O.quant_cols if fp8 else _ident
+    qt = O.quant_tiles if fp8 else _ident
     T, H, E, k, F, S = shape.T, shape.H, shape.E, shape.k, shape.F, shape.n_shared
     G = E + S
     x = f64(inp["x"])
@@ -127,12 +141,12 @@ def check_steps(shape, inp: dict, g: dict, backward: bool = True):
         if cnt[gi] == 0:
             continue
         rows = slice(off[gi], off[gi] + cnt[gi])
-        w13 = f64(W13[gi])
-        w2 = f64(W2[gi])
-        gu_ref, h_ref = O.expert_fc1(xp[rows], w13)
+        w13 = qt(f64(W13[gi]))
+        w2 = qt(f64(W2[gi]))
+        gu_ref, h_ref = O.expert_fc1(qr(xp[rows]), w13)
         assert_close(f"GU[g={gi}]", GU[rows], gu_ref)
         assert_close(f"h[g={gi}]", hh[rows], O.round_bf16(O.silu(GU[rows, :F]) * GU[rows, F:]))
-        assert_close(f"y[g={gi}]", yp[rows], O.expert_fc2(hh[rows], w2))
+        assert_close(f"y[g={gi}]", yp[rows], O.expert_fc2(qr(hh[rows]), w2))
     # a7 combine on the GPU's y and weights
     wg = f64(g["w"])
     rof = m["row_of"]
@@ -169,17 +183,18 @@ def check_steps(shape, inp: dict, g: dict, backward: bool = True):
     dW13 = g["dW13"]
     dW2 = g["dW2"]
     for gi in range(G):
-        w13 = f64(W13[gi])
-        w2 = f64(W2[gi])
+        w13 = qt(f64(W13[gi]))
+        w2 = qt(f64(W2[gi]))
         if cnt[gi] == 0:
             assert_equal(f"dW2[g={gi}] empty", f64(dW2[gi]), np.zeros((H, F)))
             assert_equal(f"dW13[g={gi}] empty", f64(dW13[gi]), np.zeros((2 * F, H)))
             continue
         rows = slice(off[gi], off[gi] + cnt[gi])
-        assert_close(f"dGU[g={gi}]", dGU[rows], O.expert_fc2_dgrad_swiglu(dO[rows], w2, GU[rows]))
-        assert_close(f"dX[g={gi}]", dX[rows], O.expert_fc1_dgrad(dGU[rows], w13))
-        assert_close(f"dW2[g={gi}]", f64(dW2[gi]), O.wgrad(dO[rows], hh[rows]))
-        assert_close(f"dW13[g={gi}]", f64(dW13[gi]), O.wgrad(dGU[rows], xp[rows]))
+        assert_close(f"dGU[g={gi}]", dGU[rows],
+                     O.expert_fc2_dgrad_swiglu(qr(dO[rows]), w2, GU[rows]))
+        assert_close(f"dX[g={gi}]", dX[rows], O.expert_fc1_dgrad(qr(dGU[rows]), w13))
+        assert_close(f"dW2[g={gi}]", f64(dW2[gi]), O.wgrad(qc(dO[rows]), qc(hh[rows])))
+        assert_close(f"dW13[g={gi}]", f64(dW13[gi]), O.wgrad(qc(dGU[rows]), qc(xp[rows])))
     # a13 + router dx
     acc = np.zeros((T, H))
     for j in range(k):
@@ -210,3 +225,31 @@ def check_end_to_end(shape, inp: dict, g: dict, backward: bool = True):
     assert_close("dW13 (e2e)", f64(g["dW13"]), bwd["dW13"])
     assert_close("dW2 (e2e)", f64(g["dW2"]), bwd["dW2"])
     assert_close("dW_r (e2e)", f64(g["dW_r"]), bwd["dW_r"], atol=1e-2, rtol=1e-2)
+
+
+def assert_close_fp8(name, got, ref, rel=5e-2):
+    """The FP8 rule: |gpu-ref| <= rel*(|ref| + rms(ref)) per element and a
+    relative Frobenius error <= rel over the tensor."""
+    got = np.asarray(got, np.float64)
+    ref = np.asarray(ref, np.float64)
+    rms = float(np.sqrt(np.mean(ref ** 2))) if ref.size else 0.0
+    assert_close(name, got, ref, atol=0.0, rtol=rel, scale=np.abs(ref) + rms)
+    den = float(np.linalg.norm(ref))
+    if den > 0:
+        fro = float(np.linalg.norm(got - ref)) / den
+        assert fro <= rel, f"{name}: relative Frobenius error {fro:.3g} > {rel}"
+
+
+def check_end_to_end_fp8(shape, inp: dict, g: dict):
+    """The FP8 layer against the oracle's FP8 layer run from the raw inputs."""
+    x = f64(inp["x"])
+    Wr = f64(inp["W_r"])
+    bias = None if inp["bias"] is None else f64(inp["bias"])
+    W13 = f64(inp["W13"])
+    W2 = f64(inp["W2"])
+    fwd = O.layer_forward_fp8(shape, x, Wr, bias, W13, W2, logits=f64(g["logits"]))
+    assert_equal("idx (fp8 e2e)", i64(g["idx"]), fwd["idx"])
+    assert_close_fp8("out (fp8 e2e)", f64(g["out"]), fwd["out"])
+    bwd = O.layer_backward_fp8(shape, x, Wr, W13, W2, fwd, f64(inp["dY"]))
+    for n in ("dx", "dW13", "dW2", "dW_r"):
+        assert_close_fp8(f"{n} (fp8 e2e)", f64(g[n]), bwd[n])

@@ -59,10 +59,18 @@ def test_invalid_configs_rejected(bad):
     assert e.value.code == 1
 
 
-def test_fp8_dtype_reported_unsupported():
-    with pytest.raises(B.MoEError) as e:
-        B.moe_query_sizes(DSV3_FP8)
+def test_fp8_scratch_holds_the_quantised_operands():
+    s = B.moe_query_sizes(DSV3_FP8)
+    G, R, H, F = 256, 256 * 640, 7168, 2048
+    quantised = G * 2 * F * H * 2 + G * H * F * 2 + (2 * R * H + R * F + R * 2 * F) * 2
+    assert s.capacity == 640 and s.rows_max == R
+    assert quantised <= s.scratch_bytes <= quantised + (1 << 20)
+    with pytest.raises(B.MoEError) as e:           # shared experts: not in FP8 mode
+        B.moe_query_sizes(DSV3_FP8.with_(n_shared=1))
     assert e.value.code == 2
+    with pytest.raises(B.MoEError) as e:
+        B.moe_query_sizes(DSV3_FP8.with_(dtype=7))
+    assert e.value.code == 1
 
 
 def test_null_and_misaligned_pointers_rejected_before_launch():

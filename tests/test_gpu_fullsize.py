@@ -22,7 +22,7 @@ import pytest
 import torch
 
 from oracle import moe_oracle as O
-from workloads import DSV3, MIXTRAL, QWEN3, make_inputs
+from workloads import DSV3, DSV3_FP8, MIXTRAL, QWEN3, make_inputs
 
 import harness as H_
 
@@ -46,9 +46,14 @@ def pick_groups(counts, E, S, rng, n_random=3):
     return sorted(gs)
 
 
-@pytest.mark.parametrize("shape", [MIXTRAL, QWEN3, DSV3], ids=lambda s: s.name)
+@pytest.mark.parametrize("shape", [MIXTRAL, QWEN3, DSV3, DSV3_FP8], ids=lambda s: s.name)
 def test_full_size_layer_matches_oracle_on_samples(shape):
     torch.cuda.empty_cache()
+    fp8 = shape.dtype == 1
+    ident = lambda a: a  # noqa: E731
+    qr = O.quant_rows if fp8 else ident
+    qc = O.quant_cols if fp8 else ident
+    qt = O.quant_tiles if fp8 else ident
     inp = make_inputs(shape, seed=0, device="cuda")
     g = H_.run_layer(shape, inp)
     rng = np.random.default_rng(0)
@@ -91,28 +96,29 @@ def test_full_size_layer_matches_oracle_on_samples(shape):
         n = int(cnt[gi])
         sel = np.sort(rng.choice(n, size=min(n, 48), replace=False)) + off[gi]
         rs = torch.as_tensor(sel, device="cuda")
-        w13, w2 = group_weights(inp, gi)
+        w13, w2 = (qt(a) for a in group_weights(inp, gi))
         xp = host(g["x_perm"][rs])
         GU = host(g["GU"][rs])
         hh = host(g["h"][rs])
-        gu_ref, _ = O.expert_fc1(xp, w13)
+        gu_ref, _ = O.expert_fc1(qr(xp), w13)
         H_.assert_close(f"GU g={gi}", GU, gu_ref)
         H_.assert_close(f"h g={gi}", hh, O.round_bf16(O.silu(GU[:, :F]) * GU[:, F:]))
-        H_.assert_close(f"y g={gi}", host(g["y_perm"][rs]), O.expert_fc2(hh, w2))
+        H_.assert_close(f"y g={gi}", host(g["y_perm"][rs]), O.expert_fc2(qr(hh), w2))
         dO = host(g["dO_perm"][rs])
         dGU = host(g["dGU"][rs])
-        H_.assert_close(f"dGU g={gi}", dGU, O.expert_fc2_dgrad_swiglu(dO, w2, GU))
-        H_.assert_close(f"dX g={gi}", host(g["dX_perm"][rs]), O.expert_fc1_dgrad(dGU, w13))
+        H_.assert_close(f"dGU g={gi}", dGU, O.expert_fc2_dgrad_swiglu(qr(dO), w2, GU))
+        H_.assert_close(f"dX g={gi}", host(g["dX_perm"][rs]), O.expert_fc1_dgrad(qr(dGU), w13))
         # weight gradients over all the group's rows, on sampled output rows
         allr = slice(int(off[gi]), int(off[gi]) + n)
         oh = rng.choice(Hd, size=32, replace=False)
         of = rng.choice(2 * F, size=32, replace=False)
-        dO_all = host(g["dO_perm"][allr][:, torch.as_tensor(oh, device="cuda")])
-        h_all = host(g["h"][allr])
+        # (128x1 quantisation is per column, so sampling columns commutes with it)
+        dO_all = qc(host(g["dO_perm"][allr][:, torch.as_tensor(oh, device="cuda")]))
+        h_all = qc(host(g["h"][allr]))
         H_.assert_close(f"dW2 g={gi}", host(g["dW2"][gi][torch.as_tensor(oh, device="cuda")]),
                         O.wgrad(dO_all, h_all))
-        dGU_all = host(g["dGU"][allr][:, torch.as_tensor(of, device="cuda")])
-        xp_all = host(g["x_perm"][allr])
+        dGU_all = qc(host(g["dGU"][allr][:, torch.as_tensor(of, device="cuda")]))
+        xp_all = qc(host(g["x_perm"][allr]))
         H_.assert_close(f"dW13 g={gi}", host(g["dW13"][gi][torch.as_tensor(of, device="cuda")]),
                         O.wgrad(dGU_all, xp_all))
     # ---- combine and its backward on sampled tokens (GPU step inputs)
@@ -166,14 +172,15 @@ def test_full_size_layer_matches_oracle_on_samples(shape):
         for j in range(k):
             if rof[t, j] < 0:
                 continue
-            w13, w2 = group_weights(inp, int(it[0, j]))
-            gu, hh = O.expert_fc1(xt, w13)
-            y = O.expert_fc2(hh, w2)
+            w13, w2 = (qt(a) for a in group_weights(inp, int(it[0, j])))
+            gu, hh = O.expert_fc1(qr(xt), w13)
+            y = O.expert_fc2(qr(hh), w2)
             acc += wt[0, j] * y[0]
             mag += np.abs(wt[0, j] * y[0])
             dw_t[j] = dy @ y[0]
             dO = O.round_bf16(wt[0, j] * dy[None, :])
-            dXs.append(O.expert_fc1_dgrad(O.expert_fc2_dgrad_swiglu(dO, w2, gu), w13)[0])
+            dG = O.expert_fc2_dgrad_swiglu(qr(dO), w2, gu)
+            dXs.append(O.expert_fc1_dgrad(qr(dG), w13)[0])
         for s in range(S):
             w13, w2 = group_weights(inp, E + s)
             gu, hh = O.expert_fc1(xt, w13)
@@ -182,11 +189,17 @@ def test_full_size_layer_matches_oracle_on_samples(shape):
             mag += np.abs(ys)
             dXs.append(O.expert_fc1_dgrad(O.expert_fc2_dgrad_swiglu(dy[None, :], w2, gu), w13)[0])
         ref = O.round_bf16(acc)
-        H_.assert_close(f"out e2e[{t}]", host(g["out"][int(t)]), ref, scale=np.abs(ref) + mag)
+        if fp8:
+            H_.assert_close_fp8(f"out e2e[{t}]", host(g["out"][int(t)]), ref)
+        else:
+            H_.assert_close(f"out e2e[{t}]", host(g["out"][int(t)]), ref, scale=np.abs(ref) + mag)
         dlt = O.router_dlogits(shape, lt, it, wt, dw_t[None, :])
         router = dlt[0] @ Wr
         ref = O.round_bf16(sum(dXs) + router)
         mag = np.abs(ref) + sum(np.abs(d) for d in dXs) + np.abs(router)
-        H_.assert_close(f"dx e2e[{t}]", host(g["dx"][int(t)]), ref, scale=mag)
+        if fp8:
+            H_.assert_close_fp8(f"dx e2e[{t}]", host(g["dx"][int(t)]), ref)
+        else:
+            H_.assert_close(f"dx e2e[{t}]", host(g["dx"][int(t)]), ref, scale=mag)
     del g, inp
     torch.cuda.empty_cache()
