@@ -39,6 +39,9 @@ constexpr int BM = 128;
 constexpr int BK = 64;                       // 64 bf16 = one 128-byte swizzle row
 constexpr int kThreads = 192;
 constexpr int kCtrlBytes = 5120;
+constexpr int kBoxBytes = 32 * 32 * 2;           // one 32 x 32 bf16 output box
+constexpr int kStageBytes = 3 * kBoxBytes;       // output staging per epilogue warp
+constexpr int kStageAll = 4 * kStageBytes;
 constexpr long long kWaitBudget = 4000000000LL;   // clock64 cycles (~2 s)
 
 enum Epi : int { kEpiSwigluFwd = 0, kEpiStore = 1, kEpiSwigluBwd = 2, kEpiWgrad = 3 };
@@ -69,7 +72,7 @@ struct Layout {
   static constexpr int B_BYTES = BN * BK * 2;
   static constexpr int STAGE = A_BYTES + B_BYTES;
   static constexpr int TILES = STAGES * STAGE;
-  static constexpr int SMEM = TILES + kCtrlBytes + 1024;
+  static constexpr int SMEM = TILES + kCtrlBytes + kStageAll + 1024;
   static constexpr int TMEM_COLS = 2 * BN;
 };
 
@@ -101,79 +104,79 @@ __device__ __forceinline__ Tile decode(int tile, const int* prefix, const int* m
 
 __device__ __forceinline__ float silu_f(float z) { return z / (1.f + expf(-z)); }
 
-// Drains one 128 x BN fp32 accumulator (this thread: row `rloc`, from tensor
-// memory at `tbase`) through the fused epilogue and stores bf16 results.
+// Output staging: every epilogue warp owns kStageBytes of shared memory for up
+// to three 32 x 32 bf16 boxes, laid out with the 64-byte swizzle that the
+// output tensor maps use (16-byte chunk j of row r sits at slot j ^ ((r>>1)&3),
+// so the 32 lanes' row writes hit distinct banks), stored to global memory by
+// TMA (coalesced, asynchronous).
+
+__device__ __forceinline__ void stage_row(uint8_t* stage, int box, int lane, const uint4 (&v)[4]) {
+  uint8_t* row = stage + box * kBoxBytes + lane * 64;
+  const int sw = (lane >> 1) & 3;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) *reinterpret_cast<uint4*>(row + ((j ^ sw) << 4)) = v[j];
+}
+
+__device__ __forceinline__ void pack_slice(const uint32_t (&r)[32], uint4 (&o)[4]) {
+#pragma unroll
+  for (int v = 0; v < 4; ++v) {
+    float f[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) f[i] = __uint_as_float(r[v * 8 + i]);
+    o[v] = pack8(f);
+  }
+}
+
+// Drains one 128 x BN fp32 accumulator through the fused epilogue. This warp
+// handles the accumulator rows q*32 .. q*32+31 (tensor-memory lane quarter q,
+// lane = row within the quarter) starting at `tbase`.
 //   mt: m-tile of the group (rows offsets[g] + 128*mt, or output rows 128*mt
-//       for weight gradients); nt: n-tile; nk: k-blocks accumulated (0 = the
-//       accumulator was never written: weight gradients of empty groups).
+//       of group g for weight gradients); nt: n-tile; nk: k-blocks accumulated
+//       (0 = the accumulator was never written: weight gradients of empty groups).
 template <int EPI, int BN>
-__device__ __forceinline__ void epilogue_tile(const Params& p, uint32_t tbase, int g, int mt,
-                                              int nt, int nk, int rloc, const int* s_off) {
-  if (EPI == kEpiSwigluFwd) {
-    const long long row = s_off[g] + mt * BM + rloc;
-    const int f0 = nt * (BN / 2);
-    __nv_bfloat16* gu = p.out + row * p.ldo;
-    __nv_bfloat16* hr = p.out2 + row * p.ldo2;
-#pragma unroll 1
-    for (int c = 0; c < BN / 2; c += 32) {
-      uint32_t rg[32], ru[32];
-      ptx::tmem_ld32(tbase + c, rg);
-      ptx::tmem_ld32(tbase + BN / 2 + c, ru);
-      ptx::tmem_ld_wait();
-#pragma unroll
-      for (int v = 0; v < 4; ++v) {
-        float gf[8], uf[8], hf[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          gf[i] = __uint_as_float(rg[v * 8 + i]);
-          uf[i] = __uint_as_float(ru[v * 8 + i]);
-        }
-        const uint4 gb = pack8(gf), ub = pack8(uf);
-        float gr[8], ur[8];
-        unpack8(gb, gr);
-        unpack8(ub, ur);
-#pragma unroll
-        for (int i = 0; i < 8; ++i) hf[i] = silu_f(gr[i]) * ur[i];
-        stg_v4(gu + f0 + c + v * 8, gb);
-        stg_v4(gu + p.F + f0 + c + v * 8, ub);
-        stg_v4(hr + f0 + c + v * 8, pack8(hf));
-      }
-    }
-  } else if (EPI == kEpiStore) {
-    const long long row = s_off[g] + mt * BM + rloc;
-    __nv_bfloat16* o = p.out + row * p.ldo + nt * BN;
-#pragma unroll 1
-    for (int c = 0; c < BN; c += 32) {
-      uint32_t r[32];
-      ptx::tmem_ld32(tbase + c, r);
-      ptx::tmem_ld_wait();
-#pragma unroll
-      for (int v = 0; v < 4; ++v) {
-        float f[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) f[i] = __uint_as_float(r[v * 8 + i]);
-        stg_v4(o + c + v * 8, pack8(f));
-      }
-    }
-  } else if (EPI == kEpiSwigluBwd) {
-    const long long row = s_off[g] + mt * BM + rloc;
-    const int f0 = nt * BN;
-    const __nv_bfloat16* gu = p.aux + row * p.ldaux;
-    __nv_bfloat16* o = p.out + row * p.ldo;
-    // G and U of the next 32 columns are loaded one slice ahead, before this
-    // slice's stores, so the loads overlap the math and the stores
-    uint4 gq[4], uq[4];
+__device__ __forceinline__ void epilogue_tile(const Params& p, const CUtensorMap* tmC,
+                                              const CUtensorMap* tmC2, uint32_t tbase, int g,
+                                              int mt, int nt, int nk, int q, int lane,
+                                              const int* s_off, uint8_t* stage,
+                                              uint32_t stage_u32) {
+  const int row0 = (EPI == kEpiWgrad) ? g * p.Mw + mt * BM + q * 32 : s_off[g] + mt * BM + q * 32;
+  const int ncols = (EPI == kEpiSwigluFwd) ? BN / 2 : BN;
+  const int f0 = (EPI == kEpiSwigluFwd) ? nt * (BN / 2) : nt * BN;
+  uint4 gq[4], uq[4];
+  const __nv_bfloat16* gu = nullptr;
+  if (EPI == kEpiSwigluBwd) {
+    // G and U of the next 32 columns are loaded one slice ahead
+    gu = p.aux + (long long)(row0 + lane) * p.ldaux;
 #pragma unroll
     for (int v = 0; v < 4; ++v) {
       gq[v] = ldg_nc_v4(gu + f0 + v * 8);
       uq[v] = ldg_nc_v4(gu + p.F + f0 + v * 8);
     }
+  }
 #pragma unroll 1
-    for (int c = 0; c < BN; c += 32) {
+  for (int c = 0; c < ncols; c += 32) {
+    uint4 o0[4], o1[4], o2[4];
+    if (EPI == kEpiSwigluFwd) {
+      uint32_t rg[32], ru[32];
+      ptx::tmem_ld32(tbase + c, rg);
+      ptx::tmem_ld32(tbase + BN / 2 + c, ru);
+      ptx::tmem_ld_wait();
+      pack_slice(rg, o0);
+      pack_slice(ru, o1);
+#pragma unroll
+      for (int v = 0; v < 4; ++v) {
+        float gr[8], ur[8], hf[8];
+        unpack8(o0[v], gr);
+        unpack8(o1[v], ur);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) hf[i] = silu_f(gr[i]) * ur[i];
+        o2[v] = pack8(hf);
+      }
+    } else if (EPI == kEpiSwigluBwd) {
       uint32_t r[32];
       ptx::tmem_ld32(tbase + c, r);
       uint4 gn[4], un[4];
-      const int cn = (c + 32 < BN) ? c + 32 : c;
+      const int cn = (c + 32 < ncols) ? c + 32 : c;
 #pragma unroll
       for (int v = 0; v < 4; ++v) {
         gn[v] = ldg_nc_v4(gu + f0 + cn + v * 8);
@@ -192,35 +195,42 @@ __device__ __forceinline__ void epilogue_tile(const Params& p, uint32_t tbase, i
           dg[i] = dh * uf[i] * sg * (1.f + gf[i] * (1.f - sg));
           du[i] = dh * gf[i] * sg;
         }
-        stg_v4(o + f0 + c + v * 8, pack8(dg));
-        stg_v4(o + p.F + f0 + c + v * 8, pack8(du));
-      }
-#pragma unroll
-      for (int v = 0; v < 4; ++v) {
+        o0[v] = pack8(dg);
+        o1[v] = pack8(du);
         gq[v] = gn[v];
         uq[v] = un[v];
       }
-    }
-  } else {  // kEpiWgrad
-    __nv_bfloat16* o = p.out + (long long)g * p.out_gstride +
-                       (long long)(mt * BM + rloc) * p.ldo + nt * BN;
-#pragma unroll 1
-    for (int c = 0; c < BN; c += 32) {
+    } else {
       uint32_t r[32];
-      if (nk > 0) {
-        ptx::tmem_ld32(tbase + c, r);
-        ptx::tmem_ld_wait();
-      } else {
+      if (EPI == kEpiWgrad && nk == 0) {
 #pragma unroll
         for (int i = 0; i < 32; ++i) r[i] = 0u;
+      } else {
+        ptx::tmem_ld32(tbase + c, r);
+        ptx::tmem_ld_wait();
       }
-#pragma unroll
-      for (int v = 0; v < 4; ++v) {
-        float f[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) f[i] = __uint_as_float(r[v * 8 + i]);
-        stg_v4(o + c + v * 8, pack8(f));
+      pack_slice(r, o0);
+    }
+    // the staging area is free once the previous boxes have been read by TMA
+    if (lane == 0) ptx::tma_store_wait_read();
+    __syncwarp();
+    stage_row(stage, 0, lane, o0);
+    if (EPI == kEpiSwigluFwd || EPI == kEpiSwigluBwd) stage_row(stage, 1, lane, o1);
+    if (EPI == kEpiSwigluFwd) stage_row(stage, 2, lane, o2);
+    ptx::fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) {
+      if (EPI == kEpiSwigluFwd) {
+        ptx::tma_store_2d(tmC, stage_u32, f0 + c, row0);                      // G
+        ptx::tma_store_2d(tmC, stage_u32 + kBoxBytes, p.F + f0 + c, row0);    // U
+        ptx::tma_store_2d(tmC2, stage_u32 + 2 * kBoxBytes, f0 + c, row0);     // h
+      } else if (EPI == kEpiSwigluBwd) {
+        ptx::tma_store_2d(tmC, stage_u32, f0 + c, row0);                      // dG
+        ptx::tma_store_2d(tmC, stage_u32 + kBoxBytes, p.F + f0 + c, row0);    // dU
+      } else {
+        ptx::tma_store_2d(tmC, stage_u32, f0 + c, row0);
       }
+      ptx::tma_store_commit();
     }
   }
 }
@@ -228,6 +238,7 @@ __device__ __forceinline__ void epilogue_tile(const Params& p, uint32_t tbase, i
 template <int EPI, int BN, int A_MN, int B_MN, int STAGES>
 __global__ void __launch_bounds__(kThreads, 1)
 grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                    const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmC2,
                     const Params p) {
   using L = Layout<BN, STAGES>;
   extern __shared__ uint8_t smem_raw[];
@@ -404,7 +415,8 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
   } else {
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;                        // tensor-memory lane quarter
-    const int rloc = q * 32 + lane;                // accumulator row of this thread
+    uint8_t* stage = ctrl + kCtrlBytes + (warp - 2) * kStageBytes;
+    const uint32_t stage_u32 = ctrl_u + kCtrlBytes + (warp - 2) * kStageBytes;
     uint32_t acc = 0, acc_phase = 0;
     for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
       const Tile t = decode(tile, prefix, mtiles, s_cnt, G, p.kgrouped, p.K);
@@ -419,7 +431,8 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
       }
       ptx::tc_fence_after();
       const uint32_t tbase = tmem_base + acc * BN + ((uint32_t)(q * 32) << 16);
-      epilogue_tile<EPI, BN>(p, tbase, t.g, t.mt, t.nt, t.nk, rloc, s_off);
+      epilogue_tile<EPI, BN>(p, &tmC, &tmC2, tbase, t.g, t.mt, t.nt, t.nk, q, lane, s_off, stage,
+                             stage_u32);
       ptx::tc_fence_before();
       ptx::mbar_arrive(bar_tempty + 8 * acc);
       if (++acc == 2) {
@@ -427,6 +440,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
         acc_phase ^= 1u;
       }
     }
+    if (lane == 0) ptx::tma_store_wait_all();
   }
   ptx::tc_fence_before();
   __syncthreads();
@@ -446,12 +460,14 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
 // both CTAs, and both epilogues report back to the even CTA.
 constexpr int kPairStages = 6;
 constexpr int kPairStage = 32768;                 // 16 KB of A + 16 KB of B per CTA
-constexpr int kPairSmem = kPairStages * kPairStage + kCtrlBytes + 1024;
+constexpr int kPairSmem = kPairStages * kPairStage + kCtrlBytes + kStageAll + 1024;
 
 template <int EPI, int A_MN, int B_MN>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA,
-                         const __grid_constant__ CUtensorMap tmB, const Params p) {
+                         const __grid_constant__ CUtensorMap tmB,
+                         const __grid_constant__ CUtensorMap tmC,
+                         const __grid_constant__ CUtensorMap tmC2, const Params p) {
   constexpr int BN = 256, STAGES = kPairStages;
   constexpr int A_BYTES = 16384;
   constexpr uint32_t TMEM_COLS = 2 * BN;
@@ -644,7 +660,8 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA,
     }
   } else {
     const int q = warp & 3;
-    const int rloc = q * 32 + lane;
+    uint8_t* stage = ctrl + kCtrlBytes + (warp - 2) * kStageBytes;
+    const uint32_t stage_u32 = ctrl_u + kCtrlBytes + (warp - 2) * kStageBytes;
     const uint32_t leader_tempty[2] = {ptx::mapa_shared(bar_tempty, 0),
                                        ptx::mapa_shared(bar_tempty + 8, 0)};
     uint32_t acc = 0, acc_phase = 0;
@@ -664,7 +681,8 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA,
       const int mt = 2 * mp + (int)rank;
       if (mt < mtiles[g]) {                        // the odd tile of a group has no partner rows
         const uint32_t tbase = tmem_base + acc * BN + ((uint32_t)(q * 32) << 16);
-        epilogue_tile<EPI, BN>(p, tbase, g, mt, nt, nk, rloc, s_off);
+        epilogue_tile<EPI, BN>(p, &tmC, &tmC2, tbase, g, mt, nt, nk, q, lane, s_off, stage,
+                               stage_u32);
       }
       ptx::tc_fence_before();
       __syncwarp();
@@ -674,6 +692,7 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA,
         acc_phase ^= 1u;
       }
     }
+    if (lane == 0) ptx::tma_store_wait_all();
   }
   ptx::tc_fence_before();
   __syncthreads();
@@ -713,9 +732,23 @@ static bool make_map(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t o
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Output view [outer rows, inner columns] for TMA stores of 32 x 32 boxes with
+// the 64-byte swizzle of the epilogue's staging layout.
+static bool make_out_map(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t outer) {
+  PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {inner * 2};
+  cuuint32_t box[2] = {32, 32};
+  cuuint32_t es[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box,
+            es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 template <int EPI, int BN, int A_MN, int B_MN, int STAGES>
-static cudaError_t run(const CUtensorMap& a, const CUtensorMap& b, const Params& p,
-                       cudaStream_t s) {
+static cudaError_t run(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& c,
+                       const CUtensorMap& c2, const Params& p, cudaStream_t s) {
   using L = Layout<BN, STAGES>;
   auto kern = grouped_gemm_kernel<EPI, BN, A_MN, B_MN, STAGES>;
   static bool attr_set = false;
@@ -724,15 +757,15 @@ static cudaError_t run(const CUtensorMap& a, const CUtensorMap& b, const Params&
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  kern<<<num_sms(), kThreads, L::SMEM, s>>>(a, b, p);
+  kern<<<num_sms(), kThreads, L::SMEM, s>>>(a, b, c, c2, p);
   return cudaGetLastError();
 }
 
 // CTA-pair launch: as many clusters as can be resident at once (the tile loop
 // strides statically over clusters, so every launched cluster must run).
 template <int EPI, int A_MN, int B_MN>
-static cudaError_t run_pair(const CUtensorMap& a, const CUtensorMap& b, const Params& p,
-                            cudaStream_t s) {
+static cudaError_t run_pair(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& c,
+                            const CUtensorMap& c2, const Params& p, cudaStream_t s) {
   auto kern = grouped_gemm_pair_kernel<EPI, A_MN, B_MN>;
   static int grid = 0;
   if (grid == 0) {
@@ -751,7 +784,7 @@ static cudaError_t run_pair(const CUtensorMap& a, const CUtensorMap& b, const Pa
     }
     grid = 2 * clusters;
   }
-  kern<<<grid, kThreads, kPairSmem, s>>>(a, b, p);
+  kern<<<grid, kThreads, kPairSmem, s>>>(a, b, c, c2, p);
   return cudaGetLastError();
 }
 
@@ -779,8 +812,9 @@ cudaError_t launch_ffn_fc1(const moe_config& c, const void* x_perm, const int32_
                            int32_t* status, cudaStream_t s) {
   const int64_t R = rows_max(c);
   const int G = c.E + c.n_shared;
-  CUtensorMap a, b;
-  if (!make_map(&a, x_perm, c.H, R, 128) || !make_map(&b, W13, c.H, (uint64_t)G * 2 * c.F, 128))
+  CUtensorMap a, b, oc, oc2;
+  if (!make_map(&a, x_perm, c.H, R, 128) || !make_map(&b, W13, c.H, (uint64_t)G * 2 * c.F, 128) ||
+      !make_out_map(&oc, GU, 2ULL * c.F, R) || !make_out_map(&oc2, h, c.F, R))
     return cudaErrorInvalidValue;
   Params p = base_params(c, counts, offsets, status);
   p.K = c.H;
@@ -789,8 +823,8 @@ cudaError_t launch_ffn_fc1(const moe_config& c, const void* x_perm, const int32_
   p.ldo = 2LL * c.F;
   p.out2 = static_cast<__nv_bfloat16*>(h);
   p.ldo2 = c.F;
-  if (use_pairs(256)) return run_pair<kEpiSwigluFwd, 0, 0>(a, b, p, s);
-  return run<kEpiSwigluFwd, 256, 0, 0, 4>(a, b, p, s);
+  if (use_pairs(256)) return run_pair<kEpiSwigluFwd, 0, 0>(a, b, oc, oc2, p, s);
+  return run<kEpiSwigluFwd, 256, 0, 0, 4>(a, b, oc, oc2, p, s);
 }
 
 cudaError_t launch_ffn_fc2(const moe_config& c, const void* h, const int32_t* counts,
@@ -800,19 +834,21 @@ cudaError_t launch_ffn_fc2(const moe_config& c, const void* h, const int32_t* co
   const int G = c.E + c.n_shared;
   const int bn = (c.H % 256 == 0) ? 256 : 128;
   const bool pair = use_pairs(c.H);
-  CUtensorMap a, b;
+  CUtensorMap a, b, oc;
   if (!make_map(&a, h, c.F, R, 128) ||
-      !make_map(&b, W2, c.F, (uint64_t)G * c.H, pair ? 128 : bn))
+      !make_map(&b, W2, c.F, (uint64_t)G * c.H, pair ? 128 : bn) ||
+      !make_out_map(&oc, y_perm, c.H, R))
     return cudaErrorInvalidValue;
+  const CUtensorMap& oc2 = oc;
   Params p = base_params(c, counts, offsets, status);
   p.N = c.H;
   p.K = c.F;
   p.b_rows = c.H;
   p.out = static_cast<__nv_bfloat16*>(y_perm);
   p.ldo = c.H;
-  if (pair) return run_pair<kEpiStore, 0, 0>(a, b, p, s);
-  return bn == 256 ? run<kEpiStore, 256, 0, 0, 4>(a, b, p, s)
-                   : run<kEpiStore, 128, 0, 0, 6>(a, b, p, s);
+  if (pair) return run_pair<kEpiStore, 0, 0>(a, b, oc, oc2, p, s);
+  return bn == 256 ? run<kEpiStore, 256, 0, 0, 4>(a, b, oc, oc2, p, s)
+                   : run<kEpiStore, 128, 0, 0, 6>(a, b, oc, oc2, p, s);
 }
 
 cudaError_t launch_ffn_fc2_dgrad(const moe_config& c, const void* dO_perm, const int32_t* counts,
@@ -821,9 +857,11 @@ cudaError_t launch_ffn_fc2_dgrad(const moe_config& c, const void* dO_perm, const
   const int64_t R = rows_max(c);
   const int G = c.E + c.n_shared;
   const int bn = (c.F % 256 == 0) ? 256 : 128;
-  CUtensorMap a, b;
-  if (!make_map(&a, dO_perm, c.H, R, 128) || !make_map(&b, W2, c.F, (uint64_t)G * c.H, 64))
+  CUtensorMap a, b, oc;
+  if (!make_map(&a, dO_perm, c.H, R, 128) || !make_map(&b, W2, c.F, (uint64_t)G * c.H, 64) ||
+      !make_out_map(&oc, dGU, 2ULL * c.F, R))
     return cudaErrorInvalidValue;
+  const CUtensorMap& oc2 = oc;
   Params p = base_params(c, counts, offsets, status);
   p.N = c.F;
   p.K = c.H;
@@ -832,9 +870,9 @@ cudaError_t launch_ffn_fc2_dgrad(const moe_config& c, const void* dO_perm, const
   p.ldo = 2LL * c.F;
   p.aux = static_cast<const __nv_bfloat16*>(GU);
   p.ldaux = 2LL * c.F;
-  if (use_pairs(c.F)) return run_pair<kEpiSwigluBwd, 0, 1>(a, b, p, s);
-  return bn == 256 ? run<kEpiSwigluBwd, 256, 0, 1, 4>(a, b, p, s)
-                   : run<kEpiSwigluBwd, 128, 0, 1, 6>(a, b, p, s);
+  if (use_pairs(c.F)) return run_pair<kEpiSwigluBwd, 0, 1>(a, b, oc, oc2, p, s);
+  return bn == 256 ? run<kEpiSwigluBwd, 256, 0, 1, 4>(a, b, oc, oc2, p, s)
+                   : run<kEpiSwigluBwd, 128, 0, 1, 6>(a, b, oc, oc2, p, s);
 }
 
 cudaError_t launch_ffn_fc1_dgrad(const moe_config& c, const void* dGU, const int32_t* counts,
@@ -843,19 +881,21 @@ cudaError_t launch_ffn_fc1_dgrad(const moe_config& c, const void* dGU, const int
   const int64_t R = rows_max(c);
   const int G = c.E + c.n_shared;
   const int bn = (c.H % 256 == 0) ? 256 : 128;
-  CUtensorMap a, b;
+  CUtensorMap a, b, oc;
   if (!make_map(&a, dGU, 2ULL * c.F, R, 128) ||
-      !make_map(&b, W13, c.H, (uint64_t)G * 2 * c.F, 64))
+      !make_map(&b, W13, c.H, (uint64_t)G * 2 * c.F, 64) ||
+      !make_out_map(&oc, dX_perm, c.H, R))
     return cudaErrorInvalidValue;
+  const CUtensorMap& oc2 = oc;
   Params p = base_params(c, counts, offsets, status);
   p.N = c.H;
   p.K = 2 * c.F;
   p.b_rows = 2 * c.F;
   p.out = static_cast<__nv_bfloat16*>(dX_perm);
   p.ldo = c.H;
-  if (use_pairs(c.H)) return run_pair<kEpiStore, 0, 1>(a, b, p, s);
-  return bn == 256 ? run<kEpiStore, 256, 0, 1, 4>(a, b, p, s)
-                   : run<kEpiStore, 128, 0, 1, 6>(a, b, p, s);
+  if (use_pairs(c.H)) return run_pair<kEpiStore, 0, 1>(a, b, oc, oc2, p, s);
+  return bn == 256 ? run<kEpiStore, 256, 0, 1, 4>(a, b, oc, oc2, p, s)
+                   : run<kEpiStore, 128, 0, 1, 6>(a, b, oc, oc2, p, s);
 }
 
 cudaError_t launch_ffn_wgrad_fc2(const moe_config& c, const void* dO_perm, const void* h,
@@ -863,9 +903,12 @@ cudaError_t launch_ffn_wgrad_fc2(const moe_config& c, const void* dO_perm, const
                                  int32_t* status, cudaStream_t s) {
   const int64_t R = rows_max(c);
   const int bn = (c.F % 256 == 0) ? 256 : 128;
-  CUtensorMap a, b;
-  if (!make_map(&a, dO_perm, c.H, R, 64) || !make_map(&b, h, c.F, R, 64))
+  const int G = c.E + c.n_shared;
+  CUtensorMap a, b, oc;
+  if (!make_map(&a, dO_perm, c.H, R, 64) || !make_map(&b, h, c.F, R, 64) ||
+      !make_out_map(&oc, dW2, c.F, (uint64_t)G * c.H))
     return cudaErrorInvalidValue;
+  const CUtensorMap& oc2 = oc;
   Params p = base_params(c, counts, offsets, status);
   p.kgrouped = 1;
   p.Mw = c.H;
@@ -873,9 +916,9 @@ cudaError_t launch_ffn_wgrad_fc2(const moe_config& c, const void* dO_perm, const
   p.out = static_cast<__nv_bfloat16*>(dW2);
   p.ldo = c.F;
   p.out_gstride = (long long)c.H * c.F;
-  if (use_pairs(c.F)) return run_pair<kEpiWgrad, 1, 1>(a, b, p, s);
-  return bn == 256 ? run<kEpiWgrad, 256, 1, 1, 4>(a, b, p, s)
-                   : run<kEpiWgrad, 128, 1, 1, 6>(a, b, p, s);
+  if (use_pairs(c.F)) return run_pair<kEpiWgrad, 1, 1>(a, b, oc, oc2, p, s);
+  return bn == 256 ? run<kEpiWgrad, 256, 1, 1, 4>(a, b, oc, oc2, p, s)
+                   : run<kEpiWgrad, 128, 1, 1, 6>(a, b, oc, oc2, p, s);
 }
 
 cudaError_t launch_ffn_wgrad_fc1(const moe_config& c, const void* dGU, const void* x_perm,
@@ -883,9 +926,12 @@ cudaError_t launch_ffn_wgrad_fc1(const moe_config& c, const void* dGU, const voi
                                  int32_t* status, cudaStream_t s) {
   const int64_t R = rows_max(c);
   const int bn = (c.H % 256 == 0) ? 256 : 128;
-  CUtensorMap a, b;
-  if (!make_map(&a, dGU, 2ULL * c.F, R, 64) || !make_map(&b, x_perm, c.H, R, 64))
+  const int G = c.E + c.n_shared;
+  CUtensorMap a, b, oc;
+  if (!make_map(&a, dGU, 2ULL * c.F, R, 64) || !make_map(&b, x_perm, c.H, R, 64) ||
+      !make_out_map(&oc, dW13, c.H, (uint64_t)G * 2 * c.F))
     return cudaErrorInvalidValue;
+  const CUtensorMap& oc2 = oc;
   Params p = base_params(c, counts, offsets, status);
   p.kgrouped = 1;
   p.Mw = 2 * c.F;
@@ -893,9 +939,9 @@ cudaError_t launch_ffn_wgrad_fc1(const moe_config& c, const void* dGU, const voi
   p.out = static_cast<__nv_bfloat16*>(dW13);
   p.ldo = c.H;
   p.out_gstride = 2LL * c.F * c.H;
-  if (use_pairs(c.H)) return run_pair<kEpiWgrad, 1, 1>(a, b, p, s);
-  return bn == 256 ? run<kEpiWgrad, 256, 1, 1, 4>(a, b, p, s)
-                   : run<kEpiWgrad, 128, 1, 1, 6>(a, b, p, s);
+  if (use_pairs(c.H)) return run_pair<kEpiWgrad, 1, 1>(a, b, oc, oc2, p, s);
+  return bn == 256 ? run<kEpiWgrad, 256, 1, 1, 4>(a, b, oc, oc2, p, s)
+                   : run<kEpiWgrad, 128, 1, 1, 6>(a, b, oc, oc2, p, s);
 }
 
 }  // namespace moe
