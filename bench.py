@@ -222,36 +222,66 @@ def run_ours(args, rank, world, local):
     fwd_gemm_ms = sum(e[0].elapsed_time(e[1]) for e in evs) / args.steps
     bwd_gemm_ms = sum(e[2].elapsed_time(e[3]) for e in evs) / args.steps
 
-    # end to end through the public layer calls, host buffers
-    xh = x.cpu().pin_memory()
-    dYh = dY.cpu().pin_memory()
-    outh = torch.empty_like(xh).pin_memory()
-    dxh = torch.empty_like(xh).pin_memory()
-    xd = torch.empty_like(x)
-    dYd = torch.empty_like(dY)
+    # end to end through the public layer calls, host buffers: every step copies
+    # its x and dY from pinned host memory and reads out and dx back. Copies run
+    # on a second stream, double-buffered and ordered by events, so step i+1's
+    # uploads and step i's downloads overlap the neighbouring compute.
+    cs = torch.cuda.Stream(dev)
+    xh = [x.cpu().pin_memory() for _ in range(2)]
+    dYh = [dY.cpu().pin_memory() for _ in range(2)]
+    outh = [torch.empty_like(xh[0]).pin_memory() for _ in range(2)]
+    dxh = [torch.empty_like(xh[0]).pin_memory() for _ in range(2)]
+    xd = [torch.empty_like(x) for _ in range(2)]
+    dYd = [torch.empty_like(dY) for _ in range(2)]
+    outd = [torch.empty_like(out) for _ in range(2)]
+    dxd = [torch.empty_like(dx) for _ in range(2)]
+    up = [torch.cuda.Event() for _ in range(2)]       # inputs of buffer b uploaded
+    done = [torch.cuda.Event() for _ in range(2)]     # compute on buffer b finished
+    down = [torch.cuda.Event() for _ in range(2)]     # results of buffer b downloaded
 
-    def e2e_step():
-        xd.copy_(xh, non_blocking=True)
-        dYd.copy_(dYh, non_blocking=True)
-        B.moe_layer_fwd(cfg, P, xd, out, bufs.fwd_struct, sc)
-        B.moe_layer_bwd(cfg, P, xd, dYd, bufs.fwd_struct, bufs.bwd_struct, dx, dW_r, dW13, dW2, sc)
-        outh.copy_(out, non_blocking=True)
-        dxh.copy_(dx, non_blocking=True)
+    def upload(b):
+        with torch.cuda.stream(cs):
+            cs.wait_event(done[b])                    # previous compute on b is finished
+            xd[b].copy_(xh[b], non_blocking=True)
+            dYd[b].copy_(dYh[b], non_blocking=True)
+            up[b].record(cs)
 
-    for _ in range(3):
-        e2e_step()
+    def e2e_run(n):
+        for b in range(2):
+            done[b].record(stream)
+            down[b].record(stream)
+        upload(0)
+        for i in range(n):
+            b = i & 1
+            if i + 1 < n:
+                upload(1 - b)
+            stream.wait_event(up[b])
+            stream.wait_event(down[b])                # results of step i-2 are out
+            B.moe_layer_fwd(cfg, P, xd[b], outd[b], bufs.fwd_struct, sc)
+            B.moe_layer_bwd(cfg, P, xd[b], dYd[b], bufs.fwd_struct, bufs.bwd_struct, dxd[b], dW_r,
+                            dW13, dW2, sc)
+            done[b].record(stream)
+            with torch.cuda.stream(cs):
+                cs.wait_event(done[b])
+                outh[b].copy_(outd[b], non_blocking=True)
+                dxh[b].copy_(dxd[b], non_blocking=True)
+                down[b].record(cs)
+        stream.wait_stream(cs)
+
+    e2e_run(3)
     torch.cuda.synchronize(dev)
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     e0.record(stream)
-    for _ in range(args.steps):
-        e2e_step()
+    e2e_run(args.steps)
     e1.record(stream)
     torch.cuda.synchronize(dev)
     e2e_ms = e0.elapsed_time(e1)
     status = B.moe_last_device_status(sc)
     if status != 0:
         raise RuntimeError(f"device status {status} after timed steps")
+    if not torch.equal(outh[(args.steps - 1) & 1], out.cpu()):
+        raise RuntimeError("end-to-end output differs from the device-resident run")
 
     times = torch.tensor([ms, e2e_ms], dtype=torch.float64, device=dev)
     if world > 1:

@@ -325,13 +325,14 @@ permute_bwd_kernel(const __nv_bfloat16* __restrict__ dX, const int32_t* __restri
 }
 
 // dW_r[e, cols] = sum over the tokens that selected e (in token order, split
-// across the block's 8 warps in a fixed interleave) of dlogits[t,e] x[t, cols].
+// across the block's 16 warps in a fixed interleave) of dlogits[t,e] x[t, cols].
 // Block (e, 256-column slab); lane owns 8 columns; warps combined in order.
-__global__ void __launch_bounds__(256)
+__global__ void __launch_bounds__(512)
 router_wgrad_kernel(const __nv_bfloat16* __restrict__ x, const int32_t* __restrict__ sel_offsets,
                     const int32_t* __restrict__ sel_tokens, const float* __restrict__ dlogits,
                     float* __restrict__ dW_r, int H, int E) {
-  __shared__ float part[8][256];
+  constexpr int NW = 16;
+  __shared__ float part[NW][256];
   const int e = blockIdx.x;
   const int col0 = blockIdx.y * 256;
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
@@ -342,12 +343,12 @@ router_wgrad_kernel(const __nv_bfloat16* __restrict__ x, const int32_t* __restri
 #pragma unroll
   for (int i = 0; i < 8; ++i) acc[i] = 0.f;
   int i = beg + wid;
-  for (; i + 24 < end; i += 32) {
+  for (; i + 3 * NW < end; i += 4 * NW) {
     int tt[4];
     float d[4];
     uint4 q[4];
 #pragma unroll
-    for (int u = 0; u < 4; ++u) tt[u] = sel_tokens[i + 8 * u];
+    for (int u = 0; u < 4; ++u) tt[u] = sel_tokens[i + NW * u];
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
       d[u] = dlogits[(size_t)tt[u] * E + e];
@@ -362,7 +363,7 @@ router_wgrad_kernel(const __nv_bfloat16* __restrict__ x, const int32_t* __restri
       for (int m = 0; m < 8; ++m) acc[m] = fmaf(d[u], f[m], acc[m]);
     }
   }
-  for (; i < end; i += 8) {
+  for (; i < end; i += NW) {
     const int t = sel_tokens[i];
     const float d = dlogits[(size_t)t * E + e];
     if (!on) continue;
@@ -374,16 +375,17 @@ router_wgrad_kernel(const __nv_bfloat16* __restrict__ x, const int32_t* __restri
 #pragma unroll
   for (int m = 0; m < 8; ++m) part[wid][lane * 8 + m] = acc[m];
   __syncthreads();
-  const int col = col0 + threadIdx.x;
-  if (col < H) {
-    float s = 0.f;
+  if (threadIdx.x < 256) {
+    const int col = col0 + threadIdx.x;
+    if (col < H) {
+      float s = 0.f;
 #pragma unroll
-    for (int q2 = 0; q2 < 8; ++q2) s += part[q2][threadIdx.x];
-    dW_r[(size_t)e * H + col] = s;
+      for (int q2 = 0; q2 < NW; ++q2) s += part[q2][threadIdx.x];
+      dW_r[(size_t)e * H + col] = s;
+    }
   }
 }
 
-// Blocks of 256 threads for one thread per 16-byte slice of every token row.
 static int grid_for_vectors(const moe_config& c) {
   const long long n = (long long)c.T * ((c.H / 8 + 31) / 32) * 32;   // up to one warp per segment
   long long blocks = (n + 255) / 256;
@@ -448,7 +450,7 @@ cudaError_t launch_router_wgrad(const moe_config& c, const void* x, const int32_
                                 const int32_t* sel_tokens, const float* dlogits, float* dW_r,
                                 cudaStream_t s) {
   dim3 grid(c.E, (c.H + 255) / 256);
-  router_wgrad_kernel<<<grid, 256, 0, s>>>(static_cast<const __nv_bfloat16*>(x), sel_offsets,
+  router_wgrad_kernel<<<grid, 512, 0, s>>>(static_cast<const __nv_bfloat16*>(x), sel_offsets,
                                           sel_tokens, dlogits, dW_r, c.H, c.E);
   return cudaGetLastError();
 }
