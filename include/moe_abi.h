@@ -150,7 +150,8 @@ MOE_API moe_status moe_query_sizes(const moe_config* cfg, moe_sizes* out);
  * selection scores of the group). Weights: softmax over the k selected
  * (renormalised), or route_scale * s_j / sum_sel s.
  * x [T,H] bf16, W_r [E,H] f32, bias [E] f32 or NULL -> logits [T,E] f32,
- * idx [T,k] i32, w [T,k] f32. */
+ * idx [T,k] i32, w [T,k] f32. For E a multiple of 128 the logits run on the
+ * tensor cores from an exact three-way bf16 split of W_r kept in `scratch`. */
 MOE_API moe_status moe_route(const moe_config* cfg, const void* x, const float* W_r, const float* bias,
                      float* logits, int32_t* idx, float* w, void* scratch, void* stream);
 
@@ -172,9 +173,9 @@ MOE_API moe_status moe_permute(const moe_config* cfg, const void* x, const int32
  * device memory, or on a path where cudaMalloc may not be called). Its scratch
  * is a fixed 512 KiB array inside the library, resident on every GPU that
  * loads the library until the process exits.
- *  - Limit: configurations whose dispatch scratch (moe_query_sizes'
- *    scratch_bytes, 4096 + 4*E*ceil(T/256) + 256 bytes) exceeds 512 KiB return
- *    MOE_ERR_WORKSPACE without launching anything.
+ *  - Limit: configurations whose dispatch scratch (4096 + 4*E*ceil(T/256) +
+ *    256 bytes, rounded up to 256) exceeds 512 KiB return MOE_ERR_WORKSPACE
+ *    without launching anything.
  *  - The first call on a device looks up the array's device address with that
  *    device current; make that first call before any stream capture.
  *  - All calls share the one array, which keeps the last call's contents:

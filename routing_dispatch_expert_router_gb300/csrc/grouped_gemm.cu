@@ -44,7 +44,8 @@ constexpr int kStageBytes = 3 * kBoxBytes;       // output staging per epilogue 
 constexpr int kStageAll = 4 * kStageBytes;
 constexpr long long kWaitBudget = 4000000000LL;   // clock64 cycles (~2 s)
 
-enum Epi : int { kEpiSwigluFwd = 0, kEpiStore = 1, kEpiSwigluBwd = 2, kEpiWgrad = 3 };
+enum Epi : int { kEpiSwigluFwd = 0, kEpiStore = 1, kEpiSwigluBwd = 2, kEpiWgrad = 3,
+                 kEpiStoreF32 = 4 };
 
 struct Params {
   int kgrouped;               // 0: row-grouped, 1: K-grouped
@@ -64,6 +65,8 @@ struct Params {
   const __nv_bfloat16* aux;   // SwiGLU-bwd: GU
   long long ldaux;
   int32_t* status;
+  int dense_rows;             // > 0: one group of this many rows at row 0 (no counts/offsets)
+  int a_kwrap;                // > 0: A's k coordinate wraps at this width (A repeated along K)
 };
 
 template <int BN, int STAGES>
@@ -200,6 +203,26 @@ __device__ __forceinline__ void epilogue_tile(const Params& p, const CUtensorMap
         gq[v] = gn[v];
         uq[v] = un[v];
       }
+    } else if (EPI == kEpiStoreF32) {
+      // fp32 output: one 32 x 32 box = 128-byte rows, 128-byte swizzle (chunk j
+      // of row r at slot j ^ (r & 7))
+      uint32_t r[32];
+      ptx::tmem_ld32(tbase + c, r);
+      ptx::tmem_ld_wait();
+      if (lane == 0) ptx::tma_store_wait_read();
+      __syncwarp();
+      uint8_t* rowp = stage + lane * 128;
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        *reinterpret_cast<uint4*>(rowp + ((j ^ (lane & 7)) << 4)) =
+            make_uint4(r[4 * j], r[4 * j + 1], r[4 * j + 2], r[4 * j + 3]);
+      ptx::fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        ptx::tma_store_2d(tmC, stage_u32, f0 + c, row0);
+        ptx::tma_store_commit();
+      }
+      continue;
     } else {
       uint32_t r[32];
       if (EPI == kEpiWgrad && nk == 0) {
@@ -264,9 +287,9 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
   const int G = p.G;
   const int NT = (EPI == kEpiSwigluFwd) ? p.F / (BN / 2) : p.N / BN;
   for (int g = tid; g < G; g += kThreads) {
-    const int c = p.counts[g];
+    const int c = p.dense_rows > 0 ? p.dense_rows : p.counts[g];
     s_cnt[g] = c;
-    s_off[g] = p.offsets[g];
+    s_off[g] = p.dense_rows > 0 ? 0 : p.offsets[g];
     const int mt = p.kgrouped ? p.Mw / BM : (c + BM - 1) / BM;
     mtiles[g] = mt;
     prefix[g] = mt * NT;
@@ -322,7 +345,8 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
           const uint32_t sB = sA + L::A_BYTES;
           const int k0 = kb * BK;
           if (A_MN == 0) {
-            ptx::tma_load_2d(sA, &tmA, fb, k0, s_off[t.g] + t.mt * BM);
+            ptx::tma_load_2d(sA, &tmA, fb, p.a_kwrap > 0 ? k0 % p.a_kwrap : k0,
+                             s_off[t.g] + t.mt * BM);
           } else {
             const int kr = s_off[t.g] + k0;
             ptx::tma_load_2d(sA, &tmA, fb, t.mt * BM, kr);
@@ -495,9 +519,9 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA,
   const int G = p.G;
   const int NT = (EPI == kEpiSwigluFwd) ? p.F / (BN / 2) : p.N / BN;
   for (int g = tid; g < G; g += kThreads) {
-    const int c = p.counts[g];
+    const int c = p.dense_rows > 0 ? p.dense_rows : p.counts[g];
     s_cnt[g] = c;
-    s_off[g] = p.offsets[g];
+    s_off[g] = p.dense_rows > 0 ? 0 : p.offsets[g];
     const int mt = p.kgrouped ? p.Mw / BM : (c + BM - 1) / BM;
     mtiles[g] = mt;
     prefix[g] = ((mt + 1) >> 1) * NT;              // pair tiles of the group
@@ -746,6 +770,19 @@ static bool make_out_map(CUtensorMap* m, const void* ptr, uint64_t inner, uint64
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// fp32 output view for TMA stores of 32 x 32 boxes (128-byte rows, 128-byte swizzle).
+static bool make_out_map_f32(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t outer) {
+  PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {inner * 4};
+  cuuint32_t box[2] = {32, 32};
+  cuuint32_t es[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void*>(ptr), dims, strides, box,
+            es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 template <int EPI, int BN, int A_MN, int B_MN, int STAGES>
 static cudaError_t run(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& c,
                        const CUtensorMap& c2, const Params& p, cudaStream_t s) {
@@ -942,6 +979,26 @@ cudaError_t launch_ffn_wgrad_fc1(const moe_config& c, const void* dGU, const voi
   if (use_pairs(c.H)) return run_pair<kEpiWgrad, 1, 1>(a, b, oc, oc2, p, s);
   return bn == 256 ? run<kEpiWgrad, 256, 1, 1, 4>(a, b, oc, oc2, p, s)
                    : run<kEpiWgrad, 128, 1, 1, 6>(a, b, oc, oc2, p, s);
+}
+
+// Router logits on the tensor cores: logits[T,E] = [x x x] . W3^T where
+// W3 = [W_hi | W_mid | W_lo] ([E, 3H] bf16, W_r = W_hi + W_mid + W_lo exactly),
+// fp32 accumulation, one dense group of T rows (rows past T read zeros and
+// are not stored). Needs E % 128 == 0.
+cudaError_t launch_router_logits_tc(const moe_config& c, const void* x, const void* W3,
+                                    float* logits, int32_t* status, cudaStream_t s) {
+  CUtensorMap a, b, oc;
+  if (!make_map(&a, x, c.H, c.T, 128) || !make_map(&b, W3, 3ULL * c.H, c.E, 128) ||
+      !make_out_map_f32(&oc, logits, c.E, c.T))
+    return cudaErrorInvalidValue;
+  Params p{};
+  p.G = 1;
+  p.dense_rows = c.T;
+  p.a_kwrap = c.H;
+  p.N = c.E;
+  p.K = 3 * c.H;
+  p.status = status;
+  return run<kEpiStoreF32, 128, 0, 0, 6>(a, b, oc, oc, p, s);
 }
 
 }  // namespace moe

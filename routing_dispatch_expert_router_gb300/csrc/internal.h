@@ -16,7 +16,7 @@ int n_chunks(const moe_config& c);
 int num_sms();
 
 cudaError_t launch_route(const moe_config& c, const void* x, const float* W_r, const float* bias,
-                         float* logits, int32_t* idx, float* w, cudaStream_t s);
+                         float* logits, int32_t* idx, float* w, uint8_t* scratch, cudaStream_t s);
 
 cudaError_t launch_permute(const moe_config& c, const void* x, const int32_t* idx,
                            int32_t* counts, int32_t* offsets, int32_t* row_of, int32_t* token_of,
@@ -58,6 +58,14 @@ struct Fp8Scratch {
   void* d2F;    // [R,2F] dGU rows, then dGU columns
 };
 Fp8Scratch fp8_scratch(const moe_config& c, void* scratch);
+
+// Router logits for E % 128 == 0 on the tensor cores (W3 = W_r split in three bf16 parts).
+cudaError_t launch_router_logits_tc(const moe_config& c, const void* x, const void* W3,
+                                    float* logits, int32_t* status, cudaStream_t s);
+bool router_on_tensor_cores(const moe_config& c);
+int64_t router_split_bytes(const moe_config& c);
+int64_t router_split_offset(const moe_config& c);   // byte offset of the split in scratch
+int64_t permute_scratch_bytes(const moe_config& c); // scratch the dispatch needs
 
 // Grouped GEMMs (tcgen05). Return cudaErrorInvalidValue when a tensor map
 // cannot be encoded for the given pointers.

@@ -41,8 +41,14 @@ int num_sms() {
 
 static int64_t align256(int64_t v) { return (v + 255) / 256 * 256; }
 
-static int64_t base_scratch_bytes(const moe_config& c) {
+int64_t permute_scratch_bytes(const moe_config& c) {
   return align256((int64_t)kScratchHist + (int64_t)n_chunks(c) * c.E * 4 + 256);
+}
+
+int64_t router_split_offset(const moe_config& c) { return permute_scratch_bytes(c); }
+
+static int64_t base_scratch_bytes(const moe_config& c) {
+  return permute_scratch_bytes(c) + router_split_bytes(c);
 }
 
 int64_t scratch_bytes(const moe_config& c) {
@@ -153,9 +159,10 @@ moe_status moe_route(const moe_config* cfg, const void* x, const float* W_r, con
   MOE_TRY(check_config(cfg));
   MOE_REQUIRE(tok16(cfg, x) && al16(W_r) && tok4(cfg, logits) && tok4(cfg, idx) && tok4(cfg, w));
   MOE_REQUIRE(bias == nullptr || al4(bias));
-  (void)scratch;
+  MOE_REQUIRE(al16(scratch));
   if (cfg->T == 0) return MOE_OK;
-  MOE_CUDA(launch_route(*cfg, x, W_r, bias, logits, idx, w, (cudaStream_t)stream));
+  MOE_CUDA(launch_route(*cfg, x, W_r, bias, logits, idx, w, static_cast<uint8_t*>(scratch),
+                        (cudaStream_t)stream));
   return MOE_OK;
 }
 

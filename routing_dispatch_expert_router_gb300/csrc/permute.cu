@@ -284,7 +284,7 @@ extern "C" moe_status moe_permute_noalloc(const moe_config* cfg, const void* x,
       !a4(offsets) || !((empty && !row_of) || a4(row_of)) || !a4(token_of) ||
       !a4(sel_offsets) || !((empty && !sel_tokens) || a4(sel_tokens)) || !a16(x_perm))
     return MOE_ERR_INVALID_ARG;
-  if ((size_t)scratch_bytes(*cfg) > kNoAllocScratchBytes) return MOE_ERR_WORKSPACE;
+  if ((size_t)permute_scratch_bytes(*cfg) > kNoAllocScratchBytes) return MOE_ERR_WORKSPACE;
   uint8_t* sc = nullptr;
   if (noalloc_scratch(&sc) != cudaSuccess) return MOE_ERR_CUDA;
   cudaStream_t s = (cudaStream_t)stream;

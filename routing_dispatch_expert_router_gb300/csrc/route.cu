@@ -306,10 +306,49 @@ route_select_kernel(const float* __restrict__ logits, const float* __restrict__ 
   }
 }
 
+// W3[e] = [hi | mid | lo] with hi = bf16(w), mid = bf16(w - hi), lo = bf16(w - hi - mid):
+// each part keeps 8 significant bits, so hi + mid + lo == w exactly for every
+// fp32 w (the two subtractions are exact).
+__global__ void __launch_bounds__(256)
+split3_kernel(const float* __restrict__ W, __nv_bfloat16* __restrict__ W3, int E, int H) {
+  const long long n = (long long)E * H;
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n;
+       i += (long long)gridDim.x * blockDim.x) {
+    const int e = (int)(i / H), h = (int)(i % H);
+    const float v = W[i];
+    const __nv_bfloat16 hi = __float2bfloat16_rn(v);
+    const float r1 = v - __bfloat162float(hi);
+    const __nv_bfloat16 mid = __float2bfloat16_rn(r1);
+    const float r2 = r1 - __bfloat162float(mid);
+    __nv_bfloat16* row = W3 + (size_t)e * 3 * H;
+    row[h] = hi;
+    row[H + h] = mid;
+    row[2 * H + h] = __float2bfloat16_rn(r2);
+  }
+}
+
+bool router_on_tensor_cores(const moe_config& c) { return c.E >= 128 && c.E % 128 == 0; }
+
+int64_t router_split_bytes(const moe_config& c) {
+  return router_on_tensor_cores(c) ? ((int64_t)c.E * 3 * c.H * 2 + 255) / 256 * 256 : 0;
+}
+
 cudaError_t launch_route(const moe_config& c, const void* x, const float* W_r, const float* bias,
-                         float* logits, int32_t* idx, float* w, cudaStream_t s) {
+                         float* logits, int32_t* idx, float* w, uint8_t* scratch, cudaStream_t s) {
   const __nv_bfloat16* xb = static_cast<const __nv_bfloat16*>(x);
-  if (c.E <= 16) {
+  if (router_on_tensor_cores(c)) {
+    // logits on the tensor cores from the exact three-way bf16 split of W_r
+    __nv_bfloat16* W3 = reinterpret_cast<__nv_bfloat16*>(scratch + router_split_offset(c));
+    const long long n = (long long)c.E * c.H;
+    long long blocks = (n + 255) / 256;
+    if (blocks > (long long)num_sms() * 16) blocks = (long long)num_sms() * 16;
+    split3_kernel<<<(int)blocks, 256, 0, s>>>(W_r, W3, c.E, c.H);
+    cudaError_t err = cudaGetLastError();
+    if (err != cudaSuccess) return err;
+    err = launch_router_logits_tc(c, x, W3, logits,
+                                  reinterpret_cast<int32_t*>(scratch + kScratchStatus), s);
+    if (err != cudaSuccess) return err;
+  } else if (c.E <= 16) {
     const int blocks = (c.T + 3) / 4;        // 4 tokens per block of 4 warps
     if (c.E <= 8)
       route_logits_few_kernel<8><<<blocks, 128, 0, s>>>(xb, W_r, logits, c.T, c.H, c.E);
@@ -319,8 +358,7 @@ cudaError_t launch_route(const moe_config& c, const void* x, const float* W_r, c
     dim3 grid((c.T + 63) / 64, (c.E + 63) / 64);
     route_logits_kernel<64, 64><<<grid, 256, 0, s>>>(xb, W_r, logits, c.T, c.H, c.E);
   }
-  cudaError_t err = cudaGetLastError();
-  if (err != cudaSuccess) return err;
+  if (cudaError_t err = cudaGetLastError(); err != cudaSuccess) return err;
   route_select_kernel<<<(c.T + 7) / 8, 256, 0, s>>>(logits, bias, idx, w, c.T, c.E, c.k,
                                                     c.score_fn, c.n_groups, c.topk_groups,
                                                     c.group_score, c.route_scale);
