@@ -111,6 +111,7 @@ __device__ __forceinline__ int find_pad_group(const int* prefix, int G, int p) {
 // One block per token (grid-stride over tokens, then over the padding rows of
 // dO, which are zeroed). Threads own 16-byte slices; the dot products are
 // reduced warp by warp and then across warps in a fixed order.
+template <int MAXR>
 __global__ void __launch_bounds__(256)
 unpermute_bwd_kernel(const __nv_bfloat16* __restrict__ dY, const __nv_bfloat16* __restrict__ y,
                      const int32_t* __restrict__ row_of, const float* __restrict__ w,
@@ -121,7 +122,7 @@ unpermute_bwd_kernel(const __nv_bfloat16* __restrict__ dY, const __nv_bfloat16* 
   __shared__ int s_off[kMaxGroups + 1];
   __shared__ int s_cnt[kMaxGroups];
   __shared__ int s_tmp[33];
-  __shared__ float s_dot[8][kMaxK];
+  __shared__ float s_dot[8][MAXR];
   const int G = E + S;
   for (int g = threadIdx.x; g <= G; g += blockDim.x) s_off[g] = offsets[g];
   for (int g = threadIdx.x; g < G; g += blockDim.x) s_cnt[g] = counts[g];
@@ -144,10 +145,10 @@ unpermute_bwd_kernel(const __nv_bfloat16* __restrict__ dY, const __nv_bfloat16* 
       continue;
     }
     const int t = v;
-    int rows[kMaxK + 4];
-    float wts[kMaxK + 4];
+    int rows[MAXR];
+    float wts[MAXR];
 #pragma unroll
-    for (int j = 0; j < kMaxK + 4; ++j) {
+    for (int j = 0; j < MAXR; ++j) {
       rows[j] = -1;
       wts[j] = 0.f;
       if (j >= nr) continue;
@@ -158,19 +159,19 @@ unpermute_bwd_kernel(const __nv_bfloat16* __restrict__ dY, const __nv_bfloat16* 
         rows[j] = s_off[E + j - k] + t;
       }
     }
-    float dot[kMaxK];
+    float dot[MAXR];
 #pragma unroll
-    for (int j = 0; j < kMaxK; ++j) dot[j] = 0.f;
+    for (int j = 0; j < MAXR; ++j) dot[j] = 0.f;
     for (int c = threadIdx.x; c < nvec; c += blockDim.x) {
       const uint4 gq = ldg_nc_v4(dY + (size_t)t * H + (size_t)c * 8);
-      uint4 yq[kMaxK];
+      uint4 yq[MAXR];
 #pragma unroll
-      for (int j = 0; j < kMaxK; ++j)
+      for (int j = 0; j < MAXR; ++j)
         if (j < k && rows[j] >= 0) yq[j] = ldg_nc_v4(y + (size_t)rows[j] * H + (size_t)c * 8);
       float g[8];
       unpack8(gq, g);
 #pragma unroll
-      for (int j = 0; j < kMaxK; ++j) {
+      for (int j = 0; j < MAXR; ++j) {
         if (j >= k || rows[j] < 0) continue;
         float f[8], o[8];
         unpack8(yq[j], f);
@@ -182,13 +183,13 @@ unpermute_bwd_kernel(const __nv_bfloat16* __restrict__ dY, const __nv_bfloat16* 
         stg_v4(dO + (size_t)rows[j] * H + (size_t)c * 8, pack8(o));
       }
 #pragma unroll
-      for (int j = 0; j < kMaxK + 4; ++j) {
+      for (int j = 0; j < MAXR; ++j) {
         if (j < k || j >= nr) continue;
         stg_v4(dO + (size_t)rows[j] * H + (size_t)c * 8, gq);
       }
     }
 #pragma unroll
-    for (int j = 0; j < kMaxK; ++j) {
+    for (int j = 0; j < MAXR; ++j) {
       const float sj = warp_sum(dot[j]);
       if (lane == 0) s_dot[wid][j] = sj;
     }
@@ -271,12 +272,12 @@ permute_bwd_kernel(const __nv_bfloat16* __restrict__ dX, const int32_t* __restri
       if ((unsigned)mye < (unsigned)E) mydl = dlogits[(size_t)t * E + mye];
       else mye = -1;
     }
-    int rows[MAXR], es[kMaxK];
-    float dls[kMaxK];
+    int rows[MAXR], es[MAXR];
+    float dls[MAXR];
 #pragma unroll
     for (int j = 0; j < MAXR; ++j) rows[j] = __shfl_sync(0xffffffffu, myrow, j);
 #pragma unroll
-    for (int j = 0; j < kMaxK; ++j) {
+    for (int j = 0; j < MAXR; ++j) {
       es[j] = __shfl_sync(0xffffffffu, mye, j);
       dls[j] = __shfl_sync(0xffffffffu, mydl, j);
     }
@@ -305,7 +306,7 @@ permute_bwd_kernel(const __nv_bfloat16* __restrict__ dX, const int32_t* __restri
         for (int m = 0; m < 8; ++m) acc[m] += f[m];
       }
 #pragma unroll
-      for (int j = 0; j < kMaxK; ++j) {
+      for (int j = 0; j < MAXR; ++j) {
         if (j >= k || es[j] < 0) continue;
         const float d = dls[j];
         const float4* wr = reinterpret_cast<const float4*>(W_r + (size_t)es[j] * H + (size_t)c * 8);
@@ -418,9 +419,16 @@ cudaError_t launch_unpermute_bwd(const moe_config& c, const void* dY, const void
                                  const int32_t* row_of, const float* w, const int32_t* counts,
                                  const int32_t* offsets, void* dO_perm, float* dw,
                                  cudaStream_t s) {
-  unpermute_bwd_kernel<<<num_sms() * 16, 256, 0, s>>>(
-      static_cast<const __nv_bfloat16*>(dY), static_cast<const __nv_bfloat16*>(y_perm), row_of, w,
-      counts, offsets, static_cast<__nv_bfloat16*>(dO_perm), dw, c.T, c.H, c.k, c.E, c.n_shared);
+  auto dYp = static_cast<const __nv_bfloat16*>(dY);
+  auto yp = static_cast<const __nv_bfloat16*>(y_perm);
+  auto dOp = static_cast<__nv_bfloat16*>(dO_perm);
+  if (c.k + c.n_shared <= 4)
+    unpermute_bwd_kernel<4><<<num_sms() * 16, 256, 0, s>>>(dYp, yp, row_of, w, counts, offsets,
+                                                           dOp, dw, c.T, c.H, c.k, c.E,
+                                                           c.n_shared);
+  else
+    unpermute_bwd_kernel<kMaxK + 4><<<num_sms() * 16, 256, 0, s>>>(
+        dYp, yp, row_of, w, counts, offsets, dOp, dw, c.T, c.H, c.k, c.E, c.n_shared);
   return cudaGetLastError();
 }
 
