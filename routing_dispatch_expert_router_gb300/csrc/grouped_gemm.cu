@@ -105,7 +105,10 @@ __device__ __forceinline__ Tile decode(int tile, const int* prefix, const int* m
   return t;
 }
 
-__device__ __forceinline__ float silu_f(float z) { return z / (1.f + expf(-z)); }
+// Logistic sigmoid and SiLU for the SwiGLU epilogues, from the hardware exp2
+// approximation (the bf16 outputs keep 8 significant bits; this is far inside).
+__device__ __forceinline__ float sigmoid_f(float z) { return __frcp_rn(1.f + __expf(-z)); }
+__device__ __forceinline__ float silu_f(float z) { return z * sigmoid_f(z); }
 
 // Output staging: every epilogue warp owns kStageBytes of shared memory for up
 // to three 32 x 32 bf16 boxes, laid out with the 64-byte swizzle that the
@@ -194,7 +197,7 @@ __device__ __forceinline__ void epilogue_tile(const Params& p, const CUtensorMap
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
           const float dh = __uint_as_float(r[v * 8 + i]);
-          const float sg = 1.f / (1.f + expf(-gf[i]));
+          const float sg = sigmoid_f(gf[i]);
           dg[i] = dh * uf[i] * sg * (1.f + gf[i] * (1.f - sg));
           du[i] = dh * gf[i] * sg;
         }
