@@ -256,6 +256,14 @@ MOE_API moe_status moe_last_device_status(const void* scratch, int32_t* code, vo
 /* Resets the device status word (async on stream). */
 MOE_API moe_status moe_clear_device_status(void* scratch, void* stream);
 
+/* Health check of the device-side failure detection: launches one kernel that
+ * waits, through the same bounded mbarrier wait every grouped-GEMM role uses,
+ * on a barrier that nothing completes. After about `budget_cycles` SM clock
+ * cycles the wait gives up and MOE_ERR_TIMEOUT is recorded in the status word
+ * of `scratch` (read it with moe_last_device_status); the kernel then exits
+ * normally and the context stays usable. */
+MOE_API moe_status moe_check_bounded_wait(void* scratch, int64_t budget_cycles, void* stream);
+
 /* Static text for a status code. */
 MOE_API const char* moe_status_string(moe_status s);
 

@@ -25,7 +25,7 @@ ENTRY_POINTS = (
     "moe_grouped_ffn_fwd", "moe_unpermute",
     "moe_unpermute_bwd", "moe_grouped_ffn_bwd", "moe_route_bwd", "moe_permute_bwd",
     "moe_router_wgrad", "moe_layer_fwd", "moe_layer_bwd", "moe_last_device_status",
-    "moe_clear_device_status", "moe_status_string",
+    "moe_clear_device_status", "moe_check_bounded_wait", "moe_status_string",
 )
 
 
@@ -220,6 +220,13 @@ def moe_last_device_status(scratch, stream=None) -> int:
            lib().moe_last_device_status(ctypes.c_void_p(_ptr(scratch)), ctypes.byref(code),
                                         ctypes.c_void_p(_stream(stream))))
     return code.value
+
+
+def moe_check_bounded_wait(scratch, budget_cycles: int, stream=None):
+    f = lib().moe_check_bounded_wait
+    _check("moe_check_bounded_wait",
+           f(ctypes.c_void_p(_ptr(scratch)), ctypes.c_int64(int(budget_cycles)),
+             ctypes.c_void_p(_stream(stream))))
 
 
 def moe_clear_device_status(scratch, stream=None):

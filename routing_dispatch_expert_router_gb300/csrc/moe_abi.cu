@@ -6,6 +6,7 @@
 
 #include "common.cuh"
 #include "internal.h"
+#include "ptx.cuh"
 
 namespace moe {
 
@@ -119,6 +120,19 @@ static moe_status cuda_status(cudaError_t e) {
 
 static int32_t* status_word(void* scratch) {
   return reinterpret_cast<int32_t*>(static_cast<uint8_t*>(scratch) + kScratchStatus);
+}
+
+// Runs the bounded mbarrier wait that every grouped-GEMM role uses on a barrier
+// that nothing ever completes: the wait gives up after `budget` clock64 cycles
+// and records MOE_ERR_TIMEOUT in the status word, exactly as a stalled GEMM
+// pipeline would.
+__global__ void bounded_wait_check_kernel(int32_t* status, long long budget) {
+  __shared__ __align__(8) uint64_t bar;
+  if (threadIdx.x != 0) return;
+  const uint32_t b = ptx::smem_u32(&bar);
+  ptx::mbar_init(b, 1);
+  ptx::fence_mbar_init();
+  if (!ptx::mbar_wait(b, 0, budget, nullptr)) record_status(status, MOE_ERR_TIMEOUT);
 }
 
 }  // namespace moe
@@ -333,6 +347,14 @@ moe_status moe_clear_device_status(void* scratch, void* stream) {
   MOE_REQUIRE(al16(scratch));
   MOE_CUDA(cudaMemsetAsync(static_cast<uint8_t*>(scratch) + kScratchStatus, 0, sizeof(int32_t),
                            (cudaStream_t)stream));
+  return MOE_OK;
+}
+
+moe_status moe_check_bounded_wait(void* scratch, int64_t budget_cycles, void* stream) {
+  MOE_REQUIRE(al16(scratch) && budget_cycles > 0);
+  bounded_wait_check_kernel<<<1, 32, 0, (cudaStream_t)stream>>>(status_word(scratch),
+                                                                (long long)budget_cycles);
+  MOE_CUDA(cudaGetLastError());
   return MOE_OK;
 }
 
