@@ -108,10 +108,13 @@ __device__ __forceinline__ int find_pad_group(const int* prefix, int G, int p) {
 }
 
 // dO[row_tj] = bf16(w_tj dY[t]); dw_tj = <dY[t], y[row_tj]>; shared rows get dY.
-// One block per token (grid-stride over tokens, then over the padding rows of
-// dO, which are zeroed). Threads own 16-byte slices; the dot products are
-// reduced warp by warp and then across warps in a fixed order.
-template <int MAXR>
+// One warp per token (grid-stride over tokens, then over the zero padding rows
+// of dO). Lanes j < k+S fetch the token's rows and weights once; then each
+// lane walks its 16-byte slices U at a time, keeping the U dY slices and the
+// U*k y slices of one step in flight together. Every lane sums its slices in
+// order and the warp combines lanes by a fixed butterfly, so dw is
+// deterministic. No block-wide synchronisation on the token path.
+template <int MAXR, int U>
 __global__ void __launch_bounds__(256)
 unpermute_bwd_kernel(const __nv_bfloat16* __restrict__ dY, const __nv_bfloat16* __restrict__ y,
                      const int32_t* __restrict__ row_of, const float* __restrict__ w,
@@ -122,7 +125,6 @@ unpermute_bwd_kernel(const __nv_bfloat16* __restrict__ dY, const __nv_bfloat16* 
   __shared__ int s_off[kMaxGroups + 1];
   __shared__ int s_cnt[kMaxGroups];
   __shared__ int s_tmp[33];
-  __shared__ float s_dot[8][MAXR];
   const int G = E + S;
   for (int g = threadIdx.x; g <= G; g += blockDim.x) s_off[g] = offsets[g];
   for (int g = threadIdx.x; g < G; g += blockDim.x) s_cnt[g] = counts[g];
@@ -132,74 +134,80 @@ unpermute_bwd_kernel(const __nv_bfloat16* __restrict__ dY, const __nv_bfloat16* 
   const int P = block_exclusive_scan(s_pp, G, s_tmp);
   if (threadIdx.x == 0) s_pp[G] = P;
   __syncthreads();
-  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, nwarp = blockDim.x >> 5;
+  const int lane = threadIdx.x & 31;
   const int nvec = H >> 3, nr = k + S;
-  for (int v = blockIdx.x; v < T + P; v += gridDim.x) {
+  const int warps = gridDim.x * (blockDim.x >> 5);
+  for (int v = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); v < T + P; v += warps) {
     if (v >= T) {
       const int p = v - T;
       const int g = find_pad_group(s_pp, G, p);
       const int r = s_off[g] + s_cnt[g] + (p - s_pp[g]);
       const uint4 z = make_uint4(0u, 0u, 0u, 0u);
-      for (int c = threadIdx.x; c < nvec; c += blockDim.x)
-        stg_v4(dO + (size_t)r * H + (size_t)c * 8, z);
+      for (int c = lane; c < nvec; c += 32) stg_v4(dO + (size_t)r * H + (size_t)c * 8, z);
       continue;
     }
     const int t = v;
+    int myrow = -1;
+    float mywt = 0.f;
+    if (lane < k) {
+      myrow = row_of[(size_t)t * k + lane];
+      mywt = w[(size_t)t * k + lane];
+    } else if (lane < nr) {
+      myrow = s_off[E + lane - k] + t;
+    }
     int rows[MAXR];
-    float wts[MAXR];
+    float wts[MAXR], dot[MAXR];
 #pragma unroll
     for (int j = 0; j < MAXR; ++j) {
-      rows[j] = -1;
-      wts[j] = 0.f;
-      if (j >= nr) continue;
-      if (j < k) {
-        rows[j] = row_of[(size_t)t * k + j];
-        wts[j] = w[(size_t)t * k + j];
-      } else {
-        rows[j] = s_off[E + j - k] + t;
-      }
+      rows[j] = __shfl_sync(0xffffffffu, myrow, j);
+      wts[j] = __shfl_sync(0xffffffffu, mywt, j);
+      dot[j] = 0.f;
     }
-    float dot[MAXR];
+    const __nv_bfloat16* gsrc = dY + (size_t)t * H;
+    for (int c0 = lane; c0 < nvec; c0 += 32 * U) {
+      uint4 gq[U], yq[U][MAXR];
 #pragma unroll
-    for (int j = 0; j < MAXR; ++j) dot[j] = 0.f;
-    for (int c = threadIdx.x; c < nvec; c += blockDim.x) {
-      const uint4 gq = ldg_nc_v4(dY + (size_t)t * H + (size_t)c * 8);
-      uint4 yq[MAXR];
+      for (int u = 0; u < U; ++u) {
+        const int c = c0 + 32 * u;
+        if (c >= nvec) continue;
+        gq[u] = ldg_nc_v4(gsrc + (size_t)c * 8);
 #pragma unroll
-      for (int j = 0; j < MAXR; ++j)
-        if (j < k && rows[j] >= 0) yq[j] = ldg_nc_v4(y + (size_t)rows[j] * H + (size_t)c * 8);
-      float g[8];
-      unpack8(gq, g);
+        for (int j = 0; j < MAXR; ++j)
+          if (j < k && rows[j] >= 0) yq[u][j] = ldg_nc_v4(y + (size_t)rows[j] * H + (size_t)c * 8);
+      }
 #pragma unroll
-      for (int j = 0; j < MAXR; ++j) {
-        if (j >= k || rows[j] < 0) continue;
-        float f[8], o[8];
-        unpack8(yq[j], f);
+      for (int u = 0; u < U; ++u) {
+        const int c = c0 + 32 * u;
+        if (c >= nvec) continue;
+        float g[8];
+        unpack8(gq[u], g);
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          dot[j] = fmaf(g[i], f[i], dot[j]);
-          o[i] = wts[j] * g[i];
+        for (int j = 0; j < MAXR; ++j) {
+          if (j >= nr || rows[j] < 0) continue;
+          __nv_bfloat16* dst = dO + (size_t)rows[j] * H + (size_t)c * 8;
+          if (j >= k) {
+            stg_v4(dst, gq[u]);
+            continue;
+          }
+          float f[8], o[8];
+          unpack8(yq[u][j], f);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            dot[j] = fmaf(g[i], f[i], dot[j]);
+            o[i] = wts[j] * g[i];
+          }
+          stg_v4(dst, pack8(o));
         }
-        stg_v4(dO + (size_t)rows[j] * H + (size_t)c * 8, pack8(o));
-      }
-#pragma unroll
-      for (int j = 0; j < MAXR; ++j) {
-        if (j < k || j >= nr) continue;
-        stg_v4(dO + (size_t)rows[j] * H + (size_t)c * 8, gq);
       }
     }
+    float mine = 0.f;
 #pragma unroll
     for (int j = 0; j < MAXR; ++j) {
+      if (j >= k) break;
       const float sj = warp_sum(dot[j]);
-      if (lane == 0) s_dot[wid][j] = sj;
+      if (lane == j) mine = (rows[j] >= 0) ? sj : 0.f;
     }
-    __syncthreads();
-    if (threadIdx.x < k) {
-      float sj = 0.f;
-      for (int q = 0; q < nwarp; ++q) sj += s_dot[q][threadIdx.x];
-      dw[(size_t)t * k + threadIdx.x] = (rows[threadIdx.x] >= 0) ? sj : 0.f;
-    }
-    __syncthreads();
+    if (lane < k) dw[(size_t)t * k + lane] = mine;
   }
 }
 
@@ -422,12 +430,13 @@ cudaError_t launch_unpermute_bwd(const moe_config& c, const void* dY, const void
   auto dYp = static_cast<const __nv_bfloat16*>(dY);
   auto yp = static_cast<const __nv_bfloat16*>(y_perm);
   auto dOp = static_cast<__nv_bfloat16*>(dO_perm);
+  // one warp per token (8 per block), capped at 16 blocks per SM
+  const int grid = grid_for_warps(c.T);
   if (c.k + c.n_shared <= 4)
-    unpermute_bwd_kernel<4><<<num_sms() * 16, 256, 0, s>>>(dYp, yp, row_of, w, counts, offsets,
-                                                           dOp, dw, c.T, c.H, c.k, c.E,
-                                                           c.n_shared);
+    unpermute_bwd_kernel<4, 4><<<grid, 256, 0, s>>>(dYp, yp, row_of, w, counts, offsets, dOp, dw,
+                                                    c.T, c.H, c.k, c.E, c.n_shared);
   else
-    unpermute_bwd_kernel<kMaxK + 4><<<num_sms() * 16, 256, 0, s>>>(
+    unpermute_bwd_kernel<kMaxK + 4, 1><<<grid, 256, 0, s>>>(
         dYp, yp, row_of, w, counts, offsets, dOp, dw, c.T, c.H, c.k, c.E, c.n_shared);
   return cudaGetLastError();
 }
