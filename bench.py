@@ -148,6 +148,46 @@ def gemm_flops(shape, counts) -> tuple:
     return fwd, bwd
 
 
+def stage_table(shape, cfg, f, stage_ms, hbm_gbs, fl_fwd, fl_bwd, tc_peak):
+    """Per-stage device time, algorithmic bytes (or flops) and roofline fraction.
+
+    Bytes count each tensor a stage must read or write once (bf16 rows 2 B per
+    element, fp32 4 B, int32 maps 4 B): A kept routed assignments, S*T shared
+    rows, P zero padding rows of the permuted buffers."""
+    T, H, E, k, S = shape.T, shape.H, shape.E, shape.k, shape.n_shared
+    counts = f["counts"].cpu().tolist()
+    offsets = f["offsets"].cpu().tolist()
+    G = E + S
+    A = sum(counts[:E])
+    rows = A + S * T                     # filled rows of the permuted buffers
+    P = offsets[G] - sum(counts)         # padding rows
+    bf = 2
+    maps = T * k * 4 * 3                 # idx / row_of / w sized reads or writes
+    work = [
+        ("route", T * H * bf + E * H * 4 + T * E * 4 + 2 * T * k * 4, "router logits + top-k"),
+        ("permute", T * H * bf + (rows + P) * H * bf + maps, "hist + rank + row scatter"),
+        ("grouped_ffn_fwd", fl_fwd, "FC1+SwiGLU, FC2 (tcgen05)"),
+        ("unpermute", rows * H * bf + T * H * bf + maps, "gather-scale-reduce"),
+        ("unpermute_bwd", T * H * bf + A * H * bf + (rows + P) * H * bf + maps,
+         "dO scatter + dw dot products"),
+        ("route_bwd", T * E * 4 * 2 + maps, "dlogits"),
+        ("grouped_ffn_bwd", fl_bwd, "FC2 dgrad+SwiGLU bwd, FC1 dgrad, dW2, dW13 (tcgen05)"),
+        ("permute_bwd", rows * H * bf + T * H * bf + maps, "dx gather-reduce + router term"),
+        ("router_wgrad", T * H * bf + E * H * 4 + T * E * 4, "dW_r (each x row once)"),
+    ]
+    out = []
+    for (name, w, what), ms in zip(work, stage_ms):
+        if name.startswith("grouped_ffn"):
+            ach = w / (ms * 1e-3) / 1e12
+            out.append({"stage": name, "what": what, "ms": ms, "tflop": w / 1e12,
+                        "tflops": ach, "frac_tensor": ach / tc_peak})
+        else:
+            ach = w / (ms * 1e-3) / 1e9
+            out.append({"stage": name, "what": what, "ms": ms, "mb": w / 1e6,
+                        "gbs": ach, "frac_hbm": ach / hbm_gbs})
+    return out
+
+
 # ---------------------------------------------------------------------------- ours
 def run_ours(args, rank, world, local):
     import routing_dispatch_expert_router_gb300.binding as B
@@ -172,26 +212,34 @@ def run_ours(args, rank, world, local):
 
     def step(ev=None):
         # the layer step through the per-stage entry points (the same launches
-        # as moe_layer_fwd + moe_layer_bwd), with events around the GEMMs
+        # as moe_layer_fwd + moe_layer_bwd); ev[i] is recorded after stage i
+        # (ev[0] before the first), so every stage gets its own device time
+        rec = (lambda i: ev[i].record(stream)) if ev else (lambda i: None)
+        rec(0)
         B.moe_route(cfg, x, inp["W_r"], inp["bias"], f["logits"], f["idx"], f["w"], sc)
+        rec(1)
         B.moe_permute(cfg, x, f["idx"], f["counts"], f["offsets"], f["row_of"], f["token_of"],
                       f["sel_offsets"], f["sel_tokens"], f["x_perm"], sc)
-        if ev: ev[0].record(stream)
+        rec(2)
         B.moe_grouped_ffn_fwd(cfg, f["x_perm"], f["counts"], f["offsets"], inp["W13"], inp["W2"],
                               f["GU"], f["h"], f["y_perm"], sc)
-        if ev: ev[1].record(stream)
+        rec(3)
         B.moe_unpermute(cfg, f["y_perm"], f["row_of"], f["w"], f["offsets"], out)
+        rec(4)
         B.moe_unpermute_bwd(cfg, dY, f["y_perm"], f["row_of"], f["w"], f["counts"], f["offsets"],
                             b["dO_perm"], b["dw"])
+        rec(5)
         B.moe_route_bwd(cfg, f["logits"], f["idx"], f["w"], b["dw"], b["dlogits"])
-        if ev: ev[2].record(stream)
+        rec(6)
         B.moe_grouped_ffn_bwd(cfg, b["dO_perm"], f["x_perm"], f["GU"], f["h"], f["counts"],
                               f["offsets"], inp["W13"], inp["W2"], b["dGU"], b["dX_perm"], dW13,
                               dW2, sc)
-        if ev: ev[3].record(stream)
+        rec(7)
         B.moe_permute_bwd(cfg, b["dX_perm"], f["row_of"], f["offsets"], f["idx"], b["dlogits"],
                           inp["W_r"], dx)
+        rec(8)
         B.moe_router_wgrad(cfg, x, f["sel_offsets"], f["sel_tokens"], b["dlogits"], dW_r)
+        rec(9)
 
     launches_per_step = 2 + 3 + 2 + 1 + 1 + 1 + 4 + 1 + 1
     for _ in range(max(args.warmup, 3)):
@@ -203,7 +251,7 @@ def run_ours(args, rank, world, local):
     counts = f["counts"].cpu().tolist()
     fl_fwd, fl_bwd = gemm_flops(shape, counts)
 
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(10)] for _ in range(args.steps)]
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
     clocks = ClockSampler(local)
@@ -218,9 +266,9 @@ def run_ours(args, rank, world, local):
     torch.cuda.synchronize(dev)
     clk = clocks.stop()
     ms = t0.elapsed_time(t1)
-    gemm_ms = sum(e[0].elapsed_time(e[1]) + e[2].elapsed_time(e[3]) for e in evs) / args.steps
-    fwd_gemm_ms = sum(e[0].elapsed_time(e[1]) for e in evs) / args.steps
-    bwd_gemm_ms = sum(e[2].elapsed_time(e[3]) for e in evs) / args.steps
+    stage_ms = [sum(e[i].elapsed_time(e[i + 1]) for e in evs) / args.steps for i in range(9)]
+    fwd_gemm_ms, bwd_gemm_ms = stage_ms[2], stage_ms[6]
+    gemm_ms = fwd_gemm_ms + bwd_gemm_ms
 
     # end to end through the public layer calls, host buffers: every step copies
     # its x and dY from pinned host memory and reads out and dx back. Copies run
@@ -320,6 +368,7 @@ def run_ours(args, rank, world, local):
                      "gemm_ms_per_step": gemm_ms,
                      "fwd_gemm_ms": fwd_gemm_ms, "bwd_gemm_ms": bwd_gemm_ms,
                      "gemm_tflop_per_step": (fl_fwd + fl_bwd) / 1e12},
+        "stages": stage_table(shape, cfg, f, stage_ms, pk["hbm_gbs"], fl_fwd, fl_bwd, peak),
         "clocks": clk,
     }
     return res, shape, inp
