@@ -147,56 +147,133 @@ route_logits_few_kernel(const __nv_bfloat16* __restrict__ x, const float* __rest
   }
 }
 
-struct Cand {
-  double key;
-  int e;  // -1 = no candidate
-};
-
-__device__ __forceinline__ bool better(const Cand& a, const Cand& b) {
-  if (a.e < 0) return false;
-  if (b.e < 0) return true;
-  if (a.key > b.key) return true;
-  if (a.key < b.key) return false;
-  return a.e < b.e;
+// ---------------------------------------------------------------- selection
+// Selection compares keys as unsigned integers whose order is the numeric
+// order of the (non-NaN) floating-point keys: one integer compare instead of
+// a floating-point one (fp64 compares are slow on this part), and a 32-bit key
+// packed with the expert index makes "larger key, then lower index" a single
+// 64-bit max.
+__device__ __forceinline__ uint32_t ord32(float f) {
+  const uint32_t u = __float_as_uint(f);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+__device__ __forceinline__ float unord32(uint32_t k) {
+  return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
+}
+__device__ __forceinline__ uint64_t ord64(double d) {
+  const uint64_t u = (uint64_t)__double_as_longlong(d);
+  return (u >> 63) ? ~u : (u | (1ull << 63));
+}
+__device__ __forceinline__ double unord64(uint64_t k) {
+  return __longlong_as_double((long long)((k >> 63) ? (k & ~(1ull << 63)) : ~k));
+}
+// (key, expert) packed so that the maximum is the largest key, ties to the
+// lower expert; 0 = no candidate (every real key packs above it).
+__device__ __forceinline__ uint64_t pack_key(float key, int e) {
+  return ((uint64_t)ord32(key) << 32) | (uint64_t)(0xffffffffu - (uint32_t)e);
+}
+__device__ __forceinline__ int packed_expert(uint64_t p) {
+  return (int)(0xffffffffu - (uint32_t)(p & 0xffffffffu));
 }
 
-__device__ __forceinline__ Cand warp_best(Cand c) {
+__device__ __forceinline__ uint64_t warp_max_u64(uint64_t v) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
-    Cand d;
-    d.key = __shfl_xor_sync(0xffffffffu, c.key, o);
-    d.e = __shfl_xor_sync(0xffffffffu, c.e, o);
-    if (better(d, c)) c = d;
+    const uint64_t w = __shfl_xor_sync(0xffffffffu, v, o);
+    v = w > v ? w : v;
   }
-  return c;
+  return v;
+}
+
+// Largest (key, lowest expert) over the warp for 64-bit keys; key 0 = none.
+__device__ __forceinline__ void warp_best_pair(uint64_t& key, int& e) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const uint64_t k2 = __shfl_xor_sync(0xffffffffu, key, o);
+    const int e2 = __shfl_xor_sync(0xffffffffu, e, o);
+    if (k2 > key || (k2 == key && e2 < e)) {
+      key = k2;
+      e = e2;
+    }
+  }
 }
 
 // The two largest values held by the warp (duplicates count twice).
-__device__ __forceinline__ void warp_top2(double& a1, double& a2) {
+__device__ __forceinline__ void warp_top2_u64(uint64_t& a1, uint64_t& a2) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
-    const double b1 = __shfl_xor_sync(0xffffffffu, a1, o);
-    const double b2 = __shfl_xor_sync(0xffffffffu, a2, o);
-    const double hi = fmax(a1, b1);
-    const double lo = fmax(fmin(a1, b1), fmax(a2, b2));
+    const uint64_t b1 = __shfl_xor_sync(0xffffffffu, a1, o);
+    const uint64_t b2 = __shfl_xor_sync(0xffffffffu, a2, o);
+    const uint64_t hi = a1 > b1 ? a1 : b1;
+    const uint64_t lo1 = a1 > b1 ? b1 : a1;
+    const uint64_t lo2 = a2 > b2 ? a2 : b2;
     a1 = hi;
-    a2 = lo;
+    a2 = lo1 > lo2 ? lo1 : lo2;
+  }
+}
+__device__ __forceinline__ void warp_top2_f(float& a1, float& a2) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float b1 = __shfl_xor_sync(0xffffffffu, a1, o);
+    const float b2 = __shfl_xor_sync(0xffffffffu, a2, o);
+    const float hi = fmaxf(a1, b1);
+    a2 = fmaxf(fminf(a1, b1), fmaxf(a2, b2));
+    a1 = hi;
   }
 }
 
-// One warp per token: selection keys, optional group limit, top-k, weights.
-// Lane l owns experts l, l+32, l+64, ... (at most 8).
+__device__ __forceinline__ void top2_insert(uint64_t v, uint64_t& a1, uint64_t& a2) {
+  if (v > a1) {
+    a2 = a1;
+    a1 = v;
+  } else if (v > a2) {
+    a2 = v;
+  }
+}
+__device__ __forceinline__ void top2_insert_f(float v, float& a1, float& a2) {
+  if (v > a1) {
+    a2 = a1;
+    a1 = v;
+  } else if (v > a2) {
+    a2 = v;
+  }
+}
+
+// Keeps the topk_groups best groups given the group scores (lane g holds group
+// g's ordered fp64 score; ties to the lower group) and clears the availability
+// of every expert outside them.
+template <int NPL>
+__device__ __forceinline__ void keep_best_groups(uint64_t gs_mine, int lane, int n_groups,
+                                                 int topk_groups, int per, int E,
+                                                 bool (&avail)[NPL]) {
+  uint32_t kept = 0;
+  for (int r = 0; r < topk_groups; ++r) {
+    uint64_t key = (lane < n_groups && !((kept >> lane) & 1u)) ? gs_mine : 0ull;
+    int g = lane;
+    warp_best_pair(key, g);
+    kept |= 1u << g;
+  }
+#pragma unroll
+  for (int i = 0; i < NPL; ++i) {
+    const int e = lane + 32 * i;
+    if (e < E && !((kept >> (e / per)) & 1u)) avail[i] = false;
+  }
+}
+
+// One warp per token, softmax router: selection key = fp32 (logit + bias)
+// (NaN ranks last), optional group limit (group score = top-1 or top-2 sum of
+// the group's keys in fp64), top-k with ties to the lower expert, weights =
+// softmax over the selected (logit + bias). Lane l owns experts l, l+32, ...
 __global__ void __launch_bounds__(256)
-route_select_kernel(const float* __restrict__ logits, const float* __restrict__ bias,
-                    int32_t* __restrict__ idx, float* __restrict__ wout, int T, int E, int k,
-                    int score_fn, int n_groups, int topk_groups, int group_score,
-                    float route_scale) {
+route_select_softmax_kernel(const float* __restrict__ logits, const float* __restrict__ bias,
+                            int32_t* __restrict__ idx, float* __restrict__ wout, int T, int E,
+                            int k, int n_groups, int topk_groups, int group_score) {
+  constexpr int NPL = kMaxExperts / 32;
   const int lane = threadIdx.x & 31;
   const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   if (t >= T) return;
   const float* lrow = logits + (size_t)t * E;
-  constexpr int NPL = kMaxExperts / 32;
-  double key[NPL];
+  float key[NPL];
   bool avail[NPL];
 #pragma unroll
   for (int i = 0; i < NPL; ++i) {
@@ -204,105 +281,197 @@ route_select_kernel(const float* __restrict__ logits, const float* __restrict__ 
     avail[i] = e < E;
     key[i] = -INFINITY;
     if (e < E) {
-      const float l = lrow[e];
-      const float b = bias ? bias[e] : 0.f;
-      double v;
-      if (score_fn == MOE_SCORE_SOFTMAX) {
-        v = (double)__fadd_rn(l, b);
-      } else {
-        const double s = 1.0 / (1.0 + exp(-(double)l));
-        v = s + (double)b;
-      }
+      // (+ 0 turns a -0 sum into +0, which compares equal to it)
+      const float v = __fadd_rn(__fadd_rn(lrow[e], bias ? bias[e] : 0.f), 0.f);
       key[i] = isnan(v) ? -INFINITY : v;
     }
   }
   if (n_groups > 1) {
     const int per = E / n_groups;
-    double gs_mine = -INFINITY;   // lane g keeps group g's score
+    const bool two = group_score == MOE_GROUP_TOP2_SUM && per >= 2;
+    uint64_t gs_mine = 0;
     for (int g = 0; g < n_groups; ++g) {
-      double a1 = -INFINITY, a2 = -INFINITY;
+      float a1 = -INFINITY, a2 = -INFINITY;
 #pragma unroll
       for (int i = 0; i < NPL; ++i) {
         const int e = lane + 32 * i;
-        if (e < E && e / per == g) {
-          const double v = key[i];
-          if (v > a1) { a2 = a1; a1 = v; }
-          else if (v > a2) { a2 = v; }
-        }
+        if (e < E && e / per == g) top2_insert_f(key[i], a1, a2);
       }
-      warp_top2(a1, a2);
-      const double gsc = (group_score == MOE_GROUP_TOP2_SUM && per >= 2) ? a1 + a2 : a1;
-      if (lane == g) gs_mine = gsc;
+      warp_top2_f(a1, a2);
+      const double gsc = two ? (double)a1 + (double)a2 : (double)a1;
+      if (lane == g) gs_mine = ord64(gsc);
     }
-    // keep the topk_groups best groups (ties -> lower group)
-    uint32_t kept = 0;
-    for (int r = 0; r < topk_groups; ++r) {
-      Cand c;
-      c.key = gs_mine;
-      c.e = (lane < n_groups && !((kept >> lane) & 1u)) ? lane : -1;
-      c = warp_best(c);
-      if (c.e >= 0) kept |= 1u << c.e;
+    keep_best_groups<NPL>(gs_mine, lane, n_groups, topk_groups, per, E, avail);
+  }
+  int my_e = 0;
+  for (int j = 0; j < k; ++j) {
+    uint64_t best = 0;
+#pragma unroll
+    for (int i = 0; i < NPL; ++i) {
+      if (!avail[i]) continue;
+      const uint64_t p = pack_key(key[i], lane + 32 * i);
+      best = p > best ? p : best;
     }
+    best = warp_max_u64(best);
+    const int e = packed_expert(best);
+#pragma unroll
+    for (int i = 0; i < NPL; ++i)
+      if (lane + 32 * i == e) avail[i] = false;
+    if (lane == j) my_e = e;
+  }
+  // weights: softmax over the selected (logit + bias), relative to the first
+  float z = 0.f, z0 = 0.f;
+  {
+    const int e0 = __shfl_sync(0xffffffffu, my_e, 0);
+    z0 = __fadd_rn(lrow[e0], bias ? bias[e0] : 0.f);
+    if (lane < k) z = expf(__fadd_rn(lrow[my_e], bias ? bias[my_e] : 0.f) - z0);
+  }
+  float zs = 0.f;
+  for (int j = 0; j < k; ++j) zs += __shfl_sync(0xffffffffu, z, j);
+  if (lane < k) {
+    idx[(size_t)t * k + lane] = my_e;
+    wout[(size_t)t * k + lane] = z / zs;
+  }
+}
+
+// One warp per token, sigmoid router: s = sigmoid(logit) and selection key
+// s + bias, both in fp64 (NaN ranks last); optional group limit; top-k with
+// ties to the lower expert; weights route_scale * s / sum(s) over the
+// selected.
+//
+// fp64 is slow on this part, so the fp64 keys are computed only where they can
+// decide anything. Every key is first formed in fp32 (A, off the fp64 key by
+// at most 3.6e-7 + 6e-8 |A|). A group's top-m (m = 2 for the top-2 sum, else
+// 1) can only contain experts with A >= (the group's m-th best A) - margin,
+// and the final top-k only experts with A >= (the k-th best A among the kept
+// groups) - margin, with margin = 1e-5 (1 + |threshold|), well above twice
+// the fp32 error: any other expert has m (or k) experts whose fp64 key is
+// strictly larger. Those candidates get their fp64 keys, and the group scores
+// and the selection are taken on fp64 keys alone, so the result is the one
+// the fp64 keys of all experts give.
+__global__ void __launch_bounds__(128)
+route_select_sigmoid_kernel(const float* __restrict__ logits, const float* __restrict__ bias,
+                            int32_t* __restrict__ idx, float* __restrict__ wout, int T, int E,
+                            int k, int n_groups, int topk_groups, int group_score,
+                            float route_scale) {
+  constexpr int NPL = kMaxExperts / 32;
+  const int lane = threadIdx.x & 31;
+  const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (t >= T) return;
+  const float* lrow = logits + (size_t)t * E;
+  float A[NPL];
+  double s64[NPL];
+  bool avail[NPL], exact[NPL];
+#pragma unroll
+  for (int i = 0; i < NPL; ++i) {
+    const int e = lane + 32 * i;
+    avail[i] = e < E;
+    exact[i] = false;
+    A[i] = -INFINITY;
+    s64[i] = 0.0;
+    if (e < E) {
+      const float s32 = __fdiv_rn(1.f, 1.f + expf(-lrow[e]));
+      const float v = __fadd_rn(s32, bias ? bias[e] : 0.f);
+      A[i] = isnan(v) ? -INFINITY : v;
+    }
+  }
+  auto margin = [](float thr) { return 1e-5f * (1.f + fabsf(thr)); };
+  // fp64 key of owned expert i (the sigmoid computed once, logit and bias
+  // re-read from cache)
+  auto key64 = [&](int i) -> uint64_t {
+    const int e = lane + 32 * i;
+    if (!exact[i]) {
+      exact[i] = true;
+      s64[i] = 1.0 / (1.0 + exp(-(double)lrow[e]));
+    }
+    const double v = s64[i] + (double)(bias ? bias[e] : 0.f);
+    return isnan(v) ? ord64(-INFINITY) : ord64(v);
+  };
+  if (n_groups > 1) {
+    const int per = E / n_groups;
+    const bool two = group_score == MOE_GROUP_TOP2_SUM && per >= 2;
+    uint64_t gs_mine = 0;
+    for (int g = 0; g < n_groups; ++g) {
+      float a1 = -INFINITY, a2 = -INFINITY;
+#pragma unroll
+      for (int i = 0; i < NPL; ++i) {
+        const int e = lane + 32 * i;
+        if (e < E && e / per == g) top2_insert_f(A[i], a1, a2);
+      }
+      warp_top2_f(a1, a2);
+      const float am = two ? a2 : a1;
+      const float thr = am - margin(am);
+      uint64_t k1 = 0, k2 = 0;
+#pragma unroll
+      for (int i = 0; i < NPL; ++i) {
+        const int e = lane + 32 * i;
+        if (e < E && e / per == g && A[i] >= thr) top2_insert(key64(i), k1, k2);
+      }
+      warp_top2_u64(k1, k2);
+      const double gsc = two ? unord64(k1) + unord64(k2) : unord64(k1);
+      if (lane == g) gs_mine = ord64(gsc);
+    }
+    keep_best_groups<NPL>(gs_mine, lane, n_groups, topk_groups, per, E, avail);
+  }
+  // the k-th best fp32 key among the available experts
+  uint64_t kth = 0;
+  {
+    bool taken[NPL];
+#pragma unroll
+    for (int i = 0; i < NPL; ++i) taken[i] = false;
+    for (int j = 0; j < k; ++j) {
+      uint64_t best = 0;
+#pragma unroll
+      for (int i = 0; i < NPL; ++i) {
+        if (!avail[i] || taken[i]) continue;
+        const uint64_t p = pack_key(A[i], lane + 32 * i);
+        best = p > best ? p : best;
+      }
+      best = warp_max_u64(best);
+      const int e = packed_expert(best);
+#pragma unroll
+      for (int i = 0; i < NPL; ++i)
+        if (lane + 32 * i == e) taken[i] = true;
+      kth = best;
+    }
+  }
+  const float ak = unord32((uint32_t)(kth >> 32));
+  const float thr = ak - margin(ak);
+  uint64_t ck[NPL];
+#pragma unroll
+  for (int i = 0; i < NPL; ++i) ck[i] = (avail[i] && A[i] >= thr) ? key64(i) : 0ull;
+  int my_e = 0;
+  double my_s = 0.0;
+  for (int j = 0; j < k; ++j) {
+    uint64_t best = 0;
+    int be = 0x7fffffff;
 #pragma unroll
     for (int i = 0; i < NPL; ++i) {
       const int e = lane + 32 * i;
-      if (e < E && !((kept >> (e / per)) & 1u)) avail[i] = false;
+      if (ck[i] > best || (ck[i] == best && ck[i] != 0ull && e < be)) {
+        best = ck[i];
+        be = e;
+      }
     }
-  }
-  int sel_e[kMaxK];
-  for (int j = 0; j < k; ++j) {
-    Cand c;
-    c.key = -INFINITY;
-    c.e = -1;
-#pragma unroll
-    for (int i = 0; i < NPL; ++i) {
-      Cand d;
-      d.key = key[i];
-      d.e = avail[i] ? lane + 32 * i : -1;
-      if (better(d, c)) c = d;
-    }
-    c = warp_best(c);
-    sel_e[j] = c.e;
+    warp_best_pair(best, be);
+    double sv = 0.0;
 #pragma unroll
     for (int i = 0; i < NPL; ++i)
-      if (lane + 32 * i == c.e) avail[i] = false;
+      if (lane + 32 * i == be) {
+        ck[i] = 0ull;
+        sv = s64[i];
+      }
+    sv = __shfl_sync(0xffffffffu, sv, be & 31);
+    if (lane == j) {
+      my_e = be;
+      my_s = sv;
+    }
   }
-  // weights: every lane computes them; lane j writes slot j
-  if (score_fn == MOE_SCORE_SOFTMAX) {
-    float z[kMaxK];
-    float zs = 0.f;
-    for (int j = 0; j < k; ++j) {
-      const int e = sel_e[j];
-      z[j] = __fadd_rn(lrow[e], bias ? bias[e] : 0.f);
-    }
-    const float z0 = z[0];
-    for (int j = 0; j < k; ++j) {
-      z[j] = expf(z[j] - z0);
-      zs += z[j];
-    }
-    if (lane < k) {
-      float v = 0.f;
-      int ee = 0;
-      for (int j = 0; j < k; ++j)
-        if (j == lane) { v = z[j]; ee = sel_e[j]; }
-      idx[(size_t)t * k + lane] = ee;
-      wout[(size_t)t * k + lane] = v / zs;
-    }
-  } else {
-    double s[kMaxK];
-    double ss = 0.0;
-    for (int j = 0; j < k; ++j) {
-      s[j] = 1.0 / (1.0 + exp(-(double)lrow[sel_e[j]]));
-      ss += s[j];
-    }
-    if (lane < k) {
-      double v = 0.0;
-      int ee = 0;
-      for (int j = 0; j < k; ++j)
-        if (j == lane) { v = s[j]; ee = sel_e[j]; }
-      idx[(size_t)t * k + lane] = ee;
-      wout[(size_t)t * k + lane] = (float)((double)route_scale * v / ss);
-    }
+  double ss = 0.0;
+  for (int j = 0; j < k; ++j) ss += __shfl_sync(0xffffffffu, my_s, j);
+  if (lane < k) {
+    idx[(size_t)t * k + lane] = my_e;
+    wout[(size_t)t * k + lane] = (float)((double)route_scale * my_s / ss);
   }
 }
 
@@ -359,9 +528,13 @@ cudaError_t launch_route(const moe_config& c, const void* x, const float* W_r, c
     route_logits_kernel<64, 64><<<grid, 256, 0, s>>>(xb, W_r, logits, c.T, c.H, c.E);
   }
   if (cudaError_t err = cudaGetLastError(); err != cudaSuccess) return err;
-  route_select_kernel<<<(c.T + 7) / 8, 256, 0, s>>>(logits, bias, idx, w, c.T, c.E, c.k,
-                                                    c.score_fn, c.n_groups, c.topk_groups,
-                                                    c.group_score, c.route_scale);
+  if (c.score_fn == MOE_SCORE_SOFTMAX)
+    route_select_softmax_kernel<<<(c.T + 7) / 8, 256, 0, s>>>(
+        logits, bias, idx, w, c.T, c.E, c.k, c.n_groups, c.topk_groups, c.group_score);
+  else
+    route_select_sigmoid_kernel<<<(c.T + 3) / 4, 128, 0, s>>>(
+        logits, bias, idx, w, c.T, c.E, c.k, c.n_groups, c.topk_groups, c.group_score,
+        c.route_scale);
   return cudaGetLastError();
 }
 
