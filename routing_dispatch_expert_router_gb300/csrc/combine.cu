@@ -40,59 +40,96 @@ __device__ __forceinline__ void slot_row(const int32_t* row_of, const float* w,
   }
 }
 
-// out[t] = bf16( sum_j w_tj y[row_tj] + sum_s y[shared row] )
-// One warp per (token, 64-slice segment of the row): lanes j < k+S fetch the
-// token's rows once, then every lane keeps the k+S loads of its two 16-byte
-// slices in flight together and sums them in slot order.
-template <int MAXR>
-__global__ void __launch_bounds__(256)
-unpermute_kernel(const __nv_bfloat16* __restrict__ y, const int32_t* __restrict__ row_of,
-                 const float* __restrict__ w, const int32_t* __restrict__ offsets,
-                 __nv_bfloat16* __restrict__ out, int T, int H, int k, int E, int S) {
+// Gather-reduce, one warp per token (grid-stride):
+//   unpermute     out[t] = bf16( sum_j w_tj y[row_tj] + sum_s y[shared row s] )
+//   permute bwd   dx[t]  = bf16( sum_j dX[row_tj] + sum_s dX[shared row s]
+//                                + sum_j dl_tj W_r[e_tj] )          (ROUTER)
+// Lanes j < k+S fetch the token's rows (and weights, experts and dlogits) once;
+// then each lane walks its 16-byte slices U at a time with the U * (k+S) row
+// loads of a step in flight together, summing in slot order (fp32, fixed
+// order). The permuted rows are read once (L2 evict-first); the W_r rows are
+// read by every token (L2 evict-last).
+template <int MAXR, int U, bool ROUTER>
+__global__ void __launch_bounds__(256, (MAXR > 4) ? 2 : 3)
+gather_reduce_kernel(const __nv_bfloat16* __restrict__ src, const int32_t* __restrict__ row_of,
+                     const float* __restrict__ w, const int32_t* __restrict__ offsets,
+                     const int32_t* __restrict__ idx, const float* __restrict__ dlogits,
+                     const float* __restrict__ W_r, __nv_bfloat16* __restrict__ out, int T,
+                     int H, int k, int E, int S) {
   const int lane = threadIdx.x & 31;
   const int nvec = H >> 3, nr = k + S;
-  constexpr int VPL = (MAXR <= 4) ? 2 : 1;   // 16-byte slices per lane
-  const int segs = (nvec + 32 * VPL - 1) / (32 * VPL);
-  const long long items = (long long)T * segs;
-  const long long warps = (long long)gridDim.x * (blockDim.x >> 5);
-  for (long long it = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); it < items;
-       it += warps) {
-    const int t = (int)(it / segs), c0 = (int)(it % segs) * (32 * VPL) + lane;
-    int myrow = -1;
-    float mywt = 0.f;
+  const int warps = gridDim.x * (blockDim.x >> 5);
+  const uint64_t stream_pol = l2_evict_first_policy();
+  const uint64_t keep_pol = ROUTER ? l2_evict_last_policy() : 0ull;
+  for (int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); t < T; t += warps) {
+    int myrow = -1, mye = -1;
+    float mywt = 0.f, mydl = 0.f;
     if (lane < nr) slot_row(row_of, w, offsets, t, lane, k, E, myrow, mywt);
-    int rows[MAXR];
-    float wts[MAXR];
+    if (ROUTER && lane < k) {
+      mye = idx[(size_t)t * k + lane];
+      if ((unsigned)mye < (unsigned)E) mydl = dlogits[(size_t)t * E + mye];
+      else mye = -1;
+    }
+    int rows[MAXR], es[MAXR];
+    float wts[MAXR], dls[MAXR];
 #pragma unroll
     for (int j = 0; j < MAXR; ++j) {
       rows[j] = __shfl_sync(0xffffffffu, myrow, j);
       wts[j] = __shfl_sync(0xffffffffu, mywt, j);
-    }
-    uint4 q[VPL][MAXR];
-#pragma unroll
-    for (int u = 0; u < VPL; ++u) {
-      const int c = c0 + 32 * u;
-#pragma unroll
-      for (int j = 0; j < MAXR; ++j)
-        if (j < nr && rows[j] >= 0 && c < nvec)
-          q[u][j] = ldg_nc_v4(y + (size_t)rows[j] * H + (size_t)c * 8);
-    }
-#pragma unroll
-    for (int u = 0; u < VPL; ++u) {
-      const int c = c0 + 32 * u;
-      if (c >= nvec) continue;
-      float acc[8];
-#pragma unroll
-      for (int m = 0; m < 8; ++m) acc[m] = 0.f;
-#pragma unroll
-      for (int j = 0; j < MAXR; ++j) {
-        if (j >= nr || rows[j] < 0) continue;
-        float f[8];
-        unpack8(q[u][j], f);
-#pragma unroll
-        for (int m = 0; m < 8; ++m) acc[m] = fmaf(wts[j], f[m], acc[m]);
+      if (ROUTER) {
+        es[j] = __shfl_sync(0xffffffffu, mye, j);
+        dls[j] = __shfl_sync(0xffffffffu, mydl, j);
       }
-      stg_v4(out + (size_t)t * H + (size_t)c * 8, pack8(acc));
+    }
+    for (int c0 = lane; c0 < nvec; c0 += 32 * U) {
+      uint4 q[U][MAXR];
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int c = c0 + 32 * u;
+#pragma unroll
+        for (int j = 0; j < MAXR; ++j)
+          if (j < nr && rows[j] >= 0 && c < nvec)
+            q[u][j] = ldg_nc_v4_pol(src + (size_t)rows[j] * H + (size_t)c * 8, stream_pol);
+      }
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int c = c0 + 32 * u;
+        if (c >= nvec) continue;
+        float acc[8];
+#pragma unroll
+        for (int m = 0; m < 8; ++m) acc[m] = 0.f;
+#pragma unroll
+        for (int j = 0; j < MAXR; ++j) {
+          if (j >= nr || rows[j] < 0) continue;
+          float f[8];
+          unpack8(q[u][j], f);
+          if (ROUTER) {
+#pragma unroll
+            for (int m = 0; m < 8; ++m) acc[m] += f[m];
+          } else {
+#pragma unroll
+            for (int m = 0; m < 8; ++m) acc[m] = fmaf(wts[j], f[m], acc[m]);
+          }
+        }
+        if (ROUTER) {
+#pragma unroll
+          for (int j = 0; j < MAXR; ++j) {
+            if (j >= k || es[j] < 0) continue;
+            const float d = dls[j];
+            const float* wr = W_r + (size_t)es[j] * H + (size_t)c * 8;
+            const float4 a = ldg_nc_f4_pol(wr, keep_pol), b = ldg_nc_f4_pol(wr + 4, keep_pol);
+            acc[0] = fmaf(d, a.x, acc[0]);
+            acc[1] = fmaf(d, a.y, acc[1]);
+            acc[2] = fmaf(d, a.z, acc[2]);
+            acc[3] = fmaf(d, a.w, acc[3]);
+            acc[4] = fmaf(d, b.x, acc[4]);
+            acc[5] = fmaf(d, b.y, acc[5]);
+            acc[6] = fmaf(d, b.z, acc[6]);
+            acc[7] = fmaf(d, b.w, acc[7]);
+          }
+        }
+        stg_v4(out + (size_t)t * H + (size_t)c * 8, pack8(acc));
+      }
     }
   }
 }
@@ -226,35 +263,33 @@ route_bwd_kernel(const float* __restrict__ logits, const int32_t* __restrict__ i
   for (int e = lane; e < E; e += 32) row[e] = 0.f;
   __syncwarp();
   int e = 0;
-  double wj = 0.0, dwj = 0.0, sj = 0.0;
+  float wj = 0.f, dwj = 0.f, sj = 0.f;
   if (lane < k) {
     e = idx[(size_t)t * k + lane];
     wj = w[(size_t)t * k + lane];
     dwj = dw[(size_t)t * k + lane];
-    if ((unsigned)e < (unsigned)E) sj = 1.0 / (1.0 + exp(-(double)logits[(size_t)t * E + e]));
+    if ((unsigned)e < (unsigned)E) sj = __fdiv_rn(1.f, 1.f + expf(-logits[(size_t)t * E + e]));
   }
-  double v;
+  // fp32 throughout (at most 8 terms, relative error ~1e-6); fp64 arithmetic
+  // is slow on this GPU
+  float v;
   if (score_fn == MOE_SCORE_SOFTMAX) {
-    double inner = wj * dwj;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) inner += __shfl_xor_sync(0xffffffffu, inner, o);
+    const float inner = warp_sum(wj * dwj);
     v = wj * (dwj - inner);
   } else {
-    double ssum = sj, sdw = sj * dwj;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      ssum += __shfl_xor_sync(0xffffffffu, ssum, o);
-      sdw += __shfl_xor_sync(0xffffffffu, sdw, o);
-    }
-    const double ds = ((double)route_scale / ssum) * (dwj - sdw / ssum);
-    v = ds * sj * (1.0 - sj);
+    const float ssum = warp_sum(sj);
+    const float sdw = warp_sum(sj * dwj);
+    const float ds = (route_scale / ssum) * (dwj - sdw / ssum);
+    v = ds * sj * (1.f - sj);
   }
-  if (lane < k && (unsigned)e < (unsigned)E) row[e] = (float)v;
+  if (lane < k && (unsigned)e < (unsigned)E) row[e] = v;
 }
 
-// dx[t] = bf16( sum_j dX[row_tj] + sum_s dX[shared row] + sum_j dl_tj W_r[e_tj] )
-// Same warp-per-segment scheme as unpermute; the router term adds k fp32 rows
-// of W_r scaled by the token's dlogits.
+// Permute backward for many rows per token (k + S > 4): the same sum as
+// gather_reduce_kernel<.., ROUTER>, one warp per (token, 256-column segment):
+// a warp holds only one 16-byte slice of each row and of each W_r row, which
+// keeps registers (and so occupancy) where the k W_r rows would otherwise
+// push them.
 template <int MAXR>
 __global__ void __launch_bounds__(256)
 permute_bwd_kernel(const __nv_bfloat16* __restrict__ dX, const int32_t* __restrict__ row_of,
@@ -267,6 +302,7 @@ permute_bwd_kernel(const __nv_bfloat16* __restrict__ dX, const int32_t* __restri
   const int segs = (nvec + 32 * VPL - 1) / (32 * VPL);
   const long long items = (long long)T * segs;
   const long long warps = (long long)gridDim.x * (blockDim.x >> 5);
+  const uint64_t stream_pol = l2_evict_first_policy(), keep_pol = l2_evict_last_policy();
   for (long long it = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); it < items;
        it += warps) {
     const int t = (int)(it / segs), c0 = (int)(it % segs) * (32 * VPL) + lane;
@@ -296,7 +332,7 @@ permute_bwd_kernel(const __nv_bfloat16* __restrict__ dX, const int32_t* __restri
 #pragma unroll
       for (int j = 0; j < MAXR; ++j)
         if (j < nr && rows[j] >= 0 && c < nvec)
-          q[u][j] = ldg_nc_v4(dX + (size_t)rows[j] * H + (size_t)c * 8);
+          q[u][j] = ldg_nc_v4_pol(dX + (size_t)rows[j] * H + (size_t)c * 8, stream_pol);
     }
 #pragma unroll
     for (int u = 0; u < VPL; ++u) {
@@ -317,8 +353,8 @@ permute_bwd_kernel(const __nv_bfloat16* __restrict__ dX, const int32_t* __restri
       for (int j = 0; j < MAXR; ++j) {
         if (j >= k || es[j] < 0) continue;
         const float d = dls[j];
-        const float4* wr = reinterpret_cast<const float4*>(W_r + (size_t)es[j] * H + (size_t)c * 8);
-        const float4 a = __ldg(wr), b = __ldg(wr + 1);
+        const float* wr = W_r + (size_t)es[j] * H + (size_t)c * 8;
+        const float4 a = ldg_nc_f4_pol(wr, keep_pol), b = ldg_nc_f4_pol(wr + 4, keep_pol);
         acc[0] = fmaf(d, a.x, acc[0]);
         acc[1] = fmaf(d, a.y, acc[1]);
         acc[2] = fmaf(d, a.z, acc[2]);
@@ -409,18 +445,37 @@ static int grid_for_warps(int n_items) {
   return blocks < cap ? (blocks > 0 ? blocks : 1) : cap;
 }
 
+template <bool ROUTER>
+static cudaError_t launch_gather_reduce(const moe_config& c, const void* src,
+                                        const int32_t* row_of, const float* w,
+                                        const int32_t* offsets, const int32_t* idx,
+                                        const float* dlogits, const float* W_r, void* out,
+                                        cudaStream_t s) {
+  auto sp = static_cast<const __nv_bfloat16*>(src);
+  auto o = static_cast<__nv_bfloat16*>(out);
+  const int nr = c.k + c.n_shared;
+  const int grid = grid_for_warps(c.T);
+  if (nr <= 2)
+    gather_reduce_kernel<2, 4, ROUTER><<<grid, 256, 0, s>>>(sp, row_of, w, offsets, idx, dlogits,
+                                                           W_r, o, c.T, c.H, c.k, c.E,
+                                                           c.n_shared);
+  else if (nr <= 4)
+    gather_reduce_kernel<4, 2, ROUTER><<<grid, 256, 0, s>>>(sp, row_of, w, offsets, idx, dlogits,
+                                                           W_r, o, c.T, c.H, c.k, c.E,
+                                                           c.n_shared);
+  else if constexpr (ROUTER)
+    permute_bwd_kernel<kMaxK + 4><<<grid_for_vectors(c), 256, 0, s>>>(
+        sp, row_of, offsets, idx, dlogits, W_r, o, c.T, c.H, c.k, c.E, c.n_shared);
+  else
+    gather_reduce_kernel<kMaxK + 4, 1, false><<<grid, 256, 0, s>>>(
+        sp, row_of, w, offsets, idx, dlogits, W_r, o, c.T, c.H, c.k, c.E, c.n_shared);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_unpermute(const moe_config& c, const void* y_perm, const int32_t* row_of,
                              const float* w, const int32_t* offsets, void* out, cudaStream_t s) {
-  auto yp = static_cast<const __nv_bfloat16*>(y_perm);
-  auto o = static_cast<__nv_bfloat16*>(out);
-  if (c.k + c.n_shared <= 4)
-    unpermute_kernel<4><<<grid_for_vectors(c), 256, 0, s>>>(yp, row_of, w, offsets, o, c.T, c.H,
-                                                           c.k, c.E, c.n_shared);
-  else
-    unpermute_kernel<kMaxK + 4><<<grid_for_vectors(c), 256, 0, s>>>(yp, row_of, w, offsets, o,
-                                                                   c.T, c.H, c.k, c.E,
-                                                                   c.n_shared);
-  return cudaGetLastError();
+  return launch_gather_reduce<false>(c, y_perm, row_of, w, offsets, nullptr, nullptr, nullptr, out,
+                                     s);
 }
 
 cudaError_t launch_unpermute_bwd(const moe_config& c, const void* dY, const void* y_perm,
@@ -451,16 +506,8 @@ cudaError_t launch_route_bwd(const moe_config& c, const float* logits, const int
 cudaError_t launch_permute_bwd(const moe_config& c, const void* dX_perm, const int32_t* row_of,
                                const int32_t* offsets, const int32_t* idx, const float* dlogits,
                                const float* W_r, void* dx, cudaStream_t s) {
-  auto dXp = static_cast<const __nv_bfloat16*>(dX_perm);
-  auto o = static_cast<__nv_bfloat16*>(dx);
-  if (c.k + c.n_shared <= 4)
-    permute_bwd_kernel<4><<<grid_for_vectors(c), 256, 0, s>>>(dXp, row_of, offsets, idx, dlogits,
-                                                             W_r, o, c.T, c.H, c.k, c.E,
-                                                             c.n_shared);
-  else
-    permute_bwd_kernel<kMaxK + 4><<<grid_for_vectors(c), 256, 0, s>>>(
-        dXp, row_of, offsets, idx, dlogits, W_r, o, c.T, c.H, c.k, c.E, c.n_shared);
-  return cudaGetLastError();
+  return launch_gather_reduce<true>(c, dX_perm, row_of, nullptr, offsets, idx, dlogits, W_r, dx,
+                                    s);
 }
 
 cudaError_t launch_router_wgrad(const moe_config& c, const void* x, const int32_t* sel_offsets,

@@ -244,7 +244,7 @@ __device__ __forceinline__ void top2_insert_f(float v, float& a1, float& a2) {
 // of every expert outside them.
 template <int NPL>
 __device__ __forceinline__ void keep_best_groups(uint64_t gs_mine, int lane, int n_groups,
-                                                 int topk_groups, int per, int E,
+                                                 int topk_groups, const int (&gid)[NPL],
                                                  bool (&avail)[NPL]) {
   uint32_t kept = 0;
   for (int r = 0; r < topk_groups; ++r) {
@@ -254,9 +254,18 @@ __device__ __forceinline__ void keep_best_groups(uint64_t gs_mine, int lane, int
     kept |= 1u << g;
   }
 #pragma unroll
+  for (int i = 0; i < NPL; ++i)
+    if (gid[i] >= 0 && !((kept >> gid[i]) & 1u)) avail[i] = false;
+}
+
+// Group of each owned expert (-1 past E), computed once: the group loops
+// below would otherwise divide in their inner loops.
+template <int NPL>
+__device__ __forceinline__ void group_ids(int lane, int E, int per, int (&gid)[NPL]) {
+#pragma unroll
   for (int i = 0; i < NPL; ++i) {
     const int e = lane + 32 * i;
-    if (e < E && !((kept >> (e / per)) & 1u)) avail[i] = false;
+    gid[i] = e < E ? e / per : -1;
   }
 }
 
@@ -289,19 +298,19 @@ route_select_softmax_kernel(const float* __restrict__ logits, const float* __res
   if (n_groups > 1) {
     const int per = E / n_groups;
     const bool two = group_score == MOE_GROUP_TOP2_SUM && per >= 2;
+    int gid[NPL];
+    group_ids<NPL>(lane, E, per, gid);
     uint64_t gs_mine = 0;
     for (int g = 0; g < n_groups; ++g) {
       float a1 = -INFINITY, a2 = -INFINITY;
 #pragma unroll
-      for (int i = 0; i < NPL; ++i) {
-        const int e = lane + 32 * i;
-        if (e < E && e / per == g) top2_insert_f(key[i], a1, a2);
-      }
+      for (int i = 0; i < NPL; ++i)
+        if (gid[i] == g) top2_insert_f(key[i], a1, a2);
       warp_top2_f(a1, a2);
       const double gsc = two ? (double)a1 + (double)a2 : (double)a1;
       if (lane == g) gs_mine = ord64(gsc);
     }
-    keep_best_groups<NPL>(gs_mine, lane, n_groups, topk_groups, per, E, avail);
+    keep_best_groups<NPL>(gs_mine, lane, n_groups, topk_groups, gid, avail);
   }
   int my_e = 0;
   for (int j = 0; j < k; ++j) {
@@ -334,6 +343,43 @@ route_select_softmax_kernel(const float* __restrict__ logits, const float* __res
   }
 }
 
+// fp64 sigmoid of every owned expert whose bit is set in `need` (bit i =
+// expert lane + 32 i), spread over the warp: the candidates of all lanes are
+// numbered (by i, then lane) and lane n evaluates candidate n (32 per round),
+// then every owner picks its values up by shuffle. A warp instruction on the
+// fp64 pipe costs the same with one lane active as with 32, so this is up to
+// 32 times cheaper than every lane evaluating its own candidates.
+template <int NPL>
+__device__ __forceinline__ void exact_sigmoids(const float* __restrict__ lrow, uint32_t need,
+                                               int lane, double (&s64)[NPL]) {
+  uint32_t b[NPL];
+  int base[NPL + 1];
+  base[0] = 0;
+#pragma unroll
+  for (int i = 0; i < NPL; ++i) {
+    b[i] = __ballot_sync(0xffffffffu, (need >> i) & 1u);
+    base[i + 1] = base[i] + __popc(b[i]);
+  }
+  const int total = base[NPL];
+  for (int r0 = 0; r0 < total; r0 += 32) {
+    const int n = r0 + lane;
+    double sv = 0.0;
+    if (n < total) {
+      int e = 0;
+#pragma unroll
+      for (int i = 0; i < NPL; ++i)
+        if (n >= base[i] && n < base[i + 1]) e = (int)__fns(b[i], 0u, n - base[i] + 1) + 32 * i;
+      sv = 1.0 / (1.0 + exp(-(double)lrow[e]));
+    }
+#pragma unroll
+    for (int i = 0; i < NPL; ++i) {
+      const int slot = base[i] + __popc(b[i] & ((1u << lane) - 1u));
+      const double got = __shfl_sync(0xffffffffu, sv, (slot - r0) & 31);
+      if (((b[i] >> lane) & 1u) && slot >= r0 && slot < r0 + 32) s64[i] = got;
+    }
+  }
+}
+
 // One warp per token, sigmoid router: s = sigmoid(logit) and selection key
 // s + bias, both in fp64 (NaN ranks last); optional group limit; top-k with
 // ties to the lower expert; weights route_scale * s / sum(s) over the
@@ -361,12 +407,11 @@ route_select_sigmoid_kernel(const float* __restrict__ logits, const float* __res
   const float* lrow = logits + (size_t)t * E;
   float A[NPL];
   double s64[NPL];
-  bool avail[NPL], exact[NPL];
+  bool avail[NPL];
 #pragma unroll
   for (int i = 0; i < NPL; ++i) {
     const int e = lane + 32 * i;
     avail[i] = e < E;
-    exact[i] = false;
     A[i] = -INFINITY;
     s64[i] = 0.0;
     if (e < E) {
@@ -376,42 +421,45 @@ route_select_sigmoid_kernel(const float* __restrict__ logits, const float* __res
     }
   }
   auto margin = [](float thr) { return 1e-5f * (1.f + fabsf(thr)); };
-  // fp64 key of owned expert i (the sigmoid computed once, logit and bias
-  // re-read from cache)
+  // ordered fp64 key of owned expert i (its s64 must have been evaluated)
   auto key64 = [&](int i) -> uint64_t {
-    const int e = lane + 32 * i;
-    if (!exact[i]) {
-      exact[i] = true;
-      s64[i] = 1.0 / (1.0 + exp(-(double)lrow[e]));
-    }
-    const double v = s64[i] + (double)(bias ? bias[e] : 0.f);
+    const double v = s64[i] + (double)(bias ? bias[lane + 32 * i] : 0.f);
     return isnan(v) ? ord64(-INFINITY) : ord64(v);
   };
+  uint32_t have = 0;                               // bit i: s64[i] evaluated
   if (n_groups > 1) {
     const int per = E / n_groups;
     const bool two = group_score == MOE_GROUP_TOP2_SUM && per >= 2;
-    uint64_t gs_mine = 0;
+    int gid[NPL];
+    group_ids<NPL>(lane, E, per, gid);
+    // candidates for every group's top-m, from the fp32 keys
+    uint32_t gc = 0;
     for (int g = 0; g < n_groups; ++g) {
       float a1 = -INFINITY, a2 = -INFINITY;
 #pragma unroll
-      for (int i = 0; i < NPL; ++i) {
-        const int e = lane + 32 * i;
-        if (e < E && e / per == g) top2_insert_f(A[i], a1, a2);
-      }
+      for (int i = 0; i < NPL; ++i)
+        if (gid[i] == g) top2_insert_f(A[i], a1, a2);
       warp_top2_f(a1, a2);
       const float am = two ? a2 : a1;
       const float thr = am - margin(am);
+#pragma unroll
+      for (int i = 0; i < NPL; ++i)
+        if (gid[i] == g && A[i] >= thr) gc |= 1u << i;
+    }
+    exact_sigmoids<NPL>(lrow, gc, lane, s64);
+    have = gc;
+    // group scores on the fp64 keys of the candidates
+    uint64_t gs_mine = 0;
+    for (int g = 0; g < n_groups; ++g) {
       uint64_t k1 = 0, k2 = 0;
 #pragma unroll
-      for (int i = 0; i < NPL; ++i) {
-        const int e = lane + 32 * i;
-        if (e < E && e / per == g && A[i] >= thr) top2_insert(key64(i), k1, k2);
-      }
+      for (int i = 0; i < NPL; ++i)
+        if (((gc >> i) & 1u) && gid[i] == g) top2_insert(key64(i), k1, k2);
       warp_top2_u64(k1, k2);
       const double gsc = two ? unord64(k1) + unord64(k2) : unord64(k1);
       if (lane == g) gs_mine = ord64(gsc);
     }
-    keep_best_groups<NPL>(gs_mine, lane, n_groups, topk_groups, per, E, avail);
+    keep_best_groups<NPL>(gs_mine, lane, n_groups, topk_groups, gid, avail);
   }
   // the k-th best fp32 key among the available experts
   uint64_t kth = 0;
@@ -437,9 +485,14 @@ route_select_sigmoid_kernel(const float* __restrict__ logits, const float* __res
   }
   const float ak = unord32((uint32_t)(kth >> 32));
   const float thr = ak - margin(ak);
+  uint32_t fc = 0;                                 // candidates for the final top-k
+#pragma unroll
+  for (int i = 0; i < NPL; ++i)
+    if (avail[i] && A[i] >= thr) fc |= 1u << i;
+  if (__any_sync(0xffffffffu, (fc & ~have) != 0u)) exact_sigmoids<NPL>(lrow, fc & ~have, lane, s64);
   uint64_t ck[NPL];
 #pragma unroll
-  for (int i = 0; i < NPL; ++i) ck[i] = (avail[i] && A[i] >= thr) ? key64(i) : 0ull;
+  for (int i = 0; i < NPL; ++i) ck[i] = ((fc >> i) & 1u) ? key64(i) : 0ull;
   int my_e = 0;
   double my_s = 0.0;
   for (int j = 0; j < k; ++j) {
