@@ -208,6 +208,31 @@ def check_steps(shape, inp: dict, g: dict, backward: bool = True):
     assert_close("dW_r", f64(g["dW_r"]), dl.T @ x, atol=1e-3, rtol=1e-4)
 
 
+def wgrad_summand_scale(shape, x, dY, fwd, bwd):
+    """Sum over each group's rows of |a_r| |b_r|^T for dW13 = dGU^T x_perm and
+    dW2 = dO^T h. End to end, the GPU and the oracle round every dGU, GU and h
+    element to bf16 independently, so one summand can move by up to 2^-8 of
+    itself; over K rows the weight gradient can then differ by up to 2^-8 of
+    this sum (far more than 2^-8 of |result| when K is large and the terms
+    cancel). The end-to-end weight-gradient checks scale the relative
+    tolerance by |result| plus this sum; the per-step checks, which feed the
+    GPU's own dGU and x_perm to the oracle, keep the plain tolerance."""
+    E, S = shape.E, shape.n_shared
+    idx, kept = fwd["idx"], fwd["maps"]["row_of"] >= 0
+    s13 = np.zeros_like(bwd["dW13"])
+    s2 = np.zeros_like(bwd["dW2"])
+    for e in range(E):
+        tt, jj = np.nonzero((idx == e) & kept)
+        if tt.size == 0:
+            continue
+        s13[e] = np.abs(bwd["dGU"][tt, jj]).T @ np.abs(x[tt])
+        s2[e] = np.abs(bwd["dO"][tt, jj]).T @ np.abs(fwd["h"][tt, jj])
+    for s in range(S):
+        s13[E + s] = np.abs(bwd["dGU_s"][s]).T @ np.abs(x)
+        s2[E + s] = np.abs(O.round_bf16(dY)).T @ np.abs(fwd["h_s"][s])
+    return s13, s2
+
+
 def check_end_to_end(shape, inp: dict, g: dict, backward: bool = True):
     """The whole layer against the oracle run from the raw inputs."""
     x = f64(inp["x"])
@@ -220,10 +245,12 @@ def check_end_to_end(shape, inp: dict, g: dict, backward: bool = True):
     assert_close("out (e2e)", f64(g["out"]), fwd["out"])
     if not backward:
         return
-    bwd = O.layer_backward(shape, x, Wr, W13, W2, fwd, f64(inp["dY"]))
+    dY = f64(inp["dY"])
+    bwd = O.layer_backward(shape, x, Wr, W13, W2, fwd, dY)
     assert_close("dx (e2e)", f64(g["dx"]), bwd["dx"])
-    assert_close("dW13 (e2e)", f64(g["dW13"]), bwd["dW13"])
-    assert_close("dW2 (e2e)", f64(g["dW2"]), bwd["dW2"])
+    s13, s2 = wgrad_summand_scale(shape, x, dY, fwd, bwd)
+    assert_close("dW13 (e2e)", f64(g["dW13"]), bwd["dW13"], scale=np.abs(bwd["dW13"]) + s13)
+    assert_close("dW2 (e2e)", f64(g["dW2"]), bwd["dW2"], scale=np.abs(bwd["dW2"]) + s2)
     assert_close("dW_r (e2e)", f64(g["dW_r"]), bwd["dW_r"], atol=1e-2, rtol=1e-2)
 
 

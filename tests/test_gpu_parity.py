@@ -26,6 +26,8 @@ SHAPES = [
     MoEShape("capacity_drop", T=1024, H=128, E=16, k=4, F=128, score_fn=SIGMOID,
              capacity_factor=0.5, bias_kind="normal"),
     MoEShape("wide_tiles", T=640, H=512, E=4, k=2, F=768, n_shared=2),
+    # >= 512 rows per expert: the CTA-pair GEMM tiles (256 rows), ragged counts
+    MoEShape("pair_tiles", T=2100, H=512, E=4, k=2, F=512, n_shared=1),
 ]
 
 
@@ -36,7 +38,7 @@ def test_layer_steps_match_oracle(shape):
     H_.check_steps(shape, inp, g)
 
 
-@pytest.mark.parametrize("shape", SHAPES[:4], ids=lambda s: s.name)
+@pytest.mark.parametrize("shape", SHAPES[:4] + SHAPES[-1:], ids=lambda s: s.name)
 def test_layer_end_to_end_matches_oracle(shape):
     inp = make_inputs(shape, seed=1)
     g = H_.run_layer(shape, inp)
