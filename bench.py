@@ -232,8 +232,8 @@ def run_ours(args, rank, world, local):
         B.moe_route_bwd(cfg, f["logits"], f["idx"], f["w"], b["dw"], b["dlogits"])
         rec(6)
         B.moe_grouped_ffn_bwd(cfg, b["dO_perm"], f["x_perm"], f["GU"], f["h"], f["counts"],
-                              f["offsets"], inp["W13"], inp["W2"], b["dGU"], b["dX_perm"], dW13,
-                              dW2, sc)
+                              f["offsets"], f["token_of"], b["dlogits"], inp["W_r"], inp["W13"],
+                              inp["W2"], b["dGU"], b["dX_perm"], dW13, dW2, sc)
         rec(7)
         B.moe_permute_bwd(cfg, b["dX_perm"], f["row_of"], f["offsets"], f["idx"], b["dlogits"],
                           inp["W_r"], dx)

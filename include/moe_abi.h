@@ -211,12 +211,21 @@ MOE_API moe_status moe_unpermute_bwd(const moe_config* cfg, const void* dY, cons
 
 /* Backward of stage 3 (the W/D split of es summary §2.3.B: separate data- and
  * weight-gradient GEMMs): dh = dO W2[g] (fp32, not stored); SwiGLU backward
- * with the stored GU -> dGU (bf16); dW2[g] = dO^T h; dX_perm = dGU W13[g];
- * dW13[g] = dGU^T x_perm (weight gradients in bf16, zero for empty groups). */
+ * with the stored GU -> dGU (bf16); dW2[g] = dO^T h; dW13[g] = dGU^T x_perm
+ * (weight gradients in bf16, zero for empty groups);
+ * dX_perm[r] = bf16( dGU[r] W13[g] + dlogits[token_of[r], g] W_r[g] ) for the
+ * rows r of a routed expert g (< E), bf16(dGU[r] W13[g]) for shared experts.
+ * The second term is the router-logit gradient of the row's assignment: the
+ * part of dx that flows through logit (t, g). It is added in the GEMM's fp32
+ * epilogue, where W_r[g] is one row for a whole tile, instead of in
+ * moe_permute_bwd, which would read k rows of W_r for every token.
+ * token_of [rows_max] i32 and dlogits [T,E] f32 come from moe_permute and
+ * moe_route_bwd; W_r [E,H] f32. */
 MOE_API moe_status moe_grouped_ffn_bwd(const moe_config* cfg, const void* dO_perm, const void* x_perm,
                                const void* GU, const void* h, const int32_t* counts,
-                               const int32_t* offsets, const void* W13, const void* W2,
-                               void* dGU, void* dX_perm, void* dW13, void* dW2,
+                               const int32_t* offsets, const int32_t* token_of,
+                               const float* dlogits, const float* W_r, const void* W13,
+                               const void* W2, void* dGU, void* dX_perm, void* dW13, void* dW2,
                                void* scratch, void* stream);
 
 /* Backward of the routing weights to the logits (dense [T,E], zero outside the
@@ -225,9 +234,13 @@ MOE_API moe_status moe_grouped_ffn_bwd(const moe_config* cfg, const void* dO_per
 MOE_API moe_status moe_route_bwd(const moe_config* cfg, const float* logits, const int32_t* idx,
                          const float* w, const float* dw, float* dlogits, void* stream);
 
-/* Backward of stage 2 plus the router's input gradient:
+/* Backward of stage 2 plus the rest of the router's input gradient:
  * dx[t] = bf16( sum_j dX_perm[row_of[t,j]] + sum_s dX_perm[offsets[E+s]+t]
- *               + sum_j dlogits[t, idx[t,j]] W_r[idx[t,j]] ). */
+ *               + sum_{j: row_of[t,j] = -1} dlogits[t, idx[t,j]] W_r[idx[t,j]] ).
+ * dX_perm as moe_grouped_ffn_bwd writes it, which already holds the router
+ * term of every kept assignment; only assignments dropped by the capacity
+ * limit add theirs here. Together: dx[t] = sum over t's rows of the expert
+ * input gradients + dlogits[t,:] W_r. */
 MOE_API moe_status moe_permute_bwd(const moe_config* cfg, const void* dX_perm, const int32_t* row_of,
                            const int32_t* offsets, const int32_t* idx, const float* dlogits,
                            const float* W_r, void* dx, void* stream);

@@ -184,10 +184,10 @@ def moe_unpermute_bwd(cfg, dY, y_perm, row_of, w, counts, offsets, dO_perm, dw, 
           _stream(stream))
 
 
-def moe_grouped_ffn_bwd(cfg, dO_perm, x_perm, GU, h, counts, offsets, W13, W2, dGU, dX_perm,
-                        dW13, dW2, scratch, stream=None):
-    _call("moe_grouped_ffn_bwd", _cfg(cfg), dO_perm, x_perm, GU, h, counts, offsets, W13, W2,
-          dGU, dX_perm, dW13, dW2, scratch, _stream(stream))
+def moe_grouped_ffn_bwd(cfg, dO_perm, x_perm, GU, h, counts, offsets, token_of, dlogits, W_r,
+                        W13, W2, dGU, dX_perm, dW13, dW2, scratch, stream=None):
+    _call("moe_grouped_ffn_bwd", _cfg(cfg), dO_perm, x_perm, GU, h, counts, offsets, token_of,
+          dlogits, W_r, W13, W2, dGU, dX_perm, dW13, dW2, scratch, _stream(stream))
 
 
 def moe_route_bwd(cfg, logits, idx, w, dw, dlogits, stream=None):

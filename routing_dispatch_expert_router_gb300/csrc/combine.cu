@@ -43,7 +43,11 @@ __device__ __forceinline__ void slot_row(const int32_t* row_of, const float* w,
 // Gather-reduce, one warp per token (grid-stride):
 //   unpermute     out[t] = bf16( sum_j w_tj y[row_tj] + sum_s y[shared row s] )
 //   permute bwd   dx[t]  = bf16( sum_j dX[row_tj] + sum_s dX[shared row s]
-//                                + sum_j dl_tj W_r[e_tj] )          (ROUTER)
+//                                + sum_{j dropped} dl_tj W_r[e_tj] )          (ROUTER)
+// (the FC1 data-gradient GEMM has already added dl_tj W_r[e_tj] to the row of
+// every kept assignment; only capacity-dropped assignments have no row, and
+// without a capacity limit the permute backward is a plain gather with unit
+// weights)
 // Lanes j < k+S fetch the token's rows (and weights, experts and dlogits) once;
 // then each lane walks its 16-byte slices U at a time with the U * (k+S) row
 // loads of a step in flight together, summing in slot order (fp32, fixed
@@ -114,7 +118,7 @@ gather_reduce_kernel(const __nv_bfloat16* __restrict__ src, const int32_t* __res
         if (ROUTER) {
 #pragma unroll
           for (int j = 0; j < MAXR; ++j) {
-            if (j >= k || es[j] < 0) continue;
+            if (j >= k || es[j] < 0 || rows[j] >= 0) continue;
             const float d = dls[j];
             const float* wr = W_r + (size_t)es[j] * H + (size_t)c * 8;
             const float4 a = ldg_nc_f4_pol(wr, keep_pol), b = ldg_nc_f4_pol(wr + 4, keep_pol);
@@ -285,8 +289,9 @@ route_bwd_kernel(const float* __restrict__ logits, const int32_t* __restrict__ i
   if (lane < k && (unsigned)e < (unsigned)E) row[e] = v;
 }
 
-// Permute backward for many rows per token (k + S > 4): the same sum as
-// gather_reduce_kernel<.., ROUTER>, one warp per (token, 256-column segment):
+// Permute backward with capacity drops and many rows per token (k + S > 4):
+// the same sum as gather_reduce_kernel<.., ROUTER>, one warp per (token,
+// 256-column segment):
 // a warp holds only one 16-byte slice of each row and of each W_r row, which
 // keeps registers (and so occupancy) where the k W_r rows would otherwise
 // push them.
@@ -351,7 +356,7 @@ permute_bwd_kernel(const __nv_bfloat16* __restrict__ dX, const int32_t* __restri
       }
 #pragma unroll
       for (int j = 0; j < MAXR; ++j) {
-        if (j >= k || es[j] < 0) continue;
+        if (j >= k || es[j] < 0 || rows[j] >= 0) continue;
         const float d = dls[j];
         const float* wr = W_r + (size_t)es[j] * H + (size_t)c * 8;
         const float4 a = ldg_nc_f4_pol(wr, keep_pol), b = ldg_nc_f4_pol(wr + 4, keep_pol);
@@ -506,6 +511,9 @@ cudaError_t launch_route_bwd(const moe_config& c, const float* logits, const int
 cudaError_t launch_permute_bwd(const moe_config& c, const void* dX_perm, const int32_t* row_of,
                                const int32_t* offsets, const int32_t* idx, const float* dlogits,
                                const float* W_r, void* dx, cudaStream_t s) {
+  if (!(c.capacity_factor > 0.f))   // no assignment is dropped
+    return launch_gather_reduce<false>(c, dX_perm, row_of, nullptr, offsets, nullptr, nullptr,
+                                       nullptr, dx, s);
   return launch_gather_reduce<true>(c, dX_perm, row_of, nullptr, offsets, idx, dlogits, W_r, dx,
                                     s);
 }

@@ -45,7 +45,7 @@ constexpr int kStageAll = 4 * kStageBytes;
 constexpr long long kWaitBudget = 4000000000LL;   // clock64 cycles (~2 s)
 
 enum Epi : int { kEpiSwigluFwd = 0, kEpiStore = 1, kEpiSwigluBwd = 2, kEpiWgrad = 3,
-                 kEpiStoreF32 = 4 };
+                 kEpiStoreF32 = 4, kEpiDgradRouter = 5 };
 
 struct Params {
   int kgrouped;               // 0: row-grouped, 1: K-grouped
@@ -67,6 +67,12 @@ struct Params {
   int32_t* status;
   int dense_rows;             // > 0: one group of this many rows at row 0 (no counts/offsets)
   int a_kwrap;                // > 0: A's k coordinate wraps at this width (A repeated along K)
+  // FC1 data gradient with the router term (kEpiDgradRouter): row r of a
+  // routed group g < router_E gains dlogits[token_of[r], g] * W_r[g, :]
+  const int32_t* token_of;
+  const float* dlogits;
+  const float* W_r;
+  int router_E;
 };
 
 template <int BN, int STAGES>
@@ -148,6 +154,14 @@ __device__ __forceinline__ void epilogue_tile(const Params& p, const CUtensorMap
   const int row0 = (EPI == kEpiWgrad) ? g * p.Mw + mt * BM + q * 32 : s_off[g] + mt * BM + q * 32;
   const int ncols = (EPI == kEpiSwigluFwd) ? BN / 2 : BN;
   const int f0 = (EPI == kEpiSwigluFwd) ? nt * (BN / 2) : nt * BN;
+  // router term of this warp's row (lane) for the FC1 data gradient
+  float rd = 0.f;
+  const float* rw = nullptr;
+  if (EPI == kEpiDgradRouter && g < p.router_E) {
+    const int t = p.token_of[row0 + lane];
+    if (t >= 0) rd = p.dlogits[(long long)t * p.router_E + g];
+    rw = p.W_r + (long long)g * p.N + f0;
+  }
   uint4 gq[4], uq[4];
   const __nv_bfloat16* gu = nullptr;
   if (EPI == kEpiSwigluBwd) {
@@ -234,6 +248,17 @@ __device__ __forceinline__ void epilogue_tile(const Params& p, const CUtensorMap
       } else {
         ptx::tmem_ld32(tbase + c, r);
         ptx::tmem_ld_wait();
+      }
+      if (EPI == kEpiDgradRouter && rw) {
+        // fp32 accumulator + dlogits * W_r, rounded to bf16 once
+#pragma unroll
+        for (int v = 0; v < 8; ++v) {
+          const float4 w4 = __ldg(reinterpret_cast<const float4*>(rw + c) + v);
+          r[4 * v] = __float_as_uint(fmaf(rd, w4.x, __uint_as_float(r[4 * v])));
+          r[4 * v + 1] = __float_as_uint(fmaf(rd, w4.y, __uint_as_float(r[4 * v + 1])));
+          r[4 * v + 2] = __float_as_uint(fmaf(rd, w4.z, __uint_as_float(r[4 * v + 2])));
+          r[4 * v + 3] = __float_as_uint(fmaf(rd, w4.w, __uint_as_float(r[4 * v + 3])));
+        }
       }
       pack_slice(r, o0);
     }
@@ -928,7 +953,8 @@ cudaError_t launch_ffn_fc2_dgrad(const moe_config& c, const void* dO_perm, const
 }
 
 cudaError_t launch_ffn_fc1_dgrad(const moe_config& c, const void* dGU, const int32_t* counts,
-                                 const int32_t* offsets, const void* W13, void* dX_perm,
+                                 const int32_t* offsets, const void* W13, const int32_t* token_of,
+                                 const float* dlogits, const float* W_r, void* dX_perm,
                                  int32_t* status, cudaStream_t s) {
   const int64_t R = rows_max(c);
   const int G = c.E + c.n_shared;
@@ -945,9 +971,13 @@ cudaError_t launch_ffn_fc1_dgrad(const moe_config& c, const void* dGU, const int
   p.b_rows = 2 * c.F;
   p.out = static_cast<__nv_bfloat16*>(dX_perm);
   p.ldo = c.H;
-  if (use_pairs(c, c.H)) return run_pair<kEpiStore, 0, 1>(a, b, oc, oc2, p, s);
-  return bn == 256 ? run<kEpiStore, 256, 0, 1, 4>(a, b, oc, oc2, p, s)
-                   : run<kEpiStore, 128, 0, 1, 6>(a, b, oc, oc2, p, s);
+  p.token_of = token_of;
+  p.dlogits = dlogits;
+  p.W_r = W_r;
+  p.router_E = c.E;
+  if (use_pairs(c, c.H)) return run_pair<kEpiDgradRouter, 0, 1>(a, b, oc, oc2, p, s);
+  return bn == 256 ? run<kEpiDgradRouter, 256, 0, 1, 4>(a, b, oc, oc2, p, s)
+                   : run<kEpiDgradRouter, 128, 0, 1, 6>(a, b, oc, oc2, p, s);
 }
 
 cudaError_t launch_ffn_wgrad_fc2(const moe_config& c, const void* dO_perm, const void* h,

@@ -79,7 +79,8 @@ cudaError_t launch_ffn_fc2_dgrad(const moe_config& c, const void* dO_perm, const
                                  const int32_t* offsets, const void* W2, const void* GU,
                                  void* dGU, int32_t* status, cudaStream_t s);
 cudaError_t launch_ffn_fc1_dgrad(const moe_config& c, const void* dGU, const int32_t* counts,
-                                 const int32_t* offsets, const void* W13, void* dX_perm,
+                                 const int32_t* offsets, const void* W13, const int32_t* token_of,
+                                 const float* dlogits, const float* W_r, void* dX_perm,
                                  int32_t* status, cudaStream_t s);
 cudaError_t launch_ffn_wgrad_fc2(const moe_config& c, const void* dO_perm, const void* h,
                                  const int32_t* counts, const int32_t* offsets, void* dW2,

@@ -239,12 +239,14 @@ moe_status moe_unpermute_bwd(const moe_config* cfg, const void* dY, const void* 
 
 moe_status moe_grouped_ffn_bwd(const moe_config* cfg, const void* dO_perm, const void* x_perm,
                                const void* GU, const void* h, const int32_t* counts,
-                               const int32_t* offsets, const void* W13, const void* W2,
-                               void* dGU, void* dX_perm, void* dW13, void* dW2, void* scratch,
-                               void* stream) {
+                               const int32_t* offsets, const int32_t* token_of,
+                               const float* dlogits, const float* W_r, const void* W13,
+                               const void* W2, void* dGU, void* dX_perm, void* dW13, void* dW2,
+                               void* scratch, void* stream) {
   MOE_TRY(check_config(cfg));
   MOE_REQUIRE(al16(dO_perm) && al16(x_perm) && al16(GU) && al16(h) && al4(counts));
-  MOE_REQUIRE(al4(offsets) && al16(W13) && al16(W2) && al16(dGU) && al16(dX_perm));
+  MOE_REQUIRE(al4(offsets) && al4(token_of) && tok4(cfg, dlogits) && al16(W_r));
+  MOE_REQUIRE(al16(W13) && al16(W2) && al16(dGU) && al16(dX_perm));
   MOE_REQUIRE(al16(dW13) && al16(dW2) && al16(scratch));
   cudaStream_t s = (cudaStream_t)stream;
   int32_t* st = status_word(scratch);
@@ -260,7 +262,8 @@ moe_status moe_grouped_ffn_bwd(const moe_config* cfg, const void* dO_perm, const
     MOE_CUDA(launch_quant_cols(h, q.bF, offsets, G, R, F, s));
     MOE_CUDA(launch_ffn_wgrad_fc2(*cfg, q.cH, q.bF, counts, offsets, dW2, st, s));
     MOE_CUDA(launch_quant_rows(dGU, q.d2F, offsets, G, R, 2 * F, s));
-    MOE_CUDA(launch_ffn_fc1_dgrad(*cfg, q.d2F, counts, offsets, q.W13q, dX_perm, st, s));
+    MOE_CUDA(launch_ffn_fc1_dgrad(*cfg, q.d2F, counts, offsets, q.W13q, token_of, dlogits, W_r,
+                                  dX_perm, st, s));
     MOE_CUDA(launch_quant_cols(dGU, q.d2F, offsets, G, R, 2 * F, s));
     MOE_CUDA(launch_quant_cols(x_perm, q.aH, offsets, G, R, H, s));
     MOE_CUDA(launch_ffn_wgrad_fc1(*cfg, q.d2F, q.aH, counts, offsets, dW13, st, s));
@@ -268,7 +271,8 @@ moe_status moe_grouped_ffn_bwd(const moe_config* cfg, const void* dO_perm, const
   }
   MOE_CUDA(launch_ffn_fc2_dgrad(*cfg, dO_perm, counts, offsets, W2, GU, dGU, st, s));
   MOE_CUDA(launch_ffn_wgrad_fc2(*cfg, dO_perm, h, counts, offsets, dW2, st, s));
-  MOE_CUDA(launch_ffn_fc1_dgrad(*cfg, dGU, counts, offsets, W13, dX_perm, st, s));
+  MOE_CUDA(launch_ffn_fc1_dgrad(*cfg, dGU, counts, offsets, W13, token_of, dlogits, W_r, dX_perm,
+                                st, s));
   MOE_CUDA(launch_ffn_wgrad_fc1(*cfg, dGU, x_perm, counts, offsets, dW13, st, s));
   return MOE_OK;
 }
@@ -326,8 +330,8 @@ moe_status moe_layer_bwd(const moe_config* cfg, const moe_params* P, const void*
                             bs->dO_perm, bs->dw, stream));
   MOE_TRY(moe_route_bwd(cfg, st->logits, st->idx, st->w, bs->dw, bs->dlogits, stream));
   MOE_TRY(moe_grouped_ffn_bwd(cfg, bs->dO_perm, st->x_perm, st->GU, st->h, st->counts,
-                              st->offsets, P->W13, P->W2, bs->dGU, bs->dX_perm, dW13, dW2,
-                              scratch, stream));
+                              st->offsets, st->token_of, bs->dlogits, P->W_r, P->W13, P->W2,
+                              bs->dGU, bs->dX_perm, dW13, dW2, scratch, stream));
   MOE_TRY(moe_permute_bwd(cfg, bs->dX_perm, st->row_of, st->offsets, st->idx, bs->dlogits,
                           P->W_r, dx, stream));
   MOE_TRY(moe_router_wgrad(cfg, x, st->sel_offsets, st->sel_tokens, bs->dlogits, dW_r, stream));

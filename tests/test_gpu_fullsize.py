@@ -92,6 +92,7 @@ def test_full_size_layer_matches_oracle_on_samples(shape):
     H_.assert_equal("x_perm rows", xp_rows, ref_rows)
     # ---- per-group steps on sampled rows
     dY_dev = inp["dY"]
+    dl_all = host(g["dlogits"])
     for gi in pick_groups(cnt, E, S, rng):
         n = int(cnt[gi])
         sel = np.sort(rng.choice(n, size=min(n, 48), replace=False)) + off[gi]
@@ -107,7 +108,10 @@ def test_full_size_layer_matches_oracle_on_samples(shape):
         dO = host(g["dO_perm"][rs])
         dGU = host(g["dGU"][rs])
         H_.assert_close(f"dGU g={gi}", dGU, O.expert_fc2_dgrad_swiglu(qr(dO), w2, GU))
-        H_.assert_close(f"dX g={gi}", host(g["dX_perm"][rs]), O.expert_fc1_dgrad(qr(dGU), w13))
+        ref_dx = O.expert_fc1_dgrad(qr(dGU), w13, rounding=False)
+        if gi < E:   # the row's router-logit gradient, added before the bf16 rounding
+            ref_dx = ref_dx + dl_all[m["token_of"][sel], gi][:, None] * Wr[gi][None, :]
+        H_.assert_close(f"dX g={gi}", host(g["dX_perm"][rs]), O.round_bf16(ref_dx))
         # weight gradients over all the group's rows, on sampled output rows
         allr = slice(int(off[gi]), int(off[gi]) + n)
         oh = rng.choice(Hd, size=32, replace=False)
@@ -148,11 +152,12 @@ def test_full_size_layer_matches_oracle_on_samples(shape):
     for t in ts[:16]:
         acc = np.zeros(Hd)
         for j in range(k):
-            if rof[t, j] >= 0:
+            if rof[t, j] >= 0:        # kept rows already hold their router term
                 acc += host(g["dX_perm"][int(rof[t, j])])
+            else:                     # dropped by the capacity limit
+                acc += dl[t, idx[t, j]] * Wr[idx[t, j]]
         for s in range(S):
             acc += host(g["dX_perm"][int(off[E + s] + t)])
-        acc += dl[t] @ Wr
         H_.assert_close(f"dx[{t}]", host(g["dx"][int(t)]), O.round_bf16(acc))
     for e in rng.choice(E, size=4, replace=False):
         st = m["sel_tokens"][m["sel_offsets"][e]:m["sel_offsets"][e + 1]]
