@@ -374,63 +374,72 @@ permute_bwd_kernel(const __nv_bfloat16* __restrict__ dX, const int32_t* __restri
   }
 }
 
-// dW_r[e, cols] = sum over the tokens that selected e (in token order, split
-// across the block's 16 warps in a fixed interleave) of dlogits[t,e] x[t, cols].
-// Block (e, 256-column slab); lane owns 8 columns; warps combined in order.
-__global__ void __launch_bounds__(512)
+// dW_r[e, cols] = sum over the tokens that selected e of dlogits[t,e] x[t, cols].
+// Block (e, slab of 32*CPL columns); lane owns CPL columns. The expert's
+// selecting tokens are taken in chunks of 8 (chunk i by warp i mod 16): lanes
+// 0..7 load the chunk's token ids and dlogits, then the warp walks the chunk in
+// token order with 4 x rows in flight. Warp partial sums are combined in warp
+// order, so the summation order is fixed (deterministic).
+template <int CPL>
+__global__ void __launch_bounds__(512, 2)
 router_wgrad_kernel(const __nv_bfloat16* __restrict__ x, const int32_t* __restrict__ sel_offsets,
                     const int32_t* __restrict__ sel_tokens, const float* __restrict__ dlogits,
                     float* __restrict__ dW_r, int H, int E) {
-  constexpr int NW = 16;
-  __shared__ float part[NW][256];
+  constexpr int NW = 16, CH = 8, U = 4, SLAB = 32 * CPL;
+  __shared__ float part[NW][SLAB];
   const int e = blockIdx.x;
-  const int col0 = blockIdx.y * 256;
+  const int col0 = blockIdx.y * SLAB;
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
-  const int c = col0 + lane * 8;
+  const int c = col0 + lane * CPL;
   const bool on = c < H;
   const int beg = sel_offsets[e], end = sel_offsets[e + 1];
-  float acc[8];
+  float acc[CPL];
 #pragma unroll
-  for (int i = 0; i < 8; ++i) acc[i] = 0.f;
-  int i = beg + wid;
-  for (; i + 3 * NW < end; i += 4 * NW) {
-    int tt[4];
-    float d[4];
-    uint4 q[4];
-#pragma unroll
-    for (int u = 0; u < 4; ++u) tt[u] = sel_tokens[i + NW * u];
-#pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      d[u] = dlogits[(size_t)tt[u] * E + e];
-      if (on) q[u] = ldg_nc_v4(x + (size_t)tt[u] * H + c);
+  for (int i = 0; i < CPL; ++i) acc[i] = 0.f;
+  for (int base = beg + CH * wid; base < end; base += CH * NW) {
+    const int n = min(CH, end - base);
+    int my_t = 0;
+    float my_d = 0.f;
+    if (lane < n) {
+      my_t = sel_tokens[base + lane];
+      my_d = dlogits[(size_t)my_t * E + e];
     }
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      if (!on) continue;
-      float f[8];
-      unpack8(q[u], f);
+    for (int u0 = 0; u0 < CH; u0 += U) {
+      uint4 q[U];
+      float d[U];
 #pragma unroll
-      for (int m = 0; m < 8; ++m) acc[m] = fmaf(d[u], f[m], acc[m]);
+      for (int u = 0; u < U; ++u) {
+        const int t = __shfl_sync(0xffffffffu, my_t, u0 + u);
+        d[u] = __shfl_sync(0xffffffffu, my_d, u0 + u);
+        if (on && u0 + u < n) {
+          if (CPL == 8) {
+            q[u] = ldg_nc_v4(x + (size_t)t * H + c);
+          } else {
+            const uint2 h2 = __ldg(reinterpret_cast<const uint2*>(x + (size_t)t * H + c));
+            q[u] = make_uint4(h2.x, h2.y, 0u, 0u);
+          }
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        if (!on || u0 + u >= n) continue;
+        float f[8];
+        unpack8(q[u], f);
+#pragma unroll
+        for (int m = 0; m < CPL; ++m) acc[m] = fmaf(d[u], f[m], acc[m]);
+      }
     }
   }
-  for (; i < end; i += NW) {
-    const int t = sel_tokens[i];
-    const float d = dlogits[(size_t)t * E + e];
-    if (!on) continue;
-    float f[8];
-    unpack8(ldg_nc_v4(x + (size_t)t * H + c), f);
 #pragma unroll
-    for (int m = 0; m < 8; ++m) acc[m] = fmaf(d, f[m], acc[m]);
-  }
-#pragma unroll
-  for (int m = 0; m < 8; ++m) part[wid][lane * 8 + m] = acc[m];
+  for (int m = 0; m < CPL; ++m) part[wid][lane * CPL + m] = acc[m];
   __syncthreads();
-  if (threadIdx.x < 256) {
-    const int col = col0 + threadIdx.x;
+  for (int i = threadIdx.x; i < SLAB; i += blockDim.x) {
+    const int col = col0 + i;
     if (col < H) {
       float s = 0.f;
 #pragma unroll
-      for (int q2 = 0; q2 < NW; ++q2) s += part[q2][threadIdx.x];
+      for (int q2 = 0; q2 < NW; ++q2) s += part[q2][i];
       dW_r[(size_t)e * H + col] = s;
     }
   }
@@ -521,9 +530,17 @@ cudaError_t launch_permute_bwd(const moe_config& c, const void* dX_perm, const i
 cudaError_t launch_router_wgrad(const moe_config& c, const void* x, const int32_t* sel_offsets,
                                 const int32_t* sel_tokens, const float* dlogits, float* dW_r,
                                 cudaStream_t s) {
-  dim3 grid(c.E, (c.H + 255) / 256);
-  router_wgrad_kernel<<<grid, 512, 0, s>>>(static_cast<const __nv_bfloat16*>(x), sel_offsets,
-                                          sel_tokens, dlogits, dW_r, c.H, c.E);
+  auto xb = static_cast<const __nv_bfloat16*>(x);
+  // few experts: 128-column slabs so that every SM gets blocks
+  if ((long long)c.E * ((c.H + 255) / 256) < 2LL * num_sms()) {
+    dim3 grid(c.E, (c.H + 127) / 128);
+    router_wgrad_kernel<4><<<grid, 512, 0, s>>>(xb, sel_offsets, sel_tokens, dlogits, dW_r, c.H,
+                                                c.E);
+  } else {
+    dim3 grid(c.E, (c.H + 255) / 256);
+    router_wgrad_kernel<8><<<grid, 512, 0, s>>>(xb, sel_offsets, sel_tokens, dlogits, dW_r, c.H,
+                                                c.E);
+  }
   return cudaGetLastError();
 }
 
