@@ -45,7 +45,8 @@ def parse():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--workload", default="mixtral", choices=sorted(W.SHAPES))
+    ap.add_argument("--workload", default="mixtral",
+                    choices=sorted(W.SHAPES) + sorted(W.PROFILE_SHAPES))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -193,7 +194,7 @@ def run_ours(args, rank, world, local):
     import routing_dispatch_expert_router_gb300.binding as B
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
-    shape = W.SHAPES[args.workload]
+    shape = {**W.SHAPES, **W.PROFILE_SHAPES}[args.workload]
     cfg = B.config(shape)
     inp = W.make_inputs(shape, seed=args.seed + rank, device=str(dev))
     bufs = B.alloc_buffers(cfg, dev)
@@ -400,7 +401,7 @@ def cpu_cores() -> int:
 
 
 def run_reference(args):
-    shape = W.SHAPES[args.workload]
+    shape = {**W.SHAPES, **W.PROFILE_SHAPES}[args.workload]
     n_tok = args.cpu_sample_tokens or (shape.T if shape.name == "tiny" else 64)
     o = oracle_inputs(W.make_inputs(shape, seed=args.seed, device="cpu"), n_tok)
     if args.warmup > 0:

@@ -96,6 +96,15 @@ DSV3_FP8 = MoEShape("dsv3_fp8", T=16384, H=7168, E=256, k=8, F=2048,
 
 SHAPES = {s.name: s for s in (TINY, MIXTRAL, DSV3, QWEN3, DSV3_FP8)}
 
+# Small cases of the same kernels for detailed profiles (a few GB on the device,
+# operands still larger than L2): Mixtral-sized experts, 2 of them with 2048
+# rows each (CTA-pair GEMM tiles, K = 4096); DeepSeek-V3-sized experts, 16 of
+# them with about 256 rows each (single-CTA tiles, short weight-gradient K).
+PROFILE_SHAPES = {
+    "mixtral_2experts": MIXTRAL.with_(name="mixtral_2experts", T=2048, E=2),
+    "dsv3_16experts": DSV3.with_(name="dsv3_16experts", T=512, E=16),
+}
+
 
 def _gen(device, seed: int) -> torch.Generator:
     g = torch.Generator(device=device)
