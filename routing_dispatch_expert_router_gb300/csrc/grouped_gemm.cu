@@ -162,6 +162,58 @@ __device__ __forceinline__ void epilogue_tile(const Params& p, const CUtensorMap
     if (t >= 0) rd = p.dlogits[(long long)t * p.router_E + g];
     rw = p.W_r + (long long)g * p.N + f0;
   }
+  if (EPI == kEpiStore || EPI == kEpiWgrad || EPI == kEpiDgradRouter) {
+    // plain bf16 output in 32 x 64 boxes: 128-byte rows (128-byte swizzle), so
+    // every store fills whole 128-byte lines; 64 accumulator columns per
+    // tensor-memory wait
+#pragma unroll 1
+    for (int c = 0; c < ncols; c += 64) {
+      uint32_t r0[32], r1[32];
+      if (EPI == kEpiWgrad && nk == 0) {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) r0[i] = r1[i] = 0u;
+      } else {
+        ptx::tmem_ld32(tbase + c, r0);
+        ptx::tmem_ld32(tbase + c + 32, r1);
+        ptx::tmem_ld_wait();
+      }
+      if (EPI == kEpiDgradRouter && rw) {
+        // fp32 accumulator + dlogits * W_r, rounded to bf16 once
+#pragma unroll
+        for (int v = 0; v < 8; ++v) {
+          const float4 w4 = __ldg(reinterpret_cast<const float4*>(rw + c) + v);
+          r0[4 * v] = __float_as_uint(fmaf(rd, w4.x, __uint_as_float(r0[4 * v])));
+          r0[4 * v + 1] = __float_as_uint(fmaf(rd, w4.y, __uint_as_float(r0[4 * v + 1])));
+          r0[4 * v + 2] = __float_as_uint(fmaf(rd, w4.z, __uint_as_float(r0[4 * v + 2])));
+          r0[4 * v + 3] = __float_as_uint(fmaf(rd, w4.w, __uint_as_float(r0[4 * v + 3])));
+          const float4 w5 = __ldg(reinterpret_cast<const float4*>(rw + c + 32) + v);
+          r1[4 * v] = __float_as_uint(fmaf(rd, w5.x, __uint_as_float(r1[4 * v])));
+          r1[4 * v + 1] = __float_as_uint(fmaf(rd, w5.y, __uint_as_float(r1[4 * v + 1])));
+          r1[4 * v + 2] = __float_as_uint(fmaf(rd, w5.z, __uint_as_float(r1[4 * v + 2])));
+          r1[4 * v + 3] = __float_as_uint(fmaf(rd, w5.w, __uint_as_float(r1[4 * v + 3])));
+        }
+      }
+      uint4 o[4], o2[4];
+      pack_slice(r0, o);
+      pack_slice(r1, o2);
+      // the staging box is free once TMA has read the previous one
+      if (lane == 0) ptx::tma_store_wait_read();
+      __syncwarp();
+      uint8_t* rowp = stage + lane * 128;             // chunk j of row r at j ^ (r & 7)
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        *reinterpret_cast<uint4*>(rowp + ((j ^ (lane & 7)) << 4)) = o[j];
+        *reinterpret_cast<uint4*>(rowp + (((j + 4) ^ (lane & 7)) << 4)) = o2[j];
+      }
+      ptx::fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        ptx::tma_store_2d(tmC, stage_u32, f0 + c, row0);
+        ptx::tma_store_commit();
+      }
+    }
+    return;
+  }
   uint4 gq[4], uq[4];
   const __nv_bfloat16* gu = nullptr;
   if (EPI == kEpiSwigluBwd) {
@@ -798,6 +850,20 @@ static bool make_out_map(CUtensorMap* m, const void* ptr, uint64_t inner, uint64
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// bf16 output view for TMA stores of 32-row x 64-column boxes (128-byte rows,
+// 128-byte swizzle): the plain-store epilogues.
+static bool make_out_map_w64(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t outer) {
+  PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {inner * 2};
+  cuuint32_t box[2] = {64, 32};
+  cuuint32_t es[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box,
+            es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // fp32 output view for TMA stores of 32 x 32 boxes (128-byte rows, 128-byte swizzle).
 static bool make_out_map_f32(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t outer) {
   PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
@@ -914,7 +980,7 @@ cudaError_t launch_ffn_fc2(const moe_config& c, const void* h, const int32_t* co
   CUtensorMap a, b, oc;
   if (!make_map(&a, h, c.F, R, 128) ||
       !make_map(&b, W2, c.F, (uint64_t)G * c.H, pair ? 128 : bn) ||
-      !make_out_map(&oc, y_perm, c.H, R))
+      !make_out_map_w64(&oc, y_perm, c.H, R))
     return cudaErrorInvalidValue;
   const CUtensorMap& oc2 = oc;
   Params p = base_params(c, counts, offsets, status);
@@ -962,7 +1028,7 @@ cudaError_t launch_ffn_fc1_dgrad(const moe_config& c, const void* dGU, const int
   CUtensorMap a, b, oc;
   if (!make_map(&a, dGU, 2ULL * c.F, R, 128) ||
       !make_map(&b, W13, c.H, (uint64_t)G * 2 * c.F, 64) ||
-      !make_out_map(&oc, dX_perm, c.H, R))
+      !make_out_map_w64(&oc, dX_perm, c.H, R))
     return cudaErrorInvalidValue;
   const CUtensorMap& oc2 = oc;
   Params p = base_params(c, counts, offsets, status);
@@ -988,7 +1054,7 @@ cudaError_t launch_ffn_wgrad_fc2(const moe_config& c, const void* dO_perm, const
   const int G = c.E + c.n_shared;
   CUtensorMap a, b, oc;
   if (!make_map(&a, dO_perm, c.H, R, 64) || !make_map(&b, h, c.F, R, 64) ||
-      !make_out_map(&oc, dW2, c.F, (uint64_t)G * c.H))
+      !make_out_map_w64(&oc, dW2, c.F, (uint64_t)G * c.H))
     return cudaErrorInvalidValue;
   const CUtensorMap& oc2 = oc;
   Params p = base_params(c, counts, offsets, status);
@@ -1011,7 +1077,7 @@ cudaError_t launch_ffn_wgrad_fc1(const moe_config& c, const void* dGU, const voi
   const int G = c.E + c.n_shared;
   CUtensorMap a, b, oc;
   if (!make_map(&a, dGU, 2ULL * c.F, R, 64) || !make_map(&b, x_perm, c.H, R, 64) ||
-      !make_out_map(&oc, dW13, c.H, (uint64_t)G * 2 * c.F))
+      !make_out_map_w64(&oc, dW13, c.H, (uint64_t)G * 2 * c.F))
     return cudaErrorInvalidValue;
   const CUtensorMap& oc2 = oc;
   Params p = base_params(c, counts, offsets, status);
