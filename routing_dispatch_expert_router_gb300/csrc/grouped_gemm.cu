@@ -66,7 +66,8 @@ struct Params {
   long long ldaux;
   int32_t* status;
   int dense_rows;             // > 0: one group of this many rows at row 0 (no counts/offsets)
-  int a_kwrap;                // > 0: A's k coordinate wraps at this width (A repeated along K)
+  int a_krep;                 // > 1: A's k-block is kb / a_krep (each A k-block used a_krep
+                              // times in a row against consecutive B k-blocks)
   // FC1 data gradient with the router term (kEpiDgradRouter): row r of a
   // routed group g < router_E gains dlogits[token_of[r], g] * W_r[g, :]
   const int32_t* token_of;
@@ -116,11 +117,13 @@ __device__ __forceinline__ Tile decode(int tile, const int* prefix, const int* m
 __device__ __forceinline__ float sigmoid_f(float z) { return __frcp_rn(1.f + __expf(-z)); }
 __device__ __forceinline__ float silu_f(float z) { return z * sigmoid_f(z); }
 
-// Output staging: every epilogue warp owns kStageBytes of shared memory for up
-// to three 32 x 32 bf16 boxes, laid out with the 64-byte swizzle that the
-// output tensor maps use (16-byte chunk j of row r sits at slot j ^ ((r>>1)&3),
-// so the 32 lanes' row writes hit distinct banks), stored to global memory by
-// TMA (coalesced, asynchronous).
+// Output staging: every epilogue warp owns kStageBytes of shared memory (1024-
+// byte aligned), stored to global memory by TMA (coalesced, asynchronous). The
+// SwiGLU epilogues stage up to three 32 x 32 bf16 boxes with the 64-byte
+// swizzle of their output maps (16-byte chunk j of row r at slot j ^ ((r>>1)&3));
+// the plain-store epilogues one 32 x 64 box with the 128-byte swizzle (chunk j
+// of row r at slot j ^ (r & 7)). Either way the 32 lanes' row writes hit
+// distinct banks.
 
 __device__ __forceinline__ void stage_row(uint8_t* stage, int box, int lane, const uint4 (&v)[4]) {
   uint8_t* row = stage + box * kBoxBytes + lane * 64;
@@ -292,33 +295,12 @@ __device__ __forceinline__ void epilogue_tile(const Params& p, const CUtensorMap
         ptx::tma_store_commit();
       }
       continue;
-    } else {
-      uint32_t r[32];
-      if (EPI == kEpiWgrad && nk == 0) {
-#pragma unroll
-        for (int i = 0; i < 32; ++i) r[i] = 0u;
-      } else {
-        ptx::tmem_ld32(tbase + c, r);
-        ptx::tmem_ld_wait();
-      }
-      if (EPI == kEpiDgradRouter && rw) {
-        // fp32 accumulator + dlogits * W_r, rounded to bf16 once
-#pragma unroll
-        for (int v = 0; v < 8; ++v) {
-          const float4 w4 = __ldg(reinterpret_cast<const float4*>(rw + c) + v);
-          r[4 * v] = __float_as_uint(fmaf(rd, w4.x, __uint_as_float(r[4 * v])));
-          r[4 * v + 1] = __float_as_uint(fmaf(rd, w4.y, __uint_as_float(r[4 * v + 1])));
-          r[4 * v + 2] = __float_as_uint(fmaf(rd, w4.z, __uint_as_float(r[4 * v + 2])));
-          r[4 * v + 3] = __float_as_uint(fmaf(rd, w4.w, __uint_as_float(r[4 * v + 3])));
-        }
-      }
-      pack_slice(r, o0);
     }
     // the staging area is free once the previous boxes have been read by TMA
     if (lane == 0) ptx::tma_store_wait_read();
     __syncwarp();
     stage_row(stage, 0, lane, o0);
-    if (EPI == kEpiSwigluFwd || EPI == kEpiSwigluBwd) stage_row(stage, 1, lane, o1);
+    stage_row(stage, 1, lane, o1);
     if (EPI == kEpiSwigluFwd) stage_row(stage, 2, lane, o2);
     ptx::fence_proxy_async_smem();
     __syncwarp();
@@ -327,11 +309,9 @@ __device__ __forceinline__ void epilogue_tile(const Params& p, const CUtensorMap
         ptx::tma_store_2d(tmC, stage_u32, f0 + c, row0);                      // G
         ptx::tma_store_2d(tmC, stage_u32 + kBoxBytes, p.F + f0 + c, row0);    // U
         ptx::tma_store_2d(tmC2, stage_u32 + 2 * kBoxBytes, f0 + c, row0);     // h
-      } else if (EPI == kEpiSwigluBwd) {
+      } else {
         ptx::tma_store_2d(tmC, stage_u32, f0 + c, row0);                      // dG
         ptx::tma_store_2d(tmC, stage_u32 + kBoxBytes, p.F + f0 + c, row0);    // dU
-      } else {
-        ptx::tma_store_2d(tmC, stage_u32, f0 + c, row0);
       }
       ptx::tma_store_commit();
     }
@@ -425,7 +405,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
           const uint32_t sB = sA + L::A_BYTES;
           const int k0 = kb * BK;
           if (A_MN == 0) {
-            ptx::tma_load_2d(sA, &tmA, fb, p.a_kwrap > 0 ? k0 % p.a_kwrap : k0,
+            ptx::tma_load_2d(sA, &tmA, fb, p.a_krep > 1 ? (kb / p.a_krep) * BK : k0,
                              s_off[t.g] + t.mt * BM);
           } else {
             const int kr = s_off[t.g] + k0;
@@ -1092,10 +1072,13 @@ cudaError_t launch_ffn_wgrad_fc1(const moe_config& c, const void* dGU, const voi
                    : run<kEpiWgrad, 128, 1, 1, 6>(a, b, oc, oc2, p, s);
 }
 
-// Router logits on the tensor cores: logits[T,E] = [x x x] . W3^T where
-// W3 = [W_hi | W_mid | W_lo] ([E, 3H] bf16, W_r = W_hi + W_mid + W_lo exactly),
-// fp32 accumulation, one dense group of T rows (rows past T read zeros and
-// are not stored). Needs E % 128 == 0.
+// Router logits on the tensor cores: logits[T,E] = sum over the three bf16
+// parts of W_r (W_r = W_hi + W_mid + W_lo exactly) of x . part^T. W3 [E, 3H]
+// holds the parts interleaved per 64-column k-block (hi, mid, lo of columns
+// 64j..64j+63, then of the next 64), and x's k-block j is used for the three
+// consecutive k-blocks 3j..3j+2, so x is read from DRAM once (the repeats hit
+// L2). fp32 accumulation, one dense group of T rows (rows past T read zeros
+// and are not stored). Needs E % 128 == 0.
 cudaError_t launch_router_logits_tc(const moe_config& c, const void* x, const void* W3,
                                     float* logits, int32_t* status, cudaStream_t s) {
   CUtensorMap a, b, oc;
@@ -1105,7 +1088,7 @@ cudaError_t launch_router_logits_tc(const moe_config& c, const void* x, const vo
   Params p{};
   p.G = 1;
   p.dense_rows = c.T;
-  p.a_kwrap = c.H;
+  p.a_krep = 3;
   p.N = c.E;
   p.K = 3 * c.H;
   p.status = status;

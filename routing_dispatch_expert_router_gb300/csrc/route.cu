@@ -528,9 +528,10 @@ route_select_sigmoid_kernel(const float* __restrict__ logits, const float* __res
   }
 }
 
-// W3[e] = [hi | mid | lo] with hi = bf16(w), mid = bf16(w - hi), lo = bf16(w - hi - mid):
-// each part keeps 8 significant bits, so hi + mid + lo == w exactly for every
-// fp32 w (the two subtractions are exact).
+// W3[e] = the three bf16 parts of row e of W_r, hi = bf16(w), mid = bf16(w - hi),
+// lo = bf16(w - hi - mid) (each keeps 8 significant bits, so hi + mid + lo == w
+// exactly for every fp32 w: the two subtractions are exact), interleaved per
+// 64 columns: columns 64j..64j+63 of hi, of mid, of lo, then the next 64.
 __global__ void __launch_bounds__(256)
 split3_kernel(const float* __restrict__ W, __nv_bfloat16* __restrict__ W3, int E, int H) {
   const long long n = (long long)E * H;
@@ -542,10 +543,10 @@ split3_kernel(const float* __restrict__ W, __nv_bfloat16* __restrict__ W3, int E
     const float r1 = v - __bfloat162float(hi);
     const __nv_bfloat16 mid = __float2bfloat16_rn(r1);
     const float r2 = r1 - __bfloat162float(mid);
-    __nv_bfloat16* row = W3 + (size_t)e * 3 * H;
-    row[h] = hi;
-    row[H + h] = mid;
-    row[2 * H + h] = __float2bfloat16_rn(r2);
+    __nv_bfloat16* blk = W3 + (size_t)e * 3 * H + (size_t)(h / 64) * 192 + (h % 64);
+    blk[0] = hi;
+    blk[64] = mid;
+    blk[128] = __float2bfloat16_rn(r2);
   }
 }
 
