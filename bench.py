@@ -51,6 +51,8 @@ def parse():
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-sample-tokens", type=int, default=0)
+    ap.add_argument("--ref-budget-s", type=float, default=120.0,
+                    help="reference arm: seconds of oracle work for all timed steps together")
     return ap.parse_args()
 
 
@@ -401,21 +403,37 @@ def cpu_cores() -> int:
 
 
 def run_reference(args):
+    """The oracle as the reference arm: every step runs its fwd+bwd (weight
+    gradients included) on a sample of the workload's tokens, on the host cores.
+
+    A step of the oracle has a floor that does not shrink with the sample (it
+    builds every expert's full-size fp64 weight gradient), so the run is held
+    to about --ref-budget-s seconds: a timed 1-token step (also the warm-up)
+    sizes the sample (1 token at least, the whole batch at most) and, when even
+    1-token steps do not fit, fewer steps than requested run; the JSON line says
+    how many ("steps", with "steps_requested")."""
     shape = {**W.SHAPES, **W.PROFILE_SHAPES}[args.workload]
-    n_tok = args.cpu_sample_tokens or (shape.T if shape.name == "tiny" else 64)
-    o = oracle_inputs(W.make_inputs(shape, seed=args.seed, device="cpu"), n_tok)
-    if args.warmup > 0:
-        oracle_sample(shape, oracle_inputs_slice(o, min(n_tok, 4)))
-    secs = [oracle_sample(shape, o) for _ in range(args.steps)]
+    want = max(args.steps, 1)
+    o_all = oracle_inputs(W.make_inputs(shape, seed=args.seed, device="cpu"), shape.T)
+    t1 = oracle_sample(shape, oracle_inputs_slice(o_all, 1))            # warm-up and probe
+    if args.cpu_sample_tokens:
+        n_tok = min(args.cpu_sample_tokens, shape.T)
+        steps = want
+    else:
+        n_tok = int(min(shape.T, max(1, args.ref_budget_s / (want * max(t1, 1e-6)))))
+        steps = int(min(want, max(1, args.ref_budget_s / (n_tok * max(t1, 1e-6)))))
+    o = oracle_inputs_slice(o_all, n_tok)
+    secs = [oracle_sample(shape, o) for _ in range(steps)]
     tot = sum(secs)
-    val = n_tok * args.steps / tot
+    val = n_tok * steps / tot
     cb = {"value": val, "unit": "tokens/s", "cores": cpu_cores(), "kind": "oracle",
-          "sample": f"first {n_tok} tokens of {shape.name} per step (routing, experts, combine, "
-                    "full backward incl. weight gradients of those tokens), fp64 numpy"}
+          "sample": f"first {n_tok} tokens of {shape.name} per step, {steps} steps (routing, "
+                    "experts, combine, full backward incl. every expert's weight gradient), "
+                    "fp64 numpy"}
     return {"impl": "reference", "metric": "MoE-layer tokens/s fwd+bwd on 1 GB300", "value": val,
-            "unit": "tokens/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
-            "ms_per_step": 1e3 * tot / args.steps, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "unit": "tokens/s", "n_gpus": 1, "steps": steps, "steps_requested": args.steps,
+            "warmup": 1, "ms_per_step": 1e3 * tot / steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": {"workload": shape.name}, "cpu_baseline": cb,
             "e2e": {"value": val, "unit": "tokens/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
