@@ -434,31 +434,53 @@ route_select_sigmoid_kernel(const float* __restrict__ logits, const float* __res
     group_ids<NPL>(lane, E, per, gid);
     // candidates for every group's top-m, from the fp32 keys
     uint32_t gc = 0;
-    for (int g = 0; g < n_groups; ++g) {
-      float a1 = -INFINITY, a2 = -INFINITY;
-#pragma unroll
-      for (int i = 0; i < NPL; ++i)
-        if (gid[i] == g) top2_insert_f(A[i], a1, a2);
-      warp_top2_f(a1, a2);
-      const float am = two ? a2 : a1;
-      const float thr = am - margin(am);
-#pragma unroll
-      for (int i = 0; i < NPL; ++i)
-        if (gid[i] == g && A[i] >= thr) gc |= 1u << i;
-    }
-    exact_sigmoids<NPL>(lrow, gc, lane, s64);
-    have = gc;
-    // group scores on the fp64 keys of the candidates
     uint64_t gs_mine = 0;
-    for (int g = 0; g < n_groups; ++g) {
-      uint64_t k1 = 0, k2 = 0;
+    if (per == 32) {
+      // groups of 32 experts: lane l's expert of group g is l + 32 g (i = g), so
+      // the per-lane scans over i disappear (fully unrolled, n_groups <= NPL)
 #pragma unroll
-      for (int i = 0; i < NPL; ++i)
-        if (((gc >> i) & 1u) && gid[i] == g) top2_insert(key64(i), k1, k2);
-      warp_top2_u64(k1, k2);
-      const double gsc = two ? unord64(k1) + unord64(k2) : unord64(k1);
-      if (lane == g) gs_mine = ord64(gsc);
+      for (int g = 0; g < NPL; ++g) {
+        if (g >= n_groups) break;
+        float a1 = A[g], a2 = -INFINITY;
+        warp_top2_f(a1, a2);
+        const float am = two ? a2 : a1;
+        if (A[g] >= am - margin(am)) gc |= 1u << g;
+      }
+      exact_sigmoids<NPL>(lrow, gc, lane, s64);
+#pragma unroll
+      for (int g = 0; g < NPL; ++g) {
+        if (g >= n_groups) break;
+        uint64_t k1 = ((gc >> g) & 1u) ? key64(g) : 0ull, k2 = 0;
+        warp_top2_u64(k1, k2);
+        const double gsc = two ? unord64(k1) + unord64(k2) : unord64(k1);
+        if (lane == g) gs_mine = ord64(gsc);
+      }
+    } else {
+      for (int g = 0; g < n_groups; ++g) {
+        float a1 = -INFINITY, a2 = -INFINITY;
+#pragma unroll
+        for (int i = 0; i < NPL; ++i)
+          if (gid[i] == g) top2_insert_f(A[i], a1, a2);
+        warp_top2_f(a1, a2);
+        const float am = two ? a2 : a1;
+        const float thr = am - margin(am);
+#pragma unroll
+        for (int i = 0; i < NPL; ++i)
+          if (gid[i] == g && A[i] >= thr) gc |= 1u << i;
+      }
+      exact_sigmoids<NPL>(lrow, gc, lane, s64);
+      // group scores on the fp64 keys of the candidates
+      for (int g = 0; g < n_groups; ++g) {
+        uint64_t k1 = 0, k2 = 0;
+#pragma unroll
+        for (int i = 0; i < NPL; ++i)
+          if (((gc >> i) & 1u) && gid[i] == g) top2_insert(key64(i), k1, k2);
+        warp_top2_u64(k1, k2);
+        const double gsc = two ? unord64(k1) + unord64(k2) : unord64(k1);
+        if (lane == g) gs_mine = ord64(gsc);
+      }
     }
+    have = gc;
     keep_best_groups<NPL>(gs_mine, lane, n_groups, topk_groups, gid, avail);
   }
   // the k-th best fp32 key among the available experts
