@@ -289,91 +289,6 @@ route_bwd_kernel(const float* __restrict__ logits, const int32_t* __restrict__ i
   if (lane < k && (unsigned)e < (unsigned)E) row[e] = v;
 }
 
-// Permute backward with capacity drops and many rows per token (k + S > 4):
-// the same sum as gather_reduce_kernel<.., ROUTER>, one warp per (token,
-// 256-column segment):
-// a warp holds only one 16-byte slice of each row and of each W_r row, which
-// keeps registers (and so occupancy) where the k W_r rows would otherwise
-// push them.
-template <int MAXR>
-__global__ void __launch_bounds__(256)
-permute_bwd_kernel(const __nv_bfloat16* __restrict__ dX, const int32_t* __restrict__ row_of,
-                   const int32_t* __restrict__ offsets, const int32_t* __restrict__ idx,
-                   const float* __restrict__ dlogits, const float* __restrict__ W_r,
-                   __nv_bfloat16* __restrict__ dx, int T, int H, int k, int E, int S) {
-  const int lane = threadIdx.x & 31;
-  const int nvec = H >> 3, nr = k + S;
-  constexpr int VPL = (MAXR <= 4) ? 2 : 1;   // 16-byte slices per lane
-  const int segs = (nvec + 32 * VPL - 1) / (32 * VPL);
-  const long long items = (long long)T * segs;
-  const long long warps = (long long)gridDim.x * (blockDim.x >> 5);
-  const uint64_t stream_pol = l2_evict_first_policy(), keep_pol = l2_evict_last_policy();
-  for (long long it = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); it < items;
-       it += warps) {
-    const int t = (int)(it / segs), c0 = (int)(it % segs) * (32 * VPL) + lane;
-    int myrow = -1;
-    float unused = 0.f;
-    if (lane < nr) slot_row(row_of, nullptr, offsets, t, lane, k, E, myrow, unused);
-    int mye = -1;
-    float mydl = 0.f;
-    if (lane < k) {
-      mye = idx[(size_t)t * k + lane];
-      if ((unsigned)mye < (unsigned)E) mydl = dlogits[(size_t)t * E + mye];
-      else mye = -1;
-    }
-    int rows[MAXR], es[MAXR];
-    float dls[MAXR];
-#pragma unroll
-    for (int j = 0; j < MAXR; ++j) rows[j] = __shfl_sync(0xffffffffu, myrow, j);
-#pragma unroll
-    for (int j = 0; j < MAXR; ++j) {
-      es[j] = __shfl_sync(0xffffffffu, mye, j);
-      dls[j] = __shfl_sync(0xffffffffu, mydl, j);
-    }
-    uint4 q[VPL][MAXR];
-#pragma unroll
-    for (int u = 0; u < VPL; ++u) {
-      const int c = c0 + 32 * u;
-#pragma unroll
-      for (int j = 0; j < MAXR; ++j)
-        if (j < nr && rows[j] >= 0 && c < nvec)
-          q[u][j] = ldg_nc_v4_pol(dX + (size_t)rows[j] * H + (size_t)c * 8, stream_pol);
-    }
-#pragma unroll
-    for (int u = 0; u < VPL; ++u) {
-      const int c = c0 + 32 * u;
-      if (c >= nvec) continue;
-      float acc[8];
-#pragma unroll
-      for (int m = 0; m < 8; ++m) acc[m] = 0.f;
-#pragma unroll
-      for (int j = 0; j < MAXR; ++j) {
-        if (j >= nr || rows[j] < 0) continue;
-        float f[8];
-        unpack8(q[u][j], f);
-#pragma unroll
-        for (int m = 0; m < 8; ++m) acc[m] += f[m];
-      }
-#pragma unroll
-      for (int j = 0; j < MAXR; ++j) {
-        if (j >= k || es[j] < 0 || rows[j] >= 0) continue;
-        const float d = dls[j];
-        const float* wr = W_r + (size_t)es[j] * H + (size_t)c * 8;
-        const float4 a = ldg_nc_f4_pol(wr, keep_pol), b = ldg_nc_f4_pol(wr + 4, keep_pol);
-        acc[0] = fmaf(d, a.x, acc[0]);
-        acc[1] = fmaf(d, a.y, acc[1]);
-        acc[2] = fmaf(d, a.z, acc[2]);
-        acc[3] = fmaf(d, a.w, acc[3]);
-        acc[4] = fmaf(d, b.x, acc[4]);
-        acc[5] = fmaf(d, b.y, acc[5]);
-        acc[6] = fmaf(d, b.z, acc[6]);
-        acc[7] = fmaf(d, b.w, acc[7]);
-      }
-      stg_v4(dx + (size_t)t * H + (size_t)c * 8, pack8(acc));
-    }
-  }
-}
-
 // dW_r[e, cols] = sum over the tokens that selected e of dlogits[t,e] x[t, cols].
 // Block (e, slab of 32*CPL columns); lane owns CPL columns. The expert's
 // selecting tokens are taken in chunks of 8 (chunk i by warp i mod 16): lanes
@@ -445,14 +360,6 @@ router_wgrad_kernel(const __nv_bfloat16* __restrict__ x, const int32_t* __restri
   }
 }
 
-static int grid_for_vectors(const moe_config& c) {
-  const long long n = (long long)c.T * ((c.H / 8 + 31) / 32) * 32;   // up to one warp per segment
-  long long blocks = (n + 255) / 256;
-  const long long cap = (long long)num_sms() * 32;
-  if (blocks > cap) blocks = cap;
-  return blocks > 0 ? (int)blocks : 1;
-}
-
 static int grid_for_warps(int n_items) {
   const int blocks = (n_items + 7) / 8;
   const int cap = num_sms() * 16;
@@ -477,11 +384,8 @@ static cudaError_t launch_gather_reduce(const moe_config& c, const void* src,
     gather_reduce_kernel<4, 2, ROUTER><<<grid, 256, 0, s>>>(sp, row_of, w, offsets, idx, dlogits,
                                                            W_r, o, c.T, c.H, c.k, c.E,
                                                            c.n_shared);
-  else if constexpr (ROUTER)
-    permute_bwd_kernel<kMaxK + 4><<<grid_for_vectors(c), 256, 0, s>>>(
-        sp, row_of, offsets, idx, dlogits, W_r, o, c.T, c.H, c.k, c.E, c.n_shared);
   else
-    gather_reduce_kernel<kMaxK + 4, 1, false><<<grid, 256, 0, s>>>(
+    gather_reduce_kernel<kMaxK + 4, 1, ROUTER><<<grid, 256, 0, s>>>(
         sp, row_of, w, offsets, idx, dlogits, W_r, o, c.T, c.H, c.k, c.E, c.n_shared);
   return cudaGetLastError();
 }
