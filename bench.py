@@ -175,7 +175,7 @@ def stage_table(shape, cfg, f, stage_ms, hbm_gbs, fl_fwd, fl_bwd, tc_peak):
          "dO scatter + dw dot products"),
         ("route_bwd", T * E * 4 * 2 + maps, "dlogits"),
         ("grouped_ffn_bwd", fl_bwd, "FC2 dgrad+SwiGLU bwd, FC1 dgrad, dW2, dW13 (tcgen05)"),
-        ("permute_bwd", rows * H * bf + T * H * bf + maps, "dx gather-reduce + router term"),
+        ("permute_bwd", rows * H * bf + T * H * bf + maps, "dx gather-reduce"),
         ("router_wgrad", T * H * bf + E * H * 4 + T * E * 4, "dW_r (each x row once)"),
     ]
     out = []
@@ -244,7 +244,14 @@ def run_ours(args, rank, world, local):
         B.moe_router_wgrad(cfg, x, f["sel_offsets"], f["sel_tokens"], b["dlogits"], dW_r)
         rec(9)
 
-    launches_per_step = 2 + 3 + 2 + 1 + 1 + 1 + 4 + 1 + 1
+    # kernels launched by one step: route (logits [+ W_r split on the tensor-core
+    # path] + selection), dispatch (hist, rank, scatter), FC1 and FC2, combine,
+    # combine bwd, route bwd, the four backward GEMMs, dispatch bwd, router wgrad;
+    # the FP8 mode adds 4 quantisation launches forward and 6 backward
+    tc_router = shape.E >= 128 and shape.E % 128 == 0
+    launches_per_step = (3 if tc_router else 2) + 3 + 2 + 1 + 1 + 1 + 4 + 1 + 1
+    if shape.dtype == W.DT_FP8:
+        launches_per_step += 4 + 6
     for _ in range(max(args.warmup, 3)):
         step()
     torch.cuda.synchronize(dev)
