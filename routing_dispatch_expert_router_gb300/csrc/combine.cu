@@ -156,7 +156,7 @@ __device__ __forceinline__ int find_pad_group(const int* prefix, int G, int p) {
 // order and the warp combines lanes by a fixed butterfly, so dw is
 // deterministic. No block-wide synchronisation on the token path.
 template <int MAXR, int U>
-__global__ void __launch_bounds__(256)
+__global__ void __launch_bounds__(256, (MAXR <= 2) ? 3 : 2)
 unpermute_bwd_kernel(const __nv_bfloat16* __restrict__ dY, const __nv_bfloat16* __restrict__ y,
                      const int32_t* __restrict__ row_of, const float* __restrict__ w,
                      const int32_t* __restrict__ counts, const int32_t* __restrict__ offsets,
@@ -405,7 +405,10 @@ cudaError_t launch_unpermute_bwd(const moe_config& c, const void* dY, const void
   auto dOp = static_cast<__nv_bfloat16*>(dO_perm);
   // one warp per token (8 per block), capped at 16 blocks per SM
   const int grid = grid_for_warps(c.T);
-  if (c.k + c.n_shared <= 4)
+  if (c.k + c.n_shared <= 2)
+    unpermute_bwd_kernel<2, 4><<<grid, 256, 0, s>>>(dYp, yp, row_of, w, counts, offsets, dOp, dw,
+                                                    c.T, c.H, c.k, c.E, c.n_shared);
+  else if (c.k + c.n_shared <= 4)
     unpermute_bwd_kernel<4, 4><<<grid, 256, 0, s>>>(dYp, yp, row_of, w, counts, offsets, dOp, dw,
                                                     c.T, c.H, c.k, c.E, c.n_shared);
   else
