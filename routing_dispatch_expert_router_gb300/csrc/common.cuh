@@ -84,18 +84,8 @@ __device__ __forceinline__ float4 ldg_nc_f4_pol(const void* p, uint64_t pol) {
   return v;
 }
 
-__device__ __forceinline__ uint4 ldg_v4(const void* p) {
-  return *reinterpret_cast<const uint4*>(p);
-}
-
 __device__ __forceinline__ void stg_v4(void* p, const uint4& v) {
   *reinterpret_cast<uint4*>(p) = v;
-}
-
-// Streaming store (written once, not re-read by this kernel).
-__device__ __forceinline__ void stg_cs_v4(void* p, const uint4& v) {
-  asm volatile("st.global.cs.v4.u32 [%0], {%1,%2,%3,%4};"
-               :: "l"(p), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w) : "memory");
 }
 
 __device__ __forceinline__ float warp_sum(float v) {
