@@ -112,10 +112,48 @@ __device__ __forceinline__ Tile decode(int tile, const int* prefix, const int* m
   return t;
 }
 
-// Logistic sigmoid and SiLU for the SwiGLU epilogues, from the hardware exp2
-// approximation (the bf16 outputs keep 8 significant bits; this is far inside).
-__device__ __forceinline__ float sigmoid_f(float z) { return __frcp_rn(1.f + __expf(-z)); }
+// Logistic sigmoid 1 / (1 + e^-z) = 1 / (1 + 2^(-z log2 e)) and SiLU for the
+// SwiGLU epilogues, on the special-function unit (a few fp32 ulp; the bf16
+// outputs keep 8 significant bits). Large |z| saturate to 0 and 1.
+constexpr float kLog2e = 1.4426950408889634f;
+__device__ __forceinline__ float sigmoid_f(float z) {
+  return ptx::rcp_approx(1.f + ptx::ex2_approx(-kLog2e * z));
+}
 __device__ __forceinline__ float silu_f(float z) { return z * sigmoid_f(z); }
+
+// SwiGLU backward of 8 consecutive columns. With s = sigmoid(g) and
+// silu(g) = g s (h = silu(g) u):
+//   dU = dh silu(g),  dG = dh u (s + silu(g) (1 - s))   [= dh u s (1 + g (1 - s))].
+// dh: 8 fp32 (tensor-memory bits); g, u: 8 bf16 each. fp32 pairs throughout.
+__device__ __forceinline__ void swiglu_bwd8(const uint32_t* dh, const uint4& g, const uint4& u,
+                                            uint4& dg, uint4& du) {
+  const uint32_t gw[4] = {g.x, g.y, g.z, g.w}, uw[4] = {u.x, u.y, u.z, u.w};
+  uint32_t dgw[4], duw[4];
+  const uint64_t one = ptx::f2_pack(1.f, 1.f);
+  const uint64_t nl2e = ptx::f2_pack(-kLog2e, -kLog2e);
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const uint64_t G = ptx::f2_pack(bf16_lo(gw[j]), bf16_hi(gw[j]));
+    const uint64_t U = ptx::f2_pack(bf16_lo(uw[j]), bf16_hi(uw[j]));
+    const uint64_t D = ptx::f2_pack(__uint_as_float(dh[2 * j]), __uint_as_float(dh[2 * j + 1]));
+    float e0, e1;
+    ptx::f2_unpack(ptx::f2_mul(G, nl2e), e0, e1);
+    float d0, d1;
+    ptx::f2_unpack(ptx::f2_add(ptx::f2_pack(ptx::ex2_approx(e0), ptx::ex2_approx(e1)), one), d0, d1);
+    const uint64_t S = ptx::f2_pack(ptx::rcp_approx(d0), ptx::rcp_approx(d1));
+    const uint64_t SILU = ptx::f2_mul(G, S);
+    const uint64_t DU = ptx::f2_mul(D, SILU);
+    const uint64_t T = ptx::f2_fma(SILU, ptx::f2_sub(one, S), S);
+    const uint64_t DG = ptx::f2_mul(ptx::f2_mul(D, U), T);
+    float a0, a1, b0, b1;
+    ptx::f2_unpack(DG, a0, a1);
+    ptx::f2_unpack(DU, b0, b1);
+    dgw[j] = pack_bf16x2(a0, a1);
+    duw[j] = pack_bf16x2(b0, b1);
+  }
+  dg = make_uint4(dgw[0], dgw[1], dgw[2], dgw[3]);
+  du = make_uint4(duw[0], duw[1], duw[2], duw[3]);
+}
 
 // Output staging: every epilogue warp owns kStageBytes of shared memory (1024-
 // byte aligned), stored to global memory by TMA (coalesced, asynchronous). The
@@ -260,18 +298,7 @@ __device__ __forceinline__ void epilogue_tile(const Params& p, const CUtensorMap
       ptx::tmem_ld_wait();
 #pragma unroll
       for (int v = 0; v < 4; ++v) {
-        float gf[8], uf[8], dg[8], du[8];
-        unpack8(gq[v], gf);
-        unpack8(uq[v], uf);
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const float dh = __uint_as_float(r[v * 8 + i]);
-          const float sg = sigmoid_f(gf[i]);
-          dg[i] = dh * uf[i] * sg * (1.f + gf[i] * (1.f - sg));
-          du[i] = dh * gf[i] * sg;
-        }
-        o0[v] = pack8(dg);
-        o1[v] = pack8(du);
+        swiglu_bwd8(r + v * 8, gq[v], uq[v], o0[v], o1[v]);
         gq[v] = gn[v];
         uq[v] = un[v];
       }
@@ -542,9 +569,50 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
 // fit in shared memory. Only the even CTA issues MMAs; both CTAs' TMA loads
 // count on the even CTA's "full" barrier, the MMA completion is multicast to
 // both CTAs, and both epilogues report back to the even CTA.
-constexpr int kPairStages = 6;
 constexpr int kPairStage = 32768;                 // 16 KB of A + 16 KB of B per CTA
-constexpr int kPairSmem = kPairStages * kPairStage + kCtrlBytes + kStageAll + 1024;
+
+// SwiGLU-backward operand ring of the pair kernel: G and U of an epilogue
+// warp's coming 32-column slices are brought into shared memory by TMA (a
+// 32 x 32 box of each, the 64-byte swizzle of the output maps) two slices
+// ahead of the slice being drained, across tile boundaries, so their DRAM
+// latency hides behind the main loop; dG and dU are written back over G and U
+// and stored by TMA from the same slot. Three slots per warp take the room of
+// one operand stage (five stages instead of six).
+constexpr int kGuSlots = 3;
+constexpr int kGuSlotBytes = 2 * kBoxBytes;
+constexpr int kGuRingBytes = kGuSlots * kGuSlotBytes;
+constexpr int kGuBarOff = 4864;                   // ring mbarriers in the control block
+
+template <int EPI>
+struct PairCfg {
+  static constexpr bool RING = EPI == kEpiSwigluBwd;
+  static constexpr int STAGES = RING ? 5 : 6;
+  static constexpr int EPI_BYTES = RING ? kGuRingBytes : kStageBytes;   // per epilogue warp
+  static constexpr int SMEM = STAGES * kPairStage + kCtrlBytes + 4 * EPI_BYTES + 1024;
+};
+static_assert(PairCfg<kEpiSwigluBwd>::SMEM <= 232448, "pair SwiGLU-bwd shared memory");
+static_assert(PairCfg<kEpiStore>::SMEM <= 232448, "pair shared memory");
+static_assert(kGuBarOff >= 4608 + 33 * 4 && kGuBarOff + 4 * kGuSlots * 8 <= kCtrlBytes,
+              "ring barriers inside the control block, after the scan scratch");
+
+// dG and dU of one 32-column slice from dH (fp32, 32 tensor-memory columns of
+// this lane's row) and the row's G and U, in place in a ring slot: 16-byte
+// chunk j of the row sits at slot j ^ ((row >> 1) & 3) of its 64 bytes.
+__device__ __forceinline__ void swiglu_bwd_slice_inplace(uint8_t* slot, int lane,
+                                                         const uint32_t (&r)[32]) {
+  uint8_t* grow = slot + lane * 64;
+  uint8_t* urow = grow + kBoxBytes;
+  const int sw = (lane >> 1) & 3;
+#pragma unroll
+  for (int v = 0; v < 4; ++v) {
+    const int pos = (v ^ sw) << 4;
+    uint4 dg, du;
+    swiglu_bwd8(r + v * 8, *reinterpret_cast<const uint4*>(grow + pos),
+                *reinterpret_cast<const uint4*>(urow + pos), dg, du);
+    *reinterpret_cast<uint4*>(grow + pos) = dg;
+    *reinterpret_cast<uint4*>(urow + pos) = du;
+  }
+}
 
 template <int EPI, int A_MN, int B_MN>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
@@ -552,7 +620,8 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA,
                          const __grid_constant__ CUtensorMap tmB,
                          const __grid_constant__ CUtensorMap tmC,
                          const __grid_constant__ CUtensorMap tmC2, const Params p) {
-  constexpr int BN = 256, STAGES = kPairStages;
+  using PC = PairCfg<EPI>;
+  constexpr int BN = 256, STAGES = PC::STAGES;
   constexpr int A_BYTES = 16384;
   constexpr uint32_t TMEM_COLS = 2 * BN;
   extern __shared__ uint8_t smem_raw[];
@@ -603,6 +672,8 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA,
       ptx::mbar_init(bar_tempty + 8 * a, 8);       // 4 epilogue warps x 2 CTAs
     }
     ptx::mbar_init(bar_drain, 1);
+    if (PC::RING)
+      for (int i = 0; i < 4 * kGuSlots; ++i) ptx::mbar_init(ctrl_u + kGuBarOff + 8 * i, 1);
     ptx::fence_mbar_init();
   }
   if (warp == 1) {
@@ -742,6 +813,100 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA,
         ptx::mbar_wait(bar_drain, 0, kWaitBudget, nullptr);
       }
     }
+  } else if constexpr (PC::RING) {
+    // ------------------------------------------- SwiGLU-backward epilogue
+    const int q = warp & 3, ew = warp - 2;
+    uint8_t* ring = ctrl + kCtrlBytes + ew * kGuRingBytes;
+    const uint32_t ring_u32 = ctrl_u + kCtrlBytes + ew * kGuRingBytes;
+    const uint32_t rbar = ctrl_u + kGuBarOff + ew * 8 * kGuSlots;
+    const uint32_t leader_tempty[2] = {ptx::mapa_shared(bar_tempty, 0),
+                                       ptx::mapa_shared(bar_tempty + 8, 0)};
+    // this CTA's rows of pair tile pt, or -1 for the odd tile of a group
+    auto tile_rows = [&](int pt, int& row0, int& f0) {
+      int g, mp, nt, nk;
+      decode_pair(pt, g, mp, nt, nk);
+      const int mt = 2 * mp + (int)rank;
+      row0 = s_off[g] + mt * BM + q * 32;
+      f0 = nt * BN;
+      return mt < mtiles[g];
+    };
+    // load cursor: the next slice whose G and U are to be fetched
+    int lpt = cluster, lc = 0, lrow = 0, lf0 = 0;
+    while (lpt < total && !tile_rows(lpt, lrow, lf0)) lpt += nclusters;
+    uint32_t issued = 0, used = 0;
+    auto issue = [&]() {
+      if (lpt >= total) return;
+      const uint32_t slot = issued % kGuSlots;
+      if (lane == 0) {
+        const uint32_t b = rbar + 8 * slot, dst = ring_u32 + slot * kGuSlotBytes;
+        ptx::mbar_arrive_expect_tx(b, kGuSlotBytes);
+        ptx::tma_load_2d(dst, &tmC2, b, lf0 + lc, lrow);                  // G
+        ptx::tma_load_2d(dst + kBoxBytes, &tmC2, b, p.F + lf0 + lc, lrow);  // U
+      }
+      ++issued;
+      lc += 32;
+      if (lc == BN) {
+        lc = 0;
+        do lpt += nclusters;
+        while (lpt < total && !tile_rows(lpt, lrow, lf0));
+      }
+    };
+    issue();
+    issue();
+    uint32_t acc = 0, acc_phase = 0;
+    bool ok = true;
+    for (int pt = cluster; pt < total && ok; pt += nclusters) {
+      int row0, f0;
+      const bool mine = tile_rows(pt, row0, f0);
+      ok = __all_sync(0xffffffffu,
+                      ptx::mbar_wait(bar_tfull + 8 * acc, acc_phase, kWaitBudget, abort_flag));
+      if (!ok) break;
+      ptx::tc_fence_after();
+      if (mine) {
+        const uint32_t tbase = tmem_base + acc * BN + ((uint32_t)(q * 32) << 16);
+#pragma unroll 1
+        for (int c = 0; c < BN; c += 32) {
+          const uint32_t slot = used % kGuSlots;
+          ok = __all_sync(0xffffffffu, ptx::mbar_wait(rbar + 8 * slot, (used / kGuSlots) & 1u,
+                                                      kWaitBudget, abort_flag));
+          if (!ok) break;
+          uint32_t r[32];
+          ptx::tmem_ld32(tbase + c, r);
+          ptx::tmem_ld_wait();
+          swiglu_bwd_slice_inplace(ring + slot * kGuSlotBytes, lane, r);
+          ptx::fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            const uint32_t src = ring_u32 + slot * kGuSlotBytes;
+            ptx::tma_store_2d(&tmC, src, f0 + c, row0);                    // dG
+            ptx::tma_store_2d(&tmC, src + kBoxBytes, p.F + f0 + c, row0);  // dU
+            ptx::tma_store_commit();
+            // the slot of the slice before this one is free once its stores have read it
+            ptx::tma_store_wait_read_1();
+          }
+          ++used;
+          issue();
+        }
+        if (!ok) break;
+      }
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive_cluster(leader_tempty[acc]);
+      if (++acc == 2) {
+        acc = 0;
+        acc_phase ^= 1u;
+      }
+    }
+    if (!ok) {
+      if (lane == 0) {
+        record_status(p.status, MOE_ERR_TIMEOUT);
+        *abort_flag = 1;
+      }
+      // loads still in flight land before the CTA may exit
+      for (; used < issued; ++used)
+        ptx::mbar_wait(rbar + 8 * (used % kGuSlots), (used / kGuSlots) & 1u, kWaitBudget, nullptr);
+    }
+    if (lane == 0) ptx::tma_store_wait_all();
   } else {
     const int q = warp & 3;
     uint8_t* stage = ctrl + kCtrlBytes + (warp - 2) * kStageBytes;
@@ -881,12 +1046,12 @@ static cudaError_t run_pair(const CUtensorMap& a, const CUtensorMap& b, const CU
   static int grid = 0;
   if (grid == 0) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         kPairSmem);
+                                         PairCfg<EPI>::SMEM);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t lc = {};
     lc.gridDim = dim3(2 * (num_sms() / 2), 1, 1);
     lc.blockDim = dim3(kThreads, 1, 1);
-    lc.dynamicSmemBytes = kPairSmem;
+    lc.dynamicSmemBytes = PairCfg<EPI>::SMEM;
     int clusters = 0;
     e = cudaOccupancyMaxActiveClusters(&clusters, kern, &lc);
     if (e != cudaSuccess || clusters <= 0) {
@@ -895,7 +1060,7 @@ static cudaError_t run_pair(const CUtensorMap& a, const CUtensorMap& b, const CU
     }
     grid = 2 * clusters;
   }
-  kern<<<grid, kThreads, kPairSmem, s>>>(a, b, c, c2, p);
+  kern<<<grid, kThreads, PairCfg<EPI>::SMEM, s>>>(a, b, c, c2, p);
   return cudaGetLastError();
 }
 
@@ -980,11 +1145,11 @@ cudaError_t launch_ffn_fc2_dgrad(const moe_config& c, const void* dO_perm, const
   const int64_t R = rows_max(c);
   const int G = c.E + c.n_shared;
   const int bn = (c.F % 256 == 0) ? 256 : 128;
-  CUtensorMap a, b, oc;
+  CUtensorMap a, b, oc, gu;
   if (!make_map(&a, dO_perm, c.H, R, 128) || !make_map(&b, W2, c.F, (uint64_t)G * c.H, 64) ||
-      !make_out_map(&oc, dGU, 2ULL * c.F, R))
+      !make_out_map(&oc, dGU, 2ULL * c.F, R) || !make_out_map(&gu, GU, 2ULL * c.F, R))
     return cudaErrorInvalidValue;
-  const CUtensorMap& oc2 = oc;
+  const CUtensorMap& oc2 = gu;    // the pair kernel loads G and U through this map
   Params p = base_params(c, counts, offsets, status);
   p.N = c.F;
   p.K = c.H;
