@@ -66,8 +66,6 @@ struct Params {
   long long ldaux;
   int32_t* status;
   int dense_rows;             // > 0: one group of this many rows at row 0 (no counts/offsets)
-  int a_krep;                 // > 1: A's k-block is kb / a_krep (each A k-block used a_krep
-                              // times in a row against consecutive B k-blocks)
   // FC1 data gradient with the router term (kEpiDgradRouter): row r of a
   // routed group g < router_E gains dlogits[token_of[r], g] * W_r[g, :]
   const int32_t* token_of;
@@ -76,11 +74,17 @@ struct Params {
   int router_E;
 };
 
-template <int BN, int STAGES>
+// Router logits (kEpiStoreF32) multiply each A k-block by the three bf16 parts
+// of the fp32 weight, held in B as three consecutive 64-column blocks: one
+// stage carries the A block once and the three B blocks.
+template <int EPI>
+constexpr int b_parts() { return EPI == kEpiStoreF32 ? 3 : 1; }
+
+template <int BN, int STAGES, int BPARTS = 1>
 struct Layout {
   static constexpr int A_BYTES = BM * BK * 2;
   static constexpr int B_BYTES = BN * BK * 2;
-  static constexpr int STAGE = A_BYTES + B_BYTES;
+  static constexpr int STAGE = A_BYTES + BPARTS * B_BYTES;
   static constexpr int TILES = STAGES * STAGE;
   static constexpr int SMEM = TILES + kCtrlBytes + kStageAll + 1024;
   static constexpr int TMEM_COLS = 2 * BN;
@@ -350,7 +354,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                     const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmC2,
                     const Params p) {
-  using L = Layout<BN, STAGES>;
+  constexpr int BPARTS = b_parts<EPI>();
+  using L = Layout<BN, STAGES, BPARTS>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = ptx::smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
@@ -432,8 +437,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
           const uint32_t sB = sA + L::A_BYTES;
           const int k0 = kb * BK;
           if (A_MN == 0) {
-            ptx::tma_load_2d(sA, &tmA, fb, p.a_krep > 1 ? (kb / p.a_krep) * BK : k0,
-                             s_off[t.g] + t.mt * BM);
+            ptx::tma_load_2d(sA, &tmA, fb, k0, s_off[t.g] + t.mt * BM);
           } else {
             const int kr = s_off[t.g] + k0;
             ptx::tma_load_2d(sA, &tmA, fb, t.mt * BM, kr);
@@ -444,7 +448,10 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             ptx::tma_load_2d(sB, &tmB, fb, k0, t.g * p.b_rows + f0);
             ptx::tma_load_2d(sB + (BN / 2) * 128, &tmB, fb, k0, t.g * p.b_rows + p.F + f0);
           } else if (B_MN == 0) {
-            ptx::tma_load_2d(sB, &tmB, fb, k0, t.g * p.b_rows + t.nt * BN);
+#pragma unroll
+            for (int q = 0; q < BPARTS; ++q)
+              ptx::tma_load_2d(sB + q * L::B_BYTES, &tmB, fb, BPARTS * k0 + q * BK,
+                               t.g * p.b_rows + t.nt * BN);
           } else {
             const int kr = p.kgrouped ? s_off[t.g] + k0 : t.g * p.b_rows + k0;
 #pragma unroll
@@ -491,13 +498,16 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
           const uint32_t sA = base + stage * L::STAGE;
           const uint32_t sB = sA + L::A_BYTES;
 #pragma unroll
-          for (int kk = 0; kk < BK / 16; ++kk) {
-            const uint64_t ad = A_MN ? ptx::smem_desc_sw128(sA + kk * 2048, 8192, 1024)
-                                     : ptx::smem_desc_sw128(sA + kk * 32, 16, 1024);
-            const uint64_t bd = B_MN ? ptx::smem_desc_sw128(sB + kk * 2048, 8192, 1024)
-                                     : ptx::smem_desc_sw128(sB + kk * 32, 16, 1024);
-            ptx::mma_bf16(d, ad, bd, IDESC, (kb | kk) ? 1u : 0u);
-          }
+          for (int q = 0; q < BPARTS; ++q)
+#pragma unroll
+            for (int kk = 0; kk < BK / 16; ++kk) {
+              const uint64_t ad = A_MN ? ptx::smem_desc_sw128(sA + kk * 2048, 8192, 1024)
+                                       : ptx::smem_desc_sw128(sA + kk * 32, 16, 1024);
+              const uint32_t sq = sB + q * L::B_BYTES;
+              const uint64_t bd = B_MN ? ptx::smem_desc_sw128(sq + kk * 2048, 8192, 1024)
+                                       : ptx::smem_desc_sw128(sq + kk * 32, 16, 1024);
+              ptx::mma_bf16(d, ad, bd, IDESC, (kb | kk | q) ? 1u : 0u);
+            }
           issued = true;
           ptx::mma_commit(bar_empty + 8 * stage);
           if (++stage == STAGES) {
@@ -1025,7 +1035,7 @@ static bool make_out_map_f32(CUtensorMap* m, const void* ptr, uint64_t inner, ui
 template <int EPI, int BN, int A_MN, int B_MN, int STAGES>
 static cudaError_t run(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& c,
                        const CUtensorMap& c2, const Params& p, cudaStream_t s) {
-  using L = Layout<BN, STAGES>;
+  using L = Layout<BN, STAGES, b_parts<EPI>()>;
   auto kern = grouped_gemm_kernel<EPI, BN, A_MN, B_MN, STAGES>;
   static bool attr_set = false;
   if (!attr_set) {
@@ -1240,10 +1250,10 @@ cudaError_t launch_ffn_wgrad_fc1(const moe_config& c, const void* dGU, const voi
 // Router logits on the tensor cores: logits[T,E] = sum over the three bf16
 // parts of W_r (W_r = W_hi + W_mid + W_lo exactly) of x . part^T. W3 [E, 3H]
 // holds the parts interleaved per 64-column k-block (hi, mid, lo of columns
-// 64j..64j+63, then of the next 64), and x's k-block j is used for the three
-// consecutive k-blocks 3j..3j+2, so x is read from DRAM once (the repeats hit
-// L2). fp32 accumulation, one dense group of T rows (rows past T read zeros
-// and are not stored). Needs E % 128 == 0.
+// 64j..64j+63, then of the next 64); one pipeline stage carries x's k-block j
+// and the three part blocks 3j..3j+2, so every x tile is loaded once. fp32
+// accumulation, one dense group of T rows (rows past T read zeros and are not
+// stored). Needs E % 128 == 0.
 cudaError_t launch_router_logits_tc(const moe_config& c, const void* x, const void* W3,
                                     float* logits, int32_t* status, cudaStream_t s) {
   CUtensorMap a, b, oc;
@@ -1253,11 +1263,10 @@ cudaError_t launch_router_logits_tc(const moe_config& c, const void* x, const vo
   Params p{};
   p.G = 1;
   p.dense_rows = c.T;
-  p.a_krep = 3;
   p.N = c.E;
-  p.K = 3 * c.H;
+  p.K = c.H;
   p.status = status;
-  return run<kEpiStoreF32, 128, 0, 0, 6>(a, b, oc, oc, p, s);
+  return run<kEpiStoreF32, 128, 0, 0, 3>(a, b, oc, oc, p, s);
 }
 
 }  // namespace moe

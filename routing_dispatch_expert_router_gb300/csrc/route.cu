@@ -77,72 +77,118 @@ route_logits_kernel(const __nv_bfloat16* __restrict__ x, const float* __restrict
   }
 }
 
-// Few experts (E <= 16): the logits are a pure stream over x. A block of 4
-// warps owns 4 consecutive tokens; warp w walks the w-th quarter of H, each
-// lane loading 16-byte slices of the 4 rows (two slices in flight per row)
-// and the matching W_r slices, which the 4 tokens share. Lane partial sums are
-// combined by a fixed butterfly, then the 4 warps' sums in warp order, so the
-// summation order is deterministic.
-template <int EP>
-__global__ void __launch_bounds__(128)
-route_logits_few_kernel(const __nv_bfloat16* __restrict__ x, const float* __restrict__ W,
+// Few experts (E <= 16): logits on the warp-level tensor-core MMA (mma.sync
+// m16n8k16, bf16 operands, fp32 accumulation): with 8 or 16 output columns a
+// tile needs no tensor memory or TMA pipeline, and the kernel is a stream over
+// x. W_r is split in registers into three bf16 parts, hi = bf16(w),
+// mid = bf16(w - hi), lo = w - hi - mid (exact: hi + mid + lo == w), so the
+// products are those of the fp32 weights. A block of 8 warps owns 16 tokens;
+// warp w takes the 32-column chunks w, w + 8, ... of H, D chunks in flight.
+// Inside a chunk the reduction index is permuted the same way in A and B so
+// that every lane's fragments are 16-byte loads: lane (g = lane / 4,
+// q = lane % 4) loads columns 8q..8q+7 of token rows g and g + 8 and of weight
+// row g (+ 8 per n-tile); the chunk's first MMA covers columns 8q..8q+3 of
+// every lane, the second 8q+4..8q+7. The warps' partial sums are added in warp
+// order through shared memory, so the summation order is fixed.
+__device__ __forceinline__ void mma_m16n8k16_bf16(float (&d)[4], uint32_t a0, uint32_t a1,
+                                                  uint32_t a2, uint32_t a3, uint32_t b0,
+                                                  uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
+      "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// Two fp32 weights -> their three packed bf16 parts (pairs: low half = first).
+__device__ __forceinline__ void split3_pair(float w0, float w1, uint32_t& hi, uint32_t& mid,
+                                            uint32_t& lo) {
+  hi = pack_bf16x2(w0, w1);
+  const float r0 = w0 - bf16_lo(hi), r1 = w1 - bf16_hi(hi);
+  mid = pack_bf16x2(r0, r1);
+  lo = pack_bf16x2(r0 - bf16_lo(mid), r1 - bf16_hi(mid));
+}
+
+template <int NT>
+__global__ void __launch_bounds__(256)
+route_logits_mma_kernel(const __nv_bfloat16* __restrict__ x, const float* __restrict__ W,
                         float* __restrict__ logits, int T, int H, int E) {
-  constexpr int TPB = 4;
-  __shared__ float part[4][TPB][EP];
+  constexpr int D = NT == 1 ? 4 : 2;               // chunks in flight per warp
+  __shared__ float part[8][16][8 * NT];
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
-  const int t0 = blockIdx.x * TPB;
-  float acc[TPB][EP];
+  const int g = lane >> 2, q = lane & 3;
+  const int t0 = blockIdx.x * 16;
+  const bool ok0 = t0 + g < T, ok1 = t0 + g + 8 < T;
+  const __nv_bfloat16* x0 = x + (size_t)(t0 + g) * H + 8 * q;
+  const __nv_bfloat16* x1 = x0 + (size_t)8 * H;
+  bool wok[NT];
+  const float* wrow[NT];
 #pragma unroll
-  for (int i = 0; i < TPB; ++i)
+  for (int n = 0; n < NT; ++n) {
+    wok[n] = 8 * n + g < E;
+    wrow[n] = W + (size_t)(8 * n + g) * H + 8 * q;
+  }
+  const int nchunks = H >> 5;
+  const int mine = nchunks > wid ? (nchunks - wid + 7) >> 3 : 0;
+  uint4 xa[D], xb[D];
+  float4 wa[D][NT], wb[D][NT];
+  auto load = [&](int d, int i) {
+    const int col = (wid + 8 * i) * 32;
+    const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+    xa[d] = ok0 ? ldg_nc_v4(x0 + col) : z;
+    xb[d] = ok1 ? ldg_nc_v4(x1 + col) : z;
 #pragma unroll
-    for (int e = 0; e < EP; ++e) acc[i][e] = 0.f;
-  const int nvec = H >> 3, per = nvec >> 2;
-  const int cbeg = wid * per, cend = cbeg + per;
-  for (int c0 = cbeg + lane; c0 < cend; c0 += 64) {
-    float xf[2][TPB][8];
-#pragma unroll
-    for (int u = 0; u < 2; ++u) {
-      const int c = c0 + 32 * u;
-#pragma unroll
-      for (int i = 0; i < TPB; ++i) {
-        if (c < cend && t0 + i < T) {
-          unpack8(ldg_nc_v4(x + (size_t)(t0 + i) * H + (size_t)c * 8), xf[u][i]);
-        } else {
-#pragma unroll
-          for (int q = 0; q < 8; ++q) xf[u][i][q] = 0.f;
-        }
-      }
+    for (int n = 0; n < NT; ++n) {
+      const float4 zf = make_float4(0.f, 0.f, 0.f, 0.f);
+      wa[d][n] = wok[n] ? __ldg(reinterpret_cast<const float4*>(wrow[n] + col)) : zf;
+      wb[d][n] = wok[n] ? __ldg(reinterpret_cast<const float4*>(wrow[n] + col) + 1) : zf;
     }
+  };
+  float acc[NT][4];
 #pragma unroll
-    for (int u = 0; u < 2; ++u) {
-      const int c = c0 + 32 * u;
-      if (c >= cend) break;
+  for (int n = 0; n < NT; ++n)
 #pragma unroll
-      for (int e = 0; e < EP; ++e) {
-        if (e >= E) break;
-        const float4* wp = reinterpret_cast<const float4*>(W + (size_t)e * H + (size_t)c * 8);
-        const float4 a = __ldg(wp), b = __ldg(wp + 1);
-        const float wv[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+    for (int j = 0; j < 4; ++j) acc[n][j] = 0.f;
 #pragma unroll
-        for (int i = 0; i < TPB; ++i)
+  for (int d = 0; d < D; ++d)
+    if (d < mine) load(d, d);
+  for (int i = 0; i < mine; i += D) {
 #pragma unroll
-          for (int q = 0; q < 8; ++q) acc[i][e] = fmaf(xf[u][i][q], wv[q], acc[i][e]);
+    for (int d = 0; d < D; ++d) {
+      if (i + d >= mine) break;
+#pragma unroll
+      for (int n = 0; n < NT; ++n) {
+        uint32_t h[4], m[4], l[4];
+        split3_pair(wa[d][n].x, wa[d][n].y, h[0], m[0], l[0]);
+        split3_pair(wa[d][n].z, wa[d][n].w, h[1], m[1], l[1]);
+        split3_pair(wb[d][n].x, wb[d][n].y, h[2], m[2], l[2]);
+        split3_pair(wb[d][n].z, wb[d][n].w, h[3], m[3], l[3]);
+        mma_m16n8k16_bf16(acc[n], xa[d].x, xb[d].x, xa[d].y, xb[d].y, h[0], h[1]);
+        mma_m16n8k16_bf16(acc[n], xa[d].z, xb[d].z, xa[d].w, xb[d].w, h[2], h[3]);
+        mma_m16n8k16_bf16(acc[n], xa[d].x, xb[d].x, xa[d].y, xb[d].y, m[0], m[1]);
+        mma_m16n8k16_bf16(acc[n], xa[d].z, xb[d].z, xa[d].w, xb[d].w, m[2], m[3]);
+        mma_m16n8k16_bf16(acc[n], xa[d].x, xb[d].x, xa[d].y, xb[d].y, l[0], l[1]);
+        mma_m16n8k16_bf16(acc[n], xa[d].z, xb[d].z, xa[d].w, xb[d].w, l[2], l[3]);
       }
+      if (i + d + D < mine) load(d, i + d + D);
     }
   }
+  // accumulator fragment: (row g, columns 2q, 2q+1) and (row g + 8, same)
 #pragma unroll
-  for (int i = 0; i < TPB; ++i)
-#pragma unroll
-    for (int e = 0; e < EP; ++e) {
-      const float v = warp_sum(acc[i][e]);
-      if (lane == 0) part[wid][i][e] = v;
-    }
+  for (int n = 0; n < NT; ++n) {
+    part[wid][g][8 * n + 2 * q] = acc[n][0];
+    part[wid][g][8 * n + 2 * q + 1] = acc[n][1];
+    part[wid][g + 8][8 * n + 2 * q] = acc[n][2];
+    part[wid][g + 8][8 * n + 2 * q + 1] = acc[n][3];
+  }
   __syncthreads();
-  if (threadIdx.x < TPB * EP) {
-    const int i = threadIdx.x / EP, e = threadIdx.x % EP;
-    if (e < E && t0 + i < T) {
-      const float v = ((part[0][i][e] + part[1][i][e]) + part[2][i][e]) + part[3][i][e];
-      logits[(size_t)(t0 + i) * E + e] = v;
+  for (int v = threadIdx.x; v < 16 * 8 * NT; v += 256) {
+    const int r = v / (8 * NT), e = v % (8 * NT);
+    if (t0 + r < T && e < E) {
+      float sum = part[0][r][e];
+#pragma unroll
+      for (int w = 1; w < 8; ++w) sum += part[w][r][e];
+      logits[(size_t)(t0 + r) * E + e] = sum;
     }
   }
 }
@@ -273,11 +319,11 @@ __device__ __forceinline__ void group_ids(int lane, int E, int per, int (&gid)[N
 // (NaN ranks last), optional group limit (group score = top-1 or top-2 sum of
 // the group's keys in fp64), top-k with ties to the lower expert, weights =
 // softmax over the selected (logit + bias). Lane l owns experts l, l+32, ...
+template <int NPL>
 __global__ void __launch_bounds__(256)
 route_select_softmax_kernel(const float* __restrict__ logits, const float* __restrict__ bias,
                             int32_t* __restrict__ idx, float* __restrict__ wout, int T, int E,
                             int k, int n_groups, int topk_groups, int group_score) {
-  constexpr int NPL = kMaxExperts / 32;
   const int lane = threadIdx.x & 31;
   const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   if (t >= T) return;
@@ -387,25 +433,33 @@ __device__ __forceinline__ void exact_sigmoids(const float* __restrict__ lrow, u
 //
 // fp64 is slow on this part, so the fp64 keys are computed only where they can
 // decide anything. Every key is first formed in fp32 (A, off the fp64 key by
-// at most 3.6e-7 + 6e-8 |A|). A group's top-m (m = 2 for the top-2 sum, else
-// 1) can only contain experts with A >= (the group's m-th best A) - margin,
-// and the final top-k only experts with A >= (the k-th best A among the kept
-// groups) - margin, with margin = 1e-5 (1 + |threshold|), well above twice
-// the fp32 error: any other expert has m (or k) experts whose fp64 key is
-// strictly larger. Those candidates get their fp64 keys, and the group scores
-// and the selection are taken on fp64 keys alone, so the result is the one
-// the fp64 keys of all experts give.
+// at most 3.6e-7 + 6e-8 |A|; margin(x) = 1e-5 (1 + |x|) is well above twice
+// that).
+//   Fast path: the group scores and the top-k are taken on the fp32 keys, and
+//   the result stands when every decision is clear by the margins: every kept
+//   group's score minus its margin (the sum of its top-m keys' margins) above
+//   every dropped group's score plus its margin, and each of the k selected
+//   keys above the next one in the order (the (k+1)-th included) by more than
+//   margin(larger |key|). The fp64 keys then select and order exactly the same
+//   way. The weights come from the fp32 sigmoids (a few ulp).
+//   Exact path (a decision within a margin): a group's top-m (m = 2 for the
+//   top-2 sum, else 1) can only contain experts with A >= (the group's m-th
+//   best A) - margin, and the final top-k only experts with A >= (the k-th best
+//   A among the kept groups) - margin: any other expert has m (or k) experts
+//   whose fp64 key is strictly larger. Those candidates get their fp64 keys,
+//   and the group scores and the selection are taken on fp64 keys alone, so the
+//   result is the one the fp64 keys of all experts give.
+template <int NPL>
 __global__ void __launch_bounds__(128)
 route_select_sigmoid_kernel(const float* __restrict__ logits, const float* __restrict__ bias,
                             int32_t* __restrict__ idx, float* __restrict__ wout, int T, int E,
                             int k, int n_groups, int topk_groups, int group_score,
                             float route_scale) {
-  constexpr int NPL = kMaxExperts / 32;
   const int lane = threadIdx.x & 31;
   const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   if (t >= T) return;
   const float* lrow = logits + (size_t)t * E;
-  float A[NPL];
+  float A[NPL], s32[NPL];
   double s64[NPL];
   bool avail[NPL];
 #pragma unroll
@@ -413,14 +467,110 @@ route_select_sigmoid_kernel(const float* __restrict__ logits, const float* __res
     const int e = lane + 32 * i;
     avail[i] = e < E;
     A[i] = -INFINITY;
+    s32[i] = 0.f;
     s64[i] = 0.0;
     if (e < E) {
-      const float s32 = __fdiv_rn(1.f, 1.f + expf(-lrow[e]));
-      const float v = __fadd_rn(s32, bias ? bias[e] : 0.f);
+      s32[i] = __fdiv_rn(1.f, 1.f + expf(-lrow[e]));
+      const float v = __fadd_rn(s32[i], bias ? bias[e] : 0.f);
       A[i] = isnan(v) ? -INFINITY : v;
     }
   }
   auto margin = [](float thr) { return 1e-5f * (1.f + fabsf(thr)); };
+  // ------------------------------------------------ fast path (fp32 decisions)
+  {
+    bool clear = true;
+    bool av[NPL];
+#pragma unroll
+    for (int i = 0; i < NPL; ++i) av[i] = avail[i];
+    if (n_groups > 1) {
+      const int per = E / n_groups;
+      const bool two = group_score == MOE_GROUP_TOP2_SUM && per >= 2;
+      int gid[NPL];
+      group_ids<NPL>(lane, E, per, gid);
+      // fp32 group scores (no fp64 instruction on this path: the fp64 pipe is
+      // narrow on this part)
+      float gs_mine = -INFINITY, gm_mine = 0.f;
+      for (int g = 0; g < n_groups; ++g) {
+        float a1 = -INFINITY, a2 = -INFINITY;
+        if (per == 32) {
+#pragma unroll
+          for (int i = 0; i < NPL; ++i)
+            if (i == g) a1 = A[i];
+        } else {
+#pragma unroll
+          for (int i = 0; i < NPL; ++i)
+            if (gid[i] == g) top2_insert_f(A[i], a1, a2);
+        }
+        warp_top2_f(a1, a2);
+        if (lane == g) {
+          gs_mine = two ? a1 + a2 : a1;
+          gm_mine = two ? margin(a1) + margin(a2) : margin(a1);
+        }
+      }
+      uint32_t kept = 0;
+      for (int r = 0; r < topk_groups; ++r) {
+        uint64_t key = (lane < n_groups && !((kept >> lane) & 1u)) ? pack_key(gs_mine, lane) : 0ull;
+        key = warp_max_u64(key);
+        kept |= 1u << packed_expert(key);
+      }
+      // clear when every kept group's lowest possible score is above every
+      // dropped group's highest possible one
+      float lo = INFINITY, hi = -INFINITY;
+      if (lane < n_groups) {
+        if ((kept >> lane) & 1u) lo = gs_mine - gm_mine;
+        else hi = gs_mine + gm_mine;
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        lo = fminf(lo, __shfl_xor_sync(0xffffffffu, lo, o));
+        hi = fmaxf(hi, __shfl_xor_sync(0xffffffffu, hi, o));
+      }
+      clear = lo > hi;
+#pragma unroll
+      for (int i = 0; i < NPL; ++i)
+        if (gid[i] >= 0 && !((kept >> gid[i]) & 1u)) av[i] = false;
+    }
+    int my_e = 0;
+    float my_s = 0.f, prev = 0.f;
+    for (int j = 0; j <= k && clear; ++j) {
+      uint64_t best = 0;
+#pragma unroll
+      for (int i = 0; i < NPL; ++i) {
+        if (!av[i]) continue;
+        const uint64_t p = pack_key(A[i], lane + 32 * i);
+        best = p > best ? p : best;
+      }
+      best = warp_max_u64(best);
+      if (best == 0) break;                        // fewer than k + 1 experts available
+      const int e = packed_expert(best);
+      const float a = unord32((uint32_t)(best >> 32));
+      if (j > 0) clear = (prev - a) > margin(fmaxf(fabsf(prev), fabsf(a)));
+      prev = a;
+      if (j == k) break;
+      float sv = 0.f;
+#pragma unroll
+      for (int i = 0; i < NPL; ++i)
+        if (lane + 32 * i == e) {
+          av[i] = false;
+          sv = s32[i];
+        }
+      sv = __shfl_sync(0xffffffffu, sv, e & 31);
+      if (lane == j) {
+        my_e = e;
+        my_s = sv;
+      }
+    }
+    if (clear) {
+      float ss = 0.f;
+      for (int j = 0; j < k; ++j) ss += __shfl_sync(0xffffffffu, my_s, j);
+      if (lane < k) {
+        idx[(size_t)t * k + lane] = my_e;
+        wout[(size_t)t * k + lane] = route_scale * my_s / ss;
+      }
+      return;
+    }
+  }
+  // ------------------------------------------------ exact path (fp64 decisions)
   // ordered fp64 key of owned expert i (its s64 must have been evaluated)
   auto key64 = [&](int i) -> uint64_t {
     const double v = s64[i] + (double)(bias ? bias[lane + 32 * i] : 0.f);
@@ -554,21 +704,30 @@ route_select_sigmoid_kernel(const float* __restrict__ logits, const float* __res
 // lo = bf16(w - hi - mid) (each keeps 8 significant bits, so hi + mid + lo == w
 // exactly for every fp32 w: the two subtractions are exact), interleaved per
 // 64 columns: columns 64j..64j+63 of hi, of mid, of lo, then the next 64.
+// One thread per 8 consecutive columns (H % 64 == 0): two 16-byte loads, three
+// 16-byte stores.
 __global__ void __launch_bounds__(256)
 split3_kernel(const float* __restrict__ W, __nv_bfloat16* __restrict__ W3, int E, int H) {
-  const long long n = (long long)E * H;
-  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n;
-       i += (long long)gridDim.x * blockDim.x) {
-    const int e = (int)(i / H), h = (int)(i % H);
-    const float v = W[i];
-    const __nv_bfloat16 hi = __float2bfloat16_rn(v);
-    const float r1 = v - __bfloat162float(hi);
-    const __nv_bfloat16 mid = __float2bfloat16_rn(r1);
-    const float r2 = r1 - __bfloat162float(mid);
-    __nv_bfloat16* blk = W3 + (size_t)e * 3 * H + (size_t)(h / 64) * 192 + (h % 64);
-    blk[0] = hi;
-    blk[64] = mid;
-    blk[128] = __float2bfloat16_rn(r2);
+  const int per_row = H >> 3;
+  const long long n = (long long)E * per_row;
+  for (long long v = (long long)blockIdx.x * blockDim.x + threadIdx.x; v < n;
+       v += (long long)gridDim.x * blockDim.x) {
+    const int e = (int)(v / per_row), h = (int)(v - (long long)e * per_row) << 3;
+    const float4* src = reinterpret_cast<const float4*>(W + (size_t)e * H + h);
+    const float4 a = __ldg(src), b = __ldg(src + 1);
+    const float f[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+    float hi[8], mid[8], lo[8];
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      hi[q] = __bfloat162float(__float2bfloat16_rn(f[q]));
+      const float r1 = f[q] - hi[q];
+      mid[q] = __bfloat162float(__float2bfloat16_rn(r1));
+      lo[q] = r1 - mid[q];
+    }
+    uint4* blk = reinterpret_cast<uint4*>(W3 + (size_t)e * 3 * H + (size_t)(h >> 6) * 192 + (h & 63));
+    blk[0] = pack8(hi);
+    blk[8] = pack8(mid);                          // + 64 columns
+    blk[16] = pack8(lo);                          // + 128 columns
   }
 }
 
@@ -584,7 +743,7 @@ cudaError_t launch_route(const moe_config& c, const void* x, const float* W_r, c
   if (router_on_tensor_cores(c)) {
     // logits on the tensor cores from the exact three-way bf16 split of W_r
     __nv_bfloat16* W3 = reinterpret_cast<__nv_bfloat16*>(scratch + router_split_offset(c));
-    const long long n = (long long)c.E * c.H;
+    const long long n = (long long)c.E * (c.H / 8);
     long long blocks = (n + 255) / 256;
     if (blocks > (long long)num_sms() * 16) blocks = (long long)num_sms() * 16;
     split3_kernel<<<(int)blocks, 256, 0, s>>>(W_r, W3, c.E, c.H);
@@ -594,23 +753,31 @@ cudaError_t launch_route(const moe_config& c, const void* x, const float* W_r, c
                                   reinterpret_cast<int32_t*>(scratch + kScratchStatus), s);
     if (err != cudaSuccess) return err;
   } else if (c.E <= 16) {
-    const int blocks = (c.T + 3) / 4;        // 4 tokens per block of 4 warps
+    const int blocks = (c.T + 15) / 16;      // 16 tokens per block of 8 warps
     if (c.E <= 8)
-      route_logits_few_kernel<8><<<blocks, 128, 0, s>>>(xb, W_r, logits, c.T, c.H, c.E);
+      route_logits_mma_kernel<1><<<blocks, 256, 0, s>>>(xb, W_r, logits, c.T, c.H, c.E);
     else
-      route_logits_few_kernel<16><<<blocks, 128, 0, s>>>(xb, W_r, logits, c.T, c.H, c.E);
+      route_logits_mma_kernel<2><<<blocks, 256, 0, s>>>(xb, W_r, logits, c.T, c.H, c.E);
   } else {
     dim3 grid((c.T + 63) / 64, (c.E + 63) / 64);
     route_logits_kernel<64, 64><<<grid, 256, 0, s>>>(xb, W_r, logits, c.T, c.H, c.E);
   }
   if (cudaError_t err = cudaGetLastError(); err != cudaSuccess) return err;
-  if (c.score_fn == MOE_SCORE_SOFTMAX)
-    route_select_softmax_kernel<<<(c.T + 7) / 8, 256, 0, s>>>(
-        logits, bias, idx, w, c.T, c.E, c.k, c.n_groups, c.topk_groups, c.group_score);
-  else
-    route_select_sigmoid_kernel<<<(c.T + 3) / 4, 128, 0, s>>>(
-        logits, bias, idx, w, c.T, c.E, c.k, c.n_groups, c.topk_groups, c.group_score,
-        c.route_scale);
+  // experts per lane: the smallest of 1, 2, 4, 8 that covers E
+  const int npl = c.E <= 32 ? 1 : c.E <= 64 ? 2 : c.E <= 128 ? 4 : 8;
+  if (c.score_fn == MOE_SCORE_SOFTMAX) {
+    auto kern = npl == 1 ? route_select_softmax_kernel<1>
+              : npl == 2 ? route_select_softmax_kernel<2>
+              : npl == 4 ? route_select_softmax_kernel<4> : route_select_softmax_kernel<8>;
+    kern<<<(c.T + 7) / 8, 256, 0, s>>>(logits, bias, idx, w, c.T, c.E, c.k, c.n_groups,
+                                       c.topk_groups, c.group_score);
+  } else {
+    auto kern = npl == 1 ? route_select_sigmoid_kernel<1>
+              : npl == 2 ? route_select_sigmoid_kernel<2>
+              : npl == 4 ? route_select_sigmoid_kernel<4> : route_select_sigmoid_kernel<8>;
+    kern<<<(c.T + 3) / 4, 128, 0, s>>>(logits, bias, idx, w, c.T, c.E, c.k, c.n_groups,
+                                       c.topk_groups, c.group_score, c.route_scale);
+  }
   return cudaGetLastError();
 }
 
