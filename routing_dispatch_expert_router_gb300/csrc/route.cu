@@ -358,21 +358,21 @@ route_select_softmax_kernel(const float* __restrict__ logits, const float* __res
     }
     keep_best_groups<NPL>(gs_mine, lane, n_groups, topk_groups, gid, avail);
   }
+  // packed keys of the available experts (0 = not available), then k rounds
+  // of a warp maximum; the winner's slot is cleared
+  uint64_t pk[NPL];
+#pragma unroll
+  for (int i = 0; i < NPL; ++i) pk[i] = avail[i] ? pack_key(key[i], lane + 32 * i) : 0ull;
   int my_e = 0;
   for (int j = 0; j < k; ++j) {
-    uint64_t best = 0;
+    uint64_t best = pk[0];
 #pragma unroll
-    for (int i = 0; i < NPL; ++i) {
-      if (!avail[i]) continue;
-      const uint64_t p = pack_key(key[i], lane + 32 * i);
-      best = p > best ? p : best;
-    }
+    for (int i = 1; i < NPL; ++i) best = pk[i] > best ? pk[i] : best;
     best = warp_max_u64(best);
-    const int e = packed_expert(best);
 #pragma unroll
     for (int i = 0; i < NPL; ++i)
-      if (lane + 32 * i == e) avail[i] = false;
-    if (lane == j) my_e = e;
+      if (pk[i] == best) pk[i] = 0ull;
+    if (lane == j) my_e = packed_expert(best);
   }
   // weights: softmax over the selected (logit + bias), relative to the first
   float z = 0.f, z0 = 0.f;
@@ -450,7 +450,7 @@ __device__ __forceinline__ void exact_sigmoids(const float* __restrict__ lrow, u
 //   and the group scores and the selection are taken on fp64 keys alone, so the
 //   result is the one the fp64 keys of all experts give.
 template <int NPL>
-__global__ void __launch_bounds__(128)
+__global__ void __launch_bounds__(128, 6)
 route_select_sigmoid_kernel(const float* __restrict__ logits, const float* __restrict__ bias,
                             int32_t* __restrict__ idx, float* __restrict__ wout, int T, int E,
                             int k, int n_groups, int topk_groups, int group_score,
@@ -459,19 +459,16 @@ route_select_sigmoid_kernel(const float* __restrict__ logits, const float* __res
   const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   if (t >= T) return;
   const float* lrow = logits + (size_t)t * E;
-  float A[NPL], s32[NPL];
-  double s64[NPL];
+  float A[NPL];
   bool avail[NPL];
 #pragma unroll
   for (int i = 0; i < NPL; ++i) {
     const int e = lane + 32 * i;
     avail[i] = e < E;
     A[i] = -INFINITY;
-    s32[i] = 0.f;
-    s64[i] = 0.0;
     if (e < E) {
-      s32[i] = __fdiv_rn(1.f, 1.f + expf(-lrow[e]));
-      const float v = __fadd_rn(s32[i], bias ? bias[e] : 0.f);
+      const float s32 = __fdiv_rn(1.f, 1.f + expf(-lrow[e]));
+      const float v = __fadd_rn(s32, bias ? bias[e] : 0.f);
       A[i] = isnan(v) ? -INFINITY : v;
     }
   }
@@ -479,35 +476,42 @@ route_select_sigmoid_kernel(const float* __restrict__ logits, const float* __res
   // ------------------------------------------------ fast path (fp32 decisions)
   {
     bool clear = true;
-    bool av[NPL];
-#pragma unroll
-    for (int i = 0; i < NPL; ++i) av[i] = avail[i];
+    uint32_t kept = 0xffffffffu;
+    int gid[NPL];
     if (n_groups > 1) {
       const int per = E / n_groups;
       const bool two = group_score == MOE_GROUP_TOP2_SUM && per >= 2;
-      int gid[NPL];
       group_ids<NPL>(lane, E, per, gid);
       // fp32 group scores (no fp64 instruction on this path: the fp64 pipe is
       // narrow on this part)
       float gs_mine = -INFINITY, gm_mine = 0.f;
-      for (int g = 0; g < n_groups; ++g) {
-        float a1 = -INFINITY, a2 = -INFINITY;
-        if (per == 32) {
+      if (per == 32) {
+        // lane l's expert of group g is l + 32 g: the groups' reductions are
+        // independent and unrolled
 #pragma unroll
-          for (int i = 0; i < NPL; ++i)
-            if (i == g) a1 = A[i];
-        } else {
+        for (int g = 0; g < NPL; ++g) {
+          if (g >= n_groups) break;
+          float a1 = A[g], a2 = -INFINITY;
+          warp_top2_f(a1, a2);
+          if (lane == g) {
+            gs_mine = two ? a1 + a2 : a1;
+            gm_mine = two ? margin(a1) + margin(a2) : margin(a1);
+          }
+        }
+      } else {
+        for (int g = 0; g < n_groups; ++g) {
+          float a1 = -INFINITY, a2 = -INFINITY;
 #pragma unroll
           for (int i = 0; i < NPL; ++i)
             if (gid[i] == g) top2_insert_f(A[i], a1, a2);
-        }
-        warp_top2_f(a1, a2);
-        if (lane == g) {
-          gs_mine = two ? a1 + a2 : a1;
-          gm_mine = two ? margin(a1) + margin(a2) : margin(a1);
+          warp_top2_f(a1, a2);
+          if (lane == g) {
+            gs_mine = two ? a1 + a2 : a1;
+            gm_mine = two ? margin(a1) + margin(a2) : margin(a1);
+          }
         }
       }
-      uint32_t kept = 0;
+      kept = 0;
       for (int r = 0; r < topk_groups; ++r) {
         uint64_t key = (lane < n_groups && !((kept >> lane) & 1u)) ? pack_key(gs_mine, lane) : 0ull;
         key = warp_max_u64(key);
@@ -526,41 +530,35 @@ route_select_sigmoid_kernel(const float* __restrict__ logits, const float* __res
         hi = fmaxf(hi, __shfl_xor_sync(0xffffffffu, hi, o));
       }
       clear = lo > hi;
+    }
+    // packed keys of the available experts (0 = not available), then k + 1
+    // rounds of a warp maximum; the winner's slot is cleared
+    uint64_t pk[NPL];
 #pragma unroll
-      for (int i = 0; i < NPL; ++i)
-        if (gid[i] >= 0 && !((kept >> gid[i]) & 1u)) av[i] = false;
+    for (int i = 0; i < NPL; ++i) {
+      const bool in = avail[i] && (n_groups <= 1 || ((kept >> gid[i]) & 1u));
+      pk[i] = in ? pack_key(A[i], lane + 32 * i) : 0ull;
     }
     int my_e = 0;
-    float my_s = 0.f, prev = 0.f;
+    float prev = 0.f;
     for (int j = 0; j <= k && clear; ++j) {
-      uint64_t best = 0;
+      uint64_t best = pk[0];
 #pragma unroll
-      for (int i = 0; i < NPL; ++i) {
-        if (!av[i]) continue;
-        const uint64_t p = pack_key(A[i], lane + 32 * i);
-        best = p > best ? p : best;
-      }
+      for (int i = 1; i < NPL; ++i) best = pk[i] > best ? pk[i] : best;
       best = warp_max_u64(best);
       if (best == 0) break;                        // fewer than k + 1 experts available
-      const int e = packed_expert(best);
       const float a = unord32((uint32_t)(best >> 32));
       if (j > 0) clear = (prev - a) > margin(fmaxf(fabsf(prev), fabsf(a)));
       prev = a;
       if (j == k) break;
-      float sv = 0.f;
 #pragma unroll
       for (int i = 0; i < NPL; ++i)
-        if (lane + 32 * i == e) {
-          av[i] = false;
-          sv = s32[i];
-        }
-      sv = __shfl_sync(0xffffffffu, sv, e & 31);
-      if (lane == j) {
-        my_e = e;
-        my_s = sv;
-      }
+        if (pk[i] == best) pk[i] = 0ull;
+      if (lane == j) my_e = packed_expert(best);
     }
     if (clear) {
+      // the selected experts' fp32 sigmoids, recomputed as above
+      const float my_s = lane < k ? __fdiv_rn(1.f, 1.f + expf(-lrow[my_e])) : 0.f;
       float ss = 0.f;
       for (int j = 0; j < k; ++j) ss += __shfl_sync(0xffffffffu, my_s, j);
       if (lane < k) {
@@ -570,6 +568,9 @@ route_select_sigmoid_kernel(const float* __restrict__ logits, const float* __res
       return;
     }
   }
+  double s64[NPL];
+#pragma unroll
+  for (int i = 0; i < NPL; ++i) s64[i] = 0.0;
   // ------------------------------------------------ exact path (fp64 decisions)
   // ordered fp64 key of owned expert i (its s64 must have been evaluated)
   auto key64 = [&](int i) -> uint64_t {
