@@ -72,6 +72,12 @@ struct Params {
   const float* dlogits;
   const float* W_r;
   int router_E;
+  // Pair-tile order: 1 = n-tiles vary fastest, else m-pairs. Weight gradients
+  // whose output is taller than wide take n-fastest: the clusters running at
+  // once then share the A slice (the group's rows x 256 output rows) and stream
+  // B, which is the smaller operand and stays in L2 (Mixtral-sized dW13: the
+  // group's dGU is read from DRAM once instead of about four times).
+  int n_fast;
 };
 
 // Router logits (kEpiStoreF32) multiply each A k-block by the three bf16 parts
@@ -704,8 +710,13 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA,
     g = find_group(prefix, G, pt);
     const int local = pt - prefix[g];
     const int npairs = (mtiles[g] + 1) >> 1;
-    mp = local % npairs;
-    nt = local / npairs;
+    if (p.n_fast) {
+      nt = local % NT;
+      mp = local / NT;
+    } else {
+      mp = local % npairs;
+      nt = local / npairs;
+    }
     nk = p.kgrouped ? (s_cnt[g] + BK - 1) / BK : p.K / BK;
   };
 
@@ -1219,6 +1230,7 @@ cudaError_t launch_ffn_wgrad_fc2(const moe_config& c, const void* dO_perm, const
   p.out = static_cast<__nv_bfloat16*>(dW2);
   p.ldo = c.F;
   p.out_gstride = (long long)c.H * c.F;
+  p.n_fast = p.Mw > p.N;
   if (use_pairs(c, c.F)) return run_pair<kEpiWgrad, 1, 1>(a, b, oc, oc2, p, s);
   return bn == 256 ? run<kEpiWgrad, 256, 1, 1, 4>(a, b, oc, oc2, p, s)
                    : run<kEpiWgrad, 128, 1, 1, 6>(a, b, oc, oc2, p, s);
@@ -1242,6 +1254,7 @@ cudaError_t launch_ffn_wgrad_fc1(const moe_config& c, const void* dGU, const voi
   p.out = static_cast<__nv_bfloat16*>(dW13);
   p.ldo = c.H;
   p.out_gstride = 2LL * c.F * c.H;
+  p.n_fast = p.Mw > p.N;
   if (use_pairs(c, c.H)) return run_pair<kEpiWgrad, 1, 1>(a, b, oc, oc2, p, s);
   return bn == 256 ? run<kEpiWgrad, 256, 1, 1, 4>(a, b, oc, oc2, p, s)
                    : run<kEpiWgrad, 128, 1, 1, 6>(a, b, oc, oc2, p, s);
