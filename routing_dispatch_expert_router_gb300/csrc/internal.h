@@ -43,10 +43,12 @@ cudaError_t launch_router_wgrad(const moe_config& c, const void* x, const int32_
 
 // FP8 block quantisation (E4M3 values with power-of-two scales, stored as bf16).
 cudaError_t launch_quant_tiles(const void* W, void* Wq, int G, int rows, int cols, cudaStream_t s);
-cudaError_t launch_quant_rows(const void* X, void* Xq, const int32_t* offsets, int G,
-                              int64_t rows_max, int cols, cudaStream_t s);
-cudaError_t launch_quant_cols(const void* X, void* Xq, const int32_t* offsets, int G,
-                              int64_t rows_max, int cols, cudaStream_t s);
+cudaError_t launch_quant_rows(const void* X, void* Xq, const int32_t* offsets,
+                              const int32_t* counts, int G, int64_t rows_max, int cols,
+                              cudaStream_t s);
+cudaError_t launch_quant_cols(const void* X, void* Xq, const int32_t* offsets,
+                              const int32_t* counts, int G, int64_t rows_max, int cols,
+                              cudaStream_t s);
 
 // Where the FP8 mode keeps its quantised tensors inside `scratch`.
 struct Fp8Scratch {

@@ -207,9 +207,9 @@ moe_status moe_grouped_ffn_fwd(const moe_config* cfg, const void* x_perm, const 
     const int64_t R = rows_max(*cfg);
     MOE_CUDA(launch_quant_tiles(W13, q.W13q, G, 2 * cfg->F, cfg->H, s));
     MOE_CUDA(launch_quant_tiles(W2, q.W2q, G, cfg->H, cfg->F, s));
-    MOE_CUDA(launch_quant_rows(x_perm, q.aH, offsets, G, R, cfg->H, s));
+    MOE_CUDA(launch_quant_rows(x_perm, q.aH, offsets, counts, G, R, cfg->H, s));
     MOE_CUDA(launch_ffn_fc1(*cfg, q.aH, counts, offsets, q.W13q, GU, h, st, s));
-    MOE_CUDA(launch_quant_rows(h, q.bF, offsets, G, R, cfg->F, s));
+    MOE_CUDA(launch_quant_rows(h, q.bF, offsets, counts, G, R, cfg->F, s));
     MOE_CUDA(launch_ffn_fc2(*cfg, q.bF, counts, offsets, q.W2q, y_perm, st, s));
     return MOE_OK;
   }
@@ -256,16 +256,16 @@ moe_status moe_grouped_ffn_bwd(const moe_config* cfg, const void* dO_perm, const
     const int G = cfg->E + cfg->n_shared;
     const int64_t R = rows_max(*cfg);
     const int H = cfg->H, F = cfg->F;
-    MOE_CUDA(launch_quant_rows(dO_perm, q.cH, offsets, G, R, H, s));
+    MOE_CUDA(launch_quant_rows(dO_perm, q.cH, offsets, counts, G, R, H, s));
     MOE_CUDA(launch_ffn_fc2_dgrad(*cfg, q.cH, counts, offsets, q.W2q, GU, dGU, st, s));
-    MOE_CUDA(launch_quant_cols(dO_perm, q.cH, offsets, G, R, H, s));
-    MOE_CUDA(launch_quant_cols(h, q.bF, offsets, G, R, F, s));
+    MOE_CUDA(launch_quant_cols(dO_perm, q.cH, offsets, counts, G, R, H, s));
+    MOE_CUDA(launch_quant_cols(h, q.bF, offsets, counts, G, R, F, s));
     MOE_CUDA(launch_ffn_wgrad_fc2(*cfg, q.cH, q.bF, counts, offsets, dW2, st, s));
-    MOE_CUDA(launch_quant_rows(dGU, q.d2F, offsets, G, R, 2 * F, s));
+    MOE_CUDA(launch_quant_rows(dGU, q.d2F, offsets, counts, G, R, 2 * F, s));
     MOE_CUDA(launch_ffn_fc1_dgrad(*cfg, q.d2F, counts, offsets, q.W13q, token_of, dlogits, W_r,
                                   dX_perm, st, s));
-    MOE_CUDA(launch_quant_cols(dGU, q.d2F, offsets, G, R, 2 * F, s));
-    MOE_CUDA(launch_quant_cols(x_perm, q.aH, offsets, G, R, H, s));
+    MOE_CUDA(launch_quant_cols(dGU, q.d2F, offsets, counts, G, R, 2 * F, s));
+    MOE_CUDA(launch_quant_cols(x_perm, q.aH, offsets, counts, G, R, H, s));
     MOE_CUDA(launch_ffn_wgrad_fc1(*cfg, q.d2F, q.aH, counts, offsets, dW13, st, s));
     return MOE_OK;
   }

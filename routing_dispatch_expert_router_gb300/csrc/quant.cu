@@ -100,56 +100,79 @@ quant_tiles_kernel(const __nv_bfloat16* __restrict__ W, __nv_bfloat16* __restric
   }
 }
 
-// 1 x 128 slices of rows [0, offsets[G]): 16 lanes per slice.
+// Whether 128-row block rb of the permuted buffer holds any row a GEMM reads:
+// group g's segment starts at offsets[g], and the GEMMs read its first
+// ceil(counts[g] / 128) blocks (capacity segments and dropless padding past
+// them are never read, so they are not quantised).
+__device__ __forceinline__ bool live_block(const int32_t* __restrict__ offsets,
+                                           const int32_t* __restrict__ counts, int G, long long rb) {
+  const long long r0 = rb * 128;
+  int lo = 0, hi = G - 1;                                 // last g with offsets[g] <= r0
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (offsets[mid] <= r0) lo = mid;
+    else hi = mid - 1;
+  }
+  return r0 - offsets[lo] < (long long)((counts[lo] + 127) / 128) * 128;
+}
+
+// 1 x 128 slices along the rows of the live 128-row blocks of [0, offsets[G]):
+// one block of 256 threads per 128-row block, 16 lanes per slice.
 __global__ void __launch_bounds__(256)
 quant_rows_kernel(const __nv_bfloat16* __restrict__ X, __nv_bfloat16* __restrict__ Xq,
-                  const int32_t* __restrict__ offsets, int G, int cols) {
-  const long long rows = offsets[G];
-  const int nvec = cols >> 3;
-  const long long n = rows * nvec;                        // nvec is a multiple of 16
-  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n;
-       i += (long long)gridDim.x * blockDim.x) {
-    float f[8];
-    unpack8(ldg_nc_v4(X + i * 8), f);
-    float m = amax8(f);
-    // the 16 lanes of this half-warp hold one 128-element slice; n is a
-    // multiple of 16, so a half-warp is either wholly in range or wholly out
-    const unsigned half = (threadIdx.x & 16) ? 0xffff0000u : 0x0000ffffu;
+                  const int32_t* __restrict__ offsets, const int32_t* __restrict__ counts, int G,
+                  int cols) {
+  const long long rblocks = offsets[G] / 128;
+  const int nvec = cols >> 3;                             // a multiple of 16
+  const int per_block = 128 * nvec;
+  for (long long rb = blockIdx.x; rb < rblocks; rb += gridDim.x) {
+    if (!live_block(offsets, counts, G, rb)) continue;
+    const __nv_bfloat16* src = X + (size_t)rb * 128 * cols;
+    __nv_bfloat16* dst = Xq + (size_t)rb * 128 * cols;
+    for (int v = threadIdx.x; v < per_block; v += 256) {
+      float f[8];
+      unpack8(ldg_nc_v4(src + (size_t)v * 8), f);
+      float m = amax8(f);
+      // the 16 lanes of this half-warp hold one 128-element slice (per_block
+      // and 256 are multiples of 16: a half-warp is wholly in range or out)
+      const unsigned half = (threadIdx.x & 16) ? 0xffff0000u : 0x0000ffffu;
 #pragma unroll
-    for (int o = 8; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(half, m, o));
-    stg_v4(Xq + i * 8, quant8(f, e4m3_scale(m)));
+      for (int o = 8; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(half, m, o));
+      stg_v4(dst + (size_t)v * 8, quant8(f, e4m3_scale(m)));
+    }
   }
 }
 
-// 128 x 1 slices: every 128-row block of [0, offsets[G]) (group segments are
-// multiples of 128 rows, so blocks never straddle two experts), thread owns
-// two adjacent columns of one block.
+// 128 x 1 slices: every live 128-row block of [0, offsets[G]) (group segments
+// are multiples of 128 rows, so blocks never straddle two experts); one block
+// of 256 threads per 128-row block, thread owns two adjacent columns.
 __global__ void __launch_bounds__(256)
 quant_cols_kernel(const __nv_bfloat16* __restrict__ X, __nv_bfloat16* __restrict__ Xq,
-                  const int32_t* __restrict__ offsets, int G, int cols) {
+                  const int32_t* __restrict__ offsets, const int32_t* __restrict__ counts, int G,
+                  int cols) {
   const long long rblocks = offsets[G] / 128;
   const int cpairs = cols >> 1;
-  const long long n = rblocks * cpairs;
-  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n;
-       i += (long long)gridDim.x * blockDim.x) {
-    const long long rb = i / cpairs;
-    const int c = (int)(i % cpairs) * 2;
-    const __nv_bfloat16* src = X + (size_t)rb * 128 * cols + c;
-    float m0 = 0.f, m1 = 0.f;
+  for (long long rb = blockIdx.x; rb < rblocks; rb += gridDim.x) {
+    if (!live_block(offsets, counts, G, rb)) continue;
+    for (int cp = threadIdx.x; cp < cpairs; cp += 256) {
+      const int c = cp * 2;
+      const __nv_bfloat16* src = X + (size_t)rb * 128 * cols + c;
+      float m0 = 0.f, m1 = 0.f;
 #pragma unroll 8
-    for (int r = 0; r < 128; ++r) {
-      const uint32_t v = *reinterpret_cast<const uint32_t*>(src + (size_t)r * cols);
-      m0 = fmaxf(m0, fabsf(bf16_lo(v)));
-      m1 = fmaxf(m1, fabsf(bf16_hi(v)));
-    }
-    const float s0 = e4m3_scale(m0), s1 = e4m3_scale(m1);
-    const float i0 = 1.f / s0, i1 = 1.f / s1;
-    __nv_bfloat16* dst = Xq + (size_t)rb * 128 * cols + c;
+      for (int r = 0; r < 128; ++r) {
+        const uint32_t v = *reinterpret_cast<const uint32_t*>(src + (size_t)r * cols);
+        m0 = fmaxf(m0, fabsf(bf16_lo(v)));
+        m1 = fmaxf(m1, fabsf(bf16_hi(v)));
+      }
+      const float s0 = e4m3_scale(m0), s1 = e4m3_scale(m1);
+      const float i0 = 1.f / s0, i1 = 1.f / s1;
+      __nv_bfloat16* dst = Xq + (size_t)rb * 128 * cols + c;
 #pragma unroll 8
-    for (int r = 0; r < 128; ++r) {
-      const uint32_t v = *reinterpret_cast<const uint32_t*>(src + (size_t)r * cols);
-      *reinterpret_cast<uint32_t*>(dst + (size_t)r * cols) =
-          pack_bf16x2(q1(bf16_lo(v), i0, s0), q1(bf16_hi(v), i1, s1));
+      for (int r = 0; r < 128; ++r) {
+        const uint32_t v = *reinterpret_cast<const uint32_t*>(src + (size_t)r * cols);
+        *reinterpret_cast<uint32_t*>(dst + (size_t)r * cols) =
+            pack_bf16x2(q1(bf16_lo(v), i0, s0), q1(bf16_hi(v), i1, s1));
+      }
     }
   }
 }
@@ -168,17 +191,21 @@ cudaError_t launch_quant_tiles(const void* W, void* Wq, int G, int rows, int col
   return cudaGetLastError();
 }
 
-cudaError_t launch_quant_rows(const void* X, void* Xq, const int32_t* offsets, int G,
-                              int64_t rows_max, int cols, cudaStream_t s) {
-  quant_rows_kernel<<<grid_cap(rows_max * (cols / 8), 256), 256, 0, s>>>(
-      static_cast<const __nv_bfloat16*>(X), static_cast<__nv_bfloat16*>(Xq), offsets, G, cols);
+cudaError_t launch_quant_rows(const void* X, void* Xq, const int32_t* offsets,
+                              const int32_t* counts, int G, int64_t rows_max, int cols,
+                              cudaStream_t s) {
+  quant_rows_kernel<<<grid_cap(rows_max / 128, 1), 256, 0, s>>>(
+      static_cast<const __nv_bfloat16*>(X), static_cast<__nv_bfloat16*>(Xq), offsets, counts, G,
+      cols);
   return cudaGetLastError();
 }
 
-cudaError_t launch_quant_cols(const void* X, void* Xq, const int32_t* offsets, int G,
-                              int64_t rows_max, int cols, cudaStream_t s) {
-  quant_cols_kernel<<<grid_cap(rows_max / 128 * (cols / 2), 256), 256, 0, s>>>(
-      static_cast<const __nv_bfloat16*>(X), static_cast<__nv_bfloat16*>(Xq), offsets, G, cols);
+cudaError_t launch_quant_cols(const void* X, void* Xq, const int32_t* offsets,
+                              const int32_t* counts, int G, int64_t rows_max, int cols,
+                              cudaStream_t s) {
+  quant_cols_kernel<<<grid_cap(rows_max / 128, 1), 256, 0, s>>>(
+      static_cast<const __nv_bfloat16*>(X), static_cast<__nv_bfloat16*>(Xq), offsets, counts, G,
+      cols);
   return cudaGetLastError();
 }
 
