@@ -241,15 +241,17 @@ def run_ours(args, rank, world, local):
         B.moe_permute_bwd(cfg, b["dX_perm"], f["row_of"], f["offsets"], f["idx"], b["dlogits"],
                           inp["W_r"], dx)
         rec(8)
-        B.moe_router_wgrad(cfg, x, f["sel_offsets"], f["sel_tokens"], b["dlogits"], dW_r)
+        B.moe_router_wgrad(cfg, x, f["sel_offsets"], f["sel_tokens"], b["dlogits"], dW_r, sc)
         rec(9)
 
     # kernels launched by one step: route (logits [+ W_r split on the tensor-core
     # path] + selection), dispatch (hist, rank, scatter), FC1 and FC2, combine,
-    # combine bwd, route bwd, the four backward GEMMs, dispatch bwd, router wgrad;
-    # the FP8 mode adds 4 quantisation launches forward and 6 backward
+    # combine bwd, route bwd, the four backward GEMMs, dispatch bwd, router wgrad
+    # (on the tensor-core path: dlogits split, GEMM, chunk sum); the FP8 mode adds
+    # 4 quantisation launches forward and 6 backward
     tc_router = shape.E >= 128 and shape.E % 128 == 0
-    launches_per_step = (3 if tc_router else 2) + 3 + 2 + 1 + 1 + 1 + 4 + 1 + 1
+    launches_per_step = ((3 if tc_router else 2) + 3 + 2 + 1 + 1 + 1 + 4 + 1
+                         + (3 if tc_router else 1))
     if shape.dtype == W.DT_FP8:
         launches_per_step += 4 + 6
     for _ in range(max(args.warmup, 3)):

@@ -246,10 +246,19 @@ MOE_API moe_status moe_permute_bwd(const moe_config* cfg, const void* dX_perm, c
                            const float* W_r, void* dx, void* stream);
 
 /* Router weight gradient: dW_r[e] = sum over tokens t that selected e of
- * dlogits[t,e] x[t] (fp32, fixed summation order). */
+ * dlogits[t,e] x[t] (fp32 [E,H]; dlogits is zero outside the selected experts,
+ * as moe_route_bwd writes it, so this is dlogits^T x). For E a multiple of 128
+ * on the tensor cores: dlogits split exactly into three bf16 parts, each chunk
+ * of at most max(1024, ~T/256) tokens summed by the tensor cores (fp32
+ * accumulation), the chunks added in order in fp32; otherwise one block per
+ * (expert, column slab) summing the expert's selecting tokens (sel_offsets /
+ * sel_tokens from moe_permute) in token order. Either way the summation order
+ * is fixed: the result is bitwise reproducible. scratch: as moe_query_sizes
+ * sizes it (the tensor-core path keeps the split dlogits and the chunk sums
+ * there). */
 MOE_API moe_status moe_router_wgrad(const moe_config* cfg, const void* x, const int32_t* sel_offsets,
                             const int32_t* sel_tokens, const float* dlogits, float* dW_r,
-                            void* stream);
+                            void* scratch, void* stream);
 
 /* The whole layer forward: route, permute, grouped FFN, unpermute. */
 MOE_API moe_status moe_layer_fwd(const moe_config* cfg, const moe_params* params, const void* x,

@@ -199,8 +199,8 @@ def moe_permute_bwd(cfg, dX_perm, row_of, offsets, idx, dlogits, W_r, dx, stream
           _stream(stream))
 
 
-def moe_router_wgrad(cfg, x, sel_offsets, sel_tokens, dlogits, dW_r, stream=None):
-    _call("moe_router_wgrad", _cfg(cfg), x, sel_offsets, sel_tokens, dlogits, dW_r,
+def moe_router_wgrad(cfg, x, sel_offsets, sel_tokens, dlogits, dW_r, scratch, stream=None):
+    _call("moe_router_wgrad", _cfg(cfg), x, sel_offsets, sel_tokens, dlogits, dW_r, scratch,
           _stream(stream))
 
 

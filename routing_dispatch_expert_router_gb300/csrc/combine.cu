@@ -434,9 +434,103 @@ cudaError_t launch_permute_bwd(const moe_config& c, const void* dX_perm, const i
                                     s);
 }
 
+// dlogits [T, E] -> its three bf16 parts stacked along rows, D3 [3 * Tp, E]
+// (part q at rows q * Tp; rows T..Tp-1 of every part zero). 8 columns per
+// thread (E % 128 == 0).
+__global__ void __launch_bounds__(256)
+split_dlogits_kernel(const float* __restrict__ dl, __nv_bfloat16* __restrict__ D3, int T,
+                     long long Tp, int E) {
+  const int per_row = E >> 3;
+  const long long n = Tp * per_row;
+  for (long long v = (long long)blockIdx.x * blockDim.x + threadIdx.x; v < n;
+       v += (long long)gridDim.x * blockDim.x) {
+    const long long t = v / per_row;
+    const int e = (int)(v - t * per_row) << 3;
+    float4 a = make_float4(0.f, 0.f, 0.f, 0.f), b = a;
+    if (t < T) {
+      const float4* src = reinterpret_cast<const float4*>(dl + t * E + e);
+      a = __ldg(src);
+      b = __ldg(src + 1);
+    }
+    uint4 hi, mid, lo;
+    split3_pair(a.x, a.y, hi.x, mid.x, lo.x);
+    split3_pair(a.z, a.w, hi.y, mid.y, lo.y);
+    split3_pair(b.x, b.y, hi.z, mid.z, lo.z);
+    split3_pair(b.z, b.w, hi.w, mid.w, lo.w);
+    __nv_bfloat16* dst = D3 + t * E + e;
+    *reinterpret_cast<uint4*>(dst) = hi;
+    *reinterpret_cast<uint4*>(dst + Tp * E) = mid;
+    *reinterpret_cast<uint4*>(dst + 2 * Tp * E) = lo;
+  }
+}
+
+// dW_r[e, h] = sum over chunks g in order of P[g * H + h, e] (fp32), through a
+// 32 x 32 shared-memory transpose: both the reads (16 bytes along e) and the
+// writes (along h) are coalesced. Thread (row r, quad j) sums P[g][h0 + r][e0 +
+// 4j .. 4j+3] over g with four chunks' loads in flight.
+__global__ void __launch_bounds__(256)
+sum_chunks_transpose_kernel(const float* __restrict__ P, float* __restrict__ dW_r, int NG, int H,
+                            int E) {
+  __shared__ float tile[32][33];
+  const int j = threadIdx.x & 7, r = threadIdx.x >> 3;
+  const int h0 = blockIdx.x * 32, e0 = blockIdx.y * 32;
+  const float* src = P + (size_t)(h0 + r) * E + e0 + 4 * j;
+  const size_t gstride = (size_t)H * E;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  int g = 0;
+  for (; g + 4 <= NG; g += 4) {
+    float4 v[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) v[u] = __ldg(reinterpret_cast<const float4*>(src + (g + u) * gstride));
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      acc.x += v[u].x;
+      acc.y += v[u].y;
+      acc.z += v[u].z;
+      acc.w += v[u].w;
+    }
+  }
+  for (; g < NG; ++g) {
+    const float4 v = __ldg(reinterpret_cast<const float4*>(src + g * gstride));
+    acc.x += v.x;
+    acc.y += v.y;
+    acc.z += v.z;
+    acc.w += v.w;
+  }
+  tile[r][4 * j] = acc.x;
+  tile[r][4 * j + 1] = acc.y;
+  tile[r][4 * j + 2] = acc.z;
+  tile[r][4 * j + 3] = acc.w;
+  __syncthreads();
+  const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) dW_r[(size_t)(e0 + ty + 8 * i) * H + h0 + tx] = tile[tx][ty + 8 * i];
+}
+
 cudaError_t launch_router_wgrad(const moe_config& c, const void* x, const int32_t* sel_offsets,
                                 const int32_t* sel_tokens, const float* dlogits, float* dW_r,
-                                cudaStream_t s) {
+                                uint8_t* scratch, cudaStream_t s) {
+  if (router_on_tensor_cores(c)) {
+    // tensor cores: dW_r^T chunk sums x^T . dlogits over chunks of tokens, then
+    // the chunks added in order (every x row read once)
+    if (c.T == 0) return cudaMemsetAsync(dW_r, 0, (size_t)c.E * c.H * 4, s);
+    uint8_t* base = scratch + router_split_offset(c);
+    const long long Tp = ((long long)c.T + 63) / 64 * 64;
+    auto D3 = reinterpret_cast<__nv_bfloat16*>(base);
+    auto P = reinterpret_cast<float*>(base + router_wgrad_split_bytes(c));
+    const int chunk = router_wgrad_chunk(c);
+    const int NG = (c.T + chunk - 1) / chunk;
+    long long blocks = (Tp * (c.E / 8) + 255) / 256;
+    if (blocks > (long long)num_sms() * 16) blocks = (long long)num_sms() * 16;
+    split_dlogits_kernel<<<(int)blocks, 256, 0, s>>>(dlogits, D3, c.T, Tp, c.E);
+    cudaError_t err = cudaGetLastError();
+    if (err != cudaSuccess) return err;
+    err = launch_router_wgrad_tc(c, x, D3, Tp, P, chunk,
+                                 reinterpret_cast<int32_t*>(scratch + kScratchStatus), s);
+    if (err != cudaSuccess) return err;
+    sum_chunks_transpose_kernel<<<dim3(c.H / 32, c.E / 32), 256, 0, s>>>(P, dW_r, NG, c.H, c.E);
+    return cudaGetLastError();
+  }
   auto xb = static_cast<const __nv_bfloat16*>(x);
   // few experts: 128-column slabs so that every SM gets blocks
   if ((long long)c.E * ((c.H + 255) / 256) < 2LL * num_sms()) {

@@ -42,6 +42,18 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return r;
 }
 
+// Two fp32 values -> their three packed bf16 parts (pairs: low half = first):
+// hi = bf16(w), mid = bf16(w - hi), lo = w - hi - mid. Each part keeps 8
+// significant bits of the 24, so both subtractions are exact, lo is exactly a
+// bf16, and hi + mid + lo == w.
+__device__ __forceinline__ void split3_pair(float w0, float w1, uint32_t& hi, uint32_t& mid,
+                                            uint32_t& lo) {
+  hi = pack_bf16x2(w0, w1);
+  const float r0 = w0 - bf16_lo(hi), r1 = w1 - bf16_hi(hi);
+  mid = pack_bf16x2(r0, r1);
+  lo = pack_bf16x2(r0 - bf16_lo(mid), r1 - bf16_hi(mid));
+}
+
 __device__ __forceinline__ uint4 pack8(const float (&f)[8]) {
   uint4 v;
   v.x = pack_bf16x2(f[0], f[1]);

@@ -41,7 +41,6 @@ constexpr int kThreads = 192;
 constexpr int kCtrlBytes = 5120;
 constexpr int kBoxBytes = 32 * 32 * 2;           // one 32 x 32 bf16 output box
 constexpr int kStageBytes = 3 * kBoxBytes;       // output staging per epilogue warp
-constexpr int kStageAll = 4 * kStageBytes;
 constexpr long long kWaitBudget = 4000000000LL;   // clock64 cycles (~2 s)
 
 enum Epi : int { kEpiSwigluFwd = 0, kEpiStore = 1, kEpiSwigluBwd = 2, kEpiWgrad = 3,
@@ -65,14 +64,19 @@ struct Params {
   const __nv_bfloat16* aux;   // SwiGLU-bwd: GU
   long long ldaux;
   int32_t* status;
-  int dense_rows;             // > 0: one group of this many rows at row 0 (no counts/offsets)
+  int dense_rows;             // > 0: one group of this many rows at row 0 (no counts/offsets),
+                              // or, with chunk_rows > 0, that many rows cut into groups of
+                              // chunk_rows consecutive rows (the last one shorter)
+  int chunk_rows;
+  long long part_rows;        // B parts (b_parts > 1) of an MN-major B: part q's rows start
+                              // at q * part_rows
   // FC1 data gradient with the router term (kEpiDgradRouter): row r of a
   // routed group g < router_E gains dlogits[token_of[r], g] * W_r[g, :]
   const int32_t* token_of;
   const float* dlogits;
   const float* W_r;
   int router_E;
-  // Pair-tile order: 1 = n-tiles vary fastest, else m-pairs. Weight gradients
+  // Tile order: 1 = n-tiles vary fastest, else m-tiles (m-pairs). Weight gradients
   // whose output is taller than wide take n-fastest: the clusters running at
   // once then share the A slice (the group's rows x 256 output rows) and stream
   // B, which is the smaller operand and stays in L2 (Mixtral-sized dW13: the
@@ -92,7 +96,7 @@ struct Layout {
   static constexpr int B_BYTES = BN * BK * 2;
   static constexpr int STAGE = A_BYTES + BPARTS * B_BYTES;
   static constexpr int TILES = STAGES * STAGE;
-  static constexpr int SMEM = TILES + kCtrlBytes + kStageAll + 1024;
+  static constexpr int SMEM = TILES + kCtrlBytes + 4 * kStageBytes + 1024;
   static constexpr int TMEM_COLS = 2 * BN;
 };
 
@@ -111,13 +115,19 @@ __device__ __forceinline__ int find_group(const int* prefix, int G, int tile) {
 }
 
 __device__ __forceinline__ Tile decode(int tile, const int* prefix, const int* mtiles,
-                                       const int* cnt, int G, int kgrouped, int K) {
+                                       const int* cnt, int G, int kgrouped, int K, int NT,
+                                       int n_fast) {
   Tile t;
   t.g = find_group(prefix, G, tile);
   const int local = tile - prefix[t.g];
   const int mt = mtiles[t.g];
-  t.mt = local % mt;
-  t.nt = local / mt;
+  if (n_fast) {
+    t.nt = local % NT;
+    t.mt = local / NT;
+  } else {
+    t.mt = local % mt;
+    t.nt = local / mt;
+  }
   t.nk = kgrouped ? (cnt[t.g] + BK - 1) / BK : K / BK;
   return t;
 }
@@ -202,7 +212,7 @@ __device__ __forceinline__ void epilogue_tile(const Params& p, const CUtensorMap
                                               int mt, int nt, int nk, int q, int lane,
                                               const int* s_off, uint8_t* stage,
                                               uint32_t stage_u32) {
-  const int row0 = (EPI == kEpiWgrad) ? g * p.Mw + mt * BM + q * 32 : s_off[g] + mt * BM + q * 32;
+  const int row0 = p.kgrouped ? g * p.Mw + mt * BM + q * 32 : s_off[g] + mt * BM + q * 32;
   const int ncols = (EPI == kEpiSwigluFwd) ? BN / 2 : BN;
   const int f0 = (EPI == kEpiSwigluFwd) ? nt * (BN / 2) : nt * BN;
   // router term of this warp's row (lane) for the FC1 data gradient
@@ -385,9 +395,10 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
   const int G = p.G;
   const int NT = (EPI == kEpiSwigluFwd) ? p.F / (BN / 2) : p.N / BN;
   for (int g = tid; g < G; g += kThreads) {
-    const int c = p.dense_rows > 0 ? p.dense_rows : p.counts[g];
+    const int c = p.chunk_rows > 0 ? min(p.chunk_rows, p.dense_rows - g * p.chunk_rows)
+                  : p.dense_rows > 0 ? p.dense_rows : p.counts[g];
     s_cnt[g] = c;
-    s_off[g] = p.dense_rows > 0 ? 0 : p.offsets[g];
+    s_off[g] = p.chunk_rows > 0 ? g * p.chunk_rows : p.dense_rows > 0 ? 0 : p.offsets[g];
     const int mt = p.kgrouped ? p.Mw / BM : (c + BM - 1) / BM;
     mtiles[g] = mt;
     prefix[g] = mt * NT;
@@ -431,7 +442,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
       uint32_t issued_mask = 0, issued_phase = 0;
       bool ok = true;
       for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
-        const Tile t = decode(tile, prefix, mtiles, s_cnt, G, p.kgrouped, p.K);
+        const Tile t = decode(tile, prefix, mtiles, s_cnt, G, p.kgrouped, p.K, NT, p.n_fast);
         for (int kb = 0; kb < t.nk; ++kb) {
           if (!ptx::mbar_wait(bar_empty + 8 * stage, phase ^ 1u, kWaitBudget, abort_flag)) {
             ok = false;
@@ -461,8 +472,11 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
           } else {
             const int kr = p.kgrouped ? s_off[t.g] + k0 : t.g * p.b_rows + k0;
 #pragma unroll
-            for (int j = 0; j < BN / 64; ++j)
-              ptx::tma_load_2d(sB + j * 8192, &tmB, fb, t.nt * BN + 64 * j, kr);
+            for (int q = 0; q < BPARTS; ++q)
+#pragma unroll
+              for (int j = 0; j < BN / 64; ++j)
+                ptx::tma_load_2d(sB + q * L::B_BYTES + j * 8192, &tmB, fb, t.nt * BN + 64 * j,
+                                 (int)(q * p.part_rows) + kr);
           }
           issued_mask |= 1u << stage;
           issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
@@ -488,7 +502,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
       uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
       bool ok = true, issued = false;
       for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
-        const Tile t = decode(tile, prefix, mtiles, s_cnt, G, p.kgrouped, p.K);
+        const Tile t = decode(tile, prefix, mtiles, s_cnt, G, p.kgrouped, p.K, NT, p.n_fast);
         if (!ptx::mbar_wait(bar_tempty + 8 * acc, acc_phase ^ 1u, kWaitBudget, abort_flag)) {
           ok = false;
           break;
@@ -546,7 +560,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
     const uint32_t stage_u32 = ctrl_u + kCtrlBytes + (warp - 2) * kStageBytes;
     uint32_t acc = 0, acc_phase = 0;
     for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
-      const Tile t = decode(tile, prefix, mtiles, s_cnt, G, p.kgrouped, p.K);
+      const Tile t = decode(tile, prefix, mtiles, s_cnt, G, p.kgrouped, p.K, NT, p.n_fast);
       bool ok = ptx::mbar_wait(bar_tfull + 8 * acc, acc_phase, kWaitBudget, abort_flag);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) {
@@ -664,9 +678,10 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA,
   const int G = p.G;
   const int NT = (EPI == kEpiSwigluFwd) ? p.F / (BN / 2) : p.N / BN;
   for (int g = tid; g < G; g += kThreads) {
-    const int c = p.dense_rows > 0 ? p.dense_rows : p.counts[g];
+    const int c = p.chunk_rows > 0 ? min(p.chunk_rows, p.dense_rows - g * p.chunk_rows)
+                  : p.dense_rows > 0 ? p.dense_rows : p.counts[g];
     s_cnt[g] = c;
-    s_off[g] = p.dense_rows > 0 ? 0 : p.offsets[g];
+    s_off[g] = p.chunk_rows > 0 ? g * p.chunk_rows : p.dense_rows > 0 ? 0 : p.offsets[g];
     const int mt = p.kgrouped ? p.Mw / BM : (c + BM - 1) / BM;
     mtiles[g] = mt;
     prefix[g] = ((mt + 1) >> 1) * NT;              // pair tiles of the group
@@ -1047,6 +1062,7 @@ template <int EPI, int BN, int A_MN, int B_MN, int STAGES>
 static cudaError_t run(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& c,
                        const CUtensorMap& c2, const Params& p, cudaStream_t s) {
   using L = Layout<BN, STAGES, b_parts<EPI>()>;
+  static_assert(L::SMEM <= 232448, "shared memory per block");
   auto kern = grouped_gemm_kernel<EPI, BN, A_MN, B_MN, STAGES>;
   static bool attr_set = false;
   if (!attr_set) {
@@ -1280,6 +1296,35 @@ cudaError_t launch_router_logits_tc(const moe_config& c, const void* x, const vo
   p.K = c.H;
   p.status = status;
   return run<kEpiStoreF32, 128, 0, 0, 3>(a, b, oc, oc, p, s);
+}
+
+// Router weight gradient on the tensor cores (E % 128 == 0), as K-grouped
+// GEMMs over chunks of `chunk` tokens: P[c] = x[chunk c]^T . dlogits[chunk c]
+// (H x E, fp32, P stacked [NG * H, E]). dlogits is split exactly into three bf16
+// parts stacked along the rows of D3 [3 * Tp, E] (part q at rows q * Tp, rows
+// T..Tp-1 zero); each pipeline stage carries one x^T k-block (MN-major, straight
+// from x [T, H]) and the three part blocks. A chunk's products accumulate on the
+// tensor cores (at most `chunk` terms); the chunks are added in order in fp32 by
+// the caller.
+cudaError_t launch_router_wgrad_tc(const moe_config& c, const void* x, const void* D3,
+                                   long long Tp, float* P, int chunk, int32_t* status,
+                                   cudaStream_t s) {
+  const int NG = (c.T + chunk - 1) / chunk;
+  if (NG > kMaxGroups) return cudaErrorInvalidValue;
+  CUtensorMap a, b, oc;
+  if (!make_map(&a, x, c.H, c.T, 64) || !make_map(&b, D3, c.E, 3ULL * Tp, 64) ||
+      !make_out_map_f32(&oc, P, c.E, (uint64_t)NG * c.H))
+    return cudaErrorInvalidValue;
+  Params p{};
+  p.kgrouped = 1;
+  p.G = NG;
+  p.dense_rows = c.T;
+  p.chunk_rows = chunk;
+  p.part_rows = Tp;
+  p.Mw = c.H;
+  p.N = c.E;
+  p.status = status;
+  return run<kEpiStoreF32, 128, 1, 1, 3>(a, b, oc, oc, p, s);
 }
 
 }  // namespace moe

@@ -39,7 +39,7 @@ cudaError_t launch_permute_bwd(const moe_config& c, const void* dX_perm, const i
 
 cudaError_t launch_router_wgrad(const moe_config& c, const void* x, const int32_t* sel_offsets,
                                 const int32_t* sel_tokens, const float* dlogits, float* dW_r,
-                                cudaStream_t s);
+                                uint8_t* scratch, cudaStream_t s);
 
 // FP8 block quantisation (E4M3 values with power-of-two scales, stored as bf16).
 cudaError_t launch_quant_tiles(const void* W, void* Wq, int G, int rows, int cols, cudaStream_t s);
@@ -64,8 +64,16 @@ Fp8Scratch fp8_scratch(const moe_config& c, void* scratch);
 // Router logits for E % 128 == 0 on the tensor cores (W3 = W_r split in three bf16 parts).
 cudaError_t launch_router_logits_tc(const moe_config& c, const void* x, const void* W3,
                                     float* logits, int32_t* status, cudaStream_t s);
+cudaError_t launch_router_wgrad_tc(const moe_config& c, const void* x, const void* D3,
+                                   long long Tp, float* P, int chunk, int32_t* status,
+                                   cudaStream_t s);
 bool router_on_tensor_cores(const moe_config& c);
-int64_t router_split_bytes(const moe_config& c);
+// tensor-core router weight gradient: tokens per chunk (<= 271 chunks), and
+// the byte offset of the chunk partial sums after the split dlogits in the
+// router region of scratch
+int router_wgrad_chunk(const moe_config& c);
+int64_t router_wgrad_split_bytes(const moe_config& c);
+int64_t router_split_bytes(const moe_config& c);   // the router region of scratch
 int64_t router_split_offset(const moe_config& c);   // byte offset of the split in scratch
 int64_t permute_scratch_bytes(const moe_config& c); // scratch the dispatch needs
 

@@ -299,11 +299,12 @@ moe_status moe_permute_bwd(const moe_config* cfg, const void* dX_perm, const int
 
 moe_status moe_router_wgrad(const moe_config* cfg, const void* x, const int32_t* sel_offsets,
                             const int32_t* sel_tokens, const float* dlogits, float* dW_r,
-                            void* stream) {
+                            void* scratch, void* stream) {
   MOE_TRY(check_config(cfg));
-  MOE_REQUIRE(tok16(cfg, x) && al4(sel_offsets) && tok4(cfg, sel_tokens) && tok4(cfg, dlogits) && al4(dW_r));
+  MOE_REQUIRE(tok16(cfg, x) && al4(sel_offsets) && tok4(cfg, sel_tokens) && tok16(cfg, dlogits));
+  MOE_REQUIRE(al16(dW_r) && al16(scratch));
   MOE_CUDA(launch_router_wgrad(*cfg, x, sel_offsets, sel_tokens, dlogits, dW_r,
-                               (cudaStream_t)stream));
+                               static_cast<uint8_t*>(scratch), (cudaStream_t)stream));
   return MOE_OK;
 }
 
@@ -334,7 +335,8 @@ moe_status moe_layer_bwd(const moe_config* cfg, const moe_params* P, const void*
                               bs->dGU, bs->dX_perm, dW13, dW2, scratch, stream));
   MOE_TRY(moe_permute_bwd(cfg, bs->dX_perm, st->row_of, st->offsets, st->idx, bs->dlogits,
                           P->W_r, dx, stream));
-  MOE_TRY(moe_router_wgrad(cfg, x, st->sel_offsets, st->sel_tokens, bs->dlogits, dW_r, stream));
+  MOE_TRY(moe_router_wgrad(cfg, x, st->sel_offsets, st->sel_tokens, bs->dlogits, dW_r, scratch,
+                           stream));
   return MOE_OK;
 }
 

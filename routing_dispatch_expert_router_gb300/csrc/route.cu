@@ -100,15 +100,6 @@ __device__ __forceinline__ void mma_m16n8k16_bf16(float (&d)[4], uint32_t a0, ui
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-// Two fp32 weights -> their three packed bf16 parts (pairs: low half = first).
-__device__ __forceinline__ void split3_pair(float w0, float w1, uint32_t& hi, uint32_t& mid,
-                                            uint32_t& lo) {
-  hi = pack_bf16x2(w0, w1);
-  const float r0 = w0 - bf16_lo(hi), r1 = w1 - bf16_hi(hi);
-  mid = pack_bf16x2(r0, r1);
-  lo = pack_bf16x2(r0 - bf16_lo(mid), r1 - bf16_hi(mid));
-}
-
 template <int NT>
 __global__ void __launch_bounds__(256)
 route_logits_mma_kernel(const __nv_bfloat16* __restrict__ x, const float* __restrict__ W,
@@ -734,8 +725,24 @@ split3_kernel(const float* __restrict__ W, __nv_bfloat16* __restrict__ W3, int E
 
 bool router_on_tensor_cores(const moe_config& c) { return c.E >= 128 && c.E % 128 == 0; }
 
+int router_wgrad_chunk(const moe_config& c) {
+  const int by_count = ((c.T + 255) / 256 + 63) / 64 * 64;   // at most 256 chunks
+  return by_count > 1024 ? by_count : 1024;
+}
+
+int64_t router_wgrad_split_bytes(const moe_config& c) {
+  const int64_t Tp = ((int64_t)c.T + 63) / 64 * 64;
+  return (3 * Tp * c.E * 2 + 255) / 256 * 256;
+}
+
+// The router region of scratch: the forward's split W_r, or the backward's
+// split dlogits and the chunk partial sums of dW_r^T, whichever is larger.
 int64_t router_split_bytes(const moe_config& c) {
-  return router_on_tensor_cores(c) ? ((int64_t)c.E * 3 * c.H * 2 + 255) / 256 * 256 : 0;
+  if (!router_on_tensor_cores(c)) return 0;
+  const int64_t fwd = ((int64_t)c.E * 3 * c.H * 2 + 255) / 256 * 256;
+  const int64_t chunks = (c.T + router_wgrad_chunk(c) - 1) / router_wgrad_chunk(c);
+  const int64_t bwd = router_wgrad_split_bytes(c) + (chunks * c.H * c.E * 4 + 255) / 256 * 256;
+  return fwd > bwd ? fwd : bwd;
 }
 
 cudaError_t launch_route(const moe_config& c, const void* x, const float* W_r, const float* bias,

@@ -71,7 +71,7 @@ def run(name: str, reps: int, flush: bool, peak: float, fl: torch.Tensor) -> Non
                                                      dO, dw),
         "route_bwd": lambda: B.moe_route_bwd(cfg, logits, idx, w, dw, dl),
         "permute_bwd": lambda: B.moe_permute_bwd(cfg, dX_perm, row_of, offsets, idx, dl, Wr, dx),
-        "router_wgrad": lambda: B.moe_router_wgrad(cfg, x, sel_off, sel_tok, dl, dWr),
+        "router_wgrad": lambda: B.moe_router_wgrad(cfg, x, sel_off, sel_tok, dl, dWr, sc),
     }
     for f in stages.values():
         f()

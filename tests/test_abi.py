@@ -63,7 +63,11 @@ def test_fp8_scratch_holds_the_quantised_operands():
     s = B.moe_query_sizes(DSV3_FP8)
     G, R, H, F = 256, 256 * 640, 7168, 2048
     quantised = G * 2 * F * H * 2 + G * H * F * 2 + (2 * R * H + R * F + R * 2 * F) * 2
-    router_split = 256 * 3 * H * 2                    # W_r as three bf16 parts (E % 128 == 0)
+    # the tensor-core router's region (E % 128 == 0): the larger of W_r as three
+    # bf16 parts (forward) and dlogits as three bf16 parts plus the chunk sums of
+    # dW_r^T over 1024-token chunks (backward)
+    T, E = 16384, 256
+    router_split = max(E * 3 * H * 2, 3 * T * E * 2 + (T // 1024) * H * E * 4)
     assert s.capacity == 640 and s.rows_max == R
     assert quantised + router_split <= s.scratch_bytes <= quantised + router_split + (1 << 20)
     with pytest.raises(B.MoEError) as e:           # shared experts: not in FP8 mode

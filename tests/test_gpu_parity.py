@@ -58,8 +58,9 @@ def test_all_tokens_on_one_expert_and_empty_experts():
     H_.check_steps(shape, inp, g)
 
 
-def test_empty_batch():
-    shape = MoEShape("empty", T=0, H=128, E=4, k=2, F=128)
+@pytest.mark.parametrize("E", [4, 128], ids=["simt_router", "tensor_core_router"])
+def test_empty_batch(E):
+    shape = MoEShape("empty", T=0, H=128, E=E, k=2, F=128)
     inp = make_inputs(shape.with_(T=1), seed=3)
     inp["x"] = inp["x"][:0].contiguous()
     inp["dY"] = inp["dY"][:0].contiguous()
