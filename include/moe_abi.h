@@ -56,7 +56,7 @@ extern "C" {
 typedef enum moe_status {
     MOE_OK = 0,
     MOE_ERR_INVALID_ARG = 1,   /* bad pointer, shape or alignment            */
-    MOE_ERR_UNSUPPORTED = 2,   /* a valid configuration this build lacks      */
+    MOE_ERR_UNSUPPORTED = 2,   /* a valid configuration the library lacks     */
     MOE_ERR_WORKSPACE = 3,     /* scratch too small                           */
     MOE_ERR_CUDA = 4,          /* a CUDA runtime call failed                  */
     MOE_ERR_TIMEOUT = 5,       /* a device-side bounded wait ran out          */

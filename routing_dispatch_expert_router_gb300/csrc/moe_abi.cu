@@ -368,7 +368,7 @@ const char* moe_status_string(moe_status s) {
   switch (s) {
     case MOE_OK: return "ok";
     case MOE_ERR_INVALID_ARG: return "invalid argument (pointer, shape or alignment)";
-    case MOE_ERR_UNSUPPORTED: return "configuration not supported by this build";
+    case MOE_ERR_UNSUPPORTED: return "configuration not supported by the library";
     case MOE_ERR_WORKSPACE: return "scratch buffer too small";
     case MOE_ERR_CUDA: return "a CUDA runtime call failed";
     case MOE_ERR_TIMEOUT: return "a device-side bounded wait ran out";

@@ -117,7 +117,8 @@ __device__ __forceinline__ bool live_block(const int32_t* __restrict__ offsets,
 }
 
 // 1 x 128 slices along the rows of the live 128-row blocks of [0, offsets[G]):
-// one block of 256 threads per 128-row block, 16 lanes per slice.
+// one block of 256 threads per 128-row block, 16 lanes per slice. (Four
+// vectors per thread in flight measured slower than one.)
 __global__ void __launch_bounds__(256)
 quant_rows_kernel(const __nv_bfloat16* __restrict__ X, __nv_bfloat16* __restrict__ Xq,
                   const int32_t* __restrict__ offsets, const int32_t* __restrict__ counts, int G,
@@ -144,36 +145,67 @@ quant_rows_kernel(const __nv_bfloat16* __restrict__ X, __nv_bfloat16* __restrict
 }
 
 // 128 x 1 slices: every live 128-row block of [0, offsets[G]) (group segments
-// are multiples of 128 rows, so blocks never straddle two experts); one block
-// of 256 threads per 128-row block, thread owns two adjacent columns.
+// are multiples of 128 rows, so blocks never straddle two experts). One block
+// of 256 threads per (128-row block, 128-column slab): the 128 x 128 tile is
+// read once into shared memory with 16-byte loads (eight per thread in
+// flight), the column maxima are taken there (two partial maxima of 64 rows
+// per column), and every thread quantises and stores eight 8-column vectors
+// read back from the tile.
 __global__ void __launch_bounds__(256)
 quant_cols_kernel(const __nv_bfloat16* __restrict__ X, __nv_bfloat16* __restrict__ Xq,
                   const int32_t* __restrict__ offsets, const int32_t* __restrict__ counts, int G,
                   int cols) {
+  extern __shared__ uint4 qc_smem[];
+  uint4 (*tile)[16] = reinterpret_cast<uint4 (*)[16]>(qc_smem);   // 128 rows x 128 bf16
+  float* part = reinterpret_cast<float*>(qc_smem + 128 * 16);      // [2][128]
+  float* scale = part + 256;                                       // [128]
   const long long rblocks = offsets[G] / 128;
-  const int cpairs = cols >> 1;
-  for (long long rb = blockIdx.x; rb < rblocks; rb += gridDim.x) {
+  const int slabs = cols >> 7;
+  const int tid = threadIdx.x;
+  for (long long w = blockIdx.x; w < rblocks * slabs; w += gridDim.x) {
+    const long long rb = w / slabs;
+    const int c0 = (int)(w - rb * slabs) * 128;
     if (!live_block(offsets, counts, G, rb)) continue;
-    for (int cp = threadIdx.x; cp < cpairs; cp += 256) {
-      const int c = cp * 2;
-      const __nv_bfloat16* src = X + (size_t)rb * 128 * cols + c;
-      float m0 = 0.f, m1 = 0.f;
-#pragma unroll 8
-      for (int r = 0; r < 128; ++r) {
-        const uint32_t v = *reinterpret_cast<const uint32_t*>(src + (size_t)r * cols);
-        m0 = fmaxf(m0, fabsf(bf16_lo(v)));
-        m1 = fmaxf(m1, fabsf(bf16_hi(v)));
+    const __nv_bfloat16* src = X + (size_t)rb * 128 * cols + c0;
+    {
+      uint4 in[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int v = tid + 256 * i, r = v >> 4, q = v & 15;
+        in[i] = ldg_nc_v4(src + (size_t)r * cols + q * 8);
       }
-      const float s0 = e4m3_scale(m0), s1 = e4m3_scale(m1);
-      const float i0 = 1.f / s0, i1 = 1.f / s1;
-      __nv_bfloat16* dst = Xq + (size_t)rb * 128 * cols + c;
-#pragma unroll 8
-      for (int r = 0; r < 128; ++r) {
-        const uint32_t v = *reinterpret_cast<const uint32_t*>(src + (size_t)r * cols);
-        *reinterpret_cast<uint32_t*>(dst + (size_t)r * cols) =
-            pack_bf16x2(q1(bf16_lo(v), i0, s0), q1(bf16_hi(v), i1, s1));
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int v = tid + 256 * i;
+        tile[v >> 4][v & 15] = in[i];
       }
     }
+    __syncthreads();
+    {
+      const int c = tid & 127, h = tid >> 7;
+      const __nv_bfloat16* col = reinterpret_cast<const __nv_bfloat16*>(&tile[0][0]) + c;
+      float m = 0.f;
+#pragma unroll 8
+      for (int r = h * 64; r < h * 64 + 64; ++r) m = fmaxf(m, fabsf(__bfloat162float(col[r * 128])));
+      part[h * 128 + c] = m;
+    }
+    __syncthreads();
+    if (tid < 128) scale[tid] = e4m3_scale(fmaxf(part[tid], part[128 + tid]));
+    __syncthreads();
+    __nv_bfloat16* dst = Xq + (size_t)rb * 128 * cols + c0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int v = tid + 256 * i, r = v >> 4, q = v & 15;
+      float f[8], o[8];
+      unpack8(tile[r][q], f);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const float sc = scale[q * 8 + j];
+        o[j] = q1(f[j], 1.f / sc, sc);
+      }
+      stg_v4(dst + (size_t)r * cols + q * 8, pack8(o));
+    }
+    __syncthreads();
   }
 }
 
@@ -203,7 +235,8 @@ cudaError_t launch_quant_rows(const void* X, void* Xq, const int32_t* offsets,
 cudaError_t launch_quant_cols(const void* X, void* Xq, const int32_t* offsets,
                               const int32_t* counts, int G, int64_t rows_max, int cols,
                               cudaStream_t s) {
-  quant_cols_kernel<<<grid_cap(rows_max / 128, 1), 256, 0, s>>>(
+  constexpr int smem = 128 * 16 * 16 + 3 * 128 * 4;     // tile + two partial maxima + scales
+  quant_cols_kernel<<<grid_cap(rows_max / 128 * (cols / 128), 1), 256, smem, s>>>(
       static_cast<const __nv_bfloat16*>(X), static_cast<__nv_bfloat16*>(Xq), offsets, counts, G,
       cols);
   return cudaGetLastError();
