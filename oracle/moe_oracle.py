@@ -27,6 +27,9 @@ readings listed below; every one of them is a reading, not a quote:
     two best selection scores (or their maximum), the best topk_groups groups
     kept (ties to the lower group), then top-k inside them; weights
     route_scale * s_j / sum_sel s (bias only steers selection);
+  * Router Replay (the summary's RL support, es "Soporte para RL"): the
+    experts come from a recorded idx [T,k] instead of the top-k, the weights
+    are the router's for those experts, in that order, from the current logits;
   * capacity C = ceil(cf * T * k / E) rounded up to row_align; an expert keeps
     its first C tokens in token order, dropped assignments contribute 0 and
     the surviving weights are not renormalised;
@@ -219,9 +222,7 @@ def route(logits, cfg, bias=None):
     T, E = l.shape
     k = cfg.k
     if cfg.score_fn == SOFTMAX:
-        # selection on the fp32 sum l + b (bit-reproducible), weights from
-        # the same sum in fp64 (identical whenever l is fp32-valued)
-        b64 = 0.0 if bias is None else np.asarray(bias, np.float32).astype(np.float64)[None, :]
+        # selection on the fp32 sum l + b (bit-reproducible)
         l32 = l.astype(np.float32)
         if bias is not None:
             l32 = l32 + np.asarray(bias, dtype=np.float32)[None, :]
@@ -230,19 +231,45 @@ def route(logits, cfg, bias=None):
         if cfg.n_groups > 1:
             masked = _group_mask(sc, cfg)
         idx = _topk_rows(sc, k, masked)
-        sel = np.take_along_axis(l + b64, idx, axis=1)
-        z = np.exp(sel - sel[:, :1])
-        w = z / z.sum(axis=1, keepdims=True)
-        return idx, w
+        return idx, route_weights(l, cfg, bias, idx)
     if cfg.score_fn == SIGMOID:
         s = sigmoid(l)
         sc = s + (0.0 if bias is None else np.asarray(bias, dtype=np.float32).astype(np.float64)[None, :])
         masked = _group_mask(sc, cfg) if cfg.n_groups > 1 else None
         idx = _topk_rows(sc, k, masked)
-        ssel = np.take_along_axis(s, idx, axis=1)
-        w = cfg.route_scale * ssel / ssel.sum(axis=1, keepdims=True)
-        return idx, w
+        return idx, route_weights(l, cfg, bias, idx)
     raise ValueError("score_fn")
+
+
+def route_weights(logits, cfg, bias, idx):
+    """Routing weights of the experts idx [T,k] (in that order) from fp32 logits.
+
+    Softmax router: the softmax over the k chosen experts of l + b (fp64, from
+    the fp32-valued logits and bias). Sigmoid router: route_scale * s_j / sum
+    of s over the chosen, s = sigmoid(l) unbiased (the bias only selects).
+    """
+    l = np.asarray(logits, dtype=np.float64)
+    idx = np.asarray(idx, dtype=np.int64)
+    if cfg.score_fn == SOFTMAX:
+        b64 = 0.0 if bias is None else np.asarray(bias, np.float32).astype(np.float64)[None, :]
+        sel = np.take_along_axis(l + b64, idx, axis=1)
+        z = np.exp(sel - sel[:, :1])
+        return z / z.sum(axis=1, keepdims=True)
+    if cfg.score_fn == SIGMOID:
+        ssel = np.take_along_axis(sigmoid(l), idx, axis=1)
+        return cfg.route_scale * ssel / ssel.sum(axis=1, keepdims=True)
+    raise ValueError("score_fn")
+
+
+def route_replay(logits, cfg, bias, idx):
+    """Router Replay: the layer routes every token to the given experts idx
+    [T,k] (decisions recorded earlier, e.g. by inference) instead of its own
+    top-k; the weights are the router's, from the current logits, for those
+    experts in that order. Follows the RL support of the Megatron Core MoE
+    summary (es summary, Resumen técnico §2, "Soporte para RL": routing
+    decisions of inference replayed in training)."""
+    idx = np.asarray(idx, dtype=np.int64)
+    return idx, route_weights(logits, cfg, bias, idx)
 
 
 def _group_mask(sc, cfg):

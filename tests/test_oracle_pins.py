@@ -154,6 +154,31 @@ def test_softmax_weights_match_torch_softmax_and_sum_to_one():
     np.testing.assert_allclose(w2.sum(1), 1.7, rtol=1e-14)
 
 
+@pytest.mark.parametrize("score_fn", [SOFTMAX, SIGMOID])
+def test_route_replay_weights_match_torch_for_any_given_experts(score_fn):
+    """Router Replay: the weights of recorded experts (here a seeded random
+    choice of k distinct experts per token, in a random order, not the top-k)
+    are torch's softmax over the chosen l + b, or route_scale * sigmoid / sum."""
+    T, E, k = 40, 12, 4
+    cfg = MoEShape("t", T=T, H=8, E=E, k=k, F=8, score_fn=score_fn, route_scale=2.5)
+    rng = np.random.default_rng(5)
+    l = O.round_f32(rng.standard_normal((T, E)) * 2)
+    b = O.round_f32(0.1 * rng.standard_normal(E)).astype(np.float32)
+    idx = np.stack([rng.permutation(E)[:k] for _ in range(T)])
+    got_idx, w = O.route_replay(l, cfg, b, idx)
+    np.testing.assert_array_equal(got_idx, idx)
+    lt, it = torch.tensor(l), torch.tensor(idx)
+    if score_fn == SOFTMAX:
+        ref = torch.softmax(torch.gather(lt + torch.tensor(b, dtype=torch.float64), 1, it), dim=1)
+    else:
+        s = torch.gather(torch.sigmoid(lt), 1, it)
+        ref = 2.5 * s / s.sum(dim=1, keepdim=True)
+    np.testing.assert_allclose(w, ref.numpy(), rtol=1e-13)
+    # replaying the router's own choice gives its own weights
+    idx0, w0 = O.route(l, cfg, b)
+    np.testing.assert_allclose(O.route_replay(l, cfg, b, idx0)[1], w0, rtol=0, atol=0)
+
+
 # --------------------------------------------------------------------------- #
 # stage 2: dispatch maps
 # --------------------------------------------------------------------------- #
