@@ -155,6 +155,20 @@ MOE_API moe_status moe_query_sizes(const moe_config* cfg, moe_sizes* out);
 MOE_API moe_status moe_route(const moe_config* cfg, const void* x, const float* W_r, const float* bias,
                      float* logits, int32_t* idx, float* w, void* scratch, void* stream);
 
+/* Router Replay (es summary §2, RL support: routing decisions recorded by
+ * inference replayed in training): stage 1 with the experts given instead of
+ * selected. logits as moe_route; idx [T,k] i32 is an input (each entry in
+ * [0, E)); w [T,k] f32 = the router's weights for those experts in that order
+ * -- softmax over their logits + bias, or route_scale * s_j / sum s -- with
+ * moe_route's own arithmetic, so replaying moe_route's idx gives its w (the
+ * sigmoid router's exact-path tokens, whose selection needed fp64 keys, can
+ * differ by a few fp32 ulp). An index outside [0, E) records
+ * MOE_ERR_DEVICE_CHECK in the status word and gets weight 0. The rest of the
+ * layer (moe_permute on the same idx, ..., the backward) is unchanged. */
+MOE_API moe_status moe_route_replay(const moe_config* cfg, const void* x, const float* W_r,
+                            const float* bias, const int32_t* idx, float* logits, float* w,
+                            void* scratch, void* stream);
+
 /* Stage 2, dispatch (es summary §2.1 step 2, done locally). A stable counting
  * sort of the (token, slot) assignments by (expert, token): expert e's kept
  * tokens occupy rows offsets[e] .. offsets[e]+counts[e]-1 in increasing token

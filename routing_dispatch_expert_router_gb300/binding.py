@@ -21,7 +21,7 @@ STATUS_NAMES = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED",
 
 # every exported entry point of include/moe_abi.h
 ENTRY_POINTS = (
-    "moe_query_sizes", "moe_route", "moe_permute", "moe_permute_noalloc",
+    "moe_query_sizes", "moe_route", "moe_route_replay", "moe_permute", "moe_permute_noalloc",
     "moe_grouped_ffn_fwd", "moe_unpermute",
     "moe_unpermute_bwd", "moe_grouped_ffn_bwd", "moe_route_bwd", "moe_permute_bwd",
     "moe_router_wgrad", "moe_layer_fwd", "moe_layer_bwd", "moe_last_device_status",
@@ -154,6 +154,11 @@ def moe_query_sizes(cfg) -> MoESizes:
 
 def moe_route(cfg, x, W_r, bias, logits, idx, w, scratch, stream=None):
     _call("moe_route", _cfg(cfg), x, W_r, bias, logits, idx, w, scratch, _stream(stream))
+
+
+def moe_route_replay(cfg, x, W_r, bias, idx, logits, w, scratch, stream=None):
+    """Router Replay: the given experts idx [T,k] (input) instead of the top-k."""
+    _call("moe_route_replay", _cfg(cfg), x, W_r, bias, idx, logits, w, scratch, _stream(stream))
 
 
 def moe_permute(cfg, x, idx, counts, offsets, row_of, token_of, sel_offsets, sel_tokens, x_perm,

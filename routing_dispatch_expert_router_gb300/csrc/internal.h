@@ -17,6 +17,9 @@ int num_sms();
 
 cudaError_t launch_route(const moe_config& c, const void* x, const float* W_r, const float* bias,
                          float* logits, int32_t* idx, float* w, uint8_t* scratch, cudaStream_t s);
+cudaError_t launch_route_replay(const moe_config& c, const void* x, const float* W_r,
+                                const float* bias, const int32_t* idx, float* logits, float* w,
+                                uint8_t* scratch, cudaStream_t s);
 
 cudaError_t launch_permute(const moe_config& c, const void* x, const int32_t* idx,
                            int32_t* counts, int32_t* offsets, int32_t* row_of, int32_t* token_of,

@@ -180,6 +180,19 @@ moe_status moe_route(const moe_config* cfg, const void* x, const float* W_r, con
   return MOE_OK;
 }
 
+moe_status moe_route_replay(const moe_config* cfg, const void* x, const float* W_r,
+                            const float* bias, const int32_t* idx, float* logits, float* w,
+                            void* scratch, void* stream) {
+  MOE_TRY(check_config(cfg));
+  MOE_REQUIRE(tok16(cfg, x) && al16(W_r) && tok4(cfg, logits) && tok4(cfg, idx) && tok4(cfg, w));
+  MOE_REQUIRE(bias == nullptr || al4(bias));
+  MOE_REQUIRE(al16(scratch));
+  if (cfg->T == 0) return MOE_OK;
+  MOE_CUDA(launch_route_replay(*cfg, x, W_r, bias, idx, logits, w,
+                               static_cast<uint8_t*>(scratch), (cudaStream_t)stream));
+  return MOE_OK;
+}
+
 moe_status moe_permute(const moe_config* cfg, const void* x, const int32_t* idx, int32_t* counts,
                        int32_t* offsets, int32_t* row_of, int32_t* token_of, int32_t* sel_offsets,
                        int32_t* sel_tokens, void* x_perm, void* scratch, void* stream) {

@@ -745,8 +745,44 @@ int64_t router_split_bytes(const moe_config& c) {
   return fwd > bwd ? fwd : bwd;
 }
 
-cudaError_t launch_route(const moe_config& c, const void* x, const float* W_r, const float* bias,
-                         float* logits, int32_t* idx, float* w, uint8_t* scratch, cudaStream_t s) {
+// Router Replay: the weights of recorded experts idx [T,k] (in that order)
+// from the logits, with the selection kernels' own arithmetic (softmax router:
+// exp of the chosen logit + bias relative to slot 0's, over their sum in slot
+// order; sigmoid router: route_scale times the fp32 sigmoid over the sum of the
+// chosen ones), so replaying the router's own choice reproduces its weights.
+// One warp per token, lane j < k takes slot j. An expert index outside [0, E)
+// records MOE_ERR_DEVICE_CHECK and counts as weight 0.
+__global__ void __launch_bounds__(256)
+route_replay_weights_kernel(const float* __restrict__ logits, const float* __restrict__ bias,
+                            const int32_t* __restrict__ idx, float* __restrict__ wout, int T,
+                            int E, int k, int score_fn, float route_scale, int32_t* status) {
+  const int lane = threadIdx.x & 31;
+  const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (t >= T) return;
+  const float* lrow = logits + (size_t)t * E;
+  int e = lane < k ? idx[(size_t)t * k + lane] : 0;
+  const bool bad = lane < k && (unsigned)e >= (unsigned)E;
+  if (bad) {
+    record_status(status, MOE_ERR_DEVICE_CHECK);
+    e = 0;
+  }
+  float v = 0.f;
+  if (score_fn == MOE_SCORE_SOFTMAX) {
+    const int e0 = __shfl_sync(0xffffffffu, e, 0);
+    const float z0 = __fadd_rn(lrow[e0], bias ? bias[e0] : 0.f);
+    if (lane < k && !bad) v = expf(__fadd_rn(lrow[e], bias ? bias[e] : 0.f) - z0);
+  } else if (lane < k && !bad) {
+    v = __fdiv_rn(1.f, 1.f + expf(-lrow[e]));
+  }
+  float sum = 0.f;
+  for (int j = 0; j < k; ++j) sum += __shfl_sync(0xffffffffu, v, j);
+  if (lane < k)
+    wout[(size_t)t * k + lane] = score_fn == MOE_SCORE_SOFTMAX ? v / sum : route_scale * v / sum;
+}
+
+// logits[T,E] = x . W_r^T in fp32, by the path the expert count selects.
+static cudaError_t launch_router_logits(const moe_config& c, const void* x, const float* W_r,
+                                        float* logits, uint8_t* scratch, cudaStream_t s) {
   const __nv_bfloat16* xb = static_cast<const __nv_bfloat16*>(x);
   if (router_on_tensor_cores(c)) {
     // logits on the tensor cores from the exact three-way bf16 split of W_r
@@ -770,7 +806,13 @@ cudaError_t launch_route(const moe_config& c, const void* x, const float* W_r, c
     dim3 grid((c.T + 63) / 64, (c.E + 63) / 64);
     route_logits_kernel<64, 64><<<grid, 256, 0, s>>>(xb, W_r, logits, c.T, c.H, c.E);
   }
-  if (cudaError_t err = cudaGetLastError(); err != cudaSuccess) return err;
+  return cudaGetLastError();
+}
+
+cudaError_t launch_route(const moe_config& c, const void* x, const float* W_r, const float* bias,
+                         float* logits, int32_t* idx, float* w, uint8_t* scratch, cudaStream_t s) {
+  if (cudaError_t err = launch_router_logits(c, x, W_r, logits, scratch, s); err != cudaSuccess)
+    return err;
   // experts per lane: the smallest of 1, 2, 4, 8 that covers E
   const int npl = c.E <= 32 ? 1 : c.E <= 64 ? 2 : c.E <= 128 ? 4 : 8;
   if (c.score_fn == MOE_SCORE_SOFTMAX) {
@@ -786,6 +828,17 @@ cudaError_t launch_route(const moe_config& c, const void* x, const float* W_r, c
     kern<<<(c.T + 3) / 4, 128, 0, s>>>(logits, bias, idx, w, c.T, c.E, c.k, c.n_groups,
                                        c.topk_groups, c.group_score, c.route_scale);
   }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_route_replay(const moe_config& c, const void* x, const float* W_r,
+                                const float* bias, const int32_t* idx, float* logits, float* w,
+                                uint8_t* scratch, cudaStream_t s) {
+  if (cudaError_t err = launch_router_logits(c, x, W_r, logits, scratch, s); err != cudaSuccess)
+    return err;
+  route_replay_weights_kernel<<<(c.T + 7) / 8, 256, 0, s>>>(
+      logits, bias, idx, w, c.T, c.E, c.k, c.score_fn, c.route_scale,
+      reinterpret_cast<int32_t*>(scratch + kScratchStatus));
   return cudaGetLastError();
 }
 

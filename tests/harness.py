@@ -55,8 +55,11 @@ def _poison(t: torch.Tensor):
     t.view(torch.uint8).fill_(0xFF)
 
 
-def run_layer(shape, inp: dict, backward: bool = True, device: str = "cuda") -> dict:
-    """One forward (+backward) through moe_layer_fwd / moe_layer_bwd."""
+def run_layer(shape, inp: dict, backward: bool = True, device: str = "cuda",
+              replay_idx=None) -> dict:
+    """One forward (+backward) through moe_layer_fwd / moe_layer_bwd; with
+    replay_idx [T,k], the forward runs its stages with moe_route_replay on those
+    experts in place of moe_route."""
     cfg = B.config(shape)
     bufs = B.alloc_buffers(cfg, device, backward=backward)
     for t in list(bufs.fwd.values()) + list(bufs.bwd.values()):
@@ -67,7 +70,18 @@ def run_layer(shape, inp: dict, backward: bool = True, device: str = "cuda") -> 
     P = B.params(d["W_r"], d["bias"], d["W13"], d["W2"])
     out = torch.empty(T, H, dtype=torch.bfloat16, device=device)
     _poison(out)
-    B.moe_layer_fwd(cfg, P, d["x"], out, bufs.fwd_struct, bufs.scratch)
+    if replay_idx is None:
+        B.moe_layer_fwd(cfg, P, d["x"], out, bufs.fwd_struct, bufs.scratch)
+    else:
+        f = bufs.fwd
+        f["idx"].copy_(torch.as_tensor(replay_idx, dtype=torch.int32).reshape(f["idx"].shape))
+        B.moe_route_replay(cfg, d["x"], d["W_r"], d["bias"], f["idx"], f["logits"], f["w"],
+                           bufs.scratch)
+        B.moe_permute(cfg, d["x"], f["idx"], f["counts"], f["offsets"], f["row_of"],
+                      f["token_of"], f["sel_offsets"], f["sel_tokens"], f["x_perm"], bufs.scratch)
+        B.moe_grouped_ffn_fwd(cfg, f["x_perm"], f["counts"], f["offsets"], d["W13"], d["W2"],
+                              f["GU"], f["h"], f["y_perm"], bufs.scratch)
+        B.moe_unpermute(cfg, f["y_perm"], f["row_of"], f["w"], f["offsets"], out)
     res = {"out": out}
     if backward:
         dx = torch.empty(T, H, dtype=torch.bfloat16, device=device)
@@ -92,7 +106,7 @@ def _ident(a):
     return a
 
 
-def check_steps(shape, inp: dict, g: dict, backward: bool = True):
+def check_steps(shape, inp: dict, g: dict, backward: bool = True, replay_idx=None):
     """Every step of the GPU path against the oracle fed the GPU's step inputs.
 
     In the FP8 configuration the oracle quantises those inputs the way the
@@ -117,8 +131,12 @@ def check_steps(shape, inp: dict, g: dict, backward: bool = True):
     scale = np.abs(x) @ np.abs(Wr).T
     bad = np.abs(lg - ref_l) > 1e-5 * scale + 1e-30
     assert not bad.any(), f"logits: {int(bad.sum())} beyond 1e-5*sum|x w|"
-    # a2: selection bit-exact on the GPU's logits, weights close
-    idx_ref, w_ref = O.route(lg, shape, bias)
+    # a2: selection bit-exact on the GPU's logits (or the replayed experts),
+    # weights close
+    if replay_idx is None:
+        idx_ref, w_ref = O.route(lg, shape, bias)
+    else:
+        idx_ref, w_ref = O.route_replay(lg, shape, bias, np.asarray(replay_idx).reshape(-1, shape.k))
     assert_equal("idx", i64(g["idx"]), idx_ref)
     assert_close("w", f64(g["w"]), w_ref, atol=1e-6, rtol=1e-5)
     # a3/a4: maps bit-exact, x_perm exact
