@@ -596,7 +596,8 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
 // SMs (a cluster of 2) with tcgen05.mma.cta_group::2: each CTA holds 128 rows
 // of the A tile and 128 of the 256 B columns, so every SM streams 32 KB per
 // 64-deep k-block instead of 48 KB for the same tensor work, and six stages
-// fit in shared memory. Only the even CTA issues MMAs; both CTAs' TMA loads
+// fit in shared memory (five with the SwiGLU-backward ring below). Only the
+// even CTA issues MMAs; both CTAs' TMA loads
 // count on the even CTA's "full" barrier, the MMA completion is multicast to
 // both CTAs, and both epilogues report back to the even CTA.
 constexpr int kPairStage = 32768;                 // 16 KB of A + 16 KB of B per CTA
