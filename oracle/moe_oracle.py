@@ -30,6 +30,13 @@ readings listed below; every one of them is a reading, not a quote:
   * Router Replay (the summary's RL support, es "Soporte para RL"): the
     experts come from a recorded idx [T,k] instead of the top-k, the weights
     are the router's for those experts, in that order, from the current logits;
+  * load-balancing loss (the pages fuse "aux-loss" computation with routing,
+    es §2.3.C, without a formula): coeff * E * sum_e f_e P_e, f_e the share of
+    the T k selections that went to e, P_e the mean over tokens of the
+    router's probability of e over all experts (softmax of l + b, or the
+    sigmoid scores normalised over all experts); its gradient flows into x
+    and W_r through the logits. The bias update: a sign step of the selection
+    bias towards the mean load (not in the pages; see bias_update);
   * capacity C = ceil(cf * T * k / E) rounded up to row_align; an expert keeps
     its first C tokens in token order, dropped assignments contribute 0 and
     the surviving weights are not renormalised;
@@ -270,6 +277,98 @@ def route_replay(logits, cfg, bias, idx):
     decisions of inference replayed in training)."""
     idx = np.asarray(idx, dtype=np.int64)
     return idx, route_weights(logits, cfg, bias, idx)
+
+
+# --------------------------------------------------------------------------- #
+# load-balancing auxiliary loss and the bias update
+# --------------------------------------------------------------------------- #
+def aux_probs(logits, cfg, bias=None):
+    """Router probability of every expert [T,E] for the load-balancing loss.
+
+    Softmax router: the softmax over all E experts of l + b. Sigmoid router:
+    s_e / sum over all E of s, s = sigmoid(l) (unbiased). Each row sums to 1.
+    """
+    l = np.asarray(logits, dtype=np.float64)
+    if cfg.score_fn == SOFTMAX:
+        b64 = 0.0 if bias is None else np.asarray(bias, np.float32).astype(np.float64)[None, :]
+        z = l + b64
+        z = np.exp(z - z.max(axis=1, keepdims=True))
+        return z / z.sum(axis=1, keepdims=True)
+    if cfg.score_fn == SIGMOID:
+        s = sigmoid(l)
+        return s / s.sum(axis=1, keepdims=True)
+    raise ValueError("score_fn")
+
+
+def aux_loss(logits, cfg, bias, idx, coeff):
+    """Load-balancing auxiliary loss of one batch (reading of the loss whose
+    computation the pages fuse with routing and permutation, es summary
+    §2.3.C "Fusión de Kernels"; the pages give no formula, so this is the
+    switch-style balance loss):
+
+      counts[e] = tokens that selected e (the router's top-k, before any
+                  capacity drop),
+      f_e = counts[e] / (T k),  P_e = mean over tokens of aux_probs[t, e],
+      loss = coeff * E * sum_e f_e P_e.
+
+    Returns (loss, counts [E] int64, P [E]). An empty batch gives 0, 0, 0.
+    """
+    idx = np.asarray(idx, dtype=np.int64)
+    T, E, k = cfg.T, cfg.E, cfg.k
+    counts = np.bincount(idx.reshape(-1), minlength=E)[:E].astype(np.int64)
+    if T == 0:
+        return 0.0, counts, np.zeros(E)
+    P = aux_probs(logits, cfg, bias).mean(axis=0)
+    f = counts / float(T * k)
+    return float(coeff * E * np.sum(f * P)), counts, P
+
+
+def aux_loss_dlogits(logits, cfg, bias, counts, coeff, dloss):
+    """dloss times the gradient of aux_loss w.r.t. the logits [T,E] (counts
+    are piecewise constant in the logits and carry none).
+
+    With g_e = coeff E counts[e] / (T^2 k) = d loss / d p[t,e]:
+      softmax: dl[t,e] = p[t,e] (g_e - sum_j p[t,j] g_j);
+      sigmoid: p = s / S, so dl[t,e] = s_e (1 - s_e) / S (g_e - sum_j p[t,j] g_j).
+    """
+    l = np.asarray(logits, dtype=np.float64)
+    T, E, k = cfg.T, cfg.E, cfg.k
+    if T == 0:
+        return np.zeros((0, E))
+    g = coeff * E * np.asarray(counts, np.float64) / (float(T) * T * k)
+    p = aux_probs(l, cfg, bias)
+    centred = g[None, :] - (p * g[None, :]).sum(axis=1, keepdims=True)
+    if cfg.score_fn == SOFTMAX:
+        return dloss * p * centred
+    s = sigmoid(l)
+    return dloss * s * (1.0 - s) / s.sum(axis=1, keepdims=True) * centred
+
+
+def aux_loss_backward(cfg, x, W_r, logits, bias, counts, coeff, dloss, dx, dW_r,
+                      rounding: bool = True):
+    """The loss's gradient added to the layer's input and router-weight
+    gradients: dl = aux_loss_dlogits(...); dx' = bf16(dx + dl W_r) and
+    dW_r' = fp32(dW_r + dl^T x) (l = x W_r^T). Returns (dl, dx', dW_r')."""
+    dl = aux_loss_dlogits(logits, cfg, bias, counts, coeff, dloss)
+    x = np.asarray(x, np.float64)
+    W_r = np.asarray(W_r, np.float64)
+    dx_new = _rb(np.asarray(dx, np.float64) + dl @ W_r, rounding)
+    dW_new = _rf(np.asarray(dW_r, np.float64) + dl.T @ x, rounding)
+    return dl, dx_new, dW_new
+
+
+def bias_update(bias, counts, cfg, rate):
+    """Auxiliary-loss-free balancing step on the per-expert selection bias.
+
+    The pages do not describe it; it is the plain sign rule that keeps the
+    selection bias of the sigmoid router with bias (the DeepSeek-V3-style
+    configuration) balanced: every expert above the mean load T k / E moves
+    its bias down by `rate`, every expert below it up by `rate`, an expert
+    exactly at the mean keeps it. fp32, as stored."""
+    b = np.zeros(cfg.E, np.float32) if bias is None else np.asarray(bias, np.float32)
+    c = np.asarray(counts, np.int64)
+    sign = np.sign(cfg.T * cfg.k - cfg.E * c).astype(np.float32)
+    return (b + np.float32(rate) * sign).astype(np.float32)
 
 
 def _group_mask(sc, cfg):

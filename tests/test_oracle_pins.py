@@ -180,6 +180,129 @@ def test_route_replay_weights_match_torch_for_any_given_experts(score_fn):
 
 
 # --------------------------------------------------------------------------- #
+# load-balancing loss and bias update
+# --------------------------------------------------------------------------- #
+@pytest.mark.parametrize("score_fn", [SOFTMAX, SIGMOID])
+def test_aux_loss_is_coeff_when_every_token_takes_every_expert(score_fn):
+    """k = E: f_e = 1/E for every expert, so the loss is coeff * sum_e P_e,
+    and the probabilities of a token sum to 1 over all experts (the sigmoid
+    scores normalised over all E, not over the selected): loss = coeff for any
+    logits."""
+    T, E = 37, 6
+    cfg = MoEShape("t", T=T, H=8, E=E, k=E, F=8, score_fn=score_fn)
+    rng = np.random.default_rng(11)
+    l = O.round_f32(rng.standard_normal((T, E)) * 3)
+    b = O.round_f32(0.3 * rng.standard_normal(E)).astype(np.float32)
+    idx = np.stack([rng.permutation(E) for _ in range(T)])
+    loss, counts, P = O.aux_loss(l, cfg, b, idx, 0.125)
+    np.testing.assert_array_equal(counts, np.full(E, T))
+    assert abs(P.sum() - 1.0) < 1e-13
+    assert abs(loss - 0.125) < 1e-13
+
+
+def test_aux_loss_uniform_routing_and_full_imbalance():
+    """Uniform probabilities and equal loads give coeff (the loss's minimum
+    over loads for uniform P); every token sending all its weight and its one
+    selection to expert 0 gives coeff * E (the maximum)."""
+    T, E = 64, 8
+    cfg = MoEShape("t", T=T, H=8, E=E, k=2, F=8)
+    idx = np.stack([[t % E, (t + 1) % E] for t in range(T)])     # 16 selections each
+    loss, counts, P = O.aux_loss(np.zeros((T, E)), cfg, None, idx, 0.01)
+    np.testing.assert_array_equal(counts, np.full(E, 16))
+    np.testing.assert_allclose(P, np.full(E, 1 / E), rtol=1e-15)
+    assert abs(loss - 0.01) < 1e-15
+    cfg1 = MoEShape("t", T=T, H=8, E=E, k=1, F=8)
+    l = np.full((T, E), -800.0)
+    l[:, 0] = 0.0                                   # softmax mass 1 (exp(-800) == 0)
+    loss1, counts1, P1 = O.aux_loss(l, cfg1, None, np.zeros((T, 1), np.int64), 0.01)
+    assert counts1[0] == T and counts1[1:].sum() == 0
+    assert P1[0] == 1.0
+    assert abs(loss1 - 0.01 * E) < 1e-15
+
+
+def test_aux_loss_hand_computed_case():
+    """T = 2, E = 3, k = 1, softmax, logits chosen so that the probabilities
+    are exact fractions: token 0 (ln 1, ln 2, ln 1) -> (1/4, 1/2, 1/4), token 1
+    (ln 3, ln 1, ln 0 -> -inf) -> (3/4, 1/4, 0). Selections 1 and 0:
+    f = (1/2, 1/2, 0), P = (1/2, 3/8, 1/8), loss = c * 3 * (1/4 + 3/16)."""
+    cfg = MoEShape("t", T=2, H=8, E=3, k=1, F=8)
+    l = np.log(np.array([[1.0, 2.0, 1.0], [3.0, 1.0, 0.0]]))
+    loss, counts, P = O.aux_loss(l, cfg, None, np.array([[1], [0]]), 2.0)
+    np.testing.assert_array_equal(counts, [1, 1, 0])
+    np.testing.assert_allclose(P, [0.5, 0.375, 0.125], rtol=1e-15)
+    assert abs(loss - 2.0 * 3 * (0.25 + 0.1875)) < 1e-14
+
+
+@pytest.mark.parametrize("score_fn", [SOFTMAX, SIGMOID])
+def test_aux_loss_gradients_match_finite_differences(score_fn):
+    """The logit gradient against central differences of aux_loss (counts
+    follow idx, which is held fixed), and the x / W_r gradients against
+    central differences of the loss of l = x W_r^T (no rounding)."""
+    T, H, E, k = 9, 5, 7, 2
+    cfg = MoEShape("t", T=T, H=H, E=E, k=k, F=8, score_fn=score_fn)
+    rng = np.random.default_rng(3)
+    x = rng.standard_normal((T, H))
+    W = rng.standard_normal((E, H)) * 0.7
+    b = O.round_f32(0.2 * rng.standard_normal(E)).astype(np.float32)
+    idx = np.stack([rng.permutation(E)[:k] for _ in range(T)])
+    coeff, dloss = 0.3, 1.7
+    L = lambda lg: dloss * O.aux_loss(lg, cfg, b, idx, coeff)[0]
+    l = x @ W.T
+    _, counts, _ = O.aux_loss(l, cfg, b, idx, coeff)
+    dl = O.aux_loss_dlogits(l, cfg, b, counts, coeff, dloss)
+    eps = 1e-6
+    for t, e in [(0, 0), (3, 4), (8, 6), (5, 1)]:
+        lp, lm = l.copy(), l.copy()
+        lp[t, e] += eps
+        lm[t, e] -= eps
+        assert abs((L(lp) - L(lm)) / (2 * eps) - dl[t, e]) < 1e-8 * (1 + abs(dl[t, e]))
+    dx0 = rng.standard_normal((T, H))
+    dW0 = rng.standard_normal((E, H))
+    _, dx, dW = O.aux_loss_backward(cfg, x, W, l, b, counts, coeff, dloss, dx0, dW0,
+                                    rounding=False)
+    for t, h in [(0, 0), (4, 3), (8, 4)]:
+        xp, xm = x.copy(), x.copy()
+        xp[t, h] += eps
+        xm[t, h] -= eps
+        fd = (L(xp @ W.T) - L(xm @ W.T)) / (2 * eps)
+        assert abs(dx[t, h] - dx0[t, h] - fd) < 1e-8 * (1 + abs(fd))
+    for e, h in [(0, 1), (6, 4), (3, 0)]:
+        Wp, Wm = W.copy(), W.copy()
+        Wp[e, h] += eps
+        Wm[e, h] -= eps
+        fd = (L(x @ Wp.T) - L(x @ Wm.T)) / (2 * eps)
+        assert abs(dW[e, h] - dW0[e, h] - fd) < 1e-8 * (1 + abs(fd))
+
+
+def test_aux_loss_dlogits_sum_to_zero_per_token_for_softmax():
+    """Softmax probabilities sum to 1 whatever the logits, so shifting all of
+    a token's logits by a constant changes nothing: each row of the softmax
+    gradient sums to 0 (a dropped centring term would break it)."""
+    T, E = 20, 16
+    cfg = MoEShape("t", T=T, H=8, E=E, k=4, F=8)
+    rng = np.random.default_rng(8)
+    l = rng.standard_normal((T, E))
+    counts = rng.integers(0, 10, E)
+    dl = O.aux_loss_dlogits(l, cfg, None, counts, 0.1, 1.0)
+    np.testing.assert_allclose(dl.sum(axis=1), 0.0, atol=1e-17)
+    assert np.abs(dl).max() > 1e-6
+
+
+def test_bias_update_moves_towards_the_mean_load():
+    """T k / E = 4 * 2 / 4 = 2: loads (3, 2, 1, 2) move the biases by (-r, 0,
+    +r, 0), in fp32; no bias counts as zeros."""
+    cfg = MoEShape("t", T=4, H=8, E=4, k=2, F=8)
+    b = np.array([0.5, -0.25, 1e-3, 0.0], np.float32)
+    out = O.bias_update(b, [3, 2, 1, 2], cfg, 1e-3)
+    assert out.dtype == np.float32
+    np.testing.assert_array_equal(
+        out, np.array([np.float32(0.5) - np.float32(1e-3), -0.25,
+                       np.float32(1e-3) + np.float32(1e-3), 0.0], np.float32))
+    np.testing.assert_array_equal(O.bias_update(None, [0, 4, 4, 0], cfg, 0.5),
+                                  np.array([0.5, -0.5, -0.5, 0.5], np.float32))
+
+
+# --------------------------------------------------------------------------- #
 # stage 2: dispatch maps
 # --------------------------------------------------------------------------- #
 def _brute_maps(idx, cfg):
