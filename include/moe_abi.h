@@ -169,6 +169,47 @@ MOE_API moe_status moe_route_replay(const moe_config* cfg, const void* x, const 
                             const float* bias, const int32_t* idx, float* logits, float* w,
                             void* scratch, void* stream);
 
+/* Load-balancing auxiliary loss of one batch, and the auxiliary-loss-free
+ * update of the selection bias, in one kernel launch after moe_route (es
+ * summary §2.3.C, "Fusión de Kernels": routing, permutation and the
+ * auxiliary-loss computation fused to save launches; the pages give no
+ * formula, so the loss is the switch-style balance loss):
+ *   sel_counts[e] = tokens whose idx row holds e (the router's selection,
+ *                   before any capacity drop), f_e = sel_counts[e] / (T k),
+ *   p_mean[e]     = P_e, the mean over tokens of the router's probability of
+ *                   e over all E experts (softmax of logits + bias; sigmoid
+ *                   router: sigmoid(logit) normalised over all E),
+ *   *loss         = coeff * E * sum_e f_e P_e (uniform routing gives coeff).
+ * bias_out (nullable; may equal bias): bias[e] + bias_rate * sign(T k / E -
+ * sel_counts[e]) (bias NULL counts as 0), the sign step that moves every
+ * expert's selection bias towards the mean load.
+ * logits [T,E] fp32 and idx [T,k] int32 as written by moe_route; sel_counts
+ * [E] int32, p_mean [E] fp32, loss [1] fp32, bias_out [E] fp32: device.
+ * Deterministic (fixed summation order). An index outside [0, E) records
+ * MOE_ERR_DEVICE_CHECK and is not counted. T == 0 gives zeros (bias_out =
+ * bias). scratch: moe_sizes.scratch_bytes bytes, zero-filled once (the
+ * launch keeps an arrival counter in it and leaves it zero). */
+MOE_API moe_status moe_route_aux(const moe_config* cfg, const float* logits, const float* bias,
+                                 const int32_t* idx, float coeff, float bias_rate,
+                                 int32_t* sel_counts, float* p_mean, float* loss,
+                                 float* bias_out, void* scratch, void* stream);
+
+/* Backward of moe_route_aux's loss, scaled by dloss (host scalar, the
+ * gradient of the training loss w.r.t. *loss), with sel_counts held fixed:
+ *   dlogits_aux[t,e] = dloss * d loss / d logits[t,e]   ([T,E] fp32, written;
+ *       softmax p (g_e - sum_j p_j g_j), sigmoid s(1-s)/S (g_e - sum_j p_j g_j),
+ *       g_e = coeff E sel_counts[e] / (T^2 k)),
+ *   dx   [T,H] bf16  += dlogits_aux . W_r   (fp32 sum over e, one rounding),
+ *   dW_r [E,H] fp32  += dlogits_aux^T . x   (every token, every expert).
+ * Call it after moe_layer_bwd (or moe_permute_bwd and moe_router_wgrad) with
+ * the same dx and dW_r: the loss's gradient reaches x and W_r through the
+ * logits like the layer's own. x, logits and bias as given to moe_route. */
+MOE_API moe_status moe_route_aux_bwd(const moe_config* cfg, const void* x, const float* logits,
+                                     const float* bias, const float* W_r,
+                                     const int32_t* sel_counts, float coeff, float dloss,
+                                     float* dlogits_aux, void* dx, float* dW_r, void* scratch,
+                                     void* stream);
+
 /* Stage 2, dispatch (es summary §2.1 step 2, done locally). A stable counting
  * sort of the (token, slot) assignments by (expert, token): expert e's kept
  * tokens occupy rows offsets[e] .. offsets[e]+counts[e]-1 in increasing token

@@ -21,7 +21,8 @@ STATUS_NAMES = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED",
 
 # every exported entry point of include/moe_abi.h
 ENTRY_POINTS = (
-    "moe_query_sizes", "moe_route", "moe_route_replay", "moe_permute", "moe_permute_noalloc",
+    "moe_query_sizes", "moe_route", "moe_route_replay", "moe_route_aux", "moe_route_aux_bwd",
+    "moe_permute", "moe_permute_noalloc",
     "moe_grouped_ffn_fwd", "moe_unpermute",
     "moe_unpermute_bwd", "moe_grouped_ffn_bwd", "moe_route_bwd", "moe_permute_bwd",
     "moe_router_wgrad", "moe_layer_fwd", "moe_layer_bwd", "moe_last_device_status",
@@ -138,6 +139,8 @@ def _call(name, *args):
     for a in args:
         if isinstance(a, ctypes.Structure):
             conv.append(ctypes.byref(a))
+        elif isinstance(a, float):
+            conv.append(ctypes.c_float(a))
         elif a is None or isinstance(a, int):
             conv.append(ctypes.c_void_p(a))
         else:
@@ -159,6 +162,20 @@ def moe_route(cfg, x, W_r, bias, logits, idx, w, scratch, stream=None):
 def moe_route_replay(cfg, x, W_r, bias, idx, logits, w, scratch, stream=None):
     """Router Replay: the given experts idx [T,k] (input) instead of the top-k."""
     _call("moe_route_replay", _cfg(cfg), x, W_r, bias, idx, logits, w, scratch, _stream(stream))
+
+
+def moe_route_aux(cfg, logits, bias, idx, coeff, bias_rate, sel_counts, p_mean, loss, bias_out,
+                  scratch, stream=None):
+    """Load-balancing loss statistics, loss and (bias_out not None) the bias update."""
+    _call("moe_route_aux", _cfg(cfg), logits, bias, idx, float(coeff), float(bias_rate),
+          sel_counts, p_mean, loss, bias_out, scratch, _stream(stream))
+
+
+def moe_route_aux_bwd(cfg, x, logits, bias, W_r, sel_counts, coeff, dloss, dlogits_aux, dx,
+                      dW_r, scratch, stream=None):
+    """The loss's gradient: writes dlogits_aux, adds into dx and dW_r."""
+    _call("moe_route_aux_bwd", _cfg(cfg), x, logits, bias, W_r, sel_counts, float(coeff),
+          float(dloss), dlogits_aux, dx, dW_r, scratch, _stream(stream))
 
 
 def moe_permute(cfg, x, idx, counts, offsets, row_of, token_of, sel_offsets, sel_tokens, x_perm,

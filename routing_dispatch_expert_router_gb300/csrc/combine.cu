@@ -289,7 +289,8 @@ route_bwd_kernel(const float* __restrict__ logits, const int32_t* __restrict__ i
   if (lane < k && (unsigned)e < (unsigned)E) row[e] = v;
 }
 
-// dW_r[e, cols] = sum over the tokens that selected e of dlogits[t,e] x[t, cols].
+// dW_r[e, cols] = sum over the tokens that selected e of dlogits[t,e] x[t, cols]
+// (sel_offsets == NULL: over all T tokens; accumulate: added to dW_r).
 // Block (e, slab of 32*CPL columns); lane owns CPL columns. The expert's
 // selecting tokens are taken in chunks of 8 (chunk i by warp i mod 16): lanes
 // 0..7 load the chunk's token ids and dlogits, then the warp walks the chunk in
@@ -299,7 +300,7 @@ template <int CPL>
 __global__ void __launch_bounds__(512, 2)
 router_wgrad_kernel(const __nv_bfloat16* __restrict__ x, const int32_t* __restrict__ sel_offsets,
                     const int32_t* __restrict__ sel_tokens, const float* __restrict__ dlogits,
-                    float* __restrict__ dW_r, int H, int E) {
+                    float* __restrict__ dW_r, int H, int E, int T, int accumulate) {
   constexpr int NW = 16, CH = 8, U = 4, SLAB = 32 * CPL;
   __shared__ float part[NW][SLAB];
   const int e = blockIdx.x;
@@ -307,7 +308,7 @@ router_wgrad_kernel(const __nv_bfloat16* __restrict__ x, const int32_t* __restri
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
   const int c = col0 + lane * CPL;
   const bool on = c < H;
-  const int beg = sel_offsets[e], end = sel_offsets[e + 1];
+  const int beg = sel_offsets ? sel_offsets[e] : 0, end = sel_offsets ? sel_offsets[e + 1] : T;
   float acc[CPL];
 #pragma unroll
   for (int i = 0; i < CPL; ++i) acc[i] = 0.f;
@@ -316,7 +317,7 @@ router_wgrad_kernel(const __nv_bfloat16* __restrict__ x, const int32_t* __restri
     int my_t = 0;
     float my_d = 0.f;
     if (lane < n) {
-      my_t = sel_tokens[base + lane];
+      my_t = sel_tokens ? sel_tokens[base + lane] : base + lane;
       my_d = dlogits[(size_t)my_t * E + e];
     }
 #pragma unroll
@@ -355,7 +356,7 @@ router_wgrad_kernel(const __nv_bfloat16* __restrict__ x, const int32_t* __restri
       float s = 0.f;
 #pragma unroll
       for (int q2 = 0; q2 < NW; ++q2) s += part[q2][i];
-      dW_r[(size_t)e * H + col] = s;
+      dW_r[(size_t)e * H + col] = accumulate ? dW_r[(size_t)e * H + col] + s : s;
     }
   }
 }
@@ -470,7 +471,7 @@ split_dlogits_kernel(const float* __restrict__ dl, __nv_bfloat16* __restrict__ D
 // 4j .. 4j+3] over g with four chunks' loads in flight.
 __global__ void __launch_bounds__(256)
 sum_chunks_transpose_kernel(const float* __restrict__ P, float* __restrict__ dW_r, int NG, int H,
-                            int E) {
+                            int E, int accumulate) {
   __shared__ float tile[32][33];
   const int j = threadIdx.x & 7, r = threadIdx.x >> 3;
   const int h0 = blockIdx.x * 32, e0 = blockIdx.y * 32;
@@ -504,16 +505,20 @@ sum_chunks_transpose_kernel(const float* __restrict__ P, float* __restrict__ dW_
   __syncthreads();
   const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
 #pragma unroll
-  for (int i = 0; i < 4; ++i) dW_r[(size_t)(e0 + ty + 8 * i) * H + h0 + tx] = tile[tx][ty + 8 * i];
+  for (int i = 0; i < 4; ++i) {
+    float* o = dW_r + (size_t)(e0 + ty + 8 * i) * H + h0 + tx;
+    *o = accumulate ? *o + tile[tx][ty + 8 * i] : tile[tx][ty + 8 * i];
+  }
 }
 
 cudaError_t launch_router_wgrad(const moe_config& c, const void* x, const int32_t* sel_offsets,
                                 const int32_t* sel_tokens, const float* dlogits, float* dW_r,
-                                uint8_t* scratch, cudaStream_t s) {
+                                uint8_t* scratch, cudaStream_t s, bool accumulate) {
   if (router_on_tensor_cores(c)) {
     // tensor cores: dW_r^T chunk sums x^T . dlogits over chunks of tokens, then
     // the chunks added in order (every x row read once)
-    if (c.T == 0) return cudaMemsetAsync(dW_r, 0, (size_t)c.E * c.H * 4, s);
+    if (c.T == 0)
+      return accumulate ? cudaSuccess : cudaMemsetAsync(dW_r, 0, (size_t)c.E * c.H * 4, s);
     uint8_t* base = scratch + router_split_offset(c);
     const long long Tp = ((long long)c.T + 63) / 64 * 64;
     auto D3 = reinterpret_cast<__nv_bfloat16*>(base);
@@ -528,7 +533,8 @@ cudaError_t launch_router_wgrad(const moe_config& c, const void* x, const int32_
     err = launch_router_wgrad_tc(c, x, D3, Tp, P, chunk,
                                  reinterpret_cast<int32_t*>(scratch + kScratchStatus), s);
     if (err != cudaSuccess) return err;
-    sum_chunks_transpose_kernel<<<dim3(c.H / 32, c.E / 32), 256, 0, s>>>(P, dW_r, NG, c.H, c.E);
+    sum_chunks_transpose_kernel<<<dim3(c.H / 32, c.E / 32), 256, 0, s>>>(P, dW_r, NG, c.H, c.E,
+                                                                         accumulate ? 1 : 0);
     return cudaGetLastError();
   }
   auto xb = static_cast<const __nv_bfloat16*>(x);
@@ -536,11 +542,11 @@ cudaError_t launch_router_wgrad(const moe_config& c, const void* x, const int32_
   if ((long long)c.E * ((c.H + 255) / 256) < 2LL * num_sms()) {
     dim3 grid(c.E, (c.H + 127) / 128);
     router_wgrad_kernel<4><<<grid, 512, 0, s>>>(xb, sel_offsets, sel_tokens, dlogits, dW_r, c.H,
-                                                c.E);
+                                                c.E, c.T, accumulate ? 1 : 0);
   } else {
     dim3 grid(c.E, (c.H + 255) / 256);
     router_wgrad_kernel<8><<<grid, 512, 0, s>>>(xb, sel_offsets, sel_tokens, dlogits, dW_r, c.H,
-                                                c.E);
+                                                c.E, c.T, accumulate ? 1 : 0);
   }
   return cudaGetLastError();
 }

@@ -16,6 +16,7 @@ constexpr int kChunkTokens = 256;              // tokens per dispatch-map chunk
 
 // Scratch layout (bytes from the start of the caller's scratch buffer).
 constexpr size_t kScratchStatus = 0;           // int32 device status word
+constexpr size_t kScratchAuxTicket = 64;       // uint32 arrival counter of the aux-loss blocks
 constexpr size_t kScratchPadPrefix = 256;      // int32 [kMaxGroups+1]
 constexpr size_t kScratchHist = 4096;          // int32 [n_chunks][E]
 

@@ -40,9 +40,25 @@ cudaError_t launch_permute_bwd(const moe_config& c, const void* dX_perm, const i
                                const int32_t* offsets, const int32_t* idx, const float* dlogits,
                                const float* W_r, void* dx, cudaStream_t s);
 
+// dW_r (= or, with accumulate, +=) sum over tokens of dlogits[t,e] x[t,:]; with
+// sel_offsets == sel_tokens == NULL every token counts for every expert
+// (dense dlogits), else only the tokens that selected e.
 cudaError_t launch_router_wgrad(const moe_config& c, const void* x, const int32_t* sel_offsets,
                                 const int32_t* sel_tokens, const float* dlogits, float* dW_r,
-                                uint8_t* scratch, cudaStream_t s);
+                                uint8_t* scratch, cudaStream_t s, bool accumulate = false);
+
+// Load-balancing loss: statistics, loss and bias update in one launch; its
+// gradient into dlogits_aux, dx and dW_r.
+cudaError_t launch_route_aux(const moe_config& c, const float* logits, const float* bias,
+                             const int32_t* idx, float coeff, float rate, int32_t* counts,
+                             float* p_mean, float* loss, float* bias_out, uint8_t* scratch,
+                             cudaStream_t s);
+cudaError_t launch_route_aux_bwd(const moe_config& c, const void* x, const float* logits,
+                                 const float* bias, const float* W_r, const int32_t* counts,
+                                 float coeff, float dloss, float* dl, void* dx, float* dW_r,
+                                 uint8_t* scratch, cudaStream_t s);
+int64_t aux_partial_bytes(const moe_config& c);    // the aux-loss region of scratch
+int64_t aux_partial_offset(const moe_config& c);   // its byte offset in scratch
 
 // FP8 block quantisation (E4M3 values with power-of-two scales, stored as bf16).
 cudaError_t launch_quant_tiles(const void* W, void* Wq, int G, int rows, int cols, cudaStream_t s);

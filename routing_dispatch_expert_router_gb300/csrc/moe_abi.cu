@@ -48,8 +48,12 @@ int64_t permute_scratch_bytes(const moe_config& c) {
 
 int64_t router_split_offset(const moe_config& c) { return permute_scratch_bytes(c); }
 
-static int64_t base_scratch_bytes(const moe_config& c) {
+int64_t aux_partial_offset(const moe_config& c) {
   return permute_scratch_bytes(c) + router_split_bytes(c);
+}
+
+static int64_t base_scratch_bytes(const moe_config& c) {
+  return aux_partial_offset(c) + aux_partial_bytes(c);
 }
 
 int64_t scratch_bytes(const moe_config& c) {
@@ -190,6 +194,34 @@ moe_status moe_route_replay(const moe_config* cfg, const void* x, const float* W
   if (cfg->T == 0) return MOE_OK;
   MOE_CUDA(launch_route_replay(*cfg, x, W_r, bias, idx, logits, w,
                                static_cast<uint8_t*>(scratch), (cudaStream_t)stream));
+  return MOE_OK;
+}
+
+moe_status moe_route_aux(const moe_config* cfg, const float* logits, const float* bias,
+                         const int32_t* idx, float coeff, float bias_rate, int32_t* sel_counts,
+                         float* p_mean, float* loss, float* bias_out, void* scratch,
+                         void* stream) {
+  MOE_TRY(check_config(cfg));
+  MOE_REQUIRE(tok4(cfg, logits) && tok4(cfg, idx) && al4(sel_counts) && al4(p_mean) && al4(loss));
+  MOE_REQUIRE((bias == nullptr || al4(bias)) && (bias_out == nullptr || al4(bias_out)));
+  MOE_REQUIRE(isfinite(coeff) && isfinite(bias_rate) && al16(scratch));
+  MOE_CUDA(launch_route_aux(*cfg, logits, bias, idx, coeff, bias_rate, sel_counts, p_mean, loss,
+                            bias_out, static_cast<uint8_t*>(scratch), (cudaStream_t)stream));
+  return MOE_OK;
+}
+
+moe_status moe_route_aux_bwd(const moe_config* cfg, const void* x, const float* logits,
+                             const float* bias, const float* W_r, const int32_t* sel_counts,
+                             float coeff, float dloss, float* dlogits_aux, void* dx, float* dW_r,
+                             void* scratch, void* stream) {
+  MOE_TRY(check_config(cfg));
+  MOE_REQUIRE(tok16(cfg, x) && tok4(cfg, logits) && al16(W_r) && al4(sel_counts));
+  MOE_REQUIRE(tok4(cfg, dlogits_aux) && tok16(cfg, dx) && al16(dW_r));
+  MOE_REQUIRE((bias == nullptr || al4(bias)) && isfinite(coeff) && isfinite(dloss));
+  MOE_REQUIRE(al16(scratch));
+  MOE_CUDA(launch_route_aux_bwd(*cfg, x, logits, bias, W_r, sel_counts, coeff, dloss,
+                                dlogits_aux, dx, dW_r, static_cast<uint8_t*>(scratch),
+                                (cudaStream_t)stream));
   return MOE_OK;
 }
 
