@@ -203,7 +203,11 @@ MOE_API moe_status moe_route_aux(const moe_config* cfg, const float* logits, con
  *   dW_r [E,H] fp32  += dlogits_aux^T . x   (every token, every expert).
  * Call it after moe_layer_bwd (or moe_permute_bwd and moe_router_wgrad) with
  * the same dx and dW_r: the loss's gradient reaches x and W_r through the
- * logits like the layer's own. x, logits and bias as given to moe_route. */
+ * logits like the layer's own. x, logits and bias as given to moe_route.
+ * For E a multiple of 128 the dx product runs on the tensor cores from the
+ * hi + mid bf16 parts of dlogits_aux and W_r (three cross products; what they
+ * leave out is about 2^-16 of sum |dl| |W_r|, far below dx's bf16 rounding),
+ * otherwise on the CUDA cores in fp32. */
 MOE_API moe_status moe_route_aux_bwd(const moe_config* cfg, const void* x, const float* logits,
                                      const float* bias, const float* W_r,
                                      const int32_t* sel_counts, float coeff, float dloss,

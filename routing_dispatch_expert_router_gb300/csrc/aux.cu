@@ -16,9 +16,10 @@
 // and the selections in shared memory, and writes its partial sums; the last
 // block to finish adds the partials in a fixed order (deterministic), writes
 // counts, P and the loss, and applies the bias update.
-// Backward: dlogits of the loss (dense [T,E]), then dx += dl W_r on the CUDA
-// cores (fp32, one bf16 rounding) and dW_r += dl^T x through the router
-// weight-gradient path.
+// Backward: dlogits of the loss (dense [T,E]), then dx += dl W_r (tensor
+// cores from the hi + mid bf16 parts of both operands when E % 128 == 0, else
+// the CUDA cores in fp32; one bf16 rounding) and dW_r += dl^T x through the
+// router weight-gradient path.
 #include <math.h>
 
 #include "common.cuh"
@@ -310,6 +311,55 @@ router_dx_dense_kernel(const float* __restrict__ dl, const float* __restrict__ W
   }
 }
 
+// A3[t, :] = [hi(dl[t,:]) | hi(dl[t,:]) | mid(dl[t,:])], 3E bf16 columns, with
+// hi = bf16(v) and mid = bf16(v - hi); one thread per 8 consecutive experts.
+__global__ void __launch_bounds__(256)
+aux_split_dl_kernel(const float* __restrict__ dl, __nv_bfloat16* __restrict__ A3, int T, int E) {
+  const int per_row = E >> 3;
+  const long long n = (long long)T * per_row;
+  for (long long v = (long long)blockIdx.x * blockDim.x + threadIdx.x; v < n;
+       v += (long long)gridDim.x * blockDim.x) {
+    const int t = (int)(v / per_row), e = (int)(v - (long long)t * per_row) << 3;
+    const float4* src = reinterpret_cast<const float4*>(dl + (size_t)t * E + e);
+    const float4 a = __ldg(src), b = __ldg(src + 1);
+    const float f[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+    float hi[8], mid[8];
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      hi[q] = __bfloat162float(__float2bfloat16_rn(f[q]));
+      mid[q] = f[q] - hi[q];
+    }
+    const uint4 h = pack8(hi);
+    uint4* row = reinterpret_cast<uint4*>(A3 + (size_t)t * 3 * E + e);
+    row[0] = h;
+    row[E / 8] = h;                                // + E columns
+    row[E / 4] = pack8(mid);                       // + 2E columns
+  }
+}
+
+// B3[h, :] = [hi(W_r[:,h]) | mid(W_r[:,h]) | hi(W_r[:,h])], 3E bf16 columns
+// (W_r transposed through a 32 x 32 shared tile).
+__global__ void __launch_bounds__(256)
+aux_split_wr_kernel(const float* __restrict__ W_r, __nv_bfloat16* __restrict__ B3, int E, int H) {
+  __shared__ float tile[32][33];
+  const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
+  const int h0 = blockIdx.x * 32, e0 = blockIdx.y * 32;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) tile[ty + 8 * i][tx] = W_r[(size_t)(e0 + ty + 8 * i) * H + h0 + tx];
+  __syncthreads();
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int h = h0 + ty + 8 * i;
+    const float w = tile[tx][ty + 8 * i];
+    const __nv_bfloat16 hi = __float2bfloat16_rn(w);
+    const __nv_bfloat16 mid = __float2bfloat16_rn(w - __bfloat162float(hi));
+    __nv_bfloat16* row = B3 + (size_t)h * 3 * E + e0 + tx;
+    row[0] = hi;
+    row[E] = mid;
+    row[2 * E] = hi;
+  }
+}
+
 static int experts_per_lane(int E) { return E <= 32 ? 1 : E <= 64 ? 2 : E <= 128 ? 4 : 8; }
 
 cudaError_t launch_route_aux(const moe_config& c, const float* logits, const float* bias,
@@ -345,9 +395,26 @@ cudaError_t launch_route_aux_bwd(const moe_config& c, const void* x, const float
                                      dl);
   cudaError_t err = cudaGetLastError();
   if (err != cudaSuccess) return err;
-  router_dx_dense_kernel<<<dim3((c.T + kDxTokens - 1) / kDxTokens, c.H / kDxCols), 256, 0, s>>>(
-      dl, W_r, static_cast<__nv_bfloat16*>(dx), c.T, c.H, c.E);
-  err = cudaGetLastError();
+  if (router_on_tensor_cores(c)) {
+    // dx on the tensor cores: dl and W_r each as hi + mid bf16 parts; the three
+    // products hi.hi + hi.mid + mid.hi (what they leave out is ~2^-16 of
+    // |dl| |W_r|, far below the bf16 rounding of dx) as one K = 3E GEMM
+    uint8_t* base = scratch + router_split_offset(c);
+    auto A3 = reinterpret_cast<__nv_bfloat16*>(base);
+    auto B3 = reinterpret_cast<__nv_bfloat16*>(base + ((int64_t)c.T * 3 * c.E * 2 + 255) / 256 * 256);
+    long long blocks = ((long long)c.T * (c.E / 8) + 255) / 256;
+    if (blocks > (long long)num_sms() * 16) blocks = (long long)num_sms() * 16;
+    aux_split_dl_kernel<<<(int)blocks, 256, 0, s>>>(dl, A3, c.T, c.E);
+    aux_split_wr_kernel<<<dim3(c.H / 32, c.E / 32), 256, 0, s>>>(W_r, B3, c.E, c.H);
+    err = cudaGetLastError();
+    if (err != cudaSuccess) return err;
+    err = launch_router_dx_tc(c, A3, B3, 3 * c.E, dx,
+                              reinterpret_cast<int32_t*>(scratch + kScratchStatus), s);
+  } else {
+    router_dx_dense_kernel<<<dim3((c.T + kDxTokens - 1) / kDxTokens, c.H / kDxCols), 256, 0,
+                             s>>>(dl, W_r, static_cast<__nv_bfloat16*>(dx), c.T, c.H, c.E);
+    err = cudaGetLastError();
+  }
   if (err != cudaSuccess) return err;
   // every token contributes to every expert's row of dW_r
   return launch_router_wgrad(c, x, nullptr, nullptr, dl, dW_r, scratch, s, true);

@@ -44,7 +44,7 @@ constexpr int kStageBytes = 3 * kBoxBytes;       // output staging per epilogue 
 constexpr long long kWaitBudget = 4000000000LL;   // clock64 cycles (~2 s)
 
 enum Epi : int { kEpiSwigluFwd = 0, kEpiStore = 1, kEpiSwigluBwd = 2, kEpiWgrad = 3,
-                 kEpiStoreF32 = 4, kEpiDgradRouter = 5 };
+                 kEpiStoreF32 = 4, kEpiDgradRouter = 5, kEpiAddBf16 = 6 };
 
 struct Params {
   int kgrouped;               // 0: row-grouped, 1: K-grouped
@@ -61,8 +61,8 @@ struct Params {
   long long out_gstride;      // K-grouped: elements between groups' outputs
   __nv_bfloat16* out2;        // SwiGLU-fwd: h
   long long ldo2;
-  const __nv_bfloat16* aux;   // SwiGLU-bwd: GU
-  long long ldaux;
+  const __nv_bfloat16* aux;   // SwiGLU-bwd: GU; add-to-output (kEpiAddBf16): the output
+  long long ldaux;            // itself, read before it is overwritten
   int32_t* status;
   int dense_rows;             // > 0: one group of this many rows at row 0 (no counts/offsets),
                               // or, with chunk_rows > 0, that many rows cut into groups of
@@ -223,7 +223,7 @@ __device__ __forceinline__ void epilogue_tile(const Params& p, const CUtensorMap
     if (t >= 0) rd = p.dlogits[(long long)t * p.router_E + g];
     rw = p.W_r + (long long)g * p.N + f0;
   }
-  if (EPI == kEpiStore || EPI == kEpiWgrad || EPI == kEpiDgradRouter) {
+  if (EPI == kEpiStore || EPI == kEpiWgrad || EPI == kEpiDgradRouter || EPI == kEpiAddBf16) {
     // plain bf16 output in 32 x 64 boxes: 128-byte rows (128-byte swizzle), so
     // every store fills whole 128-byte lines; 64 accumulator columns per
     // tensor-memory wait
@@ -252,6 +252,22 @@ __device__ __forceinline__ void epilogue_tile(const Params& p, const CUtensorMap
           r1[4 * v + 1] = __float_as_uint(fmaf(rd, w5.y, __uint_as_float(r1[4 * v + 1])));
           r1[4 * v + 2] = __float_as_uint(fmaf(rd, w5.z, __uint_as_float(r1[4 * v + 2])));
           r1[4 * v + 3] = __float_as_uint(fmaf(rd, w5.w, __uint_as_float(r1[4 * v + 3])));
+        }
+      }
+      if (EPI == kEpiAddBf16 && row0 + lane < p.dense_rows) {
+        // fp32 accumulator + the bf16 value in place, rounded to bf16 once
+        const uint4* src =
+            reinterpret_cast<const uint4*>(p.aux + (long long)(row0 + lane) * p.ldaux + f0 + c);
+#pragma unroll
+        for (int v = 0; v < 4; ++v) {
+          float f[8], f2[8];
+          unpack8(__ldg(src + v), f);
+          unpack8(__ldg(src + 4 + v), f2);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            r0[8 * v + i] = __float_as_uint(__uint_as_float(r0[8 * v + i]) + f[i]);
+            r1[8 * v + i] = __float_as_uint(__uint_as_float(r1[8 * v + i]) + f2[i]);
+          }
         }
       }
       uint4 o[4], o2[4];
@@ -1326,6 +1342,32 @@ cudaError_t launch_router_wgrad_tc(const moe_config& c, const void* x, const voi
   p.N = c.E;
   p.status = status;
   return run<kEpiStoreF32, 128, 1, 1, 3>(a, b, oc, oc, p, s);
+}
+
+// dx[T, H] (bf16, in place) += A3 . B3^T on the tensor cores, one dense group
+// of T rows (rows past T read zeros and are not stored): A3 [T, K3] and B3
+// [H, K3] bf16, both K-major. The epilogue adds the fp32 accumulator to the
+// bf16 value of dx it replaces and rounds once.
+cudaError_t launch_router_dx_tc(const moe_config& c, const void* A3, const void* B3, int K3,
+                                void* dx, int32_t* status, cudaStream_t s) {
+  const int bn = (c.H % 256 == 0) ? 256 : 128;
+  CUtensorMap a, b, oc;
+  if (!make_map(&a, A3, K3, c.T, 128) || !make_map(&b, B3, K3, c.H, bn) ||
+      !make_out_map_w64(&oc, dx, c.H, c.T))
+    return cudaErrorInvalidValue;
+  Params p{};
+  p.G = 1;
+  p.dense_rows = c.T;
+  p.N = c.H;
+  p.K = K3;
+  p.b_rows = c.H;
+  p.out = static_cast<__nv_bfloat16*>(dx);
+  p.ldo = c.H;
+  p.aux = static_cast<const __nv_bfloat16*>(dx);
+  p.ldaux = c.H;
+  p.status = status;
+  return bn == 256 ? run<kEpiAddBf16, 256, 0, 0, 4>(a, b, oc, oc, p, s)
+                   : run<kEpiAddBf16, 128, 0, 0, 6>(a, b, oc, oc, p, s);
 }
 
 }  // namespace moe

@@ -86,6 +86,9 @@ cudaError_t launch_router_logits_tc(const moe_config& c, const void* x, const vo
 cudaError_t launch_router_wgrad_tc(const moe_config& c, const void* x, const void* D3,
                                    long long Tp, float* P, int chunk, int32_t* status,
                                    cudaStream_t s);
+// dx [T,H] bf16 += A3 [T,K3] . B3 [H,K3]^T (bf16 operands, K-major), on the tensor cores.
+cudaError_t launch_router_dx_tc(const moe_config& c, const void* A3, const void* B3, int K3,
+                                void* dx, int32_t* status, cudaStream_t s);
 bool router_on_tensor_cores(const moe_config& c);
 // tensor-core router weight gradient: tokens per chunk (<= 271 chunks), and
 // the byte offset of the chunk partial sums after the split dlogits in the
@@ -93,6 +96,7 @@ bool router_on_tensor_cores(const moe_config& c);
 int router_wgrad_chunk(const moe_config& c);
 int64_t router_wgrad_split_bytes(const moe_config& c);
 int64_t router_split_bytes(const moe_config& c);   // the router region of scratch
+int64_t aux_dx_split_bytes(const moe_config& c);   // the loss's split dx operands in it
 int64_t router_split_offset(const moe_config& c);   // byte offset of the split in scratch
 int64_t permute_scratch_bytes(const moe_config& c); // scratch the dispatch needs
 

@@ -216,7 +216,7 @@ moe_status moe_route_aux_bwd(const moe_config* cfg, const void* x, const float* 
                              void* scratch, void* stream) {
   MOE_TRY(check_config(cfg));
   MOE_REQUIRE(tok16(cfg, x) && tok4(cfg, logits) && al16(W_r) && al4(sel_counts));
-  MOE_REQUIRE(tok4(cfg, dlogits_aux) && tok16(cfg, dx) && al16(dW_r));
+  MOE_REQUIRE(tok16(cfg, dlogits_aux) && tok16(cfg, dx) && al16(dW_r));
   MOE_REQUIRE((bias == nullptr || al4(bias)) && isfinite(coeff) && isfinite(dloss));
   MOE_REQUIRE(al16(scratch));
   MOE_CUDA(launch_route_aux_bwd(*cfg, x, logits, bias, W_r, sel_counts, coeff, dloss,

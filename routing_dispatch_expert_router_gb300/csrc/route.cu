@@ -735,14 +735,22 @@ int64_t router_wgrad_split_bytes(const moe_config& c) {
   return (3 * Tp * c.E * 2 + 255) / 256 * 256;
 }
 
-// The router region of scratch: the forward's split W_r, or the backward's
-// split dlogits and the chunk partial sums of dW_r^T, whichever is larger.
+// The router region of scratch: the forward's split W_r, the backward's split
+// dlogits and the chunk partial sums of dW_r^T, or the load-balancing loss's
+// split dx operands ([T, 3E] and [H, 3E] bf16), whichever is largest.
 int64_t router_split_bytes(const moe_config& c) {
   if (!router_on_tensor_cores(c)) return 0;
   const int64_t fwd = ((int64_t)c.E * 3 * c.H * 2 + 255) / 256 * 256;
   const int64_t chunks = (c.T + router_wgrad_chunk(c) - 1) / router_wgrad_chunk(c);
   const int64_t bwd = router_wgrad_split_bytes(c) + (chunks * c.H * c.E * 4 + 255) / 256 * 256;
-  return fwd > bwd ? fwd : bwd;
+  const int64_t aux = aux_dx_split_bytes(c);
+  const int64_t m = fwd > bwd ? fwd : bwd;
+  return m > aux ? m : aux;
+}
+
+int64_t aux_dx_split_bytes(const moe_config& c) {
+  return ((int64_t)c.T * 3 * c.E * 2 + 255) / 256 * 256 +
+         ((int64_t)c.H * 3 * c.E * 2 + 255) / 256 * 256;
 }
 
 // Router Replay: the weights of recorded experts idx [T,k] (in that order)

@@ -4,7 +4,7 @@
 
 For every workload (default: mixtral) the route, dispatch, combine, combine
 backward, route backward, dispatch backward and router weight-gradient entry
-points run once as warm-up and then N times (default 20), each timed with CUDA
+points, and the load-balancing loss (forward and backward), run once as warm-up and then N times (default 20), each timed with CUDA
 events after a 512 MB write that evicts L2. Prints the median time, the
 stage's algorithmic bytes (every tensor read or written once) and the rate
 against the measured copy bandwidth. The grouped GEMMs are timed by bench.py.
@@ -62,6 +62,9 @@ def run(name: str, reps: int, flush: bool, peak: float, fl: torch.Tensor) -> Non
     dl = torch.empty(T, E, device=dev)
     dX_perm = torch.randn(R, H, device=dev, generator=g).to(torch.bfloat16)
     dWr = torch.empty(E, H, device=dev)
+    sel_cnt, p_mean, loss = i32(E), torch.empty(E, device=dev), torch.empty(1, device=dev)
+    bias_out = torch.empty(E, device=dev)
+    dl_aux = torch.empty(T, E, device=dev)
     stages = {
         "route": lambda: B.moe_route(cfg, x, Wr, bias, logits, idx, w, sc),
         "permute": lambda: B.moe_permute(cfg, x, idx, counts, offsets, row_of, token_of, sel_off,
@@ -72,6 +75,10 @@ def run(name: str, reps: int, flush: bool, peak: float, fl: torch.Tensor) -> Non
         "route_bwd": lambda: B.moe_route_bwd(cfg, logits, idx, w, dw, dl),
         "permute_bwd": lambda: B.moe_permute_bwd(cfg, dX_perm, row_of, offsets, idx, dl, Wr, dx),
         "router_wgrad": lambda: B.moe_router_wgrad(cfg, x, sel_off, sel_tok, dl, dWr, sc),
+        "route_aux": lambda: B.moe_route_aux(cfg, logits, bias, idx, 0.01, 1e-3, sel_cnt, p_mean,
+                                             loss, bias_out, sc),
+        "route_aux_bwd": lambda: B.moe_route_aux_bwd(cfg, x, logits, bias, Wr, sel_cnt, 0.01, 1.0,
+                                                     dl_aux, dx, dWr, sc),
     }
     for f in stages.values():
         f()
@@ -89,6 +96,8 @@ def run(name: str, reps: int, flush: bool, peak: float, fl: torch.Tensor) -> Non
         "route_bwd": T * E * 8 + maps,
         "permute_bwd": rows * H * bf + T * H * bf + maps,
         "router_wgrad": T * H * bf + E * H * 4 + T * E * 4,
+        "route_aux": T * E * 4 + T * k * 4,
+        "route_aux_bwd": 2 * T * E * 4 + 3 * T * H * bf + 3 * E * H * 4,
     }
     print(f"== {name} T={T} H={H} E={E} k={k} S={S} A={A} P={P} "
           f"status={B.moe_last_device_status(sc)} cold_l2={flush}")
