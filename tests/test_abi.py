@@ -93,6 +93,28 @@ def test_null_and_misaligned_pointers_rejected_before_launch():
     assert rc == 1
 
 
+def test_aux_loss_entry_points_reject_bad_arguments_before_launch():
+    """Host-side checks of the load-balancing loss calls (no device work):
+    a NULL counts output, a dlogits buffer off 16 bytes, a non-finite
+    coefficient or gradient scale."""
+    cfg = B.config(TINY)
+    lib = B.lib()
+    vp, f = ctypes.c_void_p, ctypes.c_float
+    ok = vp(4096)
+    rc = lib.moe_route_aux(ctypes.byref(cfg), ok, vp(None), ok, f(0.01), f(1e-3), vp(None), ok,
+                           ok, vp(None), ok, vp(None))
+    assert rc == 1
+    rc = lib.moe_route_aux(ctypes.byref(cfg), ok, vp(None), ok, f(float("nan")), f(1e-3), ok, ok,
+                           ok, vp(None), ok, vp(None))
+    assert rc == 1
+    rc = lib.moe_route_aux_bwd(ctypes.byref(cfg), ok, ok, vp(None), ok, ok, f(0.01), f(1.0),
+                               vp(4096 + 4), ok, ok, ok, vp(None))
+    assert rc == 1
+    rc = lib.moe_route_aux_bwd(ctypes.byref(cfg), ok, ok, vp(None), ok, ok, f(0.01),
+                               f(float("inf")), ok, ok, ok, ok, vp(None))
+    assert rc == 1
+
+
 def test_status_strings():
     for code in range(7):
         assert B.status_string(code)
