@@ -252,10 +252,11 @@ route_aux_dlogits_kernel(const float* __restrict__ logits, const float* __restri
 
 // dx[t, h] = bf16(dx[t, h] + sum_e dl[t, e] W_r[e, h]), e in increasing order.
 // Block: 64 tokens x 128 columns; warp w takes tokens 8w..8w+7, lane l columns
-// 4l..4l+3. Experts in chunks of 32: dl^T and W_r chunks staged in shared
-// memory, every thread 8 x 4 fp32 accumulators.
-constexpr int kDxTokens = 64, kDxCols = 128, kDxChunk = 32;
+// 4l..4l+3. Experts in chunks of kDxChunk (8 when E <= 8, else 32): dl^T and
+// W_r chunks staged in shared memory, every thread 8 x 4 fp32 accumulators.
+constexpr int kDxTokens = 64, kDxCols = 128;
 
+template <int kDxChunk>
 __global__ void __launch_bounds__(256)
 router_dx_dense_kernel(const float* __restrict__ dl, const float* __restrict__ W_r,
                        __nv_bfloat16* __restrict__ dx, int T, int H, int E) {
@@ -411,8 +412,12 @@ cudaError_t launch_route_aux_bwd(const moe_config& c, const void* x, const float
     err = launch_router_dx_tc(c, A3, B3, 3 * c.E, dx,
                               reinterpret_cast<int32_t*>(scratch + kScratchStatus), s);
   } else {
-    router_dx_dense_kernel<<<dim3((c.T + kDxTokens - 1) / kDxTokens, c.H / kDxCols), 256, 0,
-                             s>>>(dl, W_r, static_cast<__nv_bfloat16*>(dx), c.T, c.H, c.E);
+    const dim3 grid((c.T + kDxTokens - 1) / kDxTokens, c.H / kDxCols);
+    auto dxp = static_cast<__nv_bfloat16*>(dx);
+    if (c.E <= 8)
+      router_dx_dense_kernel<8><<<grid, 256, 0, s>>>(dl, W_r, dxp, c.T, c.H, c.E);
+    else
+      router_dx_dense_kernel<32><<<grid, 256, 0, s>>>(dl, W_r, dxp, c.T, c.H, c.E);
     err = cudaGetLastError();
   }
   if (err != cudaSuccess) return err;
