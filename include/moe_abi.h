@@ -188,7 +188,9 @@ MOE_API moe_status moe_route_replay(const moe_config* cfg, const void* x, const 
  * Deterministic (fixed summation order). An index outside [0, E) records
  * MOE_ERR_DEVICE_CHECK and is not counted. T == 0 gives zeros (bias_out =
  * bias). scratch: moe_sizes.scratch_bytes bytes, zero-filled once (the
- * launch keeps an arrival counter in it and leaves it zero). */
+ * launch keeps an arrival counter in it and leaves it zero). Returns
+ * MOE_ERR_INVALID_ARG for a NULL or misaligned pointer (logits and idx may be
+ * NULL when T == 0) or a non-finite coeff or bias_rate. */
 MOE_API moe_status moe_route_aux(const moe_config* cfg, const float* logits, const float* bias,
                                  const int32_t* idx, float coeff, float bias_rate,
                                  int32_t* sel_counts, float* p_mean, float* loss,
@@ -207,7 +209,10 @@ MOE_API moe_status moe_route_aux(const moe_config* cfg, const float* logits, con
  * For E a multiple of 128 the dx product runs on the tensor cores from the
  * hi + mid bf16 parts of dlogits_aux and W_r (three cross products; what they
  * leave out is about 2^-16 of sum |dl| |W_r|, far below dx's bf16 rounding),
- * otherwise on the CUDA cores in fp32. */
+ * otherwise on the CUDA cores in fp32. dlogits_aux and dx 16-byte aligned;
+ * scratch: moe_sizes.scratch_bytes bytes (the split operands use its router
+ * region). Returns MOE_ERR_INVALID_ARG for a NULL or misaligned pointer or a
+ * non-finite coeff or dloss; T == 0 launches nothing. */
 MOE_API moe_status moe_route_aux_bwd(const moe_config* cfg, const void* x, const float* logits,
                                      const float* bias, const float* W_r,
                                      const int32_t* sel_counts, float coeff, float dloss,
