@@ -1,19 +1,22 @@
 """Benchmark of one MoE layer step (forward + backward) on GB300.
 
-    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload mixtral]
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload dsv3_fp8]
                     [--impl ours|reference]
 
 A step is one pass of the whole layer over one batch of synthetic tokens:
 route, permute, grouped SwiGLU FFN, unpermute, and the backward of all of it
-(dx, dW_r, dW13, dW2). The default workload is the Mixtral-style layer
-(T=4096, H=4096, E=8, top-2 softmax, d_ff=14336, bf16). Prints one JSON line.
+(dx, dW_r, dW13, dW2). The default workload is the largest of the five layer
+shapes, the FP8 DeepSeek-V3-shaped layer (T=16384, H=7168, E=256, top-8
+group-limited sigmoid routing, d_ff=2048, E4M3 operands with power-of-two
+block scales, capacity factor 1.25). Prints one JSON line.
 
   value      tokens/s of fwd+bwd with inputs resident in HBM (CUDA events)
   e2e        the same through the public layer calls with host buffers: each
              step copies x and dY from pinned host memory and reads out and dx
              back inside the timed region
   roofline   the grouped-GEMM kernel family (the dominant kernel) against the
-             measured dense bf16 tensor peak
+             measured dense tensor peak of its operand type (FP8: twice the
+             measured bf16 burst figure, the nominal FP8:bf16 rate ratio)
   cpu_baseline  the CPU oracle timed on a bounded sample of the same workload
 
 --impl reference times the CPU oracle instead (the reference arm of this
@@ -45,7 +48,7 @@ def parse():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--workload", default="mixtral",
+    ap.add_argument("--workload", default="dsv3_fp8",
                     choices=sorted(W.SHAPES) + sorted(W.PROFILE_SHAPES))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--seed", type=int, default=0)
@@ -87,7 +90,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", "50"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.thr = threading.Thread(target=self._read, daemon=True)
             self.thr.start()
@@ -126,38 +129,56 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
+GEMM_SOURCES = ("grouped_gemm.cu", "grouped_gemm_fp8.cu", "gemm_common.cuh", "ptx.cuh",
+                "fp8_layout.cuh")
+
+
+def gemm_sources_sha256() -> str:
+    import hashlib
+    h = hashlib.sha256()
+    for name in GEMM_SOURCES:
+        path = os.path.join(ROOT, "routing_dispatch_expert_router_gb300", "csrc", name)
+        if os.path.exists(path):
+            with open(path, "rb") as f:
+                h.update(f.read())
+    return h.hexdigest()
+
+
 def gemm_traffic(workload: str):
     """DRAM bytes per step of the grouped-GEMM launches from a committed ncu
-    capture, or None when the GEMM source changed since it was taken."""
-    import hashlib
+    capture, or None when a GEMM source changed since it was taken."""
     path = os.path.join(ROOT, "profiles", "gemm_traffic.json")
-    src = os.path.join(ROOT, "routing_dispatch_expert_router_gb300", "csrc", "grouped_gemm.cu")
     if not os.path.exists(path):
         return None
     with open(path) as f:
         d = json.load(f)
-    with open(src, "rb") as f:
-        h = hashlib.sha256(f.read()).hexdigest()
-    if d.get("grouped_gemm_cu_sha256") != h or d.get("workload") != workload:
+    if d.get("gemm_sources_sha256") != gemm_sources_sha256() or d.get("workload") != workload:
         return None
     return d.get("dram_bytes_per_step")
 
 
-def gemm_flops(shape, counts) -> tuple:
-    """Algorithmic flops of the grouped GEMMs of one step (kept rows only)."""
+def gemm_flops(shape, counts) -> float:
+    """Algorithmic flops of one pass of the grouped GEMMs (kept rows only): the
+    forward (FC1 + FC2), the data gradients and the weight gradients each do
+    this much."""
     rows = float(sum(counts))        # routed kept rows + shared rows (T each)
-    fwd = 2.0 * rows * shape.H * 2 * shape.F + 2.0 * rows * shape.F * shape.H
-    bwd = 2.0 * fwd
-    return fwd, bwd
+    return 2.0 * rows * shape.H * 2 * shape.F + 2.0 * rows * shape.F * shape.H
 
 
-def stage_table(shape, cfg, f, stage_ms, hbm_gbs, fl_fwd, fl_bwd, tc_peak):
+STAGES = ("route", "permute", "quantize_weights", "grouped_ffn_fwd", "unpermute",
+          "unpermute_bwd", "route_bwd", "grouped_ffn_dgrad", "grouped_ffn_wgrad", "permute_bwd",
+          "router_wgrad")
+
+
+def stage_table(shape, f, stage_ms, hbm_gbs, fl, tc_peak, bf16_peak):
     """Per-stage device time, algorithmic bytes (or flops) and roofline fraction.
 
     Bytes count each tensor a stage must read or write once (bf16 rows 2 B per
-    element, fp32 4 B, int32 maps 4 B): A kept routed assignments, S*T shared
-    rows, P zero padding rows of the permuted buffers."""
-    T, H, E, k, S = shape.T, shape.H, shape.E, shape.k, shape.n_shared
+    element, fp32 4 B, int32 maps 4 B, E4M3 1 B plus 1/32 B of scale atoms): A
+    kept routed assignments, S*T shared rows, P zero padding rows of the
+    permuted buffers. GEMM stages count flops against the tensor peak of their
+    operand type (FP8 forward and data gradients; weight gradients bf16)."""
+    T, H, E, k, S, F = shape.T, shape.H, shape.E, shape.k, shape.n_shared, shape.F
     counts = f["counts"].cpu().tolist()
     offsets = f["offsets"].cpu().tolist()
     G = E + S
@@ -166,25 +187,32 @@ def stage_table(shape, cfg, f, stage_ms, hbm_gbs, fl_fwd, fl_bwd, tc_peak):
     P = offsets[G] - sum(counts)         # padding rows
     bf = 2
     maps = T * k * 4 * 3                 # idx / row_of / w sized reads or writes
+    fp8 = shape.dtype == W.DT_FP8
+    wbytes = G * 3 * H * F
     work = [
         ("route", T * H * bf + E * H * 4 + T * E * 4 + 2 * T * k * 4, "router logits + top-k"),
         ("permute", T * H * bf + (rows + P) * H * bf + maps, "hist + rank + row scatter"),
-        ("grouped_ffn_fwd", fl_fwd, "FC1+SwiGLU, FC2 (tcgen05)"),
+        ("quantize_weights", (wbytes * bf + wbytes + 2 * wbytes // 32) if fp8 else 0,
+         "E4M3 weights + UE8M0 scale atoms (FP8 only)"),
+        ("grouped_ffn_fwd", fl, "FC1+SwiGLU, FC2 (tcgen05" + (" kind::mxf8f6f4)" if fp8 else ")")),
         ("unpermute", rows * H * bf + T * H * bf + maps, "gather-scale-reduce"),
         ("unpermute_bwd", T * H * bf + A * H * bf + (rows + P) * H * bf + maps,
          "dO scatter + dw dot products"),
         ("route_bwd", T * E * 4 * 2 + maps, "dlogits"),
-        ("grouped_ffn_bwd", fl_bwd, "FC2 dgrad+SwiGLU bwd, FC1 dgrad, dW2, dW13 (tcgen05)"),
+        ("grouped_ffn_dgrad", fl, "FC2 dgrad+SwiGLU bwd, FC1 dgrad (tcgen05"
+         + (" kind::mxf8f6f4)" if fp8 else ")")),
+        ("grouped_ffn_wgrad", fl, "dW2, dW13 (tcgen05 bf16)"),
         ("permute_bwd", rows * H * bf + T * H * bf + maps, "dx gather-reduce"),
         ("router_wgrad", T * H * bf + E * H * 4 + T * E * 4, "dW_r (each x row once)"),
     ]
     out = []
     for (name, w, what), ms in zip(work, stage_ms):
         if name.startswith("grouped_ffn"):
+            pk = bf16_peak if name == "grouped_ffn_wgrad" else tc_peak
             ach = w / (ms * 1e-3) / 1e12
             out.append({"stage": name, "what": what, "ms": ms, "tflop": w / 1e12,
-                        "tflops": ach, "frac_tensor": ach / tc_peak})
-        else:
+                        "tflops": ach, "frac_tensor": ach / pk})
+        elif w > 0:
             ach = w / (ms * 1e-3) / 1e9
             out.append({"stage": name, "what": what, "ms": ms, "mb": w / 1e6,
                         "gbs": ach, "frac_hbm": ach / hbm_gbs})
@@ -213,6 +241,8 @@ def run_ours(args, rank, world, local):
     stream = torch.cuda.current_stream(dev)
     sc = bufs.scratch
 
+    fp8 = shape.dtype == W.DT_FP8
+
     def step(ev=None):
         # the layer step through the per-stage entry points (the same launches
         # as moe_layer_fwd + moe_layer_bwd); ev[i] is recorded after stage i
@@ -224,36 +254,42 @@ def run_ours(args, rank, world, local):
         B.moe_permute(cfg, x, f["idx"], f["counts"], f["offsets"], f["row_of"], f["token_of"],
                       f["sel_offsets"], f["sel_tokens"], f["x_perm"], sc)
         rec(2)
+        B.moe_quantize_weights(cfg, inp["W13"], inp["W2"], sc)
+        rec(3)
         B.moe_grouped_ffn_fwd(cfg, f["x_perm"], f["counts"], f["offsets"], inp["W13"], inp["W2"],
                               f["GU"], f["h"], f["y_perm"], sc)
-        rec(3)
-        B.moe_unpermute(cfg, f["y_perm"], f["row_of"], f["w"], f["offsets"], out)
         rec(4)
+        B.moe_unpermute(cfg, f["y_perm"], f["row_of"], f["w"], f["offsets"], out)
+        rec(5)
         B.moe_unpermute_bwd(cfg, dY, f["y_perm"], f["row_of"], f["w"], f["counts"], f["offsets"],
                             b["dO_perm"], b["dw"])
-        rec(5)
-        B.moe_route_bwd(cfg, f["logits"], f["idx"], f["w"], b["dw"], b["dlogits"])
         rec(6)
-        B.moe_grouped_ffn_bwd(cfg, b["dO_perm"], f["x_perm"], f["GU"], f["h"], f["counts"],
-                              f["offsets"], f["token_of"], b["dlogits"], inp["W_r"], inp["W13"],
-                              inp["W2"], b["dGU"], b["dX_perm"], dW13, dW2, sc)
+        B.moe_route_bwd(cfg, f["logits"], f["idx"], f["w"], b["dw"], b["dlogits"])
         rec(7)
+        B.moe_grouped_ffn_dgrad(cfg, b["dO_perm"], f["GU"], f["counts"], f["offsets"],
+                                f["token_of"], b["dlogits"], inp["W_r"], inp["W13"], inp["W2"],
+                                b["dGU"], b["dX_perm"], sc)
+        rec(8)
+        B.moe_grouped_ffn_wgrad(cfg, b["dO_perm"], f["x_perm"], f["h"], b["dGU"], f["counts"],
+                                f["offsets"], dW13, dW2, sc)
+        rec(9)
         B.moe_permute_bwd(cfg, b["dX_perm"], f["row_of"], f["offsets"], f["idx"], b["dlogits"],
                           inp["W_r"], dx)
-        rec(8)
+        rec(10)
         B.moe_router_wgrad(cfg, x, f["sel_offsets"], f["sel_tokens"], b["dlogits"], dW_r, sc)
-        rec(9)
+        rec(11)
 
     # kernels launched by one step: route (logits [+ W_r split on the tensor-core
     # path] + selection), dispatch (hist, rank, scatter), FC1 and FC2, combine,
     # combine bwd, route bwd, the four backward GEMMs, dispatch bwd, router wgrad
     # (on the tensor-core path: dlogits split, GEMM, chunk sum); the FP8 mode adds
-    # 4 quantisation launches forward and 6 backward
+    # the two weight quantisers, 2 activation quantisers forward, 2 in the data
+    # gradients and 4 in the weight gradients
     tc_router = shape.E >= 128 and shape.E % 128 == 0
     launches_per_step = ((3 if tc_router else 2) + 3 + 2 + 1 + 1 + 1 + 4 + 1
                          + (3 if tc_router else 1))
-    if shape.dtype == W.DT_FP8:
-        launches_per_step += 4 + 6
+    if fp8:
+        launches_per_step += 2 + 2 + 2 + 4
     for _ in range(max(args.warmup, 3)):
         step()
     torch.cuda.synchronize(dev)
@@ -261,9 +297,11 @@ def run_ours(args, rank, world, local):
     if status != 0:
         raise RuntimeError(f"device status {status} after warm-up")
     counts = f["counts"].cpu().tolist()
-    fl_fwd, fl_bwd = gemm_flops(shape, counts)
+    fl = gemm_flops(shape, counts)
+    nst = len(STAGES)
 
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(10)] for _ in range(args.steps)]
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(nst + 1)]
+           for _ in range(args.steps)]
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
     clocks = ClockSampler(local)
@@ -276,11 +314,9 @@ def run_ours(args, rank, world, local):
         step(evs[i])
     t1.record(stream)
     torch.cuda.synchronize(dev)
-    clk = clocks.stop()
     ms = t0.elapsed_time(t1)
-    stage_ms = [sum(e[i].elapsed_time(e[i + 1]) for e in evs) / args.steps for i in range(9)]
-    fwd_gemm_ms, bwd_gemm_ms = stage_ms[2], stage_ms[6]
-    gemm_ms = fwd_gemm_ms + bwd_gemm_ms
+    stage_ms = [sum(e[i].elapsed_time(e[i + 1]) for e in evs) / args.steps for i in range(nst)]
+    sm = dict(zip(STAGES, stage_ms))
 
     # end to end through the public layer calls, host buffers: every step copies
     # its x and dY from pinned host memory and reads out and dx back. Copies run
@@ -337,6 +373,7 @@ def run_ours(args, rank, world, local):
     e1.record(stream)
     torch.cuda.synchronize(dev)
     e2e_ms = e0.elapsed_time(e1)
+    clk = clocks.stop()
     status = B.moe_last_device_status(sc)
     if status != 0:
         raise RuntimeError(f"device status {status} after timed steps")
@@ -348,9 +385,27 @@ def run_ours(args, rank, world, local):
         torch.distributed.all_reduce(times, op=torch.distributed.ReduceOp.MAX)
     ms, e2e_ms = times.tolist()
     pk, src = peaks()
-    peak = pk.get("bf16_tflops_sustained", pk["bf16_tflops"])
-    achieved = (fl_fwd + fl_bwd) / (gemm_ms * 1e-3) / 1e12
+    bf16_peak = pk["bf16_tflops"]                  # burst: the kernels are timed in a short loop
+    tc_peak = 2.0 * bf16_peak if fp8 else bf16_peak
+    if fp8:
+        gemm_ms = sm["grouped_ffn_fwd"] + sm["grouped_ffn_dgrad"]
+        gemm_fl = 2 * fl
+        kern = ("grouped_gemm_fp8_kernel (tcgen05 kind::mxf8f6f4, E4M3 x UE8M0 128-blocks: FC1+"
+                "SwiGLU, FC2, FC2 dgrad+SwiGLU bwd, FC1 dgrad)")
+        peak_src = (f"{src}: 2 x bf16_tflops (the nominal FP8:bf16 dense rate ratio; no FP8 "
+                    "figure is measured)")
+        gemm_note = ("time of the grouped_ffn_fwd and grouped_ffn_dgrad stages, which also hold "
+                     "the activation quantisers (x_perm, h, dO, dGU)")
+    else:
+        gemm_ms = sm["grouped_ffn_fwd"] + sm["grouped_ffn_dgrad"] + sm["grouped_ffn_wgrad"]
+        gemm_fl = 3 * fl
+        kern = "grouped_gemm_kernel (tcgen05 kind::f16; FC1+SwiGLU, FC2, 2 dgrad, 2 wgrad)"
+        peak_src = f"{src}: bf16_tflops"
+        gemm_note = "time of the three grouped-FFN stages"
+    achieved = gemm_fl / (gemm_ms * 1e-3) / 1e12
     tokens = T * args.steps * world
+    cf = shape.capacity_factor
+    dt_name = "fp8_e4m3_block" if fp8 else "bf16"
     res = {
         "metric": "MoE-layer tokens/s fwd+bwd on 1 GB300",
         "value": tokens / (ms * 1e-3),
@@ -362,46 +417,112 @@ def run_ours(args, rank, world, local):
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "bf16",
+        "dtype": dt_name,
+        "dtype_detail": ("E4M3 operands with UE8M0 power-of-two scales per 128x128 weight tile and "
+                         "1x128 activation slice on the forward and data-gradient GEMMs (fp32 "
+                         "accumulation); weight gradients on the bf16 tensor path over E4M3 "
+                         "values in 128x1 slices; router fp32; activations and outputs bf16"
+                         if fp8 else "bf16 operands, fp32 accumulation, fp32 router"),
         "data": "synthetic (seeded N(0,1) tokens, N(0,0.02^2) weights; no dataset)",
         "config": {"workload": f"{shape.name}: T={T} H={H} E={E}(+{S} shared) top-{shape.k} "
-                               f"F={F} fwd+bwd", "l2": "inputs larger than L2 (weights "
-                               f"{2 * G * 3 * H * F / 1e9:.2f} GB streamed per step)",
+                               f"F={F} capacity_factor={cf if cf > 0 else 'dropless'} "
+                               f"dtype={dt_name} fwd+bwd",
+                   "l2": "inputs larger than L2 (expert weights "
+                         f"{2 * G * 3 * H * F / 1e9:.2f} GB in bf16, streamed every step)",
                    "parallelism": "replicas" if world > 1 else "single GPU"},
         "e2e": {"value": tokens / (e2e_ms * 1e-3), "unit": "tokens/s",
                 "h2d_bytes_per_step": 2 * T * H * 2, "d2h_bytes_per_step": 2 * T * H * 2},
         "gpu_launches": launches_per_step * args.steps,
-        "roofline": {"kernel": "grouped_gemm_kernel (tcgen05; FC1+SwiGLU, FC2, 2 dgrad, 2 wgrad)",
-                     "bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                     "frac": achieved / peak, "peak_source": f"{src} bf16_tflops_sustained",
+        "roofline": {"kernel": kern, "bound": "tensor", "achieved": achieved, "peak": tc_peak,
+                     "unit": "TFLOP/s", "frac": achieved / tc_peak, "peak_source": peak_src,
                      "traffic": gemm_traffic(shape.name),
-                     "traffic_note": "DRAM bytes of the six grouped-GEMM launches of one step "
+                     "traffic_note": "DRAM bytes of the grouped-GEMM launches of one step "
                                      "(ncu dram__bytes_read+write); achieved is per step too",
-                     "gemm_ms_per_step": gemm_ms,
-                     "fwd_gemm_ms": fwd_gemm_ms, "bwd_gemm_ms": bwd_gemm_ms,
-                     "gemm_tflop_per_step": (fl_fwd + fl_bwd) / 1e12},
-        "stages": stage_table(shape, cfg, f, stage_ms, pk["hbm_gbs"], fl_fwd, fl_bwd, peak),
+                     "gemm_ms_per_step": gemm_ms, "gemm_time_note": gemm_note,
+                     "gemm_tflop_per_step": gemm_fl / 1e12,
+                     "frac_of_sustained": achieved / (2.0 * pk.get("bf16_tflops_sustained",
+                                                                   bf16_peak) if fp8 else
+                                                      pk.get("bf16_tflops_sustained",
+                                                             bf16_peak))},
+        "stages": stage_table(shape, f, stage_ms, pk["hbm_gbs"], fl, tc_peak, bf16_peak),
         "clocks": clk,
     }
+    if fp8:
+        wg = fl / (sm["grouped_ffn_wgrad"] * 1e-3) / 1e12
+        res["roofline_wgrad"] = {"kernel": "grouped_gemm_kernel (tcgen05 kind::f16 weight "
+                                           "gradients over E4M3 values, with their 4 quantisers)",
+                                 "achieved": wg, "peak": bf16_peak, "unit": "TFLOP/s",
+                                 "frac": wg / bf16_peak}
     return res, shape, inp
 
 
 # ---------------------------------------------------------------------- the oracle
-def oracle_inputs(inp: dict, n_tok: int) -> dict:
-    """Host fp64 copies of the first n_tok tokens and all weights (not timed)."""
-    h = lambda t: None if t is None else t.detach().to("cpu").double().numpy()  # noqa: E731
-    return {"x": h(inp["x"][:n_tok]), "dY": h(inp["dY"][:n_tok]), "W_r": h(inp["W_r"]),
-            "bias": h(inp["bias"]), "W13": h(inp["W13"]), "W2": h(inp["W2"])}
+def oracle_subproblem(shape, inp: dict, max_tokens: int, max_experts: int):
+    """A bounded sample of the workload for the CPU oracle: the first n tokens
+    (n <= max_tokens) that together select at most max(max_experts, k)
+    experts, with the layer restricted to those experts.
 
-
-def oracle_sample(shape, o: dict) -> float:
-    """Seconds the CPU oracle takes for fwd+bwd of the sampled tokens."""
+    The oracle's own router scores the sampled tokens against all E experts
+    (timed); the layer functions then run on a problem of the selected
+    experts only, so no other expert's weights are converted to fp64 and no
+    other expert's weight gradient is allocated. Each sampled token keeps its
+    experts and routing weights: the restricted logits hold the token's
+    scores (softmax: logit + bias) at its selected experts and -700 elsewhere,
+    which the restricted top-k (no groups, no bias) passes over. The first
+    tokens are never dropped by the capacity limit (it keeps an expert's first
+    C tokens, C >= 128), so the restricted problem is dropless."""
     from oracle import moe_oracle as O
-    sub = shape.with_(T=o["x"].shape[0])
+    h = lambda t: t.detach().to("cpu").double().numpy()  # noqa: E731
+    Wr = h(inp["W_r"])
+    bias = None if inp["bias"] is None else h(inp["bias"])
+    n_try = min(shape.T, max_tokens)
+    x_all = h(inp["x"][:n_try])
+    idx, _ = O.route(O.router_logits(x_all, Wr), shape, bias)
+    cap = max(max_experts, shape.k)
+    used = set(int(e) for e in idx[0])
+    n = 1
+    while n < n_try and len(used | set(int(e) for e in idx[n])) <= cap:
+        used |= set(int(e) for e in idx[n])
+        n += 1
+    U = sorted(used)
+    pos = {e: i for i, e in enumerate(U)}
+    sub = shape.with_(T=n, E=len(U), n_groups=1, topk_groups=1, capacity_factor=0.0,
+                      bias_kind="none")
+    sel = torch.as_tensor(U, device=inp["W13"].device)
+    return {"shape": shape, "sub": sub, "n": n, "experts": U, "pos": pos, "x": x_all[:n],
+            "dY": h(inp["dY"][:n]), "W_r": Wr, "bias": bias, "W_r_sub": Wr[U],
+            "W13": h(inp["W13"][sel]), "W2": h(inp["W2"][sel])}
+
+
+def oracle_sample(o: dict) -> float:
+    """Seconds the CPU oracle takes for fwd+bwd of the sampled tokens: the
+    router logits over all experts, the selection, then the layer on the
+    selected experts (FP8 layer functions for the FP8 configuration)."""
+    from oracle import moe_oracle as O
+    shape, sub = o["shape"], o["sub"]
     t0 = time.perf_counter()
-    fwd = O.layer_forward(sub, o["x"], o["W_r"], o["bias"], o["W13"], o["W2"])
-    O.layer_backward(sub, o["x"], o["W_r"], o["W13"], o["W2"], fwd, o["dY"])
+    lg = O.router_logits(o["x"], o["W_r"])
+    idx, _ = O.route(lg, shape, o["bias"])
+    score = lg + (o["bias"] if (o["bias"] is not None and shape.score_fn == O.SOFTMAX) else 0.0)
+    lg_sub = np.full((sub.T, sub.E), -700.0)
+    for t in range(sub.T):
+        for e in idx[t]:
+            lg_sub[t, o["pos"][int(e)]] = score[t, int(e)]
+    if shape.dtype == W.DT_FP8:
+        fwd = O.layer_forward_fp8(sub, o["x"], o["W_r_sub"], None, o["W13"], o["W2"], logits=lg_sub)
+        O.layer_backward_fp8(sub, o["x"], o["W_r_sub"], o["W13"], o["W2"], fwd, o["dY"])
+    else:
+        fwd = O.layer_forward(sub, o["x"], o["W_r_sub"], None, o["W13"], o["W2"], logits=lg_sub)
+        O.layer_backward(sub, o["x"], o["W_r_sub"], o["W13"], o["W2"], fwd, o["dY"])
     return time.perf_counter() - t0
+
+
+def sample_text(o: dict, steps: int = 1) -> str:
+    sh = o["shape"]
+    return (f"first {o['n']} tokens of {sh.name} ({len(o['experts'])} of {sh.E} experts "
+            f"selected), {steps} pass(es): router logits over all experts, selection, then "
+            "fwd+bwd of the selected experts incl. their weight gradients"
+            + (" (FP8 layer functions)" if sh.dtype == W.DT_FP8 else "") + ", fp64 numpy")
 
 
 def cpu_cores() -> int:
@@ -412,33 +533,26 @@ def cpu_cores() -> int:
 
 
 def run_reference(args):
-    """The oracle as the reference arm: every step runs its fwd+bwd (weight
-    gradients included) on a sample of the workload's tokens, on the host cores.
-
-    A step of the oracle has a floor that does not shrink with the sample (it
-    builds every expert's full-size fp64 weight gradient), so the run is held
-    to about --ref-budget-s seconds: a timed 1-token step (also the warm-up)
-    sizes the sample (1 token at least, the whole batch at most) and, when even
-    1-token steps do not fit, fewer steps than requested run; the JSON line says
-    how many ("steps", with "steps_requested")."""
+    """The oracle as the reference arm: each step runs the oracle's fwd+bwd on
+    the bounded sample of the workload that cpu_baseline uses, on the host
+    cores. The inputs are drawn with the same seeded recipe (on the GPU when
+    there is one, which only draws the random numbers); a step takes tens of
+    seconds on the large shapes, so fewer steps than requested run when they
+    would not fit in about --ref-budget-s seconds ("steps", with
+    "steps_requested")."""
     shape = {**W.SHAPES, **W.PROFILE_SHAPES}[args.workload]
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    inp = W.make_inputs(shape, seed=args.seed, device=dev)
+    o = oracle_subproblem(shape, inp, args.cpu_sample_tokens or 64, 8)
+    del inp
+    t1 = oracle_sample(o)                                         # warm-up and probe
     want = max(args.steps, 1)
-    o_all = oracle_inputs(W.make_inputs(shape, seed=args.seed, device="cpu"), shape.T)
-    t1 = oracle_sample(shape, oracle_inputs_slice(o_all, 1))            # warm-up and probe
-    if args.cpu_sample_tokens:
-        n_tok = min(args.cpu_sample_tokens, shape.T)
-        steps = want
-    else:
-        n_tok = int(min(shape.T, max(1, args.ref_budget_s / (want * max(t1, 1e-6)))))
-        steps = int(min(want, max(1, args.ref_budget_s / (n_tok * max(t1, 1e-6)))))
-    o = oracle_inputs_slice(o_all, n_tok)
-    secs = [oracle_sample(shape, o) for _ in range(steps)]
+    steps = int(min(want, max(1, args.ref_budget_s / max(t1, 1e-6))))
+    secs = [oracle_sample(o) for _ in range(steps)]
     tot = sum(secs)
-    val = n_tok * steps / tot
+    val = o["n"] * steps / tot
     cb = {"value": val, "unit": "tokens/s", "cores": cpu_cores(), "kind": "oracle",
-          "sample": f"first {n_tok} tokens of {shape.name} per step, {steps} steps (routing, "
-                    "experts, combine, full backward incl. every expert's weight gradient), "
-                    "fp64 numpy"}
+          "sample": sample_text(o, steps)}
     return {"impl": "reference", "metric": "MoE-layer tokens/s fwd+bwd on 1 GB300", "value": val,
             "unit": "tokens/s", "n_gpus": 1, "steps": steps, "steps_requested": args.steps,
             "warmup": 1, "ms_per_step": 1e3 * tot / steps, "higher_is_better": True,
@@ -446,13 +560,6 @@ def run_reference(args):
             "config": {"workload": shape.name}, "cpu_baseline": cb,
             "e2e": {"value": val, "unit": "tokens/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
-
-
-def oracle_inputs_slice(o: dict, n: int) -> dict:
-    d = dict(o)
-    d["x"] = o["x"][:n]
-    d["dY"] = o["dY"][:n]
-    return d
 
 
 def main():
@@ -470,13 +577,12 @@ def main():
     if rank == 0:
         if not args.no_cpu_baseline:
             n_tok = args.cpu_sample_tokens or (shape.T if shape.name == "tiny" else 64)
-            o = oracle_inputs(inp, n_tok)
+            o = oracle_subproblem(shape, inp, n_tok, 8)
             del inp
-            secs = oracle_sample(shape, o)
-            res["cpu_baseline"] = {
-                "value": n_tok / secs, "unit": "tokens/s", "cores": cpu_cores(), "kind": "oracle",
-                "sample": f"first {n_tok} tokens of {shape.name}: oracle fwd+bwd incl. weight "
-                          "gradients of those tokens, fp64 numpy, one pass"}
+            secs = oracle_sample(o)
+            res["cpu_baseline"] = {"value": o["n"] / secs, "unit": "tokens/s",
+                                   "cores": cpu_cores(), "kind": "oracle",
+                                   "sample": sample_text(o)}
         print(json.dumps(res), flush=True)
     if world > 1:
         torch.distributed.destroy_process_group()

@@ -69,11 +69,13 @@ enum { MOE_GROUP_TOP2_SUM = 0, MOE_GROUP_MAX = 1 };
  * with power-of-two block scales (2^ceil(log2(amax/448))): expert weights in
  * 128x128 tiles, activations in 1x128 slices along the dimension their GEMM
  * reduces, weight-gradient operands in 128x1 slices along each expert's
- * tokens. Router, routing weights and all outputs stay as in bf16 mode. In
- * this mode `scratch` also holds the quantised weights and activations
+ * tokens. The forward and data-gradient GEMMs run on the block-scaled FP8
+ * tensor cores. Router, routing weights and all outputs stay as in bf16 mode.
+ * In this mode `scratch` also holds the quantised weights and activations
  * (moe_query_sizes counts them), and the scratch used by a forward must be
  * passed unchanged to its backward. Shared experts are not supported in this
- * mode (n_shared must be 0). */
+ * mode (n_shared must be 0), and H and F must be multiples of 256
+ * (MOE_ERR_UNSUPPORTED otherwise). */
 enum { MOE_DTYPE_BF16 = 0, MOE_DTYPE_FP8_E4M3_BLOCK = 1 };
 
 /* One layer configuration. */
@@ -162,8 +164,9 @@ MOE_API moe_status moe_route(const moe_config* cfg, const void* x, const float* 
  * -- softmax over their logits + bias, or route_scale * s_j / sum s -- with
  * moe_route's own arithmetic, so replaying moe_route's idx gives its w (the
  * sigmoid router's exact-path tokens, whose selection needed fp64 keys, can
- * differ by a few fp32 ulp). An index outside [0, E) records
- * MOE_ERR_DEVICE_CHECK in the status word and gets weight 0. The rest of the
+ * differ by a few fp32 ulp). An index outside [0, E), or one that repeats an
+ * earlier slot of the same token, records MOE_ERR_DEVICE_CHECK in the status
+ * word and gets weight 0 (moe_permute drops the same entries). The rest of the
  * layer (moe_permute on the same idx, ..., the backward) is unchanged. */
 MOE_API moe_status moe_route_replay(const moe_config* cfg, const void* x, const float* W_r,
                             const float* bias, const int32_t* idx, float* logits, float* w,
@@ -225,6 +228,9 @@ MOE_API moe_status moe_route_aux_bwd(const moe_config* cfg, const void* x, const
  * order; segments are padded to row_align rows (or are C rows in capacity
  * mode, where the first C tokens of an expert are kept); shared experts
  * follow, one row per token. Writes the maps and x_perm (padding rows zero).
+ * An idx entry outside [0, E), or one that repeats an earlier slot of the
+ * same token (only a caller-given idx can), records MOE_ERR_DEVICE_CHECK in
+ * the status word and is dropped: row_of = -1, not counted, no row.
  * scratch: moe_sizes.scratch_bytes bytes. */
 MOE_API moe_status moe_permute(const moe_config* cfg, const void* x, const int32_t* idx,
                        int32_t* counts, int32_t* offsets, int32_t* row_of, int32_t* token_of,
@@ -240,8 +246,9 @@ MOE_API moe_status moe_permute(const moe_config* cfg, const void* x, const int32
  *  - Limit: configurations whose dispatch scratch (4096 + 4*E*ceil(T/256) +
  *    256 bytes, rounded up to 256) exceeds 512 KiB return MOE_ERR_WORKSPACE
  *    without launching anything.
- *  - The first call on a device looks up the array's device address with that
- *    device current; make that first call before any stream capture.
+ *  - Every call looks up the array's device address in the current context
+ *    (the first lookup on a device may load the library's device code, so
+ *    make the first call on each device before any stream capture).
  *  - All calls share the one array, which keeps the last call's contents:
  *    calls whose kernels overlap on the GPU (e.g. on two streams) race. Each
  *    call clears the array's status word; index problems a kernel finds are
@@ -252,10 +259,25 @@ MOE_API moe_status moe_permute_noalloc(const moe_config* cfg, const void* x, con
                                        int32_t* token_of, int32_t* sel_offsets,
                                        int32_t* sel_tokens, void* x_perm, void* stream);
 
+/* FP8 mode only (es summary §2.4: expert GEMMs in FP8, MXFP8 -- power-of-two
+ * block scales -- on Blackwell): quantises the expert weights W13 [G,2F,H] and
+ * W2 [G,H,F] (bf16) into E4M3 codes with one UE8M0 scale per 128x128 tile,
+ * kept in `scratch` for the FP8 grouped GEMMs (both orientations of every
+ * weight: forward and data gradient). Call it after every change of the
+ * weights and before moe_grouped_ffn_fwd / moe_grouped_ffn_dgrad on the same
+ * scratch (moe_layer_fwd calls it itself). A tile whose largest magnitude is
+ * below 448 * 2^-128 is scaled by 2^-127, the smallest UE8M0 scale. In bf16
+ * mode it launches nothing and returns MOE_OK. */
+MOE_API moe_status moe_quantize_weights(const moe_config* cfg, const void* W13, const void* W2,
+                                        void* scratch, void* stream);
+
 /* Stage 3, compute (es summary §2.1 step 3; grouped GEMM, §2.3.C): for every
  * group g, on its rows X: [G|U] = X W13[g]^T (GU, bf16), h = bf16(silu(G) U),
  * y_perm = bf16(h W2[g]^T). tcgen05 grouped GEMMs that read counts/offsets on
- * the device. */
+ * the device. FP8 mode: x_perm and h are quantised in 1x128 slices (E4M3 +
+ * UE8M0, kept in scratch) and both GEMMs run on the block-scaled FP8 tensor
+ * cores (tcgen05 kind::mxf8f6f4) with the weights moe_quantize_weights left in
+ * scratch; W13 and W2 are then not read. */
 MOE_API moe_status moe_grouped_ffn_fwd(const moe_config* cfg, const void* x_perm, const int32_t* counts,
                                const int32_t* offsets, const void* W13, const void* W2,
                                void* GU, void* h, void* y_perm, void* scratch, void* stream);
@@ -273,8 +295,31 @@ MOE_API moe_status moe_unpermute_bwd(const moe_config* cfg, const void* dY, cons
                              const int32_t* row_of, const float* w, const int32_t* counts,
                              const int32_t* offsets, void* dO_perm, float* dw, void* stream);
 
+/* Data-gradient half of moe_grouped_ffn_bwd (the W/D split of es summary
+ * §2.3.B): dGU and dX_perm exactly as moe_grouped_ffn_bwd writes them. FP8
+ * mode: dO and dGU are quantised in 1x128 slices and both GEMMs run on the
+ * block-scaled FP8 tensor cores with the weights moe_quantize_weights left in
+ * scratch (W13 and W2 are then not read). */
+MOE_API moe_status moe_grouped_ffn_dgrad(const moe_config* cfg, const void* dO_perm,
+                                         const void* GU, const int32_t* counts,
+                                         const int32_t* offsets, const int32_t* token_of,
+                                         const float* dlogits, const float* W_r, const void* W13,
+                                         const void* W2, void* dGU, void* dX_perm, void* scratch,
+                                         void* stream);
+
+/* Weight-gradient half of moe_grouped_ffn_bwd: dW2[g] = dO^T h and
+ * dW13[g] = dGU^T x_perm over the group's rows (bf16, zero for empty groups),
+ * after moe_grouped_ffn_dgrad has written dGU. FP8 mode: both operands are
+ * quantised in 128x1 slices along the group's tokens and multiplied as their
+ * bf16 values on the bf16 tensor path (exactly the FP8 products). */
+MOE_API moe_status moe_grouped_ffn_wgrad(const moe_config* cfg, const void* dO_perm,
+                                         const void* x_perm, const void* h, const void* dGU,
+                                         const int32_t* counts, const int32_t* offsets,
+                                         void* dW13, void* dW2, void* scratch, void* stream);
+
 /* Backward of stage 3 (the W/D split of es summary §2.3.B: separate data- and
- * weight-gradient GEMMs): dh = dO W2[g] (fp32, not stored); SwiGLU backward
+ * weight-gradient GEMMs; moe_grouped_ffn_dgrad then moe_grouped_ffn_wgrad):
+ * dh = dO W2[g] (fp32, not stored); SwiGLU backward
  * with the stored GU -> dGU (bf16); dW2[g] = dO^T h; dW13[g] = dGU^T x_perm
  * (weight gradients in bf16, zero for empty groups);
  * dX_perm[r] = bf16( dGU[r] W13[g] + dlogits[token_of[r], g] W_r[g] ) for the
@@ -324,7 +369,8 @@ MOE_API moe_status moe_router_wgrad(const moe_config* cfg, const void* x, const 
                             const int32_t* sel_tokens, const float* dlogits, float* dW_r,
                             void* scratch, void* stream);
 
-/* The whole layer forward: route, permute, grouped FFN, unpermute. */
+/* The whole layer forward: (FP8 mode: moe_quantize_weights,) route, permute,
+ * grouped FFN, unpermute. */
 MOE_API moe_status moe_layer_fwd(const moe_config* cfg, const moe_params* params, const void* x,
                          void* out, const moe_fwd_state* st, void* scratch, void* stream);
 

@@ -23,8 +23,8 @@ STATUS_NAMES = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED",
 ENTRY_POINTS = (
     "moe_query_sizes", "moe_route", "moe_route_replay", "moe_route_aux", "moe_route_aux_bwd",
     "moe_permute", "moe_permute_noalloc",
-    "moe_grouped_ffn_fwd", "moe_unpermute",
-    "moe_unpermute_bwd", "moe_grouped_ffn_bwd", "moe_route_bwd", "moe_permute_bwd",
+    "moe_quantize_weights", "moe_grouped_ffn_fwd", "moe_unpermute",
+    "moe_unpermute_bwd", "moe_grouped_ffn_dgrad", "moe_grouped_ffn_wgrad", "moe_grouped_ffn_bwd", "moe_route_bwd", "moe_permute_bwd",
     "moe_router_wgrad", "moe_layer_fwd", "moe_layer_bwd", "moe_last_device_status",
     "moe_clear_device_status", "moe_check_bounded_wait", "moe_status_string",
 )
@@ -191,6 +191,11 @@ def moe_permute_noalloc(cfg, x, idx, counts, offsets, row_of, token_of, sel_offs
           sel_offsets, sel_tokens, x_perm, _stream(stream))
 
 
+def moe_quantize_weights(cfg, W13, W2, scratch, stream=None):
+    """FP8 mode: the E4M3 weights (and scales) in scratch; no-op in bf16 mode."""
+    _call("moe_quantize_weights", _cfg(cfg), W13, W2, scratch, _stream(stream))
+
+
 def moe_grouped_ffn_fwd(cfg, x_perm, counts, offsets, W13, W2, GU, h, y_perm, scratch,
                         stream=None):
     _call("moe_grouped_ffn_fwd", _cfg(cfg), x_perm, counts, offsets, W13, W2, GU, h, y_perm,
@@ -210,6 +215,18 @@ def moe_grouped_ffn_bwd(cfg, dO_perm, x_perm, GU, h, counts, offsets, token_of, 
                         W13, W2, dGU, dX_perm, dW13, dW2, scratch, stream=None):
     _call("moe_grouped_ffn_bwd", _cfg(cfg), dO_perm, x_perm, GU, h, counts, offsets, token_of,
           dlogits, W_r, W13, W2, dGU, dX_perm, dW13, dW2, scratch, _stream(stream))
+
+
+def moe_grouped_ffn_dgrad(cfg, dO_perm, GU, counts, offsets, token_of, dlogits, W_r, W13, W2,
+                          dGU, dX_perm, scratch, stream=None):
+    _call("moe_grouped_ffn_dgrad", _cfg(cfg), dO_perm, GU, counts, offsets, token_of, dlogits,
+          W_r, W13, W2, dGU, dX_perm, scratch, _stream(stream))
+
+
+def moe_grouped_ffn_wgrad(cfg, dO_perm, x_perm, h, dGU, counts, offsets, dW13, dW2, scratch,
+                          stream=None):
+    _call("moe_grouped_ffn_wgrad", _cfg(cfg), dO_perm, x_perm, h, dGU, counts, offsets, dW13,
+          dW2, scratch, _stream(stream))
 
 
 def moe_route_bwd(cfg, logits, idx, w, dw, dlogits, stream=None):

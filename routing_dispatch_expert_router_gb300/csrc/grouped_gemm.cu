@@ -25,180 +25,10 @@
 //     dimension; the output is the group's own [Mw x N] matrix.
 // Every group segment is a multiple of 128 rows whose padding rows are zero,
 // so no tile crosses into another group and no masking is needed.
-#include <cuda.h>
-#include <cudaTypedefs.h>
-
-#include "common.cuh"
-#include "internal.h"
-#include "ptx.cuh"
+#include "gemm_common.cuh"
 
 namespace moe {
 namespace gg {
-
-constexpr int BM = 128;
-constexpr int BK = 64;                       // 64 bf16 = one 128-byte swizzle row
-constexpr int kThreads = 192;
-constexpr int kCtrlBytes = 5120;
-constexpr int kBoxBytes = 32 * 32 * 2;           // one 32 x 32 bf16 output box
-constexpr int kStageBytes = 3 * kBoxBytes;       // output staging per epilogue warp
-constexpr long long kWaitBudget = 4000000000LL;   // clock64 cycles (~2 s)
-
-enum Epi : int { kEpiSwigluFwd = 0, kEpiStore = 1, kEpiSwigluBwd = 2, kEpiWgrad = 3,
-                 kEpiStoreF32 = 4, kEpiDgradRouter = 5, kEpiAddBf16 = 6 };
-
-struct Params {
-  int kgrouped;               // 0: row-grouped, 1: K-grouped
-  int G;
-  int N;                      // output columns per group (unused by SwiGLU-fwd)
-  int K;                      // reduction length (row-grouped)
-  int Mw;                     // output rows per group (K-grouped)
-  int F;                      // SwiGLU width
-  int b_rows;                 // rows of one group in B's 2D view (row-grouped)
-  const int32_t* counts;
-  const int32_t* offsets;
-  __nv_bfloat16* out;
-  long long ldo;
-  long long out_gstride;      // K-grouped: elements between groups' outputs
-  __nv_bfloat16* out2;        // SwiGLU-fwd: h
-  long long ldo2;
-  const __nv_bfloat16* aux;   // SwiGLU-bwd: GU; add-to-output (kEpiAddBf16): the output
-  long long ldaux;            // itself, read before it is overwritten
-  int32_t* status;
-  int dense_rows;             // > 0: one group of this many rows at row 0 (no counts/offsets),
-                              // or, with chunk_rows > 0, that many rows cut into groups of
-                              // chunk_rows consecutive rows (the last one shorter)
-  int chunk_rows;
-  long long part_rows;        // B parts (b_parts > 1) of an MN-major B: part q's rows start
-                              // at q * part_rows
-  // FC1 data gradient with the router term (kEpiDgradRouter): row r of a
-  // routed group g < router_E gains dlogits[token_of[r], g] * W_r[g, :]
-  const int32_t* token_of;
-  const float* dlogits;
-  const float* W_r;
-  int router_E;
-  // Tile order: 1 = n-tiles vary fastest, else m-tiles (m-pairs). Weight gradients
-  // whose output is taller than wide take n-fastest: the clusters running at
-  // once then share the A slice (the group's rows x 256 output rows) and stream
-  // B, which is the smaller operand and stays in L2 (Mixtral-sized dW13: the
-  // group's dGU is read from DRAM once instead of about four times).
-  int n_fast;
-};
-
-// Router logits (kEpiStoreF32) multiply each A k-block by the three bf16 parts
-// of the fp32 weight, held in B as three consecutive 64-column blocks: one
-// stage carries the A block once and the three B blocks.
-template <int EPI>
-constexpr int b_parts() { return EPI == kEpiStoreF32 ? 3 : 1; }
-
-template <int BN, int STAGES, int BPARTS = 1>
-struct Layout {
-  static constexpr int A_BYTES = BM * BK * 2;
-  static constexpr int B_BYTES = BN * BK * 2;
-  static constexpr int STAGE = A_BYTES + BPARTS * B_BYTES;
-  static constexpr int TILES = STAGES * STAGE;
-  static constexpr int SMEM = TILES + kCtrlBytes + 4 * kStageBytes + 1024;
-  static constexpr int TMEM_COLS = 2 * BN;
-};
-
-struct Tile {
-  int g, mt, nt, nk;
-};
-
-__device__ __forceinline__ int find_group(const int* prefix, int G, int tile) {
-  int lo = 0, hi = G - 1;
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    if (prefix[mid] <= tile) lo = mid;
-    else hi = mid - 1;
-  }
-  return lo;
-}
-
-__device__ __forceinline__ Tile decode(int tile, const int* prefix, const int* mtiles,
-                                       const int* cnt, int G, int kgrouped, int K, int NT,
-                                       int n_fast) {
-  Tile t;
-  t.g = find_group(prefix, G, tile);
-  const int local = tile - prefix[t.g];
-  const int mt = mtiles[t.g];
-  if (n_fast) {
-    t.nt = local % NT;
-    t.mt = local / NT;
-  } else {
-    t.mt = local % mt;
-    t.nt = local / mt;
-  }
-  t.nk = kgrouped ? (cnt[t.g] + BK - 1) / BK : K / BK;
-  return t;
-}
-
-// Logistic sigmoid 1 / (1 + e^-z) = 1 / (1 + 2^(-z log2 e)) and SiLU for the
-// SwiGLU epilogues, on the special-function unit (a few fp32 ulp; the bf16
-// outputs keep 8 significant bits). Large |z| saturate to 0 and 1.
-constexpr float kLog2e = 1.4426950408889634f;
-__device__ __forceinline__ float sigmoid_f(float z) {
-  return ptx::rcp_approx(1.f + ptx::ex2_approx(-kLog2e * z));
-}
-__device__ __forceinline__ float silu_f(float z) { return z * sigmoid_f(z); }
-
-// SwiGLU backward of 8 consecutive columns. With s = sigmoid(g) and
-// silu(g) = g s (h = silu(g) u):
-//   dU = dh silu(g),  dG = dh u (s + silu(g) (1 - s))   [= dh u s (1 + g (1 - s))].
-// dh: 8 fp32 (tensor-memory bits); g, u: 8 bf16 each. fp32 pairs throughout.
-__device__ __forceinline__ void swiglu_bwd8(const uint32_t* dh, const uint4& g, const uint4& u,
-                                            uint4& dg, uint4& du) {
-  const uint32_t gw[4] = {g.x, g.y, g.z, g.w}, uw[4] = {u.x, u.y, u.z, u.w};
-  uint32_t dgw[4], duw[4];
-  const uint64_t one = ptx::f2_pack(1.f, 1.f);
-  const uint64_t nl2e = ptx::f2_pack(-kLog2e, -kLog2e);
-#pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    const uint64_t G = ptx::f2_pack(bf16_lo(gw[j]), bf16_hi(gw[j]));
-    const uint64_t U = ptx::f2_pack(bf16_lo(uw[j]), bf16_hi(uw[j]));
-    const uint64_t D = ptx::f2_pack(__uint_as_float(dh[2 * j]), __uint_as_float(dh[2 * j + 1]));
-    float e0, e1;
-    ptx::f2_unpack(ptx::f2_mul(G, nl2e), e0, e1);
-    float d0, d1;
-    ptx::f2_unpack(ptx::f2_add(ptx::f2_pack(ptx::ex2_approx(e0), ptx::ex2_approx(e1)), one), d0, d1);
-    const uint64_t S = ptx::f2_pack(ptx::rcp_approx(d0), ptx::rcp_approx(d1));
-    const uint64_t SILU = ptx::f2_mul(G, S);
-    const uint64_t DU = ptx::f2_mul(D, SILU);
-    const uint64_t T = ptx::f2_fma(SILU, ptx::f2_sub(one, S), S);
-    const uint64_t DG = ptx::f2_mul(ptx::f2_mul(D, U), T);
-    float a0, a1, b0, b1;
-    ptx::f2_unpack(DG, a0, a1);
-    ptx::f2_unpack(DU, b0, b1);
-    dgw[j] = pack_bf16x2(a0, a1);
-    duw[j] = pack_bf16x2(b0, b1);
-  }
-  dg = make_uint4(dgw[0], dgw[1], dgw[2], dgw[3]);
-  du = make_uint4(duw[0], duw[1], duw[2], duw[3]);
-}
-
-// Output staging: every epilogue warp owns kStageBytes of shared memory (1024-
-// byte aligned), stored to global memory by TMA (coalesced, asynchronous). The
-// SwiGLU epilogues stage up to three 32 x 32 bf16 boxes with the 64-byte
-// swizzle of their output maps (16-byte chunk j of row r at slot j ^ ((r>>1)&3));
-// the plain-store epilogues one 32 x 64 box with the 128-byte swizzle (chunk j
-// of row r at slot j ^ (r & 7)). Either way the 32 lanes' row writes hit
-// distinct banks.
-
-__device__ __forceinline__ void stage_row(uint8_t* stage, int box, int lane, const uint4 (&v)[4]) {
-  uint8_t* row = stage + box * kBoxBytes + lane * 64;
-  const int sw = (lane >> 1) & 3;
-#pragma unroll
-  for (int j = 0; j < 4; ++j) *reinterpret_cast<uint4*>(row + ((j ^ sw) << 4)) = v[j];
-}
-
-__device__ __forceinline__ void pack_slice(const uint32_t (&r)[32], uint4 (&o)[4]) {
-#pragma unroll
-  for (int v = 0; v < 4; ++v) {
-    float f[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) f[i] = __uint_as_float(r[v * 8 + i]);
-    o[v] = pack8(f);
-  }
-}
 
 // Drains one 128 x BN fp32 accumulator through the fused epilogue. This warp
 // handles the accumulator rows q*32 .. q*32+31 (tensor-memory lane quarter q,
@@ -220,7 +50,7 @@ __device__ __forceinline__ void epilogue_tile(const Params& p, const CUtensorMap
   const float* rw = nullptr;
   if (EPI == kEpiDgradRouter && g < p.router_E) {
     const int t = p.token_of[row0 + lane];
-    if (t >= 0) rd = p.dlogits[(long long)t * p.router_E + g];
+    if (t >= 0 && t < p.router_T) rd = p.dlogits[(long long)t * p.router_E + g];
     rw = p.W_r + (long long)g * p.N + f0;
   }
   if (EPI == kEpiStore || EPI == kEpiWgrad || EPI == kEpiDgradRouter || EPI == kEpiAddBf16) {
@@ -1005,76 +835,6 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA,
   }
 }
 
-// ----------------------------------------------------------------- host side
-static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  if (!fn) {
-    void* ptr = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
-                                         &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
-  }
-  return fn;
-}
-
-// 2D bf16 view [outer rows, inner columns] with a {64, box_outer} box and
-// 128-byte swizzle; elements outside the view read as zero.
-static bool make_map(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t outer,
-                     uint32_t box_outer) {
-  PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
-  if (!fn) return false;
-  cuuint64_t dims[2] = {inner, outer};
-  cuuint64_t strides[1] = {inner * 2};
-  cuuint32_t box[2] = {64, box_outer};
-  cuuint32_t es[2] = {1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box,
-            es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
-// Output view [outer rows, inner columns] for TMA stores of 32 x 32 boxes with
-// the 64-byte swizzle of the epilogue's staging layout.
-static bool make_out_map(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t outer) {
-  PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
-  if (!fn) return false;
-  cuuint64_t dims[2] = {inner, outer};
-  cuuint64_t strides[1] = {inner * 2};
-  cuuint32_t box[2] = {32, 32};
-  cuuint32_t es[2] = {1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box,
-            es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
-            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
-// bf16 output view for TMA stores of 32-row x 64-column boxes (128-byte rows,
-// 128-byte swizzle): the plain-store epilogues.
-static bool make_out_map_w64(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t outer) {
-  PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
-  if (!fn) return false;
-  cuuint64_t dims[2] = {inner, outer};
-  cuuint64_t strides[1] = {inner * 2};
-  cuuint32_t box[2] = {64, 32};
-  cuuint32_t es[2] = {1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box,
-            es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
-// fp32 output view for TMA stores of 32 x 32 boxes (128-byte rows, 128-byte swizzle).
-static bool make_out_map_f32(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t outer) {
-  PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
-  if (!fn) return false;
-  cuuint64_t dims[2] = {inner, outer};
-  cuuint64_t strides[1] = {inner * 4};
-  cuuint32_t box[2] = {32, 32};
-  cuuint32_t es[2] = {1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void*>(ptr), dims, strides, box,
-            es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 template <int EPI, int BN, int A_MN, int B_MN, int STAGES>
 static cudaError_t run(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& c,
                        const CUtensorMap& c2, const Params& p, cudaStream_t s) {
@@ -1132,17 +892,6 @@ static bool use_pairs(const moe_config& c, int n) {
                                    ? (long long)capacity_rows(c)
                                    : (long long)c.T * c.k / (c.E > 0 ? c.E : 1);
   return n % 256 == 0 && per_expert >= 512;
-}
-
-static Params base_params(const moe_config& c, const int32_t* counts, const int32_t* offsets,
-                          int32_t* status) {
-  Params p{};
-  p.G = c.E + c.n_shared;
-  p.F = c.F;
-  p.counts = counts;
-  p.offsets = offsets;
-  p.status = status;
-  return p;
 }
 
 }  // namespace gg
@@ -1240,6 +989,7 @@ cudaError_t launch_ffn_fc1_dgrad(const moe_config& c, const void* dGU, const int
   p.dlogits = dlogits;
   p.W_r = W_r;
   p.router_E = c.E;
+  p.router_T = c.T;
   if (use_pairs(c, c.H)) return run_pair<kEpiDgradRouter, 0, 1>(a, b, oc, oc2, p, s);
   return bn == 256 ? run<kEpiDgradRouter, 256, 0, 1, 4>(a, b, oc, oc2, p, s)
                    : run<kEpiDgradRouter, 128, 0, 1, 6>(a, b, oc, oc2, p, s);

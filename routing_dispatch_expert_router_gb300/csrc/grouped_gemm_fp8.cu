@@ -1,0 +1,513 @@
+// The expert GEMMs of the FP8 layer configuration on the block-scaled FP8
+// tensor cores: tcgen05.mma.kind::mxf8f6f4 with E4M3 operands and UE8M0 block
+// scales held in tensor memory.
+//
+// "Scalable Training of Mixture-of-Experts Models with Megatron Core" (es
+// summary, Resumen técnico §2.4) quantises the expert GEMMs to FP8 and names
+// MXFP8 -- E4M3 values with power-of-two scales applied by the hardware -- as
+// the Blackwell recipe. Here each 128 x 128 weight tile and each 1 x 128
+// activation slice along K carries one UE8M0 scale; the MMA applies scales per
+// 32-deep K slice (scale_vec::1X), so the four slices of a 128-wide K block
+// read the same scale byte (fp8_layout.cuh). Products and fp32 accumulation
+// happen in the tensor core; only the summation order differs from the fp64
+// reference.
+//
+// Row-grouped GEMMs only (forward FC1 + SwiGLU, FC2, and the two data
+// gradients); the weight gradients stay on the bf16 path (their cost is the
+// bf16 weight-gradient writes, not the MMA rate).
+//
+// One persistent kernel per GEMM, one CTA per SM, 320 threads:
+//   warp 0     TMA producer (one lane): per 128-deep k-block, A (128 rows) and
+//              B (256 columns) E4M3 tiles plus three 512-byte scale atoms;
+//   warp 1     MMA issuer (one lane) and tensor-memory owner: copies the
+//              k-block's scale atoms into tensor memory (tcgen05.cp) and issues
+//              four M=128 N=256 K=32 block-scaled MMAs;
+//   warps 2-9  epilogue, two warps per tensor-memory lane quarter, 128 of the
+//              256 accumulator columns each.
+// Tensor memory: the 128 x 256 fp32 accumulator (columns 0-255) and one
+// scale-factor slot of 16 columns per pipeline stage (A in the first 4, B in
+// the next 8). Two accumulators would fill all 512 columns and leave no room
+// for the scales, so there is one: the epilogue warps copy their 128 columns
+// into registers and release the accumulator before they convert and store,
+// which keeps the tensor cores idle only for the copy.
+#include "fp8_layout.cuh"
+#include "gemm_common.cuh"
+
+namespace moe {
+namespace gg {
+
+constexpr int kF8Threads = 320;
+constexpr int kF8Stages = 4;
+constexpr int kF8BK = 128;                        // E4M3 elements (= bytes) per k-block
+constexpr int kF8BN = 256;
+constexpr int kF8ABytes = BM * kF8BK;             // 16 KB
+constexpr int kF8BBytes = kF8BN * kF8BK;          // 32 KB
+constexpr int kF8Stage = kF8ABytes + kF8BBytes;
+constexpr int kF8SfStage = 3 * f8::kAtomBytes;    // A's atom, then B's two (128 columns each)
+constexpr int kF8EpiWarps = 8;
+constexpr int kF8Smem =
+    kF8Stages * (kF8Stage + kF8SfStage) + kCtrlBytes + kF8EpiWarps * kBoxBytes + 1024;
+constexpr uint32_t kF8TmemCols = 512;
+constexpr uint32_t kF8SfCol = 256;                // first scale-factor column
+constexpr uint32_t kF8SfSlotCols = 16;
+static_assert(kF8Smem <= 232448, "FP8 grouped GEMM shared memory");
+static_assert(kF8SfCol + kF8Stages * kF8SfSlotCols <= kF8TmemCols, "FP8 tensor-memory columns");
+
+// One 32 x 32 bf16 box (this warp's 32 rows, 32 columns) through the warp's
+// staging slot to global memory by TMA.
+__device__ __forceinline__ void f8_store_box(const CUtensorMap* tm, uint8_t* stage,
+                                             uint32_t stage_u32, int lane, const uint4 (&v)[4],
+                                             int c0, int c1) {
+  if (lane == 0) ptx::tma_store_wait_read();       // the slot's previous box has been read
+  __syncwarp();
+  stage_row(stage, 0, lane, v);
+  ptx::fence_proxy_async_smem();
+  __syncwarp();
+  if (lane == 0) {
+    ptx::tma_store_2d(tm, stage_u32, c0, c1);
+    ptx::tma_store_commit();
+  }
+}
+
+__device__ __forceinline__ const uint32_t (&slice32(const uint32_t (&r)[128], int i))[32] {
+  return *reinterpret_cast<const uint32_t(*)[32]>(&r[32 * i]);
+}
+
+template <int EPI, int B_MN>
+__global__ void __launch_bounds__(kF8Threads, 1)
+grouped_gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmA,
+                        const __grid_constant__ CUtensorMap tmB,
+                        const __grid_constant__ CUtensorMap tmC,
+                        const __grid_constant__ CUtensorMap tmC2, const Params p) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = ptx::smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* sbase = smem_raw + (base - raw);
+  const uint32_t sf_u = base + kF8Stages * kF8Stage;
+  const uint32_t ctrl_u = sf_u + kF8Stages * kF8SfStage;
+  uint8_t* ctrl = sbase + (ctrl_u - base);
+  const uint32_t epi_u = ctrl_u + kCtrlBytes;
+  uint8_t* epi = ctrl + kCtrlBytes;
+  const uint32_t bar_full = ctrl_u;                       // [kF8Stages]
+  const uint32_t bar_empty = ctrl_u + 8 * kF8Stages;      // [kF8Stages]
+  const uint32_t bar_tfull = ctrl_u + 16 * kF8Stages;
+  const uint32_t bar_tempty = bar_tfull + 8;
+  const uint32_t bar_drain = bar_tfull + 16;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(ctrl + 192);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(ctrl + 196);
+  int* prefix = reinterpret_cast<int*>(ctrl + 256);
+  int* mtiles = reinterpret_cast<int*>(ctrl + 1344);
+  int* s_off = reinterpret_cast<int*>(ctrl + 2432);
+  int* s_cnt = reinterpret_cast<int*>(ctrl + 3520);
+  int* tmp = reinterpret_cast<int*>(ctrl + 4608);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int G = p.G;
+  const int NT = (EPI == kEpiSwigluFwd) ? p.F / (kF8BN / 2) : p.N / kF8BN;
+  const int nk = p.K / kF8BK;
+  for (int g = tid; g < G; g += kF8Threads) {
+    const int c = p.counts[g];
+    s_cnt[g] = c;
+    s_off[g] = p.offsets[g];
+    const int mt = (c + BM - 1) / BM;
+    mtiles[g] = mt;
+    prefix[g] = mt * NT;
+  }
+  if (tid == 0) *abort_flag = 0;
+  __syncthreads();
+  const int total = block_exclusive_scan(prefix, G, tmp);
+  if (tid == 0) prefix[G] = total;
+  __syncthreads();
+  if ((int)blockIdx.x >= total) return;
+
+  if (tid == 0) {
+    for (int s = 0; s < kF8Stages; ++s) {
+      ptx::mbar_init(bar_full + 8 * s, 1);
+      ptx::mbar_init(bar_empty + 8 * s, 1);
+    }
+    ptx::mbar_init(bar_tfull, 1);
+    ptx::mbar_init(bar_tempty, kF8EpiWarps);
+    ptx::mbar_init(bar_drain, 1);
+    ptx::fence_mbar_init();
+  }
+  if (warp == 1) {
+    ptx::tmem_alloc(ptx::smem_u32(tmem_slot), kF8TmemCols);
+    ptx::tmem_relinquish();
+  }
+  if (tid == 0) {
+    ptx::tma_prefetch_desc(&tmA);
+    ptx::tma_prefetch_desc(&tmB);
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      uint32_t stage = 0, phase = 0;
+      uint32_t issued_mask = 0, issued_phase = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+        const Tile t = decode(tile, prefix, mtiles, s_cnt, G, 0, p.K, NT, 0);
+        const int row0 = s_off[t.g] + t.mt * BM;
+        // B: two 128-row (K-major) or 128-column (MN-major) boxes and their atoms
+        int b0, b1, nb0, nb1;
+        if (EPI == kEpiSwigluFwd) {
+          const int f0 = t.nt * (kF8BN / 2);              // gate rows f0.., up rows F+f0..
+          b0 = f0;
+          b1 = p.F + f0;
+        } else {
+          b0 = t.nt * kF8BN;
+          b1 = b0 + 128;
+        }
+        nb0 = b0 / 128;
+        nb1 = b1 / 128;
+        const uint8_t* sfa = p.sfa + (int64_t)(row0 / 128) * p.sfa_kg * f8::kAtomBytes;
+        const uint8_t* sfb0 =
+            p.sfb + ((int64_t)t.g * p.sfb_nb + nb0) * p.sfb_kg * f8::kAtomBytes;
+        const uint8_t* sfb1 =
+            p.sfb + ((int64_t)t.g * p.sfb_nb + nb1) * p.sfb_kg * f8::kAtomBytes;
+        for (int kb = 0; kb < nk; ++kb) {
+          if (!ptx::mbar_wait(bar_empty + 8 * stage, phase ^ 1u, kWaitBudget, abort_flag)) {
+            ok = false;
+            break;
+          }
+          const uint32_t fb = bar_full + 8 * stage;
+          ptx::mbar_arrive_expect_tx(fb, kF8Stage + kF8SfStage);
+          const uint32_t sA = base + stage * kF8Stage;
+          const uint32_t sB = sA + kF8ABytes;
+          const int k0 = kb * kF8BK;
+          ptx::tma_load_2d(sA, &tmA, fb, k0, row0);
+          if (B_MN == 0) {
+            ptx::tma_load_2d(sB, &tmB, fb, k0, t.g * p.b_rows + b0);
+            ptx::tma_load_2d(sB + 16384, &tmB, fb, k0, t.g * p.b_rows + b1);
+          } else {
+            ptx::tma_load_2d(sB, &tmB, fb, b0, t.g * p.b_rows + k0);
+            ptx::tma_load_2d(sB + 16384, &tmB, fb, b1, t.g * p.b_rows + k0);
+          }
+          const uint32_t sfs = sf_u + stage * kF8SfStage;
+          const int64_t a4 = (int64_t)(kb / f8::kAtomKBlocks) * f8::kAtomBytes;
+          ptx::bulk_load(sfs, sfa + a4, f8::kAtomBytes, fb);
+          ptx::bulk_load(sfs + f8::kAtomBytes, sfb0 + a4, f8::kAtomBytes, fb);
+          ptx::bulk_load(sfs + 2 * f8::kAtomBytes, sfb1 + a4, f8::kAtomBytes, fb);
+          issued_mask |= 1u << stage;
+          issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
+          if (++stage == kF8Stages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      if (!ok) {
+        record_status(p.status, MOE_ERR_TIMEOUT);
+        *abort_flag = 1;
+      }
+      // every load issued must land before the CTA may exit
+      for (int s = 0; s < kF8Stages; ++s)
+        if (issued_mask & (1u << s))
+          ptx::mbar_wait(bar_full + 8 * s, (issued_phase >> s) & 1u, kWaitBudget, nullptr);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t IDESC = ptx::idesc_mxf8_e4m3(BM, kF8BN, 0, B_MN);
+      uint32_t stage = 0, phase = 0, acc_phase = 0;
+      bool ok = true, issued = false;
+      for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+        if (!ptx::mbar_wait(bar_tempty, acc_phase ^ 1u, kWaitBudget, abort_flag)) {
+          ok = false;
+          break;
+        }
+        ptx::tc_fence_after();
+        for (int kb = 0; kb < nk; ++kb) {
+          if (!ptx::mbar_wait(bar_full + 8 * stage, phase, kWaitBudget, abort_flag)) {
+            ok = false;
+            break;
+          }
+          ptx::tc_fence_after();
+          const uint32_t sfs = sf_u + stage * kF8SfStage;
+          const uint32_t sfa_t = tmem_base + kF8SfCol + kF8SfSlotCols * stage;
+          const uint32_t sfb_t = sfa_t + 4;
+          ptx::tmem_cp_32x128b_warpx4(sfa_t, ptx::smem_desc_sf(sfs));
+          ptx::tmem_cp_32x128b_warpx4(sfb_t, ptx::smem_desc_sf(sfs + f8::kAtomBytes));
+          ptx::tmem_cp_32x128b_warpx4(sfb_t + 4, ptx::smem_desc_sf(sfs + 2 * f8::kAtomBytes));
+          const uint32_t idesc = ptx::idesc_with_sf_id(IDESC, (uint32_t)kb & 3u);
+          const uint32_t sA = base + stage * kF8Stage;
+          const uint32_t sB = sA + kF8ABytes;
+#pragma unroll
+          for (int kk = 0; kk < kF8BK / 32; ++kk) {
+            const uint64_t ad = ptx::smem_desc_sw128(sA + kk * 32, 16, 1024);
+            const uint64_t bd = B_MN ? ptx::smem_desc_sw128(sB + kk * 4096, 16384, 1024)
+                                     : ptx::smem_desc_sw128(sB + kk * 32, 16, 1024);
+            ptx::mma_mxf8(tmem_base, ad, bd, idesc, sfa_t, sfb_t, (kb | kk) ? 1u : 0u);
+          }
+          issued = true;
+          ptx::mma_commit(bar_empty + 8 * stage);
+          if (++stage == kF8Stages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        ptx::mma_commit(bar_tfull);
+        acc_phase ^= 1u;
+      }
+      if (!ok) {
+        record_status(p.status, MOE_ERR_TIMEOUT);
+        *abort_flag = 1;
+      }
+      // wait for every MMA issued by this thread before tensor memory is freed
+      if (issued) {
+        ptx::mma_commit(bar_drain);
+        ptx::mbar_wait(bar_drain, 0, kWaitBudget, nullptr);
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int q = warp & 3;                       // tensor-memory lane quarter
+    const int half = (warp - 2) >> 2;             // which 128 accumulator columns
+    uint8_t* stage = epi + (warp - 2) * kBoxBytes;
+    const uint32_t stage_u32 = epi_u + (warp - 2) * kBoxBytes;
+    const uint32_t tq = tmem_base + ((uint32_t)(q * 32) << 16);
+    uint32_t acc_phase = 0;
+    for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
+      const Tile t = decode(tile, prefix, mtiles, s_cnt, G, 0, p.K, NT, 0);
+      const int row0 = s_off[t.g] + t.mt * BM + q * 32;
+      // SwiGLU backward: G and U of the first 32 columns, loaded before the wait
+      const __nv_bfloat16* gu = nullptr;
+      uint4 gq[4], uq[4];
+      int fb = 0;
+      if (EPI == kEpiSwigluBwd) {
+        fb = t.nt * kF8BN + 128 * half;
+        gu = p.aux + (long long)(row0 + lane) * p.ldaux;
+#pragma unroll
+        for (int v = 0; v < 4; ++v) {
+          gq[v] = ldg_nc_v4(gu + fb + v * 8);
+          uq[v] = ldg_nc_v4(gu + p.F + fb + v * 8);
+        }
+      }
+      bool ok = ptx::mbar_wait(bar_tfull, acc_phase, kWaitBudget, abort_flag);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) {
+        if (lane == 0) {
+          record_status(p.status, MOE_ERR_TIMEOUT);
+          *abort_flag = 1;
+        }
+        break;
+      }
+      ptx::tc_fence_after();
+      uint32_t r[128];
+      if (EPI == kEpiSwigluFwd) {
+        // gate columns 64*half .. +63 and the matching up columns 128 + 64*half ..
+        ptx::tmem_ld32(tq + 64 * half, *reinterpret_cast<uint32_t(*)[32]>(&r[0]));
+        ptx::tmem_ld32(tq + 64 * half + 32, *reinterpret_cast<uint32_t(*)[32]>(&r[32]));
+        ptx::tmem_ld32(tq + 128 + 64 * half, *reinterpret_cast<uint32_t(*)[32]>(&r[64]));
+        ptx::tmem_ld32(tq + 160 + 64 * half, *reinterpret_cast<uint32_t(*)[32]>(&r[96]));
+      } else {
+        ptx::tmem_ld128(tq + 128 * half, r);
+      }
+      ptx::tmem_ld_wait();
+      // the accumulator is free for the next tile's MMAs
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(bar_tempty);
+      acc_phase ^= 1u;
+
+      if (EPI == kEpiSwigluFwd) {
+        const int f0 = t.nt * (kF8BN / 2) + 64 * half;
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          uint4 go[4], uo[4], ho[4];
+          pack_slice(slice32(r, c), go);
+          pack_slice(slice32(r, 2 + c), uo);
+#pragma unroll
+          for (int v = 0; v < 4; ++v) {
+            float gr[8], ur[8], hf[8];
+            unpack8(go[v], gr);
+            unpack8(uo[v], ur);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) hf[i] = silu_f(gr[i]) * ur[i];
+            ho[v] = pack8(hf);
+          }
+          f8_store_box(&tmC, stage, stage_u32, lane, go, f0 + 32 * c, row0);          // G
+          f8_store_box(&tmC, stage, stage_u32, lane, uo, p.F + f0 + 32 * c, row0);    // U
+          f8_store_box(&tmC2, stage, stage_u32, lane, ho, f0 + 32 * c, row0);         // h
+        }
+      } else if (EPI == kEpiSwigluBwd) {
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint4 dg[4], du[4];
+#pragma unroll
+          for (int v = 0; v < 4; ++v) swiglu_bwd8(&r[32 * c + 8 * v], gq[v], uq[v], dg[v], du[v]);
+          if (c + 1 < 4) {
+#pragma unroll
+            for (int v = 0; v < 4; ++v) {
+              gq[v] = ldg_nc_v4(gu + fb + 32 * (c + 1) + v * 8);
+              uq[v] = ldg_nc_v4(gu + p.F + fb + 32 * (c + 1) + v * 8);
+            }
+          }
+          f8_store_box(&tmC, stage, stage_u32, lane, dg, fb + 32 * c, row0);          // dG
+          f8_store_box(&tmC, stage, stage_u32, lane, du, p.F + fb + 32 * c, row0);    // dU
+        }
+      } else {
+        // plain store (FC2) or FC1 data gradient plus the row's router term
+        const int f0 = t.nt * kF8BN + 128 * half;
+        float rd = 0.f;
+        const float* rw = nullptr;
+        if (EPI == kEpiDgradRouter && t.g < p.router_E) {
+          const int tk = p.token_of[row0 + lane];
+          if (tk >= 0 && tk < p.router_T) rd = p.dlogits[(long long)tk * p.router_E + t.g];
+          rw = p.W_r + (long long)t.g * p.N + f0;
+        }
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          if (EPI == kEpiDgradRouter && rw) {
+#pragma unroll
+            for (int v = 0; v < 8; ++v) {
+              const float4 w4 = __ldg(reinterpret_cast<const float4*>(rw + 32 * c) + v);
+              float* a = reinterpret_cast<float*>(&r[32 * c + 4 * v]);
+              a[0] = fmaf(rd, w4.x, a[0]);
+              a[1] = fmaf(rd, w4.y, a[1]);
+              a[2] = fmaf(rd, w4.z, a[2]);
+              a[3] = fmaf(rd, w4.w, a[3]);
+            }
+          }
+          uint4 o[4];
+          pack_slice(slice32(r, c), o);
+          f8_store_box(&tmC, stage, stage_u32, lane, o, f0 + 32 * c, row0);
+        }
+      }
+    }
+    if (lane == 0) ptx::tma_store_wait_all();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem_base, kF8TmemCols);
+  }
+}
+
+template <int EPI, int B_MN>
+static cudaError_t run_fp8(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& c,
+                           const CUtensorMap& c2, const Params& p, cudaStream_t s) {
+  auto kern = grouped_gemm_fp8_kernel<EPI, B_MN>;
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kF8Smem);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  kern<<<num_sms(), kF8Threads, kF8Smem, s>>>(a, b, c, c2, p);
+  return cudaGetLastError();
+}
+
+}  // namespace gg
+
+using namespace gg;
+
+// FC1 + SwiGLU: GU = x_q W13_q^T (gate | up, bf16), h = bf16(silu(G) U).
+cudaError_t launch_ffn_fc1_fp8(const moe_config& c, const uint8_t* xq, const uint8_t* xsf,
+                               const int32_t* counts, const int32_t* offsets, const uint8_t* W13q,
+                               const uint8_t* W13sf, void* GU, void* h, int32_t* status,
+                               cudaStream_t s) {
+  const int64_t R = rows_max(c);
+  const int G = c.E + c.n_shared;
+  CUtensorMap a, b, oc, oc2;
+  if (!make_map_u8(&a, xq, c.H, R) || !make_map_u8(&b, W13q, c.H, (uint64_t)G * 2 * c.F) ||
+      !make_out_map(&oc, GU, 2ULL * c.F, R) || !make_out_map(&oc2, h, c.F, R))
+    return cudaErrorInvalidValue;
+  Params p = base_params(c, counts, offsets, status);
+  p.K = c.H;
+  p.b_rows = 2 * c.F;
+  p.sfa = xsf;
+  p.sfa_kg = (int)f8::atoms_k(c.H);
+  p.sfb = W13sf;
+  p.sfb_nb = 2 * c.F / 128;
+  p.sfb_kg = (int)f8::atoms_k(c.H);
+  return run_fp8<kEpiSwigluFwd, 0>(a, b, oc, oc2, p, s);
+}
+
+// FC2: y_perm = h_q W2_q^T (bf16).
+cudaError_t launch_ffn_fc2_fp8(const moe_config& c, const uint8_t* hq, const uint8_t* hsf,
+                               const int32_t* counts, const int32_t* offsets, const uint8_t* W2q,
+                               const uint8_t* W2sf, void* y_perm, int32_t* status,
+                               cudaStream_t s) {
+  const int64_t R = rows_max(c);
+  const int G = c.E + c.n_shared;
+  CUtensorMap a, b, oc;
+  if (!make_map_u8(&a, hq, c.F, R) || !make_map_u8(&b, W2q, c.F, (uint64_t)G * c.H) ||
+      !make_out_map(&oc, y_perm, c.H, R))
+    return cudaErrorInvalidValue;
+  Params p = base_params(c, counts, offsets, status);
+  p.N = c.H;
+  p.K = c.F;
+  p.b_rows = c.H;
+  p.sfa = hsf;
+  p.sfa_kg = (int)f8::atoms_k(c.F);
+  p.sfb = W2sf;
+  p.sfb_nb = c.H / 128;
+  p.sfb_kg = (int)f8::atoms_k(c.F);
+  return run_fp8<kEpiStore, 0>(a, b, oc, oc, p, s);
+}
+
+// FC2 data gradient + SwiGLU backward: dh = dO_q W2_q (fp32, W2 read
+// transposed: MN-major B), then dG, dU from the stored GU (bf16).
+cudaError_t launch_ffn_fc2_dgrad_fp8(const moe_config& c, const uint8_t* dOq, const uint8_t* dOsf,
+                                     const int32_t* counts, const int32_t* offsets,
+                                     const uint8_t* W2q, const uint8_t* W2sf_t, const void* GU,
+                                     void* dGU, int32_t* status, cudaStream_t s) {
+  const int64_t R = rows_max(c);
+  const int G = c.E + c.n_shared;
+  CUtensorMap a, b, oc;
+  if (!make_map_u8(&a, dOq, c.H, R) || !make_map_u8(&b, W2q, c.F, (uint64_t)G * c.H) ||
+      !make_out_map(&oc, dGU, 2ULL * c.F, R))
+    return cudaErrorInvalidValue;
+  Params p = base_params(c, counts, offsets, status);
+  p.N = c.F;
+  p.K = c.H;
+  p.b_rows = c.H;
+  p.aux = static_cast<const __nv_bfloat16*>(GU);
+  p.ldaux = 2LL * c.F;
+  p.sfa = dOsf;
+  p.sfa_kg = (int)f8::atoms_k(c.H);
+  p.sfb = W2sf_t;
+  p.sfb_nb = c.F / 128;
+  p.sfb_kg = (int)f8::atoms_k(c.H);
+  return run_fp8<kEpiSwigluBwd, 1>(a, b, oc, oc, p, s);
+}
+
+// FC1 data gradient: dX_perm = bf16(dGU_q W13_q + the row's router term)
+// (W13 read transposed: MN-major B).
+cudaError_t launch_ffn_fc1_dgrad_fp8(const moe_config& c, const uint8_t* dGq, const uint8_t* dGsf,
+                                     const int32_t* counts, const int32_t* offsets,
+                                     const uint8_t* W13q, const uint8_t* W13sf_t,
+                                     const int32_t* token_of, const float* dlogits,
+                                     const float* W_r, void* dX_perm, int32_t* status,
+                                     cudaStream_t s) {
+  const int64_t R = rows_max(c);
+  const int G = c.E + c.n_shared;
+  CUtensorMap a, b, oc;
+  if (!make_map_u8(&a, dGq, 2ULL * c.F, R) || !make_map_u8(&b, W13q, c.H, (uint64_t)G * 2 * c.F) ||
+      !make_out_map(&oc, dX_perm, c.H, R))
+    return cudaErrorInvalidValue;
+  Params p = base_params(c, counts, offsets, status);
+  p.N = c.H;
+  p.K = 2 * c.F;
+  p.b_rows = 2 * c.F;
+  p.token_of = token_of;
+  p.dlogits = dlogits;
+  p.W_r = W_r;
+  p.router_E = c.E;
+  p.router_T = c.T;
+  p.sfa = dGsf;
+  p.sfa_kg = (int)f8::atoms_k(2LL * c.F);
+  p.sfb = W13sf_t;
+  p.sfb_nb = c.H / 128;
+  p.sfb_kg = (int)f8::atoms_k(2LL * c.F);
+  return run_fp8<kEpiDgradRouter, 1>(a, b, oc, oc, p, s);
+}
+
+}  // namespace moe

@@ -60,23 +60,40 @@ cudaError_t launch_route_aux_bwd(const moe_config& c, const void* x, const float
 int64_t aux_partial_bytes(const moe_config& c);    // the aux-loss region of scratch
 int64_t aux_partial_offset(const moe_config& c);   // its byte offset in scratch
 
-// FP8 block quantisation (E4M3 values with power-of-two scales, stored as bf16).
-cudaError_t launch_quant_tiles(const void* W, void* Wq, int G, int rows, int cols, cudaStream_t s);
-cudaError_t launch_quant_rows(const void* X, void* Xq, const int32_t* offsets,
-                              const int32_t* counts, int G, int64_t rows_max, int cols,
-                              cudaStream_t s);
+// FP8 block quantisation (E4M3 values with power-of-two block scales):
+// 1-byte codes with UE8M0 scale atoms (fp8_layout.cuh) for the FP8 GEMMs --
+// weights in 128x128 tiles (atoms for both orientations of the weight),
+// activations in 1x128 slices along their rows -- and, for the bf16-path
+// weight gradients, the dequantised values of 128x1 slices along the tokens.
+cudaError_t launch_quant_tiles8(const void* W, uint8_t* Wq, uint8_t* sf_f, uint8_t* sf_d, int G,
+                                int rows, int cols, cudaStream_t s);
+cudaError_t launch_quant_rows8(const void* X, uint8_t* Xq, uint8_t* sf, const int32_t* offsets,
+                               const int32_t* counts, int G, int64_t rows_max, int cols,
+                               cudaStream_t s);
 cudaError_t launch_quant_cols(const void* X, void* Xq, const int32_t* offsets,
                               const int32_t* counts, int G, int64_t rows_max, int cols,
                               cudaStream_t s);
 
 // Where the FP8 mode keeps its quantised tensors inside `scratch`.
 struct Fp8Scratch {
-  void* W13q;   // [G,2F,H]
-  void* W2q;    // [G,H,F]
-  void* aH;     // [R,H]  x_perm rows, then x_perm columns
-  void* bF;     // [R,F]  h rows, then h columns
-  void* cH;     // [R,H]  dO rows, then dO columns
-  void* d2F;    // [R,2F] dGU rows, then dGU columns
+  uint8_t* W13q;    // [G,2F,H] E4M3
+  uint8_t* W13sf;   // atoms, N = W13 rows, K = H (forward)
+  uint8_t* W13sft;  // atoms, N = H, K = W13 rows (FC1 data gradient)
+  uint8_t* W2q;     // [G,H,F] E4M3
+  uint8_t* W2sf;    // atoms, N = H, K = F (forward)
+  uint8_t* W2sft;   // atoms, N = F, K = H (FC2 data gradient)
+  uint8_t* xq;      // [R,H] x_perm, 1x128 slices
+  uint8_t* xsf;
+  uint8_t* hq;      // [R,F] h
+  uint8_t* hsf;
+  uint8_t* dOq;     // [R,H] dO
+  uint8_t* dOsf;
+  uint8_t* dGq;     // [R,2F] dGU
+  uint8_t* dGsf;
+  void* cH;         // [R,H]  bf16 values of dO in 128x1 slices   (weight gradients)
+  void* bF;         // [R,F]  h
+  void* d2F;        // [R,2F] dGU
+  void* aH;         // [R,H]  x_perm
 };
 Fp8Scratch fp8_scratch(const moe_config& c, void* scratch);
 
@@ -121,5 +138,27 @@ cudaError_t launch_ffn_wgrad_fc2(const moe_config& c, const void* dO_perm, const
 cudaError_t launch_ffn_wgrad_fc1(const moe_config& c, const void* dGU, const void* x_perm,
                                  const int32_t* counts, const int32_t* offsets, void* dW13,
                                  int32_t* status, cudaStream_t s);
+
+// The FP8 configuration's forward and data-gradient GEMMs on the block-scaled
+// FP8 tensor cores (tcgen05 kind::mxf8f6f4): E4M3 operands with UE8M0 scale
+// atoms; the same epilogues and outputs as the bf16 launches above.
+cudaError_t launch_ffn_fc1_fp8(const moe_config& c, const uint8_t* xq, const uint8_t* xsf,
+                               const int32_t* counts, const int32_t* offsets, const uint8_t* W13q,
+                               const uint8_t* W13sf, void* GU, void* h, int32_t* status,
+                               cudaStream_t s);
+cudaError_t launch_ffn_fc2_fp8(const moe_config& c, const uint8_t* hq, const uint8_t* hsf,
+                               const int32_t* counts, const int32_t* offsets, const uint8_t* W2q,
+                               const uint8_t* W2sf, void* y_perm, int32_t* status,
+                               cudaStream_t s);
+cudaError_t launch_ffn_fc2_dgrad_fp8(const moe_config& c, const uint8_t* dOq, const uint8_t* dOsf,
+                                     const int32_t* counts, const int32_t* offsets,
+                                     const uint8_t* W2q, const uint8_t* W2sf_t, const void* GU,
+                                     void* dGU, int32_t* status, cudaStream_t s);
+cudaError_t launch_ffn_fc1_dgrad_fp8(const moe_config& c, const uint8_t* dGq, const uint8_t* dGsf,
+                                     const int32_t* counts, const int32_t* offsets,
+                                     const uint8_t* W13q, const uint8_t* W13sf_t,
+                                     const int32_t* token_of, const float* dlogits,
+                                     const float* W_r, void* dX_perm, int32_t* status,
+                                     cudaStream_t s);
 
 }  // namespace moe

@@ -5,6 +5,7 @@
 #include <stdio.h>
 
 #include "common.cuh"
+#include "fp8_layout.cuh"
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -56,31 +57,56 @@ static int64_t base_scratch_bytes(const moe_config& c) {
   return aux_partial_offset(c) + aux_partial_bytes(c);
 }
 
+// The FP8 mode's region of scratch, in order: the E4M3 weights with their
+// scale atoms for both orientations, the 1-byte activations (x_perm, h, dO,
+// dGU in 1x128 slices) with their atoms, and the bf16 values of the 128x1
+// slices that the weight gradients read.
+static int64_t fp8_region(const moe_config& c, Fp8Scratch* f, uint8_t* p) {
+  const int64_t G = c.E + c.n_shared, R = rows_max(c), H = c.H, F = c.F;
+  const int64_t sizes[18] = {
+      G * 2 * F * H, f8::sf_bytes(G * 2 * F, H), f8::sf_bytes(G * H, 2 * F),
+      G * H * F,     f8::sf_bytes(G * H, F),     f8::sf_bytes(G * F, H),
+      R * H, f8::sf_bytes(R, H), R * F, f8::sf_bytes(R, F),
+      R * H, f8::sf_bytes(R, H), R * 2 * F, f8::sf_bytes(R, 2 * F),
+      R * H * 2, R * F * 2, R * 2 * F * 2, R * H * 2};
+  uint8_t* ptrs[18];
+  int64_t off = 0;
+  for (int i = 0; i < 18; ++i) {
+    ptrs[i] = p ? p + off : nullptr;
+    off += align256(sizes[i]);
+  }
+  if (f) {
+    f->W13q = ptrs[0];
+    f->W13sf = ptrs[1];
+    f->W13sft = ptrs[2];
+    f->W2q = ptrs[3];
+    f->W2sf = ptrs[4];
+    f->W2sft = ptrs[5];
+    f->xq = ptrs[6];
+    f->xsf = ptrs[7];
+    f->hq = ptrs[8];
+    f->hsf = ptrs[9];
+    f->dOq = ptrs[10];
+    f->dOsf = ptrs[11];
+    f->dGq = ptrs[12];
+    f->dGsf = ptrs[13];
+    f->cH = ptrs[14];
+    f->bF = ptrs[15];
+    f->d2F = ptrs[16];
+    f->aH = ptrs[17];
+  }
+  return off;
+}
+
 int64_t scratch_bytes(const moe_config& c) {
   int64_t b = base_scratch_bytes(c);
-  if (c.dtype == MOE_DTYPE_FP8_E4M3_BLOCK) {
-    const int64_t G = c.E + c.n_shared, R = rows_max(c), H = c.H, F = c.F;
-    b += align256(G * 2 * F * H * 2) + align256(G * H * F * 2);
-    b += 2 * align256(R * H * 2) + align256(R * F * 2) + align256(R * 2 * F * 2);
-  }
+  if (c.dtype == MOE_DTYPE_FP8_E4M3_BLOCK) b += fp8_region(c, nullptr, nullptr);
   return b;
 }
 
 Fp8Scratch fp8_scratch(const moe_config& c, void* scratch) {
-  const int64_t G = c.E + c.n_shared, R = rows_max(c), H = c.H, F = c.F;
-  uint8_t* p = static_cast<uint8_t*>(scratch) + base_scratch_bytes(c);
   Fp8Scratch f;
-  f.W13q = p;
-  p += align256(G * 2 * F * H * 2);
-  f.W2q = p;
-  p += align256(G * H * F * 2);
-  f.aH = p;
-  p += align256(R * H * 2);
-  f.bF = p;
-  p += align256(R * F * 2);
-  f.cH = p;
-  p += align256(R * H * 2);
-  f.d2F = p;
+  fp8_region(c, &f, static_cast<uint8_t*>(scratch) + base_scratch_bytes(c));
   return f;
 }
 
@@ -102,7 +128,8 @@ moe_status check_config(const moe_config* c) {
   if (c->row_align < 128 || c->row_align % 128) return MOE_ERR_INVALID_ARG;
   if (c->dtype != MOE_DTYPE_BF16 && c->dtype != MOE_DTYPE_FP8_E4M3_BLOCK)
     return MOE_ERR_INVALID_ARG;
-  if (c->dtype == MOE_DTYPE_FP8_E4M3_BLOCK && c->n_shared != 0) return MOE_ERR_UNSUPPORTED;
+  if (c->dtype == MOE_DTYPE_FP8_E4M3_BLOCK && (c->n_shared != 0 || c->H % 256 || c->F % 256))
+    return MOE_ERR_UNSUPPORTED;
   if ((int64_t)c->T * c->k >= (1LL << 31) || rows_max(*c) >= (1LL << 31))
     return MOE_ERR_INVALID_ARG;
   if ((int64_t)c->E * 2 * c->F >= (1LL << 31) || (int64_t)(c->E + c->n_shared) * c->H >= (1LL << 31))
@@ -238,6 +265,19 @@ moe_status moe_permute(const moe_config* cfg, const void* x, const int32_t* idx,
   return MOE_OK;
 }
 
+moe_status moe_quantize_weights(const moe_config* cfg, const void* W13, const void* W2,
+                                void* scratch, void* stream) {
+  MOE_TRY(check_config(cfg));
+  MOE_REQUIRE(al16(W13) && al16(W2) && al16(scratch));
+  if (cfg->dtype != MOE_DTYPE_FP8_E4M3_BLOCK) return MOE_OK;
+  cudaStream_t s = (cudaStream_t)stream;
+  const Fp8Scratch q = fp8_scratch(*cfg, scratch);
+  const int G = cfg->E + cfg->n_shared;
+  MOE_CUDA(launch_quant_tiles8(W13, q.W13q, q.W13sf, q.W13sft, G, 2 * cfg->F, cfg->H, s));
+  MOE_CUDA(launch_quant_tiles8(W2, q.W2q, q.W2sf, q.W2sft, G, cfg->H, cfg->F, s));
+  return MOE_OK;
+}
+
 moe_status moe_grouped_ffn_fwd(const moe_config* cfg, const void* x_perm, const int32_t* counts,
                                const int32_t* offsets, const void* W13, const void* W2, void* GU,
                                void* h, void* y_perm, void* scratch, void* stream) {
@@ -247,15 +287,14 @@ moe_status moe_grouped_ffn_fwd(const moe_config* cfg, const void* x_perm, const 
   cudaStream_t s = (cudaStream_t)stream;
   int32_t* st = status_word(scratch);
   if (cfg->dtype == MOE_DTYPE_FP8_E4M3_BLOCK) {
+    // the E4M3 weights are the ones moe_quantize_weights left in scratch
     const Fp8Scratch q = fp8_scratch(*cfg, scratch);
     const int G = cfg->E + cfg->n_shared;
     const int64_t R = rows_max(*cfg);
-    MOE_CUDA(launch_quant_tiles(W13, q.W13q, G, 2 * cfg->F, cfg->H, s));
-    MOE_CUDA(launch_quant_tiles(W2, q.W2q, G, cfg->H, cfg->F, s));
-    MOE_CUDA(launch_quant_rows(x_perm, q.aH, offsets, counts, G, R, cfg->H, s));
-    MOE_CUDA(launch_ffn_fc1(*cfg, q.aH, counts, offsets, q.W13q, GU, h, st, s));
-    MOE_CUDA(launch_quant_rows(h, q.bF, offsets, counts, G, R, cfg->F, s));
-    MOE_CUDA(launch_ffn_fc2(*cfg, q.bF, counts, offsets, q.W2q, y_perm, st, s));
+    MOE_CUDA(launch_quant_rows8(x_perm, q.xq, q.xsf, offsets, counts, G, R, cfg->H, s));
+    MOE_CUDA(launch_ffn_fc1_fp8(*cfg, q.xq, q.xsf, counts, offsets, q.W13q, q.W13sf, GU, h, st, s));
+    MOE_CUDA(launch_quant_rows8(h, q.hq, q.hsf, offsets, counts, G, R, cfg->F, s));
+    MOE_CUDA(launch_ffn_fc2_fp8(*cfg, q.hq, q.hsf, counts, offsets, q.W2q, q.W2sf, y_perm, st, s));
     return MOE_OK;
   }
   MOE_CUDA(launch_ffn_fc1(*cfg, x_perm, counts, offsets, W13, GU, h, st, s));
@@ -282,43 +321,73 @@ moe_status moe_unpermute_bwd(const moe_config* cfg, const void* dY, const void* 
   return MOE_OK;
 }
 
+moe_status moe_grouped_ffn_dgrad(const moe_config* cfg, const void* dO_perm, const void* GU,
+                                 const int32_t* counts, const int32_t* offsets,
+                                 const int32_t* token_of, const float* dlogits, const float* W_r,
+                                 const void* W13, const void* W2, void* dGU, void* dX_perm,
+                                 void* scratch, void* stream) {
+  MOE_TRY(check_config(cfg));
+  MOE_REQUIRE(al16(dO_perm) && al16(GU) && al4(counts) && al4(offsets) && al4(token_of));
+  MOE_REQUIRE(tok4(cfg, dlogits) && al16(W_r) && al16(W13) && al16(W2) && al16(dGU));
+  MOE_REQUIRE(al16(dX_perm) && al16(scratch));
+  cudaStream_t s = (cudaStream_t)stream;
+  int32_t* st = status_word(scratch);
+  if (cfg->dtype == MOE_DTYPE_FP8_E4M3_BLOCK) {
+    const Fp8Scratch q = fp8_scratch(*cfg, scratch);
+    const int G = cfg->E + cfg->n_shared;
+    const int64_t R = rows_max(*cfg);
+    MOE_CUDA(launch_quant_rows8(dO_perm, q.dOq, q.dOsf, offsets, counts, G, R, cfg->H, s));
+    MOE_CUDA(launch_ffn_fc2_dgrad_fp8(*cfg, q.dOq, q.dOsf, counts, offsets, q.W2q, q.W2sft, GU,
+                                      dGU, st, s));
+    MOE_CUDA(launch_quant_rows8(dGU, q.dGq, q.dGsf, offsets, counts, G, R, 2 * cfg->F, s));
+    MOE_CUDA(launch_ffn_fc1_dgrad_fp8(*cfg, q.dGq, q.dGsf, counts, offsets, q.W13q, q.W13sft,
+                                      token_of, dlogits, W_r, dX_perm, st, s));
+    return MOE_OK;
+  }
+  MOE_CUDA(launch_ffn_fc2_dgrad(*cfg, dO_perm, counts, offsets, W2, GU, dGU, st, s));
+  MOE_CUDA(launch_ffn_fc1_dgrad(*cfg, dGU, counts, offsets, W13, token_of, dlogits, W_r, dX_perm,
+                                st, s));
+  return MOE_OK;
+}
+
+moe_status moe_grouped_ffn_wgrad(const moe_config* cfg, const void* dO_perm, const void* x_perm,
+                                 const void* h, const void* dGU, const int32_t* counts,
+                                 const int32_t* offsets, void* dW13, void* dW2, void* scratch,
+                                 void* stream) {
+  MOE_TRY(check_config(cfg));
+  MOE_REQUIRE(al16(dO_perm) && al16(x_perm) && al16(h) && al16(dGU) && al4(counts));
+  MOE_REQUIRE(al4(offsets) && al16(dW13) && al16(dW2) && al16(scratch));
+  cudaStream_t s = (cudaStream_t)stream;
+  int32_t* st = status_word(scratch);
+  if (cfg->dtype == MOE_DTYPE_FP8_E4M3_BLOCK) {
+    // both operands in 128x1 slices along each expert's tokens, as bf16 values
+    const Fp8Scratch q = fp8_scratch(*cfg, scratch);
+    const int G = cfg->E + cfg->n_shared;
+    const int64_t R = rows_max(*cfg);
+    const int H = cfg->H, F = cfg->F;
+    MOE_CUDA(launch_quant_cols(dO_perm, q.cH, offsets, counts, G, R, H, s));
+    MOE_CUDA(launch_quant_cols(h, q.bF, offsets, counts, G, R, F, s));
+    MOE_CUDA(launch_ffn_wgrad_fc2(*cfg, q.cH, q.bF, counts, offsets, dW2, st, s));
+    MOE_CUDA(launch_quant_cols(dGU, q.d2F, offsets, counts, G, R, 2 * F, s));
+    MOE_CUDA(launch_quant_cols(x_perm, q.aH, offsets, counts, G, R, H, s));
+    MOE_CUDA(launch_ffn_wgrad_fc1(*cfg, q.d2F, q.aH, counts, offsets, dW13, st, s));
+    return MOE_OK;
+  }
+  MOE_CUDA(launch_ffn_wgrad_fc2(*cfg, dO_perm, h, counts, offsets, dW2, st, s));
+  MOE_CUDA(launch_ffn_wgrad_fc1(*cfg, dGU, x_perm, counts, offsets, dW13, st, s));
+  return MOE_OK;
+}
+
 moe_status moe_grouped_ffn_bwd(const moe_config* cfg, const void* dO_perm, const void* x_perm,
                                const void* GU, const void* h, const int32_t* counts,
                                const int32_t* offsets, const int32_t* token_of,
                                const float* dlogits, const float* W_r, const void* W13,
                                const void* W2, void* dGU, void* dX_perm, void* dW13, void* dW2,
                                void* scratch, void* stream) {
-  MOE_TRY(check_config(cfg));
-  MOE_REQUIRE(al16(dO_perm) && al16(x_perm) && al16(GU) && al16(h) && al4(counts));
-  MOE_REQUIRE(al4(offsets) && al4(token_of) && tok4(cfg, dlogits) && al16(W_r));
-  MOE_REQUIRE(al16(W13) && al16(W2) && al16(dGU) && al16(dX_perm));
-  MOE_REQUIRE(al16(dW13) && al16(dW2) && al16(scratch));
-  cudaStream_t s = (cudaStream_t)stream;
-  int32_t* st = status_word(scratch);
-  if (cfg->dtype == MOE_DTYPE_FP8_E4M3_BLOCK) {
-    // the quantised weights are the ones the forward left in scratch
-    const Fp8Scratch q = fp8_scratch(*cfg, scratch);
-    const int G = cfg->E + cfg->n_shared;
-    const int64_t R = rows_max(*cfg);
-    const int H = cfg->H, F = cfg->F;
-    MOE_CUDA(launch_quant_rows(dO_perm, q.cH, offsets, counts, G, R, H, s));
-    MOE_CUDA(launch_ffn_fc2_dgrad(*cfg, q.cH, counts, offsets, q.W2q, GU, dGU, st, s));
-    MOE_CUDA(launch_quant_cols(dO_perm, q.cH, offsets, counts, G, R, H, s));
-    MOE_CUDA(launch_quant_cols(h, q.bF, offsets, counts, G, R, F, s));
-    MOE_CUDA(launch_ffn_wgrad_fc2(*cfg, q.cH, q.bF, counts, offsets, dW2, st, s));
-    MOE_CUDA(launch_quant_rows(dGU, q.d2F, offsets, counts, G, R, 2 * F, s));
-    MOE_CUDA(launch_ffn_fc1_dgrad(*cfg, q.d2F, counts, offsets, q.W13q, token_of, dlogits, W_r,
-                                  dX_perm, st, s));
-    MOE_CUDA(launch_quant_cols(dGU, q.d2F, offsets, counts, G, R, 2 * F, s));
-    MOE_CUDA(launch_quant_cols(x_perm, q.aH, offsets, counts, G, R, H, s));
-    MOE_CUDA(launch_ffn_wgrad_fc1(*cfg, q.d2F, q.aH, counts, offsets, dW13, st, s));
-    return MOE_OK;
-  }
-  MOE_CUDA(launch_ffn_fc2_dgrad(*cfg, dO_perm, counts, offsets, W2, GU, dGU, st, s));
-  MOE_CUDA(launch_ffn_wgrad_fc2(*cfg, dO_perm, h, counts, offsets, dW2, st, s));
-  MOE_CUDA(launch_ffn_fc1_dgrad(*cfg, dGU, counts, offsets, W13, token_of, dlogits, W_r, dX_perm,
-                                st, s));
-  MOE_CUDA(launch_ffn_wgrad_fc1(*cfg, dGU, x_perm, counts, offsets, dW13, st, s));
+  MOE_TRY(moe_grouped_ffn_dgrad(cfg, dO_perm, GU, counts, offsets, token_of, dlogits, W_r, W13, W2,
+                                dGU, dX_perm, scratch, stream));
+  MOE_TRY(moe_grouped_ffn_wgrad(cfg, dO_perm, x_perm, h, dGU, counts, offsets, dW13, dW2, scratch,
+                                stream));
   return MOE_OK;
 }
 
@@ -357,6 +426,7 @@ moe_status moe_layer_fwd(const moe_config* cfg, const moe_params* P, const void*
                          const moe_fwd_state* st, void* scratch, void* stream) {
   MOE_TRY(check_config(cfg));
   MOE_REQUIRE(P && st);
+  MOE_TRY(moe_quantize_weights(cfg, P->W13, P->W2, scratch, stream));
   MOE_TRY(moe_route(cfg, x, P->W_r, P->bias, st->logits, st->idx, st->w, scratch, stream));
   MOE_TRY(moe_permute(cfg, x, st->idx, st->counts, st->offsets, st->row_of, st->token_of,
                       st->sel_offsets, st->sel_tokens, st->x_perm, scratch, stream));

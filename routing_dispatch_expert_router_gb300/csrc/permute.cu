@@ -16,12 +16,21 @@
 //           expert, read from a per-expert bitmap of the chunk's tokens);
 //   scatter one warp per token: reads the row once, writes it to each of its
 //           rows with 16-byte stores; padding rows are zero-filled.
-#include <mutex>
-
 #include "common.cuh"
 #include "internal.h"
 
 namespace moe {
+
+// Whether assignment i = t*k + j names the same expert as an earlier slot of
+// token t. Such a repeat (possible only in a caller-given idx, e.g. a replayed
+// one) is reported and dropped like an out-of-range id, so that every counted
+// row of an expert segment is written exactly once.
+__device__ __forceinline__ bool repeats_earlier_slot(const int32_t* __restrict__ idx, int i, int k,
+                                                     int e) {
+  for (int i0 = i - i % k; i0 < i; ++i0)
+    if (idx[i0] == e) return true;
+  return false;
+}
 
 __global__ void __launch_bounds__(256)
 permute_hist_kernel(const int32_t* __restrict__ idx, int32_t* __restrict__ hist, int T, int k,
@@ -33,7 +42,7 @@ permute_hist_kernel(const int32_t* __restrict__ idx, int32_t* __restrict__ hist,
   const int t0 = c * kChunkTokens, t1 = min(T, t0 + kChunkTokens);
   for (int i = t0 * k + threadIdx.x; i < t1 * k; i += blockDim.x) {
     const int e = idx[i];
-    if ((unsigned)e < (unsigned)E) atomicAdd(&cnt[e], 1);
+    if ((unsigned)e < (unsigned)E && !repeats_earlier_slot(idx, i, k, e)) atomicAdd(&cnt[e], 1);
     else record_status(status, MOE_ERR_DEVICE_CHECK);
   }
   __syncthreads();
@@ -104,14 +113,14 @@ permute_rank_kernel(const int32_t* __restrict__ idx, const int32_t* __restrict__
   const int t0 = c * kChunkTokens, t1 = min(T, t0 + kChunkTokens);
   for (int i = t0 * k + tid; i < t1 * k; i += nt) {
     const int e = idx[i];
-    if ((unsigned)e >= (unsigned)E) continue;
+    if ((unsigned)e >= (unsigned)E || repeats_earlier_slot(idx, i, k, e)) continue;
     const int tl = i / k - t0;
     atomicOr(&bm[e][tl >> 5], 1u << (tl & 31));
   }
   __syncthreads();
   for (int i = t0 * k + tid; i < t1 * k; i += nt) {
     const int e = idx[i];
-    if ((unsigned)e >= (unsigned)E) {
+    if ((unsigned)e >= (unsigned)E || repeats_earlier_slot(idx, i, k, e)) {
       row_of[i] = -1;
       continue;
     }
@@ -244,25 +253,14 @@ namespace {
 constexpr size_t kNoAllocScratchBytes = 512 * 1024;
 static __device__ __align__(256) uint8_t g_permute_scratch[kNoAllocScratchBytes];
 
-constexpr int kMaxDevices = 64;
-std::mutex g_scratch_mu;
-void* g_scratch_addr[kMaxDevices] = {nullptr};
-
-// Device address of g_permute_scratch on the current device (looked up once
-// per device, on the first call made with that device current).
+// Device address of g_permute_scratch in the current context, looked up on
+// every call (cheap): a cached address would go stale after cudaDeviceReset or
+// under another context on the same device.
 cudaError_t noalloc_scratch(uint8_t** out) {
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
+  void* p = nullptr;
+  const cudaError_t e = cudaGetSymbolAddress(&p, g_permute_scratch);
   if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-  std::lock_guard<std::mutex> lock(g_scratch_mu);
-  if (!g_scratch_addr[dev]) {
-    void* p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_permute_scratch);
-    if (e != cudaSuccess) return e;
-    g_scratch_addr[dev] = p;
-  }
-  *out = static_cast<uint8_t*>(g_scratch_addr[dev]);
+  *out = static_cast<uint8_t*>(p);
   return cudaSuccess;
 }
 

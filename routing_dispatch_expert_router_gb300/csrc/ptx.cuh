@@ -180,6 +180,78 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, int a_mn, int b_
 }
 
 
+// ------------------------------------------------- FP8 block-scaled tcgen05 MMA
+// Instruction descriptor of kind::mxf8f6f4 (block-scaled, fp32 accumulation)
+// with E4M3 A and B and UE8M0 scale factors, from the bit fields of the
+// tcgen05 instruction-descriptor table for block-scaled kinds:
+//   [4,6)   scale-factor id of B (which byte of B's 32-bit scale column)
+//   [7,10)  A format (E4M3 = 0)          [10,13) B format (E4M3 = 0)
+//   [15]    A MN-major                   [16]    B MN-major
+//   [17,23) N >> 3                       [23]    scale type (UE8M0 = 1)
+//   [24,29) M >> 4                       [29,31) scale-factor id of A
+__host__ __device__ constexpr uint32_t idesc_mxf8_e4m3(int M, int N, int a_mn, int b_mn) {
+  return ((uint32_t)a_mn << 15)
+       | ((uint32_t)b_mn << 16)
+       | ((uint32_t)(N >> 3) << 17)
+       | (1u << 23)
+       | ((uint32_t)(M >> 4) << 24);
+}
+// The same descriptor with both scale-factor ids set to `id` (0..3).
+__host__ __device__ constexpr uint32_t idesc_with_sf_id(uint32_t idesc, uint32_t id) {
+  return idesc | ((id & 3u) << 4) | ((id & 3u) << 29);
+}
+
+// D[tmem] (+)= (A * scale_A) * (B * scale_B)^T, E4M3 operands from shared
+// memory, one UE8M0 scale per row of A / column of B per 32-deep K slice
+// (scale_vec::1X), the scales read from tensor memory at sfa / sfb.
+__device__ __forceinline__ void mma_mxf8(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                         uint32_t idesc, uint32_t sfa_tmem, uint32_t sfb_tmem,
+                                         uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X "
+      "[%0], %1, %2, %3, [%5], [%6], p;\n\t}"
+      :: "r"(d_tmem), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate), "r"(sfa_tmem),
+         "r"(sfb_tmem) : "memory");
+}
+
+// Shared-memory descriptor of one scale-factor atom for tcgen05.cp: 32 rows of
+// 16 bytes, no swizzle, 8-row core matrices 128 bytes apart (SBO); the atom is
+// one core matrix wide along K, so LBO is unused (0).
+__host__ __device__ __forceinline__ uint64_t smem_desc_sf(uint32_t start) {
+  uint64_t d = 0;
+  d |= (uint64_t)((start >> 4) & 0x3FFFu);
+  d |= (uint64_t)(128u >> 4) << 32;
+  d |= (uint64_t)1 << 46;
+  return d;
+}
+
+// Copies 32 rows x 128 bits from shared memory into tensor memory at columns
+// taddr .. taddr+3 of lanes 0-31, replicated into the other three lane
+// quarters (asynchronous, ordered before later tcgen05.mma of this thread).
+__device__ __forceinline__ void tmem_cp_32x128b_warpx4(uint32_t taddr, uint64_t sdesc) {
+  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;"
+               :: "r"(taddr), "l"(sdesc) : "memory");
+}
+
+// 1D bulk copy global -> shared (16-byte aligned, size a multiple of 16),
+// completion counted on `bar` in bytes.
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes,
+                                          uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+      :: "r"(dst), "l"(src), "r"(bytes), "r"(bar) : "memory");
+}
+
+// Four 32-lane x 32-column tensor-memory loads into one 128-register array.
+__device__ __forceinline__ void tmem_ld128(uint32_t taddr, uint32_t (&r)[128]) {
+  tmem_ld32(taddr, *reinterpret_cast<uint32_t(*)[32]>(&r[0]));
+  tmem_ld32(taddr + 32, *reinterpret_cast<uint32_t(*)[32]>(&r[32]));
+  tmem_ld32(taddr + 64, *reinterpret_cast<uint32_t(*)[32]>(&r[64]));
+  tmem_ld32(taddr + 96, *reinterpret_cast<uint32_t(*)[32]>(&r[96]));
+}
+
 // ------------------------------------------ packed fp32 pairs and fast MUFU ops
 // Two fp32 values in one 64-bit register ({lo, hi}); the .f32x2 forms of the
 // sm_100 family do one IEEE round-to-nearest operation per half, so the results

@@ -11,13 +11,19 @@
 //          reduces along that row),
 //   cols   128 x 1 slices along the tokens of each 128-row block of the
 //          permuted buffer (weight-gradient operands).
-// The quantised values are written back as bf16, which holds every E4M3 value
-// times a power of two exactly, so the tcgen05 bf16 GEMMs that consume them
-// form exactly the products an FP8 block-scaled MMA would (fp32 accumulation).
+// Two output forms:
+//   * 1-byte E4M3 codes with UE8M0 scale atoms (fp8_layout.cuh), the operands
+//     of the block-scaled FP8 tensor-core GEMMs (forward and data gradients:
+//     the tiles and rows quantisers);
+//   * the dequantised values written back as bf16 (the cols quantiser), which
+//     holds every E4M3 value times a power of two exactly: the weight-gradient
+//     GEMMs run these on the bf16 tensor path and form exactly the products an
+//     FP8 MMA would (fp32 accumulation).
 // E4M3 rounding (to nearest even, saturating) uses the hardware conversion.
 #include <cuda_fp16.h>
 
 #include "common.cuh"
+#include "fp8_layout.cuh"
 #include "internal.h"
 
 namespace moe {
@@ -47,12 +53,30 @@ __device__ __forceinline__ float q1(float a, float inv_s, float s) {
   return qa;
 }
 
-__device__ __forceinline__ uint4 quant8(const float (&f)[8], float s) {
-  const float inv = 1.f / s;                              // exact: s is a power of two
-  float o[8];
+// The scale used for the 1-byte form and its UE8M0 code: the block scale,
+// raised to 2^-127 (the smallest UE8M0 value) for blocks whose amax is below
+// 448 * 2^-128 -- there the scaled values keep fewer bits than the fp64
+// reference's, a case no bf16 activation or weight of normal magnitude meets.
+__device__ __forceinline__ float e4m3_scale_code(float amax, uint32_t& code) {
+  float s = e4m3_scale(amax);
+  if (s < 0x1p-127f) s = 0x1p-127f;
+  const uint32_t bits = __float_as_uint(s);
+  code = (bits >> 23) & 0xFFu;     // biased exponent = UE8M0 code (2^-127: subnormal, code 0)
+  return s;
+}
+
+// E4M3 codes of eight values divided by a power-of-two scale (exact): bytes in
+// element order.
+__device__ __forceinline__ uint2 e4m3x8(const float (&f)[8], float inv_s) {
+  uint32_t w[4];
 #pragma unroll
-  for (int i = 0; i < 8; i += 2) q2(f[i], f[i + 1], inv, s, o[i], o[i + 1]);
-  return pack8(o);
+  for (int i = 0; i < 4; ++i) {
+    uint16_t h;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;"
+        : "=h"(h) : "f"(f[2 * i + 1] * inv_s), "f"(f[2 * i] * inv_s));
+    w[i] = h;
+  }
+  return make_uint2(w[0] | (w[1] << 16), w[2] | (w[3] << 16));
 }
 
 __device__ __forceinline__ float amax8(const float (&f)[8]) {
@@ -60,44 +84,6 @@ __device__ __forceinline__ float amax8(const float (&f)[8]) {
 #pragma unroll
   for (int i = 0; i < 8; ++i) m = fmaxf(m, fabsf(f[i]));
   return m;
-}
-
-// 128 x 128 tiles: one block per tile, thread owns 8 vectors of 8 elements.
-__global__ void __launch_bounds__(256)
-quant_tiles_kernel(const __nv_bfloat16* __restrict__ W, __nv_bfloat16* __restrict__ Wq,
-                   long long n_tiles, int rows, int cols) {
-  __shared__ float red[8];
-  const int tc = cols / 128, tr = rows / 128;
-  for (long long tile = blockIdx.x; tile < n_tiles; tile += gridDim.x) {
-    const long long g = tile / ((long long)tr * tc);
-    const int rem = (int)(tile % ((long long)tr * tc));
-    const int r0 = (rem / tc) * 128, c0 = (rem % tc) * 128;
-    const size_t base = (size_t)g * rows * cols;
-    float f[8][8];
-    float m = 0.f;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const int v = threadIdx.x + 256 * i;                // 2048 vectors per tile
-      const int r = v >> 4, c = (v & 15) * 8;
-      unpack8(ldg_nc_v4(W + base + (size_t)(r0 + r) * cols + c0 + c), f[i]);
-      m = fmaxf(m, amax8(f[i]));
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = m;
-    __syncthreads();
-    float amax = red[0];
-#pragma unroll
-    for (int i = 1; i < 8; ++i) amax = fmaxf(amax, red[i]);
-    const float s = e4m3_scale(amax);
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const int v = threadIdx.x + 256 * i;
-      const int r = v >> 4, c = (v & 15) * 8;
-      stg_v4(Wq + base + (size_t)(r0 + r) * cols + c0 + c, quant8(f[i], s));
-    }
-    __syncthreads();
-  }
 }
 
 // Whether 128-row block rb of the permuted buffer holds any row a GEMM reads:
@@ -114,34 +100,6 @@ __device__ __forceinline__ bool live_block(const int32_t* __restrict__ offsets,
     else hi = mid - 1;
   }
   return r0 - offsets[lo] < (long long)((counts[lo] + 127) / 128) * 128;
-}
-
-// 1 x 128 slices along the rows of the live 128-row blocks of [0, offsets[G]):
-// one block of 256 threads per 128-row block, 16 lanes per slice. (Four
-// vectors per thread in flight measured slower than one.)
-__global__ void __launch_bounds__(256)
-quant_rows_kernel(const __nv_bfloat16* __restrict__ X, __nv_bfloat16* __restrict__ Xq,
-                  const int32_t* __restrict__ offsets, const int32_t* __restrict__ counts, int G,
-                  int cols) {
-  const long long rblocks = offsets[G] / 128;
-  const int nvec = cols >> 3;                             // a multiple of 16
-  const int per_block = 128 * nvec;
-  for (long long rb = blockIdx.x; rb < rblocks; rb += gridDim.x) {
-    if (!live_block(offsets, counts, G, rb)) continue;
-    const __nv_bfloat16* src = X + (size_t)rb * 128 * cols;
-    __nv_bfloat16* dst = Xq + (size_t)rb * 128 * cols;
-    for (int v = threadIdx.x; v < per_block; v += 256) {
-      float f[8];
-      unpack8(ldg_nc_v4(src + (size_t)v * 8), f);
-      float m = amax8(f);
-      // the 16 lanes of this half-warp hold one 128-element slice (per_block
-      // and 256 are multiples of 16: a half-warp is wholly in range or out)
-      const unsigned half = (threadIdx.x & 16) ? 0xffff0000u : 0x0000ffffu;
-#pragma unroll
-      for (int o = 8; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(half, m, o));
-      stg_v4(dst + (size_t)v * 8, quant8(f, e4m3_scale(m)));
-    }
-  }
 }
 
 // 128 x 1 slices: every live 128-row block of [0, offsets[G]) (group segments
@@ -209,6 +167,91 @@ quant_cols_kernel(const __nv_bfloat16* __restrict__ X, __nv_bfloat16* __restrict
   }
 }
 
+// 128 x 128 weight tiles -> E4M3 bytes plus the tile's UE8M0 scale, written
+// into two atom arrays: sf_f with the weight's rows as the GEMM's N index and
+// its columns as K (the forward GEMMs), sf_d with the roles swapped (the data
+// gradients, which read the weight transposed). One block per tile.
+__global__ void __launch_bounds__(256)
+quant_tiles8_kernel(const __nv_bfloat16* __restrict__ W, uint8_t* __restrict__ Wq,
+                    uint8_t* __restrict__ sf_f, uint8_t* __restrict__ sf_d, long long n_tiles,
+                    int rows, int cols) {
+  __shared__ float red[8];
+  const int tc = cols / 128, tr = rows / 128;
+  const int64_t kg_f = f8::atoms_k(cols), kg_d = f8::atoms_k(rows);
+  for (long long tile = blockIdx.x; tile < n_tiles; tile += gridDim.x) {
+    const long long g = tile / ((long long)tr * tc);
+    const int rem = (int)(tile % ((long long)tr * tc));
+    const int rt = rem / tc, ct = rem % tc;
+    const int r0 = rt * 128, c0 = ct * 128;
+    const size_t base = (size_t)g * rows * cols;
+    float f[8][8];
+    float m = 0.f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int v = threadIdx.x + 256 * i;                // 2048 vectors per tile
+      const int r = v >> 4, c = (v & 15) * 8;
+      unpack8(ldg_nc_v4(W + base + (size_t)(r0 + r) * cols + c0 + c), f[i]);
+      m = fmaxf(m, amax8(f[i]));
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = m;
+    __syncthreads();
+    float amax = red[0];
+#pragma unroll
+    for (int i = 1; i < 8; ++i) amax = fmaxf(amax, red[i]);
+    uint32_t code;
+    const float s = e4m3_scale_code(amax, code);
+    const float inv = 1.f / s;                            // exact: s is a power of two
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int v = threadIdx.x + 256 * i;
+      const int r = v >> 4, c = (v & 15) * 8;
+      *reinterpret_cast<uint2*>(Wq + base + (size_t)(r0 + r) * cols + c0 + c) = e4m3x8(f[i], inv);
+    }
+    const int n = threadIdx.x & 127;
+    if (threadIdx.x < 128)
+      sf_f[f8::atom_offset(g * tr + rt, ct, kg_f) + f8::atom_byte(n, ct)] = (uint8_t)code;
+    else
+      sf_d[f8::atom_offset(g * tc + ct, rt, kg_d) + f8::atom_byte(n, rt)] = (uint8_t)code;
+    __syncthreads();
+  }
+}
+
+// 1 x 128 slices along the rows of the live 128-row blocks of [0, offsets[G])
+// -> E4M3 bytes plus UE8M0 scale atoms (row block rb, K block kb). One block
+// of 256 threads per 128-row block, 16 lanes per slice.
+__global__ void __launch_bounds__(256)
+quant_rows8_kernel(const __nv_bfloat16* __restrict__ X, uint8_t* __restrict__ Xq,
+                   uint8_t* __restrict__ sf, const int32_t* __restrict__ offsets,
+                   const int32_t* __restrict__ counts, int G, int cols) {
+  const long long rblocks = offsets[G] / 128;
+  const int nvec = cols >> 3;                             // a multiple of 16
+  const int per_block = 128 * nvec;
+  const int64_t kg = f8::atoms_k(cols);
+  for (long long rb = blockIdx.x; rb < rblocks; rb += gridDim.x) {
+    if (!live_block(offsets, counts, G, rb)) continue;
+    const __nv_bfloat16* src = X + (size_t)rb * 128 * cols;
+    uint8_t* dst = Xq + (size_t)rb * 128 * cols;
+    for (int v = threadIdx.x; v < per_block; v += 256) {
+      float f[8];
+      unpack8(ldg_nc_v4(src + (size_t)v * 8), f);
+      float m = amax8(f);
+      const unsigned half = (threadIdx.x & 16) ? 0xffff0000u : 0x0000ffffu;
+#pragma unroll
+      for (int o = 8; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(half, m, o));
+      uint32_t code;
+      const float s = e4m3_scale_code(m, code);
+      *reinterpret_cast<uint2*>(dst + (size_t)v * 8) = e4m3x8(f, 1.f / s);
+      const int cv = v % nvec;
+      if ((cv & 15) == 0) {
+        const int r = v / nvec, kb = cv >> 4;
+        sf[f8::atom_offset(rb, kb, kg) + f8::atom_byte(r, kb)] = (uint8_t)code;
+      }
+    }
+  }
+}
+
 static int grid_cap(long long work_items, int per_block) {
   long long b = (work_items + per_block - 1) / per_block;
   const long long cap = (long long)num_sms() * 16;
@@ -216,19 +259,19 @@ static int grid_cap(long long work_items, int per_block) {
   return b > 0 ? (int)b : 1;
 }
 
-cudaError_t launch_quant_tiles(const void* W, void* Wq, int G, int rows, int cols, cudaStream_t s) {
+cudaError_t launch_quant_tiles8(const void* W, uint8_t* Wq, uint8_t* sf_f, uint8_t* sf_d, int G,
+                                int rows, int cols, cudaStream_t s) {
   const long long n = (long long)G * (rows / 128) * (cols / 128);
-  quant_tiles_kernel<<<grid_cap(n, 1), 256, 0, s>>>(static_cast<const __nv_bfloat16*>(W),
-                                                    static_cast<__nv_bfloat16*>(Wq), n, rows, cols);
+  quant_tiles8_kernel<<<grid_cap(n, 1), 256, 0, s>>>(static_cast<const __nv_bfloat16*>(W), Wq,
+                                                     sf_f, sf_d, n, rows, cols);
   return cudaGetLastError();
 }
 
-cudaError_t launch_quant_rows(const void* X, void* Xq, const int32_t* offsets,
-                              const int32_t* counts, int G, int64_t rows_max, int cols,
-                              cudaStream_t s) {
-  quant_rows_kernel<<<grid_cap(rows_max / 128, 1), 256, 0, s>>>(
-      static_cast<const __nv_bfloat16*>(X), static_cast<__nv_bfloat16*>(Xq), offsets, counts, G,
-      cols);
+cudaError_t launch_quant_rows8(const void* X, uint8_t* Xq, uint8_t* sf, const int32_t* offsets,
+                               const int32_t* counts, int G, int64_t rows_max, int cols,
+                               cudaStream_t s) {
+  quant_rows8_kernel<<<grid_cap(rows_max / 128, 1), 256, 0, s>>>(
+      static_cast<const __nv_bfloat16*>(X), Xq, sf, offsets, counts, G, cols);
   return cudaGetLastError();
 }
 

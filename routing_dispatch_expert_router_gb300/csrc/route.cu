@@ -768,12 +768,17 @@ route_replay_weights_kernel(const float* __restrict__ logits, const float* __res
   const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   if (t >= T) return;
   const float* lrow = logits + (size_t)t * E;
-  int e = lane < k ? idx[(size_t)t * k + lane] : 0;
-  const bool bad = lane < k && (unsigned)e >= (unsigned)E;
-  if (bad) {
-    record_status(status, MOE_ERR_DEVICE_CHECK);
-    e = 0;
+  int e = lane < k ? idx[(size_t)t * k + lane] : -1;
+  // an id out of range, or one that repeats an earlier slot of the token, is
+  // reported and gets weight 0 (the dispatch drops it the same way)
+  bool rep = false;
+  for (int j = 0; j < k; ++j) {
+    const int ej = __shfl_sync(0xffffffffu, e, j);
+    if (j < lane && ej == e) rep = true;
   }
+  const bool bad = lane < k && ((unsigned)e >= (unsigned)E || rep);
+  if (bad) record_status(status, MOE_ERR_DEVICE_CHECK);
+  if (bad || lane >= k) e = 0;
   float v = 0.f;
   if (score_fn == MOE_SCORE_SOFTMAX) {
     const int e0 = __shfl_sync(0xffffffffu, e, 0);

@@ -75,6 +75,7 @@ def run_layer(shape, inp: dict, backward: bool = True, device: str = "cuda",
     else:
         f = bufs.fwd
         f["idx"].copy_(torch.as_tensor(replay_idx, dtype=torch.int32).reshape(f["idx"].shape))
+        B.moe_quantize_weights(cfg, d["W13"], d["W2"], bufs.scratch)
         B.moe_route_replay(cfg, d["x"], d["W_r"], d["bias"], f["idx"], f["logits"], f["w"],
                            bufs.scratch)
         B.moe_permute(cfg, d["x"], f["idx"], f["counts"], f["offsets"], f["row_of"],

@@ -62,7 +62,17 @@ def test_invalid_configs_rejected(bad):
 def test_fp8_scratch_holds_the_quantised_operands():
     s = B.moe_query_sizes(DSV3_FP8)
     G, R, H, F = 256, 256 * 640, 7168, 2048
-    quantised = G * 2 * F * H * 2 + G * H * F * 2 + (2 * R * H + R * F + R * 2 * F) * 2
+
+    def atoms(rows, K):        # one 512-byte scale atom per 128 rows and 4 K blocks of 128
+        return rows // 128 * -(-K // 512) * 512
+
+    # E4M3 weights with their scale atoms for both orientations (forward, data gradient)
+    weights = G * 2 * F * H + G * H * F + atoms(G * 2 * F, H) + atoms(G * H, 2 * F) + \
+        atoms(G * H, F) + atoms(G * F, H)
+    # E4M3 x_perm, h, dO, dGU (1x128 slices) with atoms; bf16 values of their 128x1 slices
+    acts = R * H + R * F + R * H + R * 2 * F + atoms(R, H) + atoms(R, F) + atoms(R, H) + \
+        atoms(R, 2 * F) + (R * H + R * F + R * 2 * F + R * H) * 2
+    quantised = weights + acts
     # the tensor-core router's region (E % 128 == 0): the larger of W_r as three
     # bf16 parts (forward) and dlogits as three bf16 parts plus the chunk sums of
     # dW_r^T over 1024-token chunks (backward)
@@ -72,6 +82,9 @@ def test_fp8_scratch_holds_the_quantised_operands():
     assert quantised + router_split <= s.scratch_bytes <= quantised + router_split + (1 << 20)
     with pytest.raises(B.MoEError) as e:           # shared experts: not in FP8 mode
         B.moe_query_sizes(DSV3_FP8.with_(n_shared=1))
+    assert e.value.code == 2
+    with pytest.raises(B.MoEError) as e:           # the FP8 GEMM tiles: H, F multiples of 256
+        B.moe_query_sizes(DSV3_FP8.with_(H=7168 + 128))
     assert e.value.code == 2
     with pytest.raises(B.MoEError) as e:
         B.moe_query_sizes(DSV3_FP8.with_(dtype=7))

@@ -1,8 +1,9 @@
 """The FP8 configuration (E4M3 with power-of-two block scales) on the GPU.
 
-Every step is checked against the oracle fed the GPU's own inputs of that
-step and quantised the same way (exact on both sides, so the bf16 per-element
-tolerance applies); the whole layer is checked against the oracle's FP8 layer
+The forward and data-gradient GEMMs run on the block-scaled FP8 tensor cores
+(E4M3 codes, UE8M0 scales in tensor memory). Every step is checked against the
+oracle fed the GPU's own inputs of that step and quantised the same way (exact
+on both sides, so the bf16 per-element tolerance applies); the whole layer is checked against the oracle's FP8 layer
 run from the raw inputs with the 5e-2 rule (per element against
 |ref| + rms(ref), and on the relative Frobenius error).
 """
@@ -14,12 +15,20 @@ pytestmark = pytest.mark.gpu
 
 H_ = pytest.importorskip("harness")
 
+# One expert, 64 tokens, k = 1: every FP8 GEMM is one or two 128 x 256 tiles
+# (FC2: one tile over two 128-deep k-blocks). The first case to run.
+SINGLE_TILE = MoEShape("fp8_single_tile", T=64, H=256, E=1, k=1, F=256, score_fn=SIGMOID,
+                       bias_kind="normal", dtype=DT_FP8)
+
 SHAPES = [
+    SINGLE_TILE,
     MoEShape("fp8_groups", T=512, H=256, E=16, k=4, F=256, score_fn=SIGMOID, n_groups=4,
              topk_groups=2, bias_kind="normal", dtype=DT_FP8),
-    MoEShape("fp8_capacity_drop", T=1024, H=384, E=8, k=2, F=256, score_fn=SIGMOID,
+    # H = 768: six 128-deep k-blocks (a partly used scale atom), three N tiles
+    MoEShape("fp8_capacity_drop", T=1024, H=768, E=8, k=2, F=256, score_fn=SIGMOID,
              capacity_factor=0.5, bias_kind="normal", dtype=DT_FP8),
-    MoEShape("fp8_dsv3_like", T=2048, H=512, E=32, k=8, F=256, score_fn=SIGMOID, n_groups=8,
+    # F = 768: FC1 over six tiles of 128 gate + 128 up columns, 2F = 1536 deep FC1 dgrad
+    MoEShape("fp8_dsv3_like", T=2048, H=512, E=32, k=8, F=768, score_fn=SIGMOID, n_groups=8,
              topk_groups=4, bias_kind="normal", dtype=DT_FP8, capacity_factor=1.25),
 ]
 
@@ -31,7 +40,7 @@ def test_fp8_steps_match_oracle(shape):
     H_.check_steps(shape, inp, g)
 
 
-@pytest.mark.parametrize("shape", SHAPES[:2], ids=lambda s: s.name)
+@pytest.mark.parametrize("shape", SHAPES[:3], ids=lambda s: s.name)
 def test_fp8_layer_end_to_end(shape):
     inp = make_inputs(shape, seed=1)
     g = H_.run_layer(shape, inp)

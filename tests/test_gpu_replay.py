@@ -86,3 +86,43 @@ def test_replayed_index_out_of_range_is_reported():
     _, _, w, st = _route(shape, d, replay=idx)
     assert st == 6                 # MOE_ERR_DEVICE_CHECK
     assert float(w[5, 1]) == 0.0
+
+
+def test_replayed_repeated_expert_is_reported_and_dropped():
+    """A recorded idx row that names one expert twice: the second copy is
+    reported (MOE_ERR_DEVICE_CHECK), weighted 0 by the replay and dropped by
+    the dispatch (row_of = -1, not counted), so every counted row of an expert
+    segment is written once. The expected maps are the stable counting sort of
+    the remaining assignments, written out here."""
+    shape = TINY
+    d = make_inputs(shape, seed=16)
+    idx = _other_experts(shape, seed=17)
+    idx[9, 1] = idx[9, 0]          # token 9 names its first expert twice
+    _, idx_d, w, st = _route(shape, d, replay=idx)
+    assert st == 6
+    assert float(w[9, 1]) == 0.0 and float(w[9, 0]) > 0.0
+    cfg = B.config(shape)
+    bufs = B.alloc_buffers(cfg, "cuda", backward=False)
+    f = bufs.fwd
+    x = d["x"].to("cuda")
+    B.moe_permute(cfg, x, idx_d, f["counts"], f["offsets"], f["row_of"], f["token_of"],
+                  f["sel_offsets"], f["sel_tokens"], f["x_perm"], bufs.scratch)
+    torch.cuda.synchronize()
+    assert B.moe_last_device_status(bufs.scratch) == 6
+    T, E, k, a = shape.T, shape.E, shape.k, shape.row_align
+    keep = np.ones((T, k), dtype=bool)
+    keep[9, 1] = False
+    toks = [[t for t in range(T) for j in range(k) if keep[t, j] and idx[t, j] == e]
+            for e in range(E)]
+    counts = np.array([len(v) for v in toks])
+    offsets = np.concatenate([[0], np.cumsum((counts + a - 1) // a * a)])
+    row_of = np.full((T, k), -1)
+    for e in range(E):
+        for r, t in enumerate(toks[e]):
+            row_of[t, int(np.nonzero((idx[t] == e) & keep[t])[0][0])] = offsets[e] + r
+    H_.assert_equal("counts", H_.i64(f["counts"]), counts)
+    H_.assert_equal("offsets", H_.i64(f["offsets"]), offsets)
+    H_.assert_equal("row_of", H_.i64(f["row_of"]), row_of)
+    token_of = np.full(int(offsets[-1]), -1)
+    token_of[row_of[keep]] = np.nonzero(keep)[0]
+    H_.assert_equal("token_of", H_.i64(f["token_of"])[:offsets[-1]], token_of)
