@@ -619,6 +619,107 @@ def to_rows(per_slot, per_shared, maps, cfg, width):
 
 
 # --------------------------------------------------------------------------- #
+# the layer with the routing weight inside the expert
+# --------------------------------------------------------------------------- #
+def layer_forward_reordered(cfg, x, W_r, bias, W13, W2, logits=None, rounding: bool = True):
+    """The layer with the routing weight moved into the expert, before FC2.
+
+    "Scalable Training of Mixture-of-Experts Models with Megatron Core" (es
+    summary, Resumen técnico §2.3.A, memory: an algebraic reordering of the
+    routing weights so the permuted expert outputs need not be kept for the
+    backward). Since y = h W2^T is linear in h, w y = (w h) W2^T: each
+    assignment's expert scales its own SwiGLU output,
+        h_s = bf16(w_tj silu(G) U),   y_s = bf16(h_s W2^T),
+    and the combine is an unweighted sum, out[t] = bf16(sum_j y_s + shared).
+    Shared experts have weight 1 (h_s = h). Without rounding this is
+    layer_forward exactly; with rounding only the bf16 rounding points move.
+    """
+    x = np.asarray(x, np.float64)
+    T, H = x.shape
+    E, k, F, S = cfg.E, cfg.k, cfg.F, cfg.n_shared
+    if logits is None:
+        logits = router_logits(x, W_r, rounding)
+    logits = np.asarray(logits, np.float64)
+    idx, w = route(logits, cfg, bias)
+    maps = permutation_maps(idx, cfg)
+    kept = maps["row_of"] >= 0
+    GU = np.zeros((T, k, 2 * F))
+    hs = np.zeros((T, k, F))
+    y = np.zeros((T, k, H))
+    for e in range(E):
+        tt, jj = np.nonzero((idx == e) & kept)
+        if tt.size == 0:
+            continue
+        g = _rb(x[tt] @ np.asarray(W13[e], np.float64).T, rounding)
+        GU[tt, jj] = g
+        hs[tt, jj] = _rb(w[tt, jj][:, None] * silu(g[:, :F]) * g[:, F:], rounding)
+        y[tt, jj] = expert_fc2(hs[tt, jj], W2[e], rounding)
+    GU_s = np.zeros((S, T, 2 * F))
+    h_s = np.zeros((S, T, F))
+    y_s = np.zeros((S, T, H))
+    for s in range(S):
+        GU_s[s], h_s[s] = expert_fc1(x, W13[E + s], rounding)
+        y_s[s] = expert_fc2(h_s[s], W2[E + s], rounding)
+    acc = np.where(kept[:, :, None], y, 0.0).sum(axis=1) + y_s.sum(axis=0)
+    return dict(logits=logits, idx=idx, w=w, maps=maps, GU=GU, hs=hs, y=y, GU_s=GU_s,
+                h_s=h_s, y_s=y_s, out=_rb(acc, rounding))
+
+
+def layer_backward_reordered(cfg, x, W_r, W13, W2, fwd, dY, rounding: bool = True):
+    """Backward of layer_forward_reordered (same page and section).
+
+    The expert's output gradient is dY itself (no weighting on the way in):
+        dh_s = dY W2 (full precision),
+        dw_tj = <dh_s, h> with h = silu(G) U recomputed from the stored bf16
+                G, U (the routing weight's gradient, taken here instead of from
+                the expert outputs y, which therefore need not be kept),
+        dh = w_tj dh_s, then the SwiGLU backward as in layer_backward,
+        dW2 = sum over rows of dY^T h_s, dW13 and dX as in layer_backward.
+    The router gradient, dx and dW_r follow from dw exactly as in layer_backward.
+    """
+    x = np.asarray(x, np.float64)
+    dY = np.asarray(dY, np.float64)
+    T, H = x.shape
+    E, k, F, S = cfg.E, cfg.k, cfg.F, cfg.n_shared
+    idx, w, maps = fwd["idx"], fwd["w"], fwd["maps"]
+    kept = maps["row_of"] >= 0
+    dYb = _rb(dY, rounding)
+    dw = np.zeros((T, k))
+    dGU = np.zeros((T, k, 2 * F))
+    dX = np.zeros((T, k, H))
+    dW13 = np.zeros((E + S, 2 * F, H))
+    dW2 = np.zeros((E + S, H, F))
+    for e in range(E):
+        tt, jj = np.nonzero((idx == e) & kept)
+        if tt.size == 0:
+            continue
+        dhs = dYb[tt] @ np.asarray(W2[e], np.float64)
+        GU = fwd["GU"][tt, jj]
+        G, U = GU[:, :F], GU[:, F:]
+        dw[tt, jj] = (dhs * (silu(G) * U)).sum(axis=1)
+        dh = w[tt, jj][:, None] * dhs
+        sg = sigmoid(G)
+        d = _rb(np.concatenate([dh * U * sg * (1.0 + G * (1.0 - sg)), dh * silu(G)], axis=1),
+                rounding)
+        dGU[tt, jj] = d
+        dX[tt, jj] = expert_fc1_dgrad(d, W13[e], rounding)
+        dW2[e] = wgrad(dYb[tt], fwd["hs"][tt, jj], rounding)
+        dW13[e] = wgrad(d, x[tt], rounding)
+    dGU_s = np.zeros((S, T, 2 * F))
+    dX_s = np.zeros((S, T, H))
+    for s in range(S):
+        dGU_s[s] = expert_fc2_dgrad_swiglu(dYb, W2[E + s], fwd["GU_s"][s], rounding)
+        dX_s[s] = expert_fc1_dgrad(dGU_s[s], W13[E + s], rounding)
+        dW2[E + s] = wgrad(dYb, fwd["h_s"][s], rounding)
+        dW13[E + s] = wgrad(dGU_s[s], x, rounding)
+    dlogits = router_dlogits(cfg, fwd["logits"], idx, w, dw)
+    dx = _rb(dX.sum(axis=1) + dX_s.sum(axis=0) + dlogits @ np.asarray(W_r, np.float64), rounding)
+    dW_r = _rf(dlogits.T @ x, rounding)
+    return dict(dw=dw, dGU=dGU, dX=dX, dGU_s=dGU_s, dX_s=dX_s, dlogits=dlogits, dx=dx,
+                dW_r=dW_r, dW13=dW13, dW2=dW2)
+
+
+# --------------------------------------------------------------------------- #
 # the FP8 layer (E4M3 with power-of-two block scales)
 # --------------------------------------------------------------------------- #
 def layer_forward_fp8(cfg, x, W_r, bias, W13, W2, logits=None):

@@ -50,6 +50,28 @@ def assert_equal(name, got, ref):
                              f"gpu={got[tuple(i)]} ref={ref[tuple(i)]}")
 
 
+# End-to-end comparisons (from the raw inputs) against the plain per-element
+# rule of the bf16 outputs, 1e-2 + 1e-2 |ref|, or the FP8 configuration's
+# 5e-2 relative, whatever tolerance the check itself applies: one record per
+# tensor (name, elements beyond the plain rule, elements, largest ratio of
+# error to the plain bound). tests/conftest.py prints them after the run.
+PLAIN_RECORDS: list = []
+
+
+def plain_rule(name, got, ref, fp8: bool = False) -> float:
+    """Records how far `got` sits from the plain per-element rule; returns the
+    largest error / bound ratio (<= 1 where the plain rule holds)."""
+    got = np.asarray(got, np.float64)
+    ref = np.asarray(ref, np.float64)
+    bound = 5e-2 * np.abs(ref) if fp8 else BF16_ATOL + BF16_RTOL * np.abs(ref)
+    err = np.abs(got - ref)
+    with np.errstate(divide="ignore", invalid="ignore"):
+        ratio = np.where(err == 0, 0.0, err / bound)
+    worst = float(ratio.max()) if ratio.size else 0.0
+    PLAIN_RECORDS.append((name, int((ratio > 1).sum()), int(ratio.size), worst))
+    return worst
+
+
 def _poison(t: torch.Tensor):
     """Fill with 0xFF bytes (NaN for floats, -1 for int32): unwritten output shows."""
     t.view(torch.uint8).fill_(0xFF)
@@ -271,6 +293,7 @@ def check_end_to_end(shape, inp: dict, g: dict, backward: bool = True):
     W2 = f64(inp["W2"])
     fwd = O.layer_forward(shape, x, Wr, bias, W13, W2, logits=f64(g["logits"]))
     assert_equal("idx (e2e)", i64(g["idx"]), fwd["idx"])
+    plain_rule(f"{shape.name} out", f64(g["out"]), fwd["out"])
     assert_close("out (e2e)", f64(g["out"]), fwd["out"])
     if not backward:
         return
@@ -283,20 +306,26 @@ def check_end_to_end(shape, inp: dict, g: dict, backward: bool = True):
         np.abs(Wr)[fwd["idx"]]
     mag = np.abs(bwd["dx"]) + np.abs(bwd["dX"]).sum(axis=1) + np.abs(bwd["dX_s"]).sum(axis=0) + \
         router.sum(axis=1)
+    plain_rule(f"{shape.name} dx", f64(g["dx"]), bwd["dx"])
     assert_close("dx (e2e)", f64(g["dx"]), bwd["dx"], scale=mag)
     s13, s2 = wgrad_summand_scale(shape, x, dY, fwd, bwd)
+    plain_rule(f"{shape.name} dW13", f64(g["dW13"]), bwd["dW13"])
+    plain_rule(f"{shape.name} dW2", f64(g["dW2"]), bwd["dW2"])
     assert_close("dW13 (e2e)", f64(g["dW13"]), bwd["dW13"], scale=np.abs(bwd["dW13"]) + s13)
     assert_close("dW2 (e2e)", f64(g["dW2"]), bwd["dW2"], scale=np.abs(bwd["dW2"]) + s2)
+    plain_rule(f"{shape.name} dW_r", f64(g["dW_r"]), bwd["dW_r"])
     assert_close("dW_r (e2e)", f64(g["dW_r"]), bwd["dW_r"], atol=1e-2, rtol=1e-2)
 
 
-def assert_close_fp8(name, got, ref, rel=5e-2):
-    """The FP8 rule: |gpu-ref| <= rel*(|ref| + rms(ref)) per element and a
-    relative Frobenius error <= rel over the tensor."""
+def assert_close_fp8(name, got, ref, rel=5e-2, extra=None):
+    """The FP8 rule: |gpu-ref| <= rel*(|ref| + rms(ref) + extra) per element
+    (extra: an added per-element scale, 0 unless given) and a relative
+    Frobenius error <= rel over the tensor."""
     got = np.asarray(got, np.float64)
     ref = np.asarray(ref, np.float64)
     rms = float(np.sqrt(np.mean(ref ** 2))) if ref.size else 0.0
-    assert_close(name, got, ref, atol=0.0, rtol=rel, scale=np.abs(ref) + rms)
+    scale = np.abs(ref) + rms + (0.0 if extra is None else extra)
+    assert_close(name, got, ref, atol=0.0, rtol=rel, scale=scale)
     den = float(np.linalg.norm(ref))
     if den > 0:
         fro = float(np.linalg.norm(got - ref)) / den
@@ -312,7 +341,21 @@ def check_end_to_end_fp8(shape, inp: dict, g: dict):
     W2 = f64(inp["W2"])
     fwd = O.layer_forward_fp8(shape, x, Wr, bias, W13, W2, logits=f64(g["logits"]))
     assert_equal("idx (fp8 e2e)", i64(g["idx"]), fwd["idx"])
+    plain_rule(f"{shape.name} out", f64(g["out"]), fwd["out"], fp8=True)
     assert_close_fp8("out (fp8 e2e)", f64(g["out"]), fwd["out"])
-    bwd = O.layer_backward_fp8(shape, x, Wr, W13, W2, fwd, f64(inp["dY"]))
+    dY = f64(inp["dY"])
+    bwd = O.layer_backward_fp8(shape, x, Wr, W13, W2, fwd, dY)
+    # The weight gradients sum, over an expert's rows, products of operands
+    # that each side quantises to E4M3 from its own bf16 tensors (dGU, h, dO,
+    # x_perm differ by bf16 roundings between the two sides). Where such a
+    # difference straddles an E4M3 rounding boundary the operand moves by one
+    # E4M3 step, up to 2^-3 of itself; with hundreds of rows and cancellation
+    # that exceeds 5e-2 of a small |dW| element. So, as for the bf16 layer's
+    # weight gradients, the per-element part of the rule adds the summands'
+    # magnitudes S = sum_r |a_r| |b_r|, here weighted by 2^-4 (half an E4M3
+    # step); the relative Frobenius error stays <= 5e-2 on every tensor.
+    s13, s2 = wgrad_summand_scale(shape, x, dY, fwd, bwd)
+    extra = {"dW13": 2.0 ** -4 * s13, "dW2": 2.0 ** -4 * s2}
     for n in ("dx", "dW13", "dW2", "dW_r"):
-        assert_close_fp8(f"{n} (fp8 e2e)", f64(g[n]), bwd[n])
+        plain_rule(f"{shape.name} {n}", f64(g[n]), bwd[n], fp8=True)
+        assert_close_fp8(f"{n} (fp8 e2e)", f64(g[n]), bwd[n], extra=extra.get(n))

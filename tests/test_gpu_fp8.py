@@ -40,7 +40,10 @@ def test_fp8_steps_match_oracle(shape):
     H_.check_steps(shape, inp, g)
 
 
-@pytest.mark.parametrize("shape", SHAPES[:3], ids=lambda s: s.name)
+# (the single-tile case has one expert and k = 1: its routing weight is 1 for
+# every token, so the router gradient is identically zero and a relative rule
+# has nothing to compare; its steps are checked above)
+@pytest.mark.parametrize("shape", SHAPES[1:4], ids=lambda s: s.name)
 def test_fp8_layer_end_to_end(shape):
     inp = make_inputs(shape, seed=1)
     g = H_.run_layer(shape, inp)

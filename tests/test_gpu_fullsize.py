@@ -164,6 +164,7 @@ def test_full_size_layer_matches_oracle_on_samples(shape):
         ref = dl[st, e] @ host(x_dev[torch.as_tensor(st, device="cuda")]) if st.size else np.zeros(Hd)
         H_.assert_close(f"dW_r[{e}]", host(g["dW_r"][int(e)]), ref, atol=1e-3, rtol=1e-4)
     # ---- end to end from raw inputs for a few tokens: out[t] and dx[t]
+    e2e = {"out": ([], []), "dx": ([], [])}
     for t in ts[:4]:
         xt = host(x_dev[int(t):int(t) + 1])
         lt = O.router_logits(xt, Wr)
@@ -194,6 +195,8 @@ def test_full_size_layer_matches_oracle_on_samples(shape):
             mag += np.abs(ys)
             dXs.append(O.expert_fc1_dgrad(O.expert_fc2_dgrad_swiglu(dy[None, :], w2, gu), w13)[0])
         ref = O.round_bf16(acc)
+        e2e["out"][0].append(host(g["out"][int(t)]))
+        e2e["out"][1].append(ref)
         if fp8:
             H_.assert_close_fp8(f"out e2e[{t}]", host(g["out"][int(t)]), ref)
         else:
@@ -202,9 +205,13 @@ def test_full_size_layer_matches_oracle_on_samples(shape):
         router = dlt[0] @ Wr
         ref = O.round_bf16(sum(dXs) + router)
         mag = np.abs(ref) + sum(np.abs(d) for d in dXs) + np.abs(router)
+        e2e["dx"][0].append(host(g["dx"][int(t)]))
+        e2e["dx"][1].append(ref)
         if fp8:
             H_.assert_close_fp8(f"dx e2e[{t}]", host(g["dx"][int(t)]), ref)
         else:
             H_.assert_close(f"dx e2e[{t}]", host(g["dx"][int(t)]), ref, scale=mag)
+    for name, (got, ref) in e2e.items():
+        H_.plain_rule(f"{shape.name} {name} (4 tokens)", np.stack(got), np.stack(ref), fp8=fp8)
     del g, inp
     torch.cuda.empty_cache()

@@ -624,3 +624,79 @@ def test_fp8_single_expert_layer_is_dense_fp8_mlp():
     dW13 = _torch_bf16(cols(dGU).T @ cols(tx))
     np.testing.assert_allclose(bwd["dW2"][0], dW2.numpy(), rtol=2 ** -6, atol=1e-4)
     np.testing.assert_allclose(bwd["dW13"][0], dW13.numpy(), rtol=2 ** -6, atol=1e-4)
+
+
+# --------------------------------------------------------------------------- #
+# the routing weight inside the expert (algebraic reordering)
+# --------------------------------------------------------------------------- #
+REORDER_CFGS = [
+    MoEShape("t", T=8, H=16, E=4, k=2, F=32, bias_kind="zipf"),
+    MoEShape("t", T=8, H=16, E=8, k=3, F=16, n_shared=1, score_fn=SIGMOID, n_groups=4,
+             topk_groups=2, bias_kind="normal", route_scale=1.5),
+    MoEShape("t", T=12, H=16, E=4, k=2, F=16, capacity_factor=0.5, row_align=1,
+             score_fn=SIGMOID, bias_kind="normal"),
+]
+
+
+def _reorder_inputs(cfg, seed):
+    inp = make_inputs(cfg, seed=seed)
+    x, Wr, W13, W2, dY = (f64(inp[n]) for n in ("x", "W_r", "W13", "W2", "dY"))
+    bias = None if inp["bias"] is None else f64(inp["bias"])
+    return x, Wr, bias, W13 * 10.0, W2 * 10.0, dY
+
+
+@pytest.mark.parametrize("cfg", REORDER_CFGS)
+def test_reordered_layer_equals_the_layer_without_rounding(cfg):
+    """w (h W2^T) = (w h) W2^T and <dY, h W2^T> = <dY W2, h>: without rounding
+    the reordered forward and backward give the layer's own results."""
+    x, Wr, bias, W13, W2, dY = _reorder_inputs(cfg, 31)
+    a = O.layer_forward(cfg, x, Wr, bias, W13, W2, rounding=False)
+    b = O.layer_forward_reordered(cfg, x, Wr, bias, W13, W2, rounding=False)
+    np.testing.assert_array_equal(a["idx"], b["idx"])
+    np.testing.assert_allclose(b["out"], a["out"], rtol=1e-12, atol=1e-13)
+    ga = O.layer_backward(cfg, x, Wr, W13, W2, a, dY, rounding=False)
+    gb = O.layer_backward_reordered(cfg, x, Wr, W13, W2, b, dY, rounding=False)
+    np.testing.assert_allclose(gb["dw"], ga["dw"], rtol=1e-11, atol=1e-12)
+    for n in ("dlogits", "dx", "dW_r", "dW13", "dW2"):
+        np.testing.assert_allclose(gb[n], ga[n], rtol=1e-10, atol=1e-11, err_msg=n)
+
+
+@pytest.mark.parametrize("cfg", REORDER_CFGS)
+def test_reordered_backward_matches_finite_differences(cfg):
+    x, Wr, bias, W13, W2, dY = _reorder_inputs(cfg, 32)
+    fwd = O.layer_forward_reordered(cfg, x, Wr, bias, W13, W2, rounding=False)
+    bwd = O.layer_backward_reordered(cfg, x, Wr, W13, W2, fwd, dY, rounding=False)
+
+    def loss(xx, wr, w13, w2):
+        f = O.layer_forward_reordered(cfg, xx, wr, bias, w13, w2, rounding=False)
+        np.testing.assert_array_equal(f["idx"], fwd["idx"])
+        return float((f["out"] * dY).sum())
+    eps = 1e-6
+    for (arr_i, pos, gname) in ((0, (3, 5), "dx"), (1, (2, 7), "dW_r"), (2, (1, 3, 4), "dW13"),
+                                (3, (0, 2, 1), "dW2"), (0, (6, 11), "dx")):
+        args = [x.copy(), Wr.copy(), W13.copy(), W2.copy()]
+        args[arr_i][pos] += eps
+        lp = loss(*args)
+        args[arr_i][pos] -= 2 * eps
+        lm = loss(*args)
+        fd = (lp - lm) / (2 * eps)
+        assert abs(fd - bwd[gname][pos]) <= 1e-5 * (1 + abs(fd)), (gname, fd, bwd[gname][pos])
+
+
+def test_reordered_layer_with_rounding_stays_within_bf16_of_the_layer():
+    """With bf16 rounding the two orders differ only where the roundings fall
+    (h_s rounded after the weighting instead of y before it): a few bf16 ulps
+    of the results' magnitudes."""
+    cfg = MoEShape("t", T=64, H=64, E=8, k=2, F=64, score_fn=SIGMOID, bias_kind="normal")
+    inp = make_inputs(cfg, seed=33)
+    x, Wr, W13, W2, dY = (f64(inp[n]) for n in ("x", "W_r", "W13", "W2", "dY"))
+    bias = f64(inp["bias"])
+    a = O.layer_forward(cfg, x, Wr, bias, W13, W2)
+    b = O.layer_forward_reordered(cfg, x, Wr, bias, W13, W2)
+    scale = np.abs(a["out"]).max()
+    assert np.abs(b["out"] - a["out"]).max() <= 4 * 2.0 ** -8 * scale
+    assert (b["out"] != a["out"]).any()        # the rounding points really moved
+    ga = O.layer_backward(cfg, x, Wr, W13, W2, a, dY)
+    gb = O.layer_backward_reordered(cfg, x, Wr, W13, W2, b, dY)
+    for n in ("dx", "dW13", "dW2"):
+        assert np.abs(gb[n] - ga[n]).max() <= 4 * 2.0 ** -8 * np.abs(ga[n]).max(), n
