@@ -52,6 +52,8 @@ def parse():
                     choices=sorted(W.SHAPES) + sorted(W.PROFILE_SHAPES))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--weights-in-expert", action="store_true",
+                    help="the layer with the routing weight applied inside the expert (bf16)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-sample-tokens", type=int, default=0)
     ap.add_argument("--ref-budget-s", type=float, default=120.0,
@@ -165,6 +167,21 @@ def gemm_flops(shape, counts) -> float:
     return 2.0 * rows * shape.H * 2 * shape.F + 2.0 * rows * shape.F * shape.H
 
 
+def stash_bytes(shape, bufs) -> dict:
+    """Device bytes of the forward state the backward reads (caller-owned
+    buffers kept from the forward to the backward): with the routing weight
+    inside the expert the permuted expert outputs y_perm are read only by the
+    combine, so their buffer need not survive until the backward."""
+    f = bufs.fwd
+    kept = ["logits", "idx", "w", "counts", "offsets", "row_of", "token_of", "sel_offsets",
+            "sel_tokens", "x_perm", "GU", "h"]
+    if not shape.weights_in_expert:
+        kept.append("y_perm")
+    n = sum(f[k].numel() * f[k].element_size() for k in kept)
+    return {"forward_state_kept": n, "y_perm": f["y_perm"].numel() * f["y_perm"].element_size(),
+            "y_perm_kept": not shape.weights_in_expert}
+
+
 STAGES = ("route", "permute", "quantize_weights", "grouped_ffn_fwd", "unpermute",
           "unpermute_bwd", "route_bwd", "grouped_ffn_dgrad", "grouped_ffn_wgrad", "permute_bwd",
           "router_wgrad")
@@ -225,6 +242,8 @@ def run_ours(args, rank, world, local):
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     shape = {**W.SHAPES, **W.PROFILE_SHAPES}[args.workload]
+    if args.weights_in_expert:
+        shape = shape.with_(weights_in_expert=1)
     cfg = B.config(shape)
     inp = W.make_inputs(shape, seed=args.seed + rank, device=str(dev))
     bufs = B.alloc_buffers(cfg, dev)
@@ -242,6 +261,7 @@ def run_ours(args, rank, world, local):
     sc = bufs.scratch
 
     fp8 = shape.dtype == W.DT_FP8
+    reord = bool(shape.weights_in_expert)
 
     def step(ev=None):
         # the layer step through the per-stage entry points (the same launches
@@ -256,19 +276,38 @@ def run_ours(args, rank, world, local):
         rec(2)
         B.moe_quantize_weights(cfg, inp["W13"], inp["W2"], sc)
         rec(3)
-        B.moe_grouped_ffn_fwd(cfg, f["x_perm"], f["counts"], f["offsets"], inp["W13"], inp["W2"],
-                              f["GU"], f["h"], f["y_perm"], sc)
-        rec(4)
-        B.moe_unpermute(cfg, f["y_perm"], f["row_of"], f["w"], f["offsets"], out)
-        rec(5)
-        B.moe_unpermute_bwd(cfg, dY, f["y_perm"], f["row_of"], f["w"], f["counts"], f["offsets"],
-                            b["dO_perm"], b["dw"])
-        rec(6)
-        B.moe_route_bwd(cfg, f["logits"], f["idx"], f["w"], b["dw"], b["dlogits"])
-        rec(7)
-        B.moe_grouped_ffn_dgrad(cfg, b["dO_perm"], f["GU"], f["counts"], f["offsets"],
-                                f["token_of"], b["dlogits"], inp["W_r"], inp["W13"], inp["W2"],
-                                b["dGU"], b["dX_perm"], sc)
+        if reord:
+            # the routing weight inside the expert: no y_perm read in the
+            # backward; dw and dlogits come out of the data-gradient stage
+            B.moe_grouped_ffn_fwd_reordered(cfg, f["x_perm"], f["counts"], f["offsets"],
+                                            f["token_of"], f["row_of"], f["w"], inp["W13"],
+                                            inp["W2"], f["GU"], f["h"], f["y_perm"], sc)
+            rec(4)
+            B.moe_unpermute(cfg, f["y_perm"], f["row_of"], None, f["offsets"], out)
+            rec(5)
+            B.moe_unpermute_bwd_reordered(cfg, dY, f["row_of"], f["counts"], f["offsets"],
+                                          b["dO_perm"])
+            rec(6)
+            rec(7)
+            B.moe_grouped_ffn_dgrad_reordered(cfg, b["dO_perm"], f["GU"], f["counts"],
+                                              f["offsets"], f["token_of"], f["row_of"],
+                                              f["logits"], f["idx"], f["w"], inp["W_r"],
+                                              inp["W13"], inp["W2"], b["dGU"], b["dX_perm"],
+                                              b["dw"], b["dlogits"], sc)
+        else:
+            B.moe_grouped_ffn_fwd(cfg, f["x_perm"], f["counts"], f["offsets"], inp["W13"],
+                                  inp["W2"], f["GU"], f["h"], f["y_perm"], sc)
+            rec(4)
+            B.moe_unpermute(cfg, f["y_perm"], f["row_of"], f["w"], f["offsets"], out)
+            rec(5)
+            B.moe_unpermute_bwd(cfg, dY, f["y_perm"], f["row_of"], f["w"], f["counts"],
+                                f["offsets"], b["dO_perm"], b["dw"], sc)
+            rec(6)
+            B.moe_route_bwd(cfg, f["logits"], f["idx"], f["w"], b["dw"], b["dlogits"])
+            rec(7)
+            B.moe_grouped_ffn_dgrad(cfg, b["dO_perm"], f["GU"], f["counts"], f["offsets"],
+                                    f["token_of"], b["dlogits"], inp["W_r"], inp["W13"],
+                                    inp["W2"], b["dGU"], b["dX_perm"], sc)
         rec(8)
         B.moe_grouped_ffn_wgrad(cfg, b["dO_perm"], f["x_perm"], f["h"], b["dGU"], f["counts"],
                                 f["offsets"], dW13, dW2, sc)
@@ -290,6 +329,8 @@ def run_ours(args, rank, world, local):
                          + (3 if tc_router else 1))
     if fp8:
         launches_per_step += 2 + 2 + 2 + 4
+    if reord:
+        launches_per_step += 2          # row weights, dw reduction
     for _ in range(max(args.warmup, 3)):
         step()
     torch.cuda.synchronize(dev)
@@ -426,7 +467,8 @@ def run_ours(args, rank, world, local):
         "data": "synthetic (seeded N(0,1) tokens, N(0,0.02^2) weights; no dataset)",
         "config": {"workload": f"{shape.name}: T={T} H={H} E={E}(+{S} shared) top-{shape.k} "
                                f"F={F} capacity_factor={cf if cf > 0 else 'dropless'} "
-                               f"dtype={dt_name} fwd+bwd",
+                               f"dtype={dt_name}"
+                               + (" weights_in_expert" if reord else "") + " fwd+bwd",
                    "l2": "inputs larger than L2 (expert weights "
                          f"{2 * G * 3 * H * F / 1e9:.2f} GB in bf16, streamed every step)",
                    "parallelism": "replicas" if world > 1 else "single GPU"},
@@ -445,6 +487,7 @@ def run_ours(args, rank, world, local):
                                                       pk.get("bf16_tflops_sustained",
                                                              bf16_peak))},
         "stages": stage_table(shape, f, stage_ms, pk["hbm_gbs"], fl, tc_peak, bf16_peak),
+        "stash_bytes": stash_bytes(shape, bufs),
         "clocks": clk,
     }
     if fp8:

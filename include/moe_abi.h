@@ -90,6 +90,10 @@ typedef struct moe_config {
     int32_t dtype;           /* MOE_DTYPE_BF16 | MOE_DTYPE_FP8_E4M3_BLOCK        */
     float capacity_factor;   /* 0 = dropless; else C = ceil(cf*T*k/E) rows      */
     int32_t row_align;       /* every expert segment is a multiple of this (128)*/
+    int32_t weights_in_expert; /* 1: the routing weight scales h inside the
+                                * expert before FC2 (see moe_grouped_ffn_fwd_
+                                * reordered); bf16 mode only. 0: it scales the
+                                * expert output in the combine.              */
 } moe_config;
 
 /* Worst-case sizes of the caller-owned buffers for one configuration. */
@@ -227,10 +231,16 @@ MOE_API moe_status moe_route_aux_bwd(const moe_config* cfg, const void* x, const
  * tokens occupy rows offsets[e] .. offsets[e]+counts[e]-1 in increasing token
  * order; segments are padded to row_align rows (or are C rows in capacity
  * mode, where the first C tokens of an expert are kept); shared experts
- * follow, one row per token. Writes the maps and x_perm (padding rows zero).
+ * follow, one row per token. Writes the maps and x_perm: the padding rows in
+ * the last 128-row block of a segment (the rows the grouped GEMMs read) are
+ * zero; rows of a segment past that block (capacity mode, row_align > 128)
+ * are not written. token_of is -1 on every padding row.
  * An idx entry outside [0, E), or one that repeats an earlier slot of the
  * same token (only a caller-given idx can), records MOE_ERR_DEVICE_CHECK in
  * the status word and is dropped: row_of = -1, not counted, no row.
+ * FP8 mode: every row is also written in its 1-byte form (E4M3 codes of its
+ * 1x128 slices, UE8M0 scales) into `scratch`, where moe_grouped_ffn_fwd reads
+ * it: pass the same scratch to both.
  * scratch: moe_sizes.scratch_bytes bytes. */
 MOE_API moe_status moe_permute(const moe_config* cfg, const void* x, const int32_t* idx,
                        int32_t* counts, int32_t* offsets, int32_t* row_of, int32_t* token_of,
@@ -253,6 +263,9 @@ MOE_API moe_status moe_permute(const moe_config* cfg, const void* x, const int32
  *    calls whose kernels overlap on the GPU (e.g. on two streams) race. Each
  *    call clears the array's status word; index problems a kernel finds are
  *    recorded there and are not reported by this call.
+ *  - bf16 configurations only (MOE_ERR_UNSUPPORTED otherwise): in the FP8
+ *    configuration the dispatch also writes x_perm's E4M3 form into the
+ *    caller's scratch, which this entry point does not take.
  * Other arguments, layouts and results are those of moe_permute. */
 MOE_API moe_status moe_permute_noalloc(const moe_config* cfg, const void* x, const int32_t* idx,
                                        int32_t* counts, int32_t* offsets, int32_t* row_of,
@@ -274,32 +287,41 @@ MOE_API moe_status moe_quantize_weights(const moe_config* cfg, const void* W13, 
 /* Stage 3, compute (es summary §2.1 step 3; grouped GEMM, §2.3.C): for every
  * group g, on its rows X: [G|U] = X W13[g]^T (GU, bf16), h = bf16(silu(G) U),
  * y_perm = bf16(h W2[g]^T). tcgen05 grouped GEMMs that read counts/offsets on
- * the device. FP8 mode: x_perm and h are quantised in 1x128 slices (E4M3 +
- * UE8M0, kept in scratch) and both GEMMs run on the block-scaled FP8 tensor
- * cores (tcgen05 kind::mxf8f6f4) with the weights moe_quantize_weights left in
- * scratch; W13 and W2 are then not read. */
+ * the device. FP8 mode: both GEMMs run on the block-scaled FP8 tensor cores
+ * (tcgen05 kind::mxf8f6f4) with the weights moe_quantize_weights left in
+ * scratch and the 1-byte x_perm that moe_permute left there (W13, W2 and
+ * x_perm are then not read); h is quantised in 1x128 slices (E4M3 + UE8M0,
+ * kept in scratch) for FC2. */
 MOE_API moe_status moe_grouped_ffn_fwd(const moe_config* cfg, const void* x_perm, const int32_t* counts,
                                const int32_t* offsets, const void* W13, const void* W2,
                                void* GU, void* h, void* y_perm, void* scratch, void* stream);
 
 /* Stage 4, combine (es summary §2.1 step 4, done locally):
  * out[t] = bf16( sum_j w[t,j] y_perm[row_of[t,j]] + sum_s y_perm[offsets[E+s]+t] ),
- * fp32 accumulation; dropped assignments contribute 0. */
+ * fp32 accumulation; dropped assignments contribute 0. w may be NULL: unit
+ * weights (the layer with the weight inside the expert, whose y_perm rows
+ * already carry it). */
 MOE_API moe_status moe_unpermute(const moe_config* cfg, const void* y_perm, const int32_t* row_of,
                          const float* w, const int32_t* offsets, void* out, void* stream);
 
 /* Backward of stage 4: dO_perm[row_of[t,j]] = bf16(w[t,j] dY[t]),
  * dw[t,j] = <dY[t], y_perm[row_of[t,j]]> (0 if dropped); shared rows get dY;
- * padding rows of dO_perm are zeroed. */
+ * padding rows of dO_perm are zeroed as moe_permute zeroes those of x_perm
+ * (the ones in the last 128-row block of a segment). FP8 mode: every row is
+ * also written in its 1-byte form (E4M3 codes of its 1x128 slices, UE8M0
+ * scales) into `scratch`, where moe_grouped_ffn_dgrad reads it: pass the same
+ * scratch to both. scratch: moe_sizes.scratch_bytes bytes. */
 MOE_API moe_status moe_unpermute_bwd(const moe_config* cfg, const void* dY, const void* y_perm,
                              const int32_t* row_of, const float* w, const int32_t* counts,
-                             const int32_t* offsets, void* dO_perm, float* dw, void* stream);
+                             const int32_t* offsets, void* dO_perm, float* dw, void* scratch,
+                             void* stream);
 
 /* Data-gradient half of moe_grouped_ffn_bwd (the W/D split of es summary
  * §2.3.B): dGU and dX_perm exactly as moe_grouped_ffn_bwd writes them. FP8
- * mode: dO and dGU are quantised in 1x128 slices and both GEMMs run on the
- * block-scaled FP8 tensor cores with the weights moe_quantize_weights left in
- * scratch (W13 and W2 are then not read). */
+ * mode: both GEMMs run on the block-scaled FP8 tensor cores with the weights
+ * moe_quantize_weights left in scratch and the 1-byte dO that
+ * moe_unpermute_bwd left there (W13, W2 are then not read, dO_perm only by the
+ * weight gradients); dGU is quantised in 1x128 slices for FC1's. */
 MOE_API moe_status moe_grouped_ffn_dgrad(const moe_config* cfg, const void* dO_perm,
                                          const void* GU, const int32_t* counts,
                                          const int32_t* offsets, const int32_t* token_of,
@@ -337,6 +359,57 @@ MOE_API moe_status moe_grouped_ffn_bwd(const moe_config* cfg, const void* dO_per
                                const void* W2, void* dGU, void* dX_perm, void* dW13, void* dW2,
                                void* scratch, void* stream);
 
+/* The layer with the routing weight inside the expert (cfg->weights_in_expert
+ * = 1; the memory-efficient permutation of es summary §2.3.A: an algebraic
+ * reordering of the routing weights, so that the permuted expert outputs are
+ * not needed by the backward). Since y = h W2^T is linear in h, the weight
+ * moves before FC2:
+ *   forward:  h[r] = bf16(w_row silu(G) U) (GU as in moe_grouped_ffn_fwd),
+ *             y_perm = bf16(h W2^T), then moe_unpermute with w = NULL;
+ *   backward: dO_perm rows = dY[t] unweighted (moe_unpermute_bwd_reordered),
+ *             dh_s = dO W2 (fp32), dw[t,j] = <dh_s, silu(G) U> of the row,
+ *             dh = w_row dh_s into the SwiGLU backward -> dGU, then dlogits
+ *             from dw (as moe_route_bwd), then dX_perm as moe_grouped_ffn_bwd
+ *             with that dlogits; moe_grouped_ffn_wgrad gives dW2 = dO^T h.
+ * y_perm is read only by the combine: its buffer need not survive from the
+ * forward to the backward. w_row is w[t,j] of the row's assignment (1 for a
+ * shared expert's row, 0 for padding), kept in `scratch` by the forward: pass
+ * the forward's scratch to the backward. bf16 mode only.
+ * moe_grouped_ffn_fwd_reordered: x_perm, counts, offsets, token_of, row_of
+ * from moe_permute and w from moe_route; writes GU, h (the weighted h_s) and
+ * y_perm. Returns MOE_ERR_INVALID_ARG unless cfg->weights_in_expert = 1. */
+MOE_API moe_status moe_grouped_ffn_fwd_reordered(const moe_config* cfg, const void* x_perm,
+                                                 const int32_t* counts, const int32_t* offsets,
+                                                 const int32_t* token_of, const int32_t* row_of,
+                                                 const float* w, const void* W13, const void* W2,
+                                                 void* GU, void* h, void* y_perm, void* scratch,
+                                                 void* stream);
+
+/* dO_perm[row_of[t,j]] = dY[t] for kept assignments, shared rows get dY,
+ * padding rows zero as in moe_unpermute_bwd (no weighting, y_perm not read,
+ * no dw). */
+MOE_API moe_status moe_unpermute_bwd_reordered(const moe_config* cfg, const void* dY,
+                                               const int32_t* row_of, const int32_t* counts,
+                                               const int32_t* offsets, void* dO_perm,
+                                               void* stream);
+
+/* The data gradients of the layer with the weight inside the expert, with the
+ * routing weights' gradient: writes dGU, dw [T,k] (fp32; 0 for dropped
+ * assignments), dlogits [T,E] (as moe_route_bwd from dw) and dX_perm (as
+ * moe_grouped_ffn_bwd, router term from this dlogits). logits, idx, w from
+ * moe_route; the scratch of the forward. Deterministic: dw sums the FC2 data
+ * gradient's per-tile partial dot products in tile order. */
+MOE_API moe_status moe_grouped_ffn_dgrad_reordered(const moe_config* cfg, const void* dO_perm,
+                                                   const void* GU, const int32_t* counts,
+                                                   const int32_t* offsets,
+                                                   const int32_t* token_of,
+                                                   const int32_t* row_of, const float* logits,
+                                                   const int32_t* idx, const float* w,
+                                                   const float* W_r, const void* W13,
+                                                   const void* W2, void* dGU, void* dX_perm,
+                                                   float* dw, float* dlogits, void* scratch,
+                                                   void* stream);
+
 /* Backward of the routing weights to the logits (dense [T,E], zero outside the
  * selected experts). softmax: dl_j = w_j (dw_j - sum_i w_i dw_i); sigmoid:
  * ds_j = (r/S)(dw_j - sum_i (s_i/S) dw_i), dl_j = ds_j s_j (1 - s_j). */
@@ -370,7 +443,8 @@ MOE_API moe_status moe_router_wgrad(const moe_config* cfg, const void* x, const 
                             void* scratch, void* stream);
 
 /* The whole layer forward: (FP8 mode: moe_quantize_weights,) route, permute,
- * grouped FFN, unpermute. */
+ * grouped FFN, unpermute (with weights_in_expert = 1: the reordered grouped
+ * FFN and the unweighted combine). */
 MOE_API moe_status moe_layer_fwd(const moe_config* cfg, const moe_params* params, const void* x,
                          void* out, const moe_fwd_state* st, void* scratch, void* stream);
 

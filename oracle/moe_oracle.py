@@ -665,6 +665,22 @@ def layer_forward_reordered(cfg, x, W_r, bias, W13, W2, logits=None, rounding: b
                 h_s=h_s, y_s=y_s, out=_rb(acc, rounding))
 
 
+def expert_fc2_dgrad_swiglu_weighted(dY, W2_e, GU, w, rounding: bool = True):
+    """The FC2 data gradient of one expert with the routing weight inside it:
+    dh_s = dY W2_e (full precision), dw = <dh_s, silu(G) U> per row (G, U the
+    stored bf16 values), dh = w dh_s, then the SwiGLU backward of
+    expert_fc2_dgrad_swiglu. Returns (dGU in bf16, dw)."""
+    F = W2_e.shape[1]
+    dhs = np.asarray(dY, np.float64) @ np.asarray(W2_e, np.float64)
+    G, U = GU[:, :F], GU[:, F:]
+    dw = (dhs * (silu(G) * U)).sum(axis=1)
+    dh = np.asarray(w, np.float64)[:, None] * dhs
+    sg = sigmoid(G)
+    d = _rb(np.concatenate([dh * U * sg * (1.0 + G * (1.0 - sg)), dh * silu(G)], axis=1),
+            rounding)
+    return d, dw
+
+
 def layer_backward_reordered(cfg, x, W_r, W13, W2, fwd, dY, rounding: bool = True):
     """Backward of layer_forward_reordered (same page and section).
 
@@ -693,14 +709,8 @@ def layer_backward_reordered(cfg, x, W_r, W13, W2, fwd, dY, rounding: bool = Tru
         tt, jj = np.nonzero((idx == e) & kept)
         if tt.size == 0:
             continue
-        dhs = dYb[tt] @ np.asarray(W2[e], np.float64)
-        GU = fwd["GU"][tt, jj]
-        G, U = GU[:, :F], GU[:, F:]
-        dw[tt, jj] = (dhs * (silu(G) * U)).sum(axis=1)
-        dh = w[tt, jj][:, None] * dhs
-        sg = sigmoid(G)
-        d = _rb(np.concatenate([dh * U * sg * (1.0 + G * (1.0 - sg)), dh * silu(G)], axis=1),
-                rounding)
+        d, dw[tt, jj] = expert_fc2_dgrad_swiglu_weighted(dYb[tt], W2[e], fwd["GU"][tt, jj],
+                                                         w[tt, jj], rounding)
         dGU[tt, jj] = d
         dX[tt, jj] = expert_fc1_dgrad(d, W13[e], rounding)
         dW2[e] = wgrad(dYb[tt], fwd["hs"][tt, jj], rounding)

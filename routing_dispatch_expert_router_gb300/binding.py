@@ -24,7 +24,9 @@ ENTRY_POINTS = (
     "moe_query_sizes", "moe_route", "moe_route_replay", "moe_route_aux", "moe_route_aux_bwd",
     "moe_permute", "moe_permute_noalloc",
     "moe_quantize_weights", "moe_grouped_ffn_fwd", "moe_unpermute",
-    "moe_unpermute_bwd", "moe_grouped_ffn_dgrad", "moe_grouped_ffn_wgrad", "moe_grouped_ffn_bwd", "moe_route_bwd", "moe_permute_bwd",
+    "moe_unpermute_bwd", "moe_grouped_ffn_dgrad", "moe_grouped_ffn_wgrad", "moe_grouped_ffn_bwd",
+    "moe_grouped_ffn_fwd_reordered", "moe_unpermute_bwd_reordered",
+    "moe_grouped_ffn_dgrad_reordered", "moe_route_bwd", "moe_permute_bwd",
     "moe_router_wgrad", "moe_layer_fwd", "moe_layer_bwd", "moe_last_device_status",
     "moe_clear_device_status", "moe_check_bounded_wait", "moe_status_string",
 )
@@ -42,7 +44,8 @@ class MoEConfig(ctypes.Structure):
                 ("score_fn", ctypes.c_int32), ("n_groups", ctypes.c_int32),
                 ("topk_groups", ctypes.c_int32), ("group_score", ctypes.c_int32),
                 ("route_scale", ctypes.c_float), ("dtype", ctypes.c_int32),
-                ("capacity_factor", ctypes.c_float), ("row_align", ctypes.c_int32)]
+                ("capacity_factor", ctypes.c_float), ("row_align", ctypes.c_int32),
+                ("weights_in_expert", ctypes.c_int32)]
 
 
 class MoESizes(ctypes.Structure):
@@ -110,7 +113,8 @@ def config(shape) -> MoEConfig:
                      route_scale=getattr(shape, "route_scale", 1.0),
                      dtype=getattr(shape, "dtype", 0),
                      capacity_factor=getattr(shape, "capacity_factor", 0.0),
-                     row_align=getattr(shape, "row_align", 128))
+                     row_align=getattr(shape, "row_align", 128),
+                     weights_in_expert=getattr(shape, "weights_in_expert", 0))
 
 
 def _cfg(c) -> MoEConfig:
@@ -206,9 +210,10 @@ def moe_unpermute(cfg, y_perm, row_of, w, offsets, out, stream=None):
     _call("moe_unpermute", _cfg(cfg), y_perm, row_of, w, offsets, out, _stream(stream))
 
 
-def moe_unpermute_bwd(cfg, dY, y_perm, row_of, w, counts, offsets, dO_perm, dw, stream=None):
+def moe_unpermute_bwd(cfg, dY, y_perm, row_of, w, counts, offsets, dO_perm, dw, scratch,
+                      stream=None):
     _call("moe_unpermute_bwd", _cfg(cfg), dY, y_perm, row_of, w, counts, offsets, dO_perm, dw,
-          _stream(stream))
+          scratch, _stream(stream))
 
 
 def moe_grouped_ffn_bwd(cfg, dO_perm, x_perm, GU, h, counts, offsets, token_of, dlogits, W_r,
@@ -227,6 +232,26 @@ def moe_grouped_ffn_wgrad(cfg, dO_perm, x_perm, h, dGU, counts, offsets, dW13, d
                           stream=None):
     _call("moe_grouped_ffn_wgrad", _cfg(cfg), dO_perm, x_perm, h, dGU, counts, offsets, dW13,
           dW2, scratch, _stream(stream))
+
+
+def moe_grouped_ffn_fwd_reordered(cfg, x_perm, counts, offsets, token_of, row_of, w, W13, W2,
+                                  GU, h, y_perm, scratch, stream=None):
+    """Forward GEMMs with the routing weight inside the expert (h = w silu(G) U)."""
+    _call("moe_grouped_ffn_fwd_reordered", _cfg(cfg), x_perm, counts, offsets, token_of, row_of,
+          w, W13, W2, GU, h, y_perm, scratch, _stream(stream))
+
+
+def moe_unpermute_bwd_reordered(cfg, dY, row_of, counts, offsets, dO_perm, stream=None):
+    _call("moe_unpermute_bwd_reordered", _cfg(cfg), dY, row_of, counts, offsets, dO_perm,
+          _stream(stream))
+
+
+def moe_grouped_ffn_dgrad_reordered(cfg, dO_perm, GU, counts, offsets, token_of, row_of, logits,
+                                    idx, w, W_r, W13, W2, dGU, dX_perm, dw, dlogits, scratch,
+                                    stream=None):
+    _call("moe_grouped_ffn_dgrad_reordered", _cfg(cfg), dO_perm, GU, counts, offsets, token_of,
+          row_of, logits, idx, w, W_r, W13, W2, dGU, dX_perm, dw, dlogits, scratch,
+          _stream(stream))
 
 
 def moe_route_bwd(cfg, logits, idx, w, dw, dlogits, stream=None):

@@ -7,6 +7,7 @@
 // bandwidth-bound: one warp per token, 16-byte vector accesses, fp32
 // accumulation in a fixed order.
 #include "common.cuh"
+#include "fp8_layout.cuh"
 #include "internal.h"
 
 namespace moe {
@@ -155,13 +156,18 @@ __device__ __forceinline__ int find_pad_group(const int* prefix, int G, int p) {
 // U*k y slices of one step in flight together. Every lane sums its slices in
 // order and the warp combines lanes by a fixed butterfly, so dw is
 // deterministic. No block-wide synchronisation on the token path.
-template <int MAXR, int U>
+// COPY (the layer with the routing weight inside the expert): dO[row_tj] =
+// dY[t] unweighted, y is not read and dw is not written (it comes from the FC2
+// data gradient there). With dOq (the FP8 configuration) every row written is
+// also written in its 1-byte form -- E4M3 codes of the bf16 values' 1 x 128
+// slices with their UE8M0 scales in dOsf's atoms -- for the FC2 data gradient.
+template <int MAXR, int U, bool COPY = false>
 __global__ void __launch_bounds__(256, (MAXR <= 2) ? 3 : 2)
 unpermute_bwd_kernel(const __nv_bfloat16* __restrict__ dY, const __nv_bfloat16* __restrict__ y,
                      const int32_t* __restrict__ row_of, const float* __restrict__ w,
                      const int32_t* __restrict__ counts, const int32_t* __restrict__ offsets,
                      __nv_bfloat16* __restrict__ dO, float* __restrict__ dw, int T, int H, int k,
-                     int E, int S) {
+                     int E, int S, uint8_t* __restrict__ dOq, uint8_t* __restrict__ dOsf) {
   __shared__ int s_pp[kMaxGroups + 1];
   __shared__ int s_off[kMaxGroups + 1];
   __shared__ int s_cnt[kMaxGroups];
@@ -170,7 +176,10 @@ unpermute_bwd_kernel(const __nv_bfloat16* __restrict__ dY, const __nv_bfloat16* 
   for (int g = threadIdx.x; g <= G; g += blockDim.x) s_off[g] = offsets[g];
   for (int g = threadIdx.x; g < G; g += blockDim.x) s_cnt[g] = counts[g];
   __syncthreads();
-  for (int g = threadIdx.x; g < G; g += blockDim.x) s_pp[g] = s_off[g + 1] - s_off[g] - s_cnt[g];
+  // padding rows to zero: the rest of each segment's last 128-row block (the
+  // rows a GEMM reads; rows past it are never read)
+  for (int g = threadIdx.x; g < G; g += blockDim.x)
+    s_pp[g] = min(s_off[g + 1] - s_off[g], (s_cnt[g] + 127) / 128 * 128) - s_cnt[g];
   __syncthreads();
   const int P = block_exclusive_scan(s_pp, G, s_tmp);
   if (threadIdx.x == 0) s_pp[G] = P;
@@ -178,13 +187,21 @@ unpermute_bwd_kernel(const __nv_bfloat16* __restrict__ dY, const __nv_bfloat16* 
   const int lane = threadIdx.x & 31;
   const int nvec = H >> 3, nr = k + S;
   const int warps = gridDim.x * (blockDim.x >> 5);
+  const int64_t kg = f8::atoms_k(H);
+  const unsigned half = (lane & 16) ? 0xffff0000u : 0x0000ffffu;
   for (int v = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); v < T + P; v += warps) {
     if (v >= T) {
       const int p = v - T;
       const int g = find_pad_group(s_pp, G, p);
       const int r = s_off[g] + s_cnt[g] + (p - s_pp[g]);
       const uint4 z = make_uint4(0u, 0u, 0u, 0u);
-      for (int c = lane; c < nvec; c += 32) stg_v4(dO + (size_t)r * H + (size_t)c * 8, z);
+      for (int c = lane; c < nvec; c += 32) {
+        stg_v4(dO + (size_t)r * H + (size_t)c * 8, z);
+        if (dOq) {
+          *reinterpret_cast<uint2*>(dOq + (size_t)r * H + (size_t)c * 8) = make_uint2(0u, 0u);
+          if ((c & 15) == 0) dOsf[f8::atom_offset(r >> 7, c >> 4, kg) + f8::atom_byte(r, c >> 4)] = 127u;
+        }
+      }
       continue;
     }
     const int t = v;
@@ -192,7 +209,7 @@ unpermute_bwd_kernel(const __nv_bfloat16* __restrict__ dY, const __nv_bfloat16* 
     float mywt = 0.f;
     if (lane < k) {
       myrow = row_of[(size_t)t * k + lane];
-      mywt = w[(size_t)t * k + lane];
+      mywt = COPY ? 1.f : w[(size_t)t * k + lane];    // the copy has no weights (w NULL)
     } else if (lane < nr) {
       myrow = s_off[E + lane - k] + t;
     }
@@ -214,7 +231,8 @@ unpermute_bwd_kernel(const __nv_bfloat16* __restrict__ dY, const __nv_bfloat16* 
         gq[u] = ldg_nc_v4(gsrc + (size_t)c * 8);
 #pragma unroll
         for (int j = 0; j < MAXR; ++j)
-          if (j < k && rows[j] >= 0) yq[u][j] = ldg_nc_v4(y + (size_t)rows[j] * H + (size_t)c * 8);
+          if (!COPY && j < k && rows[j] >= 0)
+            yq[u][j] = ldg_nc_v4(y + (size_t)rows[j] * H + (size_t)c * 8);
       }
 #pragma unroll
       for (int u = 0; u < U; ++u) {
@@ -226,21 +244,38 @@ unpermute_bwd_kernel(const __nv_bfloat16* __restrict__ dY, const __nv_bfloat16* 
         for (int j = 0; j < MAXR; ++j) {
           if (j >= nr || rows[j] < 0) continue;
           __nv_bfloat16* dst = dO + (size_t)rows[j] * H + (size_t)c * 8;
-          if (j >= k) {
-            stg_v4(dst, gq[u]);
-            continue;
-          }
-          float f[8], o[8];
-          unpack8(yq[u][j], f);
+          uint4 ov;
+          if (COPY || j >= k) {
+            ov = gq[u];
+          } else {
+            float f[8], o[8];
+            unpack8(yq[u][j], f);
 #pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            dot[j] = fmaf(g[i], f[i], dot[j]);
-            o[i] = wts[j] * g[i];
+            for (int i = 0; i < 8; ++i) {
+              dot[j] = fmaf(g[i], f[i], dot[j]);
+              o[i] = wts[j] * g[i];
+            }
+            ov = pack8(o);
           }
-          stg_v4(dst, pack8(o));
+          stg_v4(dst, ov);
+          if (dOq) {
+            // a half-warp holds one 128-element slice (nvec % 32 == 0 in this mode)
+            float fq[8];
+            unpack8(ov, fq);
+            float m = amax8(fq);
+#pragma unroll
+            for (int o = 8; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(half, m, o));
+            const uint32_t code = ue8m0_code(m);
+            *reinterpret_cast<uint2*>(dOq + (size_t)rows[j] * H + (size_t)c * 8) =
+                e4m3x8(fq, ue8m0_inv(code));
+            if ((lane & 15) == 0)
+              dOsf[f8::atom_offset(rows[j] >> 7, c >> 4, kg) + f8::atom_byte(rows[j], c >> 4)] =
+                  (uint8_t)code;
+          }
         }
       }
     }
+    if (COPY) continue;
     float mine = 0.f;
 #pragma unroll
     for (int j = 0; j < MAXR; ++j) {
@@ -249,6 +284,47 @@ unpermute_bwd_kernel(const __nv_bfloat16* __restrict__ dY, const __nv_bfloat16* 
       if (lane == j) mine = (rows[j] >= 0) ? sj : 0.f;
     }
     if (lane < k) dw[(size_t)t * k + lane] = mine;
+  }
+}
+
+// Routing weight of every used row of the permuted buffer, for the layer with
+// the weight inside the expert: w[t, j] for the row of assignment (t, j), 1 for
+// a shared expert's row, 0 for padding. One thread per row.
+__global__ void __launch_bounds__(256)
+row_weights_kernel(const int32_t* __restrict__ token_of, const int32_t* __restrict__ row_of,
+                   const float* __restrict__ w, const int32_t* __restrict__ offsets,
+                   float* __restrict__ row_w, int k, int E, int S) {
+  const int used = offsets[E + S];
+  const int routed_end = offsets[E];
+  for (int r = blockIdx.x * blockDim.x + threadIdx.x; r < used; r += gridDim.x * blockDim.x) {
+    const int t = token_of[r];
+    float v = 0.f;
+    if (t >= 0) {
+      if (r >= routed_end) {
+        v = 1.f;
+      } else {
+        for (int j = 0; j < k; ++j)
+          if (row_of[(size_t)t * k + j] == r) {
+            v = w[(size_t)t * k + j];
+            break;
+          }
+      }
+    }
+    row_w[r] = v;
+  }
+}
+
+// dw[t, j] = sum over the FC2 data gradient's n-tiles (in order) of the partial
+// <dh_s, h> of the row of assignment (t, j); 0 for a dropped assignment.
+__global__ void __launch_bounds__(256)
+dw_reduce_kernel(const float* __restrict__ part, int nt, const int32_t* __restrict__ row_of,
+                 float* __restrict__ dw, int n) {
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x) {
+    const int r = row_of[i];
+    float acc = 0.f;
+    if (r >= 0)
+      for (int q = 0; q < nt; ++q) acc += part[(size_t)r * nt + q];
+    dw[i] = acc;
   }
 }
 
@@ -400,7 +476,7 @@ cudaError_t launch_unpermute(const moe_config& c, const void* y_perm, const int3
 cudaError_t launch_unpermute_bwd(const moe_config& c, const void* dY, const void* y_perm,
                                  const int32_t* row_of, const float* w, const int32_t* counts,
                                  const int32_t* offsets, void* dO_perm, float* dw,
-                                 cudaStream_t s) {
+                                 cudaStream_t s, uint8_t* dOq, uint8_t* dOsf) {
   auto dYp = static_cast<const __nv_bfloat16*>(dY);
   auto yp = static_cast<const __nv_bfloat16*>(y_perm);
   auto dOp = static_cast<__nv_bfloat16*>(dO_perm);
@@ -408,13 +484,55 @@ cudaError_t launch_unpermute_bwd(const moe_config& c, const void* dY, const void
   const int grid = grid_for_warps(c.T);
   if (c.k + c.n_shared <= 2)
     unpermute_bwd_kernel<2, 4><<<grid, 256, 0, s>>>(dYp, yp, row_of, w, counts, offsets, dOp, dw,
-                                                    c.T, c.H, c.k, c.E, c.n_shared);
+                                                    c.T, c.H, c.k, c.E, c.n_shared, dOq, dOsf);
   else if (c.k + c.n_shared <= 4)
     unpermute_bwd_kernel<4, 4><<<grid, 256, 0, s>>>(dYp, yp, row_of, w, counts, offsets, dOp, dw,
-                                                    c.T, c.H, c.k, c.E, c.n_shared);
+                                                    c.T, c.H, c.k, c.E, c.n_shared, dOq, dOsf);
   else
     unpermute_bwd_kernel<kMaxK + 4, 1><<<grid, 256, 0, s>>>(
-        dYp, yp, row_of, w, counts, offsets, dOp, dw, c.T, c.H, c.k, c.E, c.n_shared);
+        dYp, yp, row_of, w, counts, offsets, dOp, dw, c.T, c.H, c.k, c.E, c.n_shared, dOq, dOsf);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_unpermute_bwd_copy(const moe_config& c, const void* dY, const int32_t* row_of,
+                                      const int32_t* counts, const int32_t* offsets,
+                                      void* dO_perm, cudaStream_t s) {
+  auto dYp = static_cast<const __nv_bfloat16*>(dY);
+  auto dOp = static_cast<__nv_bfloat16*>(dO_perm);
+  const int grid = grid_for_warps(c.T);
+  if (c.k + c.n_shared <= 2)
+    unpermute_bwd_kernel<2, 4, true><<<grid, 256, 0, s>>>(dYp, nullptr, row_of, nullptr, counts,
+                                                          offsets, dOp, nullptr, c.T, c.H, c.k,
+                                                          c.E, c.n_shared, nullptr, nullptr);
+  else if (c.k + c.n_shared <= 4)
+    unpermute_bwd_kernel<4, 4, true><<<grid, 256, 0, s>>>(dYp, nullptr, row_of, nullptr, counts,
+                                                          offsets, dOp, nullptr, c.T, c.H, c.k,
+                                                          c.E, c.n_shared, nullptr, nullptr);
+  else
+    unpermute_bwd_kernel<kMaxK + 4, 1, true><<<grid, 256, 0, s>>>(
+        dYp, nullptr, row_of, nullptr, counts, offsets, dOp, nullptr, c.T, c.H, c.k, c.E,
+        c.n_shared, nullptr, nullptr);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_row_weights(const moe_config& c, const int32_t* token_of,
+                               const int32_t* row_of, const float* w, const int32_t* offsets,
+                               float* row_w, cudaStream_t s) {
+  const int64_t R = rows_max(c);
+  long long blocks = (R + 255) / 256;
+  if (blocks > (long long)num_sms() * 8) blocks = (long long)num_sms() * 8;
+  row_weights_kernel<<<blocks > 0 ? (int)blocks : 1, 256, 0, s>>>(token_of, row_of, w, offsets,
+                                                                  row_w, c.k, c.E, c.n_shared);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_dw_reduce(const moe_config& c, const float* dw_part, const int32_t* row_of,
+                             float* dw, cudaStream_t s) {
+  const int n = c.T * c.k;
+  long long blocks = (n + 255) / 256;
+  if (blocks > (long long)num_sms() * 8) blocks = (long long)num_sms() * 8;
+  dw_reduce_kernel<<<blocks > 0 ? (int)blocks : 1, 256, 0, s>>>(dw_part, dw_tiles(c), row_of, dw,
+                                                                 n);
   return cudaGetLastError();
 }
 

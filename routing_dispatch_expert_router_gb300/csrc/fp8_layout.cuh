@@ -14,6 +14,7 @@
 // Atoms are stored [row block][atom along K]; a UE8M0 byte e means 2^(e-127).
 #pragma once
 
+#include <cuda_runtime.h>
 #include <stdint.h>
 
 namespace moe {
@@ -40,4 +41,46 @@ __host__ __device__ constexpr int64_t sf_bytes(int64_t rows, int64_t K) {
 }
 
 }  // namespace f8
+
+// ------------------------------------------- producing the 1-byte form (device)
+// UE8M0 code (2^(code-127)) of the block scale 2^ceil(log2(amax/448)) of the
+// 1-byte form, from the bits of amax = 2^E * M (1 <= M < 2): amax/448 =
+// 2^(E-8) * M/1.75, so ceil(log2(amax/448)) = E - 8 when M <= 1.75 and E - 7
+// when M > 1.75 (the quotient of a bf16 amax and 448 never lies just below a
+// power of two, so this is the exact ceiling). amax = 0 gives scale 1 (code
+// 127). Scales below 2^-127, the smallest UE8M0 value (amax < 448 * 2^-128),
+// are raised to 2^-127; there the scaled values keep fewer bits than the fp64
+// reference's, a case no bf16 activation or weight of normal magnitude meets.
+__device__ __forceinline__ uint32_t ue8m0_code(float amax) {
+  if (!(amax > 0.f)) return 127u;
+  const uint32_t b = __float_as_uint(amax);
+  const int code = (int)(b >> 23) - 8 + ((b & 0x7FFFFFu) > 0x600000u ? 1 : 0);
+  return code < 0 ? 0u : (uint32_t)code;
+}
+// 1 / scale = 2^(127 - code), exact (a normal fp32 for every code 0..253).
+__device__ __forceinline__ float ue8m0_inv(uint32_t code) {
+  return __uint_as_float((254u - code) << 23);
+}
+
+// E4M3 codes of eight values divided by a power-of-two scale (exact): bytes in
+// element order.
+__device__ __forceinline__ uint2 e4m3x8(const float (&f)[8], float inv_s) {
+  uint32_t w[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    uint16_t h;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;"
+        : "=h"(h) : "f"(f[2 * i + 1] * inv_s), "f"(f[2 * i] * inv_s));
+    w[i] = h;
+  }
+  return make_uint2(w[0] | (w[1] << 16), w[2] | (w[3] << 16));
+}
+
+__device__ __forceinline__ float amax8(const float (&f)[8]) {
+  float m = 0.f;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) m = fmaxf(m, fabsf(f[i]));
+  return m;
+}
+
 }  // namespace moe

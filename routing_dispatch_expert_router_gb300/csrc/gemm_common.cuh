@@ -23,7 +23,13 @@ constexpr int kStageBytes = 3 * kBoxBytes;       // output staging per epilogue 
 constexpr long long kWaitBudget = 4000000000LL;   // clock64 cycles (~2 s)
 
 enum Epi : int { kEpiSwigluFwd = 0, kEpiStore = 1, kEpiSwigluBwd = 2, kEpiWgrad = 3,
-                 kEpiStoreF32 = 4, kEpiDgradRouter = 5, kEpiAddBf16 = 6 };
+                 kEpiStoreF32 = 4, kEpiDgradRouter = 5, kEpiAddBf16 = 6,
+                 // the layer with the routing weight inside the expert: FC1 writes
+                 // h_s = w_row silu(G) U; the FC2 data gradient scales dh_s by w_row
+                 // and writes each row's partial <dh_s, h> for the weight's gradient
+                 kEpiSwigluFwdW = 7, kEpiSwigluBwdW = 8 };
+constexpr bool swiglu_fwd(int epi) { return epi == kEpiSwigluFwd || epi == kEpiSwigluFwdW; }
+constexpr bool swiglu_bwd(int epi) { return epi == kEpiSwigluBwd || epi == kEpiSwigluBwdW; }
 
 struct Params {
   int kgrouped;               // 0: row-grouped, 1: K-grouped
@@ -56,6 +62,12 @@ struct Params {
   const float* W_r;
   int router_E;
   int router_T;               // rows of dlogits; a token id outside [0, router_T) adds nothing
+  // routing weight inside the expert (kEpiSwigluFwdW / kEpiSwigluBwdW): the
+  // weight of every permuted row, and the FC2 data gradient's per-tile partial
+  // dot products <dh_s, h> of every row ([R][dw_nt], fp32)
+  const float* row_w;
+  float* dw_part;
+  int dw_nt;
   // FP8 block-scaled operands (grouped_gemm_fp8.cu): UE8M0 scale atoms of A
   // ([R/128][sfa_kg]) and of B ([G * sfb_nb][sfb_kg]), fp8_layout.cuh
   const uint8_t* sfa;
@@ -148,6 +160,45 @@ __device__ __forceinline__ void swiglu_bwd8(const uint32_t* dh, const uint4& g, 
     ptx::f2_unpack(ptx::f2_add(ptx::f2_pack(ptx::ex2_approx(e0), ptx::ex2_approx(e1)), one), d0, d1);
     const uint64_t S = ptx::f2_pack(ptx::rcp_approx(d0), ptx::rcp_approx(d1));
     const uint64_t SILU = ptx::f2_mul(G, S);
+    const uint64_t DU = ptx::f2_mul(D, SILU);
+    const uint64_t T = ptx::f2_fma(SILU, ptx::f2_sub(one, S), S);
+    const uint64_t DG = ptx::f2_mul(ptx::f2_mul(D, U), T);
+    float a0, a1, b0, b1;
+    ptx::f2_unpack(DG, a0, a1);
+    ptx::f2_unpack(DU, b0, b1);
+    dgw[j] = pack_bf16x2(a0, a1);
+    duw[j] = pack_bf16x2(b0, b1);
+  }
+  dg = make_uint4(dgw[0], dgw[1], dgw[2], dgw[3]);
+  du = make_uint4(duw[0], duw[1], duw[2], duw[3]);
+}
+
+// The same with the routing weight inside the expert: dh_s (the accumulator)
+// is the gradient of h_s = w h, so dh = w dh_s, and the weight's gradient gains
+// <dh_s, h> with h = silu(g) u recomputed here (added to `dot` in column order).
+__device__ __forceinline__ void swiglu_bwd8_w(const uint32_t* dhs, const uint4& g, const uint4& u,
+                                              float w, uint4& dg, uint4& du, float& dot) {
+  const uint32_t gw[4] = {g.x, g.y, g.z, g.w}, uw[4] = {u.x, u.y, u.z, u.w};
+  uint32_t dgw[4], duw[4];
+  const uint64_t one = ptx::f2_pack(1.f, 1.f);
+  const uint64_t nl2e = ptx::f2_pack(-kLog2e, -kLog2e);
+  const uint64_t W2v = ptx::f2_pack(w, w);
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const uint64_t G = ptx::f2_pack(bf16_lo(gw[j]), bf16_hi(gw[j]));
+    const uint64_t U = ptx::f2_pack(bf16_lo(uw[j]), bf16_hi(uw[j]));
+    const uint64_t Ds = ptx::f2_pack(__uint_as_float(dhs[2 * j]), __uint_as_float(dhs[2 * j + 1]));
+    float e0, e1;
+    ptx::f2_unpack(ptx::f2_mul(G, nl2e), e0, e1);
+    float d0, d1;
+    ptx::f2_unpack(ptx::f2_add(ptx::f2_pack(ptx::ex2_approx(e0), ptx::ex2_approx(e1)), one), d0, d1);
+    const uint64_t S = ptx::f2_pack(ptx::rcp_approx(d0), ptx::rcp_approx(d1));
+    const uint64_t SILU = ptx::f2_mul(G, S);
+    float p0, p1;
+    ptx::f2_unpack(ptx::f2_mul(Ds, ptx::f2_mul(SILU, U)), p0, p1);
+    dot += p0;
+    dot += p1;
+    const uint64_t D = ptx::f2_mul(Ds, W2v);
     const uint64_t DU = ptx::f2_mul(D, SILU);
     const uint64_t T = ptx::f2_fma(SILU, ptx::f2_sub(one, S), S);
     const uint64_t DG = ptx::f2_mul(ptx::f2_mul(D, U), T);

@@ -43,8 +43,8 @@ __device__ __forceinline__ void epilogue_tile(const Params& p, const CUtensorMap
                                               const int* s_off, uint8_t* stage,
                                               uint32_t stage_u32) {
   const int row0 = p.kgrouped ? g * p.Mw + mt * BM + q * 32 : s_off[g] + mt * BM + q * 32;
-  const int ncols = (EPI == kEpiSwigluFwd) ? BN / 2 : BN;
-  const int f0 = (EPI == kEpiSwigluFwd) ? nt * (BN / 2) : nt * BN;
+  const int ncols = swiglu_fwd(EPI) ? BN / 2 : BN;
+  const int f0 = swiglu_fwd(EPI) ? nt * (BN / 2) : nt * BN;
   // router term of this warp's row (lane) for the FC1 data gradient
   float rd = 0.f;
   const float* rw = nullptr;
@@ -121,9 +121,14 @@ __device__ __forceinline__ void epilogue_tile(const Params& p, const CUtensorMap
     }
     return;
   }
+  // routing weight of this warp's row (lane) and the row's partial <dh_s, h>
+  // when the weight sits inside the expert
+  constexpr bool WGT = EPI == kEpiSwigluFwdW || EPI == kEpiSwigluBwdW;
+  const float rwt = WGT ? p.row_w[row0 + lane] : 1.f;
+  float dot = 0.f;
   uint4 gq[4], uq[4];
   const __nv_bfloat16* gu = nullptr;
-  if (EPI == kEpiSwigluBwd) {
+  if (swiglu_bwd(EPI)) {
     // G and U of the next 32 columns are loaded one slice ahead
     gu = p.aux + (long long)(row0 + lane) * p.ldaux;
 #pragma unroll
@@ -135,7 +140,7 @@ __device__ __forceinline__ void epilogue_tile(const Params& p, const CUtensorMap
 #pragma unroll 1
   for (int c = 0; c < ncols; c += 32) {
     uint4 o0[4], o1[4], o2[4];
-    if (EPI == kEpiSwigluFwd) {
+    if (swiglu_fwd(EPI)) {
       uint32_t rg[32], ru[32];
       ptx::tmem_ld32(tbase + c, rg);
       ptx::tmem_ld32(tbase + BN / 2 + c, ru);
@@ -148,10 +153,10 @@ __device__ __forceinline__ void epilogue_tile(const Params& p, const CUtensorMap
         unpack8(o0[v], gr);
         unpack8(o1[v], ur);
 #pragma unroll
-        for (int i = 0; i < 8; ++i) hf[i] = silu_f(gr[i]) * ur[i];
+        for (int i = 0; i < 8; ++i) hf[i] = WGT ? silu_f(gr[i]) * ur[i] * rwt : silu_f(gr[i]) * ur[i];
         o2[v] = pack8(hf);
       }
-    } else if (EPI == kEpiSwigluBwd) {
+    } else if (swiglu_bwd(EPI)) {
       uint32_t r[32];
       ptx::tmem_ld32(tbase + c, r);
       uint4 gn[4], un[4];
@@ -164,7 +169,8 @@ __device__ __forceinline__ void epilogue_tile(const Params& p, const CUtensorMap
       ptx::tmem_ld_wait();
 #pragma unroll
       for (int v = 0; v < 4; ++v) {
-        swiglu_bwd8(r + v * 8, gq[v], uq[v], o0[v], o1[v]);
+        if (WGT) swiglu_bwd8_w(r + v * 8, gq[v], uq[v], rwt, o0[v], o1[v], dot);
+        else swiglu_bwd8(r + v * 8, gq[v], uq[v], o0[v], o1[v]);
         gq[v] = gn[v];
         uq[v] = un[v];
       }
@@ -194,11 +200,11 @@ __device__ __forceinline__ void epilogue_tile(const Params& p, const CUtensorMap
     __syncwarp();
     stage_row(stage, 0, lane, o0);
     stage_row(stage, 1, lane, o1);
-    if (EPI == kEpiSwigluFwd) stage_row(stage, 2, lane, o2);
+    if (swiglu_fwd(EPI)) stage_row(stage, 2, lane, o2);
     ptx::fence_proxy_async_smem();
     __syncwarp();
     if (lane == 0) {
-      if (EPI == kEpiSwigluFwd) {
+      if (swiglu_fwd(EPI)) {
         ptx::tma_store_2d(tmC, stage_u32, f0 + c, row0);                      // G
         ptx::tma_store_2d(tmC, stage_u32 + kBoxBytes, p.F + f0 + c, row0);    // U
         ptx::tma_store_2d(tmC2, stage_u32 + 2 * kBoxBytes, f0 + c, row0);     // h
@@ -209,6 +215,7 @@ __device__ __forceinline__ void epilogue_tile(const Params& p, const CUtensorMap
       ptx::tma_store_commit();
     }
   }
+  if (EPI == kEpiSwigluBwdW) p.dw_part[(long long)(row0 + lane) * p.dw_nt + nt] = dot;
 }
 
 template <int EPI, int BN, int A_MN, int B_MN, int STAGES>
@@ -239,7 +246,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int G = p.G;
-  const int NT = (EPI == kEpiSwigluFwd) ? p.F / (BN / 2) : p.N / BN;
+  const int NT = swiglu_fwd(EPI) ? p.F / (BN / 2) : p.N / BN;
   for (int g = tid; g < G; g += kThreads) {
     const int c = p.chunk_rows > 0 ? min(p.chunk_rows, p.dense_rows - g * p.chunk_rows)
                   : p.dense_rows > 0 ? p.dense_rows : p.counts[g];
@@ -306,7 +313,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             ptx::tma_load_2d(sA, &tmA, fb, t.mt * BM, kr);
             ptx::tma_load_2d(sA + 8192, &tmA, fb, t.mt * BM + 64, kr);
           }
-          if (EPI == kEpiSwigluFwd) {
+          if (swiglu_fwd(EPI)) {
             const int f0 = t.nt * (BN / 2);
             ptx::tma_load_2d(sB, &tmB, fb, k0, t.g * p.b_rows + f0);
             ptx::tma_load_2d(sB + (BN / 2) * 128, &tmB, fb, k0, t.g * p.b_rows + p.F + f0);
@@ -462,7 +469,7 @@ constexpr int kGuBarOff = 4864;                   // ring mbarriers in the contr
 
 template <int EPI>
 struct PairCfg {
-  static constexpr bool RING = EPI == kEpiSwigluBwd;
+  static constexpr bool RING = swiglu_bwd(EPI);
   static constexpr int STAGES = RING ? 5 : 6;
   static constexpr int EPI_BYTES = RING ? kGuRingBytes : kStageBytes;   // per epilogue warp
   static constexpr int SMEM = STAGES * kPairStage + kCtrlBytes + 4 * EPI_BYTES + 1024;
@@ -475,8 +482,10 @@ static_assert(kGuBarOff >= 4608 + 33 * 4 && kGuBarOff + 4 * kGuSlots * 8 <= kCtr
 // dG and dU of one 32-column slice from dH (fp32, 32 tensor-memory columns of
 // this lane's row) and the row's G and U, in place in a ring slot: 16-byte
 // chunk j of the row sits at slot j ^ ((row >> 1) & 3) of its 64 bytes.
+template <bool WGT>
 __device__ __forceinline__ void swiglu_bwd_slice_inplace(uint8_t* slot, int lane,
-                                                         const uint32_t (&r)[32]) {
+                                                         const uint32_t (&r)[32], float rwt,
+                                                         float& dot) {
   uint8_t* grow = slot + lane * 64;
   uint8_t* urow = grow + kBoxBytes;
   const int sw = (lane >> 1) & 3;
@@ -484,8 +493,12 @@ __device__ __forceinline__ void swiglu_bwd_slice_inplace(uint8_t* slot, int lane
   for (int v = 0; v < 4; ++v) {
     const int pos = (v ^ sw) << 4;
     uint4 dg, du;
-    swiglu_bwd8(r + v * 8, *reinterpret_cast<const uint4*>(grow + pos),
-                *reinterpret_cast<const uint4*>(urow + pos), dg, du);
+    if (WGT)
+      swiglu_bwd8_w(r + v * 8, *reinterpret_cast<const uint4*>(grow + pos),
+                    *reinterpret_cast<const uint4*>(urow + pos), rwt, dg, du, dot);
+    else
+      swiglu_bwd8(r + v * 8, *reinterpret_cast<const uint4*>(grow + pos),
+                  *reinterpret_cast<const uint4*>(urow + pos), dg, du);
     *reinterpret_cast<uint4*>(grow + pos) = dg;
     *reinterpret_cast<uint4*>(urow + pos) = du;
   }
@@ -523,7 +536,7 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA,
   const uint32_t rank = ptx::cluster_ctarank();
   const int cluster = blockIdx.x >> 1, nclusters = gridDim.x >> 1;
   const int G = p.G;
-  const int NT = (EPI == kEpiSwigluFwd) ? p.F / (BN / 2) : p.N / BN;
+  const int NT = swiglu_fwd(EPI) ? p.F / (BN / 2) : p.N / BN;
   for (int g = tid; g < G; g += kThreads) {
     const int c = p.chunk_rows > 0 ? min(p.chunk_rows, p.dense_rows - g * p.chunk_rows)
                   : p.dense_rows > 0 ? p.dense_rows : p.counts[g];
@@ -610,7 +623,7 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA,
             ptx::tma_load_2d_pair(sA, &tmA, fb, mt * BM, kr);
             ptx::tma_load_2d_pair(sA + 8192, &tmA, fb, mt * BM + 64, kr);
           }
-          if (EPI == kEpiSwigluFwd) {
+          if (swiglu_fwd(EPI)) {
             // CTA 0 brings the 128 gate rows, CTA 1 the matching 128 up rows
             ptx::tma_load_2d_pair(sB, &tmB, fb, k0,
                                   g * p.b_rows + (rank ? p.F : 0) + nt * (BN / 2));
@@ -747,6 +760,9 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA,
       ptx::tc_fence_after();
       if (mine) {
         const uint32_t tbase = tmem_base + acc * BN + ((uint32_t)(q * 32) << 16);
+        constexpr bool WGT = EPI == kEpiSwigluBwdW;
+        const float rwt = WGT ? p.row_w[row0 + lane] : 1.f;
+        float dot = 0.f;
 #pragma unroll 1
         for (int c = 0; c < BN; c += 32) {
           const uint32_t slot = used % kGuSlots;
@@ -756,7 +772,7 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA,
           uint32_t r[32];
           ptx::tmem_ld32(tbase + c, r);
           ptx::tmem_ld_wait();
-          swiglu_bwd_slice_inplace(ring + slot * kGuSlotBytes, lane, r);
+          swiglu_bwd_slice_inplace<WGT>(ring + slot * kGuSlotBytes, lane, r, rwt, dot);
           ptx::fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0) {
@@ -771,6 +787,7 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA,
           issue();
         }
         if (!ok) break;
+        if (WGT) p.dw_part[(long long)(row0 + lane) * p.dw_nt + f0 / BN] = dot;
       }
       ptx::tc_fence_before();
       __syncwarp();
@@ -898,9 +915,13 @@ static bool use_pairs(const moe_config& c, int n) {
 
 using namespace gg;
 
+// N tiles of the FC2 data gradient (F wide): 256-column tiles when F is a
+// multiple of 256 (CTA pairs or single CTAs), else 128.
+int dw_tiles(const moe_config& c) { return c.F % 256 == 0 ? c.F / 256 : c.F / 128; }
+
 cudaError_t launch_ffn_fc1(const moe_config& c, const void* x_perm, const int32_t* counts,
                            const int32_t* offsets, const void* W13, void* GU, void* h,
-                           int32_t* status, cudaStream_t s) {
+                           int32_t* status, cudaStream_t s, const float* row_w) {
   const int64_t R = rows_max(c);
   const int G = c.E + c.n_shared;
   CUtensorMap a, b, oc, oc2;
@@ -914,6 +935,11 @@ cudaError_t launch_ffn_fc1(const moe_config& c, const void* x_perm, const int32_
   p.ldo = 2LL * c.F;
   p.out2 = static_cast<__nv_bfloat16*>(h);
   p.ldo2 = c.F;
+  if (row_w) {                                     // h_s = w_row silu(G) U
+    p.row_w = row_w;
+    if (use_pairs(c, 256)) return run_pair<kEpiSwigluFwdW, 0, 0>(a, b, oc, oc2, p, s);
+    return run<kEpiSwigluFwdW, 256, 0, 0, 4>(a, b, oc, oc2, p, s);
+  }
   if (use_pairs(c, 256)) return run_pair<kEpiSwigluFwd, 0, 0>(a, b, oc, oc2, p, s);
   return run<kEpiSwigluFwd, 256, 0, 0, 4>(a, b, oc, oc2, p, s);
 }
@@ -944,7 +970,8 @@ cudaError_t launch_ffn_fc2(const moe_config& c, const void* h, const int32_t* co
 
 cudaError_t launch_ffn_fc2_dgrad(const moe_config& c, const void* dO_perm, const int32_t* counts,
                                  const int32_t* offsets, const void* W2, const void* GU,
-                                 void* dGU, int32_t* status, cudaStream_t s) {
+                                 void* dGU, int32_t* status, cudaStream_t s, const float* row_w,
+                                 float* dw_part) {
   const int64_t R = rows_max(c);
   const int G = c.E + c.n_shared;
   const int bn = (c.F % 256 == 0) ? 256 : 128;
@@ -961,6 +988,14 @@ cudaError_t launch_ffn_fc2_dgrad(const moe_config& c, const void* dO_perm, const
   p.ldo = 2LL * c.F;
   p.aux = static_cast<const __nv_bfloat16*>(GU);
   p.ldaux = 2LL * c.F;
+  if (row_w) {                                     // dh = w_row dh_s, partial <dh_s, h>
+    p.row_w = row_w;
+    p.dw_part = dw_part;
+    p.dw_nt = dw_tiles(c);
+    if (use_pairs(c, c.F)) return run_pair<kEpiSwigluBwdW, 0, 1>(a, b, oc, oc2, p, s);
+    return bn == 256 ? run<kEpiSwigluBwdW, 256, 0, 1, 4>(a, b, oc, oc2, p, s)
+                     : run<kEpiSwigluBwdW, 128, 0, 1, 6>(a, b, oc, oc2, p, s);
+  }
   if (use_pairs(c, c.F)) return run_pair<kEpiSwigluBwd, 0, 1>(a, b, oc, oc2, p, s);
   return bn == 256 ? run<kEpiSwigluBwd, 256, 0, 1, 4>(a, b, oc, oc2, p, s)
                    : run<kEpiSwigluBwd, 128, 0, 1, 6>(a, b, oc, oc2, p, s);

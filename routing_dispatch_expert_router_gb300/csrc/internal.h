@@ -21,17 +21,40 @@ cudaError_t launch_route_replay(const moe_config& c, const void* x, const float*
                                 const float* bias, const int32_t* idx, float* logits, float* w,
                                 uint8_t* scratch, cudaStream_t s);
 
+struct Fp8Scratch;
+// fp8 (FP8 configuration, optional): also write x_perm's 1-byte form there.
 cudaError_t launch_permute(const moe_config& c, const void* x, const int32_t* idx,
                            int32_t* counts, int32_t* offsets, int32_t* row_of, int32_t* token_of,
                            int32_t* sel_offsets, int32_t* sel_tokens, void* x_perm,
-                           uint8_t* scratch, cudaStream_t s);
+                           uint8_t* scratch, cudaStream_t s, const Fp8Scratch* fp8 = nullptr);
 
 cudaError_t launch_unpermute(const moe_config& c, const void* y_perm, const int32_t* row_of,
                              const float* w, const int32_t* offsets, void* out, cudaStream_t s);
 
+// dOq, dOsf (FP8 configuration, optional): also write dO_perm's 1-byte form.
 cudaError_t launch_unpermute_bwd(const moe_config& c, const void* dY, const void* y_perm,
                                  const int32_t* row_of, const float* w, const int32_t* counts,
-                                 const int32_t* offsets, void* dO_perm, float* dw, cudaStream_t s);
+                                 const int32_t* offsets, void* dO_perm, float* dw, cudaStream_t s,
+                                 uint8_t* dOq = nullptr, uint8_t* dOsf = nullptr);
+
+// The layer with the routing weight inside the expert: the unweighted copy of
+// dY into the expert rows (dO_perm), the routing weight of every permuted row,
+// and dw from the FC2 data gradient's per-tile partial dot products.
+cudaError_t launch_unpermute_bwd_copy(const moe_config& c, const void* dY, const int32_t* row_of,
+                                      const int32_t* counts, const int32_t* offsets,
+                                      void* dO_perm, cudaStream_t s);
+cudaError_t launch_row_weights(const moe_config& c, const int32_t* token_of,
+                               const int32_t* row_of, const float* w, const int32_t* offsets,
+                               float* row_w, cudaStream_t s);
+cudaError_t launch_dw_reduce(const moe_config& c, const float* dw_part, const int32_t* row_of,
+                             float* dw, cudaStream_t s);
+// Where the layer with the weight inside the expert keeps its per-row weights
+// ([rows_max] fp32) and the partial dot products ([rows_max][dw_tiles] fp32).
+struct ReorderScratch {
+  float* row_w;
+  float* dw_part;
+};
+ReorderScratch reorder_scratch(const moe_config& c, void* scratch);
 
 cudaError_t launch_route_bwd(const moe_config& c, const float* logits, const int32_t* idx,
                              const float* w, const float* dw, float* dlogits, cudaStream_t s);
@@ -119,15 +142,20 @@ int64_t permute_scratch_bytes(const moe_config& c); // scratch the dispatch need
 
 // Grouped GEMMs (tcgen05). Return cudaErrorInvalidValue when a tensor map
 // cannot be encoded for the given pointers.
+// row_w (the routing weight inside the expert, optional): h = w_row silu(G) U.
 cudaError_t launch_ffn_fc1(const moe_config& c, const void* x_perm, const int32_t* counts,
                            const int32_t* offsets, const void* W13, void* GU, void* h,
-                           int32_t* status, cudaStream_t s);
+                           int32_t* status, cudaStream_t s, const float* row_w = nullptr);
 cudaError_t launch_ffn_fc2(const moe_config& c, const void* h, const int32_t* counts,
                            const int32_t* offsets, const void* W2, void* y_perm,
                            int32_t* status, cudaStream_t s);
+// row_w, dw_part (optional): the weight inside the expert -- dh = w_row dh_s,
+// and dw_part[r * dw_tiles(c) + n-tile] = the row's <dh_s, h> over that tile.
 cudaError_t launch_ffn_fc2_dgrad(const moe_config& c, const void* dO_perm, const int32_t* counts,
                                  const int32_t* offsets, const void* W2, const void* GU,
-                                 void* dGU, int32_t* status, cudaStream_t s);
+                                 void* dGU, int32_t* status, cudaStream_t s,
+                                 const float* row_w = nullptr, float* dw_part = nullptr);
+int dw_tiles(const moe_config& c);
 cudaError_t launch_ffn_fc1_dgrad(const moe_config& c, const void* dGU, const int32_t* counts,
                                  const int32_t* offsets, const void* W13, const int32_t* token_of,
                                  const float* dlogits, const float* W_r, void* dX_perm,

@@ -98,11 +98,30 @@ static int64_t fp8_region(const moe_config& c, Fp8Scratch* f, uint8_t* p) {
   return off;
 }
 
-int64_t scratch_bytes(const moe_config& c) {
+// The region of the layer with the routing weight inside the expert: the
+// weight of every permuted row, then the FC2 data gradient's partial dot
+// products per row and n-tile.
+static int64_t reorder_offset(const moe_config& c) {
   int64_t b = base_scratch_bytes(c);
   if (c.dtype == MOE_DTYPE_FP8_E4M3_BLOCK) b += fp8_region(c, nullptr, nullptr);
   return b;
 }
+
+static int64_t reorder_bytes(const moe_config& c) {
+  if (!c.weights_in_expert) return 0;
+  const int64_t R = rows_max(c);
+  return align256(R * 4) + align256(R * dw_tiles(c) * 4);
+}
+
+ReorderScratch reorder_scratch(const moe_config& c, void* scratch) {
+  uint8_t* p = static_cast<uint8_t*>(scratch) + reorder_offset(c);
+  ReorderScratch r;
+  r.row_w = reinterpret_cast<float*>(p);
+  r.dw_part = reinterpret_cast<float*>(p + align256(rows_max(c) * 4));
+  return r;
+}
+
+int64_t scratch_bytes(const moe_config& c) { return reorder_offset(c) + reorder_bytes(c); }
 
 Fp8Scratch fp8_scratch(const moe_config& c, void* scratch) {
   Fp8Scratch f;
@@ -130,6 +149,8 @@ moe_status check_config(const moe_config* c) {
     return MOE_ERR_INVALID_ARG;
   if (c->dtype == MOE_DTYPE_FP8_E4M3_BLOCK && (c->n_shared != 0 || c->H % 256 || c->F % 256))
     return MOE_ERR_UNSUPPORTED;
+  if (c->weights_in_expert != 0 && c->weights_in_expert != 1) return MOE_ERR_INVALID_ARG;
+  if (c->weights_in_expert && c->dtype != MOE_DTYPE_BF16) return MOE_ERR_UNSUPPORTED;
   if ((int64_t)c->T * c->k >= (1LL << 31) || rows_max(*c) >= (1LL << 31))
     return MOE_ERR_INVALID_ARG;
   if ((int64_t)c->E * 2 * c->F >= (1LL << 31) || (int64_t)(c->E + c->n_shared) * c->H >= (1LL << 31))
@@ -259,9 +280,12 @@ moe_status moe_permute(const moe_config* cfg, const void* x, const int32_t* idx,
   MOE_REQUIRE(tok16(cfg, x) && tok4(cfg, idx) && al4(counts) && al4(offsets) && tok4(cfg, row_of));
   MOE_REQUIRE(al4(token_of) && al4(sel_offsets) && tok4(cfg, sel_tokens) && al16(x_perm));
   MOE_REQUIRE(al16(scratch));
+  Fp8Scratch q;
+  const bool fp8 = cfg->dtype == MOE_DTYPE_FP8_E4M3_BLOCK;
+  if (fp8) q = fp8_scratch(*cfg, scratch);
   MOE_CUDA(launch_permute(*cfg, x, idx, counts, offsets, row_of, token_of, sel_offsets,
                           sel_tokens, x_perm, static_cast<uint8_t*>(scratch),
-                          (cudaStream_t)stream));
+                          (cudaStream_t)stream, fp8 ? &q : nullptr));
   return MOE_OK;
 }
 
@@ -287,11 +311,11 @@ moe_status moe_grouped_ffn_fwd(const moe_config* cfg, const void* x_perm, const 
   cudaStream_t s = (cudaStream_t)stream;
   int32_t* st = status_word(scratch);
   if (cfg->dtype == MOE_DTYPE_FP8_E4M3_BLOCK) {
-    // the E4M3 weights are the ones moe_quantize_weights left in scratch
+    // the E4M3 weights are the ones moe_quantize_weights left in scratch, the
+    // E4M3 x_perm the one moe_permute wrote there with the bf16 rows
     const Fp8Scratch q = fp8_scratch(*cfg, scratch);
     const int G = cfg->E + cfg->n_shared;
     const int64_t R = rows_max(*cfg);
-    MOE_CUDA(launch_quant_rows8(x_perm, q.xq, q.xsf, offsets, counts, G, R, cfg->H, s));
     MOE_CUDA(launch_ffn_fc1_fp8(*cfg, q.xq, q.xsf, counts, offsets, q.W13q, q.W13sf, GU, h, st, s));
     MOE_CUDA(launch_quant_rows8(h, q.hq, q.hsf, offsets, counts, G, R, cfg->F, s));
     MOE_CUDA(launch_ffn_fc2_fp8(*cfg, q.hq, q.hsf, counts, offsets, q.W2q, q.W2sf, y_perm, st, s));
@@ -305,19 +329,28 @@ moe_status moe_grouped_ffn_fwd(const moe_config* cfg, const void* x_perm, const 
 moe_status moe_unpermute(const moe_config* cfg, const void* y_perm, const int32_t* row_of,
                          const float* w, const int32_t* offsets, void* out, void* stream) {
   MOE_TRY(check_config(cfg));
-  MOE_REQUIRE(al16(y_perm) && tok4(cfg, row_of) && tok4(cfg, w) && al4(offsets) && tok16(cfg, out));
+  MOE_REQUIRE(al16(y_perm) && tok4(cfg, row_of) && al4(offsets) && tok16(cfg, out));
+  MOE_REQUIRE(w == nullptr || al4(w));
   MOE_CUDA(launch_unpermute(*cfg, y_perm, row_of, w, offsets, out, (cudaStream_t)stream));
   return MOE_OK;
 }
 
 moe_status moe_unpermute_bwd(const moe_config* cfg, const void* dY, const void* y_perm,
                              const int32_t* row_of, const float* w, const int32_t* counts,
-                             const int32_t* offsets, void* dO_perm, float* dw, void* stream) {
+                             const int32_t* offsets, void* dO_perm, float* dw, void* scratch,
+                             void* stream) {
   MOE_TRY(check_config(cfg));
   MOE_REQUIRE(tok16(cfg, dY) && al16(y_perm) && tok4(cfg, row_of) && tok4(cfg, w) && al4(counts));
-  MOE_REQUIRE(al4(offsets) && al16(dO_perm) && tok4(cfg, dw));
+  MOE_REQUIRE(al4(offsets) && al16(dO_perm) && tok4(cfg, dw) && al16(scratch));
+  uint8_t* dOq = nullptr;
+  uint8_t* dOsf = nullptr;
+  if (cfg->dtype == MOE_DTYPE_FP8_E4M3_BLOCK) {
+    const Fp8Scratch q = fp8_scratch(*cfg, scratch);
+    dOq = q.dOq;
+    dOsf = q.dOsf;
+  }
   MOE_CUDA(launch_unpermute_bwd(*cfg, dY, y_perm, row_of, w, counts, offsets, dO_perm, dw,
-                                (cudaStream_t)stream));
+                                (cudaStream_t)stream, dOq, dOsf));
   return MOE_OK;
 }
 
@@ -336,7 +369,7 @@ moe_status moe_grouped_ffn_dgrad(const moe_config* cfg, const void* dO_perm, con
     const Fp8Scratch q = fp8_scratch(*cfg, scratch);
     const int G = cfg->E + cfg->n_shared;
     const int64_t R = rows_max(*cfg);
-    MOE_CUDA(launch_quant_rows8(dO_perm, q.dOq, q.dOsf, offsets, counts, G, R, cfg->H, s));
+    // dO_perm's E4M3 form is the one moe_unpermute_bwd wrote into scratch
     MOE_CUDA(launch_ffn_fc2_dgrad_fp8(*cfg, q.dOq, q.dOsf, counts, offsets, q.W2q, q.W2sft, GU,
                                       dGU, st, s));
     MOE_CUDA(launch_quant_rows8(dGU, q.dGq, q.dGsf, offsets, counts, G, R, 2 * cfg->F, s));
@@ -391,6 +424,64 @@ moe_status moe_grouped_ffn_bwd(const moe_config* cfg, const void* dO_perm, const
   return MOE_OK;
 }
 
+moe_status moe_grouped_ffn_fwd_reordered(const moe_config* cfg, const void* x_perm,
+                                         const int32_t* counts, const int32_t* offsets,
+                                         const int32_t* token_of, const int32_t* row_of,
+                                         const float* w, const void* W13, const void* W2,
+                                         void* GU, void* h, void* y_perm, void* scratch,
+                                         void* stream) {
+  MOE_TRY(check_config(cfg));
+  if (!cfg->weights_in_expert) return MOE_ERR_INVALID_ARG;
+  MOE_REQUIRE(al16(x_perm) && al4(counts) && al4(offsets) && al4(token_of) && tok4(cfg, row_of));
+  MOE_REQUIRE(tok4(cfg, w) && al16(W13) && al16(W2) && al16(GU) && al16(h) && al16(y_perm));
+  MOE_REQUIRE(al16(scratch));
+  cudaStream_t s = (cudaStream_t)stream;
+  int32_t* st = status_word(scratch);
+  const ReorderScratch rs = reorder_scratch(*cfg, scratch);
+  MOE_CUDA(launch_row_weights(*cfg, token_of, row_of, w, offsets, rs.row_w, s));
+  MOE_CUDA(launch_ffn_fc1(*cfg, x_perm, counts, offsets, W13, GU, h, st, s, rs.row_w));
+  MOE_CUDA(launch_ffn_fc2(*cfg, h, counts, offsets, W2, y_perm, st, s));
+  return MOE_OK;
+}
+
+moe_status moe_unpermute_bwd_reordered(const moe_config* cfg, const void* dY,
+                                       const int32_t* row_of, const int32_t* counts,
+                                       const int32_t* offsets, void* dO_perm, void* stream) {
+  MOE_TRY(check_config(cfg));
+  MOE_REQUIRE(tok16(cfg, dY) && tok4(cfg, row_of) && al4(counts) && al4(offsets) && al16(dO_perm));
+  MOE_CUDA(launch_unpermute_bwd_copy(*cfg, dY, row_of, counts, offsets, dO_perm,
+                                     (cudaStream_t)stream));
+  return MOE_OK;
+}
+
+moe_status moe_grouped_ffn_dgrad_reordered(const moe_config* cfg, const void* dO_perm,
+                                           const void* GU, const int32_t* counts,
+                                           const int32_t* offsets, const int32_t* token_of,
+                                           const int32_t* row_of, const float* logits,
+                                           const int32_t* idx, const float* w, const float* W_r,
+                                           const void* W13, const void* W2, void* dGU,
+                                           void* dX_perm, float* dw, float* dlogits,
+                                           void* scratch, void* stream) {
+  MOE_TRY(check_config(cfg));
+  if (!cfg->weights_in_expert) return MOE_ERR_INVALID_ARG;
+  MOE_REQUIRE(al16(dO_perm) && al16(GU) && al4(counts) && al4(offsets) && al4(token_of));
+  MOE_REQUIRE(tok4(cfg, row_of) && tok4(cfg, logits) && tok4(cfg, idx) && tok4(cfg, w));
+  MOE_REQUIRE(al16(W_r) && al16(W13) && al16(W2) && al16(dGU) && al16(dX_perm));
+  MOE_REQUIRE(tok4(cfg, dw) && tok4(cfg, dlogits) && al16(scratch));
+  cudaStream_t s = (cudaStream_t)stream;
+  int32_t* st = status_word(scratch);
+  const ReorderScratch rs = reorder_scratch(*cfg, scratch);
+  MOE_CUDA(launch_ffn_fc2_dgrad(*cfg, dO_perm, counts, offsets, W2, GU, dGU, st, s, rs.row_w,
+                                rs.dw_part));
+  if (cfg->T > 0) {
+    MOE_CUDA(launch_dw_reduce(*cfg, rs.dw_part, row_of, dw, s));
+    MOE_CUDA(launch_route_bwd(*cfg, logits, idx, w, dw, dlogits, s));
+  }
+  MOE_CUDA(launch_ffn_fc1_dgrad(*cfg, dGU, counts, offsets, W13, token_of, dlogits, W_r, dX_perm,
+                                st, s));
+  return MOE_OK;
+}
+
 moe_status moe_route_bwd(const moe_config* cfg, const float* logits, const int32_t* idx,
                          const float* w, const float* dw, float* dlogits, void* stream) {
   MOE_TRY(check_config(cfg));
@@ -430,6 +521,12 @@ moe_status moe_layer_fwd(const moe_config* cfg, const moe_params* P, const void*
   MOE_TRY(moe_route(cfg, x, P->W_r, P->bias, st->logits, st->idx, st->w, scratch, stream));
   MOE_TRY(moe_permute(cfg, x, st->idx, st->counts, st->offsets, st->row_of, st->token_of,
                       st->sel_offsets, st->sel_tokens, st->x_perm, scratch, stream));
+  if (cfg->weights_in_expert) {
+    MOE_TRY(moe_grouped_ffn_fwd_reordered(cfg, st->x_perm, st->counts, st->offsets, st->token_of,
+                                          st->row_of, st->w, P->W13, P->W2, st->GU, st->h,
+                                          st->y_perm, scratch, stream));
+    return moe_unpermute(cfg, st->y_perm, st->row_of, nullptr, st->offsets, out, stream);
+  }
   MOE_TRY(moe_grouped_ffn_fwd(cfg, st->x_perm, st->counts, st->offsets, P->W13, P->W2, st->GU,
                               st->h, st->y_perm, scratch, stream));
   MOE_TRY(moe_unpermute(cfg, st->y_perm, st->row_of, st->w, st->offsets, out, stream));
@@ -442,8 +539,22 @@ moe_status moe_layer_bwd(const moe_config* cfg, const moe_params* P, const void*
                          void* stream) {
   MOE_TRY(check_config(cfg));
   MOE_REQUIRE(P && st && bs);
+  if (cfg->weights_in_expert) {
+    MOE_TRY(moe_unpermute_bwd_reordered(cfg, dY, st->row_of, st->counts, st->offsets,
+                                        bs->dO_perm, stream));
+    MOE_TRY(moe_grouped_ffn_dgrad_reordered(cfg, bs->dO_perm, st->GU, st->counts, st->offsets,
+                                            st->token_of, st->row_of, st->logits, st->idx, st->w,
+                                            P->W_r, P->W13, P->W2, bs->dGU, bs->dX_perm, bs->dw,
+                                            bs->dlogits, scratch, stream));
+    MOE_TRY(moe_grouped_ffn_wgrad(cfg, bs->dO_perm, st->x_perm, st->h, bs->dGU, st->counts,
+                                  st->offsets, dW13, dW2, scratch, stream));
+    MOE_TRY(moe_permute_bwd(cfg, bs->dX_perm, st->row_of, st->offsets, st->idx, bs->dlogits,
+                            P->W_r, dx, stream));
+    return moe_router_wgrad(cfg, x, st->sel_offsets, st->sel_tokens, bs->dlogits, dW_r, scratch,
+                            stream);
+  }
   MOE_TRY(moe_unpermute_bwd(cfg, dY, st->y_perm, st->row_of, st->w, st->counts, st->offsets,
-                            bs->dO_perm, bs->dw, stream));
+                            bs->dO_perm, bs->dw, scratch, stream));
   MOE_TRY(moe_route_bwd(cfg, st->logits, st->idx, st->w, bs->dw, bs->dlogits, stream));
   MOE_TRY(moe_grouped_ffn_bwd(cfg, bs->dO_perm, st->x_perm, st->GU, st->h, st->counts,
                               st->offsets, st->token_of, bs->dlogits, P->W_r, P->W13, P->W2,

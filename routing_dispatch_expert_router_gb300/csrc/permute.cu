@@ -17,6 +17,7 @@
 //   scatter one warp per token: reads the row once, writes it to each of its
 //           rows with 16-byte stores; padding rows are zero-filled.
 #include "common.cuh"
+#include "fp8_layout.cuh"
 #include "internal.h"
 
 namespace moe {
@@ -90,7 +91,9 @@ permute_rank_kernel(const int32_t* __restrict__ idx, const int32_t* __restrict__
     }
     kept[g] = kp;
     seg[g] = sl;
-    pad[g] = sl - kp;
+    // padding rows that a GEMM reads: the rest of the segment's last 128-row
+    // block (rows past it -- capacity segments, row_align > 128 -- are never read)
+    pad[g] = min(sl, (kp + 127) / 128 * 128) - kp;
   }
   __syncthreads();
   const int R = block_exclusive_scan(seg, G, tmp);
@@ -154,12 +157,20 @@ __device__ __forceinline__ int find_group(const int* prefix, int G, int p) {
   return lo;
 }
 
-// Virtual rows v < T copy token v to its rows; v >= T zero one padding row.
+// Virtual rows v < T copy token v to its rows; v >= T zero one padding row
+// (the padding rows inside each segment's last 128-row block, the ones a GEMM
+// reads).
+// With xq (the FP8 configuration) every row is also written in its 1-byte form
+// -- E4M3 codes of its 1 x 128 slices and their UE8M0 scales in the atoms of
+// xsf (fp8_layout.cuh) -- for the FC1 GEMM: each slice is quantised once per
+// token and written to each of the token's rows; padding rows get zero codes
+// and scale 1.
 __global__ void __launch_bounds__(256)
 permute_scatter_kernel(const __nv_bfloat16* __restrict__ x, const int32_t* __restrict__ row_of,
                        const int32_t* __restrict__ counts, const int32_t* __restrict__ offsets,
                        const int32_t* __restrict__ pad_prefix, __nv_bfloat16* __restrict__ x_perm,
-                       int T, int H, int k, int E, int S) {
+                       int T, int H, int k, int E, int S, uint8_t* __restrict__ xq,
+                       uint8_t* __restrict__ xsf) {
   __shared__ int s_pp[kMaxGroups + 1];
   __shared__ int s_off[kMaxGroups + 1];
   __shared__ int s_cnt[kMaxGroups];
@@ -173,6 +184,8 @@ permute_scatter_kernel(const __nv_bfloat16* __restrict__ x, const int32_t* __res
   const int P = s_pp[G];
   const int lane = threadIdx.x & 31;
   const int nvec = H >> 3;
+  const int64_t kg = f8::atoms_k(H);
+  const unsigned half = (lane & 16) ? 0xffff0000u : 0x0000ffffu;
   const int warps = gridDim.x * (blockDim.x >> 5);
   for (int v = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); v < T + P; v += warps) {
     if (v < T) {
@@ -189,6 +202,23 @@ permute_scatter_kernel(const __nv_bfloat16* __restrict__ x, const int32_t* __res
 #pragma unroll
         for (int u = 0; u < 4; ++u)
           if (c0 + 32 * u < nvec) q[u] = ldg_nc_v4(src + (size_t)(c0 + 32 * u) * 8);
+        // 1-byte form: a half-warp holds one 128-element slice per u (nvec is a
+        // multiple of 16, so a half-warp is wholly in range or out)
+        uint2 qb[4];
+        uint32_t code[4];
+        if (xq) {
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            if (c0 + 32 * u >= nvec) continue;
+            float f[8];
+            unpack8(q[u], f);
+            float m = amax8(f);
+#pragma unroll
+            for (int o = 8; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(half, m, o));
+            code[u] = ue8m0_code(m);
+            qb[u] = e4m3x8(f, ue8m0_inv(code[u]));
+          }
+        }
 #pragma unroll
         for (int j = 0; j < kMaxK + 4; ++j) {
           if (j >= nr || rows[j] < 0) continue;
@@ -196,6 +226,17 @@ permute_scatter_kernel(const __nv_bfloat16* __restrict__ x, const int32_t* __res
 #pragma unroll
           for (int u = 0; u < 4; ++u)
             if (c0 + 32 * u < nvec) stg_v4(dst + (size_t)(c0 + 32 * u) * 8, q[u]);
+          if (xq) {
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              const int c = c0 + 32 * u;
+              if (c >= nvec) continue;
+              *reinterpret_cast<uint2*>(xq + (size_t)rows[j] * H + (size_t)c * 8) = qb[u];
+              if ((lane & 15) == 0)
+                xsf[f8::atom_offset(rows[j] >> 7, c >> 4, kg) + f8::atom_byte(rows[j], c >> 4)] =
+                    (uint8_t)code[u];
+            }
+          }
         }
       }
     } else {
@@ -204,7 +245,14 @@ permute_scatter_kernel(const __nv_bfloat16* __restrict__ x, const int32_t* __res
       const int r = s_off[g] + s_cnt[g] + (p - s_pp[g]);
       __nv_bfloat16* dst = x_perm + (size_t)r * H;
       const uint4 z = make_uint4(0u, 0u, 0u, 0u);
-      for (int c0 = lane; c0 < nvec; c0 += 32) stg_v4(dst + (size_t)c0 * 8, z);
+      for (int c0 = lane; c0 < nvec; c0 += 32) {
+        stg_v4(dst + (size_t)c0 * 8, z);
+        if (xq) {
+          *reinterpret_cast<uint2*>(xq + (size_t)r * H + (size_t)c0 * 8) = make_uint2(0u, 0u);
+          if ((c0 & 15) == 0)
+            xsf[f8::atom_offset(r >> 7, c0 >> 4, kg) + f8::atom_byte(r, c0 >> 4)] = 127u;
+        }
+      }
     }
   }
 }
@@ -212,7 +260,7 @@ permute_scatter_kernel(const __nv_bfloat16* __restrict__ x, const int32_t* __res
 cudaError_t launch_permute(const moe_config& c, const void* x, const int32_t* idx,
                            int32_t* counts, int32_t* offsets, int32_t* row_of, int32_t* token_of,
                            int32_t* sel_offsets, int32_t* sel_tokens, void* x_perm,
-                           uint8_t* scratch, cudaStream_t s) {
+                           uint8_t* scratch, cudaStream_t s, const Fp8Scratch* fp8) {
   int32_t* status = reinterpret_cast<int32_t*>(scratch + kScratchStatus);
   int32_t* pad_prefix = reinterpret_cast<int32_t*>(scratch + kScratchPadPrefix);
   int32_t* hist = reinterpret_cast<int32_t*>(scratch + kScratchHist);
@@ -228,9 +276,15 @@ cudaError_t launch_permute(const moe_config& c, const void* x, const int32_t* id
                                          token_of, sel_offsets, sel_tokens, pad_prefix);
   err = cudaGetLastError();
   if (err != cudaSuccess) return err;
+  uint8_t* xq = nullptr;
+  uint8_t* xsf = nullptr;
+  if (c.dtype == MOE_DTYPE_FP8_E4M3_BLOCK && fp8) {
+    xq = fp8->xq;
+    xsf = fp8->xsf;
+  }
   permute_scatter_kernel<<<num_sms() * 8, 256, 0, s>>>(
       static_cast<const __nv_bfloat16*>(x), row_of, counts, offsets, pad_prefix,
-      static_cast<__nv_bfloat16*>(x_perm), c.T, c.H, c.k, c.E, c.n_shared);
+      static_cast<__nv_bfloat16*>(x_perm), c.T, c.H, c.k, c.E, c.n_shared, xq, xsf);
   return cudaGetLastError();
 }
 
@@ -275,6 +329,9 @@ extern "C" moe_status moe_permute_noalloc(const moe_config* cfg, const void* x,
   using namespace moe;
   const moe_status st = check_config(cfg);
   if (st != MOE_OK) return st;
+  // an FP8 dispatch also writes x_perm's E4M3 form into the caller's scratch,
+  // which this entry point does not take
+  if (cfg->dtype != MOE_DTYPE_BF16) return MOE_ERR_UNSUPPORTED;
   auto a16 = [](const void* p) { return p && ((uintptr_t)p & 15u) == 0; };
   auto a4 = [](const void* p) { return p && ((uintptr_t)p & 3u) == 0; };
   const bool empty = cfg->T == 0;
@@ -291,6 +348,6 @@ extern "C" moe_status moe_permute_noalloc(const moe_config* cfg, const void* x,
   if (cudaMemsetAsync(sc + kScratchStatus, 0, sizeof(int32_t), s) != cudaSuccess)
     return MOE_ERR_CUDA;
   const cudaError_t e = launch_permute(*cfg, x, idx, counts, offsets, row_of, token_of,
-                                       sel_offsets, sel_tokens, x_perm, sc, s);
+                                       sel_offsets, sel_tokens, x_perm, sc, s, nullptr);
   return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }

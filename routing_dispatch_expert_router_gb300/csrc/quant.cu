@@ -53,38 +53,6 @@ __device__ __forceinline__ float q1(float a, float inv_s, float s) {
   return qa;
 }
 
-// The scale used for the 1-byte form and its UE8M0 code: the block scale,
-// raised to 2^-127 (the smallest UE8M0 value) for blocks whose amax is below
-// 448 * 2^-128 -- there the scaled values keep fewer bits than the fp64
-// reference's, a case no bf16 activation or weight of normal magnitude meets.
-__device__ __forceinline__ float e4m3_scale_code(float amax, uint32_t& code) {
-  float s = e4m3_scale(amax);
-  if (s < 0x1p-127f) s = 0x1p-127f;
-  const uint32_t bits = __float_as_uint(s);
-  code = (bits >> 23) & 0xFFu;     // biased exponent = UE8M0 code (2^-127: subnormal, code 0)
-  return s;
-}
-
-// E4M3 codes of eight values divided by a power-of-two scale (exact): bytes in
-// element order.
-__device__ __forceinline__ uint2 e4m3x8(const float (&f)[8], float inv_s) {
-  uint32_t w[4];
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    uint16_t h;
-    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;"
-        : "=h"(h) : "f"(f[2 * i + 1] * inv_s), "f"(f[2 * i] * inv_s));
-    w[i] = h;
-  }
-  return make_uint2(w[0] | (w[1] << 16), w[2] | (w[3] << 16));
-}
-
-__device__ __forceinline__ float amax8(const float (&f)[8]) {
-  float m = 0.f;
-#pragma unroll
-  for (int i = 0; i < 8; ++i) m = fmaxf(m, fabsf(f[i]));
-  return m;
-}
 
 // Whether 128-row block rb of the permuted buffer holds any row a GEMM reads:
 // group g's segment starts at offsets[g], and the GEMMs read its first
@@ -200,9 +168,8 @@ quant_tiles8_kernel(const __nv_bfloat16* __restrict__ W, uint8_t* __restrict__ W
     float amax = red[0];
 #pragma unroll
     for (int i = 1; i < 8; ++i) amax = fmaxf(amax, red[i]);
-    uint32_t code;
-    const float s = e4m3_scale_code(amax, code);
-    const float inv = 1.f / s;                            // exact: s is a power of two
+    const uint32_t code = ue8m0_code(amax);
+    const float inv = ue8m0_inv(code);
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
       const int v = threadIdx.x + 256 * i;
@@ -220,33 +187,40 @@ quant_tiles8_kernel(const __nv_bfloat16* __restrict__ W, uint8_t* __restrict__ W
 
 // 1 x 128 slices along the rows of the live 128-row blocks of [0, offsets[G])
 // -> E4M3 bytes plus UE8M0 scale atoms (row block rb, K block kb). One block
-// of 256 threads per 128-row block, 16 lanes per slice.
+// of 256 threads per 128-row block; each half-warp owns 8 of the rows and walks
+// them two 128-element slices at a time (16 lanes x 16 bytes per slice, both
+// loads in flight together).
 __global__ void __launch_bounds__(256)
 quant_rows8_kernel(const __nv_bfloat16* __restrict__ X, uint8_t* __restrict__ Xq,
                    uint8_t* __restrict__ sf, const int32_t* __restrict__ offsets,
                    const int32_t* __restrict__ counts, int G, int cols) {
   const long long rblocks = offsets[G] / 128;
-  const int nvec = cols >> 3;                             // a multiple of 16
-  const int per_block = 128 * nvec;
+  const int KB = cols >> 7;
   const int64_t kg = f8::atoms_k(cols);
+  const int hw = threadIdx.x >> 4, l16 = threadIdx.x & 15;
+  const unsigned half = (threadIdx.x & 16) ? 0xffff0000u : 0x0000ffffu;
   for (long long rb = blockIdx.x; rb < rblocks; rb += gridDim.x) {
     if (!live_block(offsets, counts, G, rb)) continue;
-    const __nv_bfloat16* src = X + (size_t)rb * 128 * cols;
-    uint8_t* dst = Xq + (size_t)rb * 128 * cols;
-    for (int v = threadIdx.x; v < per_block; v += 256) {
-      float f[8];
-      unpack8(ldg_nc_v4(src + (size_t)v * 8), f);
-      float m = amax8(f);
-      const unsigned half = (threadIdx.x & 16) ? 0xffff0000u : 0x0000ffffu;
+    for (int r = hw; r < 128; r += 16) {
+      const size_t row = (size_t)rb * 128 + r;
+      const __nv_bfloat16* src = X + row * cols + l16 * 8;
+      uint8_t* dst = Xq + row * cols + l16 * 8;
+      for (int kb = 0; kb < KB; kb += 2) {
+        const bool two = kb + 1 < KB;
+        float f[2][8];
+        unpack8(ldg_nc_v4(src + (size_t)kb * 128), f[0]);
+        if (two) unpack8(ldg_nc_v4(src + (size_t)(kb + 1) * 128), f[1]);
 #pragma unroll
-      for (int o = 8; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(half, m, o));
-      uint32_t code;
-      const float s = e4m3_scale_code(m, code);
-      *reinterpret_cast<uint2*>(dst + (size_t)v * 8) = e4m3x8(f, 1.f / s);
-      const int cv = v % nvec;
-      if ((cv & 15) == 0) {
-        const int r = v / nvec, kb = cv >> 4;
-        sf[f8::atom_offset(rb, kb, kg) + f8::atom_byte(r, kb)] = (uint8_t)code;
+        for (int u = 0; u < 2; ++u) {
+          if (u == 1 && !two) break;
+          float m = amax8(f[u]);
+#pragma unroll
+          for (int o = 8; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(half, m, o));
+          const uint32_t code = ue8m0_code(m);
+          *reinterpret_cast<uint2*>(dst + (size_t)(kb + u) * 128) = e4m3x8(f[u], ue8m0_inv(code));
+          if (l16 == 0)
+            sf[f8::atom_offset(rb, kb + u, kg) + f8::atom_byte(r, kb + u)] = (uint8_t)code;
+        }
       }
     }
   }

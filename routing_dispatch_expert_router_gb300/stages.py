@@ -71,7 +71,7 @@ def run(name: str, reps: int, flush: bool, peak: float, fl: torch.Tensor) -> Non
                                          sel_tok, x_perm, sc),
         "unpermute": lambda: B.moe_unpermute(cfg, y_perm, row_of, w, offsets, out),
         "unpermute_bwd": lambda: B.moe_unpermute_bwd(cfg, dY, y_perm, row_of, w, counts, offsets,
-                                                     dO, dw),
+                                                     dO, dw, sc),
         "route_bwd": lambda: B.moe_route_bwd(cfg, logits, idx, w, dw, dl),
         "permute_bwd": lambda: B.moe_permute_bwd(cfg, dX_perm, row_of, offsets, idx, dl, Wr, dx),
         "router_wgrad": lambda: B.moe_router_wgrad(cfg, x, sel_off, sel_tok, dl, dWr, sc),

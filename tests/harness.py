@@ -56,6 +56,12 @@ def assert_equal(name, got, ref):
 # tensor (name, elements beyond the plain rule, elements, largest ratio of
 # error to the plain bound). tests/conftest.py prints them after the run.
 PLAIN_RECORDS: list = []
+# The bf16 end-to-end checks that need the widened bound (sums of independently
+# rounded bf16 summands: dx, dW13, dW2) are also capped at this many times the
+# plain bound; the largest ratio observed over the GPU suite is 1.8 (dW13 of
+# the CTA-pair case; 1.7 for Mixtral-sized dx), so the cap leaves about a
+# factor of two.
+PLAIN_CAP = 4.0
 
 
 def plain_rule(name, got, ref, fp8: bool = False) -> float:
@@ -70,6 +76,17 @@ def plain_rule(name, got, ref, fp8: bool = False) -> float:
     worst = float(ratio.max()) if ratio.size else 0.0
     PLAIN_RECORDS.append((name, int((ratio > 1).sum()), int(ratio.size), worst))
     return worst
+
+
+def read_rows(m) -> np.ndarray:
+    """Rows of the permuted buffers that the grouped GEMMs read (and the
+    dispatch writes): each segment's kept rows plus the rest of its last
+    128-row block."""
+    R, off, cnt = m["R"], m["offsets"], m["counts"]
+    live = np.zeros(R, dtype=bool)
+    for g in range(len(cnt)):
+        live[off[g]: min(off[g + 1], off[g] + -(-int(cnt[g]) // 128) * 128)] = True
+    return live
 
 
 def _poison(t: torch.Tensor):
@@ -171,7 +188,9 @@ def check_steps(shape, inp: dict, g: dict, backward: bool = True, replay_idx=Non
     assert_equal("token_of", i64(g["token_of"])[:R], m["token_of"])
     assert_equal("sel_offsets", i64(g["sel_offsets"]), m["sel_offsets"])
     assert_equal("sel_tokens", i64(g["sel_tokens"])[:T * k], m["sel_tokens"])
+    live = read_rows(m)
     xp = f64(g["x_perm"])[:R]
+    xp[~live] = 0.0                     # rows no GEMM reads are not written
     assert_equal("x_perm", xp, O.permute(x, m))
     # a5/a6 per group on the GPU's rows
     off, cnt = m["offsets"], m["counts"]
@@ -211,7 +230,7 @@ def check_steps(shape, inp: dict, g: dict, backward: bool = True, replay_idx=Non
         assert_close(f"dw[slot {j}]", dw[:, j], ref_dw, atol=1e-3, rtol=1e-3)
     for s in range(S):
         assert_equal("dO[shared]", dO[off[E + s]: off[E + s] + T], dY)
-    pad = m["token_of"] < 0
+    pad = (m["token_of"] < 0) & live
     assert_equal("dO padding", dO[:R][pad], np.zeros((int(pad.sum()), H)))
     assert_equal("x_perm padding", xp[pad], np.zeros((int(pad.sum()), H)))
     # a14a: dlogits on the GPU's dw
@@ -306,11 +325,11 @@ def check_end_to_end(shape, inp: dict, g: dict, backward: bool = True):
         np.abs(Wr)[fwd["idx"]]
     mag = np.abs(bwd["dx"]) + np.abs(bwd["dX"]).sum(axis=1) + np.abs(bwd["dX_s"]).sum(axis=0) + \
         router.sum(axis=1)
-    plain_rule(f"{shape.name} dx", f64(g["dx"]), bwd["dx"])
+    assert plain_rule(f"{shape.name} dx", f64(g["dx"]), bwd["dx"]) <= PLAIN_CAP
     assert_close("dx (e2e)", f64(g["dx"]), bwd["dx"], scale=mag)
     s13, s2 = wgrad_summand_scale(shape, x, dY, fwd, bwd)
-    plain_rule(f"{shape.name} dW13", f64(g["dW13"]), bwd["dW13"])
-    plain_rule(f"{shape.name} dW2", f64(g["dW2"]), bwd["dW2"])
+    assert plain_rule(f"{shape.name} dW13", f64(g["dW13"]), bwd["dW13"]) <= PLAIN_CAP
+    assert plain_rule(f"{shape.name} dW2", f64(g["dW2"]), bwd["dW2"]) <= PLAIN_CAP
     assert_close("dW13 (e2e)", f64(g["dW13"]), bwd["dW13"], scale=np.abs(bwd["dW13"]) + s13)
     assert_close("dW2 (e2e)", f64(g["dW2"]), bwd["dW2"], scale=np.abs(bwd["dW2"]) + s2)
     plain_rule(f"{shape.name} dW_r", f64(g["dW_r"]), bwd["dW_r"])

@@ -132,3 +132,30 @@ def test_status_strings():
     for code in range(7):
         assert B.status_string(code)
     assert "unknown" in B.status_string(99)
+
+
+def test_noalloc_dispatch_refuses_the_fp8_configuration_before_launch():
+    """In the FP8 configuration the dispatch also writes x_perm's E4M3 form
+    into the caller's scratch, which the no-scratch entry point cannot take."""
+    cfg = B.config(DSV3_FP8)
+    vp = ctypes.c_void_p
+    ok = vp(4096)
+    rc = B.lib().moe_permute_noalloc(ctypes.byref(cfg), ok, ok, ok, ok, ok, ok, ok, ok, ok,
+                                     vp(None))
+    assert rc == 2                 # MOE_ERR_UNSUPPORTED
+
+
+def test_reordered_layer_configuration_checks():
+    """weights_in_expert: 0 or 1, bf16 mode only; its region of scratch holds
+    one fp32 weight per permuted row and one fp32 partial per row and FC2
+    data-gradient tile."""
+    base = B.moe_query_sizes(MIXTRAL).scratch_bytes
+    s = B.moe_query_sizes(MIXTRAL.with_(weights_in_expert=1))
+    R = s.rows_max
+    assert s.scratch_bytes - base >= R * 4 + R * (14336 // 256) * 4
+    with pytest.raises(B.MoEError) as e:
+        B.moe_query_sizes(MIXTRAL.with_(weights_in_expert=2))
+    assert e.value.code == 1
+    with pytest.raises(B.MoEError) as e:
+        B.moe_query_sizes(DSV3_FP8.with_(weights_in_expert=1))
+    assert e.value.code == 2

@@ -83,7 +83,7 @@ def test_full_size_layer_matches_oracle_on_samples(shape):
     if shape is QWEN3:
         assert cnt.max() >= 8 * (T * k / E), "the Zipf bias should make hot experts"
     # ---- x_perm: sampled rows and padding rows
-    rows = rng.choice(R, size=512, replace=False)
+    rows = rng.choice(np.nonzero(H_.read_rows(m))[0], size=512, replace=False)
     tok_of = m["token_of"][rows]
     xp_rows = host(g["x_perm"][torch.as_tensor(rows, device="cuda")])
     ref_rows = np.zeros_like(xp_rows)
@@ -212,6 +212,9 @@ def test_full_size_layer_matches_oracle_on_samples(shape):
         else:
             H_.assert_close(f"dx e2e[{t}]", host(g["dx"][int(t)]), ref, scale=mag)
     for name, (got, ref) in e2e.items():
-        H_.plain_rule(f"{shape.name} {name} (4 tokens)", np.stack(got), np.stack(ref), fp8=fp8)
+        worst = H_.plain_rule(f"{shape.name} {name} (4 tokens)", np.stack(got), np.stack(ref),
+                              fp8=fp8)
+        if not fp8:
+            assert worst <= H_.PLAIN_CAP, (name, worst)
     del g, inp
     torch.cuda.empty_cache()

@@ -71,6 +71,7 @@ class MoEShape:
     dtype: int = DT_BF16
     capacity_factor: float = 0.0     # 0 = dropless
     row_align: int = 128             # per-expert segment alignment in rows
+    weights_in_expert: int = 0       # 1: routing weight applied inside the expert (bf16)
     # input recipe
     router_std: float = 0.0          # 0 -> 1/sqrt(H)
     weight_std: float = 0.02
@@ -99,10 +100,13 @@ SHAPES = {s.name: s for s in (TINY, MIXTRAL, DSV3, QWEN3, DSV3_FP8)}
 # Small cases of the same kernels for detailed profiles (a few GB on the device,
 # operands still larger than L2): Mixtral-sized experts, 2 of them with 2048
 # rows each (CTA-pair GEMM tiles, K = 4096); DeepSeek-V3-sized experts, 16 of
-# them with about 256 rows each (single-CTA tiles, short weight-gradient K).
+# them with about 256 rows each (single-CTA tiles, short weight-gradient K);
+# the FP8 layer's experts, 16 of them (the FP8 GEMMs at a few GB).
 PROFILE_SHAPES = {
     "mixtral_2experts": MIXTRAL.with_(name="mixtral_2experts", T=2048, E=2),
     "dsv3_16experts": DSV3.with_(name="dsv3_16experts", T=512, E=16),
+    # the FP8 layer's experts (capacity 640 rows, about 380 kept on average), 16 of them
+    "dsv3_fp8_16experts": DSV3_FP8.with_(name="dsv3_fp8_16experts", T=1024, E=16),
 }
 
 
