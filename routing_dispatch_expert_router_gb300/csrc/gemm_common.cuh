@@ -74,6 +74,11 @@ struct Params {
   const uint8_t* sfb;
   int sfa_kg;
   int sfb_nb, sfb_kg;
+  // and the 1-byte form of the FC1 epilogue's h for FC2 (1 x 128 slices,
+  // atoms [R/128][qsf_kg])
+  uint8_t* qout;
+  uint8_t* qsf;
+  int qsf_kg;
   // Tile order: 1 = n-tiles vary fastest, else m-tiles (m-pairs). Weight gradients
   // whose output is taller than wide take n-fastest: the clusters running at
   // once then share the A slice (the group's rows x 256 output rows) and stream

@@ -45,8 +45,15 @@ constexpr int kF8BBytes = kF8BN * kF8BK;          // 32 KB
 constexpr int kF8Stage = kF8ABytes + kF8BBytes;
 constexpr int kF8SfStage = 3 * f8::kAtomBytes;    // A's atom, then B's two (128 columns each)
 constexpr int kF8EpiWarps = 8;
-constexpr int kF8Smem =
-    kF8Stages * (kF8Stage + kF8SfStage) + kCtrlBytes + kF8EpiWarps * kBoxBytes + 1024;
+// row maxima exchanged between the two epilogue warps of a lane quarter (the
+// fused h quantisation: an h slice of 128 columns spans both warps), double
+// buffered by tile parity: [2][4 quarters][2 warps][32 rows] fp32
+constexpr int kF8XchBytes = 2 * 4 * 2 * 32 * 4;
+constexpr int kF8XbarOff = 4864;                  // their 4 mbarriers in the control block
+constexpr int kF8Smem = kF8Stages * (kF8Stage + kF8SfStage) + kCtrlBytes +
+                        kF8EpiWarps * kBoxBytes + kF8XchBytes + 1024;
+static_assert(kF8XbarOff >= 4608 + 33 * 4 && kF8XbarOff + 32 <= kCtrlBytes,
+              "exchange barriers inside the control block, after the scan scratch");
 constexpr uint32_t kF8TmemCols = 512;
 constexpr uint32_t kF8SfCol = 256;                // first scale-factor column
 constexpr uint32_t kF8SfSlotCols = 16;
@@ -88,6 +95,8 @@ grouped_gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmA,
   uint8_t* ctrl = sbase + (ctrl_u - base);
   const uint32_t epi_u = ctrl_u + kCtrlBytes;
   uint8_t* epi = ctrl + kCtrlBytes;
+  float* xch = reinterpret_cast<float*>(epi + kF8EpiWarps * kBoxBytes);
+  const uint32_t xbar = ctrl_u + kF8XbarOff;              // [4] quarters
   const uint32_t bar_full = ctrl_u;                       // [kF8Stages]
   const uint32_t bar_empty = ctrl_u + 8 * kF8Stages;      // [kF8Stages]
   const uint32_t bar_tfull = ctrl_u + 16 * kF8Stages;
@@ -128,6 +137,7 @@ grouped_gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmA,
     ptx::mbar_init(bar_tfull, 1);
     ptx::mbar_init(bar_tempty, kF8EpiWarps);
     ptx::mbar_init(bar_drain, 1);
+    for (int qq = 0; qq < 4; ++qq) ptx::mbar_init(xbar + 8 * qq, 2);
     ptx::fence_mbar_init();
   }
   if (warp == 1) {
@@ -271,7 +281,7 @@ grouped_gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmA,
     uint8_t* stage = epi + (warp - 2) * kBoxBytes;
     const uint32_t stage_u32 = epi_u + (warp - 2) * kBoxBytes;
     const uint32_t tq = tmem_base + ((uint32_t)(q * 32) << 16);
-    uint32_t acc_phase = 0;
+    uint32_t acc_phase = 0, x_phase = 0;
     for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
       const Tile t = decode(tile, prefix, mtiles, s_cnt, G, 0, p.K, NT, 0);
       const int row0 = s_off[t.g] + t.mt * BM + q * 32;
@@ -317,9 +327,10 @@ grouped_gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmA,
 
       if (EPI == kEpiSwigluFwd) {
         const int f0 = t.nt * (kF8BN / 2) + 64 * half;
+        uint4 ho[2][4];
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
-          uint4 go[4], uo[4], ho[4];
+          uint4 go[4], uo[4];
           pack_slice(slice32(r, c), go);
           pack_slice(slice32(r, 2 + c), uo);
 #pragma unroll
@@ -329,11 +340,57 @@ grouped_gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmA,
             unpack8(uo[v], ur);
 #pragma unroll
             for (int i = 0; i < 8; ++i) hf[i] = silu_f(gr[i]) * ur[i];
-            ho[v] = pack8(hf);
+            ho[c][v] = pack8(hf);
           }
           f8_store_box(&tmC, stage, stage_u32, lane, go, f0 + 32 * c, row0);          // G
           f8_store_box(&tmC, stage, stage_u32, lane, uo, p.F + f0 + 32 * c, row0);    // U
-          f8_store_box(&tmC2, stage, stage_u32, lane, ho, f0 + 32 * c, row0);         // h
+          f8_store_box(&tmC2, stage, stage_u32, lane, ho[c], f0 + 32 * c, row0);      // h
+        }
+        if (p.qout) {
+          // h's 1 x 128 slice (columns nt*128 ..) is this warp's 64 columns and
+          // its partner's: exchange the row maxima, then write the E4M3 codes
+          float m = 0.f;
+#pragma unroll
+          for (int c = 0; c < 2; ++c)
+#pragma unroll
+            for (int v = 0; v < 4; ++v) {
+              float f[8];
+              unpack8(ho[c][v], f);
+              m = fmaxf(m, amax8(f));
+            }
+          float* xs = xch + ((x_phase * 4 + q) * 2) * 32;
+          xs[half * 32 + lane] = m;
+          __syncwarp();
+          if (lane == 0) ptx::mbar_arrive(xbar + 8 * q);
+          ok = __all_sync(0xffffffffu,
+                          ptx::mbar_wait(xbar + 8 * q, x_phase, kWaitBudget, abort_flag));
+          if (!ok) {
+            if (lane == 0) {
+              record_status(p.status, MOE_ERR_TIMEOUT);
+              *abort_flag = 1;
+            }
+            break;
+          }
+          const uint32_t code = ue8m0_code(fmaxf(m, xs[(half ^ 1) * 32 + lane]));
+          const float inv = ue8m0_inv(code);
+          const int row = row0 + lane;
+          uint8_t* dst = p.qout + (size_t)row * p.F + f0;
+#pragma unroll
+          for (int c = 0; c < 2; ++c) {
+            uint2 b[4];
+#pragma unroll
+            for (int v = 0; v < 4; ++v) {
+              float f[8];
+              unpack8(ho[c][v], f);
+              b[v] = e4m3x8(f, inv);
+            }
+            *reinterpret_cast<uint4*>(dst + 32 * c) = make_uint4(b[0].x, b[0].y, b[1].x, b[1].y);
+            *reinterpret_cast<uint4*>(dst + 32 * c + 16) = make_uint4(b[2].x, b[2].y, b[3].x, b[3].y);
+          }
+          if (half == 0)
+            p.qsf[f8::atom_offset(row >> 7, t.nt, p.qsf_kg) + f8::atom_byte(row, t.nt)] =
+                (uint8_t)code;
+          x_phase ^= 1u;
         }
       } else if (EPI == kEpiSwigluBwd) {
 #pragma unroll
@@ -408,11 +465,12 @@ static cudaError_t run_fp8(const CUtensorMap& a, const CUtensorMap& b, const CUt
 
 using namespace gg;
 
-// FC1 + SwiGLU: GU = x_q W13_q^T (gate | up, bf16), h = bf16(silu(G) U).
+// FC1 + SwiGLU: GU = x_q W13_q^T (gate | up, bf16), h = bf16(silu(G) U), and
+// h's 1-byte form (hq, hsf; 1 x 128 slices) for FC2.
 cudaError_t launch_ffn_fc1_fp8(const moe_config& c, const uint8_t* xq, const uint8_t* xsf,
                                const int32_t* counts, const int32_t* offsets, const uint8_t* W13q,
-                               const uint8_t* W13sf, void* GU, void* h, int32_t* status,
-                               cudaStream_t s) {
+                               const uint8_t* W13sf, void* GU, void* h, uint8_t* hq, uint8_t* hsf,
+                               int32_t* status, cudaStream_t s) {
   const int64_t R = rows_max(c);
   const int G = c.E + c.n_shared;
   CUtensorMap a, b, oc, oc2;
@@ -427,6 +485,9 @@ cudaError_t launch_ffn_fc1_fp8(const moe_config& c, const uint8_t* xq, const uin
   p.sfb = W13sf;
   p.sfb_nb = 2 * c.F / 128;
   p.sfb_kg = (int)f8::atoms_k(c.H);
+  p.qout = hq;
+  p.qsf = hsf;
+  p.qsf_kg = (int)f8::atoms_k(c.F);
   return run_fp8<kEpiSwigluFwd, 0>(a, b, oc, oc2, p, s);
 }
 

@@ -172,8 +172,8 @@ cudaError_t launch_ffn_wgrad_fc1(const moe_config& c, const void* dGU, const voi
 // atoms; the same epilogues and outputs as the bf16 launches above.
 cudaError_t launch_ffn_fc1_fp8(const moe_config& c, const uint8_t* xq, const uint8_t* xsf,
                                const int32_t* counts, const int32_t* offsets, const uint8_t* W13q,
-                               const uint8_t* W13sf, void* GU, void* h, int32_t* status,
-                               cudaStream_t s);
+                               const uint8_t* W13sf, void* GU, void* h, uint8_t* hq, uint8_t* hsf,
+                               int32_t* status, cudaStream_t s);
 cudaError_t launch_ffn_fc2_fp8(const moe_config& c, const uint8_t* hq, const uint8_t* hsf,
                                const int32_t* counts, const int32_t* offsets, const uint8_t* W2q,
                                const uint8_t* W2sf, void* y_perm, int32_t* status,

@@ -316,8 +316,8 @@ moe_status moe_grouped_ffn_fwd(const moe_config* cfg, const void* x_perm, const 
     const Fp8Scratch q = fp8_scratch(*cfg, scratch);
     const int G = cfg->E + cfg->n_shared;
     const int64_t R = rows_max(*cfg);
-    MOE_CUDA(launch_ffn_fc1_fp8(*cfg, q.xq, q.xsf, counts, offsets, q.W13q, q.W13sf, GU, h, st, s));
-    MOE_CUDA(launch_quant_rows8(h, q.hq, q.hsf, offsets, counts, G, R, cfg->F, s));
+    MOE_CUDA(launch_ffn_fc1_fp8(*cfg, q.xq, q.xsf, counts, offsets, q.W13q, q.W13sf, GU, h, q.hq,
+                                q.hsf, st, s));
     MOE_CUDA(launch_ffn_fc2_fp8(*cfg, q.hq, q.hsf, counts, offsets, q.W2q, q.W2sf, y_perm, st, s));
     return MOE_OK;
   }
