@@ -272,6 +272,12 @@ MOE_API moe_status moe_permute_noalloc(const moe_config* cfg, const void* x, con
                                        int32_t* token_of, int32_t* sel_offsets,
                                        int32_t* sel_tokens, void* x_perm, void* stream);
 
+/* The status word of the no-scratch dispatch's array: synchronises `stream`,
+ * then copies to *code (host) what the last moe_permute_noalloc call on the
+ * current device recorded -- 0, or MOE_ERR_DEVICE_CHECK for an idx entry
+ * outside [0, E) or repeated within a token. Allocates nothing. */
+MOE_API moe_status moe_permute_noalloc_status(int32_t* code, void* stream);
+
 /* FP8 mode only (es summary §2.4: expert GEMMs in FP8, MXFP8 -- power-of-two
  * block scales -- on Blackwell): quantises the expert weights W13 [G,2F,H] and
  * W2 [G,H,F] (bf16) into E4M3 codes with one UE8M0 scale per 128x128 tile,

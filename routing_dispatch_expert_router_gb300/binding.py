@@ -22,7 +22,7 @@ STATUS_NAMES = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED",
 # every exported entry point of include/moe_abi.h
 ENTRY_POINTS = (
     "moe_query_sizes", "moe_route", "moe_route_replay", "moe_route_aux", "moe_route_aux_bwd",
-    "moe_permute", "moe_permute_noalloc",
+    "moe_permute", "moe_permute_noalloc", "moe_permute_noalloc_status",
     "moe_quantize_weights", "moe_grouped_ffn_fwd", "moe_unpermute",
     "moe_unpermute_bwd", "moe_grouped_ffn_dgrad", "moe_grouped_ffn_wgrad", "moe_grouped_ffn_bwd",
     "moe_grouped_ffn_fwd_reordered", "moe_unpermute_bwd_reordered",
@@ -198,6 +198,14 @@ def moe_permute_noalloc(cfg, x, idx, counts, offsets, row_of, token_of, sel_offs
 def moe_quantize_weights(cfg, W13, W2, scratch, stream=None):
     """FP8 mode: the E4M3 weights (and scales) in scratch; no-op in bf16 mode."""
     _call("moe_quantize_weights", _cfg(cfg), W13, W2, scratch, _stream(stream))
+
+
+def moe_permute_noalloc_status(stream=None) -> int:
+    """The status word the last moe_permute_noalloc call left (synchronises)."""
+    code = ctypes.c_int32(0)
+    _check("moe_permute_noalloc_status",
+           lib().moe_permute_noalloc_status(ctypes.byref(code), ctypes.c_void_p(_stream(stream))))
+    return code.value
 
 
 def moe_grouped_ffn_fwd(cfg, x_perm, counts, offsets, W13, W2, GU, h, y_perm, scratch,

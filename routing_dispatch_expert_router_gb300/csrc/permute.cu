@@ -351,3 +351,17 @@ extern "C" moe_status moe_permute_noalloc(const moe_config* cfg, const void* x,
                                        sel_offsets, sel_tokens, x_perm, sc, s, nullptr);
   return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
+
+// Reads back what the last moe_permute_noalloc call recorded in its status
+// word (an index out of range or repeated): synchronises `stream`, then copies
+// the word from the library's array on the current device.
+extern "C" moe_status moe_permute_noalloc_status(int32_t* code, void* stream) {
+  using namespace moe;
+  if (!code) return MOE_ERR_INVALID_ARG;
+  uint8_t* sc = nullptr;
+  if (noalloc_scratch(&sc) != cudaSuccess) return MOE_ERR_CUDA;
+  if (cudaStreamSynchronize((cudaStream_t)stream) != cudaSuccess) return MOE_ERR_CUDA;
+  if (cudaMemcpy(code, sc + kScratchStatus, sizeof(int32_t), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  return MOE_OK;
+}

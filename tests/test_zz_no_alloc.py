@@ -7,8 +7,9 @@ moe_permute_noalloc serves them with a fixed scratch array inside the library.
 These tests call it through the C-ABI and check that its results equal
 moe_permute's (maps bit-exact, dispatched rows exact) on two calls in a row,
 the second with a smaller problem that runs on whatever the first call left in
-the shared array; and that a problem too large for the array is refused
-before anything is launched.
+the shared array; that a problem too large for the array is refused before
+anything is launched; and that an index problem found on the device is read
+back through moe_permute_noalloc_status.
 """
 import pytest
 import torch
@@ -84,3 +85,26 @@ def test_noalloc_refuses_problems_larger_than_its_array():
         B.moe_permute_noalloc(cfg, t(64, torch.bfloat16), t(64), t(300), t(300), t(64), t(64),
                               t(300), t(64), t(64, torch.bfloat16))
     assert e.value.code == 3     # MOE_ERR_WORKSPACE, nothing launched
+
+
+def test_noalloc_status_reports_index_problems():
+    """An expert index past the last expert, and one repeated within a token,
+    are recorded in the array's status word (MOE_ERR_DEVICE_CHECK) and dropped
+    (row_of = -1); the next clean call starts from a cleared word."""
+    dev = torch.device("cuda")
+    shape = SHAPES[1]
+    cfg, bufs, x = _routed(shape, dev)
+    f = bufs.fwd
+    idx = f["idx"]
+    _permute(B.moe_permute_noalloc, cfg, bufs, x)
+    assert B.moe_permute_noalloc_status() == 0
+    bad = idx.clone()
+    bad[3, 0] = shape.E                 # out of range
+    bad[7, 1] = bad[7, 0]               # the same expert twice
+    f["idx"].copy_(bad)
+    _permute(B.moe_permute_noalloc, cfg, bufs, x)
+    assert B.moe_permute_noalloc_status() == 6
+    assert int(f["row_of"][3, 0]) == -1 and int(f["row_of"][7, 1]) == -1
+    f["idx"].copy_(idx)
+    _permute(B.moe_permute_noalloc, cfg, bufs, x)
+    assert B.moe_permute_noalloc_status() == 0
