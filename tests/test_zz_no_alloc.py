@@ -95,7 +95,7 @@ def test_noalloc_status_reports_index_problems():
     shape = SHAPES[1]
     cfg, bufs, x = _routed(shape, dev)
     f = bufs.fwd
-    idx = f["idx"]
+    idx = f["idx"].clone()
     _permute(B.moe_permute_noalloc, cfg, bufs, x)
     assert B.moe_permute_noalloc_status() == 0
     bad = idx.clone()
