@@ -187,6 +187,16 @@ STAGES = ("route", "permute", "quantize_weights", "grouped_ffn_fwd", "unpermute"
           "router_wgrad")
 
 
+def wgrad_bytes(shape, f) -> int:
+    """Bytes the FP8 weight-gradient stage must move: per live row of the
+    permuted buffers, dO, h, dGU and x_perm read in bf16 (2 B), written as
+    E4M3 (1 B) and read back by the GEMMs (1 B); dW2 and dW13 written in bf16."""
+    H, F, G = shape.H, shape.F, shape.E + shape.n_shared
+    counts = f["counts"].cpu().tolist()
+    live = sum(-(-c // 128) * 128 for c in counts)
+    return live * (H + F + 2 * F + H) * 4 + G * 3 * H * F * 2
+
+
 def stage_table(shape, f, stage_ms, hbm_gbs, fl, tc_peak, bf16_peak):
     """Per-stage device time, algorithmic bytes (or flops) and roofline fraction.
 
@@ -194,7 +204,9 @@ def stage_table(shape, f, stage_ms, hbm_gbs, fl, tc_peak, bf16_peak):
     element, fp32 4 B, int32 maps 4 B, E4M3 1 B plus 1/32 B of scale atoms): A
     kept routed assignments, S*T shared rows, P zero padding rows of the
     permuted buffers. GEMM stages count flops against the tensor peak of their
-    operand type (FP8 forward and data gradients; weight gradients bf16)."""
+    operand type. The FP8 weight-gradient stage also gets its bytes: its four
+    128x1 quantisers read the bf16 operands' live rows and write their E4M3
+    codes, the two GEMMs read those codes and write dW2 and dW13 in bf16."""
     T, H, E, k, S, F = shape.T, shape.H, shape.E, shape.k, shape.n_shared, shape.F
     counts = f["counts"].cpu().tolist()
     offsets = f["offsets"].cpu().tolist()
@@ -218,17 +230,22 @@ def stage_table(shape, f, stage_ms, hbm_gbs, fl, tc_peak, bf16_peak):
         ("route_bwd", T * E * 4 * 2 + maps, "dlogits"),
         ("grouped_ffn_dgrad", fl, "FC2 dgrad+SwiGLU bwd, FC1 dgrad (tcgen05"
          + (" kind::mxf8f6f4)" if fp8 else ")")),
-        ("grouped_ffn_wgrad", fl, "dW2, dW13 (tcgen05 bf16)"),
+        ("grouped_ffn_wgrad", fl, "dW2, dW13 (tcgen05"
+         + (" kind::mxf8f6f4, with their four 128x1 quantisers)" if fp8 else " bf16)")),
         ("permute_bwd", rows * H * bf + T * H * bf + maps, "dx gather-reduce"),
         ("router_wgrad", T * H * bf + E * H * 4 + T * E * 4, "dW_r (each x row once)"),
     ]
     out = []
     for (name, w, what), ms in zip(work, stage_ms):
         if name.startswith("grouped_ffn"):
-            pk = bf16_peak if name == "grouped_ffn_wgrad" else tc_peak
             ach = w / (ms * 1e-3) / 1e12
-            out.append({"stage": name, "what": what, "ms": ms, "tflop": w / 1e12,
-                        "tflops": ach, "frac_tensor": ach / pk})
+            row = {"stage": name, "what": what, "ms": ms, "tflop": w / 1e12,
+                   "tflops": ach, "frac_tensor": ach / tc_peak}
+            if fp8 and name == "grouped_ffn_wgrad":
+                wb = wgrad_bytes(shape, f)
+                row.update({"mb": wb / 1e6, "gbs": wb / (ms * 1e-3) / 1e9,
+                            "frac_hbm": wb / (ms * 1e-3) / 1e9 / hbm_gbs})
+            out.append(row)
         elif w > 0:
             ach = w / (ms * 1e-3) / 1e9
             out.append({"stage": name, "what": what, "ms": ms, "mb": w / 1e6,
@@ -459,10 +476,11 @@ def run_ours(args, rank, world, local):
         "scaling": "weak",
         "vs_baseline": None,
         "dtype": dt_name,
-        "dtype_detail": ("E4M3 operands with UE8M0 power-of-two scales per 128x128 weight tile and "
-                         "1x128 activation slice on the forward and data-gradient GEMMs (fp32 "
-                         "accumulation); weight gradients on the bf16 tensor path over E4M3 "
-                         "values in 128x1 slices; router fp32; activations and outputs bf16"
+        "dtype_detail": ("E4M3 operands with UE8M0 power-of-two scales per 128x128 weight tile, "
+                         "1x128 activation slice along K (forward and data gradients) and 128x1 "
+                         "slice along the tokens (weight gradients); all six expert GEMMs on the "
+                         "block-scaled FP8 tensor cores with fp32 accumulation; router fp32; "
+                         "activations and outputs bf16"
                          if fp8 else "bf16 operands, fp32 accumulation, fp32 router"),
         "data": "synthetic (seeded N(0,1) tokens, N(0,0.02^2) weights; no dataset)",
         "config": {"workload": f"{shape.name}: T={T} H={H} E={E}(+{S} shared) top-{shape.k} "
@@ -491,11 +509,20 @@ def run_ours(args, rank, world, local):
         "clocks": clk,
     }
     if fp8:
-        wg = fl / (sm["grouped_ffn_wgrad"] * 1e-3) / 1e12
-        res["roofline_wgrad"] = {"kernel": "grouped_gemm_kernel (tcgen05 kind::f16 weight "
-                                           "gradients over E4M3 values, with their 4 quantisers)",
-                                 "achieved": wg, "peak": bf16_peak, "unit": "TFLOP/s",
-                                 "frac": wg / bf16_peak}
+        # the weight gradients write both expert weights in bf16 every step:
+        # bound by HBM, not by the FP8 tensor rate
+        wb = wgrad_bytes(shape, f)
+        wms = sm["grouped_ffn_wgrad"]
+        res["roofline_wgrad"] = {
+            "kernel": ("grouped_gemm_fp8_kernel<kEpiWgrad> (tcgen05 kind::mxf8f6f4, K = each "
+                       "expert's rows) with its four 128x1 quantisers"),
+            "bound": "hbm", "achieved": wb / (wms * 1e-3) / 1e9, "peak": pk["hbm_gbs"],
+            "unit": "GB/s", "frac": wb / (wms * 1e-3) / 1e9 / pk["hbm_gbs"],
+            "bytes_per_step": wb, "ms_per_step": wms,
+            "tflops": fl / (wms * 1e-3) / 1e12,
+            "note": "of measured copy bandwidth; the stage writes the weight gradients "
+                    f"({G * 3 * H * F * 2 / 1e9:.2f} GB bf16), and this part's write-only rate "
+                    "is below its copy rate"}
     return res, shape, inp
 
 

@@ -69,8 +69,8 @@ enum { MOE_GROUP_TOP2_SUM = 0, MOE_GROUP_MAX = 1 };
  * with power-of-two block scales (2^ceil(log2(amax/448))): expert weights in
  * 128x128 tiles, activations in 1x128 slices along the dimension their GEMM
  * reduces, weight-gradient operands in 128x1 slices along each expert's
- * tokens. The forward and data-gradient GEMMs run on the block-scaled FP8
- * tensor cores. Router, routing weights and all outputs stay as in bf16 mode.
+ * tokens. All six expert GEMMs run on the block-scaled FP8 tensor cores.
+ * Router, routing weights and all outputs stay as in bf16 mode.
  * In this mode `scratch` also holds the quantised weights and activations
  * (moe_query_sizes counts them), and the scratch used by a forward must be
  * passed unchanged to its backward. Shared experts are not supported in this
@@ -338,8 +338,8 @@ MOE_API moe_status moe_grouped_ffn_dgrad(const moe_config* cfg, const void* dO_p
 /* Weight-gradient half of moe_grouped_ffn_bwd: dW2[g] = dO^T h and
  * dW13[g] = dGU^T x_perm over the group's rows (bf16, zero for empty groups),
  * after moe_grouped_ffn_dgrad has written dGU. FP8 mode: both operands are
- * quantised in 128x1 slices along the group's tokens and multiplied as their
- * bf16 values on the bf16 tensor path (exactly the FP8 products). */
+ * quantised to E4M3 in 128x1 slices along the group's tokens (into scratch)
+ * and multiplied on the block-scaled FP8 tensor cores. */
 MOE_API moe_status moe_grouped_ffn_wgrad(const moe_config* cfg, const void* dO_perm,
                                          const void* x_perm, const void* h, const void* dGU,
                                          const int32_t* counts, const int32_t* offsets,

@@ -76,6 +76,19 @@ __device__ __forceinline__ uint2 e4m3x8(const float (&f)[8], float inv_s) {
   return make_uint2(w[0] | (w[1] << 16), w[2] | (w[3] << 16));
 }
 
+// The same with a scale per value (eight columns, each its own 128 x 1 block).
+__device__ __forceinline__ uint2 e4m3x8_each(const float (&f)[8], const float* inv_s) {
+  uint32_t w[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    uint16_t h;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;"
+        : "=h"(h) : "f"(f[2 * i + 1] * inv_s[2 * i + 1]), "f"(f[2 * i] * inv_s[2 * i]));
+    w[i] = h;
+  }
+  return make_uint2(w[0] | (w[1] << 16), w[2] | (w[3] << 16));
+}
+
 __device__ __forceinline__ float amax8(const float (&f)[8]) {
   float m = 0.f;
 #pragma unroll

@@ -12,9 +12,11 @@
 // happen in the tensor core; only the summation order differs from the fp64
 // reference.
 //
-// Row-grouped GEMMs only (forward FC1 + SwiGLU, FC2, and the two data
-// gradients); the weight gradients stay on the bf16 path (their cost is the
-// bf16 weight-gradient writes, not the MMA rate).
+// All six expert GEMMs: the row-grouped ones (forward FC1 + SwiGLU, FC2, the
+// two data gradients; M = a group's rows, K = H or F) and the two weight
+// gradients (K-grouped: M x N = the weight's shape, K = the group's rows, both
+// operands read MN-major from their [rows, columns] buffers, quantised in
+// 128 x 1 slices along the tokens).
 //
 // One persistent kernel per GEMM, one CTA per SM, 320 threads:
 //   warp 0     TMA producer (one lane): per 128-deep k-block, A (128 rows) and
@@ -37,7 +39,7 @@ namespace moe {
 namespace gg {
 
 constexpr int kF8Threads = 320;
-constexpr int kF8Stages = 4;
+constexpr int kF8MaxStages = 4;                   // size of the barrier arrays
 constexpr int kF8BK = 128;                        // E4M3 elements (= bytes) per k-block
 constexpr int kF8BN = 256;
 constexpr int kF8ABytes = BM * kF8BK;             // 16 KB
@@ -50,15 +52,31 @@ constexpr int kF8EpiWarps = 8;
 // buffered by tile parity: [2][4 quarters][2 warps][32 rows] fp32
 constexpr int kF8XchBytes = 2 * 4 * 2 * 32 * 4;
 constexpr int kF8XbarOff = 4864;                  // their 4 mbarriers in the control block
-constexpr int kF8Smem = kF8Stages * (kF8Stage + kF8SfStage) + kCtrlBytes +
-                        kF8EpiWarps * kBoxBytes + kF8XchBytes + 1024;
 static_assert(kF8XbarOff >= 4608 + 33 * 4 && kF8XbarOff + 32 <= kCtrlBytes,
               "exchange barriers inside the control block, after the scan scratch");
 constexpr uint32_t kF8TmemCols = 512;
 constexpr uint32_t kF8SfCol = 256;                // first scale-factor column
 constexpr uint32_t kF8SfSlotCols = 16;
-static_assert(kF8Smem <= 232448, "FP8 grouped GEMM shared memory");
-static_assert(kF8SfCol + kF8Stages * kF8SfSlotCols <= kF8TmemCols, "FP8 tensor-memory columns");
+
+// Shared-memory plan per epilogue. The weight gradients stage their bf16
+// output in 32 x 64 boxes (whole 128-byte lines, 4 KB per warp: the kernel is
+// bound by these writes) and keep three operand stages, enough for their
+// K of a few 128-row blocks per tile; the others stage 32 x 32 boxes (2 KB)
+// behind four stages.
+template <int EPI>
+struct F8Cfg {
+  static constexpr bool KG = EPI == kEpiWgrad;
+  static constexpr int STAGES = KG ? 3 : 4;
+  static constexpr int BOX = KG ? 4096 : kBoxBytes;
+  static constexpr int SF_OFF = STAGES * kF8Stage;
+  static constexpr int CTRL_OFF = SF_OFF + STAGES * kF8SfStage;
+  static constexpr int EPI_OFF = (CTRL_OFF + kCtrlBytes + 1023) / 1024 * 1024;
+  static constexpr int XCH_OFF = EPI_OFF + kF8EpiWarps * BOX;
+  static constexpr int SMEM = XCH_OFF + kF8XchBytes + 1024;
+  static_assert(STAGES <= kF8MaxStages, "barrier arrays");
+  static_assert(SMEM <= 232448, "FP8 grouped GEMM shared memory");
+  static_assert(kF8SfCol + STAGES * kF8SfSlotCols <= kF8TmemCols, "FP8 tensor-memory columns");
+};
 
 // One 32 x 32 bf16 box (this warp's 32 rows, 32 columns) through the warp's
 // staging slot to global memory by TMA.
@@ -86,20 +104,22 @@ grouped_gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmA,
                         const __grid_constant__ CUtensorMap tmB,
                         const __grid_constant__ CUtensorMap tmC,
                         const __grid_constant__ CUtensorMap tmC2, const Params p) {
+  using C = F8Cfg<EPI>;
+  constexpr int kStages = C::STAGES;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = ptx::smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t* sbase = smem_raw + (base - raw);
-  const uint32_t sf_u = base + kF8Stages * kF8Stage;
-  const uint32_t ctrl_u = sf_u + kF8Stages * kF8SfStage;
-  uint8_t* ctrl = sbase + (ctrl_u - base);
-  const uint32_t epi_u = ctrl_u + kCtrlBytes;
-  uint8_t* epi = ctrl + kCtrlBytes;
-  float* xch = reinterpret_cast<float*>(epi + kF8EpiWarps * kBoxBytes);
+  const uint32_t sf_u = base + C::SF_OFF;
+  const uint32_t ctrl_u = base + C::CTRL_OFF;
+  uint8_t* ctrl = sbase + C::CTRL_OFF;
+  const uint32_t epi_u = base + C::EPI_OFF;
+  uint8_t* epi = sbase + C::EPI_OFF;
+  float* xch = reinterpret_cast<float*>(sbase + C::XCH_OFF);
   const uint32_t xbar = ctrl_u + kF8XbarOff;              // [4] quarters
-  const uint32_t bar_full = ctrl_u;                       // [kF8Stages]
-  const uint32_t bar_empty = ctrl_u + 8 * kF8Stages;      // [kF8Stages]
-  const uint32_t bar_tfull = ctrl_u + 16 * kF8Stages;
+  const uint32_t bar_full = ctrl_u;                       // [kStages]
+  const uint32_t bar_empty = ctrl_u + 8 * kF8MaxStages;   // [kStages]
+  const uint32_t bar_tfull = ctrl_u + 16 * kF8MaxStages;
   const uint32_t bar_tempty = bar_tfull + 8;
   const uint32_t bar_drain = bar_tfull + 16;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(ctrl + 192);
@@ -113,12 +133,14 @@ grouped_gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmA,
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int G = p.G;
   const int NT = (EPI == kEpiSwigluFwd) ? p.F / (kF8BN / 2) : p.N / kF8BN;
-  const int nk = p.K / kF8BK;
+  // k-blocks per tile: K / 128, or the group's row blocks (weight gradients)
+  const int nk_fixed = C::KG ? 0 : p.K / kF8BK;
+  const int n_fast = C::KG ? p.n_fast : 0;
   for (int g = tid; g < G; g += kF8Threads) {
     const int c = p.counts[g];
     s_cnt[g] = c;
     s_off[g] = p.offsets[g];
-    const int mt = (c + BM - 1) / BM;
+    const int mt = C::KG ? p.Mw / BM : (c + BM - 1) / BM;
     mtiles[g] = mt;
     prefix[g] = mt * NT;
   }
@@ -130,7 +152,7 @@ grouped_gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmA,
   if ((int)blockIdx.x >= total) return;
 
   if (tid == 0) {
-    for (int s = 0; s < kF8Stages; ++s) {
+    for (int s = 0; s < kStages; ++s) {
       ptx::mbar_init(bar_full + 8 * s, 1);
       ptx::mbar_init(bar_empty + 8 * s, 1);
     }
@@ -160,8 +182,12 @@ grouped_gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmA,
       uint32_t issued_mask = 0, issued_phase = 0;
       bool ok = true;
       for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
-        const Tile t = decode(tile, prefix, mtiles, s_cnt, G, 0, p.K, NT, 0);
-        const int row0 = s_off[t.g] + t.mt * BM;
+        const Tile t = decode(tile, prefix, mtiles, s_cnt, G, 0, p.K, NT, n_fast);
+        const int nk = C::KG ? (s_cnt[t.g] + kF8BK - 1) / kF8BK : nk_fixed;
+        // A: rows row0.. (K-major), or columns m0.. of the group's rows k0..
+        // (MN-major, weight gradients)
+        const int row0 = C::KG ? t.mt * BM : s_off[t.g] + t.mt * BM;
+        const int kr0 = C::KG ? s_off[t.g] : 0;
         // B: two 128-row (K-major) or 128-column (MN-major) boxes and their atoms
         int b0, b1, nb0, nb1;
         if (EPI == kEpiSwigluFwd) {
@@ -174,11 +200,12 @@ grouped_gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmA,
         }
         nb0 = b0 / 128;
         nb1 = b1 / 128;
+        // atom rows: per group for the weights, shared by all groups for the
+        // weight-gradient operands (their K blocks are the buffer's row blocks)
+        const int64_t gb = C::KG ? 0 : (int64_t)t.g * p.sfb_nb;
         const uint8_t* sfa = p.sfa + (int64_t)(row0 / 128) * p.sfa_kg * f8::kAtomBytes;
-        const uint8_t* sfb0 =
-            p.sfb + ((int64_t)t.g * p.sfb_nb + nb0) * p.sfb_kg * f8::kAtomBytes;
-        const uint8_t* sfb1 =
-            p.sfb + ((int64_t)t.g * p.sfb_nb + nb1) * p.sfb_kg * f8::kAtomBytes;
+        const uint8_t* sfb0 = p.sfb + (gb + nb0) * p.sfb_kg * f8::kAtomBytes;
+        const uint8_t* sfb1 = p.sfb + (gb + nb1) * p.sfb_kg * f8::kAtomBytes;
         for (int kb = 0; kb < nk; ++kb) {
           if (!ptx::mbar_wait(bar_empty + 8 * stage, phase ^ 1u, kWaitBudget, abort_flag)) {
             ok = false;
@@ -188,23 +215,25 @@ grouped_gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmA,
           ptx::mbar_arrive_expect_tx(fb, kF8Stage + kF8SfStage);
           const uint32_t sA = base + stage * kF8Stage;
           const uint32_t sB = sA + kF8ABytes;
-          const int k0 = kb * kF8BK;
-          ptx::tma_load_2d(sA, &tmA, fb, k0, row0);
+          const int k0 = kr0 + kb * kF8BK;
+          const int brow = C::KG ? k0 : t.g * p.b_rows + k0;
+          if (C::KG) ptx::tma_load_2d(sA, &tmA, fb, row0, k0);
+          else ptx::tma_load_2d(sA, &tmA, fb, k0, row0);
           if (B_MN == 0) {
             ptx::tma_load_2d(sB, &tmB, fb, k0, t.g * p.b_rows + b0);
             ptx::tma_load_2d(sB + 16384, &tmB, fb, k0, t.g * p.b_rows + b1);
           } else {
-            ptx::tma_load_2d(sB, &tmB, fb, b0, t.g * p.b_rows + k0);
-            ptx::tma_load_2d(sB + 16384, &tmB, fb, b1, t.g * p.b_rows + k0);
+            ptx::tma_load_2d(sB, &tmB, fb, b0, brow);
+            ptx::tma_load_2d(sB + 16384, &tmB, fb, b1, brow);
           }
           const uint32_t sfs = sf_u + stage * kF8SfStage;
-          const int64_t a4 = (int64_t)(kb / f8::kAtomKBlocks) * f8::kAtomBytes;
+          const int64_t a4 = (int64_t)(k0 / kF8BK / f8::kAtomKBlocks) * f8::kAtomBytes;
           ptx::bulk_load(sfs, sfa + a4, f8::kAtomBytes, fb);
           ptx::bulk_load(sfs + f8::kAtomBytes, sfb0 + a4, f8::kAtomBytes, fb);
           ptx::bulk_load(sfs + 2 * f8::kAtomBytes, sfb1 + a4, f8::kAtomBytes, fb);
           issued_mask |= 1u << stage;
           issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
-          if (++stage == kF8Stages) {
+          if (++stage == kStages) {
             stage = 0;
             phase ^= 1u;
           }
@@ -215,17 +244,26 @@ grouped_gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmA,
         *abort_flag = 1;
       }
       // every load issued must land before the CTA may exit
-      for (int s = 0; s < kF8Stages; ++s)
+      for (int s = 0; s < kStages; ++s)
         if (issued_mask & (1u << s))
           ptx::mbar_wait(bar_full + 8 * s, (issued_phase >> s) & 1u, kWaitBudget, nullptr);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      constexpr uint32_t IDESC = ptx::idesc_mxf8_e4m3(BM, kF8BN, 0, B_MN);
+      constexpr uint32_t IDESC = ptx::idesc_mxf8_e4m3(BM, kF8BN, C::KG ? 1 : 0, B_MN);
       uint32_t stage = 0, phase = 0, acc_phase = 0;
       bool ok = true, issued = false;
       for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+        int nk = nk_fixed, kb0 = 0;
+        if (C::KG) {
+          // the group's row blocks; an empty group's tile takes no MMA (its
+          // epilogue writes zeros without the accumulator)
+          const Tile t = decode(tile, prefix, mtiles, s_cnt, G, 0, p.K, NT, n_fast);
+          nk = (s_cnt[t.g] + kF8BK - 1) / kF8BK;
+          kb0 = s_off[t.g] / kF8BK;
+          if (nk == 0) continue;
+        }
         if (!ptx::mbar_wait(bar_tempty, acc_phase ^ 1u, kWaitBudget, abort_flag)) {
           ok = false;
           break;
@@ -243,19 +281,23 @@ grouped_gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmA,
           ptx::tmem_cp_32x128b_warpx4(sfa_t, ptx::smem_desc_sf(sfs));
           ptx::tmem_cp_32x128b_warpx4(sfb_t, ptx::smem_desc_sf(sfs + f8::kAtomBytes));
           ptx::tmem_cp_32x128b_warpx4(sfb_t + 4, ptx::smem_desc_sf(sfs + 2 * f8::kAtomBytes));
-          const uint32_t idesc = ptx::idesc_with_sf_id(IDESC, (uint32_t)kb & 3u);
+          // the scale byte of this K block inside its atom (K blocks counted
+          // from the start of the operand: the buffer's row blocks for the
+          // weight gradients)
+          const uint32_t idesc = ptx::idesc_with_sf_id(IDESC, (uint32_t)(kb0 + kb) & 3u);
           const uint32_t sA = base + stage * kF8Stage;
           const uint32_t sB = sA + kF8ABytes;
 #pragma unroll
           for (int kk = 0; kk < kF8BK / 32; ++kk) {
-            const uint64_t ad = ptx::smem_desc_sw128(sA + kk * 32, 16, 1024);
+            const uint64_t ad = C::KG ? ptx::smem_desc_sw128(sA + kk * 4096, 16384, 1024)
+                                      : ptx::smem_desc_sw128(sA + kk * 32, 16, 1024);
             const uint64_t bd = B_MN ? ptx::smem_desc_sw128(sB + kk * 4096, 16384, 1024)
                                      : ptx::smem_desc_sw128(sB + kk * 32, 16, 1024);
             ptx::mma_mxf8(tmem_base, ad, bd, idesc, sfa_t, sfb_t, (kb | kk) ? 1u : 0u);
           }
           issued = true;
           ptx::mma_commit(bar_empty + 8 * stage);
-          if (++stage == kF8Stages) {
+          if (++stage == kStages) {
             stage = 0;
             phase ^= 1u;
           }
@@ -278,13 +320,15 @@ grouped_gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmA,
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;                       // tensor-memory lane quarter
     const int half = (warp - 2) >> 2;             // which 128 accumulator columns
-    uint8_t* stage = epi + (warp - 2) * kBoxBytes;
-    const uint32_t stage_u32 = epi_u + (warp - 2) * kBoxBytes;
+    uint8_t* stage = epi + (warp - 2) * C::BOX;
+    const uint32_t stage_u32 = epi_u + (warp - 2) * C::BOX;
     const uint32_t tq = tmem_base + ((uint32_t)(q * 32) << 16);
     uint32_t acc_phase = 0, x_phase = 0;
     for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
-      const Tile t = decode(tile, prefix, mtiles, s_cnt, G, 0, p.K, NT, 0);
-      const int row0 = s_off[t.g] + t.mt * BM + q * 32;
+      const Tile t = decode(tile, prefix, mtiles, s_cnt, G, 0, p.K, NT, n_fast);
+      const int row0 = C::KG ? t.g * p.Mw + t.mt * BM + q * 32 : s_off[t.g] + t.mt * BM + q * 32;
+      // an empty group's weight-gradient tile: zeros, no accumulator
+      const bool acc = !C::KG || s_cnt[t.g] > 0;
       // SwiGLU backward: G and U of the first 32 columns, loaded before the wait
       const __nv_bfloat16* gu = nullptr;
       uint4 gq[4], uq[4];
@@ -298,8 +342,12 @@ grouped_gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmA,
           uq[v] = ldg_nc_v4(gu + p.F + fb + v * 8);
         }
       }
-      bool ok = ptx::mbar_wait(bar_tfull, acc_phase, kWaitBudget, abort_flag);
-      ok = __all_sync(0xffffffffu, ok);
+      uint32_t r[128];
+      bool ok = true;
+      if (acc) {
+        ok = ptx::mbar_wait(bar_tfull, acc_phase, kWaitBudget, abort_flag);
+        ok = __all_sync(0xffffffffu, ok);
+      }
       if (!ok) {
         if (lane == 0) {
           record_status(p.status, MOE_ERR_TIMEOUT);
@@ -307,23 +355,27 @@ grouped_gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmA,
         }
         break;
       }
-      ptx::tc_fence_after();
-      uint32_t r[128];
-      if (EPI == kEpiSwigluFwd) {
-        // gate columns 64*half .. +63 and the matching up columns 128 + 64*half ..
-        ptx::tmem_ld32(tq + 64 * half, *reinterpret_cast<uint32_t(*)[32]>(&r[0]));
-        ptx::tmem_ld32(tq + 64 * half + 32, *reinterpret_cast<uint32_t(*)[32]>(&r[32]));
-        ptx::tmem_ld32(tq + 128 + 64 * half, *reinterpret_cast<uint32_t(*)[32]>(&r[64]));
-        ptx::tmem_ld32(tq + 160 + 64 * half, *reinterpret_cast<uint32_t(*)[32]>(&r[96]));
+      if (!acc) {
+#pragma unroll
+        for (int i = 0; i < 128; ++i) r[i] = 0u;
       } else {
-        ptx::tmem_ld128(tq + 128 * half, r);
+        ptx::tc_fence_after();
+        if (EPI == kEpiSwigluFwd) {
+          // gate columns 64*half .. +63 and the matching up columns 128 + 64*half ..
+          ptx::tmem_ld32(tq + 64 * half, *reinterpret_cast<uint32_t(*)[32]>(&r[0]));
+          ptx::tmem_ld32(tq + 64 * half + 32, *reinterpret_cast<uint32_t(*)[32]>(&r[32]));
+          ptx::tmem_ld32(tq + 128 + 64 * half, *reinterpret_cast<uint32_t(*)[32]>(&r[64]));
+          ptx::tmem_ld32(tq + 160 + 64 * half, *reinterpret_cast<uint32_t(*)[32]>(&r[96]));
+        } else {
+          ptx::tmem_ld128(tq + 128 * half, r);
+        }
+        ptx::tmem_ld_wait();
+        // the accumulator is free for the next tile's MMAs
+        ptx::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(bar_tempty);
+        acc_phase ^= 1u;
       }
-      ptx::tmem_ld_wait();
-      // the accumulator is free for the next tile's MMAs
-      ptx::tc_fence_before();
-      __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(bar_tempty);
-      acc_phase ^= 1u;
 
       if (EPI == kEpiSwigluFwd) {
         const int f0 = t.nt * (kF8BN / 2) + 64 * half;
@@ -392,6 +444,30 @@ grouped_gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmA,
                 (uint8_t)code;
           x_phase ^= 1u;
         }
+      } else if (EPI == kEpiWgrad) {
+        // dW rows g*Mw + m-tile.., columns n-tile*256 + 128*half.. in 32 x 64
+        // boxes (128-byte rows, 128-byte swizzle: chunk j of row r at j ^ (r & 7))
+        const int c0 = t.nt * kF8BN + 128 * half;
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+          uint4 o[4], o2[4];
+          pack_slice(slice32(r, 2 * j), o);
+          pack_slice(slice32(r, 2 * j + 1), o2);
+          if (lane == 0) ptx::tma_store_wait_read();
+          __syncwarp();
+          uint8_t* rowp = stage + lane * 128;
+#pragma unroll
+          for (int v = 0; v < 4; ++v) {
+            *reinterpret_cast<uint4*>(rowp + ((v ^ (lane & 7)) << 4)) = o[v];
+            *reinterpret_cast<uint4*>(rowp + (((v + 4) ^ (lane & 7)) << 4)) = o2[v];
+          }
+          ptx::fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            ptx::tma_store_2d(&tmC, stage_u32, c0 + 64 * j, row0);
+            ptx::tma_store_commit();
+          }
+        }
       } else if (EPI == kEpiSwigluBwd) {
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
@@ -451,13 +527,14 @@ template <int EPI, int B_MN>
 static cudaError_t run_fp8(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& c,
                            const CUtensorMap& c2, const Params& p, cudaStream_t s) {
   auto kern = grouped_gemm_fp8_kernel<EPI, B_MN>;
+  constexpr int smem = F8Cfg<EPI>::SMEM;
   static bool attr_set = false;
   if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kF8Smem);
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  kern<<<num_sms(), kF8Threads, kF8Smem, s>>>(a, b, c, c2, p);
+  kern<<<num_sms(), kF8Threads, smem, s>>>(a, b, c, c2, p);
   return cudaGetLastError();
 }
 
@@ -569,6 +646,54 @@ cudaError_t launch_ffn_fc1_dgrad_fp8(const moe_config& c, const uint8_t* dGq, co
   p.sfb_nb = c.H / 128;
   p.sfb_kg = (int)f8::atoms_k(2LL * c.F);
   return run_fp8<kEpiDgradRouter, 1>(a, b, oc, oc, p, s);
+}
+
+// Weight gradients (K = each group's rows, both operands MN-major from their
+// [rows, columns] buffers, 128 x 1 slices along the tokens):
+// dW2[g] = dO_q^T h_q (M = H, N = F).
+cudaError_t launch_ffn_wgrad_fc2_fp8(const moe_config& c, const uint8_t* dOq, const uint8_t* dOsf,
+                                     const uint8_t* hq, const uint8_t* hsf, const int32_t* counts,
+                                     const int32_t* offsets, void* dW2, int32_t* status,
+                                     cudaStream_t s) {
+  const int64_t R = rows_max(c);
+  const int G = c.E + c.n_shared;
+  CUtensorMap a, b, oc;
+  if (!make_map_u8(&a, dOq, c.H, R) || !make_map_u8(&b, hq, c.F, R) ||
+      !make_out_map_w64(&oc, dW2, c.F, (uint64_t)G * c.H))
+    return cudaErrorInvalidValue;
+  Params p = base_params(c, counts, offsets, status);
+  p.Mw = c.H;
+  p.N = c.F;
+  p.K = 0;
+  p.n_fast = p.Mw > p.N;
+  p.sfa = dOsf;
+  p.sfa_kg = (int)f8::atoms_k(R);
+  p.sfb = hsf;
+  p.sfb_kg = (int)f8::atoms_k(R);
+  return run_fp8<kEpiWgrad, 1>(a, b, oc, oc, p, s);
+}
+
+// dW13[g] = dGU_q^T x_q (M = 2F, N = H).
+cudaError_t launch_ffn_wgrad_fc1_fp8(const moe_config& c, const uint8_t* dGq, const uint8_t* dGsf,
+                                     const uint8_t* xq, const uint8_t* xsf, const int32_t* counts,
+                                     const int32_t* offsets, void* dW13, int32_t* status,
+                                     cudaStream_t s) {
+  const int64_t R = rows_max(c);
+  const int G = c.E + c.n_shared;
+  CUtensorMap a, b, oc;
+  if (!make_map_u8(&a, dGq, 2ULL * c.F, R) || !make_map_u8(&b, xq, c.H, R) ||
+      !make_out_map_w64(&oc, dW13, c.H, (uint64_t)G * 2 * c.F))
+    return cudaErrorInvalidValue;
+  Params p = base_params(c, counts, offsets, status);
+  p.Mw = 2 * c.F;
+  p.N = c.H;
+  p.K = 0;
+  p.n_fast = p.Mw > p.N;
+  p.sfa = dGsf;
+  p.sfa_kg = (int)f8::atoms_k(R);
+  p.sfb = xsf;
+  p.sfb_kg = (int)f8::atoms_k(R);
+  return run_fp8<kEpiWgrad, 1>(a, b, oc, oc, p, s);
 }
 
 }  // namespace moe

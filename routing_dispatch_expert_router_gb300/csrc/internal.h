@@ -93,9 +93,9 @@ cudaError_t launch_quant_tiles8(const void* W, uint8_t* Wq, uint8_t* sf_f, uint8
 cudaError_t launch_quant_rows8(const void* X, uint8_t* Xq, uint8_t* sf, const int32_t* offsets,
                                const int32_t* counts, int G, int64_t rows_max, int cols,
                                cudaStream_t s);
-cudaError_t launch_quant_cols(const void* X, void* Xq, const int32_t* offsets,
-                              const int32_t* counts, int G, int64_t rows_max, int cols,
-                              cudaStream_t s);
+cudaError_t launch_quant_cols8(const void* X, uint8_t* Xq, uint8_t* sf, const int32_t* offsets,
+                               const int32_t* counts, int G, int64_t rows_max, int cols,
+                               cudaStream_t s);
 
 // Where the FP8 mode keeps its quantised tensors inside `scratch`.
 struct Fp8Scratch {
@@ -113,10 +113,16 @@ struct Fp8Scratch {
   uint8_t* dOsf;
   uint8_t* dGq;     // [R,2F] dGU
   uint8_t* dGsf;
-  void* cH;         // [R,H]  bf16 values of dO in 128x1 slices   (weight gradients)
-  void* bF;         // [R,F]  h
-  void* d2F;        // [R,2F] dGU
-  void* aH;         // [R,H]  x_perm
+  // 128x1 slices along the tokens (weight gradients): E4M3 codes, then atoms
+  // [columns / 128][row blocks / 4]
+  uint8_t* cHq;     // [R,H]  dO
+  uint8_t* cHsf;
+  uint8_t* bFq;     // [R,F]  h
+  uint8_t* bFsf;
+  uint8_t* d2Fq;    // [R,2F] dGU
+  uint8_t* d2Fsf;
+  uint8_t* aHq;     // [R,H]  x_perm
+  uint8_t* aHsf;
 };
 Fp8Scratch fp8_scratch(const moe_config& c, void* scratch);
 
@@ -187,6 +193,16 @@ cudaError_t launch_ffn_fc1_dgrad_fp8(const moe_config& c, const uint8_t* dGq, co
                                      const uint8_t* W13q, const uint8_t* W13sf_t,
                                      const int32_t* token_of, const float* dlogits,
                                      const float* W_r, void* dX_perm, int32_t* status,
+                                     cudaStream_t s);
+// Weight gradients over the 128x1-slice operands (K = each group's rows):
+// dW2[g] = dO^T h, dW13[g] = dGU^T x_perm (bf16; zero for empty groups).
+cudaError_t launch_ffn_wgrad_fc2_fp8(const moe_config& c, const uint8_t* dOq, const uint8_t* dOsf,
+                                     const uint8_t* hq, const uint8_t* hsf, const int32_t* counts,
+                                     const int32_t* offsets, void* dW2, int32_t* status,
+                                     cudaStream_t s);
+cudaError_t launch_ffn_wgrad_fc1_fp8(const moe_config& c, const uint8_t* dGq, const uint8_t* dGsf,
+                                     const uint8_t* xq, const uint8_t* xsf, const int32_t* counts,
+                                     const int32_t* offsets, void* dW13, int32_t* status,
                                      cudaStream_t s);
 
 }  // namespace moe

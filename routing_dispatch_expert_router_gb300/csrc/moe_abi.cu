@@ -59,19 +59,21 @@ static int64_t base_scratch_bytes(const moe_config& c) {
 
 // The FP8 mode's region of scratch, in order: the E4M3 weights with their
 // scale atoms for both orientations, the 1-byte activations (x_perm, h, dO,
-// dGU in 1x128 slices) with their atoms, and the bf16 values of the 128x1
-// slices that the weight gradients read.
+// dGU in 1x128 slices) with their atoms, and the 1-byte weight-gradient
+// operands (dO, h, dGU, x_perm in 128x1 slices) with theirs.
 static int64_t fp8_region(const moe_config& c, Fp8Scratch* f, uint8_t* p) {
+  constexpr int kRegions = 22;
   const int64_t G = c.E + c.n_shared, R = rows_max(c), H = c.H, F = c.F;
-  const int64_t sizes[18] = {
+  const int64_t sizes[kRegions] = {
       G * 2 * F * H, f8::sf_bytes(G * 2 * F, H), f8::sf_bytes(G * H, 2 * F),
       G * H * F,     f8::sf_bytes(G * H, F),     f8::sf_bytes(G * F, H),
       R * H, f8::sf_bytes(R, H), R * F, f8::sf_bytes(R, F),
       R * H, f8::sf_bytes(R, H), R * 2 * F, f8::sf_bytes(R, 2 * F),
-      R * H * 2, R * F * 2, R * 2 * F * 2, R * H * 2};
-  uint8_t* ptrs[18];
+      R * H, f8::sf_bytes(H, R), R * F, f8::sf_bytes(F, R),
+      R * 2 * F, f8::sf_bytes(2 * F, R), R * H, f8::sf_bytes(H, R)};
+  uint8_t* ptrs[kRegions];
   int64_t off = 0;
-  for (int i = 0; i < 18; ++i) {
+  for (int i = 0; i < kRegions; ++i) {
     ptrs[i] = p ? p + off : nullptr;
     off += align256(sizes[i]);
   }
@@ -90,10 +92,14 @@ static int64_t fp8_region(const moe_config& c, Fp8Scratch* f, uint8_t* p) {
     f->dOsf = ptrs[11];
     f->dGq = ptrs[12];
     f->dGsf = ptrs[13];
-    f->cH = ptrs[14];
-    f->bF = ptrs[15];
-    f->d2F = ptrs[16];
-    f->aH = ptrs[17];
+    f->cHq = ptrs[14];
+    f->cHsf = ptrs[15];
+    f->bFq = ptrs[16];
+    f->bFsf = ptrs[17];
+    f->d2Fq = ptrs[18];
+    f->d2Fsf = ptrs[19];
+    f->aHq = ptrs[20];
+    f->aHsf = ptrs[21];
   }
   return off;
 }
@@ -393,17 +399,20 @@ moe_status moe_grouped_ffn_wgrad(const moe_config* cfg, const void* dO_perm, con
   cudaStream_t s = (cudaStream_t)stream;
   int32_t* st = status_word(scratch);
   if (cfg->dtype == MOE_DTYPE_FP8_E4M3_BLOCK) {
-    // both operands in 128x1 slices along each expert's tokens, as bf16 values
+    // both operands in 128x1 slices along each expert's tokens (E4M3 codes
+    // and scale atoms), multiplied on the block-scaled FP8 tensor cores
     const Fp8Scratch q = fp8_scratch(*cfg, scratch);
     const int G = cfg->E + cfg->n_shared;
     const int64_t R = rows_max(*cfg);
     const int H = cfg->H, F = cfg->F;
-    MOE_CUDA(launch_quant_cols(dO_perm, q.cH, offsets, counts, G, R, H, s));
-    MOE_CUDA(launch_quant_cols(h, q.bF, offsets, counts, G, R, F, s));
-    MOE_CUDA(launch_ffn_wgrad_fc2(*cfg, q.cH, q.bF, counts, offsets, dW2, st, s));
-    MOE_CUDA(launch_quant_cols(dGU, q.d2F, offsets, counts, G, R, 2 * F, s));
-    MOE_CUDA(launch_quant_cols(x_perm, q.aH, offsets, counts, G, R, H, s));
-    MOE_CUDA(launch_ffn_wgrad_fc1(*cfg, q.d2F, q.aH, counts, offsets, dW13, st, s));
+    MOE_CUDA(launch_quant_cols8(dO_perm, q.cHq, q.cHsf, offsets, counts, G, R, H, s));
+    MOE_CUDA(launch_quant_cols8(h, q.bFq, q.bFsf, offsets, counts, G, R, F, s));
+    MOE_CUDA(launch_ffn_wgrad_fc2_fp8(*cfg, q.cHq, q.cHsf, q.bFq, q.bFsf, counts, offsets, dW2,
+                                      st, s));
+    MOE_CUDA(launch_quant_cols8(dGU, q.d2Fq, q.d2Fsf, offsets, counts, G, R, 2 * F, s));
+    MOE_CUDA(launch_quant_cols8(x_perm, q.aHq, q.aHsf, offsets, counts, G, R, H, s));
+    MOE_CUDA(launch_ffn_wgrad_fc1_fp8(*cfg, q.d2Fq, q.d2Fsf, q.aHq, q.aHsf, counts, offsets, dW13,
+                                      st, s));
     return MOE_OK;
   }
   MOE_CUDA(launch_ffn_wgrad_fc2(*cfg, dO_perm, h, counts, offsets, dW2, st, s));

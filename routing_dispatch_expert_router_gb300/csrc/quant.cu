@@ -11,48 +11,16 @@
 //          reduces along that row),
 //   cols   128 x 1 slices along the tokens of each 128-row block of the
 //          permuted buffer (weight-gradient operands).
-// Two output forms:
-//   * 1-byte E4M3 codes with UE8M0 scale atoms (fp8_layout.cuh), the operands
-//     of the block-scaled FP8 tensor-core GEMMs (forward and data gradients:
-//     the tiles and rows quantisers);
-//   * the dequantised values written back as bf16 (the cols quantiser), which
-//     holds every E4M3 value times a power of two exactly: the weight-gradient
-//     GEMMs run these on the bf16 tensor path and form exactly the products an
-//     FP8 MMA would (fp32 accumulation).
+// Output: 1-byte E4M3 codes with UE8M0 scale atoms (fp8_layout.cuh), the
+// operands of the block-scaled FP8 tensor-core GEMMs. For the 128 x 1 slices
+// the atom's rows are the buffer's columns and its K blocks the 128-row
+// blocks of the permuted buffer (the weight gradients reduce over tokens).
 // E4M3 rounding (to nearest even, saturating) uses the hardware conversion.
-#include <cuda_fp16.h>
-
 #include "common.cuh"
 #include "fp8_layout.cuh"
 #include "internal.h"
 
 namespace moe {
-
-__device__ __forceinline__ float e4m3_scale(float amax) {
-  if (!(amax > 0.f)) return 1.f;
-  int e;
-  const float m = frexpf(__fdiv_rn(amax, 448.f), &e);   // amax/448 = m * 2^e
-  return ldexpf(1.f, m == 0.5f ? e - 1 : e);
-}
-
-// E4M3(a / s) * s for two values (s a power of two, so a / s and the product
-// are exact).
-__device__ __forceinline__ void q2(float a, float b, float inv_s, float s, float& qa, float& qb) {
-  uint16_t packed;
-  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(packed) : "f"(b * inv_s), "f"(a * inv_s));
-  uint32_t h2;
-  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(packed));
-  const __half2 hv = *reinterpret_cast<const __half2*>(&h2);
-  qa = __low2float(hv) * s;
-  qb = __high2float(hv) * s;
-}
-
-__device__ __forceinline__ float q1(float a, float inv_s, float s) {
-  float qa, unused;
-  q2(a, 0.f, inv_s, s, qa, unused);
-  return qa;
-}
-
 
 // Whether 128-row block rb of the permuted buffer holds any row a GEMM reads:
 // group g's segment starts at offsets[g], and the GEMMs read its first
@@ -71,26 +39,28 @@ __device__ __forceinline__ bool live_block(const int32_t* __restrict__ offsets,
 }
 
 // 128 x 1 slices: every live 128-row block of [0, offsets[G]) (group segments
-// are multiples of 128 rows, so blocks never straddle two experts). One block
-// of 256 threads per (128-row block, 128-column slab): the 128 x 128 tile is
-// read once into shared memory with 16-byte loads (eight per thread in
-// flight), the column maxima are taken there (two partial maxima of 64 rows
-// per column), and every thread quantises and stores eight 8-column vectors
-// read back from the tile.
+// are multiples of 128 rows, so blocks never straddle two experts) -> E4M3
+// bytes plus the UE8M0 scale atoms [cols / 128][atoms along the rows]. One
+// block of 256 threads per (128-row block, 128-column slab): the 128 x 128
+// tile is read once into shared memory with 16-byte loads (eight per thread
+// in flight), the column maxima are taken there (two partial maxima of 64
+// rows per column), and every thread quantises eight 8-column vectors read
+// back from the tile and stores their codes (8 bytes each).
 __global__ void __launch_bounds__(256)
-quant_cols_kernel(const __nv_bfloat16* __restrict__ X, __nv_bfloat16* __restrict__ Xq,
-                  const int32_t* __restrict__ offsets, const int32_t* __restrict__ counts, int G,
-                  int cols) {
+quant_cols8_kernel(const __nv_bfloat16* __restrict__ X, uint8_t* __restrict__ Xq,
+                   uint8_t* __restrict__ sf, const int32_t* __restrict__ offsets,
+                   const int32_t* __restrict__ counts, int G, int cols, long long kg) {
   extern __shared__ uint4 qc_smem[];
   uint4 (*tile)[16] = reinterpret_cast<uint4 (*)[16]>(qc_smem);   // 128 rows x 128 bf16
   float* part = reinterpret_cast<float*>(qc_smem + 128 * 16);      // [2][128]
-  float* scale = part + 256;                                       // [128]
+  float* inv = part + 256;                                         // [128]
   const long long rblocks = offsets[G] / 128;
   const int slabs = cols >> 7;
   const int tid = threadIdx.x;
   for (long long w = blockIdx.x; w < rblocks * slabs; w += gridDim.x) {
     const long long rb = w / slabs;
-    const int c0 = (int)(w - rb * slabs) * 128;
+    const int cs = (int)(w - rb * slabs);
+    const int c0 = cs * 128;
     if (!live_block(offsets, counts, G, rb)) continue;
     const __nv_bfloat16* src = X + (size_t)rb * 128 * cols + c0;
     {
@@ -116,20 +86,19 @@ quant_cols_kernel(const __nv_bfloat16* __restrict__ X, __nv_bfloat16* __restrict
       part[h * 128 + c] = m;
     }
     __syncthreads();
-    if (tid < 128) scale[tid] = e4m3_scale(fmaxf(part[tid], part[128 + tid]));
+    if (tid < 128) {
+      const uint32_t code = ue8m0_code(fmaxf(part[tid], part[128 + tid]));
+      inv[tid] = ue8m0_inv(code);
+      sf[f8::atom_offset(cs, rb, kg) + f8::atom_byte(tid, (int)rb)] = (uint8_t)code;
+    }
     __syncthreads();
-    __nv_bfloat16* dst = Xq + (size_t)rb * 128 * cols + c0;
+    uint8_t* dst = Xq + (size_t)rb * 128 * cols + c0;
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
       const int v = tid + 256 * i, r = v >> 4, q = v & 15;
-      float f[8], o[8];
+      float f[8];
       unpack8(tile[r][q], f);
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const float sc = scale[q * 8 + j];
-        o[j] = q1(f[j], 1.f / sc, sc);
-      }
-      stg_v4(dst + (size_t)r * cols + q * 8, pack8(o));
+      *reinterpret_cast<uint2*>(dst + (size_t)r * cols + q * 8) = e4m3x8_each(f, inv + q * 8);
     }
     __syncthreads();
   }
@@ -249,13 +218,13 @@ cudaError_t launch_quant_rows8(const void* X, uint8_t* Xq, uint8_t* sf, const in
   return cudaGetLastError();
 }
 
-cudaError_t launch_quant_cols(const void* X, void* Xq, const int32_t* offsets,
-                              const int32_t* counts, int G, int64_t rows_max, int cols,
-                              cudaStream_t s) {
-  constexpr int smem = 128 * 16 * 16 + 3 * 128 * 4;     // tile + two partial maxima + scales
-  quant_cols_kernel<<<grid_cap(rows_max / 128 * (cols / 128), 1), 256, smem, s>>>(
-      static_cast<const __nv_bfloat16*>(X), static_cast<__nv_bfloat16*>(Xq), offsets, counts, G,
-      cols);
+cudaError_t launch_quant_cols8(const void* X, uint8_t* Xq, uint8_t* sf, const int32_t* offsets,
+                               const int32_t* counts, int G, int64_t rows_max, int cols,
+                               cudaStream_t s) {
+  constexpr int smem = 128 * 16 * 16 + 3 * 128 * 4;     // tile + two partial maxima + 1/scales
+  quant_cols8_kernel<<<grid_cap(rows_max / 128 * (cols / 128), 1), 256, smem, s>>>(
+      static_cast<const __nv_bfloat16*>(X), Xq, sf, offsets, counts, G, cols,
+      (long long)f8::atoms_k(rows_max));
   return cudaGetLastError();
 }
 

@@ -69,9 +69,11 @@ def test_fp8_scratch_holds_the_quantised_operands():
     # E4M3 weights with their scale atoms for both orientations (forward, data gradient)
     weights = G * 2 * F * H + G * H * F + atoms(G * 2 * F, H) + atoms(G * H, 2 * F) + \
         atoms(G * H, F) + atoms(G * F, H)
-    # E4M3 x_perm, h, dO, dGU (1x128 slices) with atoms; bf16 values of their 128x1 slices
+    # E4M3 x_perm, h, dO, dGU (1x128 slices) with atoms; the same four in 128x1
+    # slices (atoms: the columns as rows, the buffer's row blocks as K)
     acts = R * H + R * F + R * H + R * 2 * F + atoms(R, H) + atoms(R, F) + atoms(R, H) + \
-        atoms(R, 2 * F) + (R * H + R * F + R * 2 * F + R * H) * 2
+        atoms(R, 2 * F) + R * H + R * F + R * 2 * F + R * H + atoms(H, R) + atoms(F, R) + \
+        atoms(2 * F, R) + atoms(H, R)
     quantised = weights + acts
     # the tensor-core router's region (E % 128 == 0): the larger of W_r as three
     # bf16 parts (forward) and dlogits as three bf16 parts plus the chunk sums of
