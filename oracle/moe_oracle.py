@@ -56,8 +56,13 @@ FP8 (the FP8 configuration): E4M3 values with power-of-two block scales
 scale = 2^ceil(log2(amax/448)), 1 for an all-zero block); activations take
 1x128 blocks along the reduction dimension of the GEMM that consumes them,
 expert weights 128x128 blocks, weight-gradient operands 128x1 blocks along
-the tokens of each expert (quantised from the bf16 tensors). Quantised values
-are exact in bf16 and in fp64, so the GEMMs below multiply them exactly.
+the tokens of each expert (quantised from the bf16 tensors). The MXFP8
+configuration uses 32-element blocks instead (the MX formats' block length)
+for the activations (1x32) and the weight-gradient operands (32x1), and
+quantises each expert weight twice: 1x32 along its input dimension for the
+forward GEMM, 32x1 along its output dimension for the data gradient (the
+dimension each GEMM reduces). Quantised values are exact in bf16 and in fp64,
+so the GEMMs below multiply them exactly.
 
 Rounding: ``round_bf16`` is round-to-nearest-even onto the bf16 grid, written
 from the format (8 exponent bits, 7 stored fraction bits). Pass
@@ -732,13 +737,36 @@ def layer_backward_reordered(cfg, x, W_r, W13, W2, fwd, dY, rounding: bool = Tru
 # --------------------------------------------------------------------------- #
 # the FP8 layer (E4M3 with power-of-two block scales)
 # --------------------------------------------------------------------------- #
+DT_FP8_BLOCK = 1      # 128-element blocks, 128x128 weight tiles
+DT_MXFP8 = 2          # 32-element blocks along the reduced dimension (MX)
+
+
+def fp8_block(cfg) -> int:
+    """Quantisation block length of an FP8 configuration: 32 for MXFP8 (the MX
+    formats share one scale per 32 consecutive elements), else 128."""
+    return 32 if getattr(cfg, "dtype", DT_FP8_BLOCK) == DT_MXFP8 else 128
+
+
+def fp8_weights(cfg, W):
+    """The two E4M3 forms of one expert weight W [out, in]: the forward GEMM's
+    (reduces over `in`) and the data gradient's (reduces over `out`). Block
+    recipe: one 128x128 tile quantisation serves both. MXFP8: 1x32 blocks
+    along `in` for the forward, 32x1 blocks along `out` for the data gradient."""
+    if fp8_block(cfg) == 128:
+        q = quant_tiles(W)
+        return q, q
+    return quant_rows(W, 32), quant_cols(W, 32)
+
+
 def layer_forward_fp8(cfg, x, W_r, bias, W13, W2, logits=None):
     """The layer with its expert GEMMs on E4M3-quantised operands.
 
     Routing stays in fp32 (es summary §2.4: the router keeps high precision).
-    Per expert: X_q = quant_rows(X) (1x128 along H), W13_q/W2_q = quant_tiles
-    (128x128), GU = bf16(X_q W13_q^T), h = bf16(silu(G) U),
-    y = bf16(quant_rows(h) W2_q^T) (1x128 along F); combine as in bf16.
+    Per expert, with b = fp8_block(cfg): X_q = quant_rows(X, b) (1 x b along
+    H), the weights' forward forms (fp8_weights), GU = bf16(X_q W13_q^T),
+    h = bf16(silu(G) U), y = bf16(quant_rows(h, b) W2_q^T) (1 x b along F);
+    combine as in bf16. The data-gradient forms of the weights are kept for
+    the backward (Wd13, Wd2).
     """
     x = np.asarray(x, np.float64)
     T, H = x.shape
@@ -752,34 +780,37 @@ def layer_forward_fp8(cfg, x, W_r, bias, W13, W2, logits=None):
     GU = np.zeros((T, k, 2 * F))
     h = np.zeros((T, k, F))
     y = np.zeros((T, k, H))
-    Wq13, Wq2 = {}, {}
+    b = fp8_block(cfg)
+    Wq13, Wq2, Wd13, Wd2 = {}, {}, {}, {}
     for e in range(E):
         tt, jj = np.nonzero((idx == e) & kept)
         if tt.size == 0:
             continue
         order = np.argsort(tt, kind="stable")            # rows in token order
         tt, jj = tt[order], jj[order]
-        Wq13[e] = quant_tiles(W13[e])
-        Wq2[e] = quant_tiles(W2[e])
-        g, hh = expert_fc1(quant_rows(x[tt]), Wq13[e])
+        Wq13[e], Wd13[e] = fp8_weights(cfg, W13[e])
+        Wq2[e], Wd2[e] = fp8_weights(cfg, W2[e])
+        g, hh = expert_fc1(quant_rows(x[tt], b), Wq13[e])
         GU[tt, jj], h[tt, jj] = g, hh
-        y[tt, jj] = expert_fc2(quant_rows(hh), Wq2[e])
+        y[tt, jj] = expert_fc2(quant_rows(hh, b), Wq2[e])
     acc = np.einsum("tj,tjh->th", np.where(kept, w, 0.0), y)
     return dict(logits=logits, idx=idx, w=w, maps=maps, GU=GU, h=h, y=y, out=round_bf16(acc),
-                Wq13=Wq13, Wq2=Wq2)
+                Wq13=Wq13, Wq2=Wq2, Wd13=Wd13, Wd2=Wd2)
 
 
 def layer_backward_fp8(cfg, x, W_r, W13, W2, fwd, dY):
-    """Backward of layer_forward_fp8. Data gradients: dO and dGU quantised in
-    1x128 slices along the dimension their GEMM reduces (H, 2F), weights as in
-    the forward; weight gradients: both operands quantised in 128x1 slices
-    along the expert's tokens (in token order)."""
+    """Backward of layer_forward_fp8, with b = fp8_block(cfg). Data gradients:
+    dO and dGU quantised in 1 x b slices along the dimension their GEMM reduces
+    (H, 2F), the weights in their data-gradient forms; weight gradients: both
+    operands quantised in b x 1 slices along the expert's tokens (in token
+    order)."""
     x = np.asarray(x, np.float64)
     dY = np.asarray(dY, np.float64)
     T, H = x.shape
     E, k, F = cfg.E, cfg.k, cfg.F
     idx, w, maps = fwd["idx"], fwd["w"], fwd["maps"]
     kept = maps["row_of"] >= 0
+    b = fp8_block(cfg)
     dO = round_bf16(np.where(kept, w, 0.0)[:, :, None] * dY[:, None, :])
     dw = np.where(kept, np.einsum("th,tjh->tj", dY, fwd["y"]), 0.0)
     dGU = np.zeros((T, k, 2 * F))
@@ -792,13 +823,13 @@ def layer_backward_fp8(cfg, x, W_r, W13, W2, fwd, dY):
             continue
         order = np.argsort(tt, kind="stable")
         tt, jj = tt[order], jj[order]
-        Wq13, Wq2 = fwd["Wq13"][e], fwd["Wq2"][e]
+        Wd13, Wd2 = fwd["Wd13"][e], fwd["Wd2"][e]
         dOe = dO[tt, jj]
-        d = expert_fc2_dgrad_swiglu(quant_rows(dOe), Wq2, fwd["GU"][tt, jj])
+        d = expert_fc2_dgrad_swiglu(quant_rows(dOe, b), Wd2, fwd["GU"][tt, jj])
         dGU[tt, jj] = d
-        dX[tt, jj] = expert_fc1_dgrad(quant_rows(d), Wq13)
-        dW2[e] = wgrad(quant_cols(dOe), quant_cols(fwd["h"][tt, jj]))
-        dW13[e] = wgrad(quant_cols(d), quant_cols(x[tt]))
+        dX[tt, jj] = expert_fc1_dgrad(quant_rows(d, b), Wd13)
+        dW2[e] = wgrad(quant_cols(dOe, b), quant_cols(fwd["h"][tt, jj], b))
+        dW13[e] = wgrad(quant_cols(d, b), quant_cols(x[tt], b))
     dlogits = router_dlogits(cfg, fwd["logits"], idx, w, dw)
     dx = round_bf16(dX.sum(axis=1) + dlogits @ np.asarray(W_r, np.float64))
     dW_r = round_f32(dlogits.T @ x)

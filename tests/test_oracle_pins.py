@@ -626,6 +626,72 @@ def test_fp8_single_expert_layer_is_dense_fp8_mlp():
     np.testing.assert_allclose(bwd["dW13"][0], dW13.numpy(), rtol=2 ** -6, atol=1e-4)
 
 
+def test_mx_weight_forms_and_reduction_to_the_block_recipe():
+    """MXFP8: the forward form quantises 1x32 along a weight's input dimension,
+    the data-gradient form 32x1 along its output dimension (= 1x32 rows of the
+    transpose); where every 32-long row and column piece of a 128x128 tile holds
+    the tile's largest magnitude, both equal the 128x128 tile quantisation."""
+    rng = np.random.default_rng(21)
+    W = rng.standard_normal((256, 384)) * 0.02
+    mx = MoEShape("t", T=1, H=384, E=1, k=1, F=128, dtype=O.DT_MXFP8)
+    blk = MoEShape("t", T=1, H=384, E=1, k=1, F=128, dtype=O.DT_FP8_BLOCK)
+    assert O.fp8_block(mx) == 32 and O.fp8_block(blk) == 128
+    f, d = O.fp8_weights(mx, W)
+    np.testing.assert_array_equal(f, O.quant_rows(W, 32))
+    np.testing.assert_array_equal(d, O.quant_rows(W.T, 32).T)
+    for r in range(0, 256, 32):                      # each 1x32 piece on its own
+        s = O.e4m3_scale(np.abs(W[r, 64:96]).max())
+        np.testing.assert_array_equal(f[r, 64:96], O.round_e4m3(W[r, 64:96] / s) * s)
+    # the tile maximum in every 32-long piece: i % 32 == j % 32 inside each tile
+    M = np.abs(W).max() * 3.0
+    ii, jj = np.meshgrid(np.arange(256), np.arange(384), indexing="ij")
+    W2 = np.where(ii % 32 == jj % 32, np.where((ii + jj) % 2 == 0, M, -M), W)
+    f2, d2 = O.fp8_weights(mx, W2)
+    t2, t2d = O.fp8_weights(blk, W2)
+    np.testing.assert_array_equal(t2, t2d)
+    np.testing.assert_array_equal(f2, t2)
+    np.testing.assert_array_equal(d2, t2)
+
+
+def test_mxfp8_single_expert_layer_is_dense_mx_mlp():
+    """One expert, every token routed to it with weight 1: each stage of the
+    MXFP8 layer is the dense SwiGLU MLP's on operands fake-quantised with
+    torch's float8 in 32-long pieces along the GEMM's reduced dimension
+    (weights: along H for FC1 and F for FC2, along 2F and H for the data
+    gradients; tokens for the weight gradients). Each stage starts from the
+    oracle's own bf16 inputs to it, so a one-ulp difference upstream cannot move
+    a block scale downstream."""
+    cfg = MoEShape("t", T=256, H=256, E=1, k=1, F=256, dtype=O.DT_MXFP8)
+    inp = make_inputs(cfg, seed=17)
+    x, Wr, W13, W2, dY = (f64(inp[n]) for n in ("x", "W_r", "W13", "W2", "dY"))
+    # weight columns (input dimension) of magnitudes 2^0..2^7 inside every 32-long
+    # piece, so the 1x32 (forward) and 32x1 (data-gradient) forms differ widely
+    W13 = W13 * 2.0 ** (np.arange(256) % 8)[None, None, :]
+    W2 = W2 * 2.0 ** (np.arange(256) % 8)[None, None, :]
+    fwd = O.layer_forward_fp8(cfg, x, Wr, None, W13, W2)
+    bwd = O.layer_backward_fp8(cfg, x, Wr, W13, W2, fwd, dY)
+    T_ = lambda a: torch.tensor(np.asarray(a, np.float64))  # noqa: E731
+    tx, t13, t2, dO = T_(x), T_(W13[0]), T_(W2[0]), T_(dY)   # weight 1: dO = dY
+    rows = lambda t: _torch_fq(t.view(t.shape[0], -1, 32), (2,)).view(t.shape)  # noqa: E731
+    cols = lambda t: rows(t.T.contiguous()).T  # noqa: E731
+    GU, h, dGU = T_(fwd["GU"][:, 0]), T_(fwd["h"][:, 0]), T_(bwd["dGU"][:, 0])
+    close = lambda got, ref, rt: np.testing.assert_allclose(got, ref.numpy(), rtol=rt, atol=1e-6)  # noqa: E731
+    close(fwd["GU"][:, 0], _torch_bf16(rows(tx) @ rows(t13).T), 2 ** -7)
+    close(fwd["h"][:, 0], _torch_bf16(torch.nn.functional.silu(GU[:, :256]) * GU[:, 256:]), 2 ** -7)
+    close(fwd["out"], _torch_bf16(rows(h) @ rows(t2).T), 2 ** -7)
+    dh = rows(dO) @ cols(t2)
+    G, U = GU[:, :256], GU[:, 256:]
+    sg = torch.sigmoid(G)
+    close(bwd["dGU"][:, 0], _torch_bf16(torch.cat([dh * U * sg * (1 + G * (1 - sg)), dh * G * sg],
+                                                  dim=1)), 2 ** -7)
+    close(bwd["dX"][:, 0], _torch_bf16(rows(dGU) @ cols(t13)), 2 ** -7)
+    close(bwd["dW2"][0], _torch_bf16(cols(dO).T @ cols(h)), 2 ** -7)
+    close(bwd["dW13"][0], _torch_bf16(cols(dGU).T @ cols(tx)), 2 ** -7)
+    # not the block recipe: the 1x32 pieces give a different (finer) result
+    blk = O.layer_forward_fp8(cfg.with_(dtype=O.DT_FP8_BLOCK), x, Wr, None, W13, W2)
+    assert not np.array_equal(blk["out"], fwd["out"])
+
+
 # --------------------------------------------------------------------------- #
 # the routing weight inside the expert (algebraic reordering)
 # --------------------------------------------------------------------------- #
