@@ -146,9 +146,10 @@ def gemm_sources_sha256() -> str:
     return h.hexdigest()
 
 
-def gemm_traffic(workload: str):
+def gemm_traffic(workload: str, key: str = "dram_bytes_per_step"):
     """DRAM bytes per step of the grouped-GEMM launches from a committed ncu
-    capture, or None when a GEMM source changed since it was taken."""
+    capture (`key`: the roofline kernel's launches, or the FP8 weight-gradient
+    stage's), or None when a GEMM source changed since it was taken."""
     path = os.path.join(ROOT, "profiles", "gemm_traffic.json")
     if not os.path.exists(path):
         return None
@@ -156,7 +157,7 @@ def gemm_traffic(workload: str):
         d = json.load(f)
     if d.get("gemm_sources_sha256") != gemm_sources_sha256() or d.get("workload") != workload:
         return None
-    return d.get("dram_bytes_per_step")
+    return d.get(key)
 
 
 def gemm_flops(shape, counts) -> float:
@@ -216,12 +217,18 @@ def stage_table(shape, f, stage_ms, hbm_gbs, fl, tc_peak, bf16_peak):
     P = offsets[G] - sum(counts)         # padding rows
     bf = 2
     maps = T * k * 4 * 3                 # idx / row_of / w sized reads or writes
-    fp8 = shape.dtype == W.DT_FP8
+    fp8 = shape.dtype in W.FP8_DTYPES
+    mx = shape.dtype == W.DT_MXFP8
     wbytes = G * 3 * H * F
+    blk = 32 if mx else 128
     work = [
         ("route", T * H * bf + E * H * 4 + T * E * 4 + 2 * T * k * 4, "router logits + top-k"),
         ("permute", T * H * bf + (rows + P) * H * bf + maps, "hist + rank + row scatter"),
-        ("quantize_weights", (wbytes * bf + wbytes + 2 * wbytes // 32) if fp8 else 0,
+        # bf16 read, E4M3 written (twice for MX: forward and data-gradient
+        # forms); scale bytes: 128 per 128x128 tile for each of the two atom
+        # arrays, or one per 32 elements for each form (MX)
+        ("quantize_weights", (wbytes * bf + (2 * wbytes + wbytes // 16 if mx else
+                                             wbytes + wbytes // 64)) if fp8 else 0,
          "E4M3 weights + UE8M0 scale atoms (FP8 only)"),
         ("grouped_ffn_fwd", fl, "FC1+SwiGLU, FC2 (tcgen05" + (" kind::mxf8f6f4)" if fp8 else ")")),
         ("unpermute", rows * H * bf + T * H * bf + maps, "gather-scale-reduce"),
@@ -231,7 +238,7 @@ def stage_table(shape, f, stage_ms, hbm_gbs, fl, tc_peak, bf16_peak):
         ("grouped_ffn_dgrad", fl, "FC2 dgrad+SwiGLU bwd, FC1 dgrad (tcgen05"
          + (" kind::mxf8f6f4)" if fp8 else ")")),
         ("grouped_ffn_wgrad", fl, "dW2, dW13 (tcgen05"
-         + (" kind::mxf8f6f4, with their four 128x1 quantisers)" if fp8 else " bf16)")),
+         + (f" kind::mxf8f6f4, with their four {blk}x1 quantisers)" if fp8 else " bf16)")),
         ("permute_bwd", rows * H * bf + T * H * bf + maps, "dx gather-reduce"),
         ("router_wgrad", T * H * bf + E * H * 4 + T * E * 4, "dW_r (each x row once)"),
     ]
@@ -277,7 +284,8 @@ def run_ours(args, rank, world, local):
     stream = torch.cuda.current_stream(dev)
     sc = bufs.scratch
 
-    fp8 = shape.dtype == W.DT_FP8
+    fp8 = shape.dtype in W.FP8_DTYPES
+    mx = shape.dtype == W.DT_MXFP8
     reord = bool(shape.weights_in_expert)
 
     def step(ev=None):
@@ -340,12 +348,13 @@ def run_ours(args, rank, world, local):
     # combine bwd, route bwd, the four backward GEMMs, dispatch bwd, router wgrad
     # (on the tensor-core path: dlogits split, GEMM, chunk sum); the FP8 mode adds
     # the two weight quantisers, 2 activation quantisers forward, 2 in the data
-    # gradients and 4 in the weight gradients
+    # gradients and 4 in the weight gradients (MXFP8: x_perm, h and dO are
+    # quantised by passes of their own, three more)
     tc_router = shape.E >= 128 and shape.E % 128 == 0
     launches_per_step = ((3 if tc_router else 2) + 3 + 2 + 1 + 1 + 1 + 4 + 1
                          + (3 if tc_router else 1))
     if fp8:
-        launches_per_step += 2 + 2 + 2 + 4
+        launches_per_step += 2 + 2 + 2 + 4 + (3 if mx else 0)
     if reord:
         launches_per_step += 2          # row weights, dw reduction
     for _ in range(max(args.warmup, 3)):
@@ -448,12 +457,13 @@ def run_ours(args, rank, world, local):
     if fp8:
         gemm_ms = sm["grouped_ffn_fwd"] + sm["grouped_ffn_dgrad"]
         gemm_fl = 2 * fl
-        kern = ("grouped_gemm_fp8_kernel (tcgen05 kind::mxf8f6f4, E4M3 x UE8M0 128-blocks: FC1+"
-                "SwiGLU, FC2, FC2 dgrad+SwiGLU bwd, FC1 dgrad)")
+        kern = (f"grouped_gemm_fp8_kernel (tcgen05 kind::mxf8f6f4, E4M3 x UE8M0 "
+                f"{32 if mx else 128}-blocks: FC1+SwiGLU, FC2, FC2 dgrad+SwiGLU bwd, FC1 dgrad)")
         peak_src = (f"{src}: 2 x bf16_tflops (the nominal FP8:bf16 dense rate ratio; no FP8 "
                     "figure is measured)")
         gemm_note = ("time of the grouped_ffn_fwd and grouped_ffn_dgrad stages, which also hold "
-                     "the activation quantisers (x_perm, h, dO, dGU)")
+                     "the activation quantisers (h and dGU; MXFP8 also x_perm's and dO's "
+                     "passes run in the dispatch and combine-backward stages)")
     else:
         gemm_ms = sm["grouped_ffn_fwd"] + sm["grouped_ffn_dgrad"] + sm["grouped_ffn_wgrad"]
         gemm_fl = 3 * fl
@@ -463,7 +473,7 @@ def run_ours(args, rank, world, local):
     achieved = gemm_fl / (gemm_ms * 1e-3) / 1e12
     tokens = T * args.steps * world
     cf = shape.capacity_factor
-    dt_name = "fp8_e4m3_block" if fp8 else "bf16"
+    dt_name = ("mxfp8_e4m3_32" if mx else "fp8_e4m3_block") if fp8 else "bf16"
     res = {
         "metric": "MoE-layer tokens/s fwd+bwd on 1 GB300",
         "value": tokens / (ms * 1e-3),
@@ -476,11 +486,15 @@ def run_ours(args, rank, world, local):
         "scaling": "weak",
         "vs_baseline": None,
         "dtype": dt_name,
-        "dtype_detail": ("E4M3 operands with UE8M0 power-of-two scales per 128x128 weight tile, "
-                         "1x128 activation slice along K (forward and data gradients) and 128x1 "
-                         "slice along the tokens (weight gradients); all six expert GEMMs on the "
-                         "block-scaled FP8 tensor cores with fp32 accumulation; router fp32; "
-                         "activations and outputs bf16"
+        "dtype_detail": (("E4M3 operands with one UE8M0 power-of-two scale per 32 elements (MX): "
+                          "1x32 along K for activations, each weight in two forms (1x32 along K "
+                          "for the forward, 32x1 for the data gradients), 32x1 along the tokens "
+                          "for the weight gradients" if mx else
+                          "E4M3 operands with UE8M0 power-of-two scales per 128x128 weight tile, "
+                          "1x128 activation slice along K (forward and data gradients) and "
+                          "128x1 slice along the tokens (weight gradients)")
+                         + "; all six expert GEMMs on the block-scaled FP8 tensor cores with "
+                         "fp32 accumulation; router fp32; activations and outputs bf16"
                          if fp8 else "bf16 operands, fp32 accumulation, fp32 router"),
         "data": "synthetic (seeded N(0,1) tokens, N(0,0.02^2) weights; no dataset)",
         "config": {"workload": f"{shape.name}: T={T} H={H} E={E}(+{S} shared) top-{shape.k} "
@@ -496,8 +510,9 @@ def run_ours(args, rank, world, local):
         "roofline": {"kernel": kern, "bound": "tensor", "achieved": achieved, "peak": tc_peak,
                      "unit": "TFLOP/s", "frac": achieved / tc_peak, "peak_source": peak_src,
                      "traffic": gemm_traffic(shape.name),
-                     "traffic_note": "DRAM bytes of the grouped-GEMM launches of one step "
-                                     "(ncu dram__bytes_read+write); achieved is per step too",
+                     "traffic_note": "DRAM bytes of this kernel's launches in one step "
+                                     "(ncu dram__bytes_read+write, profiles/gemm_traffic.json); "
+                                     "achieved is per step too",
                      "gemm_ms_per_step": gemm_ms, "gemm_time_note": gemm_note,
                      "gemm_tflop_per_step": gemm_fl / 1e12,
                      "frac_of_sustained": achieved / (2.0 * pk.get("bf16_tflops_sustained",
@@ -519,6 +534,7 @@ def run_ours(args, rank, world, local):
             "bound": "hbm", "achieved": wb / (wms * 1e-3) / 1e9, "peak": pk["hbm_gbs"],
             "unit": "GB/s", "frac": wb / (wms * 1e-3) / 1e9 / pk["hbm_gbs"],
             "bytes_per_step": wb, "ms_per_step": wms,
+            "traffic": gemm_traffic(shape.name, "wgrad_stage_dram_bytes_per_step"),
             "tflops": fl / (wms * 1e-3) / 1e12,
             "note": "of measured copy bandwidth; the stage writes the weight gradients "
                     f"({G * 3 * H * F * 2 / 1e9:.2f} GB bf16), and this part's write-only rate "
@@ -578,7 +594,7 @@ def oracle_sample(o: dict) -> float:
     for t in range(sub.T):
         for e in idx[t]:
             lg_sub[t, o["pos"][int(e)]] = score[t, int(e)]
-    if shape.dtype == W.DT_FP8:
+    if shape.dtype in W.FP8_DTYPES:
         fwd = O.layer_forward_fp8(sub, o["x"], o["W_r_sub"], None, o["W13"], o["W2"], logits=lg_sub)
         O.layer_backward_fp8(sub, o["x"], o["W_r_sub"], o["W13"], o["W2"], fwd, o["dY"])
     else:
@@ -592,7 +608,7 @@ def sample_text(o: dict, steps: int = 1) -> str:
     return (f"first {o['n']} tokens of {sh.name} ({len(o['experts'])} of {sh.E} experts "
             f"selected), {steps} pass(es): router logits over all experts, selection, then "
             "fwd+bwd of the selected experts incl. their weight gradients"
-            + (" (FP8 layer functions)" if sh.dtype == W.DT_FP8 else "") + ", fp64 numpy")
+            + (" (FP8 layer functions)" if sh.dtype in W.FP8_DTYPES else "") + ", fp64 numpy")
 
 
 def cpu_cores() -> int:

@@ -75,8 +75,14 @@ enum { MOE_GROUP_TOP2_SUM = 0, MOE_GROUP_MAX = 1 };
  * (moe_query_sizes counts them), and the scratch used by a forward must be
  * passed unchanged to its backward. Shared experts are not supported in this
  * mode (n_shared must be 0), and H and F must be multiples of 256
- * (MOE_ERR_UNSUPPORTED otherwise). */
-enum { MOE_DTYPE_BF16 = 0, MOE_DTYPE_FP8_E4M3_BLOCK = 1 };
+ * (MOE_ERR_UNSUPPORTED otherwise).
+ * MOE_DTYPE_MXFP8: the same with the MX formats' 32-element blocks (the MXFP8
+ * recipe the es summary §2.4 names for Blackwell): activations in 1x32 slices
+ * along the reduced dimension, weight-gradient operands in 32x1 slices along
+ * the tokens, and each expert weight quantised twice -- 1x32 along its input
+ * dimension for the forward GEMMs and 32x1 along its output dimension for the
+ * data gradients (scratch holds both forms). Same restrictions. */
+enum { MOE_DTYPE_BF16 = 0, MOE_DTYPE_FP8_E4M3_BLOCK = 1, MOE_DTYPE_MXFP8 = 2 };
 
 /* One layer configuration. */
 typedef struct moe_config {
@@ -87,7 +93,7 @@ typedef struct moe_config {
     int32_t topk_groups;     /* groups kept per token                           */
     int32_t group_score;     /* MOE_GROUP_TOP2_SUM | MOE_GROUP_MAX              */
     float route_scale;       /* sigmoid weights: route_scale * s_j / sum s      */
-    int32_t dtype;           /* MOE_DTYPE_BF16 | MOE_DTYPE_FP8_E4M3_BLOCK        */
+    int32_t dtype;           /* MOE_DTYPE_BF16 | _FP8_E4M3_BLOCK | _MXFP8         */
     float capacity_factor;   /* 0 = dropless; else C = ceil(cf*T*k/E) rows      */
     int32_t row_align;       /* every expert segment is a multiple of this (128)*/
     int32_t weights_in_expert; /* 1: the routing weight scales h inside the

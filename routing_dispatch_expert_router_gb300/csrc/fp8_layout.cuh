@@ -12,6 +12,12 @@
 // the MMA then finds the scale of row r in column c + (r % 128) / 32, lane
 // r % 32, byte kb % 4 (the byte picked by the instruction's scale-factor id).
 // Atoms are stored [row block][atom along K]; a UE8M0 byte e means 2^(e-127).
+//
+// MX layout (the MXFP8 configuration: one scale per 32 consecutive K
+// elements): one atom per 128 rows and ONE 128-wide K block; byte
+// atom_byte(r, j) holds the scale of the j-th 32-wide piece of that K block,
+// and the MMA of K slice j (scale_vec::1X, K = 32) selects it with its
+// scale-factor id j.
 #pragma once
 
 #include <cuda_runtime.h>
@@ -38,6 +44,22 @@ __host__ __device__ constexpr int64_t atom_offset(int64_t rb, int64_t kb, int64_
 // bytes of the scale atoms of a rows x K operand (rows a multiple of 128)
 __host__ __device__ constexpr int64_t sf_bytes(int64_t rows, int64_t K) {
   return rows / 128 * atoms_k(K) * kAtomBytes;
+}
+
+// MX layout: atom of (row block rb, K block kb), KB = K / 128
+__host__ __device__ constexpr int64_t mx_atom_offset(int64_t rb, int64_t kb, int64_t KB) {
+  return (rb * KB + kb) * kAtomBytes;
+}
+__host__ __device__ constexpr int64_t mx_sf_bytes(int64_t rows, int64_t K) {
+  return rows / 128 * (K / kBlock) * kAtomBytes;
+}
+// atoms per 128-row block along K, and the scale bytes of a rows x K operand,
+// in either layout
+__host__ __device__ constexpr int64_t sf_stride(int64_t K, bool mx) {
+  return mx ? K / kBlock : atoms_k(K);
+}
+__host__ __device__ constexpr int64_t sf_bytes_of(int64_t rows, int64_t K, bool mx) {
+  return mx ? mx_sf_bytes(rows, K) : sf_bytes(rows, K);
 }
 
 }  // namespace f8

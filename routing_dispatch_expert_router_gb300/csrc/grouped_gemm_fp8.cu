@@ -10,7 +10,9 @@
 // 32-deep K slice (scale_vec::1X), so the four slices of a 128-wide K block
 // read the same scale byte (fp8_layout.cuh). Products and fp32 accumulation
 // happen in the tensor core; only the summation order differs from the fp64
-// reference.
+// reference. The MXFP8 configuration (MX = 1) gives every 32-wide K slice its
+// own scale (MX atom layout: one atom per 128-wide K block, the slice's byte
+// picked by the MMA's scale-factor id).
 //
 // All six expert GEMMs: the row-grouped ones (forward FC1 + SwiGLU, FC2, the
 // two data gradients; M = a group's rows, K = H or F) and the two weight
@@ -98,7 +100,7 @@ __device__ __forceinline__ const uint32_t (&slice32(const uint32_t (&r)[128], in
   return *reinterpret_cast<const uint32_t(*)[32]>(&r[32 * i]);
 }
 
-template <int EPI, int B_MN>
+template <int EPI, int B_MN, int MX>
 __global__ void __launch_bounds__(kF8Threads, 1)
 grouped_gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmA,
                         const __grid_constant__ CUtensorMap tmB,
@@ -227,7 +229,9 @@ grouped_gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmA,
             ptx::tma_load_2d(sB + 16384, &tmB, fb, b1, brow);
           }
           const uint32_t sfs = sf_u + stage * kF8SfStage;
-          const int64_t a4 = (int64_t)(k0 / kF8BK / f8::kAtomKBlocks) * f8::kAtomBytes;
+          // the atom of this K block: one per K block (MX) or per four
+          const int64_t a4 = (int64_t)(MX ? k0 / kF8BK : k0 / kF8BK / f8::kAtomKBlocks) *
+                             f8::kAtomBytes;
           ptx::bulk_load(sfs, sfa + a4, f8::kAtomBytes, fb);
           ptx::bulk_load(sfs + f8::kAtomBytes, sfb0 + a4, f8::kAtomBytes, fb);
           ptx::bulk_load(sfs + 2 * f8::kAtomBytes, sfb1 + a4, f8::kAtomBytes, fb);
@@ -281,9 +285,9 @@ grouped_gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmA,
           ptx::tmem_cp_32x128b_warpx4(sfa_t, ptx::smem_desc_sf(sfs));
           ptx::tmem_cp_32x128b_warpx4(sfb_t, ptx::smem_desc_sf(sfs + f8::kAtomBytes));
           ptx::tmem_cp_32x128b_warpx4(sfb_t + 4, ptx::smem_desc_sf(sfs + 2 * f8::kAtomBytes));
-          // the scale byte of this K block inside its atom (K blocks counted
+          // the scale byte inside the atom: this K block's (K blocks counted
           // from the start of the operand: the buffer's row blocks for the
-          // weight gradients)
+          // weight gradients), or (MX) the 32-wide slice's
           const uint32_t idesc = ptx::idesc_with_sf_id(IDESC, (uint32_t)(kb0 + kb) & 3u);
           const uint32_t sA = base + stage * kF8Stage;
           const uint32_t sB = sA + kF8ABytes;
@@ -293,7 +297,8 @@ grouped_gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmA,
                                       : ptx::smem_desc_sw128(sA + kk * 32, 16, 1024);
             const uint64_t bd = B_MN ? ptx::smem_desc_sw128(sB + kk * 4096, 16384, 1024)
                                      : ptx::smem_desc_sw128(sB + kk * 32, 16, 1024);
-            ptx::mma_mxf8(tmem_base, ad, bd, idesc, sfa_t, sfb_t, (kb | kk) ? 1u : 0u);
+            const uint32_t id = MX ? ptx::idesc_with_sf_id(IDESC, (uint32_t)kk) : idesc;
+            ptx::mma_mxf8(tmem_base, ad, bd, id, sfa_t, sfb_t, (kb | kk) ? 1u : 0u);
           }
           issued = true;
           ptx::mma_commit(bar_empty + 8 * stage);
@@ -398,7 +403,7 @@ grouped_gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmA,
           f8_store_box(&tmC, stage, stage_u32, lane, uo, p.F + f0 + 32 * c, row0);    // U
           f8_store_box(&tmC2, stage, stage_u32, lane, ho[c], f0 + 32 * c, row0);      // h
         }
-        if (p.qout) {
+        if (!MX && p.qout) {
           // h's 1 x 128 slice (columns nt*128 ..) is this warp's 64 columns and
           // its partner's: exchange the row maxima, then write the E4M3 codes
           float m = 0.f;
@@ -523,10 +528,10 @@ grouped_gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmA,
   }
 }
 
-template <int EPI, int B_MN>
-static cudaError_t run_fp8(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& c,
-                           const CUtensorMap& c2, const Params& p, cudaStream_t s) {
-  auto kern = grouped_gemm_fp8_kernel<EPI, B_MN>;
+template <int EPI, int B_MN, int MX>
+static cudaError_t run_fp8_t(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& c,
+                             const CUtensorMap& c2, const Params& p, cudaStream_t s) {
+  auto kern = grouped_gemm_fp8_kernel<EPI, B_MN, MX>;
   constexpr int smem = F8Cfg<EPI>::SMEM;
   static bool attr_set = false;
   if (!attr_set) {
@@ -537,6 +542,16 @@ static cudaError_t run_fp8(const CUtensorMap& a, const CUtensorMap& b, const CUt
   kern<<<num_sms(), kF8Threads, smem, s>>>(a, b, c, c2, p);
   return cudaGetLastError();
 }
+
+template <int EPI, int B_MN>
+static cudaError_t run_fp8(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& c,
+                           const CUtensorMap& c2, const Params& p, bool mx, cudaStream_t s) {
+  return mx ? run_fp8_t<EPI, B_MN, 1>(a, b, c, c2, p, s) : run_fp8_t<EPI, B_MN, 0>(a, b, c, c2, p, s);
+}
+
+static bool is_mx(const moe_config& c) { return c.dtype == MOE_DTYPE_MXFP8; }
+// atoms per 128-row block of a K-long operand
+static int sf_kg(const moe_config& c, int64_t K) { return (int)f8::sf_stride(K, is_mx(c)); }
 
 }  // namespace gg
 
@@ -558,14 +573,14 @@ cudaError_t launch_ffn_fc1_fp8(const moe_config& c, const uint8_t* xq, const uin
   p.K = c.H;
   p.b_rows = 2 * c.F;
   p.sfa = xsf;
-  p.sfa_kg = (int)f8::atoms_k(c.H);
+  p.sfa_kg = sf_kg(c, c.H);
   p.sfb = W13sf;
   p.sfb_nb = 2 * c.F / 128;
-  p.sfb_kg = (int)f8::atoms_k(c.H);
-  p.qout = hq;
+  p.sfb_kg = sf_kg(c, c.H);
+  p.qout = is_mx(c) ? nullptr : hq;         // MX: h is quantised by its own pass
   p.qsf = hsf;
-  p.qsf_kg = (int)f8::atoms_k(c.F);
-  return run_fp8<kEpiSwigluFwd, 0>(a, b, oc, oc2, p, s);
+  p.qsf_kg = sf_kg(c, c.F);
+  return run_fp8<kEpiSwigluFwd, 0>(a, b, oc, oc2, p, is_mx(c), s);
 }
 
 // FC2: y_perm = h_q W2_q^T (bf16).
@@ -584,11 +599,11 @@ cudaError_t launch_ffn_fc2_fp8(const moe_config& c, const uint8_t* hq, const uin
   p.K = c.F;
   p.b_rows = c.H;
   p.sfa = hsf;
-  p.sfa_kg = (int)f8::atoms_k(c.F);
+  p.sfa_kg = sf_kg(c, c.F);
   p.sfb = W2sf;
   p.sfb_nb = c.H / 128;
-  p.sfb_kg = (int)f8::atoms_k(c.F);
-  return run_fp8<kEpiStore, 0>(a, b, oc, oc, p, s);
+  p.sfb_kg = sf_kg(c, c.F);
+  return run_fp8<kEpiStore, 0>(a, b, oc, oc, p, is_mx(c), s);
 }
 
 // FC2 data gradient + SwiGLU backward: dh = dO_q W2_q (fp32, W2 read
@@ -610,11 +625,11 @@ cudaError_t launch_ffn_fc2_dgrad_fp8(const moe_config& c, const uint8_t* dOq, co
   p.aux = static_cast<const __nv_bfloat16*>(GU);
   p.ldaux = 2LL * c.F;
   p.sfa = dOsf;
-  p.sfa_kg = (int)f8::atoms_k(c.H);
+  p.sfa_kg = sf_kg(c, c.H);
   p.sfb = W2sf_t;
   p.sfb_nb = c.F / 128;
-  p.sfb_kg = (int)f8::atoms_k(c.H);
-  return run_fp8<kEpiSwigluBwd, 1>(a, b, oc, oc, p, s);
+  p.sfb_kg = sf_kg(c, c.H);
+  return run_fp8<kEpiSwigluBwd, 1>(a, b, oc, oc, p, is_mx(c), s);
 }
 
 // FC1 data gradient: dX_perm = bf16(dGU_q W13_q + the row's router term)
@@ -641,11 +656,11 @@ cudaError_t launch_ffn_fc1_dgrad_fp8(const moe_config& c, const uint8_t* dGq, co
   p.router_E = c.E;
   p.router_T = c.T;
   p.sfa = dGsf;
-  p.sfa_kg = (int)f8::atoms_k(2LL * c.F);
+  p.sfa_kg = sf_kg(c, 2LL * c.F);
   p.sfb = W13sf_t;
   p.sfb_nb = c.H / 128;
-  p.sfb_kg = (int)f8::atoms_k(2LL * c.F);
-  return run_fp8<kEpiDgradRouter, 1>(a, b, oc, oc, p, s);
+  p.sfb_kg = sf_kg(c, 2LL * c.F);
+  return run_fp8<kEpiDgradRouter, 1>(a, b, oc, oc, p, is_mx(c), s);
 }
 
 // Weight gradients (K = each group's rows, both operands MN-major from their
@@ -667,10 +682,10 @@ cudaError_t launch_ffn_wgrad_fc2_fp8(const moe_config& c, const uint8_t* dOq, co
   p.K = 0;
   p.n_fast = p.Mw > p.N;
   p.sfa = dOsf;
-  p.sfa_kg = (int)f8::atoms_k(R);
+  p.sfa_kg = sf_kg(c, R);
   p.sfb = hsf;
-  p.sfb_kg = (int)f8::atoms_k(R);
-  return run_fp8<kEpiWgrad, 1>(a, b, oc, oc, p, s);
+  p.sfb_kg = sf_kg(c, R);
+  return run_fp8<kEpiWgrad, 1>(a, b, oc, oc, p, is_mx(c), s);
 }
 
 // dW13[g] = dGU_q^T x_q (M = 2F, N = H).
@@ -690,10 +705,10 @@ cudaError_t launch_ffn_wgrad_fc1_fp8(const moe_config& c, const uint8_t* dGq, co
   p.K = 0;
   p.n_fast = p.Mw > p.N;
   p.sfa = dGsf;
-  p.sfa_kg = (int)f8::atoms_k(R);
+  p.sfa_kg = sf_kg(c, R);
   p.sfb = xsf;
-  p.sfb_kg = (int)f8::atoms_k(R);
-  return run_fp8<kEpiWgrad, 1>(a, b, oc, oc, p, s);
+  p.sfb_kg = sf_kg(c, R);
+  return run_fp8<kEpiWgrad, 1>(a, b, oc, oc, p, is_mx(c), s);
 }
 
 }  // namespace moe

@@ -90,19 +90,26 @@ int64_t aux_partial_offset(const moe_config& c);   // its byte offset in scratch
 // weight gradients, the dequantised values of 128x1 slices along the tokens.
 cudaError_t launch_quant_tiles8(const void* W, uint8_t* Wq, uint8_t* sf_f, uint8_t* sf_d, int G,
                                 int rows, int cols, cudaStream_t s);
+// mx: 32-element blocks and the MX atom layout (MXFP8), else 128.
 cudaError_t launch_quant_rows8(const void* X, uint8_t* Xq, uint8_t* sf, const int32_t* offsets,
                                const int32_t* counts, int G, int64_t rows_max, int cols,
-                               cudaStream_t s);
+                               cudaStream_t s, bool mx = false);
 cudaError_t launch_quant_cols8(const void* X, uint8_t* Xq, uint8_t* sf, const int32_t* offsets,
                                const int32_t* counts, int G, int64_t rows_max, int cols,
-                               cudaStream_t s);
+                               cudaStream_t s, bool mx = false);
+// MXFP8 weights: forward (1x32 along cols) and data-gradient (32x1 along rows) forms.
+cudaError_t launch_quant_wmx(const void* W, uint8_t* Wf, uint8_t* Wd, uint8_t* sf_f, uint8_t* sf_d,
+                             int G, int rows, int cols, cudaStream_t s);
 
 // Where the FP8 mode keeps its quantised tensors inside `scratch`.
 struct Fp8Scratch {
-  uint8_t* W13q;    // [G,2F,H] E4M3
+  bool mx;          // MXFP8: 32-element blocks, MX atom layout, two weight forms
+  uint8_t* W13q;    // [G,2F,H] E4M3 (forward form)
+  uint8_t* W13qd;   // data-gradient form (MX), else W13q
   uint8_t* W13sf;   // atoms, N = W13 rows, K = H (forward)
   uint8_t* W13sft;  // atoms, N = H, K = W13 rows (FC1 data gradient)
-  uint8_t* W2q;     // [G,H,F] E4M3
+  uint8_t* W2q;     // [G,H,F] E4M3 (forward form)
+  uint8_t* W2qd;    // data-gradient form (MX), else W2q
   uint8_t* W2sf;    // atoms, N = H, K = F (forward)
   uint8_t* W2sft;   // atoms, N = F, K = H (FC2 data gradient)
   uint8_t* xq;      // [R,H] x_perm, 1x128 slices

@@ -57,20 +57,27 @@ static int64_t base_scratch_bytes(const moe_config& c) {
   return aux_partial_offset(c) + aux_partial_bytes(c);
 }
 
-// The FP8 mode's region of scratch, in order: the E4M3 weights with their
-// scale atoms for both orientations, the 1-byte activations (x_perm, h, dO,
-// dGU in 1x128 slices) with their atoms, and the 1-byte weight-gradient
-// operands (dO, h, dGU, x_perm in 128x1 slices) with theirs.
+static bool is_fp8(const moe_config& c) {
+  return c.dtype == MOE_DTYPE_FP8_E4M3_BLOCK || c.dtype == MOE_DTYPE_MXFP8;
+}
+
+// The FP8 modes' region of scratch, in order: the E4M3 weights (the MXFP8
+// mode's second, data-gradient form after each) with their scale atoms for
+// both orientations, the 1-byte activations (x_perm, h, dO, dGU in slices
+// along each row) with their atoms, and the 1-byte weight-gradient operands
+// (dO, h, dGU, x_perm in slices along the tokens) with theirs.
 static int64_t fp8_region(const moe_config& c, Fp8Scratch* f, uint8_t* p) {
-  constexpr int kRegions = 22;
+  constexpr int kRegions = 24;
   const int64_t G = c.E + c.n_shared, R = rows_max(c), H = c.H, F = c.F;
+  const bool mx = c.dtype == MOE_DTYPE_MXFP8;
+  auto sfb = [mx](int64_t rows, int64_t K) { return f8::sf_bytes_of(rows, K, mx); };
   const int64_t sizes[kRegions] = {
-      G * 2 * F * H, f8::sf_bytes(G * 2 * F, H), f8::sf_bytes(G * H, 2 * F),
-      G * H * F,     f8::sf_bytes(G * H, F),     f8::sf_bytes(G * F, H),
-      R * H, f8::sf_bytes(R, H), R * F, f8::sf_bytes(R, F),
-      R * H, f8::sf_bytes(R, H), R * 2 * F, f8::sf_bytes(R, 2 * F),
-      R * H, f8::sf_bytes(H, R), R * F, f8::sf_bytes(F, R),
-      R * 2 * F, f8::sf_bytes(2 * F, R), R * H, f8::sf_bytes(H, R)};
+      G * 2 * F * H, mx ? G * 2 * F * H : 0, sfb(G * 2 * F, H), sfb(G * H, 2 * F),
+      G * H * F,     mx ? G * H * F : 0,     sfb(G * H, F),     sfb(G * F, H),
+      R * H, sfb(R, H), R * F, sfb(R, F),
+      R * H, sfb(R, H), R * 2 * F, sfb(R, 2 * F),
+      R * H, sfb(H, R), R * F, sfb(F, R),
+      R * 2 * F, sfb(2 * F, R), R * H, sfb(H, R)};
   uint8_t* ptrs[kRegions];
   int64_t off = 0;
   for (int i = 0; i < kRegions; ++i) {
@@ -78,28 +85,31 @@ static int64_t fp8_region(const moe_config& c, Fp8Scratch* f, uint8_t* p) {
     off += align256(sizes[i]);
   }
   if (f) {
+    f->mx = mx;
     f->W13q = ptrs[0];
-    f->W13sf = ptrs[1];
-    f->W13sft = ptrs[2];
-    f->W2q = ptrs[3];
-    f->W2sf = ptrs[4];
-    f->W2sft = ptrs[5];
-    f->xq = ptrs[6];
-    f->xsf = ptrs[7];
-    f->hq = ptrs[8];
-    f->hsf = ptrs[9];
-    f->dOq = ptrs[10];
-    f->dOsf = ptrs[11];
-    f->dGq = ptrs[12];
-    f->dGsf = ptrs[13];
-    f->cHq = ptrs[14];
-    f->cHsf = ptrs[15];
-    f->bFq = ptrs[16];
-    f->bFsf = ptrs[17];
-    f->d2Fq = ptrs[18];
-    f->d2Fsf = ptrs[19];
-    f->aHq = ptrs[20];
-    f->aHsf = ptrs[21];
+    f->W13qd = mx ? ptrs[1] : ptrs[0];
+    f->W13sf = ptrs[2];
+    f->W13sft = ptrs[3];
+    f->W2q = ptrs[4];
+    f->W2qd = mx ? ptrs[5] : ptrs[4];
+    f->W2sf = ptrs[6];
+    f->W2sft = ptrs[7];
+    f->xq = ptrs[8];
+    f->xsf = ptrs[9];
+    f->hq = ptrs[10];
+    f->hsf = ptrs[11];
+    f->dOq = ptrs[12];
+    f->dOsf = ptrs[13];
+    f->dGq = ptrs[14];
+    f->dGsf = ptrs[15];
+    f->cHq = ptrs[16];
+    f->cHsf = ptrs[17];
+    f->bFq = ptrs[18];
+    f->bFsf = ptrs[19];
+    f->d2Fq = ptrs[20];
+    f->d2Fsf = ptrs[21];
+    f->aHq = ptrs[22];
+    f->aHsf = ptrs[23];
   }
   return off;
 }
@@ -109,7 +119,7 @@ static int64_t fp8_region(const moe_config& c, Fp8Scratch* f, uint8_t* p) {
 // products per row and n-tile.
 static int64_t reorder_offset(const moe_config& c) {
   int64_t b = base_scratch_bytes(c);
-  if (c.dtype == MOE_DTYPE_FP8_E4M3_BLOCK) b += fp8_region(c, nullptr, nullptr);
+  if (is_fp8(c)) b += fp8_region(c, nullptr, nullptr);
   return b;
 }
 
@@ -151,9 +161,8 @@ moe_status check_config(const moe_config* c) {
   if (!(c->capacity_factor >= 0.f) || !isfinite(c->capacity_factor)) return MOE_ERR_INVALID_ARG;
   if (!isfinite(c->route_scale)) return MOE_ERR_INVALID_ARG;
   if (c->row_align < 128 || c->row_align % 128) return MOE_ERR_INVALID_ARG;
-  if (c->dtype != MOE_DTYPE_BF16 && c->dtype != MOE_DTYPE_FP8_E4M3_BLOCK)
-    return MOE_ERR_INVALID_ARG;
-  if (c->dtype == MOE_DTYPE_FP8_E4M3_BLOCK && (c->n_shared != 0 || c->H % 256 || c->F % 256))
+  if (c->dtype != MOE_DTYPE_BF16 && !is_fp8(*c)) return MOE_ERR_INVALID_ARG;
+  if (is_fp8(*c) && (c->n_shared != 0 || c->H % 256 || c->F % 256))
     return MOE_ERR_UNSUPPORTED;
   if (c->weights_in_expert != 0 && c->weights_in_expert != 1) return MOE_ERR_INVALID_ARG;
   if (c->weights_in_expert && c->dtype != MOE_DTYPE_BF16) return MOE_ERR_UNSUPPORTED;
@@ -287,11 +296,17 @@ moe_status moe_permute(const moe_config* cfg, const void* x, const int32_t* idx,
   MOE_REQUIRE(al4(token_of) && al4(sel_offsets) && tok4(cfg, sel_tokens) && al16(x_perm));
   MOE_REQUIRE(al16(scratch));
   Fp8Scratch q;
-  const bool fp8 = cfg->dtype == MOE_DTYPE_FP8_E4M3_BLOCK;
+  const bool fp8 = is_fp8(*cfg);
   if (fp8) q = fp8_scratch(*cfg, scratch);
+  cudaStream_t s = (cudaStream_t)stream;
+  // the block recipe writes x_perm's 1x128 E4M3 form in the scatter itself;
+  // MXFP8's 1x32 form is a pass of its own
   MOE_CUDA(launch_permute(*cfg, x, idx, counts, offsets, row_of, token_of, sel_offsets,
-                          sel_tokens, x_perm, static_cast<uint8_t*>(scratch),
-                          (cudaStream_t)stream, fp8 ? &q : nullptr));
+                          sel_tokens, x_perm, static_cast<uint8_t*>(scratch), s,
+                          fp8 && !q.mx ? &q : nullptr));
+  if (fp8 && q.mx)
+    MOE_CUDA(launch_quant_rows8(x_perm, q.xq, q.xsf, offsets, counts, cfg->E + cfg->n_shared,
+                                rows_max(*cfg), cfg->H, s, true));
   return MOE_OK;
 }
 
@@ -299,10 +314,15 @@ moe_status moe_quantize_weights(const moe_config* cfg, const void* W13, const vo
                                 void* scratch, void* stream) {
   MOE_TRY(check_config(cfg));
   MOE_REQUIRE(al16(W13) && al16(W2) && al16(scratch));
-  if (cfg->dtype != MOE_DTYPE_FP8_E4M3_BLOCK) return MOE_OK;
+  if (!is_fp8(*cfg)) return MOE_OK;
   cudaStream_t s = (cudaStream_t)stream;
   const Fp8Scratch q = fp8_scratch(*cfg, scratch);
   const int G = cfg->E + cfg->n_shared;
+  if (q.mx) {
+    MOE_CUDA(launch_quant_wmx(W13, q.W13q, q.W13qd, q.W13sf, q.W13sft, G, 2 * cfg->F, cfg->H, s));
+    MOE_CUDA(launch_quant_wmx(W2, q.W2q, q.W2qd, q.W2sf, q.W2sft, G, cfg->H, cfg->F, s));
+    return MOE_OK;
+  }
   MOE_CUDA(launch_quant_tiles8(W13, q.W13q, q.W13sf, q.W13sft, G, 2 * cfg->F, cfg->H, s));
   MOE_CUDA(launch_quant_tiles8(W2, q.W2q, q.W2sf, q.W2sft, G, cfg->H, cfg->F, s));
   return MOE_OK;
@@ -316,14 +336,16 @@ moe_status moe_grouped_ffn_fwd(const moe_config* cfg, const void* x_perm, const 
   MOE_REQUIRE(al16(GU) && al16(h) && al16(y_perm) && al16(scratch));
   cudaStream_t s = (cudaStream_t)stream;
   int32_t* st = status_word(scratch);
-  if (cfg->dtype == MOE_DTYPE_FP8_E4M3_BLOCK) {
+  if (is_fp8(*cfg)) {
     // the E4M3 weights are the ones moe_quantize_weights left in scratch, the
-    // E4M3 x_perm the one moe_permute wrote there with the bf16 rows
+    // E4M3 x_perm the one moe_permute wrote there with the bf16 rows; h's
+    // E4M3 form comes out of the FC1 epilogue (block recipe) or its own pass
     const Fp8Scratch q = fp8_scratch(*cfg, scratch);
     const int G = cfg->E + cfg->n_shared;
     const int64_t R = rows_max(*cfg);
     MOE_CUDA(launch_ffn_fc1_fp8(*cfg, q.xq, q.xsf, counts, offsets, q.W13q, q.W13sf, GU, h, q.hq,
                                 q.hsf, st, s));
+    if (q.mx) MOE_CUDA(launch_quant_rows8(h, q.hq, q.hsf, offsets, counts, G, R, cfg->F, s, true));
     MOE_CUDA(launch_ffn_fc2_fp8(*cfg, q.hq, q.hsf, counts, offsets, q.W2q, q.W2sf, y_perm, st, s));
     return MOE_OK;
   }
@@ -350,13 +372,19 @@ moe_status moe_unpermute_bwd(const moe_config* cfg, const void* dY, const void* 
   MOE_REQUIRE(al4(offsets) && al16(dO_perm) && tok4(cfg, dw) && al16(scratch));
   uint8_t* dOq = nullptr;
   uint8_t* dOsf = nullptr;
-  if (cfg->dtype == MOE_DTYPE_FP8_E4M3_BLOCK) {
-    const Fp8Scratch q = fp8_scratch(*cfg, scratch);
+  Fp8Scratch q;
+  const bool fp8 = is_fp8(*cfg);
+  if (fp8) q = fp8_scratch(*cfg, scratch);
+  if (fp8 && !q.mx) {                 // dO's 1x128 E4M3 form written by the scatter itself
     dOq = q.dOq;
     dOsf = q.dOsf;
   }
-  MOE_CUDA(launch_unpermute_bwd(*cfg, dY, y_perm, row_of, w, counts, offsets, dO_perm, dw,
-                                (cudaStream_t)stream, dOq, dOsf));
+  cudaStream_t s = (cudaStream_t)stream;
+  MOE_CUDA(launch_unpermute_bwd(*cfg, dY, y_perm, row_of, w, counts, offsets, dO_perm, dw, s, dOq,
+                                dOsf));
+  if (fp8 && q.mx)
+    MOE_CUDA(launch_quant_rows8(dO_perm, q.dOq, q.dOsf, offsets, counts, cfg->E + cfg->n_shared,
+                                rows_max(*cfg), cfg->H, s, true));
   return MOE_OK;
 }
 
@@ -371,15 +399,16 @@ moe_status moe_grouped_ffn_dgrad(const moe_config* cfg, const void* dO_perm, con
   MOE_REQUIRE(al16(dX_perm) && al16(scratch));
   cudaStream_t s = (cudaStream_t)stream;
   int32_t* st = status_word(scratch);
-  if (cfg->dtype == MOE_DTYPE_FP8_E4M3_BLOCK) {
+  if (is_fp8(*cfg)) {
     const Fp8Scratch q = fp8_scratch(*cfg, scratch);
     const int G = cfg->E + cfg->n_shared;
     const int64_t R = rows_max(*cfg);
-    // dO_perm's E4M3 form is the one moe_unpermute_bwd wrote into scratch
-    MOE_CUDA(launch_ffn_fc2_dgrad_fp8(*cfg, q.dOq, q.dOsf, counts, offsets, q.W2q, q.W2sft, GU,
+    // dO_perm's E4M3 form is the one moe_unpermute_bwd wrote into scratch;
+    // the weights in their data-gradient forms
+    MOE_CUDA(launch_ffn_fc2_dgrad_fp8(*cfg, q.dOq, q.dOsf, counts, offsets, q.W2qd, q.W2sft, GU,
                                       dGU, st, s));
-    MOE_CUDA(launch_quant_rows8(dGU, q.dGq, q.dGsf, offsets, counts, G, R, 2 * cfg->F, s));
-    MOE_CUDA(launch_ffn_fc1_dgrad_fp8(*cfg, q.dGq, q.dGsf, counts, offsets, q.W13q, q.W13sft,
+    MOE_CUDA(launch_quant_rows8(dGU, q.dGq, q.dGsf, offsets, counts, G, R, 2 * cfg->F, s, q.mx));
+    MOE_CUDA(launch_ffn_fc1_dgrad_fp8(*cfg, q.dGq, q.dGsf, counts, offsets, q.W13qd, q.W13sft,
                                       token_of, dlogits, W_r, dX_perm, st, s));
     return MOE_OK;
   }
@@ -398,19 +427,20 @@ moe_status moe_grouped_ffn_wgrad(const moe_config* cfg, const void* dO_perm, con
   MOE_REQUIRE(al4(offsets) && al16(dW13) && al16(dW2) && al16(scratch));
   cudaStream_t s = (cudaStream_t)stream;
   int32_t* st = status_word(scratch);
-  if (cfg->dtype == MOE_DTYPE_FP8_E4M3_BLOCK) {
-    // both operands in 128x1 slices along each expert's tokens (E4M3 codes
-    // and scale atoms), multiplied on the block-scaled FP8 tensor cores
+  if (is_fp8(*cfg)) {
+    // both operands in slices along each expert's tokens (128x1, or 32x1 for
+    // MXFP8; E4M3 codes and scale atoms), multiplied on the block-scaled FP8
+    // tensor cores
     const Fp8Scratch q = fp8_scratch(*cfg, scratch);
     const int G = cfg->E + cfg->n_shared;
     const int64_t R = rows_max(*cfg);
     const int H = cfg->H, F = cfg->F;
-    MOE_CUDA(launch_quant_cols8(dO_perm, q.cHq, q.cHsf, offsets, counts, G, R, H, s));
-    MOE_CUDA(launch_quant_cols8(h, q.bFq, q.bFsf, offsets, counts, G, R, F, s));
+    MOE_CUDA(launch_quant_cols8(dO_perm, q.cHq, q.cHsf, offsets, counts, G, R, H, s, q.mx));
+    MOE_CUDA(launch_quant_cols8(h, q.bFq, q.bFsf, offsets, counts, G, R, F, s, q.mx));
     MOE_CUDA(launch_ffn_wgrad_fc2_fp8(*cfg, q.cHq, q.cHsf, q.bFq, q.bFsf, counts, offsets, dW2,
                                       st, s));
-    MOE_CUDA(launch_quant_cols8(dGU, q.d2Fq, q.d2Fsf, offsets, counts, G, R, 2 * F, s));
-    MOE_CUDA(launch_quant_cols8(x_perm, q.aHq, q.aHsf, offsets, counts, G, R, H, s));
+    MOE_CUDA(launch_quant_cols8(dGU, q.d2Fq, q.d2Fsf, offsets, counts, G, R, 2 * F, s, q.mx));
+    MOE_CUDA(launch_quant_cols8(x_perm, q.aHq, q.aHsf, offsets, counts, G, R, H, s, q.mx));
     MOE_CUDA(launch_ffn_wgrad_fc1_fp8(*cfg, q.d2Fq, q.d2Fsf, q.aHq, q.aHsf, counts, offsets, dW13,
                                       st, s));
     return MOE_OK;

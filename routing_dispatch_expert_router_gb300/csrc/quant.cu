@@ -11,8 +11,12 @@
 //          reduces along that row),
 //   cols   128 x 1 slices along the tokens of each 128-row block of the
 //          permuted buffer (weight-gradient operands).
+// The MXFP8 configuration uses 32-element blocks instead (1 x 32 rows, 32 x 1
+// columns) and quantises each expert weight twice: 1 x 32 along its input
+// dimension (forward GEMMs) and 32 x 1 along its output dimension (data
+// gradients).
 // Output: 1-byte E4M3 codes with UE8M0 scale atoms (fp8_layout.cuh), the
-// operands of the block-scaled FP8 tensor-core GEMMs. For the 128 x 1 slices
+// operands of the block-scaled FP8 tensor-core GEMMs. For the column slices
 // the atom's rows are the buffer's columns and its K blocks the 128-row
 // blocks of the permuted buffer (the weight gradients reduce over tokens).
 // E4M3 rounding (to nearest even, saturating) uses the hardware conversion.
@@ -38,22 +42,25 @@ __device__ __forceinline__ bool live_block(const int32_t* __restrict__ offsets,
   return r0 - offsets[lo] < (long long)((counts[lo] + 127) / 128) * 128;
 }
 
-// 128 x 1 slices: every live 128-row block of [0, offsets[G]) (group segments
-// are multiples of 128 rows, so blocks never straddle two experts) -> E4M3
-// bytes plus the UE8M0 scale atoms [cols / 128][atoms along the rows]. One
-// block of 256 threads per (128-row block, 128-column slab): the 128 x 128
-// tile is read once into shared memory with 16-byte loads (eight per thread
-// in flight), the column maxima are taken there (two partial maxima of 64
-// rows per column), and every thread quantises eight 8-column vectors read
-// back from the tile and stores their codes (8 bytes each).
+// BLK x 1 slices (BLK = 128, or 32 for MX): every live 128-row block of
+// [0, offsets[G]) (group segments are multiples of 128 rows, so blocks never
+// straddle two experts) -> E4M3 bytes plus the UE8M0 scale atoms [cols / 128]
+// [along the rows]. One block of 256 threads per (128-row block, 128-column
+// slab): the 128 x 128 tile is read once into shared memory with 16-byte
+// loads (eight per thread in flight), the maxima of each column's four
+// 32-row pieces are taken there (combined into one for BLK = 128), and every
+// thread quantises eight 8-column vectors read back from the tile and stores
+// their codes (8 bytes each).
+template <int BLK>
 __global__ void __launch_bounds__(256)
 quant_cols8_kernel(const __nv_bfloat16* __restrict__ X, uint8_t* __restrict__ Xq,
                    uint8_t* __restrict__ sf, const int32_t* __restrict__ offsets,
                    const int32_t* __restrict__ counts, int G, int cols, long long kg) {
+  static_assert(BLK == 128 || BLK == 32, "block length");
   extern __shared__ uint4 qc_smem[];
   uint4 (*tile)[16] = reinterpret_cast<uint4 (*)[16]>(qc_smem);   // 128 rows x 128 bf16
-  float* part = reinterpret_cast<float*>(qc_smem + 128 * 16);      // [2][128]
-  float* inv = part + 256;                                         // [128]
+  float* part = reinterpret_cast<float*>(qc_smem + 128 * 16);      // [4 pieces][128]
+  float* inv = part + 512;                                         // [4 pieces][128]
   const long long rblocks = offsets[G] / 128;
   const int slabs = cols >> 7;
   const int tid = threadIdx.x;
@@ -78,18 +85,36 @@ quant_cols8_kernel(const __nv_bfloat16* __restrict__ X, uint8_t* __restrict__ Xq
     }
     __syncthreads();
     {
+      // column c, 32-row pieces 2h and 2h + 1
       const int c = tid & 127, h = tid >> 7;
       const __nv_bfloat16* col = reinterpret_cast<const __nv_bfloat16*>(&tile[0][0]) + c;
-      float m = 0.f;
+#pragma unroll
+      for (int j = 2 * h; j < 2 * h + 2; ++j) {
+        float m = 0.f;
 #pragma unroll 8
-      for (int r = h * 64; r < h * 64 + 64; ++r) m = fmaxf(m, fabsf(__bfloat162float(col[r * 128])));
-      part[h * 128 + c] = m;
+        for (int r = 32 * j; r < 32 * j + 32; ++r) m = fmaxf(m, fabsf(__bfloat162float(col[r * 128])));
+        part[j * 128 + c] = m;
+      }
     }
     __syncthreads();
-    if (tid < 128) {
-      const uint32_t code = ue8m0_code(fmaxf(part[tid], part[128 + tid]));
-      inv[tid] = ue8m0_inv(code);
-      sf[f8::atom_offset(cs, rb, kg) + f8::atom_byte(tid, (int)rb)] = (uint8_t)code;
+    if (BLK == 128) {
+      if (tid < 128) {
+        const float m = fmaxf(fmaxf(part[tid], part[128 + tid]), fmaxf(part[256 + tid], part[384 + tid]));
+        const uint32_t code = ue8m0_code(m);
+        const float iv = ue8m0_inv(code);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) inv[j * 128 + tid] = iv;
+        sf[f8::atom_offset(cs, rb, kg) + f8::atom_byte(tid, (int)rb)] = (uint8_t)code;
+      }
+    } else {
+      // column c = tid & 127, pieces 2h, 2h + 1 (one scale byte each)
+      const int c = tid & 127, h = tid >> 7;
+#pragma unroll
+      for (int j = 2 * h; j < 2 * h + 2; ++j) {
+        const uint32_t code = ue8m0_code(part[j * 128 + c]);
+        inv[j * 128 + c] = ue8m0_inv(code);
+        sf[f8::mx_atom_offset(cs, rb, kg) + f8::atom_byte(c, j)] = (uint8_t)code;
+      }
     }
     __syncthreads();
     uint8_t* dst = Xq + (size_t)rb * 128 * cols + c0;
@@ -98,7 +123,8 @@ quant_cols8_kernel(const __nv_bfloat16* __restrict__ X, uint8_t* __restrict__ Xq
       const int v = tid + 256 * i, r = v >> 4, q = v & 15;
       float f[8];
       unpack8(tile[r][q], f);
-      *reinterpret_cast<uint2*>(dst + (size_t)r * cols + q * 8) = e4m3x8_each(f, inv + q * 8);
+      *reinterpret_cast<uint2*>(dst + (size_t)r * cols + q * 8) =
+          e4m3x8_each(f, inv + (r >> 5) * 128 + q * 8);
     }
     __syncthreads();
   }
@@ -154,44 +180,127 @@ quant_tiles8_kernel(const __nv_bfloat16* __restrict__ W, uint8_t* __restrict__ W
   }
 }
 
-// 1 x 128 slices along the rows of the live 128-row blocks of [0, offsets[G])
-// -> E4M3 bytes plus UE8M0 scale atoms (row block rb, K block kb). One block
-// of 256 threads per 128-row block; each half-warp owns 8 of the rows and walks
-// them two 128-element slices at a time (16 lanes x 16 bytes per slice, both
-// loads in flight together).
+// 1 x BLK slices (BLK = 128, or 32 for MX) along the rows of the live
+// 128-row blocks of [0, offsets[G]) -> E4M3 bytes plus UE8M0 scale atoms.
+// Work items of 16 rows (eight per 128-row block, so the grid's last wave is
+// short); each half-warp owns one row and walks it two 128-element K blocks at
+// a time (16 lanes x 16 bytes per block, both loads in flight together). The
+// scale of a BLK-wide piece is the maximum over the BLK / 8 lanes holding it.
+template <int BLK>
 __global__ void __launch_bounds__(256)
 quant_rows8_kernel(const __nv_bfloat16* __restrict__ X, uint8_t* __restrict__ Xq,
                    uint8_t* __restrict__ sf, const int32_t* __restrict__ offsets,
-                   const int32_t* __restrict__ counts, int G, int cols) {
-  const long long rblocks = offsets[G] / 128;
+                   const int32_t* __restrict__ counts, int G, int cols, long long kg) {
+  static_assert(BLK == 128 || BLK == 32, "block length");
+  constexpr int LANES = BLK / 8;                          // lanes per scale piece
+  const long long items = offsets[G] / 128 * 8;
   const int KB = cols >> 7;
-  const int64_t kg = f8::atoms_k(cols);
   const int hw = threadIdx.x >> 4, l16 = threadIdx.x & 15;
   const unsigned half = (threadIdx.x & 16) ? 0xffff0000u : 0x0000ffffu;
-  for (long long rb = blockIdx.x; rb < rblocks; rb += gridDim.x) {
+  for (long long it = blockIdx.x; it < items; it += gridDim.x) {
+    const long long rb = it >> 3;
     if (!live_block(offsets, counts, G, rb)) continue;
-    for (int r = hw; r < 128; r += 16) {
-      const size_t row = (size_t)rb * 128 + r;
-      const __nv_bfloat16* src = X + row * cols + l16 * 8;
-      uint8_t* dst = Xq + row * cols + l16 * 8;
-      for (int kb = 0; kb < KB; kb += 2) {
-        const bool two = kb + 1 < KB;
-        float f[2][8];
-        unpack8(ldg_nc_v4(src + (size_t)kb * 128), f[0]);
-        if (two) unpack8(ldg_nc_v4(src + (size_t)(kb + 1) * 128), f[1]);
+    const int r = (int)(it & 7) * 16 + hw;                // row inside the 128-row block
+    const size_t row = (size_t)rb * 128 + r;
+    const __nv_bfloat16* src = X + row * cols + l16 * 8;
+    uint8_t* dst = Xq + row * cols + l16 * 8;
+    for (int kb = 0; kb < KB; kb += 2) {
+      const bool two = kb + 1 < KB;
+      float f[2][8];
+      unpack8(ldg_nc_v4(src + (size_t)kb * 128), f[0]);
+      if (two) unpack8(ldg_nc_v4(src + (size_t)(kb + 1) * 128), f[1]);
 #pragma unroll
-        for (int u = 0; u < 2; ++u) {
-          if (u == 1 && !two) break;
-          float m = amax8(f[u]);
+      for (int u = 0; u < 2; ++u) {
+        if (u == 1 && !two) break;
+        float m = amax8(f[u]);
 #pragma unroll
-          for (int o = 8; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(half, m, o));
-          const uint32_t code = ue8m0_code(m);
-          *reinterpret_cast<uint2*>(dst + (size_t)(kb + u) * 128) = e4m3x8(f[u], ue8m0_inv(code));
-          if (l16 == 0)
+        for (int o = LANES / 2; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(half, m, o));
+        const uint32_t code = ue8m0_code(m);
+        *reinterpret_cast<uint2*>(dst + (size_t)(kb + u) * 128) = e4m3x8(f[u], ue8m0_inv(code));
+        if ((l16 & (LANES - 1)) == 0) {
+          if (BLK == 128)
             sf[f8::atom_offset(rb, kb + u, kg) + f8::atom_byte(r, kb + u)] = (uint8_t)code;
+          else
+            sf[f8::mx_atom_offset(rb, kb + u, kg) + f8::atom_byte(r, l16 / LANES)] = (uint8_t)code;
         }
       }
     }
+  }
+}
+
+// MX weights: every 128 x 128 tile of W [G, rows, cols] (bf16) -> two E4M3
+// forms. Forward (Wf, sf_f): 1 x 32 pieces along the columns (the forward
+// GEMM's K), atoms with the weight's rows as N. Data gradient (Wd, sf_d):
+// 32 x 1 pieces along the rows (the data gradient's K), atoms with the
+// columns as N. One block of 256 threads per tile: the tile is staged in
+// shared memory once and both forms are written from there (few registers, so
+// six blocks share an SM and keep their loads in flight together).
+__global__ void __launch_bounds__(256, 3)
+quant_wmx_kernel(const __nv_bfloat16* __restrict__ W, uint8_t* __restrict__ Wf,
+                 uint8_t* __restrict__ Wd, uint8_t* __restrict__ sf_f, uint8_t* __restrict__ sf_d,
+                 long long n_tiles, int rows, int cols) {
+  __shared__ uint4 tile[128][16];                         // 128 rows x 128 bf16
+  __shared__ float inv_d[4][128];                         // [row piece][column]
+  const int tc = cols / 128, tr = rows / 128;
+  const int tid = threadIdx.x;
+  for (long long t = blockIdx.x; t < n_tiles; t += gridDim.x) {
+    const long long g = t / ((long long)tr * tc);
+    const int rem = (int)(t % ((long long)tr * tc));
+    const int rt = rem / tc, ct = rem % tc;
+    const size_t base = (size_t)g * rows * cols + (size_t)rt * 128 * cols + (size_t)ct * 128;
+    {
+      uint4 in[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int v = tid + 256 * i, r = v >> 4, q = v & 15;
+        in[i] = ldg_nc_v4(W + base + (size_t)r * cols + q * 8);
+      }
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int v = tid + 256 * i;
+        tile[v >> 4][v & 15] = in[i];
+      }
+    }
+    // forward form: a 1 x 32 piece is four consecutive lanes' vectors (each
+    // thread reads back the vectors it stored)
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int v = tid + 256 * i, r = v >> 4, q = v & 15;
+      float f[8];
+      unpack8(tile[r][q], f);
+      float m = amax8(f);
+      m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
+      m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
+      const uint32_t code = ue8m0_code(m);
+      *reinterpret_cast<uint2*>(Wf + base + (size_t)r * cols + q * 8) = e4m3x8(f, ue8m0_inv(code));
+      if ((q & 3) == 0)
+        sf_f[f8::mx_atom_offset(g * tr + rt, ct, tc) + f8::atom_byte(r, q >> 2)] = (uint8_t)code;
+    }
+    __syncthreads();
+    {
+      // data-gradient form: column c, 32-row pieces 2h and 2h + 1
+      const int c = tid & 127, h = tid >> 7;
+      const __nv_bfloat16* col = reinterpret_cast<const __nv_bfloat16*>(&tile[0][0]) + c;
+#pragma unroll
+      for (int j = 2 * h; j < 2 * h + 2; ++j) {
+        float m = 0.f;
+#pragma unroll 8
+        for (int r = 32 * j; r < 32 * j + 32; ++r) m = fmaxf(m, fabsf(__bfloat162float(col[r * 128])));
+        const uint32_t code = ue8m0_code(m);
+        inv_d[j][c] = ue8m0_inv(code);
+        sf_d[f8::mx_atom_offset(g * tc + ct, rt, tr) + f8::atom_byte(c, j)] = (uint8_t)code;
+      }
+    }
+    __syncthreads();
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int v = tid + 256 * i, r = v >> 4, q = v & 15;
+      float f[8];
+      unpack8(tile[r][q], f);
+      *reinterpret_cast<uint2*>(Wd + base + (size_t)r * cols + q * 8) =
+          e4m3x8_each(f, &inv_d[r >> 5][q * 8]);
+    }
+    __syncthreads();
   }
 }
 
@@ -210,21 +319,34 @@ cudaError_t launch_quant_tiles8(const void* W, uint8_t* Wq, uint8_t* sf_f, uint8
   return cudaGetLastError();
 }
 
+cudaError_t launch_quant_wmx(const void* W, uint8_t* Wf, uint8_t* Wd, uint8_t* sf_f, uint8_t* sf_d,
+                             int G, int rows, int cols, cudaStream_t s) {
+  const long long n = (long long)G * (rows / 128) * (cols / 128);
+  quant_wmx_kernel<<<grid_cap(n, 1), 256, 0, s>>>(static_cast<const __nv_bfloat16*>(W), Wf, Wd,
+                                                  sf_f, sf_d, n, rows, cols);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_quant_rows8(const void* X, uint8_t* Xq, uint8_t* sf, const int32_t* offsets,
                                const int32_t* counts, int G, int64_t rows_max, int cols,
-                               cudaStream_t s) {
-  quant_rows8_kernel<<<grid_cap(rows_max / 128, 1), 256, 0, s>>>(
-      static_cast<const __nv_bfloat16*>(X), Xq, sf, offsets, counts, G, cols);
+                               cudaStream_t s, bool mx) {
+  const int grid = grid_cap(rows_max / 128 * 8, 1);
+  const long long kg = f8::sf_stride(cols, mx);
+  const __nv_bfloat16* x = static_cast<const __nv_bfloat16*>(X);
+  if (mx) quant_rows8_kernel<32><<<grid, 256, 0, s>>>(x, Xq, sf, offsets, counts, G, cols, kg);
+  else quant_rows8_kernel<128><<<grid, 256, 0, s>>>(x, Xq, sf, offsets, counts, G, cols, kg);
   return cudaGetLastError();
 }
 
 cudaError_t launch_quant_cols8(const void* X, uint8_t* Xq, uint8_t* sf, const int32_t* offsets,
                                const int32_t* counts, int G, int64_t rows_max, int cols,
-                               cudaStream_t s) {
-  constexpr int smem = 128 * 16 * 16 + 3 * 128 * 4;     // tile + two partial maxima + 1/scales
-  quant_cols8_kernel<<<grid_cap(rows_max / 128 * (cols / 128), 1), 256, smem, s>>>(
-      static_cast<const __nv_bfloat16*>(X), Xq, sf, offsets, counts, G, cols,
-      (long long)f8::atoms_k(rows_max));
+                               cudaStream_t s, bool mx) {
+  constexpr int smem = 128 * 16 * 16 + 8 * 128 * 4;     // tile + piece maxima + 1/scales
+  const int grid = grid_cap(rows_max / 128 * (cols / 128), 1);
+  const long long kg = f8::sf_stride(rows_max, mx);
+  const __nv_bfloat16* x = static_cast<const __nv_bfloat16*>(X);
+  if (mx) quant_cols8_kernel<32><<<grid, 256, smem, s>>>(x, Xq, sf, offsets, counts, G, cols, kg);
+  else quant_cols8_kernel<128><<<grid, 256, smem, s>>>(x, Xq, sf, offsets, counts, G, cols, kg);
   return cudaGetLastError();
 }
 

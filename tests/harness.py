@@ -149,15 +149,19 @@ def _ident(a):
 def check_steps(shape, inp: dict, g: dict, backward: bool = True, replay_idx=None):
     """Every step of the GPU path against the oracle fed the GPU's step inputs.
 
-    In the FP8 configuration the oracle quantises those inputs the way the
-    layer does (weights in 128x128 tiles, activations in 1x128 slices along
-    the reduction, weight-gradient operands in 128x1 slices along tokens);
-    quantising identical inputs is exact on both sides, so the same per-element
-    tolerance applies."""
-    fp8 = getattr(shape, "dtype", 0) == 1
-    qr = O.quant_rows if fp8 else _ident
-    qc = O.quant_cols if fp8 else _ident
-    qt = O.quant_tiles if fp8 else _ident
+    In the FP8 configurations the oracle quantises those inputs the way the
+    layer does (block recipe: weights in 128x128 tiles, activations in 1x128
+    slices along the reduction, weight-gradient operands in 128x1 slices along
+    tokens; MXFP8: 32-element slices, each weight in its forward and its
+    data-gradient form); quantising identical inputs is exact on both sides, so
+    the same per-element tolerance applies."""
+    fp8 = getattr(shape, "dtype", 0) in (1, 2)
+    blk = O.fp8_block(shape) if fp8 else 128
+    qr = (lambda a: O.quant_rows(a, blk)) if fp8 else _ident
+    qc = (lambda a: O.quant_cols(a, blk)) if fp8 else _ident
+    # the weights as the forward GEMMs and as the data gradients read them
+    wf = (lambda W: O.fp8_weights(shape, W)[0]) if fp8 else _ident
+    wd = (lambda W: O.fp8_weights(shape, W)[1]) if fp8 else _ident
     T, H, E, k, F, S = shape.T, shape.H, shape.E, shape.k, shape.F, shape.n_shared
     G = E + S
     x = f64(inp["x"])
@@ -201,8 +205,8 @@ def check_steps(shape, inp: dict, g: dict, backward: bool = True, replay_idx=Non
         if cnt[gi] == 0:
             continue
         rows = slice(off[gi], off[gi] + cnt[gi])
-        w13 = qt(f64(W13[gi]))
-        w2 = qt(f64(W2[gi]))
+        w13 = wf(f64(W13[gi]))
+        w2 = wf(f64(W2[gi]))
         gu_ref, h_ref = O.expert_fc1(qr(xp[rows]), w13)
         assert_close(f"GU[g={gi}]", GU[rows], gu_ref)
         assert_close(f"h[g={gi}]", hh[rows], O.round_bf16(O.silu(GU[rows, :F]) * GU[rows, F:]))
@@ -243,8 +247,8 @@ def check_steps(shape, inp: dict, g: dict, backward: bool = True, replay_idx=Non
     dW13 = g["dW13"]
     dW2 = g["dW2"]
     for gi in range(G):
-        w13 = qt(f64(W13[gi]))
-        w2 = qt(f64(W2[gi]))
+        w13 = wd(f64(W13[gi]))
+        w2 = wd(f64(W2[gi]))
         if cnt[gi] == 0:
             assert_equal(f"dW2[g={gi}] empty", f64(dW2[gi]), np.zeros((H, F)))
             assert_equal(f"dW13[g={gi}] empty", f64(dW13[gi]), np.zeros((2 * F, H)))

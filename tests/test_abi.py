@@ -93,6 +93,30 @@ def test_fp8_scratch_holds_the_quantised_operands():
     assert e.value.code == 1
 
 
+def test_mxfp8_scratch_holds_both_weight_forms():
+    """MXFP8: the weights in two E4M3 forms and one scale byte per 32 elements
+    (atoms of 128 rows x one 128-wide K block) for weights and activations."""
+    mx = DSV3_FP8.with_(dtype=2)
+    s = B.moe_query_sizes(mx)
+    G, R, H, F = 256, 256 * 640, 7168, 2048
+    sfb = lambda rows, K: rows * K // 32          # noqa: E731
+    weights = 2 * (G * 2 * F * H + G * H * F) + sfb(G * 2 * F, H) + sfb(G * H, 2 * F) + \
+        sfb(G * H, F) + sfb(G * F, H)
+    acts = 2 * (R * H + R * F + R * H + R * 2 * F) + sfb(R, H) + sfb(R, F) + sfb(R, H) + \
+        sfb(R, 2 * F) + sfb(H, R) + sfb(F, R) + sfb(2 * F, R) + sfb(H, R)
+    T, E = 16384, 256
+    router_split = max(E * 3 * H * 2, 3 * T * E * 2 + (T // 1024) * H * E * 4)
+    assert s.rows_max == R
+    assert weights + acts + router_split <= s.scratch_bytes <= weights + acts + router_split + (1 << 20)
+    # same restrictions as the block recipe
+    with pytest.raises(B.MoEError) as e:
+        B.moe_query_sizes(mx.with_(n_shared=1))
+    assert e.value.code == 2
+    with pytest.raises(B.MoEError) as e:
+        B.moe_query_sizes(mx.with_(weights_in_expert=1))
+    assert e.value.code == 2
+
+
 def test_null_and_misaligned_pointers_rejected_before_launch():
     cfg = B.config(TINY)
     lib = B.lib()

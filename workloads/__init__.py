@@ -38,6 +38,8 @@ GROUP_TOP2_SUM = 0
 GROUP_MAX = 1
 DT_BF16 = 0
 DT_FP8 = 1
+DT_MXFP8 = 2
+FP8_DTYPES = (DT_FP8, DT_MXFP8)
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 
@@ -107,6 +109,10 @@ PROFILE_SHAPES = {
     "dsv3_16experts": DSV3.with_(name="dsv3_16experts", T=512, E=16),
     # the FP8 layer's experts (capacity 640 rows, about 380 kept on average), 16 of them
     "dsv3_fp8_16experts": DSV3_FP8.with_(name="dsv3_fp8_16experts", T=1024, E=16),
+    # the same layer in the MXFP8 recipe (32-element blocks), full size and 16 experts
+    "dsv3_mxfp8": DSV3_FP8.with_(name="dsv3_mxfp8", dtype=DT_MXFP8),
+    "dsv3_mxfp8_16experts": DSV3_FP8.with_(name="dsv3_mxfp8_16experts", T=1024, E=16,
+                                           dtype=DT_MXFP8),
 }
 
 
