@@ -386,10 +386,12 @@ def run_ours(args, rank, world, local):
     sm = dict(zip(STAGES, stage_ms))
 
     # end to end through the public layer calls, host buffers: every step copies
-    # its x and dY from pinned host memory and reads out and dx back. Copies run
-    # on a second stream, double-buffered and ordered by events, so step i+1's
-    # uploads and step i's downloads overlap the neighbouring compute.
-    cs = torch.cuda.Stream(dev)
+    # its x and dY from pinned host memory and reads out and dx back. Uploads and
+    # downloads run on two more streams (one per direction, so the two copy
+    # directions proceed at once), double-buffered and ordered by events, so
+    # step i+1's uploads and step i's downloads overlap the neighbouring compute.
+    cs = torch.cuda.Stream(dev)                       # uploads
+    cd = torch.cuda.Stream(dev)                       # downloads
     xh = [x.cpu().pin_memory() for _ in range(2)]
     dYh = [dY.cpu().pin_memory() for _ in range(2)]
     outh = [torch.empty_like(xh[0]).pin_memory() for _ in range(2)]
@@ -424,12 +426,13 @@ def run_ours(args, rank, world, local):
             B.moe_layer_bwd(cfg, P, xd[b], dYd[b], bufs.fwd_struct, bufs.bwd_struct, dxd[b], dW_r,
                             dW13, dW2, sc)
             done[b].record(stream)
-            with torch.cuda.stream(cs):
-                cs.wait_event(done[b])
+            with torch.cuda.stream(cd):
+                cd.wait_event(done[b])
                 outh[b].copy_(outd[b], non_blocking=True)
                 dxh[b].copy_(dxd[b], non_blocking=True)
-                down[b].record(cs)
+                down[b].record(cd)
         stream.wait_stream(cs)
+        stream.wait_stream(cd)
 
     e2e_run(3)
     torch.cuda.synchronize(dev)
