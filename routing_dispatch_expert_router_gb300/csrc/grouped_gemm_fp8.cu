@@ -100,6 +100,157 @@ __device__ __forceinline__ const uint32_t (&slice32(const uint32_t (&r)[128], in
   return *reinterpret_cast<const uint32_t(*)[32]>(&r[32 * i]);
 }
 
+// The epilogue of one 128 x 256 tile once its accumulator columns are in
+// registers (r: this warp's 32 rows x 128 columns, half = which 128): the
+// SwiGLU forward with h's 1 x 128 E4M3 form (the two warps of a lane quarter
+// exchange row maxima through `xch` under the mbarrier xbar + 8q), the SwiGLU
+// backward (G, U of the first 32 columns already in gq, uq), the weight
+// gradient's 32 x 64 boxes, or the plain / router-term store. Returns false
+// when the exchange wait ran out (status recorded).
+template <int EPI, int MX>
+__device__ __forceinline__ bool f8_epilogue_tile(
+    const Params& p, const CUtensorMap* tmC, const CUtensorMap* tmC2, uint8_t* stage,
+    uint32_t stage_u32, float* xch, uint32_t xbar, volatile int* abort_flag, int g, int nt,
+    int row0, int q, int half, int lane, uint32_t (&r)[128], const __nv_bfloat16* gu,
+    uint4 (&gq)[4], uint4 (&uq)[4], int fb, uint32_t& x_phase) {
+  if (EPI == kEpiSwigluFwd) {
+    const int f0 = nt * (kF8BN / 2) + 64 * half;
+    uint4 ho[2][4];
+#pragma unroll
+    for (int c = 0; c < 2; ++c) {
+      uint4 go[4], uo[4];
+      pack_slice(slice32(r, c), go);
+      pack_slice(slice32(r, 2 + c), uo);
+#pragma unroll
+      for (int v = 0; v < 4; ++v) {
+        float gr[8], ur[8], hf[8];
+        unpack8(go[v], gr);
+        unpack8(uo[v], ur);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) hf[i] = silu_f(gr[i]) * ur[i];
+        ho[c][v] = pack8(hf);
+      }
+      f8_store_box(tmC, stage, stage_u32, lane, go, f0 + 32 * c, row0);          // G
+      f8_store_box(tmC, stage, stage_u32, lane, uo, p.F + f0 + 32 * c, row0);    // U
+      f8_store_box(tmC2, stage, stage_u32, lane, ho[c], f0 + 32 * c, row0);      // h
+    }
+    if (!MX && p.qout) {
+      // h's 1 x 128 slice (columns nt*128 ..) is this warp's 64 columns and
+      // its partner's: exchange the row maxima, then write the E4M3 codes
+      float m = 0.f;
+#pragma unroll
+      for (int c = 0; c < 2; ++c)
+#pragma unroll
+        for (int v = 0; v < 4; ++v) {
+          float f[8];
+          unpack8(ho[c][v], f);
+          m = fmaxf(m, amax8(f));
+        }
+      float* xs = xch + ((x_phase * 4 + q) * 2) * 32;
+      xs[half * 32 + lane] = m;
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(xbar + 8 * q);
+      const bool ok = __all_sync(
+          0xffffffffu, ptx::mbar_wait(xbar + 8 * q, x_phase, kWaitBudget, abort_flag));
+      if (!ok) {
+        if (lane == 0) {
+          record_status(p.status, MOE_ERR_TIMEOUT);
+          *abort_flag = 1;
+        }
+        return false;
+      }
+      const uint32_t code = ue8m0_code(fmaxf(m, xs[(half ^ 1) * 32 + lane]));
+      const float inv = ue8m0_inv(code);
+      const int row = row0 + lane;
+      uint8_t* dst = p.qout + (size_t)row * p.F + f0;
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        uint2 b[4];
+#pragma unroll
+        for (int v = 0; v < 4; ++v) {
+          float f[8];
+          unpack8(ho[c][v], f);
+          b[v] = e4m3x8(f, inv);
+        }
+        *reinterpret_cast<uint4*>(dst + 32 * c) = make_uint4(b[0].x, b[0].y, b[1].x, b[1].y);
+        *reinterpret_cast<uint4*>(dst + 32 * c + 16) = make_uint4(b[2].x, b[2].y, b[3].x, b[3].y);
+      }
+      if (half == 0)
+        p.qsf[f8::atom_offset(row >> 7, nt, p.qsf_kg) + f8::atom_byte(row, nt)] =
+            (uint8_t)code;
+      x_phase ^= 1u;
+    }
+  } else if (EPI == kEpiWgrad) {
+    // dW rows g*Mw + m-tile.., columns n-tile*256 + 128*half.. in 32 x 64
+    // boxes (128-byte rows, 128-byte swizzle: chunk j of row r at j ^ (r & 7))
+    const int c0 = nt * kF8BN + 128 * half;
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      uint4 o[4], o2[4];
+      pack_slice(slice32(r, 2 * j), o);
+      pack_slice(slice32(r, 2 * j + 1), o2);
+      if (lane == 0) ptx::tma_store_wait_read();
+      __syncwarp();
+      uint8_t* rowp = stage + lane * 128;
+#pragma unroll
+      for (int v = 0; v < 4; ++v) {
+        *reinterpret_cast<uint4*>(rowp + ((v ^ (lane & 7)) << 4)) = o[v];
+        *reinterpret_cast<uint4*>(rowp + (((v + 4) ^ (lane & 7)) << 4)) = o2[v];
+      }
+      ptx::fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        ptx::tma_store_2d(tmC, stage_u32, c0 + 64 * j, row0);
+        ptx::tma_store_commit();
+      }
+    }
+  } else if (EPI == kEpiSwigluBwd) {
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      uint4 dg[4], du[4];
+#pragma unroll
+      for (int v = 0; v < 4; ++v) swiglu_bwd8(&r[32 * c + 8 * v], gq[v], uq[v], dg[v], du[v]);
+      if (c + 1 < 4) {
+#pragma unroll
+        for (int v = 0; v < 4; ++v) {
+          gq[v] = ldg_nc_v4(gu + fb + 32 * (c + 1) + v * 8);
+          uq[v] = ldg_nc_v4(gu + p.F + fb + 32 * (c + 1) + v * 8);
+        }
+      }
+      f8_store_box(tmC, stage, stage_u32, lane, dg, fb + 32 * c, row0);          // dG
+      f8_store_box(tmC, stage, stage_u32, lane, du, p.F + fb + 32 * c, row0);    // dU
+    }
+  } else {
+    // plain store (FC2) or FC1 data gradient plus the row's router term
+    const int f0 = nt * kF8BN + 128 * half;
+    float rd = 0.f;
+    const float* rw = nullptr;
+    if (EPI == kEpiDgradRouter && g < p.router_E) {
+      const int tk = p.token_of[row0 + lane];
+      if (tk >= 0 && tk < p.router_T) rd = p.dlogits[(long long)tk * p.router_E + g];
+      rw = p.W_r + (long long)g * p.N + f0;
+    }
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      if (EPI == kEpiDgradRouter && rw) {
+#pragma unroll
+        for (int v = 0; v < 8; ++v) {
+          const float4 w4 = __ldg(reinterpret_cast<const float4*>(rw + 32 * c) + v);
+          float* a = reinterpret_cast<float*>(&r[32 * c + 4 * v]);
+          a[0] = fmaf(rd, w4.x, a[0]);
+          a[1] = fmaf(rd, w4.y, a[1]);
+          a[2] = fmaf(rd, w4.z, a[2]);
+          a[3] = fmaf(rd, w4.w, a[3]);
+        }
+      }
+      uint4 o[4];
+      pack_slice(slice32(r, c), o);
+      f8_store_box(tmC, stage, stage_u32, lane, o, f0 + 32 * c, row0);
+    }
+  }
+  return true;
+}
+
 template <int EPI, int B_MN, int MX>
 __global__ void __launch_bounds__(kF8Threads, 1)
 grouped_gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmA,
@@ -257,6 +408,7 @@ grouped_gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmA,
     if (lane == 0) {
       constexpr uint32_t IDESC = ptx::idesc_mxf8_e4m3(BM, kF8BN, C::KG ? 1 : 0, B_MN);
       uint32_t stage = 0, phase = 0, acc_phase = 0;
+      uint32_t sf_slot = 0;                          // block recipe: current scale slot
       bool ok = true, issued = false;
       for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
         int nk = nk_fixed, kb0 = 0;
@@ -280,11 +432,26 @@ grouped_gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmA,
           }
           ptx::tc_fence_after();
           const uint32_t sfs = sf_u + stage * kF8SfStage;
-          const uint32_t sfa_t = tmem_base + kF8SfCol + kF8SfSlotCols * stage;
+          // scale atoms into tensor memory: MX has one per K block (a slot per
+          // stage); in the block recipe an atom holds four consecutive K
+          // blocks' scales, so it is copied when a tile starts and at every
+          // fourth K block, into two alternating slots (the copies and the MMAs
+          // of this thread run in issue order, so a slot is rewritten only
+          // after the MMAs of the group before last)
+          bool copy = true;
+          uint32_t slot = stage;
+          if (!MX) {
+            copy = kb == 0 || ((kb0 + kb) & 3) == 0;
+            if (copy) sf_slot ^= 1u;
+            slot = sf_slot;
+          }
+          const uint32_t sfa_t = tmem_base + kF8SfCol + kF8SfSlotCols * slot;
           const uint32_t sfb_t = sfa_t + 4;
-          ptx::tmem_cp_32x128b_warpx4(sfa_t, ptx::smem_desc_sf(sfs));
-          ptx::tmem_cp_32x128b_warpx4(sfb_t, ptx::smem_desc_sf(sfs + f8::kAtomBytes));
-          ptx::tmem_cp_32x128b_warpx4(sfb_t + 4, ptx::smem_desc_sf(sfs + 2 * f8::kAtomBytes));
+          if (copy) {
+            ptx::tmem_cp_32x128b_warpx4(sfa_t, ptx::smem_desc_sf(sfs));
+            ptx::tmem_cp_32x128b_warpx4(sfb_t, ptx::smem_desc_sf(sfs + f8::kAtomBytes));
+            ptx::tmem_cp_32x128b_warpx4(sfb_t + 4, ptx::smem_desc_sf(sfs + 2 * f8::kAtomBytes));
+          }
           // the scale byte inside the atom: this K block's (K blocks counted
           // from the start of the operand: the buffer's row blocks for the
           // weight gradients), or (MX) the 32-wide slice's
@@ -382,141 +549,9 @@ grouped_gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmA,
         acc_phase ^= 1u;
       }
 
-      if (EPI == kEpiSwigluFwd) {
-        const int f0 = t.nt * (kF8BN / 2) + 64 * half;
-        uint4 ho[2][4];
-#pragma unroll
-        for (int c = 0; c < 2; ++c) {
-          uint4 go[4], uo[4];
-          pack_slice(slice32(r, c), go);
-          pack_slice(slice32(r, 2 + c), uo);
-#pragma unroll
-          for (int v = 0; v < 4; ++v) {
-            float gr[8], ur[8], hf[8];
-            unpack8(go[v], gr);
-            unpack8(uo[v], ur);
-#pragma unroll
-            for (int i = 0; i < 8; ++i) hf[i] = silu_f(gr[i]) * ur[i];
-            ho[c][v] = pack8(hf);
-          }
-          f8_store_box(&tmC, stage, stage_u32, lane, go, f0 + 32 * c, row0);          // G
-          f8_store_box(&tmC, stage, stage_u32, lane, uo, p.F + f0 + 32 * c, row0);    // U
-          f8_store_box(&tmC2, stage, stage_u32, lane, ho[c], f0 + 32 * c, row0);      // h
-        }
-        if (!MX && p.qout) {
-          // h's 1 x 128 slice (columns nt*128 ..) is this warp's 64 columns and
-          // its partner's: exchange the row maxima, then write the E4M3 codes
-          float m = 0.f;
-#pragma unroll
-          for (int c = 0; c < 2; ++c)
-#pragma unroll
-            for (int v = 0; v < 4; ++v) {
-              float f[8];
-              unpack8(ho[c][v], f);
-              m = fmaxf(m, amax8(f));
-            }
-          float* xs = xch + ((x_phase * 4 + q) * 2) * 32;
-          xs[half * 32 + lane] = m;
-          __syncwarp();
-          if (lane == 0) ptx::mbar_arrive(xbar + 8 * q);
-          ok = __all_sync(0xffffffffu,
-                          ptx::mbar_wait(xbar + 8 * q, x_phase, kWaitBudget, abort_flag));
-          if (!ok) {
-            if (lane == 0) {
-              record_status(p.status, MOE_ERR_TIMEOUT);
-              *abort_flag = 1;
-            }
-            break;
-          }
-          const uint32_t code = ue8m0_code(fmaxf(m, xs[(half ^ 1) * 32 + lane]));
-          const float inv = ue8m0_inv(code);
-          const int row = row0 + lane;
-          uint8_t* dst = p.qout + (size_t)row * p.F + f0;
-#pragma unroll
-          for (int c = 0; c < 2; ++c) {
-            uint2 b[4];
-#pragma unroll
-            for (int v = 0; v < 4; ++v) {
-              float f[8];
-              unpack8(ho[c][v], f);
-              b[v] = e4m3x8(f, inv);
-            }
-            *reinterpret_cast<uint4*>(dst + 32 * c) = make_uint4(b[0].x, b[0].y, b[1].x, b[1].y);
-            *reinterpret_cast<uint4*>(dst + 32 * c + 16) = make_uint4(b[2].x, b[2].y, b[3].x, b[3].y);
-          }
-          if (half == 0)
-            p.qsf[f8::atom_offset(row >> 7, t.nt, p.qsf_kg) + f8::atom_byte(row, t.nt)] =
-                (uint8_t)code;
-          x_phase ^= 1u;
-        }
-      } else if (EPI == kEpiWgrad) {
-        // dW rows g*Mw + m-tile.., columns n-tile*256 + 128*half.. in 32 x 64
-        // boxes (128-byte rows, 128-byte swizzle: chunk j of row r at j ^ (r & 7))
-        const int c0 = t.nt * kF8BN + 128 * half;
-#pragma unroll
-        for (int j = 0; j < 2; ++j) {
-          uint4 o[4], o2[4];
-          pack_slice(slice32(r, 2 * j), o);
-          pack_slice(slice32(r, 2 * j + 1), o2);
-          if (lane == 0) ptx::tma_store_wait_read();
-          __syncwarp();
-          uint8_t* rowp = stage + lane * 128;
-#pragma unroll
-          for (int v = 0; v < 4; ++v) {
-            *reinterpret_cast<uint4*>(rowp + ((v ^ (lane & 7)) << 4)) = o[v];
-            *reinterpret_cast<uint4*>(rowp + (((v + 4) ^ (lane & 7)) << 4)) = o2[v];
-          }
-          ptx::fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0) {
-            ptx::tma_store_2d(&tmC, stage_u32, c0 + 64 * j, row0);
-            ptx::tma_store_commit();
-          }
-        }
-      } else if (EPI == kEpiSwigluBwd) {
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          uint4 dg[4], du[4];
-#pragma unroll
-          for (int v = 0; v < 4; ++v) swiglu_bwd8(&r[32 * c + 8 * v], gq[v], uq[v], dg[v], du[v]);
-          if (c + 1 < 4) {
-#pragma unroll
-            for (int v = 0; v < 4; ++v) {
-              gq[v] = ldg_nc_v4(gu + fb + 32 * (c + 1) + v * 8);
-              uq[v] = ldg_nc_v4(gu + p.F + fb + 32 * (c + 1) + v * 8);
-            }
-          }
-          f8_store_box(&tmC, stage, stage_u32, lane, dg, fb + 32 * c, row0);          // dG
-          f8_store_box(&tmC, stage, stage_u32, lane, du, p.F + fb + 32 * c, row0);    // dU
-        }
-      } else {
-        // plain store (FC2) or FC1 data gradient plus the row's router term
-        const int f0 = t.nt * kF8BN + 128 * half;
-        float rd = 0.f;
-        const float* rw = nullptr;
-        if (EPI == kEpiDgradRouter && t.g < p.router_E) {
-          const int tk = p.token_of[row0 + lane];
-          if (tk >= 0 && tk < p.router_T) rd = p.dlogits[(long long)tk * p.router_E + t.g];
-          rw = p.W_r + (long long)t.g * p.N + f0;
-        }
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          if (EPI == kEpiDgradRouter && rw) {
-#pragma unroll
-            for (int v = 0; v < 8; ++v) {
-              const float4 w4 = __ldg(reinterpret_cast<const float4*>(rw + 32 * c) + v);
-              float* a = reinterpret_cast<float*>(&r[32 * c + 4 * v]);
-              a[0] = fmaf(rd, w4.x, a[0]);
-              a[1] = fmaf(rd, w4.y, a[1]);
-              a[2] = fmaf(rd, w4.z, a[2]);
-              a[3] = fmaf(rd, w4.w, a[3]);
-            }
-          }
-          uint4 o[4];
-          pack_slice(slice32(r, c), o);
-          f8_store_box(&tmC, stage, stage_u32, lane, o, f0 + 32 * c, row0);
-        }
-      }
+      if (!f8_epilogue_tile<EPI, MX>(p, &tmC, &tmC2, stage, stage_u32, xch, xbar, abort_flag, t.g,
+                                     t.nt, row0, q, half, lane, r, gu, gq, uq, fb, x_phase))
+        break;
     }
     if (lane == 0) ptx::tma_store_wait_all();
   }

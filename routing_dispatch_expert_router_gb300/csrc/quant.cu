@@ -134,27 +134,38 @@ quant_cols8_kernel(const __nv_bfloat16* __restrict__ X, uint8_t* __restrict__ Xq
 // into two atom arrays: sf_f with the weight's rows as the GEMM's N index and
 // its columns as K (the forward GEMMs), sf_d with the roles swapped (the data
 // gradients, which read the weight transposed). One block per tile.
-__global__ void __launch_bounds__(256)
+__global__ void __launch_bounds__(256, 3)
 quant_tiles8_kernel(const __nv_bfloat16* __restrict__ W, uint8_t* __restrict__ Wq,
                     uint8_t* __restrict__ sf_f, uint8_t* __restrict__ sf_d, long long n_tiles,
                     int rows, int cols) {
+  // the tile is staged in shared memory between its maximum and its
+  // conversion (few registers: three blocks share an SM)
+  __shared__ uint4 tile[2048];                            // 128 rows x 128 bf16
   __shared__ float red[8];
   const int tc = cols / 128, tr = rows / 128;
   const int64_t kg_f = f8::atoms_k(cols), kg_d = f8::atoms_k(rows);
-  for (long long tile = blockIdx.x; tile < n_tiles; tile += gridDim.x) {
-    const long long g = tile / ((long long)tr * tc);
-    const int rem = (int)(tile % ((long long)tr * tc));
+  for (long long t = blockIdx.x; t < n_tiles; t += gridDim.x) {
+    const long long g = t / ((long long)tr * tc);
+    const int rem = (int)(t % ((long long)tr * tc));
     const int rt = rem / tc, ct = rem % tc;
     const int r0 = rt * 128, c0 = ct * 128;
     const size_t base = (size_t)g * rows * cols;
-    float f[8][8];
     float m = 0.f;
+    {
+      uint4 in[8];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const int v = threadIdx.x + 256 * i;                // 2048 vectors per tile
-      const int r = v >> 4, c = (v & 15) * 8;
-      unpack8(ldg_nc_v4(W + base + (size_t)(r0 + r) * cols + c0 + c), f[i]);
-      m = fmaxf(m, amax8(f[i]));
+      for (int i = 0; i < 8; ++i) {
+        const int v = threadIdx.x + 256 * i;              // 2048 vectors per tile
+        const int r = v >> 4, c = (v & 15) * 8;
+        in[i] = ldg_nc_v4(W + base + (size_t)(r0 + r) * cols + c0 + c);
+      }
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        float f[8];
+        unpack8(in[i], f);
+        m = fmaxf(m, amax8(f));
+        tile[threadIdx.x + 256 * i] = in[i];
+      }
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
@@ -167,9 +178,11 @@ quant_tiles8_kernel(const __nv_bfloat16* __restrict__ W, uint8_t* __restrict__ W
     const float inv = ue8m0_inv(code);
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
-      const int v = threadIdx.x + 256 * i;
+      const int v = threadIdx.x + 256 * i;                // each thread reads back its own
       const int r = v >> 4, c = (v & 15) * 8;
-      *reinterpret_cast<uint2*>(Wq + base + (size_t)(r0 + r) * cols + c0 + c) = e4m3x8(f[i], inv);
+      float f[8];
+      unpack8(tile[v], f);
+      *reinterpret_cast<uint2*>(Wq + base + (size_t)(r0 + r) * cols + c0 + c) = e4m3x8(f, inv);
     }
     const int n = threadIdx.x & 127;
     if (threadIdx.x < 128)
