@@ -314,21 +314,6 @@ static inline bool make_map_u8(CUtensorMap* m, const void* ptr, uint64_t inner, 
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// Scale atoms as a 2D tensor of [atoms][128] 32-bit words (512 bytes each),
-// one atom per box: the CTA-pair kernels load atoms with tensor copies, whose
-// completion may be counted on the peer CTA's mbarrier.
-static inline bool make_map_sf(CUtensorMap* m, const void* ptr, uint64_t n_atoms) {
-  PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
-  if (!fn) return false;
-  cuuint64_t dims[2] = {128, n_atoms};
-  cuuint64_t strides[1] = {512};
-  cuuint32_t box[2] = {128, 1};
-  cuuint32_t es[2] = {1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<void*>(ptr), dims, strides, box, es,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
-            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 // fp32 output view for TMA stores of 32 x 32 boxes (128-byte rows, 128-byte swizzle).
 static inline bool make_out_map_f32(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t outer) {
   PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();

@@ -358,29 +358,6 @@ __device__ __forceinline__ void mma_bf16_pair(uint32_t d_tmem, uint64_t adesc, u
       :: "r"(d_tmem), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate) : "memory");
 }
 
-// Pair block-scaled FP8 MMA (issued by one thread of the even CTA): as
-// mma_bf16_pair for the operands; each CTA's tensor memory holds, at sfa / sfb,
-// the scales of its own 128 rows of A and of all N columns of B.
-__device__ __forceinline__ void mma_mxf8_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
-                                              uint32_t idesc, uint32_t sfa_tmem,
-                                              uint32_t sfb_tmem, uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::2.kind::mxf8f6f4.block_scale.scale_vec::1X "
-      "[%0], %1, %2, %3, [%5], [%6], p;\n\t}"
-      :: "r"(d_tmem), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate), "r"(sfa_tmem),
-         "r"(sfb_tmem) : "memory");
-}
-
-// Pair form of tmem_cp_32x128b_warpx4 (issued by one thread of the even CTA):
-// each CTA of the pair copies the atom at this shared-memory offset of its own
-// shared memory into its own tensor memory at taddr.
-__device__ __forceinline__ void tmem_cp_32x128b_warpx4_pair(uint32_t taddr, uint64_t sdesc) {
-  asm volatile("tcgen05.cp.cta_group::2.32x128b.warpx4 [%0], %1;"
-               :: "r"(taddr), "l"(sdesc) : "memory");
-}
-
 // Arrive once on the mbarrier at this offset in every CTA of `mask` when the
 // pair MMAs issued so far by this thread are done.
 __device__ __forceinline__ void mma_commit_pair(uint32_t bar, uint16_t mask) {

@@ -1,7 +1,7 @@
 """The FP8 configuration (E4M3 with power-of-two block scales) on the GPU.
 
-The forward and data-gradient GEMMs run on the block-scaled FP8 tensor cores
-(E4M3 codes, UE8M0 scales in tensor memory). Every step is checked against the
+All six expert GEMMs run on the block-scaled FP8 tensor cores (E4M3 codes,
+UE8M0 scales in tensor memory). Every step is checked against the
 oracle fed the GPU's own inputs of that step and quantised the same way (exact
 on both sides, so the bf16 per-element tolerance applies); the whole layer is checked against the oracle's FP8 layer
 run from the raw inputs with the 5e-2 rule (per element against
@@ -20,8 +20,14 @@ H_ = pytest.importorskip("harness")
 SINGLE_TILE = MoEShape("fp8_single_tile", T=64, H=256, E=1, k=1, F=256, score_fn=SIGMOID,
                        bias_kind="normal", dtype=DT_FP8)
 
+# Two experts of 512 rows each (four 128-row tiles), one 256-wide N tile of FC2
+# and two of FC1, every token on both experts.
+PAIR_TILES = MoEShape("fp8_two_experts", T=512, H=256, E=2, k=2, F=256, score_fn=SIGMOID,
+                      bias_kind="normal", dtype=DT_FP8)
+
 SHAPES = [
     SINGLE_TILE,
+    PAIR_TILES,
     MoEShape("fp8_groups", T=512, H=256, E=16, k=4, F=256, score_fn=SIGMOID, n_groups=4,
              topk_groups=2, bias_kind="normal", dtype=DT_FP8),
     # H = 768: six 128-deep k-blocks (a partly used scale atom), three N tiles
@@ -43,7 +49,7 @@ def test_fp8_steps_match_oracle(shape):
 # (the single-tile case has one expert and k = 1: its routing weight is 1 for
 # every token, so the router gradient is identically zero and a relative rule
 # has nothing to compare; its steps are checked above)
-@pytest.mark.parametrize("shape", SHAPES[1:4], ids=lambda s: s.name)
+@pytest.mark.parametrize("shape", SHAPES[1:], ids=lambda s: s.name)
 def test_fp8_layer_end_to_end(shape):
     inp = make_inputs(shape, seed=1)
     g = H_.run_layer(shape, inp)

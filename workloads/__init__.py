@@ -109,6 +109,8 @@ PROFILE_SHAPES = {
     "dsv3_16experts": DSV3.with_(name="dsv3_16experts", T=512, E=16),
     # the FP8 layer's experts (capacity 640 rows, about 380 kept on average), 16 of them
     "dsv3_fp8_16experts": DSV3_FP8.with_(name="dsv3_fp8_16experts", T=1024, E=16),
+    # Mixtral-shaped experts (1024 rows each, F = 14336) in the FP8 block recipe
+    "mixtral_fp8": MIXTRAL.with_(name="mixtral_fp8", dtype=DT_FP8),
     # the same layer in the MXFP8 recipe (32-element blocks), full size and 16 experts
     "dsv3_mxfp8": DSV3_FP8.with_(name="dsv3_mxfp8", dtype=DT_MXFP8),
     "dsv3_mxfp8_16experts": DSV3_FP8.with_(name="dsv3_mxfp8_16experts", T=1024, E=16,
