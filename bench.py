@@ -54,6 +54,9 @@ def parse():
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--weights-in-expert", action="store_true",
                     help="the layer with the routing weight applied inside the expert (bf16)")
+    ap.add_argument("--recompute-h", action="store_true",
+                    help="the backward rewrites h from GU (fine-grained recompute): h need not "
+                         "survive from the forward to the backward")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-sample-tokens", type=int, default=0)
     ap.add_argument("--ref-budget-s", type=float, default=120.0,
@@ -172,15 +175,19 @@ def stash_bytes(shape, bufs) -> dict:
     """Device bytes of the forward state the backward reads (caller-owned
     buffers kept from the forward to the backward): with the routing weight
     inside the expert the permuted expert outputs y_perm are read only by the
-    combine, so their buffer need not survive until the backward."""
+    combine, so their buffer need not survive until the backward; with the
+    fine-grained recompute the backward rewrites h from GU, so neither does h's."""
     f = bufs.fwd
     kept = ["logits", "idx", "w", "counts", "offsets", "row_of", "token_of", "sel_offsets",
-            "sel_tokens", "x_perm", "GU", "h"]
+            "sel_tokens", "x_perm", "GU"]
     if not shape.weights_in_expert:
         kept.append("y_perm")
+    if not shape.recompute_h:
+        kept.append("h")
     n = sum(f[k].numel() * f[k].element_size() for k in kept)
     return {"forward_state_kept": n, "y_perm": f["y_perm"].numel() * f["y_perm"].element_size(),
-            "y_perm_kept": not shape.weights_in_expert}
+            "y_perm_kept": not shape.weights_in_expert,
+            "h": f["h"].numel() * f["h"].element_size(), "h_kept": not shape.recompute_h}
 
 
 STAGES = ("route", "permute", "quantize_weights", "grouped_ffn_fwd", "unpermute",
@@ -268,6 +275,8 @@ def run_ours(args, rank, world, local):
     shape = {**W.SHAPES, **W.PROFILE_SHAPES}[args.workload]
     if args.weights_in_expert:
         shape = shape.with_(weights_in_expert=1)
+    if args.recompute_h:
+        shape = shape.with_(recompute_h=1)
     cfg = B.config(shape)
     inp = W.make_inputs(shape, seed=args.seed + rank, device=str(dev))
     bufs = B.alloc_buffers(cfg, dev)
@@ -287,6 +296,8 @@ def run_ours(args, rank, world, local):
     fp8 = shape.dtype in W.FP8_DTYPES
     mx = shape.dtype == W.DT_MXFP8
     reord = bool(shape.weights_in_expert)
+    # fine-grained recompute: the data gradient rewrites h from GU
+    h_re = f["h"] if shape.recompute_h else None
 
     def step(ev=None):
         # the layer step through the per-stage entry points (the same launches
@@ -314,7 +325,7 @@ def run_ours(args, rank, world, local):
                                           b["dO_perm"])
             rec(6)
             rec(7)
-            B.moe_grouped_ffn_dgrad_reordered(cfg, b["dO_perm"], f["GU"], f["counts"],
+            B.moe_grouped_ffn_dgrad_reordered(cfg, b["dO_perm"], f["GU"], h_re, f["counts"],
                                               f["offsets"], f["token_of"], f["row_of"],
                                               f["logits"], f["idx"], f["w"], inp["W_r"],
                                               inp["W13"], inp["W2"], b["dGU"], b["dX_perm"],
@@ -330,7 +341,7 @@ def run_ours(args, rank, world, local):
             rec(6)
             B.moe_route_bwd(cfg, f["logits"], f["idx"], f["w"], b["dw"], b["dlogits"])
             rec(7)
-            B.moe_grouped_ffn_dgrad(cfg, b["dO_perm"], f["GU"], f["counts"], f["offsets"],
+            B.moe_grouped_ffn_dgrad(cfg, b["dO_perm"], f["GU"], h_re, f["counts"], f["offsets"],
                                     f["token_of"], b["dlogits"], inp["W_r"], inp["W13"],
                                     inp["W2"], b["dGU"], b["dX_perm"], sc)
         rec(8)
@@ -503,7 +514,8 @@ def run_ours(args, rank, world, local):
         "config": {"workload": f"{shape.name}: T={T} H={H} E={E}(+{S} shared) top-{shape.k} "
                                f"F={F} capacity_factor={cf if cf > 0 else 'dropless'} "
                                f"dtype={dt_name}"
-                               + (" weights_in_expert" if reord else "") + " fwd+bwd",
+                               + (" weights_in_expert" if reord else "")
+                               + (" recompute_h" if shape.recompute_h else "") + " fwd+bwd",
                    "l2": "inputs larger than L2 (expert weights "
                          f"{2 * G * 3 * H * F / 1e9:.2f} GB in bf16, streamed every step)",
                    "parallelism": "replicas" if world > 1 else "single GPU"},

@@ -100,6 +100,12 @@ typedef struct moe_config {
                                 * expert before FC2 (see moe_grouped_ffn_fwd_
                                 * reordered); bf16 mode only. 0: it scales the
                                 * expert output in the combine.              */
+    int32_t recompute_h;     /* 1: the backward rewrites h from GU (the
+                              * fine-grained recompute of the activation
+                              * function, es summary §2.3.A): moe_layer_bwd and
+                              * moe_grouped_ffn_bwd pass h to the data gradient,
+                              * so the h the forward wrote need not survive
+                              * until the backward. 0: h is read as stored.  */
 } moe_config;
 
 /* Worst-case sizes of the caller-owned buffers for one configuration. */
@@ -333,9 +339,13 @@ MOE_API moe_status moe_unpermute_bwd(const moe_config* cfg, const void* dY, cons
  * mode: both GEMMs run on the block-scaled FP8 tensor cores with the weights
  * moe_quantize_weights left in scratch and the 1-byte dO that
  * moe_unpermute_bwd left there (W13, W2 are then not read, dO_perm only by the
- * weight gradients); dGU is quantised in 1x128 slices for FC1's. */
+ * weight gradients); dGU is quantised in 1x128 slices for FC1's.
+ * h: NULL, or h [R,F] bf16 to rewrite from GU in the FC2 data-gradient
+ * epilogue (bit for bit the forward's h: the fine-grained recompute of the
+ * activation function), so that the weight gradient can run after the forward's
+ * h was discarded. */
 MOE_API moe_status moe_grouped_ffn_dgrad(const moe_config* cfg, const void* dO_perm,
-                                         const void* GU, const int32_t* counts,
+                                         const void* GU, void* h, const int32_t* counts,
                                          const int32_t* offsets, const int32_t* token_of,
                                          const float* dlogits, const float* W_r, const void* W13,
                                          const void* W2, void* dGU, void* dX_perm, void* scratch,
@@ -410,9 +420,11 @@ MOE_API moe_status moe_unpermute_bwd_reordered(const moe_config* cfg, const void
  * assignments), dlogits [T,E] (as moe_route_bwd from dw) and dX_perm (as
  * moe_grouped_ffn_bwd, router term from this dlogits). logits, idx, w from
  * moe_route; the scratch of the forward. Deterministic: dw sums the FC2 data
- * gradient's per-tile partial dot products in tile order. */
+ * gradient's per-tile partial dot products in tile order. h: NULL, or h_s
+ * [R,F] to rewrite from GU and the rows' weights (as moe_grouped_ffn_dgrad). */
 MOE_API moe_status moe_grouped_ffn_dgrad_reordered(const moe_config* cfg, const void* dO_perm,
-                                                   const void* GU, const int32_t* counts,
+                                                   const void* GU, void* h,
+                                                   const int32_t* counts,
                                                    const int32_t* offsets,
                                                    const int32_t* token_of,
                                                    const int32_t* row_of, const float* logits,

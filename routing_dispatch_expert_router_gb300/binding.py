@@ -45,7 +45,7 @@ class MoEConfig(ctypes.Structure):
                 ("topk_groups", ctypes.c_int32), ("group_score", ctypes.c_int32),
                 ("route_scale", ctypes.c_float), ("dtype", ctypes.c_int32),
                 ("capacity_factor", ctypes.c_float), ("row_align", ctypes.c_int32),
-                ("weights_in_expert", ctypes.c_int32)]
+                ("weights_in_expert", ctypes.c_int32), ("recompute_h", ctypes.c_int32)]
 
 
 class MoESizes(ctypes.Structure):
@@ -114,7 +114,8 @@ def config(shape) -> MoEConfig:
                      dtype=getattr(shape, "dtype", 0),
                      capacity_factor=getattr(shape, "capacity_factor", 0.0),
                      row_align=getattr(shape, "row_align", 128),
-                     weights_in_expert=getattr(shape, "weights_in_expert", 0))
+                     weights_in_expert=getattr(shape, "weights_in_expert", 0),
+                     recompute_h=getattr(shape, "recompute_h", 0))
 
 
 def _cfg(c) -> MoEConfig:
@@ -230,9 +231,10 @@ def moe_grouped_ffn_bwd(cfg, dO_perm, x_perm, GU, h, counts, offsets, token_of, 
           dlogits, W_r, W13, W2, dGU, dX_perm, dW13, dW2, scratch, _stream(stream))
 
 
-def moe_grouped_ffn_dgrad(cfg, dO_perm, GU, counts, offsets, token_of, dlogits, W_r, W13, W2,
+def moe_grouped_ffn_dgrad(cfg, dO_perm, GU, h, counts, offsets, token_of, dlogits, W_r, W13, W2,
                           dGU, dX_perm, scratch, stream=None):
-    _call("moe_grouped_ffn_dgrad", _cfg(cfg), dO_perm, GU, counts, offsets, token_of, dlogits,
+    """h: None, or the buffer to rewrite h into from GU (fine-grained recompute)."""
+    _call("moe_grouped_ffn_dgrad", _cfg(cfg), dO_perm, GU, h, counts, offsets, token_of, dlogits,
           W_r, W13, W2, dGU, dX_perm, scratch, _stream(stream))
 
 
@@ -254,11 +256,11 @@ def moe_unpermute_bwd_reordered(cfg, dY, row_of, counts, offsets, dO_perm, strea
           _stream(stream))
 
 
-def moe_grouped_ffn_dgrad_reordered(cfg, dO_perm, GU, counts, offsets, token_of, row_of, logits,
-                                    idx, w, W_r, W13, W2, dGU, dX_perm, dw, dlogits, scratch,
-                                    stream=None):
-    _call("moe_grouped_ffn_dgrad_reordered", _cfg(cfg), dO_perm, GU, counts, offsets, token_of,
-          row_of, logits, idx, w, W_r, W13, W2, dGU, dX_perm, dw, dlogits, scratch,
+def moe_grouped_ffn_dgrad_reordered(cfg, dO_perm, GU, h, counts, offsets, token_of, row_of,
+                                    logits, idx, w, W_r, W13, W2, dGU, dX_perm, dw, dlogits,
+                                    scratch, stream=None):
+    _call("moe_grouped_ffn_dgrad_reordered", _cfg(cfg), dO_perm, GU, h, counts, offsets,
+          token_of, row_of, logits, idx, w, W_r, W13, W2, dGU, dX_perm, dw, dlogits, scratch,
           _stream(stream))
 
 

@@ -67,6 +67,7 @@ struct Params {
   // dot products <dh_s, h> of every row ([R][dw_nt], fp32)
   const float* row_w;
   float* dw_part;
+  __nv_bfloat16* h_out;       // SwiGLU-bwd: h rewritten from GU ([rows, F]), or null
   int dw_nt;
   // FP8 block-scaled operands (grouped_gemm_fp8.cu): UE8M0 scale atoms of A
   // ([R/128][sfa_kg]) and of B ([G * sfb_nb][sfb_kg]), fp8_layout.cuh
@@ -176,6 +177,20 @@ __device__ __forceinline__ void swiglu_bwd8(const uint32_t* dh, const uint4& g, 
   }
   dg = make_uint4(dgw[0], dgw[1], dgw[2], dgw[3]);
   du = make_uint4(duw[0], duw[1], duw[2], duw[3]);
+}
+
+// h = bf16(silu(g) u), times the row's routing weight when it sits inside the
+// expert, of 8 columns from the stored bf16 G and U: the forward epilogue's
+// arithmetic exactly, so the h recomputed in the backward (fine-grained
+// recompute of the activation function) equals the forward's bit for bit.
+template <bool WGT>
+__device__ __forceinline__ uint4 swiglu_h8(const uint4& g, const uint4& u, float rwt) {
+  float gr[8], ur[8], hf[8];
+  unpack8(g, gr);
+  unpack8(u, ur);
+#pragma unroll
+  for (int i = 0; i < 8; ++i) hf[i] = WGT ? silu_f(gr[i]) * ur[i] * rwt : silu_f(gr[i]) * ur[i];
+  return pack8(hf);
 }
 
 // The same with the routing weight inside the expert: dh_s (the accumulator)

@@ -167,10 +167,14 @@ __device__ __forceinline__ void epilogue_tile(const Params& p, const CUtensorMap
         un[v] = ldg_nc_v4(gu + p.F + f0 + cn + v * 8);
       }
       ptx::tmem_ld_wait();
+      __nv_bfloat16* hrow =
+          p.h_out ? p.h_out + (long long)(row0 + lane) * p.F + f0 + c : nullptr;
 #pragma unroll
       for (int v = 0; v < 4; ++v) {
         if (WGT) swiglu_bwd8_w(r + v * 8, gq[v], uq[v], rwt, o0[v], o1[v], dot);
         else swiglu_bwd8(r + v * 8, gq[v], uq[v], o0[v], o1[v]);
+        // fine-grained recompute: h of these columns from the stored G, U
+        if (hrow) stg_v4(hrow + 8 * v, swiglu_h8<WGT>(gq[v], uq[v], rwt));
         gq[v] = gn[v];
         uq[v] = un[v];
       }
@@ -485,7 +489,7 @@ static_assert(kGuBarOff >= 4608 + 33 * 4 && kGuBarOff + 4 * kGuSlots * 8 <= kCtr
 template <bool WGT>
 __device__ __forceinline__ void swiglu_bwd_slice_inplace(uint8_t* slot, int lane,
                                                          const uint32_t (&r)[32], float rwt,
-                                                         float& dot) {
+                                                         float& dot, __nv_bfloat16* hrow) {
   uint8_t* grow = slot + lane * 64;
   uint8_t* urow = grow + kBoxBytes;
   const int sw = (lane >> 1) & 3;
@@ -493,6 +497,10 @@ __device__ __forceinline__ void swiglu_bwd_slice_inplace(uint8_t* slot, int lane
   for (int v = 0; v < 4; ++v) {
     const int pos = (v ^ sw) << 4;
     uint4 dg, du;
+    // fine-grained recompute: h of these 8 columns from the stored G, U
+    if (hrow)
+      stg_v4(hrow + 8 * v, swiglu_h8<WGT>(*reinterpret_cast<const uint4*>(grow + pos),
+                                          *reinterpret_cast<const uint4*>(urow + pos), rwt));
     if (WGT)
       swiglu_bwd8_w(r + v * 8, *reinterpret_cast<const uint4*>(grow + pos),
                     *reinterpret_cast<const uint4*>(urow + pos), rwt, dg, du, dot);
@@ -772,7 +780,9 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA,
           uint32_t r[32];
           ptx::tmem_ld32(tbase + c, r);
           ptx::tmem_ld_wait();
-          swiglu_bwd_slice_inplace<WGT>(ring + slot * kGuSlotBytes, lane, r, rwt, dot);
+          swiglu_bwd_slice_inplace<WGT>(
+              ring + slot * kGuSlotBytes, lane, r, rwt, dot,
+              p.h_out ? p.h_out + (long long)(row0 + lane) * p.F + f0 + c : nullptr);
           ptx::fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0) {
@@ -971,7 +981,7 @@ cudaError_t launch_ffn_fc2(const moe_config& c, const void* h, const int32_t* co
 cudaError_t launch_ffn_fc2_dgrad(const moe_config& c, const void* dO_perm, const int32_t* counts,
                                  const int32_t* offsets, const void* W2, const void* GU,
                                  void* dGU, int32_t* status, cudaStream_t s, const float* row_w,
-                                 float* dw_part) {
+                                 float* dw_part, void* h_out) {
   const int64_t R = rows_max(c);
   const int G = c.E + c.n_shared;
   const int bn = (c.F % 256 == 0) ? 256 : 128;
@@ -988,6 +998,7 @@ cudaError_t launch_ffn_fc2_dgrad(const moe_config& c, const void* dO_perm, const
   p.ldo = 2LL * c.F;
   p.aux = static_cast<const __nv_bfloat16*>(GU);
   p.ldaux = 2LL * c.F;
+  p.h_out = static_cast<__nv_bfloat16*>(h_out);
   if (row_w) {                                     // dh = w_row dh_s, partial <dh_s, h>
     p.row_w = row_w;
     p.dw_part = dw_part;

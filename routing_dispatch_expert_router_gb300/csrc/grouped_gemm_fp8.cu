@@ -210,6 +210,12 @@ __device__ __forceinline__ bool f8_epilogue_tile(
       uint4 dg[4], du[4];
 #pragma unroll
       for (int v = 0; v < 4; ++v) swiglu_bwd8(&r[32 * c + 8 * v], gq[v], uq[v], dg[v], du[v]);
+      if (p.h_out) {
+        // fine-grained recompute: h of these 32 columns from the stored G, U
+        __nv_bfloat16* hrow = p.h_out + (long long)(row0 + lane) * p.F + fb + 32 * c;
+#pragma unroll
+        for (int v = 0; v < 4; ++v) stg_v4(hrow + 8 * v, swiglu_h8<false>(gq[v], uq[v], 1.f));
+      }
       if (c + 1 < 4) {
 #pragma unroll
         for (int v = 0; v < 4; ++v) {
@@ -646,7 +652,7 @@ cudaError_t launch_ffn_fc2_fp8(const moe_config& c, const uint8_t* hq, const uin
 cudaError_t launch_ffn_fc2_dgrad_fp8(const moe_config& c, const uint8_t* dOq, const uint8_t* dOsf,
                                      const int32_t* counts, const int32_t* offsets,
                                      const uint8_t* W2q, const uint8_t* W2sf_t, const void* GU,
-                                     void* dGU, int32_t* status, cudaStream_t s) {
+                                     void* dGU, int32_t* status, cudaStream_t s, void* h_out) {
   const int64_t R = rows_max(c);
   const int G = c.E + c.n_shared;
   CUtensorMap a, b, oc;
@@ -659,6 +665,7 @@ cudaError_t launch_ffn_fc2_dgrad_fp8(const moe_config& c, const uint8_t* dOq, co
   p.b_rows = c.H;
   p.aux = static_cast<const __nv_bfloat16*>(GU);
   p.ldaux = 2LL * c.F;
+  p.h_out = static_cast<__nv_bfloat16*>(h_out);
   p.sfa = dOsf;
   p.sfa_kg = sf_kg(c, c.H);
   p.sfb = W2sf_t;

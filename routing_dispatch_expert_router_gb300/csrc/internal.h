@@ -164,10 +164,12 @@ cudaError_t launch_ffn_fc2(const moe_config& c, const void* h, const int32_t* co
                            int32_t* status, cudaStream_t s);
 // row_w, dw_part (optional): the weight inside the expert -- dh = w_row dh_s,
 // and dw_part[r * dw_tiles(c) + n-tile] = the row's <dh_s, h> over that tile.
+// h_out (optional): h [rows, F] rewritten from GU (fine-grained recompute).
 cudaError_t launch_ffn_fc2_dgrad(const moe_config& c, const void* dO_perm, const int32_t* counts,
                                  const int32_t* offsets, const void* W2, const void* GU,
                                  void* dGU, int32_t* status, cudaStream_t s,
-                                 const float* row_w = nullptr, float* dw_part = nullptr);
+                                 const float* row_w = nullptr, float* dw_part = nullptr,
+                                 void* h_out = nullptr);
 int dw_tiles(const moe_config& c);
 cudaError_t launch_ffn_fc1_dgrad(const moe_config& c, const void* dGU, const int32_t* counts,
                                  const int32_t* offsets, const void* W13, const int32_t* token_of,
@@ -194,7 +196,8 @@ cudaError_t launch_ffn_fc2_fp8(const moe_config& c, const uint8_t* hq, const uin
 cudaError_t launch_ffn_fc2_dgrad_fp8(const moe_config& c, const uint8_t* dOq, const uint8_t* dOsf,
                                      const int32_t* counts, const int32_t* offsets,
                                      const uint8_t* W2q, const uint8_t* W2sf_t, const void* GU,
-                                     void* dGU, int32_t* status, cudaStream_t s);
+                                     void* dGU, int32_t* status, cudaStream_t s,
+                                     void* h_out = nullptr);
 cudaError_t launch_ffn_fc1_dgrad_fp8(const moe_config& c, const uint8_t* dGq, const uint8_t* dGsf,
                                      const int32_t* counts, const int32_t* offsets,
                                      const uint8_t* W13q, const uint8_t* W13sf_t,

@@ -165,6 +165,7 @@ moe_status check_config(const moe_config* c) {
   if (is_fp8(*c) && (c->n_shared != 0 || c->H % 256 || c->F % 256))
     return MOE_ERR_UNSUPPORTED;
   if (c->weights_in_expert != 0 && c->weights_in_expert != 1) return MOE_ERR_INVALID_ARG;
+  if (c->recompute_h != 0 && c->recompute_h != 1) return MOE_ERR_INVALID_ARG;
   if (c->weights_in_expert && c->dtype != MOE_DTYPE_BF16) return MOE_ERR_UNSUPPORTED;
   if ((int64_t)c->T * c->k >= (1LL << 31) || rows_max(*c) >= (1LL << 31))
     return MOE_ERR_INVALID_ARG;
@@ -389,14 +390,14 @@ moe_status moe_unpermute_bwd(const moe_config* cfg, const void* dY, const void* 
 }
 
 moe_status moe_grouped_ffn_dgrad(const moe_config* cfg, const void* dO_perm, const void* GU,
-                                 const int32_t* counts, const int32_t* offsets,
+                                 void* h, const int32_t* counts, const int32_t* offsets,
                                  const int32_t* token_of, const float* dlogits, const float* W_r,
                                  const void* W13, const void* W2, void* dGU, void* dX_perm,
                                  void* scratch, void* stream) {
   MOE_TRY(check_config(cfg));
   MOE_REQUIRE(al16(dO_perm) && al16(GU) && al4(counts) && al4(offsets) && al4(token_of));
   MOE_REQUIRE(tok4(cfg, dlogits) && al16(W_r) && al16(W13) && al16(W2) && al16(dGU));
-  MOE_REQUIRE(al16(dX_perm) && al16(scratch));
+  MOE_REQUIRE(al16(dX_perm) && al16(scratch) && (h == nullptr || al16(h)));
   cudaStream_t s = (cudaStream_t)stream;
   int32_t* st = status_word(scratch);
   if (is_fp8(*cfg)) {
@@ -406,13 +407,14 @@ moe_status moe_grouped_ffn_dgrad(const moe_config* cfg, const void* dO_perm, con
     // dO_perm's E4M3 form is the one moe_unpermute_bwd wrote into scratch;
     // the weights in their data-gradient forms
     MOE_CUDA(launch_ffn_fc2_dgrad_fp8(*cfg, q.dOq, q.dOsf, counts, offsets, q.W2qd, q.W2sft, GU,
-                                      dGU, st, s));
+                                      dGU, st, s, h));
     MOE_CUDA(launch_quant_rows8(dGU, q.dGq, q.dGsf, offsets, counts, G, R, 2 * cfg->F, s, q.mx));
     MOE_CUDA(launch_ffn_fc1_dgrad_fp8(*cfg, q.dGq, q.dGsf, counts, offsets, q.W13qd, q.W13sft,
                                       token_of, dlogits, W_r, dX_perm, st, s));
     return MOE_OK;
   }
-  MOE_CUDA(launch_ffn_fc2_dgrad(*cfg, dO_perm, counts, offsets, W2, GU, dGU, st, s));
+  MOE_CUDA(launch_ffn_fc2_dgrad(*cfg, dO_perm, counts, offsets, W2, GU, dGU, st, s, nullptr,
+                                nullptr, h));
   MOE_CUDA(launch_ffn_fc1_dgrad(*cfg, dGU, counts, offsets, W13, token_of, dlogits, W_r, dX_perm,
                                 st, s));
   return MOE_OK;
@@ -456,7 +458,10 @@ moe_status moe_grouped_ffn_bwd(const moe_config* cfg, const void* dO_perm, const
                                const float* dlogits, const float* W_r, const void* W13,
                                const void* W2, void* dGU, void* dX_perm, void* dW13, void* dW2,
                                void* scratch, void* stream) {
-  MOE_TRY(moe_grouped_ffn_dgrad(cfg, dO_perm, GU, counts, offsets, token_of, dlogits, W_r, W13, W2,
+  // fine-grained recompute: the data gradient rewrites h from GU before the
+  // weight gradient reads it
+  MOE_TRY(moe_grouped_ffn_dgrad(cfg, dO_perm, GU, cfg->recompute_h ? const_cast<void*>(h) : nullptr,
+                                counts, offsets, token_of, dlogits, W_r, W13, W2,
                                 dGU, dX_perm, scratch, stream));
   MOE_TRY(moe_grouped_ffn_wgrad(cfg, dO_perm, x_perm, h, dGU, counts, offsets, dW13, dW2, scratch,
                                 stream));
@@ -494,7 +499,7 @@ moe_status moe_unpermute_bwd_reordered(const moe_config* cfg, const void* dY,
 }
 
 moe_status moe_grouped_ffn_dgrad_reordered(const moe_config* cfg, const void* dO_perm,
-                                           const void* GU, const int32_t* counts,
+                                           const void* GU, void* h, const int32_t* counts,
                                            const int32_t* offsets, const int32_t* token_of,
                                            const int32_t* row_of, const float* logits,
                                            const int32_t* idx, const float* w, const float* W_r,
@@ -507,11 +512,12 @@ moe_status moe_grouped_ffn_dgrad_reordered(const moe_config* cfg, const void* dO
   MOE_REQUIRE(tok4(cfg, row_of) && tok4(cfg, logits) && tok4(cfg, idx) && tok4(cfg, w));
   MOE_REQUIRE(al16(W_r) && al16(W13) && al16(W2) && al16(dGU) && al16(dX_perm));
   MOE_REQUIRE(tok4(cfg, dw) && tok4(cfg, dlogits) && al16(scratch));
+  MOE_REQUIRE(h == nullptr || al16(h));
   cudaStream_t s = (cudaStream_t)stream;
   int32_t* st = status_word(scratch);
   const ReorderScratch rs = reorder_scratch(*cfg, scratch);
   MOE_CUDA(launch_ffn_fc2_dgrad(*cfg, dO_perm, counts, offsets, W2, GU, dGU, st, s, rs.row_w,
-                                rs.dw_part));
+                                rs.dw_part, h));
   if (cfg->T > 0) {
     MOE_CUDA(launch_dw_reduce(*cfg, rs.dw_part, row_of, dw, s));
     MOE_CUDA(launch_route_bwd(*cfg, logits, idx, w, dw, dlogits, s));
@@ -581,7 +587,9 @@ moe_status moe_layer_bwd(const moe_config* cfg, const moe_params* P, const void*
   if (cfg->weights_in_expert) {
     MOE_TRY(moe_unpermute_bwd_reordered(cfg, dY, st->row_of, st->counts, st->offsets,
                                         bs->dO_perm, stream));
-    MOE_TRY(moe_grouped_ffn_dgrad_reordered(cfg, bs->dO_perm, st->GU, st->counts, st->offsets,
+    MOE_TRY(moe_grouped_ffn_dgrad_reordered(cfg, bs->dO_perm, st->GU,
+                                            cfg->recompute_h ? st->h : nullptr, st->counts,
+                                            st->offsets,
                                             st->token_of, st->row_of, st->logits, st->idx, st->w,
                                             P->W_r, P->W13, P->W2, bs->dGU, bs->dX_perm, bs->dw,
                                             bs->dlogits, scratch, stream));

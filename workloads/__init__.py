@@ -74,6 +74,7 @@ class MoEShape:
     capacity_factor: float = 0.0     # 0 = dropless
     row_align: int = 128             # per-expert segment alignment in rows
     weights_in_expert: int = 0       # 1: routing weight applied inside the expert (bf16)
+    recompute_h: int = 0             # 1: the backward rewrites h from GU
     # input recipe
     router_std: float = 0.0          # 0 -> 1/sqrt(H)
     weight_std: float = 0.02
