@@ -139,13 +139,19 @@ GEMM_SOURCES = ("grouped_gemm.cu", "grouped_gemm_fp8.cu", "gemm_common.cuh", "pt
 
 
 def gemm_sources_sha256() -> str:
+    """Hash of the GEMM sources' code: comments (// to the end of a line) and
+    whitespace are left out, so only a change to the code itself retires a
+    committed capture of the kernels' DRAM traffic."""
     import hashlib
+    import re
     h = hashlib.sha256()
     for name in GEMM_SOURCES:
         path = os.path.join(ROOT, "routing_dispatch_expert_router_gb300", "csrc", name)
         if os.path.exists(path):
-            with open(path, "rb") as f:
-                h.update(f.read())
+            with open(path, encoding="utf-8") as f:
+                text = f.read()
+            code = re.sub(r"//[^\n]*", "", text)
+            h.update(re.sub(r"\s+", "", code).encode())
     return h.hexdigest()
 
 

@@ -104,7 +104,7 @@ __device__ __forceinline__ const uint32_t (&slice32(const uint32_t (&r)[128], in
 // SwiGLU forward with h's 1 x 128 E4M3 form (the two warps of a lane quarter
 // exchange row maxima through `xch` under the mbarrier xbar + 8q), the SwiGLU
 // backward (G, U of the first 32 columns already in gq, uq), the weight
-// gradient's 32 x 64 boxes, or the plain / router-term store. Returns false
+// gradient's 32 x 32 boxes, or the plain / router-term store. Returns false
 // when the exchange wait ran out (status recorded).
 template <int EPI, int MX>
 __device__ __forceinline__ bool f8_epilogue_tile(
