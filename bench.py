@@ -364,14 +364,15 @@ def run_ours(args, rank, world, local):
     # path] + selection), dispatch (hist, rank, scatter), FC1 and FC2, combine,
     # combine bwd, route bwd, the four backward GEMMs, dispatch bwd, router wgrad
     # (on the tensor-core path: dlogits split, GEMM, chunk sum); the FP8 mode adds
-    # the two weight quantisers, 2 activation quantisers forward, 2 in the data
-    # gradients and 4 in the weight gradients (MXFP8: x_perm, h and dO are
-    # quantised by passes of their own, three more)
+    # the two weight quantisers, dGU's row quantiser in the data gradients and
+    # the four column quantisers of the weight gradients (x_perm's, h's and dO's
+    # row forms come out of the scatter, the FC1 epilogue and the combine
+    # backward; MXFP8 quantises those three by passes of their own)
     tc_router = shape.E >= 128 and shape.E % 128 == 0
     launches_per_step = ((3 if tc_router else 2) + 3 + 2 + 1 + 1 + 1 + 4 + 1
                          + (3 if tc_router else 1))
     if fp8:
-        launches_per_step += 2 + 2 + 2 + 4 + (3 if mx else 0)
+        launches_per_step += 2 + 1 + 4 + (3 if mx else 0)
     if reord:
         launches_per_step += 2          # row weights, dw reduction
     for _ in range(max(args.warmup, 3)):
