@@ -134,8 +134,10 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
+# the sources of the launches in profiles/gemm_traffic.json (the GEMMs and the
+# weight-gradient stage's quantisers)
 GEMM_SOURCES = ("grouped_gemm.cu", "grouped_gemm_fp8.cu", "gemm_common.cuh", "ptx.cuh",
-                "fp8_layout.cuh")
+                "fp8_layout.cuh", "quant.cu")
 
 
 def gemm_sources_sha256() -> str:
@@ -203,12 +205,14 @@ STAGES = ("route", "permute", "quantize_weights", "grouped_ffn_fwd", "unpermute"
 
 def wgrad_bytes(shape, f) -> int:
     """Bytes the FP8 weight-gradient stage must move: per live row of the
-    permuted buffers, dO, h, dGU and x_perm read in bf16 (2 B), written as
-    E4M3 (1 B) and read back by the GEMMs (1 B); dW2 and dW13 written in bf16."""
+    permuted buffers, dO, h and x_perm read in bf16 (2 B), written as E4M3
+    (1 B) and read back by the GEMMs (1 B), and dGU's E4M3 column form (which
+    the data-gradient stage writes) read by the GEMM (1 B); dW2 and dW13
+    written in bf16."""
     H, F, G = shape.H, shape.F, shape.E + shape.n_shared
     counts = f["counts"].cpu().tolist()
     live = sum(-(-c // 128) * 128 for c in counts)
-    return live * (H + F + 2 * F + H) * 4 + G * 3 * H * F * 2
+    return live * ((H + F + H) * 4 + 2 * F) + G * 3 * H * F * 2
 
 
 def stage_table(shape, f, stage_ms, hbm_gbs, fl, tc_peak, bf16_peak):
@@ -251,7 +255,7 @@ def stage_table(shape, f, stage_ms, hbm_gbs, fl, tc_peak, bf16_peak):
         ("grouped_ffn_dgrad", fl, "FC2 dgrad+SwiGLU bwd, FC1 dgrad (tcgen05"
          + (" kind::mxf8f6f4)" if fp8 else ")")),
         ("grouped_ffn_wgrad", fl, "dW2, dW13 (tcgen05"
-         + (f" kind::mxf8f6f4, with their four {blk}x1 quantisers)" if fp8 else " bf16)")),
+         + (f" kind::mxf8f6f4, with their three {blk}x1 quantisers)" if fp8 else " bf16)")),
         ("permute_bwd", rows * H * bf + T * H * bf + maps, "dx gather-reduce"),
         ("router_wgrad", T * H * bf + E * H * 4 + T * E * 4, "dW_r (each x row once)"),
     ]
@@ -364,15 +368,15 @@ def run_ours(args, rank, world, local):
     # path] + selection), dispatch (hist, rank, scatter), FC1 and FC2, combine,
     # combine bwd, route bwd, the four backward GEMMs, dispatch bwd, router wgrad
     # (on the tensor-core path: dlogits split, GEMM, chunk sum); the FP8 mode adds
-    # the two weight quantisers, dGU's row quantiser in the data gradients and
-    # the four column quantisers of the weight gradients (x_perm's, h's and dO's
+    # the two weight quantisers, dGU's row-and-column quantiser in the data
+    # gradients and three column quantisers in the weight gradients (x_perm's, h's and dO's
     # row forms come out of the scatter, the FC1 epilogue and the combine
     # backward; MXFP8 quantises those three by passes of their own)
     tc_router = shape.E >= 128 and shape.E % 128 == 0
     launches_per_step = ((3 if tc_router else 2) + 3 + 2 + 1 + 1 + 1 + 4 + 1
                          + (3 if tc_router else 1))
     if fp8:
-        launches_per_step += 2 + 1 + 4 + (3 if mx else 0)
+        launches_per_step += 2 + 1 + 3 + (3 if mx else 0)
     if reord:
         launches_per_step += 2          # row weights, dw reduction
     for _ in range(max(args.warmup, 3)):
@@ -552,7 +556,7 @@ def run_ours(args, rank, world, local):
         wms = sm["grouped_ffn_wgrad"]
         res["roofline_wgrad"] = {
             "kernel": ("grouped_gemm_fp8_kernel<kEpiWgrad> (tcgen05 kind::mxf8f6f4, K = each "
-                       "expert's rows) with its four 128x1 quantisers"),
+                       "expert's rows) with the column quantisers of dO, h and x_perm"),
             "bound": "hbm", "achieved": wb / (wms * 1e-3) / 1e9, "peak": pk["hbm_gbs"],
             "unit": "GB/s", "frac": wb / (wms * 1e-3) / 1e9 / pk["hbm_gbs"],
             "bytes_per_step": wb, "ms_per_step": wms,

@@ -339,7 +339,8 @@ MOE_API moe_status moe_unpermute_bwd(const moe_config* cfg, const void* dY, cons
  * mode: both GEMMs run on the block-scaled FP8 tensor cores with the weights
  * moe_quantize_weights left in scratch and the 1-byte dO that
  * moe_unpermute_bwd left there (W13, W2 are then not read, dO_perm only by the
- * weight gradients); dGU is quantised in 1x128 slices for FC1's.
+ * weight gradients); dGU is quantised in 1x128 slices for FC1's and, in the
+ * same pass, in 128x1 slices for moe_grouped_ffn_wgrad.
  * h: NULL, or h [R,F] bf16 to rewrite from GU in the FC2 data-gradient
  * epilogue (bit for bit the forward's h: the fine-grained recompute of the
  * activation function), so that the weight gradient can run after the forward's
@@ -355,7 +356,9 @@ MOE_API moe_status moe_grouped_ffn_dgrad(const moe_config* cfg, const void* dO_p
  * dW13[g] = dGU^T x_perm over the group's rows (bf16, zero for empty groups),
  * after moe_grouped_ffn_dgrad has written dGU. FP8 mode: both operands are
  * quantised to E4M3 in 128x1 slices along the group's tokens (into scratch)
- * and multiplied on the block-scaled FP8 tensor cores. */
+ * and multiplied on the block-scaled FP8 tensor cores; dGU's E4M3 form is the
+ * one moe_grouped_ffn_dgrad left in scratch (the dGU argument is not read), so
+ * pass the scratch of that call. */
 MOE_API moe_status moe_grouped_ffn_wgrad(const moe_config* cfg, const void* dO_perm,
                                          const void* x_perm, const void* h, const void* dGU,
                                          const int32_t* counts, const int32_t* offsets,

@@ -97,6 +97,12 @@ cudaError_t launch_quant_rows8(const void* X, uint8_t* Xq, uint8_t* sf, const in
 cudaError_t launch_quant_cols8(const void* X, uint8_t* Xq, uint8_t* sf, const int32_t* offsets,
                                const int32_t* counts, int G, int64_t rows_max, int cols,
                                cudaStream_t s, bool mx = false);
+// Both forms of one tensor from a single read: 1xBLK rows (Xr, sfr) and
+// BLKx1 columns (Xc, sfc).
+cudaError_t launch_quant_rows_cols8(const void* X, uint8_t* Xr, uint8_t* sfr, uint8_t* Xc,
+                                    uint8_t* sfc, const int32_t* offsets, const int32_t* counts,
+                                    int G, int64_t rows_max, int cols, cudaStream_t s,
+                                    bool mx = false);
 // MXFP8 weights: forward (1x32 along cols) and data-gradient (32x1 along rows) forms.
 cudaError_t launch_quant_wmx(const void* W, uint8_t* Wf, uint8_t* Wd, uint8_t* sf_f, uint8_t* sf_d,
                              int G, int rows, int cols, cudaStream_t s);

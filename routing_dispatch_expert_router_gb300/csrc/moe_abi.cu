@@ -408,7 +408,10 @@ moe_status moe_grouped_ffn_dgrad(const moe_config* cfg, const void* dO_perm, con
     // the weights in their data-gradient forms
     MOE_CUDA(launch_ffn_fc2_dgrad_fp8(*cfg, q.dOq, q.dOsf, counts, offsets, q.W2qd, q.W2sft, GU,
                                       dGU, st, s, h));
-    MOE_CUDA(launch_quant_rows8(dGU, q.dGq, q.dGsf, offsets, counts, G, R, 2 * cfg->F, s, q.mx));
+    // dGU's row form for FC1's data gradient and its column form for the
+    // weight gradient, from one read
+    MOE_CUDA(launch_quant_rows_cols8(dGU, q.dGq, q.dGsf, q.d2Fq, q.d2Fsf, offsets, counts, G, R,
+                                     2 * cfg->F, s, q.mx));
     MOE_CUDA(launch_ffn_fc1_dgrad_fp8(*cfg, q.dGq, q.dGsf, counts, offsets, q.W13qd, q.W13sft,
                                       token_of, dlogits, W_r, dX_perm, st, s));
     return MOE_OK;
@@ -441,7 +444,7 @@ moe_status moe_grouped_ffn_wgrad(const moe_config* cfg, const void* dO_perm, con
     MOE_CUDA(launch_quant_cols8(h, q.bFq, q.bFsf, offsets, counts, G, R, F, s, q.mx));
     MOE_CUDA(launch_ffn_wgrad_fc2_fp8(*cfg, q.cHq, q.cHsf, q.bFq, q.bFsf, counts, offsets, dW2,
                                       st, s));
-    MOE_CUDA(launch_quant_cols8(dGU, q.d2Fq, q.d2Fsf, offsets, counts, G, R, 2 * F, s, q.mx));
+    // (dGU's column form is the one moe_grouped_ffn_dgrad left in scratch)
     MOE_CUDA(launch_quant_cols8(x_perm, q.aHq, q.aHsf, offsets, counts, G, R, H, s, q.mx));
     MOE_CUDA(launch_ffn_wgrad_fc1_fp8(*cfg, q.d2Fq, q.d2Fsf, q.aHq, q.aHsf, counts, offsets, dW13,
                                       st, s));

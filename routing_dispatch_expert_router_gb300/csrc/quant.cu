@@ -50,12 +50,16 @@ __device__ __forceinline__ bool live_block(const int32_t* __restrict__ offsets,
 // loads (eight per thread in flight), the maxima of each column's four
 // 32-row pieces are taken there (combined into one for BLK = 128), and every
 // thread quantises eight 8-column vectors read back from the tile and stores
-// their codes (8 bytes each).
-template <int BLK>
+// their codes (8 bytes each). With ROWS, the same pass also writes the tile's
+// 1 x BLK row form (Xr, sfr; a row's 16 vectors sit in 16 consecutive lanes,
+// whose maxima meet by shuffles), so a tensor both GEMM directions need is read
+// once.
+template <int BLK, bool ROWS>
 __global__ void __launch_bounds__(256)
 quant_cols8_kernel(const __nv_bfloat16* __restrict__ X, uint8_t* __restrict__ Xq,
                    uint8_t* __restrict__ sf, const int32_t* __restrict__ offsets,
-                   const int32_t* __restrict__ counts, int G, int cols, long long kg) {
+                   const int32_t* __restrict__ counts, int G, int cols, long long kg,
+                   uint8_t* __restrict__ Xr, uint8_t* __restrict__ sfr, long long kgr) {
   static_assert(BLK == 128 || BLK == 32, "block length");
   extern __shared__ uint4 qc_smem[];
   uint4 (*tile)[16] = reinterpret_cast<uint4 (*)[16]>(qc_smem);   // 128 rows x 128 bf16
@@ -125,6 +129,22 @@ quant_cols8_kernel(const __nv_bfloat16* __restrict__ X, uint8_t* __restrict__ Xq
       unpack8(tile[r][q], f);
       *reinterpret_cast<uint2*>(dst + (size_t)r * cols + q * 8) =
           e4m3x8_each(f, inv + (r >> 5) * 128 + q * 8);
+      if (ROWS) {
+        // row r's 1 x BLK pieces of this 128-column K block
+        constexpr int LANES = BLK / 8;
+        float m = amax8(f);
+#pragma unroll
+        for (int o = LANES / 2; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+        const uint32_t code = ue8m0_code(m);
+        *reinterpret_cast<uint2*>(Xr + ((size_t)rb * 128 + r) * cols + c0 + q * 8) =
+            e4m3x8(f, ue8m0_inv(code));
+        if ((q & (LANES - 1)) == 0) {
+          if (BLK == 128)
+            sfr[f8::atom_offset(rb, cs, kgr) + f8::atom_byte(r, cs)] = (uint8_t)code;
+          else
+            sfr[f8::mx_atom_offset(rb, cs, kgr) + f8::atom_byte(r, q / LANES)] = (uint8_t)code;
+        }
+      }
     }
     __syncthreads();
   }
@@ -358,8 +378,28 @@ cudaError_t launch_quant_cols8(const void* X, uint8_t* Xq, uint8_t* sf, const in
   const int grid = grid_cap(rows_max / 128 * (cols / 128), 1);
   const long long kg = f8::sf_stride(rows_max, mx);
   const __nv_bfloat16* x = static_cast<const __nv_bfloat16*>(X);
-  if (mx) quant_cols8_kernel<32><<<grid, 256, smem, s>>>(x, Xq, sf, offsets, counts, G, cols, kg);
-  else quant_cols8_kernel<128><<<grid, 256, smem, s>>>(x, Xq, sf, offsets, counts, G, cols, kg);
+  if (mx)
+    quant_cols8_kernel<32, false><<<grid, 256, smem, s>>>(x, Xq, sf, offsets, counts, G, cols, kg,
+                                                           nullptr, nullptr, 0);
+  else
+    quant_cols8_kernel<128, false><<<grid, 256, smem, s>>>(x, Xq, sf, offsets, counts, G, cols,
+                                                            kg, nullptr, nullptr, 0);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_quant_rows_cols8(const void* X, uint8_t* Xr, uint8_t* sfr, uint8_t* Xc,
+                                    uint8_t* sfc, const int32_t* offsets, const int32_t* counts,
+                                    int G, int64_t rows_max, int cols, cudaStream_t s, bool mx) {
+  constexpr int smem = 128 * 16 * 16 + 8 * 128 * 4;
+  const int grid = grid_cap(rows_max / 128 * (cols / 128), 1);
+  const long long kgc = f8::sf_stride(rows_max, mx), kgr = f8::sf_stride(cols, mx);
+  const __nv_bfloat16* x = static_cast<const __nv_bfloat16*>(X);
+  if (mx)
+    quant_cols8_kernel<32, true><<<grid, 256, smem, s>>>(x, Xc, sfc, offsets, counts, G, cols,
+                                                          kgc, Xr, sfr, kgr);
+  else
+    quant_cols8_kernel<128, true><<<grid, 256, smem, s>>>(x, Xc, sfc, offsets, counts, G, cols,
+                                                           kgc, Xr, sfr, kgr);
   return cudaGetLastError();
 }
 
