@@ -451,6 +451,40 @@ def permutation_maps(idx, cfg) -> dict:
                 sel_offsets=sel_offsets, sel_tokens=sel_tokens, R=R, C=C)
 
 
+def stash_page_table(counts, offsets, rows_max: int, pool_pages: int, top: int):
+    """Page table of one layer's paged stash.
+
+    Reading of the pages' paged stashing (es summary, Resumen técnico §2.3.C:
+    the dynamic buffers are managed inside the CUDA graph so that none is
+    reserved for the worst case): the rows a layer keeps for its backward live
+    in a pool of `pool_pages` pages of 128 rows, plus a spill page numbered
+    `pool_pages`. The layer takes one page for every 128-row block of its
+    permuted rows that holds a kept row -- the first ceil(counts[g] / 128)
+    blocks of group g's segment, which starts at row offsets[g] -- numbered
+    consecutively from `top` in block order. Every other block, and the block
+    just past the last row, maps to the spill page. A layer whose blocks do not
+    all fit takes no page: every block maps to the spill page and the pool is
+    reported full.
+
+    Returns (table, top_after, full): table has rows_max // 128 + 2 entries,
+    table[b] the page of block b for b <= rows_max // 128 and table[-1] the
+    first page taken (= top).
+    """
+    nblk = rows_max // 128
+    live = []
+    for g in range(len(counts)):
+        first = int(offsets[g]) // 128
+        for i in range((int(counts[g]) + 127) // 128):
+            live.append(first + i)
+    table = np.full(nblk + 2, pool_pages, dtype=np.int64)
+    table[-1] = top
+    if top + len(live) > pool_pages:
+        return table, top, True
+    for n, b in enumerate(live):
+        table[b] = top + n
+    return table, top + len(live), False
+
+
 def permute(x, maps) -> np.ndarray:
     """x_perm[r] = x[token_of[r]], zero rows for padding."""
     x = np.asarray(x, dtype=np.float64)

@@ -363,6 +363,79 @@ def test_maps_invariants_and_brute_force(E, k, align, cf, shared):
         np.testing.assert_array_equal(st, np.nonzero((idx == e).any(1))[0])
 
 
+def _gemm_row_tiles(m):
+    """128-row tiles the row-grouped GEMMs run: ceil(count / 128) per group."""
+    return sum(-(-int(c) // 128) for c in m["counts"])
+
+
+@pytest.mark.parametrize("E,k,cf,shared,T", [(16, 4, 0.0, 1, 700), (8, 2, 1.0, 0, 900),
+                                              (64, 1, 1.25, 0, 1500), (5, 5, 0.0, 2, 97)])
+def test_stash_page_table_covers_exactly_the_kept_rows(E, k, cf, shared, T):
+    """Paged stash: every kept row (and every row of its 128-row block, which the
+    GEMM tiles read) gets a pool row of its own inside the pages the layer took;
+    the layer takes as many pages as the grouped GEMMs run 128-row tiles."""
+    cfg = MoEShape("t", T=T, H=8, E=E, k=k, F=8, row_align=128, capacity_factor=cf,
+                   n_shared=shared)
+    rng = np.random.default_rng(T + E)
+    p = np.arange(1, E + 1, dtype=np.float64) ** -1.5
+    p /= p.sum()
+    idx = np.stack([rng.choice(E, size=k, replace=False, p=p) for _ in range(T)])
+    m = O.permutation_maps(idx, cfg)
+    rows_max = int(m["R"])
+    n_tiles = _gemm_row_tiles(m)
+    top = 3
+    P = top + n_tiles + 5
+    table, top_after, full = O.stash_page_table(m["counts"], m["offsets"], rows_max, P, top)
+    assert not full and top_after == top + n_tiles
+    assert table.shape == (rows_max // 128 + 2,) and table[-1] == top
+    read = np.zeros(rows_max, dtype=bool)        # rows the GEMM tiles read (brute force)
+    for g in range(len(m["counts"])):
+        for r in range(int(m["counts"][g])):
+            rr = int(m["offsets"][g]) + r
+            read[rr - rr % 128: rr - rr % 128 + 128] = True
+    rows = np.nonzero(read)[0]
+    phys = table[rows // 128] * 128 + rows % 128
+    assert len(set(phys.tolist())) == rows.size                 # no two rows share a pool row
+    assert phys.min() >= top * 128 and phys.max() < top_after * 128
+    assert rows.size == n_tiles * 128                           # and no page is left unused
+    # every other block (and the one past the last row) is the spill page
+    other = np.setdiff1d(np.arange(rows_max // 128 + 1), np.unique(rows // 128))
+    assert (table[other] == P).all()
+    # pages follow the block order (stable in the rows' order)
+    assert (np.diff(table[np.unique(rows // 128)]) == 1).all()
+
+
+def test_stash_page_table_dropless_is_the_contiguous_layout():
+    """Dropless segments are padded to 128 rows, so every block below offsets[G]
+    is live and the table is the identity shifted by the first page."""
+    cfg = MoEShape("t", T=300, H=8, E=8, k=2, F=8)
+    rng = np.random.default_rng(5)
+    idx = np.stack([rng.choice(8, size=2, replace=False) for _ in range(300)])
+    m = O.permutation_maps(idx, cfg)
+    used = int(m["offsets"][-1]) // 128
+    table, top_after, full = O.stash_page_table(m["counts"], m["offsets"], int(m["R"]) + 1024,
+                                                1000, 17)
+    np.testing.assert_array_equal(table[:used], 17 + np.arange(used))
+    assert top_after == 17 + used and not full
+
+
+def test_stash_page_table_full_pool_and_stacked_layers():
+    counts = np.array([130, 0, 1, 256])
+    offsets = np.array([0, 256, 256, 384, 640])
+    need = 2 + 0 + 1 + 2
+    t, top, full = O.stash_page_table(counts, offsets, 640, need - 1, 0)
+    assert full and top == 0 and (t[:-1] == need - 1).all() and t[-1] == 0
+    t, top, full = O.stash_page_table(counts, offsets, 640, need, 0)
+    assert not full and top == need
+    # blocks 0, 1 (group 0), 2 (group 2; group 1 is empty), 3, 4 (group 3); block 5
+    # is the one past the last row
+    np.testing.assert_array_equal(t, [0, 1, 2, 3, 4, need, 0])
+    # a second layer on the same pool takes the pages after the first's
+    t2, top2, full2 = O.stash_page_table(counts, offsets, 640, 2 * need, top)
+    assert not full2 and top2 == 2 * need and t2[-1] == need
+    np.testing.assert_array_equal(t2[:5], need + np.arange(need))
+
+
 def test_capacity_value_and_keep_first_tokens():
     cfg = MoEShape("t", T=16384, H=8, E=256, k=8, F=8, capacity_factor=1.25)
     assert O.capacity(cfg) == 640
