@@ -57,6 +57,10 @@ def parse():
     ap.add_argument("--recompute-h", action="store_true",
                     help="the backward rewrites h from GU (fine-grained recompute): h need not "
                          "survive from the forward to the backward")
+    ap.add_argument("--paged-stash", action="store_true",
+                    help="the end-to-end leg keeps x_perm, GU, h and y_perm in a stash pool of "
+                         "128-row pages sized to the layer's live rows (paged stashing) instead "
+                         "of worst-case buffers")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-sample-tokens", type=int, default=0)
     ap.add_argument("--ref-budget-s", type=float, default=120.0,
@@ -412,6 +416,23 @@ def run_ours(args, rank, world, local):
     # downloads run on two more streams (one per direction, so the two copy
     # directions proceed at once), double-buffered and ordered by events, so
     # step i+1's uploads and step i's downloads overlap the neighbouring compute.
+    # paged stash: the end-to-end leg runs on a pool of exactly the pages the
+    # layer's kept rows need (its own page table, scratch and backward buffers);
+    # the device-resident step above keeps the worst-case buffers
+    cfg_e, bufs_e, stash = cfg, bufs, None
+    if args.paged_stash:
+        pages = sum(-(-int(c) // 128) for c in counts)
+        cfg_e = B.config(shape)
+        cfg_e.stash_pool_pages = pages
+        pool = B.alloc_stash_pool(cfg_e, pages, dev)
+        bufs_e = B.alloc_buffers(cfg_e, dev, pool=pool)
+        row_bytes = 2 * H + 4 * F + 2 * F + 2 * H        # x_perm, GU, h, y_perm (bf16)
+        R = int(bufs.sizes.rows_max)
+        stash = {"pool_pages": pages, "pool_rows": (pages + 1) * 128,
+                 "pool_bytes": (pages + 1) * 128 * row_bytes,
+                 "worst_case_rows": R, "worst_case_bytes": R * row_bytes,
+                 "what": "x_perm, GU, h, y_perm of the end-to-end leg in a pool of 128-row pages "
+                         "taken on the device (one spill page more), against rows_max rows"}
     cs = torch.cuda.Stream(dev)                       # uploads
     cd = torch.cuda.Stream(dev)                       # downloads
     xh = [x.cpu().pin_memory() for _ in range(2)]
@@ -444,9 +465,9 @@ def run_ours(args, rank, world, local):
                 upload(1 - b)
             stream.wait_event(up[b])
             stream.wait_event(down[b])                # results of step i-2 are out
-            B.moe_layer_fwd(cfg, P, xd[b], outd[b], bufs.fwd_struct, sc)
-            B.moe_layer_bwd(cfg, P, xd[b], dYd[b], bufs.fwd_struct, bufs.bwd_struct, dxd[b], dW_r,
-                            dW13, dW2, sc)
+            B.moe_layer_fwd(cfg_e, P, xd[b], outd[b], bufs_e.fwd_struct, bufs_e.scratch)
+            B.moe_layer_bwd(cfg_e, P, xd[b], dYd[b], bufs_e.fwd_struct, bufs_e.bwd_struct,
+                            dxd[b], dW_r, dW13, dW2, bufs_e.scratch)
             done[b].record(stream)
             with torch.cuda.stream(cd):
                 cd.wait_event(done[b])
@@ -466,7 +487,7 @@ def run_ours(args, rank, world, local):
     torch.cuda.synchronize(dev)
     e2e_ms = e0.elapsed_time(e1)
     clk = clocks.stop()
-    status = B.moe_last_device_status(sc)
+    status = B.moe_last_device_status(sc) or B.moe_last_device_status(bufs_e.scratch)
     if status != 0:
         raise RuntimeError(f"device status {status} after timed steps")
     if not torch.equal(outh[(args.steps - 1) & 1], out.cpu()):
@@ -526,7 +547,8 @@ def run_ours(args, rank, world, local):
                                f"F={F} capacity_factor={cf if cf > 0 else 'dropless'} "
                                f"dtype={dt_name}"
                                + (" weights_in_expert" if reord else "")
-                               + (" recompute_h" if shape.recompute_h else "") + " fwd+bwd",
+                               + (" recompute_h" if shape.recompute_h else "")
+                               + (" paged_stash(e2e)" if args.paged_stash else "") + " fwd+bwd",
                    "l2": "inputs larger than L2 (expert weights "
                          f"{2 * G * 3 * H * F / 1e9:.2f} GB in bf16, streamed every step)",
                    "parallelism": "replicas" if world > 1 else "single GPU"},
@@ -547,6 +569,7 @@ def run_ours(args, rank, world, local):
                                                              bf16_peak))},
         "stages": stage_table(shape, f, stage_ms, pk["hbm_gbs"], fl, tc_peak, bf16_peak),
         "stash_bytes": stash_bytes(shape, bufs),
+        "paged_stash": stash,
         "clocks": clk,
     }
     if fp8:

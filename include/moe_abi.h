@@ -60,7 +60,8 @@ typedef enum moe_status {
     MOE_ERR_WORKSPACE = 3,     /* scratch too small                           */
     MOE_ERR_CUDA = 4,          /* a CUDA runtime call failed                  */
     MOE_ERR_TIMEOUT = 5,       /* a device-side bounded wait ran out          */
-    MOE_ERR_DEVICE_CHECK = 6   /* a kernel found an out-of-range index        */
+    MOE_ERR_DEVICE_CHECK = 6,  /* a kernel found an out-of-range index        */
+    MOE_ERR_STASH_FULL = 7     /* a layer's rows did not fit its stash pool   */
 } moe_status;
 
 enum { MOE_SCORE_SOFTMAX = 0, MOE_SCORE_SIGMOID = 1 };
@@ -106,6 +107,16 @@ typedef struct moe_config {
                               * moe_grouped_ffn_bwd pass h to the data gradient,
                               * so the h the forward wrote need not survive
                               * until the backward. 0: h is read as stored.  */
+    int32_t stash_pool_pages; /* 0: x_perm, GU, h and y_perm of moe_fwd_state
+                               * are this layer's own R-row buffers. P > 0:
+                               * they are the tensors of a stash pool of P
+                               * pages of 128 rows (plus one spill page:
+                               * (P + 1) * 128 rows each), shared by every layer
+                               * of a step; moe_layer_fwd takes the pages its
+                               * rows need on the device (paged stashing inside
+                               * a CUDA graph instead of worst-case buffers,
+                               * es summary §2.3.C), moe_layer_bwd gives them
+                               * back. See moe_fwd_state.stash_table.       */
 } moe_config;
 
 /* Worst-case sizes of the caller-owned buffers for one configuration. */
@@ -114,6 +125,8 @@ typedef struct moe_sizes {
     int64_t groups;          /* G = E + n_shared                                */
     int64_t capacity;        /* C rows per expert (0 = dropless)                */
     int64_t scratch_bytes;   /* bytes of `scratch` (zero-fill it once)          */
+    int64_t stash_table_len; /* int32 entries of moe_fwd_state.stash_table:
+                              * R / 128 + 2                                     */
 } moe_sizes;
 
 /* Layer parameters (device pointers).
@@ -143,6 +156,23 @@ typedef struct moe_fwd_state {
     void* GU;                /* [R,2F]  bf16 gate|up pre-activations            */
     void* h;                 /* [R,F]   bf16 SwiGLU output                      */
     void* y_perm;            /* [R,H]   bf16 expert outputs                     */
+    /* Paged stash (cfg->stash_pool_pages = P > 0; both NULL otherwise).
+     * The four row tensors above then hold (P + 1) * 128 rows and are shared
+     * by the layers of a pool; row r of this layer (r as in row_of, token_of,
+     * offsets) is row stash_table[r / 128] * 128 + r % 128 of them.
+     * moe_layer_fwd writes the table on the device: the 128-row blocks that
+     * hold the layer's kept rows (ceil(counts[g] / 128) blocks of group g, at
+     * offsets[g] / 128 ...) get consecutive pages from *stash_top on, every
+     * other block gets the spill page P; entry R/128 + 1 holds the first page
+     * taken. When the blocks do not fit (*stash_top + blocks > P) no page is
+     * taken, every block gets page P, MOE_ERR_STASH_FULL is recorded in the
+     * status word and the step's results are invalid (all writes stay inside
+     * the pool). moe_layer_bwd (or moe_stash_release) resets *stash_top to
+     * that first page, so the layers of a pool must run their backward in the
+     * reverse order of their forward. */
+    int32_t* stash_table;    /* [R/128 + 2] int32, caller-owned, per layer       */
+    int32_t* stash_top;      /* [1] int32: pages in use, shared by the pool's
+                              * layers; zero it once before the first forward   */
 } moe_fwd_state;
 
 /* Backward temporaries (device pointers, caller-owned). */
@@ -476,11 +506,17 @@ MOE_API moe_status moe_layer_fwd(const moe_config* cfg, const moe_params* params
                          void* out, const moe_fwd_state* st, void* scratch, void* stream);
 
 /* The whole layer backward from the forward state: dx (bf16), dW_r (fp32),
- * dW13, dW2 (bf16). */
+ * dW13, dW2 (bf16). With a paged stash it ends with moe_stash_release. */
 MOE_API moe_status moe_layer_bwd(const moe_config* cfg, const moe_params* params, const void* x,
                          const void* dY, const moe_fwd_state* st, const moe_bwd_state* bs,
                          void* dx, float* dW_r, void* dW13, void* dW2, void* scratch,
                          void* stream);
+
+/* Gives back the stash pages the layer's forward took (cfg->stash_pool_pages
+ * > 0): *stash_top = the layer's first page, on the device. moe_layer_bwd calls
+ * it; a forward that is not followed by a backward (evaluation) calls it
+ * itself. Returns MOE_ERR_INVALID_ARG without a pool or for NULL pointers. */
+MOE_API moe_status moe_stash_release(const moe_config* cfg, const moe_fwd_state* st, void* stream);
 
 /* Synchronises `stream`, then copies the device status word from scratch to
  * *code (0 = no problem recorded). */

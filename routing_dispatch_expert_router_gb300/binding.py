@@ -17,7 +17,7 @@ from .build import LIB_PATH
 MOE_OK = 0
 STATUS_NAMES = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED",
                 3: "MOE_ERR_WORKSPACE", 4: "MOE_ERR_CUDA", 5: "MOE_ERR_TIMEOUT",
-                6: "MOE_ERR_DEVICE_CHECK"}
+                6: "MOE_ERR_DEVICE_CHECK", 7: "MOE_ERR_STASH_FULL"}
 
 # every exported entry point of include/moe_abi.h
 ENTRY_POINTS = (
@@ -27,7 +27,8 @@ ENTRY_POINTS = (
     "moe_unpermute_bwd", "moe_grouped_ffn_dgrad", "moe_grouped_ffn_wgrad", "moe_grouped_ffn_bwd",
     "moe_grouped_ffn_fwd_reordered", "moe_unpermute_bwd_reordered",
     "moe_grouped_ffn_dgrad_reordered", "moe_route_bwd", "moe_permute_bwd",
-    "moe_router_wgrad", "moe_layer_fwd", "moe_layer_bwd", "moe_last_device_status",
+    "moe_router_wgrad", "moe_layer_fwd", "moe_layer_bwd", "moe_stash_release",
+    "moe_last_device_status",
     "moe_clear_device_status", "moe_check_bounded_wait", "moe_status_string",
 )
 
@@ -45,12 +46,14 @@ class MoEConfig(ctypes.Structure):
                 ("topk_groups", ctypes.c_int32), ("group_score", ctypes.c_int32),
                 ("route_scale", ctypes.c_float), ("dtype", ctypes.c_int32),
                 ("capacity_factor", ctypes.c_float), ("row_align", ctypes.c_int32),
-                ("weights_in_expert", ctypes.c_int32), ("recompute_h", ctypes.c_int32)]
+                ("weights_in_expert", ctypes.c_int32), ("recompute_h", ctypes.c_int32),
+                ("stash_pool_pages", ctypes.c_int32)]
 
 
 class MoESizes(ctypes.Structure):
     _fields_ = [("rows_max", ctypes.c_int64), ("groups", ctypes.c_int64),
-                ("capacity", ctypes.c_int64), ("scratch_bytes", ctypes.c_int64)]
+                ("capacity", ctypes.c_int64), ("scratch_bytes", ctypes.c_int64),
+                ("stash_table_len", ctypes.c_int64)]
 
 
 _P = ctypes.c_void_p
@@ -65,8 +68,12 @@ FWD_FIELDS = ("logits", "idx", "w", "counts", "offsets", "row_of", "token_of", "
 BWD_FIELDS = ("dO_perm", "dw", "dlogits", "dGU", "dX_perm")
 
 
+# the paged stash's per-layer page table and the pool's page counter
+STASH_FIELDS = ("stash_table", "stash_top")
+
+
 class MoEFwdState(ctypes.Structure):
-    _fields_ = [(n, _P) for n in FWD_FIELDS]
+    _fields_ = [(n, _P) for n in FWD_FIELDS + STASH_FIELDS]
 
 
 class MoEBwdState(ctypes.Structure):
@@ -115,7 +122,8 @@ def config(shape) -> MoEConfig:
                      capacity_factor=getattr(shape, "capacity_factor", 0.0),
                      row_align=getattr(shape, "row_align", 128),
                      weights_in_expert=getattr(shape, "weights_in_expert", 0),
-                     recompute_h=getattr(shape, "recompute_h", 0))
+                     recompute_h=getattr(shape, "recompute_h", 0),
+                     stash_pool_pages=getattr(shape, "stash_pool_pages", 0))
 
 
 def _cfg(c) -> MoEConfig:
@@ -288,6 +296,10 @@ def moe_layer_bwd(cfg, params: MoEParams, x, dY, fwd: MoEFwdState, bwd: MoEBwdSt
           _stream(stream))
 
 
+def moe_stash_release(cfg, fwd: MoEFwdState, stream=None):
+    _call("moe_stash_release", _cfg(cfg), fwd, _stream(stream))
+
+
 def moe_last_device_status(scratch, stream=None) -> int:
     code = ctypes.c_int32(0)
     _check("moe_last_device_status",
@@ -319,8 +331,30 @@ class LayerBuffers:
     bwd_struct: MoEBwdState
 
 
-def alloc_buffers(cfg, device="cuda", backward: bool = True) -> LayerBuffers:
-    """Allocates (torch.empty / zeros) every buffer the layer calls need."""
+@dataclass
+class StashPool:
+    """The rows layers keep for their backward, in pages of 128 rows shared by
+    the layers of a step: x_perm, GU, h, y_perm with (pages + 1) * 128 rows
+    (the last page is the spill page) and the device page counter."""
+    pages: int
+    tensors: dict
+    top: torch.Tensor
+
+
+def alloc_stash_pool(cfg, pages: int, device="cuda") -> StashPool:
+    c = _cfg(cfg)
+    rows = (int(pages) + 1) * 128
+    bf = torch.bfloat16
+    e = lambda *s: torch.empty(*s, dtype=bf, device=device)  # noqa: E731
+    t = dict(x_perm=e(rows, c.H), GU=e(rows, 2 * c.F), h=e(rows, c.F), y_perm=e(rows, c.H))
+    return StashPool(int(pages), t, torch.zeros(1, dtype=torch.int32, device=device))
+
+
+def alloc_buffers(cfg, device="cuda", backward: bool = True,
+                  pool: StashPool | None = None) -> LayerBuffers:
+    """Allocates (torch.empty / zeros) every buffer the layer calls need; with
+    a stash pool (cfg.stash_pool_pages == pool.pages) the four stashed row
+    tensors are the pool's and the layer gets its own page table."""
     c = _cfg(cfg)
     sz = moe_query_sizes(c)
     R, G = int(sz.rows_max), int(sz.groups)
@@ -330,14 +364,22 @@ def alloc_buffers(cfg, device="cuda", backward: bool = True) -> LayerBuffers:
     fwd = dict(logits=e(T, E, dt=f32), idx=e(T, k, dt=i32), w=e(T, k, dt=f32),
                counts=e(G, dt=i32), offsets=e(G + 1, dt=i32), row_of=e(T, k, dt=i32),
                token_of=e(R, dt=i32), sel_offsets=e(E + 1, dt=i32),
-               sel_tokens=e(max(T * k, 1), dt=i32), x_perm=e(R, H, dt=bf),
-               GU=e(R, 2 * F, dt=bf), h=e(R, F, dt=bf), y_perm=e(R, H, dt=bf))
+               sel_tokens=e(max(T * k, 1), dt=i32))
+    if pool is None:
+        fwd.update(x_perm=e(R, H, dt=bf), GU=e(R, 2 * F, dt=bf), h=e(R, F, dt=bf),
+                   y_perm=e(R, H, dt=bf))
+    else:
+        if c.stash_pool_pages != pool.pages:
+            raise ValueError("cfg.stash_pool_pages must equal the pool's pages")
+        fwd.update(pool.tensors)
+        fwd.update(stash_table=e(int(sz.stash_table_len), dt=i32), stash_top=pool.top)
     bwd = {}
     if backward:
         bwd = dict(dO_perm=e(R, H, dt=bf), dw=e(T, k, dt=f32), dlogits=e(T, E, dt=f32),
                    dGU=e(R, 2 * F, dt=bf), dX_perm=e(R, H, dt=bf))
     scratch = torch.zeros(int(sz.scratch_bytes), dtype=torch.uint8, device=device)
-    fs = MoEFwdState(**{n: fwd[n].data_ptr() for n in FWD_FIELDS})
+    fs = MoEFwdState(**{n: (fwd[n].data_ptr() if n in fwd else 0)
+                        for n in FWD_FIELDS + STASH_FIELDS})
     bs = MoEBwdState(**{n: (bwd[n].data_ptr() if bwd else 0) for n in BWD_FIELDS})
     return LayerBuffers(sz, fwd, bwd, scratch, fs, bs)
 

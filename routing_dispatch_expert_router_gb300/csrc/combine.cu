@@ -60,7 +60,7 @@ gather_reduce_kernel(const __nv_bfloat16* __restrict__ src, const int32_t* __res
                      const float* __restrict__ w, const int32_t* __restrict__ offsets,
                      const int32_t* __restrict__ idx, const float* __restrict__ dlogits,
                      const float* __restrict__ W_r, __nv_bfloat16* __restrict__ out, int T,
-                     int H, int k, int E, int S) {
+                     int H, int k, int E, int S, const int32_t* __restrict__ pages) {
   const int lane = threadIdx.x & 31;
   const int nvec = H >> 3, nr = k + S;
   const int warps = gridDim.x * (blockDim.x >> 5);
@@ -69,19 +69,24 @@ gather_reduce_kernel(const __nv_bfloat16* __restrict__ src, const int32_t* __res
   for (int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); t < T; t += warps) {
     int myrow = -1, mye = -1;
     float mywt = 0.f, mydl = 0.f;
-    if (lane < nr) slot_row(row_of, w, offsets, t, lane, k, E, myrow, mywt);
+    if (lane < nr) {
+      slot_row(row_of, w, offsets, t, lane, k, E, myrow, mywt);
+      if (myrow >= 0) myrow = stash_row(pages, myrow);
+    }
     if (ROUTER && lane < k) {
       mye = idx[(size_t)t * k + lane];
       if ((unsigned)mye < (unsigned)E) mydl = dlogits[(size_t)t * E + mye];
       else mye = -1;
     }
-    int rows[MAXR], es[MAXR];
-    float wts[MAXR], dls[MAXR];
+    // (router terms exist for the k routed slots only, k <= kMaxK)
+    constexpr int RK = MAXR < kMaxK ? MAXR : kMaxK;
+    int rows[MAXR], es[RK];
+    float wts[MAXR], dls[RK];
 #pragma unroll
     for (int j = 0; j < MAXR; ++j) {
       rows[j] = __shfl_sync(0xffffffffu, myrow, j);
       wts[j] = __shfl_sync(0xffffffffu, mywt, j);
-      if (ROUTER) {
+      if (ROUTER && j < RK) {
         es[j] = __shfl_sync(0xffffffffu, mye, j);
         dls[j] = __shfl_sync(0xffffffffu, mydl, j);
       }
@@ -118,7 +123,7 @@ gather_reduce_kernel(const __nv_bfloat16* __restrict__ src, const int32_t* __res
         }
         if (ROUTER) {
 #pragma unroll
-          for (int j = 0; j < MAXR; ++j) {
+          for (int j = 0; j < RK; ++j) {
             if (j >= k || es[j] < 0 || rows[j] >= 0) continue;
             const float d = dls[j];
             const float* wr = W_r + (size_t)es[j] * H + (size_t)c * 8;
@@ -167,7 +172,8 @@ unpermute_bwd_kernel(const __nv_bfloat16* __restrict__ dY, const __nv_bfloat16* 
                      const int32_t* __restrict__ row_of, const float* __restrict__ w,
                      const int32_t* __restrict__ counts, const int32_t* __restrict__ offsets,
                      __nv_bfloat16* __restrict__ dO, float* __restrict__ dw, int T, int H, int k,
-                     int E, int S, uint8_t* __restrict__ dOq, uint8_t* __restrict__ dOsf) {
+                     int E, int S, uint8_t* __restrict__ dOq, uint8_t* __restrict__ dOsf,
+                     const int32_t* __restrict__ pages) {
   __shared__ int s_pp[kMaxGroups + 1];
   __shared__ int s_off[kMaxGroups + 1];
   __shared__ int s_cnt[kMaxGroups];
@@ -231,8 +237,8 @@ unpermute_bwd_kernel(const __nv_bfloat16* __restrict__ dY, const __nv_bfloat16* 
         gq[u] = ldg_nc_v4(gsrc + (size_t)c * 8);
 #pragma unroll
         for (int j = 0; j < MAXR; ++j)
-          if (!COPY && j < k && rows[j] >= 0)
-            yq[u][j] = ldg_nc_v4(y + (size_t)rows[j] * H + (size_t)c * 8);
+          if (!COPY && j < k && rows[j] >= 0)     // y_perm may live in stash pages, dO_perm not
+            yq[u][j] = ldg_nc_v4(y + (size_t)stash_row(pages, rows[j]) * H + (size_t)c * 8);
       }
 #pragma unroll
       for (int u = 0; u < U; ++u) {
@@ -448,7 +454,7 @@ static cudaError_t launch_gather_reduce(const moe_config& c, const void* src,
                                         const int32_t* row_of, const float* w,
                                         const int32_t* offsets, const int32_t* idx,
                                         const float* dlogits, const float* W_r, void* out,
-                                        cudaStream_t s) {
+                                        cudaStream_t s, const int32_t* pages = nullptr) {
   auto sp = static_cast<const __nv_bfloat16*>(src);
   auto o = static_cast<__nv_bfloat16*>(out);
   const int nr = c.k + c.n_shared;
@@ -456,27 +462,33 @@ static cudaError_t launch_gather_reduce(const moe_config& c, const void* src,
   if (nr <= 2)
     gather_reduce_kernel<2, 4, ROUTER><<<grid, 256, 0, s>>>(sp, row_of, w, offsets, idx, dlogits,
                                                            W_r, o, c.T, c.H, c.k, c.E,
-                                                           c.n_shared);
+                                                           c.n_shared, pages);
   else if (nr <= 4)
     gather_reduce_kernel<4, 2, ROUTER><<<grid, 256, 0, s>>>(sp, row_of, w, offsets, idx, dlogits,
                                                            W_r, o, c.T, c.H, c.k, c.E,
-                                                           c.n_shared);
+                                                           c.n_shared, pages);
+  else if (nr <= 8)    // top-8 without shared experts: a third fewer registers than 12
+    gather_reduce_kernel<8, 1, ROUTER><<<grid, 256, 0, s>>>(sp, row_of, w, offsets, idx, dlogits,
+                                                           W_r, o, c.T, c.H, c.k, c.E,
+                                                           c.n_shared, pages);
   else
     gather_reduce_kernel<kMaxK + 4, 1, ROUTER><<<grid, 256, 0, s>>>(
-        sp, row_of, w, offsets, idx, dlogits, W_r, o, c.T, c.H, c.k, c.E, c.n_shared);
+        sp, row_of, w, offsets, idx, dlogits, W_r, o, c.T, c.H, c.k, c.E, c.n_shared, pages);
   return cudaGetLastError();
 }
 
 cudaError_t launch_unpermute(const moe_config& c, const void* y_perm, const int32_t* row_of,
-                             const float* w, const int32_t* offsets, void* out, cudaStream_t s) {
+                             const float* w, const int32_t* offsets, void* out, cudaStream_t s,
+                             const int32_t* pages) {
   return launch_gather_reduce<false>(c, y_perm, row_of, w, offsets, nullptr, nullptr, nullptr, out,
-                                     s);
+                                     s, pages);
 }
 
 cudaError_t launch_unpermute_bwd(const moe_config& c, const void* dY, const void* y_perm,
                                  const int32_t* row_of, const float* w, const int32_t* counts,
                                  const int32_t* offsets, void* dO_perm, float* dw,
-                                 cudaStream_t s, uint8_t* dOq, uint8_t* dOsf) {
+                                 cudaStream_t s, uint8_t* dOq, uint8_t* dOsf,
+                                 const int32_t* pages) {
   auto dYp = static_cast<const __nv_bfloat16*>(dY);
   auto yp = static_cast<const __nv_bfloat16*>(y_perm);
   auto dOp = static_cast<__nv_bfloat16*>(dO_perm);
@@ -484,13 +496,20 @@ cudaError_t launch_unpermute_bwd(const moe_config& c, const void* dY, const void
   const int grid = grid_for_warps(c.T);
   if (c.k + c.n_shared <= 2)
     unpermute_bwd_kernel<2, 4><<<grid, 256, 0, s>>>(dYp, yp, row_of, w, counts, offsets, dOp, dw,
-                                                    c.T, c.H, c.k, c.E, c.n_shared, dOq, dOsf);
+                                                    c.T, c.H, c.k, c.E, c.n_shared, dOq, dOsf,
+                                                    pages);
   else if (c.k + c.n_shared <= 4)
     unpermute_bwd_kernel<4, 4><<<grid, 256, 0, s>>>(dYp, yp, row_of, w, counts, offsets, dOp, dw,
-                                                    c.T, c.H, c.k, c.E, c.n_shared, dOq, dOsf);
+                                                    c.T, c.H, c.k, c.E, c.n_shared, dOq, dOsf,
+                                                    pages);
+  else if (c.k + c.n_shared <= 8)
+    unpermute_bwd_kernel<8, 1><<<grid, 256, 0, s>>>(dYp, yp, row_of, w, counts, offsets, dOp, dw,
+                                                    c.T, c.H, c.k, c.E, c.n_shared, dOq, dOsf,
+                                                    pages);
   else
     unpermute_bwd_kernel<kMaxK + 4, 1><<<grid, 256, 0, s>>>(
-        dYp, yp, row_of, w, counts, offsets, dOp, dw, c.T, c.H, c.k, c.E, c.n_shared, dOq, dOsf);
+        dYp, yp, row_of, w, counts, offsets, dOp, dw, c.T, c.H, c.k, c.E, c.n_shared, dOq, dOsf,
+        pages);
   return cudaGetLastError();
 }
 
@@ -503,15 +522,17 @@ cudaError_t launch_unpermute_bwd_copy(const moe_config& c, const void* dY, const
   if (c.k + c.n_shared <= 2)
     unpermute_bwd_kernel<2, 4, true><<<grid, 256, 0, s>>>(dYp, nullptr, row_of, nullptr, counts,
                                                           offsets, dOp, nullptr, c.T, c.H, c.k,
-                                                          c.E, c.n_shared, nullptr, nullptr);
+                                                          c.E, c.n_shared, nullptr, nullptr,
+                                                          nullptr);
   else if (c.k + c.n_shared <= 4)
     unpermute_bwd_kernel<4, 4, true><<<grid, 256, 0, s>>>(dYp, nullptr, row_of, nullptr, counts,
                                                           offsets, dOp, nullptr, c.T, c.H, c.k,
-                                                          c.E, c.n_shared, nullptr, nullptr);
+                                                          c.E, c.n_shared, nullptr, nullptr,
+                                                          nullptr);
   else
     unpermute_bwd_kernel<kMaxK + 4, 1, true><<<grid, 256, 0, s>>>(
         dYp, nullptr, row_of, nullptr, counts, offsets, dOp, nullptr, c.T, c.H, c.k, c.E,
-        c.n_shared, nullptr, nullptr);
+        c.n_shared, nullptr, nullptr, nullptr);
   return cudaGetLastError();
 }
 

@@ -25,6 +25,14 @@ __device__ __forceinline__ void record_status(int32_t* status, int32_t code) {
   if (status) atomicCAS(status, 0, code);
 }
 
+// Row of a layer's stash tensors (x_perm, GU, h, y_perm) that holds its row r:
+// with a stash page table (paged stashing), row r lives in page pages[r / 128]
+// of the pool; without one (pages == nullptr) the layer's own buffers hold it
+// at row r.
+__device__ __forceinline__ int stash_row(const int32_t* __restrict__ pages, int r) {
+  return pages ? (__ldg(pages + (r >> 7)) << 7) | (r & 127) : r;
+}
+
 __device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xffff0000u); }
 

@@ -86,7 +86,23 @@ struct Params {
   // B, which is the smaller operand and stays in L2 (Mixtral-sized dW13: the
   // group's dGU is read from DRAM once instead of about four times).
   int n_fast;
+  // Paged stash: the row tensors marked in page_ops (kPage*) are pool tensors
+  // whose row r is row pages[r / 128] * 128 + r % 128 (every tile and k-block
+  // stays inside one 128-row block, so one look-up serves a whole box).
+  const int32_t* pages;
+  int page_ops;
 };
+
+enum PageOps : int {
+  kPageA = 1,     // A's rows (row-grouped: the tile's rows; K-grouped: the k-block's)
+  kPageB = 2,     // B's k-block rows of a K-grouped launch
+  kPageOut = 4,   // the rows the epilogue stores (row-grouped launches)
+  kPageAux = 8,   // the SwiGLU backward's GU rows and the rows of h_out
+};
+
+__device__ __forceinline__ int page_row(const Params& p, int op, int r) {
+  return (p.page_ops & op) ? stash_row(p.pages, r) : r;
+}
 
 // Router logits (kEpiStoreF32) multiply each A k-block by the three bf16 parts
 // of the fp32 weight, held in B as three consecutive 64-column blocks: one

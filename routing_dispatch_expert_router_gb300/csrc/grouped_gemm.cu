@@ -43,6 +43,9 @@ __device__ __forceinline__ void epilogue_tile(const Params& p, const CUtensorMap
                                               const int* s_off, uint8_t* stage,
                                               uint32_t stage_u32) {
   const int row0 = p.kgrouped ? g * p.Mw + mt * BM + q * 32 : s_off[g] + mt * BM + q * 32;
+  // rows of the stored tensor and of GU / h_out (these 32 rows share a 128-row block)
+  const int orow = p.kgrouped ? row0 : page_row(p, kPageOut, row0);
+  const int xrow = p.kgrouped ? row0 : page_row(p, kPageAux, row0);
   const int ncols = swiglu_fwd(EPI) ? BN / 2 : BN;
   const int f0 = swiglu_fwd(EPI) ? nt * (BN / 2) : nt * BN;
   // router term of this warp's row (lane) for the FC1 data gradient
@@ -115,7 +118,7 @@ __device__ __forceinline__ void epilogue_tile(const Params& p, const CUtensorMap
       ptx::fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) {
-        ptx::tma_store_2d(tmC, stage_u32, f0 + c, row0);
+        ptx::tma_store_2d(tmC, stage_u32, f0 + c, orow);
         ptx::tma_store_commit();
       }
     }
@@ -130,7 +133,7 @@ __device__ __forceinline__ void epilogue_tile(const Params& p, const CUtensorMap
   const __nv_bfloat16* gu = nullptr;
   if (swiglu_bwd(EPI)) {
     // G and U of the next 32 columns are loaded one slice ahead
-    gu = p.aux + (long long)(row0 + lane) * p.ldaux;
+    gu = p.aux + (long long)(xrow + lane) * p.ldaux;
 #pragma unroll
     for (int v = 0; v < 4; ++v) {
       gq[v] = ldg_nc_v4(gu + f0 + v * 8);
@@ -168,7 +171,7 @@ __device__ __forceinline__ void epilogue_tile(const Params& p, const CUtensorMap
       }
       ptx::tmem_ld_wait();
       __nv_bfloat16* hrow =
-          p.h_out ? p.h_out + (long long)(row0 + lane) * p.F + f0 + c : nullptr;
+          p.h_out ? p.h_out + (long long)(xrow + lane) * p.F + f0 + c : nullptr;
 #pragma unroll
       for (int v = 0; v < 4; ++v) {
         if (WGT) swiglu_bwd8_w(r + v * 8, gq[v], uq[v], rwt, o0[v], o1[v], dot);
@@ -194,7 +197,7 @@ __device__ __forceinline__ void epilogue_tile(const Params& p, const CUtensorMap
       ptx::fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) {
-        ptx::tma_store_2d(tmC, stage_u32, f0 + c, row0);
+        ptx::tma_store_2d(tmC, stage_u32, f0 + c, orow);
         ptx::tma_store_commit();
       }
       continue;
@@ -209,12 +212,12 @@ __device__ __forceinline__ void epilogue_tile(const Params& p, const CUtensorMap
     __syncwarp();
     if (lane == 0) {
       if (swiglu_fwd(EPI)) {
-        ptx::tma_store_2d(tmC, stage_u32, f0 + c, row0);                      // G
-        ptx::tma_store_2d(tmC, stage_u32 + kBoxBytes, p.F + f0 + c, row0);    // U
-        ptx::tma_store_2d(tmC2, stage_u32 + 2 * kBoxBytes, f0 + c, row0);     // h
+        ptx::tma_store_2d(tmC, stage_u32, f0 + c, orow);                      // G
+        ptx::tma_store_2d(tmC, stage_u32 + kBoxBytes, p.F + f0 + c, orow);    // U
+        ptx::tma_store_2d(tmC2, stage_u32 + 2 * kBoxBytes, f0 + c, orow);     // h
       } else {
-        ptx::tma_store_2d(tmC, stage_u32, f0 + c, row0);                      // dG
-        ptx::tma_store_2d(tmC, stage_u32 + kBoxBytes, p.F + f0 + c, row0);    // dU
+        ptx::tma_store_2d(tmC, stage_u32, f0 + c, orow);                      // dG
+        ptx::tma_store_2d(tmC, stage_u32 + kBoxBytes, p.F + f0 + c, orow);    // dU
       }
       ptx::tma_store_commit();
     }
@@ -311,9 +314,9 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
           const uint32_t sB = sA + L::A_BYTES;
           const int k0 = kb * BK;
           if (A_MN == 0) {
-            ptx::tma_load_2d(sA, &tmA, fb, k0, s_off[t.g] + t.mt * BM);
+            ptx::tma_load_2d(sA, &tmA, fb, k0, page_row(p, kPageA, s_off[t.g] + t.mt * BM));
           } else {
-            const int kr = s_off[t.g] + k0;
+            const int kr = page_row(p, kPageA, s_off[t.g] + k0);
             ptx::tma_load_2d(sA, &tmA, fb, t.mt * BM, kr);
             ptx::tma_load_2d(sA + 8192, &tmA, fb, t.mt * BM + 64, kr);
           }
@@ -327,7 +330,8 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
               ptx::tma_load_2d(sB + q * L::B_BYTES, &tmB, fb, BPARTS * k0 + q * BK,
                                t.g * p.b_rows + t.nt * BN);
           } else {
-            const int kr = p.kgrouped ? s_off[t.g] + k0 : t.g * p.b_rows + k0;
+            const int kr =
+                p.kgrouped ? page_row(p, kPageB, s_off[t.g] + k0) : t.g * p.b_rows + k0;
 #pragma unroll
             for (int q = 0; q < BPARTS; ++q)
 #pragma unroll
@@ -625,9 +629,9 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA,
           const uint32_t sB = sA + A_BYTES;
           const int k0 = kb * BK;
           if (A_MN == 0) {
-            ptx::tma_load_2d_pair(sA, &tmA, fb, k0, s_off[g] + mt * BM);
+            ptx::tma_load_2d_pair(sA, &tmA, fb, k0, page_row(p, kPageA, s_off[g] + mt * BM));
           } else {
-            const int kr = s_off[g] + k0;
+            const int kr = page_row(p, kPageA, s_off[g] + k0);
             ptx::tma_load_2d_pair(sA, &tmA, fb, mt * BM, kr);
             ptx::tma_load_2d_pair(sA + 8192, &tmA, fb, mt * BM + 64, kr);
           }
@@ -638,7 +642,7 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA,
           } else if (B_MN == 0) {
             ptx::tma_load_2d_pair(sB, &tmB, fb, k0, g * p.b_rows + nt * BN + (int)rank * 128);
           } else {
-            const int kr = p.kgrouped ? s_off[g] + k0 : g * p.b_rows + k0;
+            const int kr = p.kgrouped ? page_row(p, kPageB, s_off[g] + k0) : g * p.b_rows + k0;
             ptx::tma_load_2d_pair(sB, &tmB, fb, nt * BN + (int)rank * 128, kr);
             ptx::tma_load_2d_pair(sB + 8192, &tmB, fb, nt * BN + (int)rank * 128 + 64, kr);
           }
@@ -744,8 +748,9 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA,
       if (lane == 0) {
         const uint32_t b = rbar + 8 * slot, dst = ring_u32 + slot * kGuSlotBytes;
         ptx::mbar_arrive_expect_tx(b, kGuSlotBytes);
-        ptx::tma_load_2d(dst, &tmC2, b, lf0 + lc, lrow);                  // G
-        ptx::tma_load_2d(dst + kBoxBytes, &tmC2, b, p.F + lf0 + lc, lrow);  // U
+        const int grow = page_row(p, kPageAux, lrow);
+        ptx::tma_load_2d(dst, &tmC2, b, lf0 + lc, grow);                  // G
+        ptx::tma_load_2d(dst + kBoxBytes, &tmC2, b, p.F + lf0 + lc, grow);  // U
       }
       ++issued;
       lc += 32;
@@ -782,13 +787,15 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA,
           ptx::tmem_ld_wait();
           swiglu_bwd_slice_inplace<WGT>(
               ring + slot * kGuSlotBytes, lane, r, rwt, dot,
-              p.h_out ? p.h_out + (long long)(row0 + lane) * p.F + f0 + c : nullptr);
+              p.h_out ? p.h_out + (long long)(page_row(p, kPageAux, row0) + lane) * p.F + f0 + c
+                      : nullptr);
           ptx::fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0) {
             const uint32_t src = ring_u32 + slot * kGuSlotBytes;
-            ptx::tma_store_2d(&tmC, src, f0 + c, row0);                    // dG
-            ptx::tma_store_2d(&tmC, src + kBoxBytes, p.F + f0 + c, row0);  // dU
+            const int orow = page_row(p, kPageOut, row0);
+            ptx::tma_store_2d(&tmC, src, f0 + c, orow);                    // dG
+            ptx::tma_store_2d(&tmC, src + kBoxBytes, p.F + f0 + c, orow);  // dU
             ptx::tma_store_commit();
             // the slot of the slice before this one is free once its stores have read it
             ptx::tma_store_wait_read_1();
@@ -931,14 +938,18 @@ int dw_tiles(const moe_config& c) { return c.F % 256 == 0 ? c.F / 256 : c.F / 12
 
 cudaError_t launch_ffn_fc1(const moe_config& c, const void* x_perm, const int32_t* counts,
                            const int32_t* offsets, const void* W13, void* GU, void* h,
-                           int32_t* status, cudaStream_t s, const float* row_w) {
-  const int64_t R = rows_max(c);
+                           int32_t* status, cudaStream_t s, const float* row_w,
+                           const StashMap& sm) {
+  const int64_t SR = stash_rows(c, sm);
   const int G = c.E + c.n_shared;
   CUtensorMap a, b, oc, oc2;
-  if (!make_map(&a, x_perm, c.H, R, 128) || !make_map(&b, W13, c.H, (uint64_t)G * 2 * c.F, 128) ||
-      !make_out_map(&oc, GU, 2ULL * c.F, R) || !make_out_map(&oc2, h, c.F, R))
+  if (!make_map(&a, x_perm, c.H, SR, 128) ||
+      !make_map(&b, W13, c.H, (uint64_t)G * 2 * c.F, 128) ||
+      !make_out_map(&oc, GU, 2ULL * c.F, SR) || !make_out_map(&oc2, h, c.F, SR))
     return cudaErrorInvalidValue;
   Params p = base_params(c, counts, offsets, status);
+  p.pages = sm.pages;
+  p.page_ops = sm.pages ? kPageA | kPageOut : 0;
   p.K = c.H;
   p.b_rows = 2 * c.F;
   p.out = static_cast<__nv_bfloat16*>(GU);
@@ -956,18 +967,20 @@ cudaError_t launch_ffn_fc1(const moe_config& c, const void* x_perm, const int32_
 
 cudaError_t launch_ffn_fc2(const moe_config& c, const void* h, const int32_t* counts,
                            const int32_t* offsets, const void* W2, void* y_perm,
-                           int32_t* status, cudaStream_t s) {
-  const int64_t R = rows_max(c);
+                           int32_t* status, cudaStream_t s, const StashMap& sm) {
+  const int64_t SR = stash_rows(c, sm);
   const int G = c.E + c.n_shared;
   const int bn = (c.H % 256 == 0) ? 256 : 128;
   const bool pair = use_pairs(c, c.H);
   CUtensorMap a, b, oc;
-  if (!make_map(&a, h, c.F, R, 128) ||
+  if (!make_map(&a, h, c.F, SR, 128) ||
       !make_map(&b, W2, c.F, (uint64_t)G * c.H, pair ? 128 : bn) ||
-      !make_out_map_w64(&oc, y_perm, c.H, R))
+      !make_out_map_w64(&oc, y_perm, c.H, SR))
     return cudaErrorInvalidValue;
   const CUtensorMap& oc2 = oc;
   Params p = base_params(c, counts, offsets, status);
+  p.pages = sm.pages;
+  p.page_ops = sm.pages ? kPageA | kPageOut : 0;
   p.N = c.H;
   p.K = c.F;
   p.b_rows = c.H;
@@ -981,16 +994,19 @@ cudaError_t launch_ffn_fc2(const moe_config& c, const void* h, const int32_t* co
 cudaError_t launch_ffn_fc2_dgrad(const moe_config& c, const void* dO_perm, const int32_t* counts,
                                  const int32_t* offsets, const void* W2, const void* GU,
                                  void* dGU, int32_t* status, cudaStream_t s, const float* row_w,
-                                 float* dw_part, void* h_out) {
+                                 float* dw_part, void* h_out, const StashMap& sm) {
   const int64_t R = rows_max(c);
   const int G = c.E + c.n_shared;
   const int bn = (c.F % 256 == 0) ? 256 : 128;
   CUtensorMap a, b, oc, gu;
   if (!make_map(&a, dO_perm, c.H, R, 128) || !make_map(&b, W2, c.F, (uint64_t)G * c.H, 64) ||
-      !make_out_map(&oc, dGU, 2ULL * c.F, R) || !make_out_map(&gu, GU, 2ULL * c.F, R))
+      !make_out_map(&oc, dGU, 2ULL * c.F, R) ||
+      !make_out_map(&gu, GU, 2ULL * c.F, stash_rows(c, sm)))
     return cudaErrorInvalidValue;
   const CUtensorMap& oc2 = gu;    // the pair kernel loads G and U through this map
   Params p = base_params(c, counts, offsets, status);
+  p.pages = sm.pages;
+  p.page_ops = sm.pages ? kPageAux : 0;
   p.N = c.F;
   p.K = c.H;
   p.b_rows = c.H;
@@ -1043,16 +1059,18 @@ cudaError_t launch_ffn_fc1_dgrad(const moe_config& c, const void* dGU, const int
 
 cudaError_t launch_ffn_wgrad_fc2(const moe_config& c, const void* dO_perm, const void* h,
                                  const int32_t* counts, const int32_t* offsets, void* dW2,
-                                 int32_t* status, cudaStream_t s) {
+                                 int32_t* status, cudaStream_t s, const StashMap& sm) {
   const int64_t R = rows_max(c);
   const int bn = (c.F % 256 == 0) ? 256 : 128;
   const int G = c.E + c.n_shared;
   CUtensorMap a, b, oc;
-  if (!make_map(&a, dO_perm, c.H, R, 64) || !make_map(&b, h, c.F, R, 64) ||
+  if (!make_map(&a, dO_perm, c.H, R, 64) || !make_map(&b, h, c.F, stash_rows(c, sm), 64) ||
       !make_out_map_w64(&oc, dW2, c.F, (uint64_t)G * c.H))
     return cudaErrorInvalidValue;
   const CUtensorMap& oc2 = oc;
   Params p = base_params(c, counts, offsets, status);
+  p.pages = sm.pages;
+  p.page_ops = sm.pages ? kPageB : 0;
   p.kgrouped = 1;
   p.Mw = c.H;
   p.N = c.F;
@@ -1067,16 +1085,18 @@ cudaError_t launch_ffn_wgrad_fc2(const moe_config& c, const void* dO_perm, const
 
 cudaError_t launch_ffn_wgrad_fc1(const moe_config& c, const void* dGU, const void* x_perm,
                                  const int32_t* counts, const int32_t* offsets, void* dW13,
-                                 int32_t* status, cudaStream_t s) {
+                                 int32_t* status, cudaStream_t s, const StashMap& sm) {
   const int64_t R = rows_max(c);
   const int bn = (c.H % 256 == 0) ? 256 : 128;
   const int G = c.E + c.n_shared;
   CUtensorMap a, b, oc;
-  if (!make_map(&a, dGU, 2ULL * c.F, R, 64) || !make_map(&b, x_perm, c.H, R, 64) ||
+  if (!make_map(&a, dGU, 2ULL * c.F, R, 64) || !make_map(&b, x_perm, c.H, stash_rows(c, sm), 64) ||
       !make_out_map_w64(&oc, dW13, c.H, (uint64_t)G * 2 * c.F))
     return cudaErrorInvalidValue;
   const CUtensorMap& oc2 = oc;
   Params p = base_params(c, counts, offsets, status);
+  p.pages = sm.pages;
+  p.page_ops = sm.pages ? kPageB : 0;
   p.kgrouped = 1;
   p.Mw = 2 * c.F;
   p.N = c.H;

@@ -112,6 +112,9 @@ __device__ __forceinline__ bool f8_epilogue_tile(
     uint32_t stage_u32, float* xch, uint32_t xbar, volatile int* abort_flag, int g, int nt,
     int row0, int q, int half, int lane, uint32_t (&r)[128], const __nv_bfloat16* gu,
     uint4 (&gq)[4], uint4 (&uq)[4], int fb, uint32_t& x_phase) {
+  // rows of the stored tensor and of h_out (a paged stash keeps these 32 rows in one page)
+  const int orow = EPI == kEpiWgrad ? row0 : page_row(p, kPageOut, row0);
+  const int xrow = EPI == kEpiWgrad ? row0 : page_row(p, kPageAux, row0);
   if (EPI == kEpiSwigluFwd) {
     const int f0 = nt * (kF8BN / 2) + 64 * half;
     uint4 ho[2][4];
@@ -129,9 +132,9 @@ __device__ __forceinline__ bool f8_epilogue_tile(
         for (int i = 0; i < 8; ++i) hf[i] = silu_f(gr[i]) * ur[i];
         ho[c][v] = pack8(hf);
       }
-      f8_store_box(tmC, stage, stage_u32, lane, go, f0 + 32 * c, row0);          // G
-      f8_store_box(tmC, stage, stage_u32, lane, uo, p.F + f0 + 32 * c, row0);    // U
-      f8_store_box(tmC2, stage, stage_u32, lane, ho[c], f0 + 32 * c, row0);      // h
+      f8_store_box(tmC, stage, stage_u32, lane, go, f0 + 32 * c, orow);          // G
+      f8_store_box(tmC, stage, stage_u32, lane, uo, p.F + f0 + 32 * c, orow);    // U
+      f8_store_box(tmC2, stage, stage_u32, lane, ho[c], f0 + 32 * c, orow);      // h
     }
     if (!MX && p.qout) {
       // h's 1 x 128 slice (columns nt*128 ..) is this warp's 64 columns and
@@ -196,7 +199,7 @@ __device__ __forceinline__ bool f8_epilogue_tile(
       for (int v = 0; v < 4; ++v) swiglu_bwd8(&r[32 * c + 8 * v], gq[v], uq[v], dg[v], du[v]);
       if (p.h_out) {
         // fine-grained recompute: h of these 32 columns from the stored G, U
-        __nv_bfloat16* hrow = p.h_out + (long long)(row0 + lane) * p.F + fb + 32 * c;
+        __nv_bfloat16* hrow = p.h_out + (long long)(xrow + lane) * p.F + fb + 32 * c;
 #pragma unroll
         for (int v = 0; v < 4; ++v) stg_v4(hrow + 8 * v, swiglu_h8<false>(gq[v], uq[v], 1.f));
       }
@@ -207,8 +210,8 @@ __device__ __forceinline__ bool f8_epilogue_tile(
           uq[v] = ldg_nc_v4(gu + p.F + fb + 32 * (c + 1) + v * 8);
         }
       }
-      f8_store_box(tmC, stage, stage_u32, lane, dg, fb + 32 * c, row0);          // dG
-      f8_store_box(tmC, stage, stage_u32, lane, du, p.F + fb + 32 * c, row0);    // dU
+      f8_store_box(tmC, stage, stage_u32, lane, dg, fb + 32 * c, orow);          // dG
+      f8_store_box(tmC, stage, stage_u32, lane, du, p.F + fb + 32 * c, orow);    // dU
     }
   } else {
     // plain store (FC2) or FC1 data gradient plus the row's router term
@@ -235,7 +238,7 @@ __device__ __forceinline__ bool f8_epilogue_tile(
       }
       uint4 o[4];
       pack_slice(slice32(r, c), o);
-      f8_store_box(tmC, stage, stage_u32, lane, o, f0 + 32 * c, row0);
+      f8_store_box(tmC, stage, stage_u32, lane, o, f0 + 32 * c, orow);
     }
   }
   return true;
@@ -497,7 +500,7 @@ grouped_gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmA,
       int fb = 0;
       if (EPI == kEpiSwigluBwd) {
         fb = t.nt * kF8BN + 128 * half;
-        gu = p.aux + (long long)(row0 + lane) * p.ldaux;
+        gu = p.aux + (long long)(page_row(p, kPageAux, row0) + lane) * p.ldaux;
 #pragma unroll
         for (int v = 0; v < 4; ++v) {
           gq[v] = ldg_nc_v4(gu + fb + v * 8);
@@ -587,14 +590,16 @@ using namespace gg;
 cudaError_t launch_ffn_fc1_fp8(const moe_config& c, const uint8_t* xq, const uint8_t* xsf,
                                const int32_t* counts, const int32_t* offsets, const uint8_t* W13q,
                                const uint8_t* W13sf, void* GU, void* h, uint8_t* hq, uint8_t* hsf,
-                               int32_t* status, cudaStream_t s) {
-  const int64_t R = rows_max(c);
+                               int32_t* status, cudaStream_t s, const StashMap& sm) {
+  const int64_t R = rows_max(c), SR = stash_rows(c, sm);
   const int G = c.E + c.n_shared;
   CUtensorMap a, b, oc, oc2;
   if (!make_map_u8(&a, xq, c.H, R) || !make_map_u8(&b, W13q, c.H, (uint64_t)G * 2 * c.F) ||
-      !make_out_map(&oc, GU, 2ULL * c.F, R) || !make_out_map(&oc2, h, c.F, R))
+      !make_out_map(&oc, GU, 2ULL * c.F, SR) || !make_out_map(&oc2, h, c.F, SR))
     return cudaErrorInvalidValue;
   Params p = base_params(c, counts, offsets, status);
+  p.pages = sm.pages;
+  p.page_ops = sm.pages ? kPageOut : 0;       // GU and h; x and h's 1-byte forms are not paged
   p.K = c.H;
   p.b_rows = 2 * c.F;
   p.sfa = xsf;
@@ -612,14 +617,16 @@ cudaError_t launch_ffn_fc1_fp8(const moe_config& c, const uint8_t* xq, const uin
 cudaError_t launch_ffn_fc2_fp8(const moe_config& c, const uint8_t* hq, const uint8_t* hsf,
                                const int32_t* counts, const int32_t* offsets, const uint8_t* W2q,
                                const uint8_t* W2sf, void* y_perm, int32_t* status,
-                               cudaStream_t s) {
+                               cudaStream_t s, const StashMap& sm) {
   const int64_t R = rows_max(c);
   const int G = c.E + c.n_shared;
   CUtensorMap a, b, oc;
   if (!make_map_u8(&a, hq, c.F, R) || !make_map_u8(&b, W2q, c.F, (uint64_t)G * c.H) ||
-      !make_out_map(&oc, y_perm, c.H, R))
+      !make_out_map(&oc, y_perm, c.H, stash_rows(c, sm)))
     return cudaErrorInvalidValue;
   Params p = base_params(c, counts, offsets, status);
+  p.pages = sm.pages;
+  p.page_ops = sm.pages ? kPageOut : 0;
   p.N = c.H;
   p.K = c.F;
   p.b_rows = c.H;
@@ -636,7 +643,8 @@ cudaError_t launch_ffn_fc2_fp8(const moe_config& c, const uint8_t* hq, const uin
 cudaError_t launch_ffn_fc2_dgrad_fp8(const moe_config& c, const uint8_t* dOq, const uint8_t* dOsf,
                                      const int32_t* counts, const int32_t* offsets,
                                      const uint8_t* W2q, const uint8_t* W2sf_t, const void* GU,
-                                     void* dGU, int32_t* status, cudaStream_t s, void* h_out) {
+                                     void* dGU, int32_t* status, cudaStream_t s, void* h_out,
+                                     const StashMap& sm) {
   const int64_t R = rows_max(c);
   const int G = c.E + c.n_shared;
   CUtensorMap a, b, oc;
@@ -644,6 +652,8 @@ cudaError_t launch_ffn_fc2_dgrad_fp8(const moe_config& c, const uint8_t* dOq, co
       !make_out_map(&oc, dGU, 2ULL * c.F, R))
     return cudaErrorInvalidValue;
   Params p = base_params(c, counts, offsets, status);
+  p.pages = sm.pages;
+  p.page_ops = sm.pages ? kPageAux : 0;       // GU and h_out
   p.N = c.F;
   p.K = c.H;
   p.b_rows = c.H;

@@ -21,21 +21,47 @@ cudaError_t launch_route_replay(const moe_config& c, const void* x, const float*
                                 const float* bias, const int32_t* idx, float* logits, float* w,
                                 uint8_t* scratch, cudaStream_t s);
 
+// Where a layer keeps the rows its backward reads (x_perm, GU, h, y_perm):
+// row r is row pages[r / 128] * 128 + r % 128 of pool tensors of `rows` rows
+// (paged stash), or row r of the layer's own rows_max-row buffers
+// (pages == nullptr, rows == 0).
+struct StashMap {
+  const int32_t* pages = nullptr;
+  int64_t rows = 0;
+};
+int64_t stash_rows(const moe_config& c, const StashMap& sm);
+// The paged stash's allocation, done by the dispatch once the segment
+// offsets are known: the layer's page table and the pool's page counter.
+struct StashAlloc {
+  int32_t* table;
+  int32_t* top;
+  int pool_pages;
+};
+// Gives the layer's pages back: *top = table[rows_max / 128 + 1].
+cudaError_t launch_stash_release(const moe_config& c, const int32_t* table, int32_t* top,
+                                 cudaStream_t s);
+
 struct Fp8Scratch;
 // fp8 (FP8 configuration, optional): also write x_perm's 1-byte form there.
+// alloc (optional): take the layer's stash pages and write x_perm into them.
 cudaError_t launch_permute(const moe_config& c, const void* x, const int32_t* idx,
                            int32_t* counts, int32_t* offsets, int32_t* row_of, int32_t* token_of,
                            int32_t* sel_offsets, int32_t* sel_tokens, void* x_perm,
-                           uint8_t* scratch, cudaStream_t s, const Fp8Scratch* fp8 = nullptr);
+                           uint8_t* scratch, cudaStream_t s, const Fp8Scratch* fp8 = nullptr,
+                           const StashAlloc* alloc = nullptr);
 
+// pages (optional): y_perm is paged (StashMap).
 cudaError_t launch_unpermute(const moe_config& c, const void* y_perm, const int32_t* row_of,
-                             const float* w, const int32_t* offsets, void* out, cudaStream_t s);
+                             const float* w, const int32_t* offsets, void* out, cudaStream_t s,
+                             const int32_t* pages = nullptr);
 
 // dOq, dOsf (FP8 configuration, optional): also write dO_perm's 1-byte form.
+// pages (optional): y_perm is paged; dO_perm is not.
 cudaError_t launch_unpermute_bwd(const moe_config& c, const void* dY, const void* y_perm,
                                  const int32_t* row_of, const float* w, const int32_t* counts,
                                  const int32_t* offsets, void* dO_perm, float* dw, cudaStream_t s,
-                                 uint8_t* dOq = nullptr, uint8_t* dOsf = nullptr);
+                                 uint8_t* dOq = nullptr, uint8_t* dOsf = nullptr,
+                                 const int32_t* pages = nullptr);
 
 // The layer with the routing weight inside the expert: the unweighted copy of
 // dY into the expert rows (dO_perm), the routing weight of every permuted row,
@@ -91,12 +117,13 @@ int64_t aux_partial_offset(const moe_config& c);   // its byte offset in scratch
 cudaError_t launch_quant_tiles8(const void* W, uint8_t* Wq, uint8_t* sf_f, uint8_t* sf_d, int G,
                                 int rows, int cols, cudaStream_t s);
 // mx: 32-element blocks and the MX atom layout (MXFP8), else 128.
+// pages (optional): X is a paged stash tensor (StashMap); the outputs are not.
 cudaError_t launch_quant_rows8(const void* X, uint8_t* Xq, uint8_t* sf, const int32_t* offsets,
                                const int32_t* counts, int G, int64_t rows_max, int cols,
-                               cudaStream_t s, bool mx = false);
+                               cudaStream_t s, bool mx = false, const int32_t* pages = nullptr);
 cudaError_t launch_quant_cols8(const void* X, uint8_t* Xq, uint8_t* sf, const int32_t* offsets,
                                const int32_t* counts, int G, int64_t rows_max, int cols,
-                               cudaStream_t s, bool mx = false);
+                               cudaStream_t s, bool mx = false, const int32_t* pages = nullptr);
 // Both forms of one tensor from a single read: 1xBLK rows (Xr, sfr) and
 // BLKx1 columns (Xc, sfc).
 cudaError_t launch_quant_rows_cols8(const void* X, uint8_t* Xr, uint8_t* sfr, uint8_t* Xc,
@@ -160,14 +187,16 @@ int64_t router_split_offset(const moe_config& c);   // byte offset of the split 
 int64_t permute_scratch_bytes(const moe_config& c); // scratch the dispatch needs
 
 // Grouped GEMMs (tcgen05). Return cudaErrorInvalidValue when a tensor map
-// cannot be encoded for the given pointers.
+// cannot be encoded for the given pointers. sm: where x_perm, GU, h and y_perm
+// live (the other row tensors are the layer's own, at their rows).
 // row_w (the routing weight inside the expert, optional): h = w_row silu(G) U.
 cudaError_t launch_ffn_fc1(const moe_config& c, const void* x_perm, const int32_t* counts,
                            const int32_t* offsets, const void* W13, void* GU, void* h,
-                           int32_t* status, cudaStream_t s, const float* row_w = nullptr);
+                           int32_t* status, cudaStream_t s, const float* row_w = nullptr,
+                           const StashMap& sm = StashMap());
 cudaError_t launch_ffn_fc2(const moe_config& c, const void* h, const int32_t* counts,
                            const int32_t* offsets, const void* W2, void* y_perm,
-                           int32_t* status, cudaStream_t s);
+                           int32_t* status, cudaStream_t s, const StashMap& sm = StashMap());
 // row_w, dw_part (optional): the weight inside the expert -- dh = w_row dh_s,
 // and dw_part[r * dw_tiles(c) + n-tile] = the row's <dh_s, h> over that tile.
 // h_out (optional): h [rows, F] rewritten from GU (fine-grained recompute).
@@ -175,7 +204,7 @@ cudaError_t launch_ffn_fc2_dgrad(const moe_config& c, const void* dO_perm, const
                                  const int32_t* offsets, const void* W2, const void* GU,
                                  void* dGU, int32_t* status, cudaStream_t s,
                                  const float* row_w = nullptr, float* dw_part = nullptr,
-                                 void* h_out = nullptr);
+                                 void* h_out = nullptr, const StashMap& sm = StashMap());
 int dw_tiles(const moe_config& c);
 cudaError_t launch_ffn_fc1_dgrad(const moe_config& c, const void* dGU, const int32_t* counts,
                                  const int32_t* offsets, const void* W13, const int32_t* token_of,
@@ -183,10 +212,10 @@ cudaError_t launch_ffn_fc1_dgrad(const moe_config& c, const void* dGU, const int
                                  int32_t* status, cudaStream_t s);
 cudaError_t launch_ffn_wgrad_fc2(const moe_config& c, const void* dO_perm, const void* h,
                                  const int32_t* counts, const int32_t* offsets, void* dW2,
-                                 int32_t* status, cudaStream_t s);
+                                 int32_t* status, cudaStream_t s, const StashMap& sm = StashMap());
 cudaError_t launch_ffn_wgrad_fc1(const moe_config& c, const void* dGU, const void* x_perm,
                                  const int32_t* counts, const int32_t* offsets, void* dW13,
-                                 int32_t* status, cudaStream_t s);
+                                 int32_t* status, cudaStream_t s, const StashMap& sm = StashMap());
 
 // The FP8 configuration's forward and data-gradient GEMMs on the block-scaled
 // FP8 tensor cores (tcgen05 kind::mxf8f6f4): E4M3 operands with UE8M0 scale
@@ -194,16 +223,16 @@ cudaError_t launch_ffn_wgrad_fc1(const moe_config& c, const void* dGU, const voi
 cudaError_t launch_ffn_fc1_fp8(const moe_config& c, const uint8_t* xq, const uint8_t* xsf,
                                const int32_t* counts, const int32_t* offsets, const uint8_t* W13q,
                                const uint8_t* W13sf, void* GU, void* h, uint8_t* hq, uint8_t* hsf,
-                               int32_t* status, cudaStream_t s);
+                               int32_t* status, cudaStream_t s, const StashMap& sm = StashMap());
 cudaError_t launch_ffn_fc2_fp8(const moe_config& c, const uint8_t* hq, const uint8_t* hsf,
                                const int32_t* counts, const int32_t* offsets, const uint8_t* W2q,
                                const uint8_t* W2sf, void* y_perm, int32_t* status,
-                               cudaStream_t s);
+                               cudaStream_t s, const StashMap& sm = StashMap());
 cudaError_t launch_ffn_fc2_dgrad_fp8(const moe_config& c, const uint8_t* dOq, const uint8_t* dOsf,
                                      const int32_t* counts, const int32_t* offsets,
                                      const uint8_t* W2q, const uint8_t* W2sf_t, const void* GU,
                                      void* dGU, int32_t* status, cudaStream_t s,
-                                     void* h_out = nullptr);
+                                     void* h_out = nullptr, const StashMap& sm = StashMap());
 cudaError_t launch_ffn_fc1_dgrad_fp8(const moe_config& c, const uint8_t* dGq, const uint8_t* dGsf,
                                      const int32_t* counts, const int32_t* offsets,
                                      const uint8_t* W13q, const uint8_t* W13sf_t,

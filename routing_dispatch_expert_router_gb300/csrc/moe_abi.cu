@@ -166,12 +166,18 @@ moe_status check_config(const moe_config* c) {
     return MOE_ERR_UNSUPPORTED;
   if (c->weights_in_expert != 0 && c->weights_in_expert != 1) return MOE_ERR_INVALID_ARG;
   if (c->recompute_h != 0 && c->recompute_h != 1) return MOE_ERR_INVALID_ARG;
+  if (c->stash_pool_pages < 0 || ((int64_t)c->stash_pool_pages + 1) * 128 >= (1LL << 31))
+    return MOE_ERR_INVALID_ARG;
   if (c->weights_in_expert && c->dtype != MOE_DTYPE_BF16) return MOE_ERR_UNSUPPORTED;
   if ((int64_t)c->T * c->k >= (1LL << 31) || rows_max(*c) >= (1LL << 31))
     return MOE_ERR_INVALID_ARG;
   if ((int64_t)c->E * 2 * c->F >= (1LL << 31) || (int64_t)(c->E + c->n_shared) * c->H >= (1LL << 31))
     return MOE_ERR_INVALID_ARG;
   return MOE_OK;
+}
+
+int64_t stash_rows(const moe_config& c, const StashMap& sm) {
+  return sm.pages ? sm.rows : rows_max(c);
 }
 
 static bool al16(const void* p) { return p && ((uintptr_t)p & 15u) == 0; }
@@ -224,6 +230,229 @@ using namespace moe;
     if (!(cond)) return MOE_ERR_INVALID_ARG; \
   } while (0)
 
+// The paged stash of a layer (cfg->stash_pool_pages > 0): its page table and
+// the pool's row count; the layer's own buffers otherwise.
+static moe_status stash_of(const moe_config* cfg, const moe_fwd_state* st, StashMap* sm) {
+  *sm = StashMap();
+  if (cfg->stash_pool_pages == 0) return MOE_OK;
+  MOE_REQUIRE(al4(st->stash_table) && al4(st->stash_top));
+  sm->pages = st->stash_table;
+  sm->rows = ((int64_t)cfg->stash_pool_pages + 1) * 128;
+  return MOE_OK;
+}
+
+// The stage bodies, shared by the per-stage entry points (the layer's own
+// buffers) and by moe_layer_fwd / moe_layer_bwd (which may keep the stashed
+// rows in pool pages).
+static moe_status permute_impl(const moe_config* cfg, const void* x, const int32_t* idx, int32_t* counts,
+                       int32_t* offsets, int32_t* row_of, int32_t* token_of, int32_t* sel_offsets,
+                       int32_t* sel_tokens, void* x_perm, void* scratch, void* stream,
+    const StashAlloc* alloc) {
+  MOE_TRY(check_config(cfg));
+  MOE_REQUIRE(tok16(cfg, x) && tok4(cfg, idx) && al4(counts) && al4(offsets) && tok4(cfg, row_of));
+  MOE_REQUIRE(al4(token_of) && al4(sel_offsets) && tok4(cfg, sel_tokens) && al16(x_perm));
+  MOE_REQUIRE(al16(scratch));
+  Fp8Scratch q;
+  const bool fp8 = is_fp8(*cfg);
+  if (fp8) q = fp8_scratch(*cfg, scratch);
+  cudaStream_t s = (cudaStream_t)stream;
+  // the block recipe writes x_perm's 1x128 E4M3 form in the scatter itself;
+  // MXFP8's 1x32 form is a pass of its own
+  MOE_CUDA(launch_permute(*cfg, x, idx, counts, offsets, row_of, token_of, sel_offsets,
+                          sel_tokens, x_perm, static_cast<uint8_t*>(scratch), s,
+                          fp8 && !q.mx ? &q : nullptr, alloc));
+  if (fp8 && q.mx)
+    MOE_CUDA(launch_quant_rows8(x_perm, q.xq, q.xsf, offsets, counts, cfg->E + cfg->n_shared,
+                                rows_max(*cfg), cfg->H, s, true, alloc ? alloc->table : nullptr));
+  return MOE_OK;
+}
+
+static moe_status ffn_fwd_impl(const moe_config* cfg, const void* x_perm, const int32_t* counts,
+                               const int32_t* offsets, const void* W13, const void* W2, void* GU,
+                               void* h, void* y_perm, void* scratch, void* stream,
+    const StashMap& sm) {
+  MOE_TRY(check_config(cfg));
+  MOE_REQUIRE(al16(x_perm) && al4(counts) && al4(offsets) && al16(W13) && al16(W2));
+  MOE_REQUIRE(al16(GU) && al16(h) && al16(y_perm) && al16(scratch));
+  cudaStream_t s = (cudaStream_t)stream;
+  int32_t* st = status_word(scratch);
+  if (is_fp8(*cfg)) {
+    // the E4M3 weights are the ones moe_quantize_weights left in scratch, the
+    // E4M3 x_perm the one moe_permute wrote there with the bf16 rows; h's
+    // E4M3 form comes out of the FC1 epilogue (block recipe) or its own pass
+    const Fp8Scratch q = fp8_scratch(*cfg, scratch);
+    const int G = cfg->E + cfg->n_shared;
+    const int64_t R = rows_max(*cfg);
+    MOE_CUDA(launch_ffn_fc1_fp8(*cfg, q.xq, q.xsf, counts, offsets, q.W13q, q.W13sf, GU, h, q.hq,
+                                q.hsf, st, s, sm));
+    if (q.mx)
+      MOE_CUDA(launch_quant_rows8(h, q.hq, q.hsf, offsets, counts, G, R, cfg->F, s, true,
+                                  sm.pages));
+    MOE_CUDA(launch_ffn_fc2_fp8(*cfg, q.hq, q.hsf, counts, offsets, q.W2q, q.W2sf, y_perm, st, s,
+                                sm));
+    return MOE_OK;
+  }
+  MOE_CUDA(launch_ffn_fc1(*cfg, x_perm, counts, offsets, W13, GU, h, st, s, nullptr, sm));
+  MOE_CUDA(launch_ffn_fc2(*cfg, h, counts, offsets, W2, y_perm, st, s, sm));
+  return MOE_OK;
+}
+
+static moe_status unpermute_impl(const moe_config* cfg, const void* y_perm, const int32_t* row_of,
+                         const float* w, const int32_t* offsets, void* out, void* stream,
+    const int32_t* pages) {
+  MOE_TRY(check_config(cfg));
+  MOE_REQUIRE(al16(y_perm) && tok4(cfg, row_of) && al4(offsets) && tok16(cfg, out));
+  MOE_REQUIRE(w == nullptr || al4(w));
+  MOE_CUDA(launch_unpermute(*cfg, y_perm, row_of, w, offsets, out, (cudaStream_t)stream, pages));
+  return MOE_OK;
+}
+
+static moe_status unpermute_bwd_impl(const moe_config* cfg, const void* dY, const void* y_perm,
+                             const int32_t* row_of, const float* w, const int32_t* counts,
+                             const int32_t* offsets, void* dO_perm, float* dw, void* scratch,
+                             void* stream,
+    const int32_t* pages) {
+  MOE_TRY(check_config(cfg));
+  MOE_REQUIRE(tok16(cfg, dY) && al16(y_perm) && tok4(cfg, row_of) && tok4(cfg, w) && al4(counts));
+  MOE_REQUIRE(al4(offsets) && al16(dO_perm) && tok4(cfg, dw) && al16(scratch));
+  uint8_t* dOq = nullptr;
+  uint8_t* dOsf = nullptr;
+  Fp8Scratch q;
+  const bool fp8 = is_fp8(*cfg);
+  if (fp8) q = fp8_scratch(*cfg, scratch);
+  if (fp8 && !q.mx) {                 // dO's 1x128 E4M3 form written by the scatter itself
+    dOq = q.dOq;
+    dOsf = q.dOsf;
+  }
+  cudaStream_t s = (cudaStream_t)stream;
+  MOE_CUDA(launch_unpermute_bwd(*cfg, dY, y_perm, row_of, w, counts, offsets, dO_perm, dw, s, dOq,
+                                dOsf, pages));
+  if (fp8 && q.mx)
+    MOE_CUDA(launch_quant_rows8(dO_perm, q.dOq, q.dOsf, offsets, counts, cfg->E + cfg->n_shared,
+                                rows_max(*cfg), cfg->H, s, true));
+  return MOE_OK;
+}
+
+static moe_status ffn_dgrad_impl(const moe_config* cfg, const void* dO_perm, const void* GU,
+                                 void* h, const int32_t* counts, const int32_t* offsets,
+                                 const int32_t* token_of, const float* dlogits, const float* W_r,
+                                 const void* W13, const void* W2, void* dGU, void* dX_perm,
+                                 void* scratch, void* stream,
+    const StashMap& sm) {
+  MOE_TRY(check_config(cfg));
+  MOE_REQUIRE(al16(dO_perm) && al16(GU) && al4(counts) && al4(offsets) && al4(token_of));
+  MOE_REQUIRE(tok4(cfg, dlogits) && al16(W_r) && al16(W13) && al16(W2) && al16(dGU));
+  MOE_REQUIRE(al16(dX_perm) && al16(scratch) && (h == nullptr || al16(h)));
+  cudaStream_t s = (cudaStream_t)stream;
+  int32_t* st = status_word(scratch);
+  if (is_fp8(*cfg)) {
+    const Fp8Scratch q = fp8_scratch(*cfg, scratch);
+    const int G = cfg->E + cfg->n_shared;
+    const int64_t R = rows_max(*cfg);
+    // dO_perm's E4M3 form is the one moe_unpermute_bwd wrote into scratch;
+    // the weights in their data-gradient forms
+    MOE_CUDA(launch_ffn_fc2_dgrad_fp8(*cfg, q.dOq, q.dOsf, counts, offsets, q.W2qd, q.W2sft, GU,
+                                      dGU, st, s, h, sm));
+    // dGU's row form for FC1's data gradient and its column form for the
+    // weight gradient, from one read
+    MOE_CUDA(launch_quant_rows_cols8(dGU, q.dGq, q.dGsf, q.d2Fq, q.d2Fsf, offsets, counts, G, R,
+                                     2 * cfg->F, s, q.mx));
+    MOE_CUDA(launch_ffn_fc1_dgrad_fp8(*cfg, q.dGq, q.dGsf, counts, offsets, q.W13qd, q.W13sft,
+                                      token_of, dlogits, W_r, dX_perm, st, s));
+    return MOE_OK;
+  }
+  MOE_CUDA(launch_ffn_fc2_dgrad(*cfg, dO_perm, counts, offsets, W2, GU, dGU, st, s, nullptr,
+                                nullptr, h, sm));
+  MOE_CUDA(launch_ffn_fc1_dgrad(*cfg, dGU, counts, offsets, W13, token_of, dlogits, W_r, dX_perm,
+                                st, s));
+  return MOE_OK;
+}
+
+static moe_status ffn_wgrad_impl(const moe_config* cfg, const void* dO_perm, const void* x_perm,
+                                 const void* h, const void* dGU, const int32_t* counts,
+                                 const int32_t* offsets, void* dW13, void* dW2, void* scratch,
+                                 void* stream,
+    const StashMap& sm) {
+  MOE_TRY(check_config(cfg));
+  MOE_REQUIRE(al16(dO_perm) && al16(x_perm) && al16(h) && al16(dGU) && al4(counts));
+  MOE_REQUIRE(al4(offsets) && al16(dW13) && al16(dW2) && al16(scratch));
+  cudaStream_t s = (cudaStream_t)stream;
+  int32_t* st = status_word(scratch);
+  if (is_fp8(*cfg)) {
+    // both operands in slices along each expert's tokens (128x1, or 32x1 for
+    // MXFP8; E4M3 codes and scale atoms), multiplied on the block-scaled FP8
+    // tensor cores
+    const Fp8Scratch q = fp8_scratch(*cfg, scratch);
+    const int G = cfg->E + cfg->n_shared;
+    const int64_t R = rows_max(*cfg);
+    const int H = cfg->H, F = cfg->F;
+    MOE_CUDA(launch_quant_cols8(dO_perm, q.cHq, q.cHsf, offsets, counts, G, R, H, s, q.mx));
+    MOE_CUDA(launch_quant_cols8(h, q.bFq, q.bFsf, offsets, counts, G, R, F, s, q.mx, sm.pages));
+    MOE_CUDA(launch_ffn_wgrad_fc2_fp8(*cfg, q.cHq, q.cHsf, q.bFq, q.bFsf, counts, offsets, dW2,
+                                      st, s));
+    // (dGU's column form is the one moe_grouped_ffn_dgrad left in scratch)
+    MOE_CUDA(launch_quant_cols8(x_perm, q.aHq, q.aHsf, offsets, counts, G, R, H, s, q.mx,
+                                sm.pages));
+    MOE_CUDA(launch_ffn_wgrad_fc1_fp8(*cfg, q.d2Fq, q.d2Fsf, q.aHq, q.aHsf, counts, offsets, dW13,
+                                      st, s));
+    return MOE_OK;
+  }
+  MOE_CUDA(launch_ffn_wgrad_fc2(*cfg, dO_perm, h, counts, offsets, dW2, st, s, sm));
+  MOE_CUDA(launch_ffn_wgrad_fc1(*cfg, dGU, x_perm, counts, offsets, dW13, st, s, sm));
+  return MOE_OK;
+}
+
+static moe_status ffn_fwd_reordered_impl(const moe_config* cfg, const void* x_perm,
+                                         const int32_t* counts, const int32_t* offsets,
+                                         const int32_t* token_of, const int32_t* row_of,
+                                         const float* w, const void* W13, const void* W2,
+                                         void* GU, void* h, void* y_perm, void* scratch,
+                                         void* stream,
+    const StashMap& sm) {
+  MOE_TRY(check_config(cfg));
+  if (!cfg->weights_in_expert) return MOE_ERR_INVALID_ARG;
+  MOE_REQUIRE(al16(x_perm) && al4(counts) && al4(offsets) && al4(token_of) && tok4(cfg, row_of));
+  MOE_REQUIRE(tok4(cfg, w) && al16(W13) && al16(W2) && al16(GU) && al16(h) && al16(y_perm));
+  MOE_REQUIRE(al16(scratch));
+  cudaStream_t s = (cudaStream_t)stream;
+  int32_t* st = status_word(scratch);
+  const ReorderScratch rs = reorder_scratch(*cfg, scratch);
+  MOE_CUDA(launch_row_weights(*cfg, token_of, row_of, w, offsets, rs.row_w, s));
+  MOE_CUDA(launch_ffn_fc1(*cfg, x_perm, counts, offsets, W13, GU, h, st, s, rs.row_w, sm));
+  MOE_CUDA(launch_ffn_fc2(*cfg, h, counts, offsets, W2, y_perm, st, s, sm));
+  return MOE_OK;
+}
+
+static moe_status ffn_dgrad_reordered_impl(const moe_config* cfg, const void* dO_perm,
+                                           const void* GU, void* h, const int32_t* counts,
+                                           const int32_t* offsets, const int32_t* token_of,
+                                           const int32_t* row_of, const float* logits,
+                                           const int32_t* idx, const float* w, const float* W_r,
+                                           const void* W13, const void* W2, void* dGU,
+                                           void* dX_perm, float* dw, float* dlogits,
+                                           void* scratch, void* stream,
+    const StashMap& sm) {
+  MOE_TRY(check_config(cfg));
+  if (!cfg->weights_in_expert) return MOE_ERR_INVALID_ARG;
+  MOE_REQUIRE(al16(dO_perm) && al16(GU) && al4(counts) && al4(offsets) && al4(token_of));
+  MOE_REQUIRE(tok4(cfg, row_of) && tok4(cfg, logits) && tok4(cfg, idx) && tok4(cfg, w));
+  MOE_REQUIRE(al16(W_r) && al16(W13) && al16(W2) && al16(dGU) && al16(dX_perm));
+  MOE_REQUIRE(tok4(cfg, dw) && tok4(cfg, dlogits) && al16(scratch));
+  MOE_REQUIRE(h == nullptr || al16(h));
+  cudaStream_t s = (cudaStream_t)stream;
+  int32_t* st = status_word(scratch);
+  const ReorderScratch rs = reorder_scratch(*cfg, scratch);
+  MOE_CUDA(launch_ffn_fc2_dgrad(*cfg, dO_perm, counts, offsets, W2, GU, dGU, st, s, rs.row_w,
+                                rs.dw_part, h, sm));
+  if (cfg->T > 0) {
+    MOE_CUDA(launch_dw_reduce(*cfg, rs.dw_part, row_of, dw, s));
+    MOE_CUDA(launch_route_bwd(*cfg, logits, idx, w, dw, dlogits, s));
+  }
+  MOE_CUDA(launch_ffn_fc1_dgrad(*cfg, dGU, counts, offsets, W13, token_of, dlogits, W_r, dX_perm,
+                                st, s));
+  return MOE_OK;
+}
+
 extern "C" {
 
 moe_status moe_query_sizes(const moe_config* cfg, moe_sizes* out) {
@@ -233,6 +462,7 @@ moe_status moe_query_sizes(const moe_config* cfg, moe_sizes* out) {
   out->groups = cfg->E + cfg->n_shared;
   out->capacity = capacity_rows(*cfg);
   out->scratch_bytes = scratch_bytes(*cfg);
+  out->stash_table_len = rows_max(*cfg) / 128 + 2;
   return MOE_OK;
 }
 
@@ -292,23 +522,8 @@ moe_status moe_route_aux_bwd(const moe_config* cfg, const void* x, const float* 
 moe_status moe_permute(const moe_config* cfg, const void* x, const int32_t* idx, int32_t* counts,
                        int32_t* offsets, int32_t* row_of, int32_t* token_of, int32_t* sel_offsets,
                        int32_t* sel_tokens, void* x_perm, void* scratch, void* stream) {
-  MOE_TRY(check_config(cfg));
-  MOE_REQUIRE(tok16(cfg, x) && tok4(cfg, idx) && al4(counts) && al4(offsets) && tok4(cfg, row_of));
-  MOE_REQUIRE(al4(token_of) && al4(sel_offsets) && tok4(cfg, sel_tokens) && al16(x_perm));
-  MOE_REQUIRE(al16(scratch));
-  Fp8Scratch q;
-  const bool fp8 = is_fp8(*cfg);
-  if (fp8) q = fp8_scratch(*cfg, scratch);
-  cudaStream_t s = (cudaStream_t)stream;
-  // the block recipe writes x_perm's 1x128 E4M3 form in the scatter itself;
-  // MXFP8's 1x32 form is a pass of its own
-  MOE_CUDA(launch_permute(*cfg, x, idx, counts, offsets, row_of, token_of, sel_offsets,
-                          sel_tokens, x_perm, static_cast<uint8_t*>(scratch), s,
-                          fp8 && !q.mx ? &q : nullptr));
-  if (fp8 && q.mx)
-    MOE_CUDA(launch_quant_rows8(x_perm, q.xq, q.xsf, offsets, counts, cfg->E + cfg->n_shared,
-                                rows_max(*cfg), cfg->H, s, true));
-  return MOE_OK;
+  return permute_impl(cfg, x, idx, counts, offsets, row_of, token_of, sel_offsets, sel_tokens,
+                      x_perm, scratch, stream, nullptr);
 }
 
 moe_status moe_quantize_weights(const moe_config* cfg, const void* W13, const void* W2,
@@ -332,61 +547,21 @@ moe_status moe_quantize_weights(const moe_config* cfg, const void* W13, const vo
 moe_status moe_grouped_ffn_fwd(const moe_config* cfg, const void* x_perm, const int32_t* counts,
                                const int32_t* offsets, const void* W13, const void* W2, void* GU,
                                void* h, void* y_perm, void* scratch, void* stream) {
-  MOE_TRY(check_config(cfg));
-  MOE_REQUIRE(al16(x_perm) && al4(counts) && al4(offsets) && al16(W13) && al16(W2));
-  MOE_REQUIRE(al16(GU) && al16(h) && al16(y_perm) && al16(scratch));
-  cudaStream_t s = (cudaStream_t)stream;
-  int32_t* st = status_word(scratch);
-  if (is_fp8(*cfg)) {
-    // the E4M3 weights are the ones moe_quantize_weights left in scratch, the
-    // E4M3 x_perm the one moe_permute wrote there with the bf16 rows; h's
-    // E4M3 form comes out of the FC1 epilogue (block recipe) or its own pass
-    const Fp8Scratch q = fp8_scratch(*cfg, scratch);
-    const int G = cfg->E + cfg->n_shared;
-    const int64_t R = rows_max(*cfg);
-    MOE_CUDA(launch_ffn_fc1_fp8(*cfg, q.xq, q.xsf, counts, offsets, q.W13q, q.W13sf, GU, h, q.hq,
-                                q.hsf, st, s));
-    if (q.mx) MOE_CUDA(launch_quant_rows8(h, q.hq, q.hsf, offsets, counts, G, R, cfg->F, s, true));
-    MOE_CUDA(launch_ffn_fc2_fp8(*cfg, q.hq, q.hsf, counts, offsets, q.W2q, q.W2sf, y_perm, st, s));
-    return MOE_OK;
-  }
-  MOE_CUDA(launch_ffn_fc1(*cfg, x_perm, counts, offsets, W13, GU, h, st, s));
-  MOE_CUDA(launch_ffn_fc2(*cfg, h, counts, offsets, W2, y_perm, st, s));
-  return MOE_OK;
+  return ffn_fwd_impl(cfg, x_perm, counts, offsets, W13, W2, GU, h, y_perm, scratch, stream,
+                      StashMap());
 }
 
 moe_status moe_unpermute(const moe_config* cfg, const void* y_perm, const int32_t* row_of,
                          const float* w, const int32_t* offsets, void* out, void* stream) {
-  MOE_TRY(check_config(cfg));
-  MOE_REQUIRE(al16(y_perm) && tok4(cfg, row_of) && al4(offsets) && tok16(cfg, out));
-  MOE_REQUIRE(w == nullptr || al4(w));
-  MOE_CUDA(launch_unpermute(*cfg, y_perm, row_of, w, offsets, out, (cudaStream_t)stream));
-  return MOE_OK;
+  return unpermute_impl(cfg, y_perm, row_of, w, offsets, out, stream, nullptr);
 }
 
 moe_status moe_unpermute_bwd(const moe_config* cfg, const void* dY, const void* y_perm,
                              const int32_t* row_of, const float* w, const int32_t* counts,
                              const int32_t* offsets, void* dO_perm, float* dw, void* scratch,
                              void* stream) {
-  MOE_TRY(check_config(cfg));
-  MOE_REQUIRE(tok16(cfg, dY) && al16(y_perm) && tok4(cfg, row_of) && tok4(cfg, w) && al4(counts));
-  MOE_REQUIRE(al4(offsets) && al16(dO_perm) && tok4(cfg, dw) && al16(scratch));
-  uint8_t* dOq = nullptr;
-  uint8_t* dOsf = nullptr;
-  Fp8Scratch q;
-  const bool fp8 = is_fp8(*cfg);
-  if (fp8) q = fp8_scratch(*cfg, scratch);
-  if (fp8 && !q.mx) {                 // dO's 1x128 E4M3 form written by the scatter itself
-    dOq = q.dOq;
-    dOsf = q.dOsf;
-  }
-  cudaStream_t s = (cudaStream_t)stream;
-  MOE_CUDA(launch_unpermute_bwd(*cfg, dY, y_perm, row_of, w, counts, offsets, dO_perm, dw, s, dOq,
-                                dOsf));
-  if (fp8 && q.mx)
-    MOE_CUDA(launch_quant_rows8(dO_perm, q.dOq, q.dOsf, offsets, counts, cfg->E + cfg->n_shared,
-                                rows_max(*cfg), cfg->H, s, true));
-  return MOE_OK;
+  return unpermute_bwd_impl(cfg, dY, y_perm, row_of, w, counts, offsets, dO_perm, dw, scratch,
+                            stream, nullptr);
 }
 
 moe_status moe_grouped_ffn_dgrad(const moe_config* cfg, const void* dO_perm, const void* GU,
@@ -394,65 +569,16 @@ moe_status moe_grouped_ffn_dgrad(const moe_config* cfg, const void* dO_perm, con
                                  const int32_t* token_of, const float* dlogits, const float* W_r,
                                  const void* W13, const void* W2, void* dGU, void* dX_perm,
                                  void* scratch, void* stream) {
-  MOE_TRY(check_config(cfg));
-  MOE_REQUIRE(al16(dO_perm) && al16(GU) && al4(counts) && al4(offsets) && al4(token_of));
-  MOE_REQUIRE(tok4(cfg, dlogits) && al16(W_r) && al16(W13) && al16(W2) && al16(dGU));
-  MOE_REQUIRE(al16(dX_perm) && al16(scratch) && (h == nullptr || al16(h)));
-  cudaStream_t s = (cudaStream_t)stream;
-  int32_t* st = status_word(scratch);
-  if (is_fp8(*cfg)) {
-    const Fp8Scratch q = fp8_scratch(*cfg, scratch);
-    const int G = cfg->E + cfg->n_shared;
-    const int64_t R = rows_max(*cfg);
-    // dO_perm's E4M3 form is the one moe_unpermute_bwd wrote into scratch;
-    // the weights in their data-gradient forms
-    MOE_CUDA(launch_ffn_fc2_dgrad_fp8(*cfg, q.dOq, q.dOsf, counts, offsets, q.W2qd, q.W2sft, GU,
-                                      dGU, st, s, h));
-    // dGU's row form for FC1's data gradient and its column form for the
-    // weight gradient, from one read
-    MOE_CUDA(launch_quant_rows_cols8(dGU, q.dGq, q.dGsf, q.d2Fq, q.d2Fsf, offsets, counts, G, R,
-                                     2 * cfg->F, s, q.mx));
-    MOE_CUDA(launch_ffn_fc1_dgrad_fp8(*cfg, q.dGq, q.dGsf, counts, offsets, q.W13qd, q.W13sft,
-                                      token_of, dlogits, W_r, dX_perm, st, s));
-    return MOE_OK;
-  }
-  MOE_CUDA(launch_ffn_fc2_dgrad(*cfg, dO_perm, counts, offsets, W2, GU, dGU, st, s, nullptr,
-                                nullptr, h));
-  MOE_CUDA(launch_ffn_fc1_dgrad(*cfg, dGU, counts, offsets, W13, token_of, dlogits, W_r, dX_perm,
-                                st, s));
-  return MOE_OK;
+  return ffn_dgrad_impl(cfg, dO_perm, GU, h, counts, offsets, token_of, dlogits, W_r, W13, W2, dGU,
+                        dX_perm, scratch, stream, StashMap());
 }
 
 moe_status moe_grouped_ffn_wgrad(const moe_config* cfg, const void* dO_perm, const void* x_perm,
                                  const void* h, const void* dGU, const int32_t* counts,
                                  const int32_t* offsets, void* dW13, void* dW2, void* scratch,
                                  void* stream) {
-  MOE_TRY(check_config(cfg));
-  MOE_REQUIRE(al16(dO_perm) && al16(x_perm) && al16(h) && al16(dGU) && al4(counts));
-  MOE_REQUIRE(al4(offsets) && al16(dW13) && al16(dW2) && al16(scratch));
-  cudaStream_t s = (cudaStream_t)stream;
-  int32_t* st = status_word(scratch);
-  if (is_fp8(*cfg)) {
-    // both operands in slices along each expert's tokens (128x1, or 32x1 for
-    // MXFP8; E4M3 codes and scale atoms), multiplied on the block-scaled FP8
-    // tensor cores
-    const Fp8Scratch q = fp8_scratch(*cfg, scratch);
-    const int G = cfg->E + cfg->n_shared;
-    const int64_t R = rows_max(*cfg);
-    const int H = cfg->H, F = cfg->F;
-    MOE_CUDA(launch_quant_cols8(dO_perm, q.cHq, q.cHsf, offsets, counts, G, R, H, s, q.mx));
-    MOE_CUDA(launch_quant_cols8(h, q.bFq, q.bFsf, offsets, counts, G, R, F, s, q.mx));
-    MOE_CUDA(launch_ffn_wgrad_fc2_fp8(*cfg, q.cHq, q.cHsf, q.bFq, q.bFsf, counts, offsets, dW2,
-                                      st, s));
-    // (dGU's column form is the one moe_grouped_ffn_dgrad left in scratch)
-    MOE_CUDA(launch_quant_cols8(x_perm, q.aHq, q.aHsf, offsets, counts, G, R, H, s, q.mx));
-    MOE_CUDA(launch_ffn_wgrad_fc1_fp8(*cfg, q.d2Fq, q.d2Fsf, q.aHq, q.aHsf, counts, offsets, dW13,
-                                      st, s));
-    return MOE_OK;
-  }
-  MOE_CUDA(launch_ffn_wgrad_fc2(*cfg, dO_perm, h, counts, offsets, dW2, st, s));
-  MOE_CUDA(launch_ffn_wgrad_fc1(*cfg, dGU, x_perm, counts, offsets, dW13, st, s));
-  return MOE_OK;
+  return ffn_wgrad_impl(cfg, dO_perm, x_perm, h, dGU, counts, offsets, dW13, dW2, scratch, stream,
+                        StashMap());
 }
 
 moe_status moe_grouped_ffn_bwd(const moe_config* cfg, const void* dO_perm, const void* x_perm,
@@ -477,18 +603,8 @@ moe_status moe_grouped_ffn_fwd_reordered(const moe_config* cfg, const void* x_pe
                                          const float* w, const void* W13, const void* W2,
                                          void* GU, void* h, void* y_perm, void* scratch,
                                          void* stream) {
-  MOE_TRY(check_config(cfg));
-  if (!cfg->weights_in_expert) return MOE_ERR_INVALID_ARG;
-  MOE_REQUIRE(al16(x_perm) && al4(counts) && al4(offsets) && al4(token_of) && tok4(cfg, row_of));
-  MOE_REQUIRE(tok4(cfg, w) && al16(W13) && al16(W2) && al16(GU) && al16(h) && al16(y_perm));
-  MOE_REQUIRE(al16(scratch));
-  cudaStream_t s = (cudaStream_t)stream;
-  int32_t* st = status_word(scratch);
-  const ReorderScratch rs = reorder_scratch(*cfg, scratch);
-  MOE_CUDA(launch_row_weights(*cfg, token_of, row_of, w, offsets, rs.row_w, s));
-  MOE_CUDA(launch_ffn_fc1(*cfg, x_perm, counts, offsets, W13, GU, h, st, s, rs.row_w));
-  MOE_CUDA(launch_ffn_fc2(*cfg, h, counts, offsets, W2, y_perm, st, s));
-  return MOE_OK;
+  return ffn_fwd_reordered_impl(cfg, x_perm, counts, offsets, token_of, row_of, w, W13, W2, GU, h,
+                                y_perm, scratch, stream, StashMap());
 }
 
 moe_status moe_unpermute_bwd_reordered(const moe_config* cfg, const void* dY,
@@ -509,25 +625,9 @@ moe_status moe_grouped_ffn_dgrad_reordered(const moe_config* cfg, const void* dO
                                            const void* W13, const void* W2, void* dGU,
                                            void* dX_perm, float* dw, float* dlogits,
                                            void* scratch, void* stream) {
-  MOE_TRY(check_config(cfg));
-  if (!cfg->weights_in_expert) return MOE_ERR_INVALID_ARG;
-  MOE_REQUIRE(al16(dO_perm) && al16(GU) && al4(counts) && al4(offsets) && al4(token_of));
-  MOE_REQUIRE(tok4(cfg, row_of) && tok4(cfg, logits) && tok4(cfg, idx) && tok4(cfg, w));
-  MOE_REQUIRE(al16(W_r) && al16(W13) && al16(W2) && al16(dGU) && al16(dX_perm));
-  MOE_REQUIRE(tok4(cfg, dw) && tok4(cfg, dlogits) && al16(scratch));
-  MOE_REQUIRE(h == nullptr || al16(h));
-  cudaStream_t s = (cudaStream_t)stream;
-  int32_t* st = status_word(scratch);
-  const ReorderScratch rs = reorder_scratch(*cfg, scratch);
-  MOE_CUDA(launch_ffn_fc2_dgrad(*cfg, dO_perm, counts, offsets, W2, GU, dGU, st, s, rs.row_w,
-                                rs.dw_part, h));
-  if (cfg->T > 0) {
-    MOE_CUDA(launch_dw_reduce(*cfg, rs.dw_part, row_of, dw, s));
-    MOE_CUDA(launch_route_bwd(*cfg, logits, idx, w, dw, dlogits, s));
-  }
-  MOE_CUDA(launch_ffn_fc1_dgrad(*cfg, dGU, counts, offsets, W13, token_of, dlogits, W_r, dX_perm,
-                                st, s));
-  return MOE_OK;
+  return ffn_dgrad_reordered_impl(cfg, dO_perm, GU, h, counts, offsets, token_of, row_of, logits,
+                                  idx, w, W_r, W13, W2, dGU, dX_perm, dw, dlogits, scratch, stream,
+                                  StashMap());
 }
 
 moe_status moe_route_bwd(const moe_config* cfg, const float* logits, const int32_t* idx,
@@ -565,19 +665,24 @@ moe_status moe_layer_fwd(const moe_config* cfg, const moe_params* P, const void*
                          const moe_fwd_state* st, void* scratch, void* stream) {
   MOE_TRY(check_config(cfg));
   MOE_REQUIRE(P && st);
+  StashMap sm;
+  MOE_TRY(stash_of(cfg, st, &sm));
+  const StashAlloc alloc{st->stash_table, st->stash_top, cfg->stash_pool_pages};
   MOE_TRY(moe_quantize_weights(cfg, P->W13, P->W2, scratch, stream));
   MOE_TRY(moe_route(cfg, x, P->W_r, P->bias, st->logits, st->idx, st->w, scratch, stream));
-  MOE_TRY(moe_permute(cfg, x, st->idx, st->counts, st->offsets, st->row_of, st->token_of,
-                      st->sel_offsets, st->sel_tokens, st->x_perm, scratch, stream));
+  MOE_TRY(permute_impl(cfg, x, st->idx, st->counts, st->offsets, st->row_of, st->token_of,
+                       st->sel_offsets, st->sel_tokens, st->x_perm, scratch, stream,
+                       sm.pages ? &alloc : nullptr));
   if (cfg->weights_in_expert) {
-    MOE_TRY(moe_grouped_ffn_fwd_reordered(cfg, st->x_perm, st->counts, st->offsets, st->token_of,
-                                          st->row_of, st->w, P->W13, P->W2, st->GU, st->h,
-                                          st->y_perm, scratch, stream));
-    return moe_unpermute(cfg, st->y_perm, st->row_of, nullptr, st->offsets, out, stream);
+    MOE_TRY(ffn_fwd_reordered_impl(cfg, st->x_perm, st->counts, st->offsets, st->token_of,
+                                   st->row_of, st->w, P->W13, P->W2, st->GU, st->h, st->y_perm,
+                                   scratch, stream, sm));
+    return unpermute_impl(cfg, st->y_perm, st->row_of, nullptr, st->offsets, out, stream,
+                          sm.pages);
   }
-  MOE_TRY(moe_grouped_ffn_fwd(cfg, st->x_perm, st->counts, st->offsets, P->W13, P->W2, st->GU,
-                              st->h, st->y_perm, scratch, stream));
-  MOE_TRY(moe_unpermute(cfg, st->y_perm, st->row_of, st->w, st->offsets, out, stream));
+  MOE_TRY(ffn_fwd_impl(cfg, st->x_perm, st->counts, st->offsets, P->W13, P->W2, st->GU, st->h,
+                       st->y_perm, scratch, stream, sm));
+  MOE_TRY(unpermute_impl(cfg, st->y_perm, st->row_of, st->w, st->offsets, out, stream, sm.pages));
   return MOE_OK;
 }
 
@@ -587,32 +692,40 @@ moe_status moe_layer_bwd(const moe_config* cfg, const moe_params* P, const void*
                          void* stream) {
   MOE_TRY(check_config(cfg));
   MOE_REQUIRE(P && st && bs);
+  StashMap sm;
+  MOE_TRY(stash_of(cfg, st, &sm));
+  // fine-grained recompute: the data gradient rewrites h from GU before the
+  // weight gradient reads it
+  void* h_out = cfg->recompute_h ? st->h : nullptr;
   if (cfg->weights_in_expert) {
     MOE_TRY(moe_unpermute_bwd_reordered(cfg, dY, st->row_of, st->counts, st->offsets,
                                         bs->dO_perm, stream));
-    MOE_TRY(moe_grouped_ffn_dgrad_reordered(cfg, bs->dO_perm, st->GU,
-                                            cfg->recompute_h ? st->h : nullptr, st->counts,
-                                            st->offsets,
-                                            st->token_of, st->row_of, st->logits, st->idx, st->w,
-                                            P->W_r, P->W13, P->W2, bs->dGU, bs->dX_perm, bs->dw,
-                                            bs->dlogits, scratch, stream));
-    MOE_TRY(moe_grouped_ffn_wgrad(cfg, bs->dO_perm, st->x_perm, st->h, bs->dGU, st->counts,
-                                  st->offsets, dW13, dW2, scratch, stream));
-    MOE_TRY(moe_permute_bwd(cfg, bs->dX_perm, st->row_of, st->offsets, st->idx, bs->dlogits,
-                            P->W_r, dx, stream));
-    return moe_router_wgrad(cfg, x, st->sel_offsets, st->sel_tokens, bs->dlogits, dW_r, scratch,
-                            stream);
+    MOE_TRY(ffn_dgrad_reordered_impl(cfg, bs->dO_perm, st->GU, h_out, st->counts, st->offsets,
+                                     st->token_of, st->row_of, st->logits, st->idx, st->w,
+                                     P->W_r, P->W13, P->W2, bs->dGU, bs->dX_perm, bs->dw,
+                                     bs->dlogits, scratch, stream, sm));
+  } else {
+    MOE_TRY(unpermute_bwd_impl(cfg, dY, st->y_perm, st->row_of, st->w, st->counts, st->offsets,
+                               bs->dO_perm, bs->dw, scratch, stream, sm.pages));
+    MOE_TRY(moe_route_bwd(cfg, st->logits, st->idx, st->w, bs->dw, bs->dlogits, stream));
+    MOE_TRY(ffn_dgrad_impl(cfg, bs->dO_perm, st->GU, h_out, st->counts, st->offsets,
+                           st->token_of, bs->dlogits, P->W_r, P->W13, P->W2, bs->dGU,
+                           bs->dX_perm, scratch, stream, sm));
   }
-  MOE_TRY(moe_unpermute_bwd(cfg, dY, st->y_perm, st->row_of, st->w, st->counts, st->offsets,
-                            bs->dO_perm, bs->dw, scratch, stream));
-  MOE_TRY(moe_route_bwd(cfg, st->logits, st->idx, st->w, bs->dw, bs->dlogits, stream));
-  MOE_TRY(moe_grouped_ffn_bwd(cfg, bs->dO_perm, st->x_perm, st->GU, st->h, st->counts,
-                              st->offsets, st->token_of, bs->dlogits, P->W_r, P->W13, P->W2,
-                              bs->dGU, bs->dX_perm, dW13, dW2, scratch, stream));
+  MOE_TRY(ffn_wgrad_impl(cfg, bs->dO_perm, st->x_perm, st->h, bs->dGU, st->counts, st->offsets,
+                         dW13, dW2, scratch, stream, sm));
   MOE_TRY(moe_permute_bwd(cfg, bs->dX_perm, st->row_of, st->offsets, st->idx, bs->dlogits,
                           P->W_r, dx, stream));
   MOE_TRY(moe_router_wgrad(cfg, x, st->sel_offsets, st->sel_tokens, bs->dlogits, dW_r, scratch,
                            stream));
+  if (sm.pages) MOE_TRY(moe_stash_release(cfg, st, stream));
+  return MOE_OK;
+}
+
+moe_status moe_stash_release(const moe_config* cfg, const moe_fwd_state* st, void* stream) {
+  MOE_TRY(check_config(cfg));
+  MOE_REQUIRE(st && cfg->stash_pool_pages > 0 && al4(st->stash_table) && al4(st->stash_top));
+  MOE_CUDA(launch_stash_release(*cfg, st->stash_table, st->stash_top, (cudaStream_t)stream));
   return MOE_OK;
 }
 
@@ -649,6 +762,7 @@ const char* moe_status_string(moe_status s) {
     case MOE_ERR_CUDA: return "a CUDA runtime call failed";
     case MOE_ERR_TIMEOUT: return "a device-side bounded wait ran out";
     case MOE_ERR_DEVICE_CHECK: return "a kernel found an out-of-range index";
+    case MOE_ERR_STASH_FULL: return "a layer's rows did not fit its stash pool";
   }
   return "unknown status";
 }

@@ -8,12 +8,13 @@
 // are computed without atomics whose order matters, so they are
 // deterministic and bit-identical from run to run.
 //
-// Three launches:
+// Three launches (four with a paged stash):
 //   hist    one block per chunk of 256 tokens: per-expert counts of the chunk;
 //   rank    one block per chunk: global counts, segment offsets, and the rank
 //           of every assignment = (assignments of its expert in earlier
 //           chunks) + (earlier tokens of this chunk that chose the same
 //           expert, read from a per-expert bitmap of the chunk's tokens);
+//   alloc   (paged stash) one block: the layer's stash pages and page table;
 //   scatter one warp per token: reads the row once, writes it to each of its
 //           rows with 16-byte stores; padding rows are zero-filled.
 #include "common.cuh"
@@ -146,6 +147,76 @@ permute_rank_kernel(const int32_t* __restrict__ idx, const int32_t* __restrict__
     for (int r = seg[g] + kept[g] + tid; r < seg[g + 1]; r += nt) token_of[r] = -1;
 }
 
+// Paged stashing (es summary §2.3.C: the dynamic buffers are managed inside
+// the CUDA graph instead of being reserved for the worst case). The rows a
+// layer keeps for its backward live in a pool of 128-row pages shared by the
+// layers of a step. Once the segment offsets are on the device, one block
+// takes as many pages as the layer has live 128-row blocks -- the
+// ceil(counts[g] / 128) blocks of group g from offsets[g] / 128 on, the ones
+// the grouped GEMMs' row tiles cover -- from the pool's counter (a
+// compare-and-swap, so layers on other streams can allocate too), numbers
+// them in block order, and maps every other block, including the one past the
+// last row (the odd half of a CTA-pair tile reads there), to the spill page P.
+// A layer that does not fit takes no page: all of its blocks map to the spill
+// page, MOE_ERR_STASH_FULL is recorded, and every access stays in the pool.
+// Entry nblk + 1 keeps the first page taken (the counter's value before),
+// which the release writes back.
+__global__ void __launch_bounds__(256)
+stash_alloc_kernel(const int32_t* __restrict__ counts, const int32_t* __restrict__ offsets,
+                   int G, int nblk, int P, int32_t* __restrict__ top,
+                   int32_t* __restrict__ table, int32_t* status) {
+  __shared__ int pre[kMaxGroups + 1];
+  __shared__ int blk0[kMaxGroups + 1];
+  __shared__ int tmp[33];
+  __shared__ int s_first, s_ok;
+  const int tid = threadIdx.x, nt = blockDim.x;
+  for (int g = tid; g < G; g += nt) {
+    pre[g] = (counts[g] + 127) >> 7;
+    blk0[g] = offsets[g] >> 7;
+  }
+  if (tid == 0) blk0[G] = offsets[G] >> 7;
+  __syncthreads();
+  const int n = block_exclusive_scan(pre, G, tmp);
+  if (tid == 0) {
+    pre[G] = n;
+    int old = atomicAdd(top, 0);
+    int first = -1;
+    while (old >= 0 && old <= P - n) {
+      const int seen = atomicCAS(top, old, old + n);
+      if (seen == old) {
+        first = old;
+        break;
+      }
+      old = seen;
+    }
+    s_ok = first >= 0;
+    s_first = first >= 0 ? first : old;
+    if (first < 0) record_status(status, MOE_ERR_STASH_FULL);
+    table[nblk + 1] = s_first;
+  }
+  __syncthreads();
+  for (int b = tid; b <= nblk; b += nt) {
+    int page = P;
+    if (s_ok) {
+      // the group whose segment holds block b: the last g with blk0[g] <= b
+      int lo = 0, hi = G - 1;
+      while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (blk0[mid] <= b) lo = mid;
+        else hi = mid - 1;
+      }
+      const int i = b - blk0[lo];
+      if (G > 0 && i >= 0 && i < pre[lo + 1] - pre[lo]) page = s_first + pre[lo] + i;
+    }
+    table[b] = page;
+  }
+}
+
+__global__ void stash_release_kernel(const int32_t* __restrict__ table, int nblk,
+                                     int32_t* __restrict__ top) {
+  if (threadIdx.x == 0) *top = table[nblk + 1];
+}
+
 // Finds the group whose padding range holds padding row number p.
 __device__ __forceinline__ int find_group(const int* prefix, int G, int p) {
   int lo = 0, hi = G - 1;
@@ -170,7 +241,7 @@ permute_scatter_kernel(const __nv_bfloat16* __restrict__ x, const int32_t* __res
                        const int32_t* __restrict__ counts, const int32_t* __restrict__ offsets,
                        const int32_t* __restrict__ pad_prefix, __nv_bfloat16* __restrict__ x_perm,
                        int T, int H, int k, int E, int S, uint8_t* __restrict__ xq,
-                       uint8_t* __restrict__ xsf) {
+                       uint8_t* __restrict__ xsf, const int32_t* __restrict__ pages) {
   __shared__ int s_pp[kMaxGroups + 1];
   __shared__ int s_off[kMaxGroups + 1];
   __shared__ int s_cnt[kMaxGroups];
@@ -222,7 +293,7 @@ permute_scatter_kernel(const __nv_bfloat16* __restrict__ x, const int32_t* __res
 #pragma unroll
         for (int j = 0; j < kMaxK + 4; ++j) {
           if (j >= nr || rows[j] < 0) continue;
-          __nv_bfloat16* dst = x_perm + (size_t)rows[j] * H;
+          __nv_bfloat16* dst = x_perm + (size_t)stash_row(pages, rows[j]) * H;
 #pragma unroll
           for (int u = 0; u < 4; ++u)
             if (c0 + 32 * u < nvec) stg_v4(dst + (size_t)(c0 + 32 * u) * 8, q[u]);
@@ -243,7 +314,7 @@ permute_scatter_kernel(const __nv_bfloat16* __restrict__ x, const int32_t* __res
       const int p = v - T;
       const int g = find_group(s_pp, G, p);
       const int r = s_off[g] + s_cnt[g] + (p - s_pp[g]);
-      __nv_bfloat16* dst = x_perm + (size_t)r * H;
+      __nv_bfloat16* dst = x_perm + (size_t)stash_row(pages, r) * H;
       const uint4 z = make_uint4(0u, 0u, 0u, 0u);
       for (int c0 = lane; c0 < nvec; c0 += 32) {
         stg_v4(dst + (size_t)c0 * 8, z);
@@ -260,7 +331,8 @@ permute_scatter_kernel(const __nv_bfloat16* __restrict__ x, const int32_t* __res
 cudaError_t launch_permute(const moe_config& c, const void* x, const int32_t* idx,
                            int32_t* counts, int32_t* offsets, int32_t* row_of, int32_t* token_of,
                            int32_t* sel_offsets, int32_t* sel_tokens, void* x_perm,
-                           uint8_t* scratch, cudaStream_t s, const Fp8Scratch* fp8) {
+                           uint8_t* scratch, cudaStream_t s, const Fp8Scratch* fp8,
+                           const StashAlloc* alloc) {
   int32_t* status = reinterpret_cast<int32_t*>(scratch + kScratchStatus);
   int32_t* pad_prefix = reinterpret_cast<int32_t*>(scratch + kScratchPadPrefix);
   int32_t* hist = reinterpret_cast<int32_t*>(scratch + kScratchHist);
@@ -276,6 +348,15 @@ cudaError_t launch_permute(const moe_config& c, const void* x, const int32_t* id
                                          token_of, sel_offsets, sel_tokens, pad_prefix);
   err = cudaGetLastError();
   if (err != cudaSuccess) return err;
+  const int32_t* pages = nullptr;
+  if (alloc) {
+    stash_alloc_kernel<<<1, 256, 0, s>>>(counts, offsets, c.E + c.n_shared,
+                                         (int)(rows_max(c) / 128), alloc->pool_pages, alloc->top,
+                                         alloc->table, status);
+    err = cudaGetLastError();
+    if (err != cudaSuccess) return err;
+    pages = alloc->table;
+  }
   uint8_t* xq = nullptr;
   uint8_t* xsf = nullptr;
   if (c.dtype == MOE_DTYPE_FP8_E4M3_BLOCK && fp8) {
@@ -284,7 +365,13 @@ cudaError_t launch_permute(const moe_config& c, const void* x, const int32_t* id
   }
   permute_scatter_kernel<<<num_sms() * 8, 256, 0, s>>>(
       static_cast<const __nv_bfloat16*>(x), row_of, counts, offsets, pad_prefix,
-      static_cast<__nv_bfloat16*>(x_perm), c.T, c.H, c.k, c.E, c.n_shared, xq, xsf);
+      static_cast<__nv_bfloat16*>(x_perm), c.T, c.H, c.k, c.E, c.n_shared, xq, xsf, pages);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_stash_release(const moe_config& c, const int32_t* table, int32_t* top,
+                                 cudaStream_t s) {
+  stash_release_kernel<<<1, 32, 0, s>>>(table, (int)(rows_max(c) / 128), top);
   return cudaGetLastError();
 }
 

@@ -59,7 +59,8 @@ __global__ void __launch_bounds__(256)
 quant_cols8_kernel(const __nv_bfloat16* __restrict__ X, uint8_t* __restrict__ Xq,
                    uint8_t* __restrict__ sf, const int32_t* __restrict__ offsets,
                    const int32_t* __restrict__ counts, int G, int cols, long long kg,
-                   uint8_t* __restrict__ Xr, uint8_t* __restrict__ sfr, long long kgr) {
+                   uint8_t* __restrict__ Xr, uint8_t* __restrict__ sfr, long long kgr,
+                   const int32_t* __restrict__ pages) {
   static_assert(BLK == 128 || BLK == 32, "block length");
   extern __shared__ uint4 qc_smem[];
   uint4 (*tile)[16] = reinterpret_cast<uint4 (*)[16]>(qc_smem);   // 128 rows x 128 bf16
@@ -73,7 +74,8 @@ quant_cols8_kernel(const __nv_bfloat16* __restrict__ X, uint8_t* __restrict__ Xq
     const int cs = (int)(w - rb * slabs);
     const int c0 = cs * 128;
     if (!live_block(offsets, counts, G, rb)) continue;
-    const __nv_bfloat16* src = X + (size_t)rb * 128 * cols + c0;
+    // (a paged stash tensor keeps the block in one page)
+    const __nv_bfloat16* src = X + (size_t)stash_row(pages, (int)rb * 128) * cols + c0;
     {
       uint4 in[8];
 #pragma unroll
@@ -223,7 +225,8 @@ template <int BLK>
 __global__ void __launch_bounds__(256)
 quant_rows8_kernel(const __nv_bfloat16* __restrict__ X, uint8_t* __restrict__ Xq,
                    uint8_t* __restrict__ sf, const int32_t* __restrict__ offsets,
-                   const int32_t* __restrict__ counts, int G, int cols, long long kg) {
+                   const int32_t* __restrict__ counts, int G, int cols, long long kg,
+                   const int32_t* __restrict__ pages) {
   static_assert(BLK == 128 || BLK == 32, "block length");
   constexpr int LANES = BLK / 8;                          // lanes per scale piece
   const long long items = offsets[G] / 128 * 8;
@@ -235,7 +238,7 @@ quant_rows8_kernel(const __nv_bfloat16* __restrict__ X, uint8_t* __restrict__ Xq
     if (!live_block(offsets, counts, G, rb)) continue;
     const int r = (int)(it & 7) * 16 + hw;                // row inside the 128-row block
     const size_t row = (size_t)rb * 128 + r;
-    const __nv_bfloat16* src = X + row * cols + l16 * 8;
+    const __nv_bfloat16* src = X + (size_t)stash_row(pages, (int)row) * cols + l16 * 8;
     uint8_t* dst = Xq + row * cols + l16 * 8;
     for (int kb = 0; kb < KB; kb += 2) {
       const bool two = kb + 1 < KB;
@@ -362,28 +365,30 @@ cudaError_t launch_quant_wmx(const void* W, uint8_t* Wf, uint8_t* Wd, uint8_t* s
 
 cudaError_t launch_quant_rows8(const void* X, uint8_t* Xq, uint8_t* sf, const int32_t* offsets,
                                const int32_t* counts, int G, int64_t rows_max, int cols,
-                               cudaStream_t s, bool mx) {
+                               cudaStream_t s, bool mx, const int32_t* pages) {
   const int grid = grid_cap(rows_max / 128 * 8, 1);
   const long long kg = f8::sf_stride(cols, mx);
   const __nv_bfloat16* x = static_cast<const __nv_bfloat16*>(X);
-  if (mx) quant_rows8_kernel<32><<<grid, 256, 0, s>>>(x, Xq, sf, offsets, counts, G, cols, kg);
-  else quant_rows8_kernel<128><<<grid, 256, 0, s>>>(x, Xq, sf, offsets, counts, G, cols, kg);
+  if (mx)
+    quant_rows8_kernel<32><<<grid, 256, 0, s>>>(x, Xq, sf, offsets, counts, G, cols, kg, pages);
+  else
+    quant_rows8_kernel<128><<<grid, 256, 0, s>>>(x, Xq, sf, offsets, counts, G, cols, kg, pages);
   return cudaGetLastError();
 }
 
 cudaError_t launch_quant_cols8(const void* X, uint8_t* Xq, uint8_t* sf, const int32_t* offsets,
                                const int32_t* counts, int G, int64_t rows_max, int cols,
-                               cudaStream_t s, bool mx) {
+                               cudaStream_t s, bool mx, const int32_t* pages) {
   constexpr int smem = 128 * 16 * 16 + 8 * 128 * 4;     // tile + piece maxima + 1/scales
   const int grid = grid_cap(rows_max / 128 * (cols / 128), 1);
   const long long kg = f8::sf_stride(rows_max, mx);
   const __nv_bfloat16* x = static_cast<const __nv_bfloat16*>(X);
   if (mx)
     quant_cols8_kernel<32, false><<<grid, 256, smem, s>>>(x, Xq, sf, offsets, counts, G, cols, kg,
-                                                           nullptr, nullptr, 0);
+                                                           nullptr, nullptr, 0, pages);
   else
     quant_cols8_kernel<128, false><<<grid, 256, smem, s>>>(x, Xq, sf, offsets, counts, G, cols,
-                                                            kg, nullptr, nullptr, 0);
+                                                            kg, nullptr, nullptr, 0, pages);
   return cudaGetLastError();
 }
 
@@ -396,10 +401,10 @@ cudaError_t launch_quant_rows_cols8(const void* X, uint8_t* Xr, uint8_t* sfr, ui
   const __nv_bfloat16* x = static_cast<const __nv_bfloat16*>(X);
   if (mx)
     quant_cols8_kernel<32, true><<<grid, 256, smem, s>>>(x, Xc, sfc, offsets, counts, G, cols,
-                                                          kgc, Xr, sfr, kgr);
+                                                          kgc, Xr, sfr, kgr, nullptr);
   else
     quant_cols8_kernel<128, true><<<grid, 256, smem, s>>>(x, Xc, sfc, offsets, counts, G, cols,
-                                                           kgc, Xr, sfr, kgr);
+                                                           kgc, Xr, sfr, kgr, nullptr);
   return cudaGetLastError();
 }
 
