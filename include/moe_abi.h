@@ -18,7 +18,10 @@
  *  - The caller owns every buffer; the library never allocates or frees
  *    device memory. Buffers are sized for the worst case with
  *    moe_query_sizes() (the Hybrid-EP article's "worst-case pre-reservation",
- *    hyper.ai, on dynamic token counts).
+ *    hyper.ai, on dynamic token counts), except, with a paged stash
+ *    (moe_config.stash_pool_pages), the four row tensors a layer keeps for
+ *    its backward: those come from a pool of pages shared by several layers,
+ *    which the layers take and give back on the device.
  *  - All calls are asynchronous on `stream` (a cudaStream_t, NULL = legacy
  *    default stream) and never synchronise the host or read device memory
  *    from the host, except moe_last_device_status(). Token counts stay on the
