@@ -358,7 +358,11 @@ grouped_gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmA,
             break;
           }
           const uint32_t fb = bar_full + 8 * stage;
-          ptx::mbar_arrive_expect_tx(fb, kF8Stage + kF8SfStage);
+          // the scale atoms travel only with the stages whose atoms the MMA
+          // thread copies into tensor memory (every stage for MX; in the block
+          // recipe a tile's first and every fourth K block of the operand)
+          const bool with_sf = MX || kb == 0 || (((kr0 / kF8BK) + kb) & 3) == 0;
+          ptx::mbar_arrive_expect_tx(fb, kF8Stage + (with_sf ? kF8SfStage : 0));
           const uint32_t sA = base + stage * kF8Stage;
           const uint32_t sB = sA + kF8ABytes;
           const int k0 = kr0 + kb * kF8BK;
@@ -376,9 +380,11 @@ grouped_gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmA,
           // the atom of this K block: one per K block (MX) or per four
           const int64_t a4 = (int64_t)(MX ? k0 / kF8BK : k0 / kF8BK / f8::kAtomKBlocks) *
                              f8::kAtomBytes;
-          ptx::bulk_load(sfs, sfa + a4, f8::kAtomBytes, fb);
-          ptx::bulk_load(sfs + f8::kAtomBytes, sfb0 + a4, f8::kAtomBytes, fb);
-          ptx::bulk_load(sfs + 2 * f8::kAtomBytes, sfb1 + a4, f8::kAtomBytes, fb);
+          if (with_sf) {
+            ptx::bulk_load(sfs, sfa + a4, f8::kAtomBytes, fb);
+            ptx::bulk_load(sfs + f8::kAtomBytes, sfb0 + a4, f8::kAtomBytes, fb);
+            ptx::bulk_load(sfs + 2 * f8::kAtomBytes, sfb1 + a4, f8::kAtomBytes, fb);
+          }
           issued_mask |= 1u << stage;
           issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
           if (++stage == kStages) {
