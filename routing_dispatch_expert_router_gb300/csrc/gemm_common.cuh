@@ -331,14 +331,16 @@ static inline bool make_out_map_w64(CUtensorMap* m, const void* ptr, uint64_t in
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// 2D view of 1-byte (E4M3) elements [outer rows, inner columns] with a 128 x 128
-// box and the 128-byte swizzle (one box row = one 128-byte swizzle row).
-static inline bool make_map_u8(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t outer) {
+// 2D view of 1-byte (E4M3) elements [outer rows, inner columns] with a 128 x
+// box_outer box (128 or 256 rows) and the 128-byte swizzle (one box row = one
+// 128-byte swizzle row).
+static inline bool make_map_u8(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t outer,
+                               uint32_t box_outer = 128) {
   PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
   if (!fn) return false;
   cuuint64_t dims[2] = {inner, outer};
   cuuint64_t strides[1] = {inner};
-  cuuint32_t box[2] = {128, 128};
+  cuuint32_t box[2] = {128, box_outer};
   cuuint32_t es[2] = {1, 1};
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(ptr), dims, strides, box, es,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,

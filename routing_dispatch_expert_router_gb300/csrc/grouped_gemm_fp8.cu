@@ -369,7 +369,10 @@ grouped_gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmA,
           const int brow = C::KG ? k0 : t.g * p.b_rows + k0;
           if (C::KG) ptx::tma_load_2d(sA, &tmA, fb, row0, k0);
           else ptx::tma_load_2d(sA, &tmA, fb, k0, row0);
-          if (B_MN == 0) {
+          if (B_MN == 0 && EPI != kEpiSwigluFwd) {
+            // rows b0 .. b0 + 255 in one 256-row box (FC2's map)
+            ptx::tma_load_2d(sB, &tmB, fb, k0, t.g * p.b_rows + b0);
+          } else if (B_MN == 0) {
             ptx::tma_load_2d(sB, &tmB, fb, k0, t.g * p.b_rows + b0);
             ptx::tma_load_2d(sB + 16384, &tmB, fb, k0, t.g * p.b_rows + b1);
           } else {
@@ -627,7 +630,8 @@ cudaError_t launch_ffn_fc2_fp8(const moe_config& c, const uint8_t* hq, const uin
   const int64_t R = rows_max(c);
   const int G = c.E + c.n_shared;
   CUtensorMap a, b, oc;
-  if (!make_map_u8(&a, hq, c.F, R) || !make_map_u8(&b, W2q, c.F, (uint64_t)G * c.H) ||
+  // B: W2's rows of one 256-wide n-tile in a single box
+  if (!make_map_u8(&a, hq, c.F, R) || !make_map_u8(&b, W2q, c.F, (uint64_t)G * c.H, 256) ||
       !make_out_map(&oc, y_perm, c.H, stash_rows(c, sm)))
     return cudaErrorInvalidValue;
   Params p = base_params(c, counts, offsets, status);
