@@ -375,12 +375,12 @@ def run_ours(args, rank, world, local):
     # the two weight quantisers, dGU's row-and-column quantiser in the data
     # gradients and three column quantisers in the weight gradients (x_perm's, h's and dO's
     # row forms come out of the scatter, the FC1 epilogue and the combine
-    # backward; MXFP8 quantises those three by passes of their own)
+    # backward, in either recipe)
     tc_router = shape.E >= 128 and shape.E % 128 == 0
     launches_per_step = ((3 if tc_router else 2) + 3 + 2 + 1 + 1 + 1 + 4 + 1
                          + (3 if tc_router else 1))
     if fp8:
-        launches_per_step += 2 + 1 + 3 + (3 if mx else 0)
+        launches_per_step += 2 + 1 + 3
     if reord:
         launches_per_step += 2          # row weights, dw reduction
     for _ in range(max(args.warmup, 3)):
@@ -508,8 +508,7 @@ def run_ours(args, rank, world, local):
         peak_src = (f"{src}: 2 x bf16_tflops (the nominal FP8:bf16 dense rate ratio; no FP8 "
                     "figure is measured)")
         gemm_note = ("time of the grouped_ffn_fwd and grouped_ffn_dgrad stages, which also hold "
-                     "the activation quantisers (h and dGU; MXFP8 also x_perm's and dO's "
-                     "passes run in the dispatch and combine-backward stages)")
+                     "the activation quantisers (h's in the FC1 epilogue, dGU's pass)")
     else:
         gemm_ms = sm["grouped_ffn_fwd"] + sm["grouped_ffn_dgrad"] + sm["grouped_ffn_wgrad"]
         gemm_fl = 3 * fl

@@ -163,10 +163,11 @@ __device__ __forceinline__ int find_pad_group(const int* prefix, int G, int p) {
 // deterministic. No block-wide synchronisation on the token path.
 // COPY (the layer with the routing weight inside the expert): dO[row_tj] =
 // dY[t] unweighted, y is not read and dw is not written (it comes from the FC2
-// data gradient there). With dOq (the FP8 configuration) every row written is
+// data gradient there). With dOq (the FP8 configurations) every row written is
 // also written in its 1-byte form -- E4M3 codes of the bf16 values' 1 x 128
-// slices with their UE8M0 scales in dOsf's atoms -- for the FC2 data gradient.
-template <int MAXR, int U, bool COPY = false>
+// slices (MXFP8: 1 x 32) with their UE8M0 scales in dOsf's atoms -- for the
+// FC2 data gradient.
+template <int MAXR, int U, bool COPY = false, bool MX = false>
 __global__ void __launch_bounds__(256, (MAXR <= 2) ? 3 : 2)
 unpermute_bwd_kernel(const __nv_bfloat16* __restrict__ dY, const __nv_bfloat16* __restrict__ y,
                      const int32_t* __restrict__ row_of, const float* __restrict__ w,
@@ -193,8 +194,9 @@ unpermute_bwd_kernel(const __nv_bfloat16* __restrict__ dY, const __nv_bfloat16* 
   const int lane = threadIdx.x & 31;
   const int nvec = H >> 3, nr = k + S;
   const int warps = gridDim.x * (blockDim.x >> 5);
-  const int64_t kg = f8::atoms_k(H);
+  const int64_t kg = f8::sf_stride(H, MX);
   const unsigned half = (lane & 16) ? 0xffff0000u : 0x0000ffffu;
+  constexpr int piece_lanes = MX ? 4 : 16;         // lanes per scale piece
   for (int v = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); v < T + P; v += warps) {
     if (v >= T) {
       const int p = v - T;
@@ -205,7 +207,7 @@ unpermute_bwd_kernel(const __nv_bfloat16* __restrict__ dY, const __nv_bfloat16* 
         stg_v4(dO + (size_t)r * H + (size_t)c * 8, z);
         if (dOq) {
           *reinterpret_cast<uint2*>(dOq + (size_t)r * H + (size_t)c * 8) = make_uint2(0u, 0u);
-          if ((c & 15) == 0) dOsf[f8::atom_offset(r >> 7, c >> 4, kg) + f8::atom_byte(r, c >> 4)] = 127u;
+          if ((c & (piece_lanes - 1)) == 0) dOsf[f8::row_sf_index(r, c, kg, MX)] = 127u;
         }
       }
       continue;
@@ -265,18 +267,19 @@ unpermute_bwd_kernel(const __nv_bfloat16* __restrict__ dY, const __nv_bfloat16* 
           }
           stg_v4(dst, ov);
           if (dOq) {
-            // a half-warp holds one 128-element slice (nvec % 32 == 0 in this mode)
+            // a half-warp holds one 128-element slice, four lanes a 32-element
+            // piece (nvec % 32 == 0 in this mode)
             float fq[8];
             unpack8(ov, fq);
             float m = amax8(fq);
 #pragma unroll
-            for (int o = 8; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(half, m, o));
+            for (int o = piece_lanes / 2; o > 0; o >>= 1)
+              m = fmaxf(m, __shfl_xor_sync(half, m, o));
             const uint32_t code = ue8m0_code(m);
             *reinterpret_cast<uint2*>(dOq + (size_t)rows[j] * H + (size_t)c * 8) =
                 e4m3x8(fq, ue8m0_inv(code));
-            if ((lane & 15) == 0)
-              dOsf[f8::atom_offset(rows[j] >> 7, c >> 4, kg) + f8::atom_byte(rows[j], c >> 4)] =
-                  (uint8_t)code;
+            if ((lane & (piece_lanes - 1)) == 0)
+              dOsf[f8::row_sf_index(rows[j], c, kg, MX)] = (uint8_t)code;
           }
         }
       }
@@ -484,6 +487,33 @@ cudaError_t launch_unpermute(const moe_config& c, const void* y_perm, const int3
                                      s, pages);
 }
 
+template <bool MX>
+static void unpermute_bwd_launch(const moe_config& c, const __nv_bfloat16* dYp,
+                                 const __nv_bfloat16* yp, const int32_t* row_of, const float* w,
+                                 const int32_t* counts, const int32_t* offsets,
+                                 __nv_bfloat16* dOp, float* dw, cudaStream_t s, uint8_t* dOq,
+                                 uint8_t* dOsf, const int32_t* pages) {
+  // one warp per token (8 per block), capped at 16 blocks per SM
+  const int grid = grid_for_warps(c.T);
+  const int nr = c.k + c.n_shared;
+  if (nr <= 2)
+    unpermute_bwd_kernel<2, 4, false, MX><<<grid, 256, 0, s>>>(
+        dYp, yp, row_of, w, counts, offsets, dOp, dw, c.T, c.H, c.k, c.E, c.n_shared, dOq, dOsf,
+        pages);
+  else if (nr <= 4)
+    unpermute_bwd_kernel<4, 4, false, MX><<<grid, 256, 0, s>>>(
+        dYp, yp, row_of, w, counts, offsets, dOp, dw, c.T, c.H, c.k, c.E, c.n_shared, dOq, dOsf,
+        pages);
+  else if (nr <= 8)
+    unpermute_bwd_kernel<8, 1, false, MX><<<grid, 256, 0, s>>>(
+        dYp, yp, row_of, w, counts, offsets, dOp, dw, c.T, c.H, c.k, c.E, c.n_shared, dOq, dOsf,
+        pages);
+  else
+    unpermute_bwd_kernel<kMaxK + 4, 1, false, MX><<<grid, 256, 0, s>>>(
+        dYp, yp, row_of, w, counts, offsets, dOp, dw, c.T, c.H, c.k, c.E, c.n_shared, dOq, dOsf,
+        pages);
+}
+
 cudaError_t launch_unpermute_bwd(const moe_config& c, const void* dY, const void* y_perm,
                                  const int32_t* row_of, const float* w, const int32_t* counts,
                                  const int32_t* offsets, void* dO_perm, float* dw,
@@ -492,24 +522,13 @@ cudaError_t launch_unpermute_bwd(const moe_config& c, const void* dY, const void
   auto dYp = static_cast<const __nv_bfloat16*>(dY);
   auto yp = static_cast<const __nv_bfloat16*>(y_perm);
   auto dOp = static_cast<__nv_bfloat16*>(dO_perm);
-  // one warp per token (8 per block), capped at 16 blocks per SM
-  const int grid = grid_for_warps(c.T);
-  if (c.k + c.n_shared <= 2)
-    unpermute_bwd_kernel<2, 4><<<grid, 256, 0, s>>>(dYp, yp, row_of, w, counts, offsets, dOp, dw,
-                                                    c.T, c.H, c.k, c.E, c.n_shared, dOq, dOsf,
-                                                    pages);
-  else if (c.k + c.n_shared <= 4)
-    unpermute_bwd_kernel<4, 4><<<grid, 256, 0, s>>>(dYp, yp, row_of, w, counts, offsets, dOp, dw,
-                                                    c.T, c.H, c.k, c.E, c.n_shared, dOq, dOsf,
-                                                    pages);
-  else if (c.k + c.n_shared <= 8)
-    unpermute_bwd_kernel<8, 1><<<grid, 256, 0, s>>>(dYp, yp, row_of, w, counts, offsets, dOp, dw,
-                                                    c.T, c.H, c.k, c.E, c.n_shared, dOq, dOsf,
-                                                    pages);
+  // (the MX pieces of dO's 1-byte form are 32 elements, the block recipe's 128)
+  if (c.dtype == MOE_DTYPE_MXFP8 && dOq)
+    unpermute_bwd_launch<true>(c, dYp, yp, row_of, w, counts, offsets, dOp, dw, s, dOq, dOsf,
+                               pages);
   else
-    unpermute_bwd_kernel<kMaxK + 4, 1><<<grid, 256, 0, s>>>(
-        dYp, yp, row_of, w, counts, offsets, dOp, dw, c.T, c.H, c.k, c.E, c.n_shared, dOq, dOsf,
-        pages);
+    unpermute_bwd_launch<false>(c, dYp, yp, row_of, w, counts, offsets, dOp, dw, s, dOq, dOsf,
+                                pages);
   return cudaGetLastError();
 }
 

@@ -61,6 +61,13 @@ __host__ __device__ constexpr int64_t sf_stride(int64_t K, bool mx) {
 __host__ __device__ constexpr int64_t sf_bytes_of(int64_t rows, int64_t K, bool mx) {
   return mx ? mx_sf_bytes(rows, K) : sf_bytes(rows, K);
 }
+// Scale byte of row r's piece holding its 8-element vector c in a row form
+// (1 x 128 pieces: one per 16 vectors, atoms_k layout; MX 1 x 32 pieces: one
+// per 4 vectors, MX layout); kg = sf_stride(row length, mx).
+__host__ __device__ constexpr int64_t row_sf_index(int64_t r, int c, int64_t kg, bool mx) {
+  return mx ? mx_atom_offset(r >> 7, c >> 4, kg) + atom_byte((int)r, (c >> 2) & 3)
+            : atom_offset(r >> 7, c >> 4, kg) + atom_byte((int)r, c >> 4);
+}
 
 }  // namespace f8
 

@@ -182,6 +182,35 @@ __device__ __forceinline__ bool f8_epilogue_tile(
             (uint8_t)code;
       x_phase ^= 1u;
     }
+    if (MX && p.qout) {
+      // h's 1 x 32 pieces (MXFP8): each is one of this thread's 32-column chunks
+      const int row = row0 + lane;
+      uint8_t* dst = p.qout + (size_t)row * p.F + f0;
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        float m = 0.f;
+#pragma unroll
+        for (int v = 0; v < 4; ++v) {
+          float f[8];
+          unpack8(ho[c][v], f);
+          m = fmaxf(m, amax8(f));
+        }
+        const uint32_t code = ue8m0_code(m);
+        const float inv = ue8m0_inv(code);
+        uint2 b[4];
+#pragma unroll
+        for (int v = 0; v < 4; ++v) {
+          float f[8];
+          unpack8(ho[c][v], f);
+          b[v] = e4m3x8(f, inv);
+        }
+        *reinterpret_cast<uint4*>(dst + 32 * c) = make_uint4(b[0].x, b[0].y, b[1].x, b[1].y);
+        *reinterpret_cast<uint4*>(dst + 32 * c + 16) = make_uint4(b[2].x, b[2].y, b[3].x, b[3].y);
+        const int col = f0 + 32 * c;
+        p.qsf[f8::mx_atom_offset(row >> 7, col >> 7, p.qsf_kg) + f8::atom_byte(row, (col >> 5) & 3)] =
+            (uint8_t)code;
+      }
+    }
   } else if (EPI == kEpiWgrad) {
     // dW rows g*Mw + m-tile.., columns n-tile*256 + 128*half.. in 32 x 32 boxes
     const int c0 = nt * kF8BN + 128 * half;
@@ -616,7 +645,7 @@ cudaError_t launch_ffn_fc1_fp8(const moe_config& c, const uint8_t* xq, const uin
   p.sfb = W13sf;
   p.sfb_nb = 2 * c.F / 128;
   p.sfb_kg = sf_kg(c, c.H);
-  p.qout = is_mx(c) ? nullptr : hq;         // MX: h is quantised by its own pass
+  p.qout = hq;
   p.qsf = hsf;
   p.qsf_kg = sf_kg(c, c.F);
   return run_fp8<kEpiSwigluFwd, 0>(a, b, oc, oc2, p, is_mx(c), s);

@@ -118,9 +118,6 @@ cudaError_t launch_quant_tiles8(const void* W, uint8_t* Wq, uint8_t* sf_f, uint8
                                 int rows, int cols, cudaStream_t s);
 // mx: 32-element blocks and the MX atom layout (MXFP8), else 128.
 // pages (optional): X is a paged stash tensor (StashMap); the outputs are not.
-cudaError_t launch_quant_rows8(const void* X, uint8_t* Xq, uint8_t* sf, const int32_t* offsets,
-                               const int32_t* counts, int G, int64_t rows_max, int cols,
-                               cudaStream_t s, bool mx = false, const int32_t* pages = nullptr);
 cudaError_t launch_quant_cols8(const void* X, uint8_t* Xq, uint8_t* sf, const int32_t* offsets,
                                const int32_t* counts, int G, int64_t rows_max, int cols,
                                cudaStream_t s, bool mx = false, const int32_t* pages = nullptr);

@@ -256,14 +256,10 @@ static moe_status permute_impl(const moe_config* cfg, const void* x, const int32
   const bool fp8 = is_fp8(*cfg);
   if (fp8) q = fp8_scratch(*cfg, scratch);
   cudaStream_t s = (cudaStream_t)stream;
-  // the block recipe writes x_perm's 1x128 E4M3 form in the scatter itself;
-  // MXFP8's 1x32 form is a pass of its own
+  // x_perm's E4M3 form (1x128, or 1x32 for MXFP8) is written by the scatter itself
   MOE_CUDA(launch_permute(*cfg, x, idx, counts, offsets, row_of, token_of, sel_offsets,
                           sel_tokens, x_perm, static_cast<uint8_t*>(scratch), s,
-                          fp8 && !q.mx ? &q : nullptr, alloc));
-  if (fp8 && q.mx)
-    MOE_CUDA(launch_quant_rows8(x_perm, q.xq, q.xsf, offsets, counts, cfg->E + cfg->n_shared,
-                                rows_max(*cfg), cfg->H, s, true, alloc ? alloc->table : nullptr));
+                          fp8 ? &q : nullptr, alloc));
   return MOE_OK;
 }
 
@@ -279,15 +275,10 @@ static moe_status ffn_fwd_impl(const moe_config* cfg, const void* x_perm, const 
   if (is_fp8(*cfg)) {
     // the E4M3 weights are the ones moe_quantize_weights left in scratch, the
     // E4M3 x_perm the one moe_permute wrote there with the bf16 rows; h's
-    // E4M3 form comes out of the FC1 epilogue (block recipe) or its own pass
+    // E4M3 form comes out of the FC1 epilogue
     const Fp8Scratch q = fp8_scratch(*cfg, scratch);
-    const int G = cfg->E + cfg->n_shared;
-    const int64_t R = rows_max(*cfg);
     MOE_CUDA(launch_ffn_fc1_fp8(*cfg, q.xq, q.xsf, counts, offsets, q.W13q, q.W13sf, GU, h, q.hq,
                                 q.hsf, st, s, sm));
-    if (q.mx)
-      MOE_CUDA(launch_quant_rows8(h, q.hq, q.hsf, offsets, counts, G, R, cfg->F, s, true,
-                                  sm.pages));
     MOE_CUDA(launch_ffn_fc2_fp8(*cfg, q.hq, q.hsf, counts, offsets, q.W2q, q.W2sf, y_perm, st, s,
                                 sm));
     return MOE_OK;
@@ -320,16 +311,13 @@ static moe_status unpermute_bwd_impl(const moe_config* cfg, const void* dY, cons
   Fp8Scratch q;
   const bool fp8 = is_fp8(*cfg);
   if (fp8) q = fp8_scratch(*cfg, scratch);
-  if (fp8 && !q.mx) {                 // dO's 1x128 E4M3 form written by the scatter itself
+  if (fp8) {                          // dO's E4M3 form written by the scatter itself
     dOq = q.dOq;
     dOsf = q.dOsf;
   }
   cudaStream_t s = (cudaStream_t)stream;
   MOE_CUDA(launch_unpermute_bwd(*cfg, dY, y_perm, row_of, w, counts, offsets, dO_perm, dw, s, dOq,
                                 dOsf, pages));
-  if (fp8 && q.mx)
-    MOE_CUDA(launch_quant_rows8(dO_perm, q.dOq, q.dOsf, offsets, counts, cfg->E + cfg->n_shared,
-                                rows_max(*cfg), cfg->H, s, true));
   return MOE_OK;
 }
 

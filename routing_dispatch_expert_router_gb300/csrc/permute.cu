@@ -231,11 +231,12 @@ __device__ __forceinline__ int find_group(const int* prefix, int G, int p) {
 // Virtual rows v < T copy token v to its rows; v >= T zero one padding row
 // (the padding rows inside each segment's last 128-row block, the ones a GEMM
 // reads).
-// With xq (the FP8 configuration) every row is also written in its 1-byte form
-// -- E4M3 codes of its 1 x 128 slices and their UE8M0 scales in the atoms of
-// xsf (fp8_layout.cuh) -- for the FC1 GEMM: each slice is quantised once per
-// token and written to each of the token's rows; padding rows get zero codes
-// and scale 1.
+// With xq (the FP8 configurations) every row is also written in its 1-byte
+// form -- E4M3 codes of its 1 x 128 slices (MXFP8: 1 x 32) and their UE8M0
+// scales in the atoms of xsf (fp8_layout.cuh) -- for the FC1 GEMM: each slice
+// is quantised once per token and written to each of the token's rows;
+// padding rows get zero codes and scale 1.
+template <bool MX>
 __global__ void __launch_bounds__(256)
 permute_scatter_kernel(const __nv_bfloat16* __restrict__ x, const int32_t* __restrict__ row_of,
                        const int32_t* __restrict__ counts, const int32_t* __restrict__ offsets,
@@ -255,8 +256,9 @@ permute_scatter_kernel(const __nv_bfloat16* __restrict__ x, const int32_t* __res
   const int P = s_pp[G];
   const int lane = threadIdx.x & 31;
   const int nvec = H >> 3;
-  const int64_t kg = f8::atoms_k(H);
+  const int64_t kg = f8::sf_stride(H, MX);
   const unsigned half = (lane & 16) ? 0xffff0000u : 0x0000ffffu;
+  constexpr int piece_lanes = MX ? 4 : 16;         // lanes per scale piece
   const int warps = gridDim.x * (blockDim.x >> 5);
   for (int v = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); v < T + P; v += warps) {
     if (v < T) {
@@ -273,8 +275,9 @@ permute_scatter_kernel(const __nv_bfloat16* __restrict__ x, const int32_t* __res
 #pragma unroll
         for (int u = 0; u < 4; ++u)
           if (c0 + 32 * u < nvec) q[u] = ldg_nc_v4(src + (size_t)(c0 + 32 * u) * 8);
-        // 1-byte form: a half-warp holds one 128-element slice per u (nvec is a
-        // multiple of 16, so a half-warp is wholly in range or out)
+        // 1-byte form: a half-warp holds one 128-element slice per u, four
+        // lanes one 32-element piece (nvec is a multiple of 16, so a half-warp
+        // is wholly in range or out)
         uint2 qb[4];
         uint32_t code[4];
         if (xq) {
@@ -285,7 +288,8 @@ permute_scatter_kernel(const __nv_bfloat16* __restrict__ x, const int32_t* __res
             unpack8(q[u], f);
             float m = amax8(f);
 #pragma unroll
-            for (int o = 8; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(half, m, o));
+            for (int o = piece_lanes / 2; o > 0; o >>= 1)
+              m = fmaxf(m, __shfl_xor_sync(half, m, o));
             code[u] = ue8m0_code(m);
             qb[u] = e4m3x8(f, ue8m0_inv(code[u]));
           }
@@ -303,9 +307,8 @@ permute_scatter_kernel(const __nv_bfloat16* __restrict__ x, const int32_t* __res
               const int c = c0 + 32 * u;
               if (c >= nvec) continue;
               *reinterpret_cast<uint2*>(xq + (size_t)rows[j] * H + (size_t)c * 8) = qb[u];
-              if ((lane & 15) == 0)
-                xsf[f8::atom_offset(rows[j] >> 7, c >> 4, kg) + f8::atom_byte(rows[j], c >> 4)] =
-                    (uint8_t)code[u];
+              if ((lane & (piece_lanes - 1)) == 0)
+                xsf[f8::row_sf_index(rows[j], c, kg, MX)] = (uint8_t)code[u];
             }
           }
         }
@@ -320,8 +323,7 @@ permute_scatter_kernel(const __nv_bfloat16* __restrict__ x, const int32_t* __res
         stg_v4(dst + (size_t)c0 * 8, z);
         if (xq) {
           *reinterpret_cast<uint2*>(xq + (size_t)r * H + (size_t)c0 * 8) = make_uint2(0u, 0u);
-          if ((c0 & 15) == 0)
-            xsf[f8::atom_offset(r >> 7, c0 >> 4, kg) + f8::atom_byte(r, c0 >> 4)] = 127u;
+          if ((c0 & (piece_lanes - 1)) == 0) xsf[f8::row_sf_index(r, c0, kg, MX)] = 127u;
         }
       }
     }
@@ -359,11 +361,14 @@ cudaError_t launch_permute(const moe_config& c, const void* x, const int32_t* id
   }
   uint8_t* xq = nullptr;
   uint8_t* xsf = nullptr;
-  if (c.dtype == MOE_DTYPE_FP8_E4M3_BLOCK && fp8) {
+  if (c.dtype != MOE_DTYPE_BF16 && fp8) {
     xq = fp8->xq;
     xsf = fp8->xsf;
   }
-  permute_scatter_kernel<<<num_sms() * 8, 256, 0, s>>>(
+  // (the MX pieces of x_perm's 1-byte form are 32 elements, the block recipe's 128)
+  auto kern = (c.dtype == MOE_DTYPE_MXFP8 && xq) ? permute_scatter_kernel<true>
+                                                 : permute_scatter_kernel<false>;
+  kern<<<num_sms() * 8, 256, 0, s>>>(
       static_cast<const __nv_bfloat16*>(x), row_of, counts, offsets, pad_prefix,
       static_cast<__nv_bfloat16*>(x_perm), c.T, c.H, c.k, c.E, c.n_shared, xq, xsf, pages);
   return cudaGetLastError();

@@ -215,55 +215,6 @@ quant_tiles8_kernel(const __nv_bfloat16* __restrict__ W, uint8_t* __restrict__ W
   }
 }
 
-// 1 x BLK slices (BLK = 128, or 32 for MX) along the rows of the live
-// 128-row blocks of [0, offsets[G]) -> E4M3 bytes plus UE8M0 scale atoms.
-// Work items of 16 rows (eight per 128-row block, so the grid's last wave is
-// short); each half-warp owns one row and walks it two 128-element K blocks at
-// a time (16 lanes x 16 bytes per block, both loads in flight together). The
-// scale of a BLK-wide piece is the maximum over the BLK / 8 lanes holding it.
-template <int BLK>
-__global__ void __launch_bounds__(256)
-quant_rows8_kernel(const __nv_bfloat16* __restrict__ X, uint8_t* __restrict__ Xq,
-                   uint8_t* __restrict__ sf, const int32_t* __restrict__ offsets,
-                   const int32_t* __restrict__ counts, int G, int cols, long long kg,
-                   const int32_t* __restrict__ pages) {
-  static_assert(BLK == 128 || BLK == 32, "block length");
-  constexpr int LANES = BLK / 8;                          // lanes per scale piece
-  const long long items = offsets[G] / 128 * 8;
-  const int KB = cols >> 7;
-  const int hw = threadIdx.x >> 4, l16 = threadIdx.x & 15;
-  const unsigned half = (threadIdx.x & 16) ? 0xffff0000u : 0x0000ffffu;
-  for (long long it = blockIdx.x; it < items; it += gridDim.x) {
-    const long long rb = it >> 3;
-    if (!live_block(offsets, counts, G, rb)) continue;
-    const int r = (int)(it & 7) * 16 + hw;                // row inside the 128-row block
-    const size_t row = (size_t)rb * 128 + r;
-    const __nv_bfloat16* src = X + (size_t)stash_row(pages, (int)row) * cols + l16 * 8;
-    uint8_t* dst = Xq + row * cols + l16 * 8;
-    for (int kb = 0; kb < KB; kb += 2) {
-      const bool two = kb + 1 < KB;
-      float f[2][8];
-      unpack8(ldg_nc_v4(src + (size_t)kb * 128), f[0]);
-      if (two) unpack8(ldg_nc_v4(src + (size_t)(kb + 1) * 128), f[1]);
-#pragma unroll
-      for (int u = 0; u < 2; ++u) {
-        if (u == 1 && !two) break;
-        float m = amax8(f[u]);
-#pragma unroll
-        for (int o = LANES / 2; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(half, m, o));
-        const uint32_t code = ue8m0_code(m);
-        *reinterpret_cast<uint2*>(dst + (size_t)(kb + u) * 128) = e4m3x8(f[u], ue8m0_inv(code));
-        if ((l16 & (LANES - 1)) == 0) {
-          if (BLK == 128)
-            sf[f8::atom_offset(rb, kb + u, kg) + f8::atom_byte(r, kb + u)] = (uint8_t)code;
-          else
-            sf[f8::mx_atom_offset(rb, kb + u, kg) + f8::atom_byte(r, l16 / LANES)] = (uint8_t)code;
-        }
-      }
-    }
-  }
-}
-
 // MX weights: every 128 x 128 tile of W [G, rows, cols] (bf16) -> two E4M3
 // forms. Forward (Wf, sf_f): 1 x 32 pieces along the columns (the forward
 // GEMM's K), atoms with the weight's rows as N. Data gradient (Wd, sf_d):
@@ -360,19 +311,6 @@ cudaError_t launch_quant_wmx(const void* W, uint8_t* Wf, uint8_t* Wd, uint8_t* s
   const long long n = (long long)G * (rows / 128) * (cols / 128);
   quant_wmx_kernel<<<grid_cap(n, 1), 256, 0, s>>>(static_cast<const __nv_bfloat16*>(W), Wf, Wd,
                                                   sf_f, sf_d, n, rows, cols);
-  return cudaGetLastError();
-}
-
-cudaError_t launch_quant_rows8(const void* X, uint8_t* Xq, uint8_t* sf, const int32_t* offsets,
-                               const int32_t* counts, int G, int64_t rows_max, int cols,
-                               cudaStream_t s, bool mx, const int32_t* pages) {
-  const int grid = grid_cap(rows_max / 128 * 8, 1);
-  const long long kg = f8::sf_stride(cols, mx);
-  const __nv_bfloat16* x = static_cast<const __nv_bfloat16*>(X);
-  if (mx)
-    quant_rows8_kernel<32><<<grid, 256, 0, s>>>(x, Xq, sf, offsets, counts, G, cols, kg, pages);
-  else
-    quant_rows8_kernel<128><<<grid, 256, 0, s>>>(x, Xq, sf, offsets, counts, G, cols, kg, pages);
   return cudaGetLastError();
 }
 
