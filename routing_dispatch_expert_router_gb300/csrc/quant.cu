@@ -235,26 +235,24 @@ quant_wmx_kernel(const __nv_bfloat16* __restrict__ W, uint8_t* __restrict__ Wf,
     const int rem = (int)(t % ((long long)tr * tc));
     const int rt = rem / tc, ct = rem % tc;
     const size_t base = (size_t)g * rows * cols + (size_t)rt * 128 * cols + (size_t)ct * 128;
-    {
-      uint4 in[8];
+    uint4 in[8];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const int v = tid + 256 * i, r = v >> 4, q = v & 15;
-        in[i] = ldg_nc_v4(W + base + (size_t)r * cols + q * 8);
-      }
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const int v = tid + 256 * i;
-        tile[v >> 4][v & 15] = in[i];
-      }
+    for (int i = 0; i < 8; ++i) {
+      const int v = tid + 256 * i, r = v >> 4, q = v & 15;
+      in[i] = ldg_nc_v4(W + base + (size_t)r * cols + q * 8);
     }
-    // forward form: a 1 x 32 piece is four consecutive lanes' vectors (each
-    // thread reads back the vectors it stored)
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int v = tid + 256 * i;
+      tile[v >> 4][v & 15] = in[i];
+    }
+    // forward form: a 1 x 32 piece is four consecutive lanes' vectors (from the
+    // registers the tile was loaded into)
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
       const int v = tid + 256 * i, r = v >> 4, q = v & 15;
       float f[8];
-      unpack8(tile[r][q], f);
+      unpack8(in[i], f);
       float m = amax8(f);
       m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
       m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
@@ -265,18 +263,23 @@ quant_wmx_kernel(const __nv_bfloat16* __restrict__ W, uint8_t* __restrict__ Wf,
     }
     __syncthreads();
     {
-      // data-gradient form: column c, 32-row pieces 2h and 2h + 1
-      const int c = tid & 127, h = tid >> 7;
-      const __nv_bfloat16* col = reinterpret_cast<const __nv_bfloat16*>(&tile[0][0]) + c;
-#pragma unroll
-      for (int j = 2 * h; j < 2 * h + 2; ++j) {
-        float m = 0.f;
+      // data-gradient form: columns c and c + 1 (one bf16 pair per 4-byte read,
+      // consecutive lanes on consecutive words), 32-row piece j
+      const int c = 2 * (tid & 63), j = tid >> 6;
+      const uint32_t* pair = reinterpret_cast<const uint32_t*>(&tile[0][0]) + (c >> 1);
+      float m0 = 0.f, m1 = 0.f;
 #pragma unroll 8
-        for (int r = 32 * j; r < 32 * j + 32; ++r) m = fmaxf(m, fabsf(__bfloat162float(col[r * 128])));
-        const uint32_t code = ue8m0_code(m);
-        inv_d[j][c] = ue8m0_inv(code);
-        sf_d[f8::mx_atom_offset(g * tc + ct, rt, tr) + f8::atom_byte(c, j)] = (uint8_t)code;
+      for (int r = 32 * j; r < 32 * j + 32; ++r) {
+        const uint32_t w2 = pair[r * 64];
+        m0 = fmaxf(m0, fabsf(bf16_lo(w2)));
+        m1 = fmaxf(m1, fabsf(bf16_hi(w2)));
       }
+      const uint32_t code0 = ue8m0_code(m0), code1 = ue8m0_code(m1);
+      inv_d[j][c] = ue8m0_inv(code0);
+      inv_d[j][c + 1] = ue8m0_inv(code1);
+      const int64_t at = f8::mx_atom_offset(g * tc + ct, rt, tr);
+      sf_d[at + f8::atom_byte(c, j)] = (uint8_t)code0;
+      sf_d[at + f8::atom_byte(c + 1, j)] = (uint8_t)code1;
     }
     __syncthreads();
 #pragma unroll
