@@ -48,7 +48,8 @@ __device__ __forceinline__ bool live_block(const int32_t* __restrict__ offsets,
 // [along the rows]. One block of 256 threads per (128-row block, 128-column
 // slab): the 128 x 128 tile is read once into shared memory with 16-byte
 // loads (eight per thread in flight), the maxima of each column's four
-// 32-row pieces are taken there (combined into one for BLK = 128), and every
+// 32-row pieces are taken there (a bf16 pair of columns per read; combined into
+// one for BLK = 128), and every
 // thread quantises eight 8-column vectors read back from the tile and stores
 // their codes (8 bytes each). With ROWS, the same pass also writes the tile's
 // 1 x BLK row form (Xr, sfr; a row's 16 vectors sit in 16 consecutive lanes,
@@ -91,16 +92,19 @@ quant_cols8_kernel(const __nv_bfloat16* __restrict__ X, uint8_t* __restrict__ Xq
     }
     __syncthreads();
     {
-      // column c, 32-row pieces 2h and 2h + 1
-      const int c = tid & 127, h = tid >> 7;
-      const __nv_bfloat16* col = reinterpret_cast<const __nv_bfloat16*>(&tile[0][0]) + c;
-#pragma unroll
-      for (int j = 2 * h; j < 2 * h + 2; ++j) {
-        float m = 0.f;
+      // columns c and c + 1 (one bf16 pair per 4-byte read, consecutive lanes on
+      // consecutive words), 32-row piece j
+      const int c = 2 * (tid & 63), j = tid >> 6;
+      const uint32_t* pair = reinterpret_cast<const uint32_t*>(&tile[0][0]) + (c >> 1);
+      float m0 = 0.f, m1 = 0.f;
 #pragma unroll 8
-        for (int r = 32 * j; r < 32 * j + 32; ++r) m = fmaxf(m, fabsf(__bfloat162float(col[r * 128])));
-        part[j * 128 + c] = m;
+      for (int r = 32 * j; r < 32 * j + 32; ++r) {
+        const uint32_t w2 = pair[r * 64];
+        m0 = fmaxf(m0, fabsf(bf16_lo(w2)));
+        m1 = fmaxf(m1, fabsf(bf16_hi(w2)));
       }
+      part[j * 128 + c] = m0;
+      part[j * 128 + c + 1] = m1;
     }
     __syncthreads();
     if (BLK == 128) {
