@@ -177,6 +177,10 @@ typedef struct moe_fwd_state {
     int32_t* stash_top;      /* [1] int32: pages in use, shared by the pool's
                               * layers; zero it once before the first forward   */
 } moe_fwd_state;
+/* The per-stage entry points below (moe_permute, moe_grouped_ffn_*,
+ * moe_unpermute*, their _reordered forms) take the layer's own R-row buffers:
+ * with cfg->stash_pool_pages > 0 they return MOE_ERR_UNSUPPORTED, and paged
+ * stashing runs through moe_layer_fwd / moe_layer_bwd. */
 
 /* Backward temporaries (device pointers, caller-owned). */
 typedef struct moe_bwd_state {

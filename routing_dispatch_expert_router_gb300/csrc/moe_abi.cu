@@ -241,6 +241,13 @@ static moe_status stash_of(const moe_config* cfg, const moe_fwd_state* st, Stash
   return MOE_OK;
 }
 
+// The per-stage entry points take the layer's own rows_max-row buffers; a
+// paged stash (whose pool tensors have fewer rows) runs through the layer calls.
+static moe_status own_buffers(const moe_config* cfg) {
+  if (!cfg) return MOE_ERR_INVALID_ARG;
+  return cfg->stash_pool_pages > 0 ? MOE_ERR_UNSUPPORTED : MOE_OK;
+}
+
 // The stage bodies, shared by the per-stage entry points (the layer's own
 // buffers) and by moe_layer_fwd / moe_layer_bwd (which may keep the stashed
 // rows in pool pages).
@@ -510,6 +517,7 @@ moe_status moe_route_aux_bwd(const moe_config* cfg, const void* x, const float* 
 moe_status moe_permute(const moe_config* cfg, const void* x, const int32_t* idx, int32_t* counts,
                        int32_t* offsets, int32_t* row_of, int32_t* token_of, int32_t* sel_offsets,
                        int32_t* sel_tokens, void* x_perm, void* scratch, void* stream) {
+  MOE_TRY(own_buffers(cfg));
   return permute_impl(cfg, x, idx, counts, offsets, row_of, token_of, sel_offsets, sel_tokens,
                       x_perm, scratch, stream, nullptr);
 }
@@ -535,12 +543,14 @@ moe_status moe_quantize_weights(const moe_config* cfg, const void* W13, const vo
 moe_status moe_grouped_ffn_fwd(const moe_config* cfg, const void* x_perm, const int32_t* counts,
                                const int32_t* offsets, const void* W13, const void* W2, void* GU,
                                void* h, void* y_perm, void* scratch, void* stream) {
+  MOE_TRY(own_buffers(cfg));
   return ffn_fwd_impl(cfg, x_perm, counts, offsets, W13, W2, GU, h, y_perm, scratch, stream,
                       StashMap());
 }
 
 moe_status moe_unpermute(const moe_config* cfg, const void* y_perm, const int32_t* row_of,
                          const float* w, const int32_t* offsets, void* out, void* stream) {
+  MOE_TRY(own_buffers(cfg));
   return unpermute_impl(cfg, y_perm, row_of, w, offsets, out, stream, nullptr);
 }
 
@@ -548,6 +558,7 @@ moe_status moe_unpermute_bwd(const moe_config* cfg, const void* dY, const void* 
                              const int32_t* row_of, const float* w, const int32_t* counts,
                              const int32_t* offsets, void* dO_perm, float* dw, void* scratch,
                              void* stream) {
+  MOE_TRY(own_buffers(cfg));
   return unpermute_bwd_impl(cfg, dY, y_perm, row_of, w, counts, offsets, dO_perm, dw, scratch,
                             stream, nullptr);
 }
@@ -557,6 +568,7 @@ moe_status moe_grouped_ffn_dgrad(const moe_config* cfg, const void* dO_perm, con
                                  const int32_t* token_of, const float* dlogits, const float* W_r,
                                  const void* W13, const void* W2, void* dGU, void* dX_perm,
                                  void* scratch, void* stream) {
+  MOE_TRY(own_buffers(cfg));
   return ffn_dgrad_impl(cfg, dO_perm, GU, h, counts, offsets, token_of, dlogits, W_r, W13, W2, dGU,
                         dX_perm, scratch, stream, StashMap());
 }
@@ -565,6 +577,7 @@ moe_status moe_grouped_ffn_wgrad(const moe_config* cfg, const void* dO_perm, con
                                  const void* h, const void* dGU, const int32_t* counts,
                                  const int32_t* offsets, void* dW13, void* dW2, void* scratch,
                                  void* stream) {
+  MOE_TRY(own_buffers(cfg));
   return ffn_wgrad_impl(cfg, dO_perm, x_perm, h, dGU, counts, offsets, dW13, dW2, scratch, stream,
                         StashMap());
 }
@@ -591,6 +604,7 @@ moe_status moe_grouped_ffn_fwd_reordered(const moe_config* cfg, const void* x_pe
                                          const float* w, const void* W13, const void* W2,
                                          void* GU, void* h, void* y_perm, void* scratch,
                                          void* stream) {
+  MOE_TRY(own_buffers(cfg));
   return ffn_fwd_reordered_impl(cfg, x_perm, counts, offsets, token_of, row_of, w, W13, W2, GU, h,
                                 y_perm, scratch, stream, StashMap());
 }
@@ -613,6 +627,7 @@ moe_status moe_grouped_ffn_dgrad_reordered(const moe_config* cfg, const void* dO
                                            const void* W13, const void* W2, void* dGU,
                                            void* dX_perm, float* dw, float* dlogits,
                                            void* scratch, void* stream) {
+  MOE_TRY(own_buffers(cfg));
   return ffn_dgrad_reordered_impl(cfg, dO_perm, GU, h, counts, offsets, token_of, row_of, logits,
                                   idx, w, W_r, W13, W2, dGU, dX_perm, dw, dlogits, scratch, stream,
                                   StashMap());

@@ -155,7 +155,7 @@ def test_aux_loss_entry_points_reject_bad_arguments_before_launch():
 
 
 def test_status_strings():
-    for code in range(7):
+    for code in range(8):
         assert B.status_string(code)
     assert "unknown" in B.status_string(99)
 
@@ -185,3 +185,35 @@ def test_reordered_layer_configuration_checks():
     with pytest.raises(B.MoEError) as e:
         B.moe_query_sizes(DSV3_FP8.with_(weights_in_expert=1))
     assert e.value.code == 2
+
+
+def test_paged_stash_configuration_checks():
+    """stash_pool_pages: the table length moe_query_sizes reports, the pool's
+    range, the layer calls' pointer checks and the per-stage entry points'
+    refusal (their buffers are the layer's own R rows) -- all before any launch."""
+    s = B.moe_query_sizes(DSV3_FP8)
+    assert s.stash_table_len == s.rows_max // 128 + 2
+    cfg = B.config(TINY)
+    lib = B.lib()
+    vp = ctypes.c_void_p
+    ok = vp(4096)
+    for bad in (-1, (1 << 24)):
+        cfg.stash_pool_pages = bad
+        sz = B.MoESizes()
+        assert lib.moe_query_sizes(ctypes.byref(cfg), ctypes.byref(sz)) == 1
+    cfg.stash_pool_pages = 16
+    # per-stage entry points: MOE_ERR_UNSUPPORTED with a pool configuration
+    assert lib.moe_permute(ctypes.byref(cfg), ok, ok, ok, ok, ok, ok, ok, ok, ok, ok,
+                           vp(None)) == 2
+    assert lib.moe_grouped_ffn_fwd(ctypes.byref(cfg), ok, ok, ok, ok, ok, ok, ok, ok, ok,
+                                   vp(None)) == 2
+    assert lib.moe_unpermute(ctypes.byref(cfg), ok, ok, ok, ok, ok, vp(None)) == 2
+    # the layer forward wants the page table and the pool counter
+    fs = B.MoEFwdState(**{n: 4096 for n in B.FWD_FIELDS})
+    P = B.MoEParams(W_r=4096, bias=None, W13=4096, W2=4096)
+    assert lib.moe_layer_fwd(ctypes.byref(cfg), ctypes.byref(P), ok, ok, ctypes.byref(fs), ok,
+                             vp(None)) == 1
+    # releasing needs a pool
+    cfg.stash_pool_pages = 0
+    fs.stash_table, fs.stash_top = 4096, 4096
+    assert lib.moe_stash_release(ctypes.byref(cfg), ctypes.byref(fs), vp(None)) == 1

@@ -208,3 +208,32 @@ def test_two_layer_step_with_a_pool_replays_from_a_cuda_graph(shape):
         for (who, k), v in ref.items():
             got = (oA if who == "A" else oB)[k]
             assert torch.equal(got, v), (who, k)
+
+
+@pytest.mark.slow
+def test_paged_stash_at_full_size_is_bit_identical():
+    """The FP8 DeepSeek-V3-shaped layer (T=16384, H=7168, E=256, top-8, capacity 1.25),
+    the benched workload, on a pool of exactly its live pages -- fewer rows than its
+    worst-case buffers -- against the same layer on its own buffers: every output the
+    same bits."""
+    from workloads import DSV3_FP8
+    shape = DSV3_FP8
+    torch.cuda.empty_cache()
+    d = make_inputs(shape, seed=0, device="cuda")
+    ref, counts, _ = _own_buffers(shape, d)
+    torch.cuda.empty_cache()
+    P = _pages(counts)
+    cfg = _paged_cfg(shape, P)
+    pool = B.alloc_stash_pool(cfg, P)
+    bufs = B.alloc_buffers(cfg, "cuda", pool=pool)
+    assert (P + 1) * 128 < int(bufs.sizes.rows_max)      # capacity mode: the pool is smaller
+    o = _outs(shape)
+    _fwd(cfg, d, bufs, o)
+    torch.cuda.synchronize()
+    assert int(pool.top.item()) == P
+    _bwd(cfg, d, bufs, o)
+    torch.cuda.synchronize()
+    assert B.moe_last_device_status(bufs.scratch) == 0
+    assert int(pool.top.item()) == 0
+    for name in OUTS:
+        assert torch.equal(o[name], ref[name]), name
