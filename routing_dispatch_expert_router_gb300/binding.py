@@ -343,6 +343,8 @@ class StashPool:
 
 def alloc_stash_pool(cfg, pages: int, device="cuda") -> StashPool:
     c = _cfg(cfg)
+    if int(pages) < 1:
+        raise ValueError("a stash pool has at least one page (stash_pool_pages = 0 means no pool)")
     rows = (int(pages) + 1) * 128
     bf = torch.bfloat16
     e = lambda *s: torch.empty(*s, dtype=bf, device=device)  # noqa: E731
@@ -369,8 +371,8 @@ def alloc_buffers(cfg, device="cuda", backward: bool = True,
         fwd.update(x_perm=e(R, H, dt=bf), GU=e(R, 2 * F, dt=bf), h=e(R, F, dt=bf),
                    y_perm=e(R, H, dt=bf))
     else:
-        if c.stash_pool_pages != pool.pages:
-            raise ValueError("cfg.stash_pool_pages must equal the pool's pages")
+        if c.stash_pool_pages < 1 or c.stash_pool_pages != pool.pages:
+            raise ValueError("cfg.stash_pool_pages must equal the pool's pages (at least 1)")
         fwd.update(pool.tensors)
         fwd.update(stash_table=e(int(sz.stash_table_len), dt=i32), stash_top=pool.top)
     bwd = {}

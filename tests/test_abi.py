@@ -217,3 +217,20 @@ def test_paged_stash_configuration_checks():
     cfg.stash_pool_pages = 0
     fs.stash_table, fs.stash_top = 4096, 4096
     assert lib.moe_stash_release(ctypes.byref(cfg), ctypes.byref(fs), vp(None)) == 1
+
+
+def test_stash_pool_binding_guards():
+    """A pool has at least one page, and a pool's tensors are only handed to a
+    configuration that says it uses that pool (else the library would take
+    them for the layer's own R-row buffers)."""
+    cfg = B.config(TINY)
+    with pytest.raises(ValueError):
+        B.alloc_stash_pool(cfg, 0, device="cpu")
+    pool = B.alloc_stash_pool(cfg, 3, device="cpu")
+    assert pool.tensors["x_perm"].shape == (4 * 128, TINY.H)
+    with pytest.raises(ValueError):
+        B.alloc_buffers(cfg, "cpu", backward=False, pool=pool)      # cfg has no pool
+    cfg.stash_pool_pages = 3
+    bufs = B.alloc_buffers(cfg, "cpu", backward=False, pool=pool)
+    assert bufs.fwd["x_perm"].data_ptr() == pool.tensors["x_perm"].data_ptr()
+    assert bufs.fwd["stash_table"].numel() == bufs.sizes.stash_table_len
