@@ -339,6 +339,20 @@ MOE_API moe_status moe_permute_noalloc_status(int32_t* code, void* stream);
 MOE_API moe_status moe_quantize_weights(const moe_config* cfg, const void* W13, const void* W2,
                                         void* scratch, void* stream);
 
+/* FP8 block recipe (MOE_DTYPE_FP8_E4M3_BLOCK; MOE_ERR_UNSUPPORTED otherwise):
+ * expert weights the caller quantised itself, in place of moe_quantize_weights.
+ * W13_e4m3 [G,2F,H] and W2_e4m3 [G,H,F]: E4M3 codes (1 byte each, 16-byte
+ * aligned); W13_scale [G, 2F/128, H/128] and W2_scale [G, H/128, F/128]: one
+ * UE8M0 code per 128x128 tile (the tile's weights are code value x
+ * 2^(scale - 127)). The codes are copied into `scratch` and the scales laid
+ * out as the GEMMs read them, for both orientations. moe_layer_fwd skips its
+ * own weight quantisation when params->W13 and params->W2 are both NULL in
+ * an FP8 mode and uses what scratch holds (so E4M3 weights kept across several
+ * steps are loaded once); the FP8 backward never reads the bf16 weights. */
+MOE_API moe_status moe_load_fp8_weights(const moe_config* cfg, const void* W13_e4m3,
+                                        const uint8_t* W13_scale, const void* W2_e4m3,
+                                        const uint8_t* W2_scale, void* scratch, void* stream);
+
 /* Stage 3, compute (es summary §2.1 step 3; grouped GEMM, §2.3.C): for every
  * group g, on its rows X: [G|U] = X W13[g]^T (GU, bf16), h = bf16(silu(G) U),
  * y_perm = bf16(h W2[g]^T). tcgen05 grouped GEMMs that read counts/offsets on

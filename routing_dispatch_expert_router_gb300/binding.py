@@ -23,7 +23,7 @@ STATUS_NAMES = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED",
 ENTRY_POINTS = (
     "moe_query_sizes", "moe_route", "moe_route_replay", "moe_route_aux", "moe_route_aux_bwd",
     "moe_permute", "moe_permute_noalloc", "moe_permute_noalloc_status",
-    "moe_quantize_weights", "moe_grouped_ffn_fwd", "moe_unpermute",
+    "moe_quantize_weights", "moe_load_fp8_weights", "moe_grouped_ffn_fwd", "moe_unpermute",
     "moe_unpermute_bwd", "moe_grouped_ffn_dgrad", "moe_grouped_ffn_wgrad", "moe_grouped_ffn_bwd",
     "moe_grouped_ffn_fwd_reordered", "moe_unpermute_bwd_reordered",
     "moe_grouped_ffn_dgrad_reordered", "moe_route_bwd", "moe_permute_bwd",
@@ -207,6 +207,11 @@ def moe_permute_noalloc(cfg, x, idx, counts, offsets, row_of, token_of, sel_offs
 def moe_quantize_weights(cfg, W13, W2, scratch, stream=None):
     """FP8 mode: the E4M3 weights (and scales) in scratch; no-op in bf16 mode."""
     _call("moe_quantize_weights", _cfg(cfg), W13, W2, scratch, _stream(stream))
+
+
+def moe_load_fp8_weights(cfg, W13_e4m3, W13_scale, W2_e4m3, W2_scale, scratch, stream=None):
+    _call("moe_load_fp8_weights", _cfg(cfg), W13_e4m3, W13_scale, W2_e4m3, W2_scale, scratch,
+          _stream(stream))
 
 
 def moe_permute_noalloc_status(stream=None) -> int:

@@ -127,6 +127,9 @@ cudaError_t launch_quant_rows_cols8(const void* X, uint8_t* Xr, uint8_t* sfr, ui
                                     uint8_t* sfc, const int32_t* offsets, const int32_t* counts,
                                     int G, int64_t rows_max, int cols, cudaStream_t s,
                                     bool mx = false);
+// The atoms of caller-quantised E4M3 weights from one UE8M0 code per 128x128 tile.
+cudaError_t launch_load_fp8_scales(const uint8_t* scale, uint8_t* sf_f, uint8_t* sf_d, int G,
+                                   int rows, int cols, cudaStream_t s);
 // MXFP8 weights: forward (1x32 along cols) and data-gradient (32x1 along rows) forms.
 cudaError_t launch_quant_wmx(const void* W, uint8_t* Wf, uint8_t* Wd, uint8_t* sf_f, uint8_t* sf_d,
                              int G, int rows, int cols, cudaStream_t s);

@@ -181,6 +181,7 @@ int64_t stash_rows(const moe_config& c, const StashMap& sm) {
 }
 
 static bool al16(const void* p) { return p && ((uintptr_t)p & 15u) == 0; }
+static bool al16_or_null(const void* p) { return !p || ((uintptr_t)p & 15u) == 0; }
 static bool al4(const void* p) { return p && ((uintptr_t)p & 3u) == 0; }
 // Token-indexed buffers may be NULL when the batch is empty (T == 0).
 static bool tok16(const moe_config* c, const void* p) { return (c->T == 0 && !p) || al16(p); }
@@ -241,6 +242,12 @@ static moe_status stash_of(const moe_config* cfg, const moe_fwd_state* st, Stash
   return MOE_OK;
 }
 
+// The bf16 expert weights: read by the bf16 GEMMs; in the FP8 modes only by the
+// weight quantisation (moe_quantize_weights), so they may be NULL there.
+static bool weights_ok(const moe_config* cfg, const void* W13, const void* W2) {
+  return is_fp8(*cfg) ? (al16_or_null(W13) && al16_or_null(W2)) : (al16(W13) && al16(W2));
+}
+
 // The per-stage entry points take the layer's own rows_max-row buffers; a
 // paged stash (whose pool tensors have fewer rows) runs through the layer calls.
 static moe_status own_buffers(const moe_config* cfg) {
@@ -275,7 +282,7 @@ static moe_status ffn_fwd_impl(const moe_config* cfg, const void* x_perm, const 
                                void* h, void* y_perm, void* scratch, void* stream,
     const StashMap& sm) {
   MOE_TRY(check_config(cfg));
-  MOE_REQUIRE(al16(x_perm) && al4(counts) && al4(offsets) && al16(W13) && al16(W2));
+  MOE_REQUIRE(al16(x_perm) && al4(counts) && al4(offsets) && weights_ok(cfg, W13, W2));
   MOE_REQUIRE(al16(GU) && al16(h) && al16(y_perm) && al16(scratch));
   cudaStream_t s = (cudaStream_t)stream;
   int32_t* st = status_word(scratch);
@@ -336,7 +343,7 @@ static moe_status ffn_dgrad_impl(const moe_config* cfg, const void* dO_perm, con
     const StashMap& sm) {
   MOE_TRY(check_config(cfg));
   MOE_REQUIRE(al16(dO_perm) && al16(GU) && al4(counts) && al4(offsets) && al4(token_of));
-  MOE_REQUIRE(tok4(cfg, dlogits) && al16(W_r) && al16(W13) && al16(W2) && al16(dGU));
+  MOE_REQUIRE(tok4(cfg, dlogits) && al16(W_r) && weights_ok(cfg, W13, W2) && al16(dGU));
   MOE_REQUIRE(al16(dX_perm) && al16(scratch) && (h == nullptr || al16(h)));
   cudaStream_t s = (cudaStream_t)stream;
   int32_t* st = status_word(scratch);
@@ -540,6 +547,23 @@ moe_status moe_quantize_weights(const moe_config* cfg, const void* W13, const vo
   return MOE_OK;
 }
 
+moe_status moe_load_fp8_weights(const moe_config* cfg, const void* W13_e4m3,
+                                const uint8_t* W13_scale, const void* W2_e4m3,
+                                const uint8_t* W2_scale, void* scratch, void* stream) {
+  MOE_TRY(check_config(cfg));
+  if (cfg->dtype != MOE_DTYPE_FP8_E4M3_BLOCK) return MOE_ERR_UNSUPPORTED;
+  MOE_REQUIRE(al16(W13_e4m3) && al16(W2_e4m3) && W13_scale && W2_scale && al16(scratch));
+  cudaStream_t s = (cudaStream_t)stream;
+  const Fp8Scratch q = fp8_scratch(*cfg, scratch);
+  const int G = cfg->E + cfg->n_shared;
+  const int64_t n13 = (int64_t)G * 2 * cfg->F * cfg->H, n2 = (int64_t)G * cfg->H * cfg->F;
+  MOE_CUDA(cudaMemcpyAsync(q.W13q, W13_e4m3, (size_t)n13, cudaMemcpyDeviceToDevice, s));
+  MOE_CUDA(cudaMemcpyAsync(q.W2q, W2_e4m3, (size_t)n2, cudaMemcpyDeviceToDevice, s));
+  MOE_CUDA(launch_load_fp8_scales(W13_scale, q.W13sf, q.W13sft, G, 2 * cfg->F, cfg->H, s));
+  MOE_CUDA(launch_load_fp8_scales(W2_scale, q.W2sf, q.W2sft, G, cfg->H, cfg->F, s));
+  return MOE_OK;
+}
+
 moe_status moe_grouped_ffn_fwd(const moe_config* cfg, const void* x_perm, const int32_t* counts,
                                const int32_t* offsets, const void* W13, const void* W2, void* GU,
                                void* h, void* y_perm, void* scratch, void* stream) {
@@ -671,7 +695,10 @@ moe_status moe_layer_fwd(const moe_config* cfg, const moe_params* P, const void*
   StashMap sm;
   MOE_TRY(stash_of(cfg, st, &sm));
   const StashAlloc alloc{st->stash_table, st->stash_top, cfg->stash_pool_pages};
-  MOE_TRY(moe_quantize_weights(cfg, P->W13, P->W2, scratch, stream));
+  // FP8 with no bf16 weights: the E4M3 weights moe_load_fp8_weights (or an
+  // earlier moe_quantize_weights) left in scratch are used as they are
+  if (!(is_fp8(*cfg) && !P->W13 && !P->W2))
+    MOE_TRY(moe_quantize_weights(cfg, P->W13, P->W2, scratch, stream));
   MOE_TRY(moe_route(cfg, x, P->W_r, P->bias, st->logits, st->idx, st->w, scratch, stream));
   MOE_TRY(permute_impl(cfg, x, st->idx, st->counts, st->offsets, st->row_of, st->token_of,
                        st->sel_offsets, st->sel_tokens, st->x_perm, scratch, stream,

@@ -298,6 +298,28 @@ quant_wmx_kernel(const __nv_bfloat16* __restrict__ W, uint8_t* __restrict__ Wf,
   }
 }
 
+// Scale atoms of E4M3 weights quantised by the caller: one UE8M0 code per
+// 128 x 128 tile (scale [G][rows / 128][cols / 128]) into the same two atom
+// arrays quant_tiles8_kernel writes (the tile's code for each of its 128 rows
+// in sf_f, for each of its 128 columns in sf_d). One thread per (tile, row).
+__global__ void __launch_bounds__(256)
+load_fp8_scales_kernel(const uint8_t* __restrict__ scale, uint8_t* __restrict__ sf_f,
+                       uint8_t* __restrict__ sf_d, long long n_tiles, int rows, int cols) {
+  const int tc = cols / 128, tr = rows / 128;
+  const int64_t kg_f = f8::atoms_k(cols), kg_d = f8::atoms_k(rows);
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n_tiles * 128;
+       i += (long long)gridDim.x * blockDim.x) {
+    const long long t = i >> 7;
+    const int n = (int)(i & 127);
+    const long long g = t / ((long long)tr * tc);
+    const int rem = (int)(t % ((long long)tr * tc));
+    const int rt = rem / tc, ct = rem % tc;
+    const uint8_t code = scale[t];
+    sf_f[f8::atom_offset(g * tr + rt, ct, kg_f) + f8::atom_byte(n, ct)] = code;
+    sf_d[f8::atom_offset(g * tc + ct, rt, kg_d) + f8::atom_byte(n, rt)] = code;
+  }
+}
+
 static int grid_cap(long long work_items, int per_block) {
   long long b = (work_items + per_block - 1) / per_block;
   const long long cap = (long long)num_sms() * 16;
@@ -310,6 +332,13 @@ cudaError_t launch_quant_tiles8(const void* W, uint8_t* Wq, uint8_t* sf_f, uint8
   const long long n = (long long)G * (rows / 128) * (cols / 128);
   quant_tiles8_kernel<<<grid_cap(n, 1), 256, 0, s>>>(static_cast<const __nv_bfloat16*>(W), Wq,
                                                      sf_f, sf_d, n, rows, cols);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_load_fp8_scales(const uint8_t* scale, uint8_t* sf_f, uint8_t* sf_d, int G,
+                                   int rows, int cols, cudaStream_t s) {
+  const long long n = (long long)G * (rows / 128) * (cols / 128);
+  load_fp8_scales_kernel<<<grid_cap(n * 128, 256), 256, 0, s>>>(scale, sf_f, sf_d, n, rows, cols);
   return cudaGetLastError();
 }
 
