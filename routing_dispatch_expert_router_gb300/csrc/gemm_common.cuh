@@ -347,6 +347,42 @@ static inline bool make_map_u8(CUtensorMap* m, const void* ptr, uint64_t inner, 
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// An MN-major operand of 1-byte elements [outer rows, inner columns] seen as
+// 128-column chunks: dims {128 columns of a chunk, rows, chunk index} with
+// strides {inner bytes per row, 128 bytes per chunk}, a {128, 128, chunks} box
+// and the 128-byte swizzle. One load brings `chunks` consecutive 128-column
+// slices of 128 rows, each slice 16 KB after the previous in shared memory --
+// the layout of `chunks` separate 2D boxes, in one request.
+static inline bool make_map_u8_chunks(CUtensorMap* m, const void* ptr, uint64_t inner,
+                                      uint64_t outer, uint32_t chunks) {
+  PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
+  if (!fn || inner % 128) return false;
+  cuuint64_t dims[3] = {128, outer, inner / 128};
+  cuuint64_t strides[2] = {inner, 128};
+  cuuint32_t box[3] = {128, 128, chunks};
+  cuuint32_t es[3] = {1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(ptr), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// The bf16 form of the chunked view: dims {64 columns of a chunk, rows, chunk
+// index}, strides {inner * 2 bytes per row, 128 bytes per chunk}, a {64, 64,
+// chunks} box (64 rows = one bf16 k-block): `chunks` 64-column slices of 64 rows,
+// 8 KB apart in shared memory, in one request.
+static inline bool make_map_chunks(CUtensorMap* m, const void* ptr, uint64_t inner,
+                                   uint64_t outer, uint32_t chunks) {
+  PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
+  if (!fn || inner % 64) return false;
+  cuuint64_t dims[3] = {64, outer, inner / 64};
+  cuuint64_t strides[2] = {inner * 2, 128};
+  cuuint32_t box[3] = {64, 64, chunks};
+  cuuint32_t es[3] = {1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box,
+            es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // fp32 output view for TMA stores of 32 x 32 boxes (128-byte rows, 128-byte swizzle).
 static inline bool make_out_map_f32(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t outer) {
   PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();

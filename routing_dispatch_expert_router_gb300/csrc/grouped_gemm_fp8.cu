@@ -405,8 +405,9 @@ grouped_gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmA,
             ptx::tma_load_2d(sB, &tmB, fb, k0, t.g * p.b_rows + b0);
             ptx::tma_load_2d(sB + 16384, &tmB, fb, k0, t.g * p.b_rows + b1);
           } else {
-            ptx::tma_load_2d(sB, &tmB, fb, b0, brow);
-            ptx::tma_load_2d(sB + 16384, &tmB, fb, b1, brow);
+            // MN-major: columns b0 .. b0 + 255 of rows brow.. as two 128-column
+            // chunks in one request (the chunked 3D map)
+            ptx::tma_load_3d(sB, &tmB, fb, 0, brow, b0 / 128);
           }
           const uint32_t sfs = sf_u + stage * kF8SfStage;
           // the atom of this K block: one per K block (MX) or per four
@@ -687,7 +688,7 @@ cudaError_t launch_ffn_fc2_dgrad_fp8(const moe_config& c, const uint8_t* dOq, co
   const int64_t R = rows_max(c);
   const int G = c.E + c.n_shared;
   CUtensorMap a, b, oc;
-  if (!make_map_u8(&a, dOq, c.H, R) || !make_map_u8(&b, W2q, c.F, (uint64_t)G * c.H) ||
+  if (!make_map_u8(&a, dOq, c.H, R) || !make_map_u8_chunks(&b, W2q, c.F, (uint64_t)G * c.H, 2) ||
       !make_out_map(&oc, dGU, 2ULL * c.F, R))
     return cudaErrorInvalidValue;
   Params p = base_params(c, counts, offsets, status);
@@ -718,7 +719,8 @@ cudaError_t launch_ffn_fc1_dgrad_fp8(const moe_config& c, const uint8_t* dGq, co
   const int64_t R = rows_max(c);
   const int G = c.E + c.n_shared;
   CUtensorMap a, b, oc;
-  if (!make_map_u8(&a, dGq, 2ULL * c.F, R) || !make_map_u8(&b, W13q, c.H, (uint64_t)G * 2 * c.F) ||
+  if (!make_map_u8(&a, dGq, 2ULL * c.F, R) ||
+      !make_map_u8_chunks(&b, W13q, c.H, (uint64_t)G * 2 * c.F, 2) ||
       !make_out_map(&oc, dX_perm, c.H, R))
     return cudaErrorInvalidValue;
   Params p = base_params(c, counts, offsets, status);
@@ -748,7 +750,7 @@ cudaError_t launch_ffn_wgrad_fc2_fp8(const moe_config& c, const uint8_t* dOq, co
   const int64_t R = rows_max(c);
   const int G = c.E + c.n_shared;
   CUtensorMap a, b, oc;
-  if (!make_map_u8(&a, dOq, c.H, R) || !make_map_u8(&b, hq, c.F, R) ||
+  if (!make_map_u8(&a, dOq, c.H, R) || !make_map_u8_chunks(&b, hq, c.F, R, 2) ||
       !make_out_map(&oc, dW2, c.F, (uint64_t)G * c.H))
     return cudaErrorInvalidValue;
   Params p = base_params(c, counts, offsets, status);
@@ -771,7 +773,7 @@ cudaError_t launch_ffn_wgrad_fc1_fp8(const moe_config& c, const uint8_t* dGq, co
   const int64_t R = rows_max(c);
   const int G = c.E + c.n_shared;
   CUtensorMap a, b, oc;
-  if (!make_map_u8(&a, dGq, 2ULL * c.F, R) || !make_map_u8(&b, xq, c.H, R) ||
+  if (!make_map_u8(&a, dGq, 2ULL * c.F, R) || !make_map_u8_chunks(&b, xq, c.H, R, 2) ||
       !make_out_map(&oc, dW13, c.H, (uint64_t)G * 2 * c.F))
     return cudaErrorInvalidValue;
   Params p = base_params(c, counts, offsets, status);
