@@ -315,6 +315,10 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
           const int k0 = kb * BK;
           if (A_MN == 0) {
             ptx::tma_load_2d(sA, &tmA, fb, k0, page_row(p, kPageA, s_off[t.g] + t.mt * BM));
+          } else if constexpr (EPI != kEpiStoreF32) {
+            // MN-major A: its two 64-column chunks in one request (chunked map)
+            const int kr = page_row(p, kPageA, s_off[t.g] + k0);
+            ptx::tma_load_3d(sA, &tmA, fb, 0, kr, t.mt * BM / 64);
           } else {
             const int kr = page_row(p, kPageA, s_off[t.g] + k0);
             ptx::tma_load_2d(sA, &tmA, fb, t.mt * BM, kr);
@@ -329,7 +333,13 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             for (int q = 0; q < BPARTS; ++q)
               ptx::tma_load_2d(sB + q * L::B_BYTES, &tmB, fb, BPARTS * k0 + q * BK,
                                t.g * p.b_rows + t.nt * BN);
+          } else if constexpr (EPI != kEpiStoreF32) {
+            // MN-major B: its BN / 64 chunks in one request (chunked map)
+            const int kr =
+                p.kgrouped ? page_row(p, kPageB, s_off[t.g] + k0) : t.g * p.b_rows + k0;
+            ptx::tma_load_3d(sB, &tmB, fb, 0, kr, t.nt * BN / 64);
           } else {
+            // (the router's three-part B keeps the 2D map)
             const int kr =
                 p.kgrouped ? page_row(p, kPageB, s_off[t.g] + k0) : t.g * p.b_rows + k0;
 #pragma unroll
@@ -632,8 +642,7 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA,
             ptx::tma_load_2d_pair(sA, &tmA, fb, k0, page_row(p, kPageA, s_off[g] + mt * BM));
           } else {
             const int kr = page_row(p, kPageA, s_off[g] + k0);
-            ptx::tma_load_2d_pair(sA, &tmA, fb, mt * BM, kr);
-            ptx::tma_load_2d_pair(sA + 8192, &tmA, fb, mt * BM + 64, kr);
+            ptx::tma_load_3d_pair(sA, &tmA, fb, 0, kr, mt * BM / 64);      // two 64-column chunks
           }
           if (swiglu_fwd(EPI)) {
             // CTA 0 brings the 128 gate rows, CTA 1 the matching 128 up rows
@@ -643,8 +652,7 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA,
             ptx::tma_load_2d_pair(sB, &tmB, fb, k0, g * p.b_rows + nt * BN + (int)rank * 128);
           } else {
             const int kr = p.kgrouped ? page_row(p, kPageB, s_off[g] + k0) : g * p.b_rows + k0;
-            ptx::tma_load_2d_pair(sB, &tmB, fb, nt * BN + (int)rank * 128, kr);
-            ptx::tma_load_2d_pair(sB + 8192, &tmB, fb, nt * BN + (int)rank * 128 + 64, kr);
+            ptx::tma_load_3d_pair(sB, &tmB, fb, 0, kr, (nt * BN + (int)rank * 128) / 64);
           }
           if (++stage == STAGES) {
             stage = 0;
@@ -999,7 +1007,8 @@ cudaError_t launch_ffn_fc2_dgrad(const moe_config& c, const void* dO_perm, const
   const int G = c.E + c.n_shared;
   const int bn = (c.F % 256 == 0) ? 256 : 128;
   CUtensorMap a, b, oc, gu;
-  if (!make_map(&a, dO_perm, c.H, R, 128) || !make_map(&b, W2, c.F, (uint64_t)G * c.H, 64) ||
+  if (!make_map(&a, dO_perm, c.H, R, 128) ||
+      !make_map_chunks(&b, W2, c.F, (uint64_t)G * c.H, use_pairs(c, c.F) ? 2 : bn / 64) ||
       !make_out_map(&oc, dGU, 2ULL * c.F, R) ||
       !make_out_map(&gu, GU, 2ULL * c.F, stash_rows(c, sm)))
     return cudaErrorInvalidValue;
@@ -1037,7 +1046,7 @@ cudaError_t launch_ffn_fc1_dgrad(const moe_config& c, const void* dGU, const int
   const int bn = (c.H % 256 == 0) ? 256 : 128;
   CUtensorMap a, b, oc;
   if (!make_map(&a, dGU, 2ULL * c.F, R, 128) ||
-      !make_map(&b, W13, c.H, (uint64_t)G * 2 * c.F, 64) ||
+      !make_map_chunks(&b, W13, c.H, (uint64_t)G * 2 * c.F, use_pairs(c, c.H) ? 2 : bn / 64) ||
       !make_out_map_w64(&oc, dX_perm, c.H, R))
     return cudaErrorInvalidValue;
   const CUtensorMap& oc2 = oc;
@@ -1064,7 +1073,8 @@ cudaError_t launch_ffn_wgrad_fc2(const moe_config& c, const void* dO_perm, const
   const int bn = (c.F % 256 == 0) ? 256 : 128;
   const int G = c.E + c.n_shared;
   CUtensorMap a, b, oc;
-  if (!make_map(&a, dO_perm, c.H, R, 64) || !make_map(&b, h, c.F, stash_rows(c, sm), 64) ||
+  if (!make_map_chunks(&a, dO_perm, c.H, R, 2) ||
+      !make_map_chunks(&b, h, c.F, stash_rows(c, sm), use_pairs(c, c.F) ? 2 : bn / 64) ||
       !make_out_map_w64(&oc, dW2, c.F, (uint64_t)G * c.H))
     return cudaErrorInvalidValue;
   const CUtensorMap& oc2 = oc;
@@ -1090,7 +1100,8 @@ cudaError_t launch_ffn_wgrad_fc1(const moe_config& c, const void* dGU, const voi
   const int bn = (c.H % 256 == 0) ? 256 : 128;
   const int G = c.E + c.n_shared;
   CUtensorMap a, b, oc;
-  if (!make_map(&a, dGU, 2ULL * c.F, R, 64) || !make_map(&b, x_perm, c.H, stash_rows(c, sm), 64) ||
+  if (!make_map_chunks(&a, dGU, 2ULL * c.F, R, 2) ||
+      !make_map_chunks(&b, x_perm, c.H, stash_rows(c, sm), use_pairs(c, c.H) ? 2 : bn / 64) ||
       !make_out_map_w64(&oc, dW13, c.H, (uint64_t)G * 2 * c.F))
     return cudaErrorInvalidValue;
   const CUtensorMap& oc2 = oc;
