@@ -20,128 +20,164 @@
 // the atom's rows are the buffer's columns and its K blocks the 128-row
 // blocks of the permuted buffer (the weight gradients reduce over tokens).
 // E4M3 rounding (to nearest even, saturating) uses the hardware conversion.
+#include <algorithm>
+
 #include "common.cuh"
 #include "fp8_layout.cuh"
 #include "internal.h"
 
 namespace moe {
 
-// Whether 128-row block rb of the permuted buffer holds any row a GEMM reads:
-// group g's segment starts at offsets[g], and the GEMMs read its first
+// The live 128-row blocks of the permuted buffer: group g's segment starts at
+// offsets[g] (a multiple of 128 rows), and the GEMMs read its first
 // ceil(counts[g] / 128) blocks (capacity segments and dropless padding past
-// them are never read, so they are not quantised).
-__device__ __forceinline__ bool live_block(const int32_t* __restrict__ offsets,
-                                           const int32_t* __restrict__ counts, int G, long long rb) {
-  const long long r0 = rb * 128;
-  int lo = 0, hi = G - 1;                                 // last g with offsets[g] <= r0
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    if (offsets[mid] <= r0) lo = mid;
-    else hi = mid - 1;
+// them are never read, so they are not quantised). Every block of 256 threads
+// writes pre[g] = the live blocks of the groups before g, for g = 0 .. G
+// (pre[G] = all of them), into its shared memory; G <= 511.
+__device__ __forceinline__ int live_block_prefix(const int32_t* __restrict__ counts, int G,
+                                                 int* pre, int* wsum) {
+  const int t = threadIdx.x, lane = t & 31, wid = t >> 5;
+  const int g0 = 2 * t, g1 = 2 * t + 1;
+  const int n0 = g0 < G ? (counts[g0] + 127) / 128 : 0;
+  const int n1 = g1 < G ? (counts[g1] + 127) / 128 : 0;
+  int v = n0 + n1;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, v, o);
+    if (lane >= o) v += y;
   }
-  return r0 - offsets[lo] < (long long)((counts[lo] + 127) / 128) * 128;
+  if (lane == 31) wsum[wid] = v;
+  __syncthreads();
+  int excl = v - n0 - n1;
+  for (int w = 0; w < wid; ++w) excl += wsum[w];
+  if (g0 <= G) pre[g0] = excl;
+  if (g1 <= G) pre[g1] = excl + n0;
+  __syncthreads();
+  return pre[G];
 }
 
-// BLK x 1 slices (BLK = 128, or 32 for MX): every live 128-row block of
-// [0, offsets[G]) (group segments are multiples of 128 rows, so blocks never
-// straddle two experts) -> E4M3 bytes plus the UE8M0 scale atoms [cols / 128]
-// [along the rows]. One block of 256 threads per (128-row block, 128-column
-// slab): the 128 x 128 tile is read once into shared memory with 16-byte
-// loads (eight per thread in flight), the maxima of each column's four
-// 32-row pieces are taken there (a bf16 pair of columns per read; combined into
-// one for BLK = 128), and every
-// thread quantises eight 8-column vectors read back from the tile and stores
-// their codes (8 bytes each). With ROWS, the same pass also writes the tile's
-// 1 x BLK row form (Xr, sfr; a row's 16 vectors sit in 16 consecutive lanes,
-// whose maxima meet by shuffles), so a tensor both GEMM directions need is read
-// once.
+// Row block of live block lb: the last group g with pre[g] <= lb holds it.
+__device__ __forceinline__ long long live_row_block(const int* pre, const int32_t* offsets, int G,
+                                                    int lb) {
+  int lo = 0, hi = G - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (pre[mid] <= lb) lo = mid;
+    else hi = mid - 1;
+  }
+  return offsets[lo] / 128 + (lb - pre[lo]);
+}
+
+// BLK x 1 slices (BLK = 128, or 32 for MX): every live 128-row block (group
+// segments are multiples of 128 rows, so blocks never straddle two experts)
+// -> E4M3 bytes plus the UE8M0 scale atoms [cols / 128][along the rows]. One
+// block of 256 threads per (128-row block, 128-column slab), looping over the
+// live tiles: thread (m, q) = (tid / 16, tid % 16) holds rows m + 16 i (i < 8)
+// of the slab's columns 8q .. 8q + 7 in registers (16-byte loads, two 256-byte
+// rows per warp instruction), takes its maxima of each column's 32-row pieces
+// there, meets lane q + 16 (rows m ^ 1) by one shuffle and the other seven
+// warps in shared memory, and quantises its own vectors; the next tile's eight
+// loads are issued before this tile is processed, so they are in flight during
+// it. With ROWS, the same pass also writes the tile's 1 x BLK row form (Xr,
+// sfr; a row's 16 vectors sit in 16 consecutive lanes, whose maxima meet by
+// shuffles), so a tensor both GEMM directions need is read once.
 template <int BLK, bool ROWS>
-__global__ void __launch_bounds__(256)
+__global__ void __launch_bounds__(256, 2)
 quant_cols8_kernel(const __nv_bfloat16* __restrict__ X, uint8_t* __restrict__ Xq,
                    uint8_t* __restrict__ sf, const int32_t* __restrict__ offsets,
                    const int32_t* __restrict__ counts, int G, int cols, long long kg,
                    uint8_t* __restrict__ Xr, uint8_t* __restrict__ sfr, long long kgr,
                    const int32_t* __restrict__ pages) {
   static_assert(BLK == 128 || BLK == 32, "block length");
-  extern __shared__ uint4 qc_smem[];
-  uint4 (*tile)[16] = reinterpret_cast<uint4 (*)[16]>(qc_smem);   // 128 rows x 128 bf16
-  float* part = reinterpret_cast<float*>(qc_smem + 128 * 16);      // [4 pieces][128]
-  float* inv = part + 512;                                         // [4 pieces][128]
-  const long long rblocks = offsets[G] / 128;
+  constexpr int NP = 128 / BLK;                  // pieces of a 128-row block
+  constexpr int IP = 8 / NP;                     // a thread's rows per piece
+  __shared__ int pre[kMaxGroups + 1];
+  __shared__ int wsum[8];
+  __shared__ uint32_t part[8][NP][64];          // [warp][piece][column pair] bf16 maxima
+  __shared__ __align__(16) float inv[NP][128];   // [piece][column] 1 / scale
   const int slabs = cols >> 7;
-  const int tid = threadIdx.x;
-  for (long long w = blockIdx.x; w < rblocks * slabs; w += gridDim.x) {
-    const long long rb = w / slabs;
-    const int cs = (int)(w - rb * slabs);
+  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+  const int q = tid & 15, m = tid >> 4;
+  // (live tiles only, dealt round-robin: every block of the resident grid
+  // gets the same number of tiles, to within one)
+  const long long work = (long long)live_block_prefix(counts, G, pre, wsum) * slabs;
+  auto tile_of = [&](long long w, int& cs) -> long long {
+    const int lb = (int)(w / slabs);
+    cs = (int)(w - (long long)lb * slabs);
+    return live_row_block(pre, offsets, G, lb);
+  };
+  // (a paged stash tensor keeps the block in one page)
+  auto load = [&](long long w, uint4 (&v)[8]) {
+    int cs;
+    const long long rb = tile_of(w, cs);
+    const __nv_bfloat16* src = X + (size_t)stash_row(pages, (int)rb * 128) * cols + cs * 128;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) v[i] = ldg_nc_v4(src + (size_t)(m + 16 * i) * cols + q * 8);
+  };
+  uint4 cur[8], nxt[8];
+  long long w = blockIdx.x;
+  if (w < work) load(w, cur);
+  for (; w < work; w += gridDim.x) {
+    if (w + gridDim.x < work) load(w + gridDim.x, nxt);
+    int cs;
+    const long long rb = tile_of(w, cs);
     const int c0 = cs * 128;
-    if (!live_block(offsets, counts, G, rb)) continue;
-    // (a paged stash tensor keeps the block in one page)
-    const __nv_bfloat16* src = X + (size_t)stash_row(pages, (int)rb * 128) * cols + c0;
-    {
-      uint4 in[8];
+    // |x| maxima on packed bf16 pairs (exact: the maximum of bf16 values is one of them)
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const int v = tid + 256 * i, r = v >> 4, q = v & 15;
-        in[i] = ldg_nc_v4(src + (size_t)r * cols + q * 8);
+    for (int p = 0; p < NP; ++p) {
+      __nv_bfloat162 mx[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) mx[j] = __float2bfloat162_rn(0.f);
+#pragma unroll
+      for (int i = p * IP; i < (p + 1) * IP; ++i) {
+        const __nv_bfloat162* v = reinterpret_cast<const __nv_bfloat162*>(&cur[i]);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) mx[j] = __hmax2(mx[j], __habs2(v[j]));
       }
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const int v = tid + 256 * i;
-        tile[v >> 4][v & 15] = in[i];
+      for (int j = 0; j < 4; ++j) {
+        uint32_t u = *reinterpret_cast<const uint32_t*>(&mx[j]);
+        u = __shfl_xor_sync(0xffffffffu, u, 16);
+        mx[j] = __hmax2(mx[j], *reinterpret_cast<const __nv_bfloat162*>(&u));
+      }
+      if (lane < 16) {
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          part[wid][p][q * 4 + j] = *reinterpret_cast<const uint32_t*>(&mx[j]);
       }
     }
     __syncthreads();
-    {
-      // columns c and c + 1 (one bf16 pair per 4-byte read, consecutive lanes on
-      // consecutive words), 32-row piece j
-      const int c = 2 * (tid & 63), j = tid >> 6;
-      const uint32_t* pair = reinterpret_cast<const uint32_t*>(&tile[0][0]) + (c >> 1);
-      float m0 = 0.f, m1 = 0.f;
-#pragma unroll 8
-      for (int r = 32 * j; r < 32 * j + 32; ++r) {
-        const uint32_t w2 = pair[r * 64];
-        m0 = fmaxf(m0, fabsf(bf16_lo(w2)));
-        m1 = fmaxf(m1, fabsf(bf16_hi(w2)));
-      }
-      part[j * 128 + c] = m0;
-      part[j * 128 + c + 1] = m1;
-    }
-    __syncthreads();
-    if (BLK == 128) {
-      if (tid < 128) {
-        const float m = fmaxf(fmaxf(part[tid], part[128 + tid]), fmaxf(part[256 + tid], part[384 + tid]));
-        const uint32_t code = ue8m0_code(m);
-        const float iv = ue8m0_inv(code);
+    for (int x = tid; x < NP * 128; x += 256) {
+      const int p = x >> 7, c = x & 127;
+      float a = 0.f;
 #pragma unroll
-        for (int j = 0; j < 4; ++j) inv[j * 128 + tid] = iv;
-        sf[f8::atom_offset(cs, rb, kg) + f8::atom_byte(tid, (int)rb)] = (uint8_t)code;
+      for (int w2 = 0; w2 < 8; ++w2) {
+        const uint32_t u = part[w2][p][c >> 1];
+        a = fmaxf(a, (c & 1) ? bf16_hi(u) : bf16_lo(u));
       }
-    } else {
-      // column c = tid & 127, pieces 2h, 2h + 1 (one scale byte each)
-      const int c = tid & 127, h = tid >> 7;
-#pragma unroll
-      for (int j = 2 * h; j < 2 * h + 2; ++j) {
-        const uint32_t code = ue8m0_code(part[j * 128 + c]);
-        inv[j * 128 + c] = ue8m0_inv(code);
-        sf[f8::mx_atom_offset(cs, rb, kg) + f8::atom_byte(c, j)] = (uint8_t)code;
-      }
+      const uint32_t code = ue8m0_code(a);
+      inv[p][c] = ue8m0_inv(code);
+      if (BLK == 128)
+        sf[f8::atom_offset(cs, rb, kg) + f8::atom_byte(c, (int)rb)] = (uint8_t)code;
+      else
+        sf[f8::mx_atom_offset(cs, rb, kg) + f8::atom_byte(c, p)] = (uint8_t)code;
     }
     __syncthreads();
     uint8_t* dst = Xq + (size_t)rb * 128 * cols + c0;
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
-      const int v = tid + 256 * i, r = v >> 4, q = v & 15;
+      const int r = m + 16 * i;
       float f[8];
-      unpack8(tile[r][q], f);
+      unpack8(cur[i], f);
       *reinterpret_cast<uint2*>(dst + (size_t)r * cols + q * 8) =
-          e4m3x8_each(f, inv + (r >> 5) * 128 + q * 8);
+          e4m3x8_each(f, &inv[i / IP][q * 8]);
       if (ROWS) {
         // row r's 1 x BLK pieces of this 128-column K block
         constexpr int LANES = BLK / 8;
-        float m = amax8(f);
+        float a = amax8(f);
 #pragma unroll
-        for (int o = LANES / 2; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-        const uint32_t code = ue8m0_code(m);
+        for (int o = LANES / 2; o > 0; o >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
+        const uint32_t code = ue8m0_code(a);
         *reinterpret_cast<uint2*>(Xr + ((size_t)rb * 128 + r) * cols + c0 + q * 8) =
             e4m3x8(f, ue8m0_inv(code));
         if ((q & (LANES - 1)) == 0) {
@@ -152,7 +188,8 @@ quant_cols8_kernel(const __nv_bfloat16* __restrict__ X, uint8_t* __restrict__ Xq
         }
       }
     }
-    __syncthreads();
+#pragma unroll
+    for (int i = 0; i < 8; ++i) cur[i] = nxt[i];
   }
 }
 
@@ -327,10 +364,26 @@ static int grid_cap(long long work_items, int per_block) {
   return b > 0 ? (int)b : 1;
 }
 
+// Grid of a kernel whose blocks loop over equal work items: the blocks that
+// fit on the GPU at once, or fewer when there is less work. A larger grid runs
+// in rounds, and its last partial round of long-lived blocks leaves most SMs
+// idle for the length of a whole block's loop.
+template <typename Kern>
+static int resident_grid(Kern kern, size_t smem, long long work_items) {
+  int per_sm = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, 256, smem) != cudaSuccess ||
+      per_sm < 1)
+    per_sm = 1;
+  long long b = (long long)num_sms() * per_sm;
+  if (b > work_items) b = work_items;
+  return b > 0 ? (int)b : 1;
+}
+
 cudaError_t launch_quant_tiles8(const void* W, uint8_t* Wq, uint8_t* sf_f, uint8_t* sf_d, int G,
                                 int rows, int cols, cudaStream_t s) {
   const long long n = (long long)G * (rows / 128) * (cols / 128);
-  quant_tiles8_kernel<<<grid_cap(n, 1), 256, 0, s>>>(static_cast<const __nv_bfloat16*>(W), Wq,
+  static const int resident = resident_grid(quant_tiles8_kernel, 0, 1LL << 40);
+  quant_tiles8_kernel<<<(int)(n < resident ? (n > 0 ? n : 1) : resident), 256, 0, s>>>(static_cast<const __nv_bfloat16*>(W), Wq,
                                                      sf_f, sf_d, n, rows, cols);
   return cudaGetLastError();
 }
@@ -345,7 +398,8 @@ cudaError_t launch_load_fp8_scales(const uint8_t* scale, uint8_t* sf_f, uint8_t*
 cudaError_t launch_quant_wmx(const void* W, uint8_t* Wf, uint8_t* Wd, uint8_t* sf_f, uint8_t* sf_d,
                              int G, int rows, int cols, cudaStream_t s) {
   const long long n = (long long)G * (rows / 128) * (cols / 128);
-  quant_wmx_kernel<<<grid_cap(n, 1), 256, 0, s>>>(static_cast<const __nv_bfloat16*>(W), Wf, Wd,
+  static const int resident = resident_grid(quant_wmx_kernel, 0, 1LL << 40);
+  quant_wmx_kernel<<<(int)(n < resident ? (n > 0 ? n : 1) : resident), 256, 0, s>>>(static_cast<const __nv_bfloat16*>(W), Wf, Wd,
                                                   sf_f, sf_d, n, rows, cols);
   return cudaGetLastError();
 }
@@ -353,10 +407,13 @@ cudaError_t launch_quant_wmx(const void* W, uint8_t* Wf, uint8_t* Wd, uint8_t* s
 cudaError_t launch_quant_cols8(const void* X, uint8_t* Xq, uint8_t* sf, const int32_t* offsets,
                                const int32_t* counts, int G, int64_t rows_max, int cols,
                                cudaStream_t s, bool mx, const int32_t* pages) {
-  constexpr int smem = 128 * 16 * 16 + 8 * 128 * 4;     // tile + piece maxima + 1/scales
-  const int grid = grid_cap(rows_max / 128 * (cols / 128), 1);
+  constexpr int smem = 0;                              // (static shared memory only)
+  const long long tiles = rows_max / 128 * (cols / 128);
+  static const int res32 = resident_grid(quant_cols8_kernel<32, false>, smem, 1LL << 40);
+  static const int res128 = resident_grid(quant_cols8_kernel<128, false>, smem, 1LL << 40);
   const long long kg = f8::sf_stride(rows_max, mx);
   const __nv_bfloat16* x = static_cast<const __nv_bfloat16*>(X);
+  const int grid = (int)std::max(1LL, std::min(tiles, (long long)(mx ? res32 : res128)));
   if (mx)
     quant_cols8_kernel<32, false><<<grid, 256, smem, s>>>(x, Xq, sf, offsets, counts, G, cols, kg,
                                                            nullptr, nullptr, 0, pages);
@@ -369,8 +426,11 @@ cudaError_t launch_quant_cols8(const void* X, uint8_t* Xq, uint8_t* sf, const in
 cudaError_t launch_quant_rows_cols8(const void* X, uint8_t* Xr, uint8_t* sfr, uint8_t* Xc,
                                     uint8_t* sfc, const int32_t* offsets, const int32_t* counts,
                                     int G, int64_t rows_max, int cols, cudaStream_t s, bool mx) {
-  constexpr int smem = 128 * 16 * 16 + 8 * 128 * 4;
-  const int grid = grid_cap(rows_max / 128 * (cols / 128), 1);
+  constexpr int smem = 0;
+  const long long tiles = rows_max / 128 * (cols / 128);
+  static const int res32 = resident_grid(quant_cols8_kernel<32, true>, smem, 1LL << 40);
+  static const int res128 = resident_grid(quant_cols8_kernel<128, true>, smem, 1LL << 40);
+  const int grid = (int)std::max(1LL, std::min(tiles, (long long)(mx ? res32 : res128)));
   const long long kgc = f8::sf_stride(rows_max, mx), kgr = f8::sf_stride(cols, mx);
   const __nv_bfloat16* x = static_cast<const __nv_bfloat16*>(X);
   if (mx)
