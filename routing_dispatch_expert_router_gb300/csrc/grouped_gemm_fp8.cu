@@ -757,7 +757,7 @@ cudaError_t launch_ffn_wgrad_fc2_fp8(const moe_config& c, const uint8_t* dOq, co
   p.Mw = c.H;
   p.N = c.F;
   p.K = 0;
-  p.n_fast = p.Mw > p.N;
+  p.n_fast = 1;                 // see launch_ffn_wgrad_fc1_fp8
   p.sfa = dOsf;
   p.sfa_kg = sf_kg(c, R);
   p.sfb = hsf;
@@ -780,7 +780,11 @@ cudaError_t launch_ffn_wgrad_fc1_fp8(const moe_config& c, const uint8_t* dGq, co
   p.Mw = 2 * c.F;
   p.N = c.H;
   p.K = 0;
-  p.n_fast = p.Mw > p.N;
+  // tiles n-fastest: the CTAs running at once write whole rows of dW (full
+  // 14 KB rows of dW13 rather than 512-byte pieces of every row), which HBM
+  // takes faster (weight-gradient stage of the 256-expert FP8 layer 6.59 ->
+  // 6.41 ms; dW2's order makes no difference)
+  p.n_fast = 1;
   p.sfa = dGsf;
   p.sfa_kg = sf_kg(c, R);
   p.sfb = xsf;
