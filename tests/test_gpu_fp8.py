@@ -8,8 +8,9 @@ run from the raw inputs with the 5e-2 rule (per element against
 |ref| + rms(ref), and on the relative Frobenius error).
 """
 import pytest
+import torch
 
-from workloads import DT_FP8, SIGMOID, MoEShape, make_inputs
+from workloads import DT_FP8, DT_MXFP8, SIGMOID, MoEShape, make_inputs
 
 pytestmark = pytest.mark.gpu
 
@@ -54,3 +55,22 @@ def test_fp8_layer_end_to_end(shape):
     inp = make_inputs(shape, seed=1)
     g = H_.run_layer(shape, inp)
     H_.check_end_to_end_fp8(shape, inp, g)
+
+
+@pytest.mark.parametrize("dtype", [DT_FP8, DT_MXFP8], ids=["block", "mx"])
+def test_fp8_hot_and_empty_experts(dtype):
+    """Every token on experts 3 and 5, six experts without a row: the column
+    quantisers must deal only the two live segments' blocks, and the empty
+    experts' weight-gradient tiles come out as zeros."""
+    shape = MoEShape("fp8_hot", T=700, H=256, E=8, k=2, F=256, dtype=dtype)
+    inp = make_inputs(shape, seed=2)
+    b = torch.zeros(8)
+    b[3] = 100.0                       # every token picks expert 3 first
+    b[5] = 50.0                        # ... and expert 5 second
+    inp["bias"] = b
+    g = H_.run_layer(shape, inp)
+    cnt = g["counts"].cpu().numpy()
+    assert cnt[3] == 700 and cnt[5] == 700 and cnt.sum() == 1400
+    for e in (0, 1, 2, 4, 6, 7):
+        assert (g["dW13"][e].float().cpu() == 0).all() and (g["dW2"][e].float().cpu() == 0).all()
+    H_.check_steps(shape, inp, g)
