@@ -585,8 +585,7 @@ def run_ours(args, rank, world, local):
             "traffic": gemm_traffic(shape.name, "wgrad_stage_dram_bytes_per_step"),
             "tflops": fl / (wms * 1e-3) / 1e12,
             "note": "of measured copy bandwidth; the stage writes the weight gradients "
-                    f"({G * 3 * H * F * 2 / 1e9:.2f} GB bf16), and this part's write-only rate "
-                    "is below its copy rate"}
+                    f"({G * 3 * H * F * 2 / 1e9:.2f} GB bf16)"}
     return res, shape, inp
 
 
